@@ -1,0 +1,495 @@
+#!/usr/bin/env python
+"""Benchmark of the multi-adapter LoRA path on one GB300 (or N, one process each).
+
+A step is one pass of the whole path over one batch: lora_segments_build (grouping
+the batch's tokens by adapter, work lists) followed by lora_apply (gather + shrink
++ scale + expand through the page table, in place in y).  The default workload is
+the decode batch: 64 tokens (one per request), q_proj 4096 -> 4096, 100 rank-16
+adapters, uniformly random adapter per token.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU fp64 oracle on the
+same workload instead (the reference arm of this build: there is no runnable
+upstream implementation).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SGMV/BGMV adapter-path tokens/s and achieved HBM GB/s (% of roofline), 1×GB300"
+UNIT = "tokens/s"
+
+WORKLOAD_TEXT = {
+    "decode": "decode BGMV: 64 tokens (1 per request), q_proj 4096->4096, 100 adapters rank 16, "
+              "uniform adapter per token, bf16",
+    "prefill": "prefill SGMV: 32 requests of U{64..512} tokens, 4096->4096, 200 adapters rank 16, "
+               "Zipf(1.1) popularity, contiguous segments, bf16",
+    "hetero": "heterogeneous ranks: 256 decode tokens, 500 adapters r in {8,16,32,64}, "
+              "MLP up 4096->11008 (one call), paged 4096-element pages, bf16",
+    "tiny": "tiny SGMV: d=256, 4 adapters rank 8, 16 tokens in segments [3,5,1,7]",
+}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="decode")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="bounded CPU work for the oracle baseline (0 disables it)")
+    p.add_argument("--e2e-steps", type=int, default=2000)
+    p.add_argument("--soak-seconds", type=float, default=1.0,
+                   help="untimed steady load before the timed region while clocks are sampled")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ helpers --
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "200"]
+        if gpu_id:
+            cmd[1:1] = ["-i", gpu_id]
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [c.strip() for c in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(kernel_key: str, workload: str, current_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if absent or if the
+    kernel's sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[kernel_key][workload]
+        if e.get("source_hash") != current_hash:
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------- workloads --
+
+def make_workload(name: str, seed: int):
+    from segmented_gather_gemm_lora_gb300 import workloads as W
+
+    if name == "hetero":
+        wl = W.hetero(seed, which="up")
+    else:
+        wl = W.WORKLOADS[name](seed)
+    return wl
+
+
+def algorithmic_bytes(batch, pool) -> int:
+    """Bytes the fused apply must move at least once: every distinct adapter used (A and B
+    at its own rank, no padding), x read, y read and written (bf16)."""
+    ids = batch.ids
+    valid = ids >= 0
+    distinct = np.unique(ids[valid])
+    ranks = pool.ranks[distinct].astype(np.int64)
+    adapters = int((ranks * (pool.d_in + pool.d_out)).sum()) * 2
+    n = int(valid.sum())
+    return adapters + n * pool.d_in * 2 + n * pool.d_out * 2 * 2
+
+
+def algorithmic_flops(batch, pool) -> int:
+    ids = batch.ids
+    r = pool.ranks[ids[ids >= 0]].astype(np.int64)
+    return int((2 * r * (pool.d_in + pool.d_out)).sum())
+
+
+# -------------------------------------------------------------- our arm --
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from segmented_gather_gemm_lora_gb300 import binding as B
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
+
+    # Rotating input sets whose total exceeds 2x L2, so every step reads from HBM.
+    wl0 = make_workload(args.workload, 1000 * rank)
+    set_bytes = wl0.pools[0].pool.nbytes + wl0.batch.x.nbytes + wl0.batch.y0.nbytes
+    n_sets = max(2, math.ceil(2 * l2 / max(set_bytes, 1)) + 1)
+    sets = []
+    for s in range(n_sets):
+        wl = wl0 if s == 0 else make_workload(args.workload, 1000 * rank + s)
+        pool = wl.pools[0]
+        view = B.PoolView.from_host(pool, device=dev)
+        x = torch.from_numpy(wl.batch.x.view(np.int16)).to(dev).view(torch.bfloat16)
+        y = torch.from_numpy(wl.batch.y0.view(np.int16)).to(dev).view(torch.bfloat16)
+        ids = torch.from_numpy(wl.batch.ids).to(dev)
+        seg = B.Segments(wl.batch.T, device=dev)
+        sets.append(dict(wl=wl, view=view, x=x, y=y, ids=ids, seg=seg,
+                         bytes=algorithmic_bytes(wl.batch, pool), flops=algorithmic_flops(wl.batch, pool),
+                         T=int((wl.batch.ids >= 0).sum())))
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    mode = sets[0]["wl"].mode
+    n_ad = sets[0]["wl"].n_adapters
+
+    def step(k):
+        S = sets[k % n_sets]
+        B.lora_segments_build(S["ids"], n_ad, S["seg"], mode=mode, err=err)
+        B.lora_apply(S["x"], S["y"], S["seg"], S["view"], err=err)
+
+    # warm-up (eager), then a CUDA graph of one pass over all sets.
+    for k in range(max(args.warmup, 3)):
+        step(k)
+    torch.cuda.synchronize()
+    g_steps = n_sets * max(1, 64 // n_sets)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device=dev)
+    with torch.cuda.graph(graph, stream=cap):
+        for k in range(g_steps):
+            step(k)
+    rem = args.steps % g_steps
+    graph_rem = None
+    if rem:
+        graph_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_rem, stream=cap):
+            for k in range(rem):
+                step(k)
+    reps = args.steps // g_steps
+    graph.replay()
+    torch.cuda.synchronize()
+
+    # clocks: steady load before and during the timed region
+    gpu_id = str(getattr(props, "uuid", "") or "")
+    if gpu_id and not gpu_id.startswith("GPU-"):
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id)
+    t_end = time.perf_counter() + args.soak_seconds
+    while time.perf_counter() < t_end:
+        graph.replay()
+        torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps ----
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    if graph_rem is not None:
+        graph_rem.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms_local = e0.elapsed_time(e1)
+    ms = max_over_ranks(ms_local, world)
+    assert int(err.item()) == 0, "device error word %d" % int(err.item())
+
+    tokens_per_step = statistics.fmean(S["T"] for S in sets)  # sets are visited uniformly per pass
+    per_pass = [sets[k % n_sets]["T"] for k in range(g_steps)]
+    tokens_timed = reps * sum(per_pass) + sum(sets[k % n_sets]["T"] for k in range(rem))
+    total_tokens = sum_over_ranks(tokens_timed, world)
+    value = total_tokens / (ms / 1e3)
+
+    # ---- per-launch duration of the dominant kernel (the fused apply) ----
+    # The stream is held by a sleep kernel while the host queues every launch, so
+    # the events bracket GPU execution only.
+    n_k = min(args.steps, 4 * g_steps)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_k)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e8))
+    for k in range(n_k):
+        S = sets[k % n_sets]
+        B.lora_segments_build(S["ids"], n_ad, S["seg"], mode=mode, err=err)
+        evs[k][0].record()
+        B.lora_apply(S["x"], S["y"], S["seg"], S["view"], err=err)
+        evs[k][1].record()
+    torch.cuda.synchronize()
+    apply_ms = [a.elapsed_time(b) for a, b in evs]
+    apply_avg_s = statistics.fmean(apply_ms) / 1e3
+    bytes_avg = statistics.fmean(sets[k % n_sets]["bytes"] for k in range(n_k))
+    flops_avg = statistics.fmean(sets[k % n_sets]["flops"] for k in range(n_k))
+    hbm_peak, tc_peak, peak_kind = read_peaks()
+    achieved_gbs = bytes_avg / apply_avg_s / 1e9
+    csrc = os.path.join(ROOT, "segmented_gather_gemm_lora_gb300", "csrc")
+    kernel_hash = source_hash([os.path.join(csrc, f) for f in sorted(os.listdir(csrc))])
+    traffic = profile_traffic("lora_apply", args.workload, kernel_hash)
+
+    # ---- end to end: host buffers in, result out, through the public API ----
+    S0 = sets[0]
+    wl = S0["wl"]
+    hx = torch.from_numpy(wl.batch.x.view(np.int16).copy()).pin_memory()
+    hy0 = torch.from_numpy(wl.batch.y0.view(np.int16).copy()).pin_memory()
+    hids = torch.from_numpy(wl.batch.ids.copy()).pin_memory()
+    hy = torch.empty_like(hy0).pin_memory()
+    dx = S0["x"].view(torch.int16)
+    dy = S0["y"].view(torch.int16)
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        dy.copy_(hy0, non_blocking=True)
+        S0["ids"].copy_(hids, non_blocking=True)
+        B.lora_segments_build(S0["ids"], n_ad, S0["seg"], mode=mode, err=err)
+        B.lora_apply(S0["x"], S0["y"], S0["seg"], S0["view"], err=err)
+        hy.copy_(dy, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_value = sum_over_ranks(e2e_steps * S0["T"], world) / e2e_s
+    h2d = hx.numel() * 2 + hy0.numel() * 2 + hids.numel() * 4
+    d2h = hy.numel() * 2
+
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD_TEXT[args.workload],
+            "tokens_per_step": tokens_per_step,
+            "segments": "GROUP" if mode == 0 else "CONTIGUOUS",
+            "step": "lora_segments_build + lora_apply",
+            "l2": "inputs larger than L2: %d rotating input sets (%.0f MB in all, L2 %.0f MB)"
+                  % (n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
+            "timing": "CUDA graph of %d steps replayed; CUDA events on the launching stream" % g_steps,
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "lora_apply (gather_kernel)",
+            "achieved": achieved_gbs,
+            "peak": hbm_peak,
+            "unit": "GB/s",
+            "frac": achieved_gbs / hbm_peak,
+            "peak_kind": peak_kind,
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": bytes_avg,
+            "avg_launch_us": apply_avg_s * 1e6,
+            "tflops": flops_avg / apply_avg_s / 1e12,
+        },
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                   "reasons": clocks["reasons"], "samples": clocks["samples"]},
+    }
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        out["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    return out
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def cpu_baseline(wl, seconds: float):
+    """The fp64 oracle as it stands, single-threaded, on the batch repeated for a bounded
+    time; tokens/s."""
+    import oracle
+
+    pool = wl.pools[0]
+    b = wl.batch
+    n_tok = int((b.ids >= 0).sum())
+    oracle.lora_apply(b.x[:1], b.y0[:1], b.ids[:1], pool)  # load/compile outside the clock
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.lora_apply(b.x, b.y0, b.ids, pool)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": reps * n_tok / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "the full batch (%d tokens) %d times, %.1f s" % (b.T, reps, dt)}
+
+
+def run_reference(args, world, rank):
+    import oracle
+
+    wl = make_workload(args.workload, 0)
+    pool = wl.pools[0]
+    b = wl.batch
+    n_tok = int((b.ids >= 0).sum())
+    for _ in range(max(args.warmup, 3) if args.warmup < 50 else 3):
+        oracle.lora_apply(b.x, b.y0, b.ids, pool)
+    # bounded: at most ~60 s of oracle work whatever K is
+    t1 = time.perf_counter()
+    oracle.lora_apply(b.x, b.y0, b.ids, pool)
+    one = time.perf_counter() - t1
+    steps = args.steps if args.steps * one <= 60.0 else max(1, int(60.0 / max(one, 1e-9)))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.lora_apply(b.x, b.y0, b.ids, pool)
+    dt = time.perf_counter() - t0
+    value = steps * n_tok / dt
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt / steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload],
+                   "step": "the CPU fp64 oracle over the whole batch"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "the full batch (%d tokens) per step, %d steps" % (b.T, steps)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_info()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, world, rank)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        dist.init_process_group(backend="nccl")
+    out = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,225 @@
+/*
+ * lora_sgmv.h -- C ABI of the GB300 (sm_103a) multi-adapter LoRA library.
+ *
+ * The library computes, for a batch of T token rows that each carry their own
+ * adapter i = a(t),
+ *
+ *     y[t, :] = y0[t, :] + s_i * (x[t, :] . A_i) . B_i,     s_i = alpha_i / r_i,
+ *
+ * in place in the caller's base output y (which holds y0 = x . W0 on entry).
+ * The per-token form is the one of "Multi-LoRA serving: the single translator
+ * with a thousand glossaries", section "SGMV: the kernel that holds it all up"
+ * (y_t = W x_t + B_a(t) A_a(t) x_t for every t in the batch); the row-vector
+ * orientation and the alpha/r scale are those of "Multi-LoRA Serving in
+ * Production", section "Mathematical Formulation and the Batching Challenge"
+ * (y = x W0 + (alpha/r) (x A) B, A in R^{d_in x r}, B in R^{r x d_out}).
+ *
+ * Data types: x, y and the adapter pool are bf16 (passed as void*, 2 bytes per
+ * element, round-to-nearest-even on output); the rank-r intermediate h and the
+ * scales are fp32; products accumulate in fp32.
+ *
+ * Storage of one adapter i of rank r_i for a projection d_in -> d_out:
+ *   A_i: r_i rows x d_in elements, row-major (row j = column j of the math A_i);
+ *   B_i: r_i rows x d_out elements, row-major (the math B_i as is).
+ * Both live in a paged pool ("Multi-LoRA Serving in Production", section
+ * "Unified Paged Memory": adapter matrices sliced into fixed-size pages, a
+ * software page table mapping them to non-contiguous physical frames):
+ * logical element e of a matrix whose first page-list slot is page0 lives at
+ *     pool[page_list[page0 + e / page_elems] * page_elems + e % page_elems].
+ * Low ranks are not padded: an adapter holds ceil(r_i * d / page_elems) pages
+ * per matrix, only the last one partly used.
+ *
+ * Ownership and threading.  The caller owns every buffer (x, y, h, pool, page
+ * list, descriptors, segment buffer, error word); all device buffers are plain
+ * device pointers from any allocator.  The library allocates no device memory,
+ * keeps no per-call state, and its entry points may be called from several
+ * host threads.  Every compute entry point is asynchronous on the given CUDA
+ * stream (NULL = the legacy default stream) and does not synchronise.
+ *
+ * Errors.  Argument errors found on the host are returned before anything is
+ * launched.  A failed launch returns LORA_ERR_CUDA.  Errors that only the
+ * device can see (an adapter id outside [-1, n_adapters), a rank outside
+ * [1, max_rank], a page-list slot or page outside the pool, a wait that ran
+ * out) OR a LORA_DERR_* bit into *dev_err (a device int32 the caller zeroes
+ * and reads after its own synchronisation); the affected tokens' outputs are
+ * left as they were, every other token is still computed.
+ */
+#ifndef LORA_SGMV_H
+#define LORA_SGMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/** A CUDA stream (cudaStream_t); NULL means the legacy default stream. */
+typedef struct CUstream_st* lora_stream_t;
+
+typedef int32_t lora_status_t;
+#define LORA_OK 0
+#define LORA_ERR_INVALID_ARG (-1) /* null/misaligned pointer, bad size or stride, aliasing */
+#define LORA_ERR_UNSUPPORTED (-2) /* valid but outside what this build handles */
+#define LORA_ERR_CUDA (-3)        /* a CUDA runtime call or launch failed */
+#define LORA_ERR_WORKSPACE (-4)   /* the segment buffer is too small */
+
+/* Bits OR-ed into the caller's device error word. */
+#define LORA_DERR_BAD_ADAPTER 1 /* adapter id outside [-1, n_adapters) */
+#define LORA_DERR_BAD_PAGE 2    /* page-list slot or physical page outside the pool */
+#define LORA_DERR_BAD_RANK 4    /* adapter rank outside [1, max_rank] */
+#define LORA_DERR_TIMEOUT 8     /* a bounded wait inside a kernel ran out */
+
+/** Highest adapter rank this build supports (LORA_ERR_UNSUPPORTED above). */
+#define LORA_MAX_RANK 64
+/** Largest adapter count lora_segments_build accepts. */
+#define LORA_MAX_ADAPTERS 32768
+/** Segments of at most this many tokens take the gather (CUDA-core) path of
+ *  lora_apply / lora_sgmv_*; longer ones are cut into tiles of LORA_TILE_M
+ *  tokens for the tensor-core path ("Multi-LoRA serving: ...", section "SGMV:
+ *  the kernel that holds it all up": large segments through tensor cores, small
+ *  ones through a batched gather path). */
+#define LORA_SHORT_MAX_TOKENS 8
+#define LORA_TILE_M 128
+
+/** Segmentation modes of lora_segments_build. */
+#define LORA_SEG_GROUP 0      /* one segment per adapter id, ascending id, tokens ascending */
+#define LORA_SEG_CONTIGUOUS 1 /* one segment per maximal run of equal ids, in token order */
+
+/** One adapter of one projection (16 bytes, device array of n_adapters). */
+typedef struct {
+  int32_t rank;    /* r_i; 0 marks an adapter that is not resident */
+  float scale;     /* s_i = alpha_i / r_i, applied as given (never derived from rank) */
+  int32_t a_page0; /* page-list slot of A_i's first page */
+  int32_t b_page0; /* page-list slot of B_i's first page */
+} lora_adapter_desc_t;
+
+/** One projection's view of the paged adapter pool (host struct, device pointers). */
+typedef struct {
+  const void* pool;                    /* device bf16 [n_pages * page_elems], 16-byte aligned */
+  int64_t n_pages;                     /* physical pages in the pool */
+  const int32_t* page_list;            /* device int32 [n_page_list]: slot -> physical page */
+  int64_t n_page_list;                 /* slots in page_list */
+  const lora_adapter_desc_t* adapters; /* device [n_adapters] */
+  int32_t n_adapters;
+  int32_t page_elems; /* elements per page: a power of two, >= 64 */
+  int32_t max_rank;   /* largest rank any call may meet, 1 .. LORA_MAX_RANK */
+  int32_t d_in;       /* projection input width, a multiple of 8 */
+  int32_t d_out;      /* projection output width, a multiple of 8 */
+} lora_pool_view_t;
+
+/**
+ * Segments of one batch, laid out by lora_segments_carve in one caller-owned
+ * device buffer.  Filled by lora_segments_build; read by the compute calls.
+ * token_perm lists the segments' tokens in segment order; segment s covers
+ * token_perm[seg_indptr[s] .. seg_indptr[s+1]) and uses adapter seg_adapter[s].
+ * meta[0] = number of segments, meta[1] = tokens placed, meta[2] = short work
+ * units, meta[3] = long work units.  short_units lists the segments of at most
+ * LORA_SHORT_MAX_TOKENS tokens; long_units lists (segment, offset) pairs, one
+ * per LORA_TILE_M-token tile of every longer segment, both in segment order.
+ * The remaining arrays are the build's scratch.
+ */
+typedef struct {
+  int32_t T;              /* tokens the buffer was carved for */
+  int32_t max_long_units; /* capacity of long_units (pairs) */
+  int32_t* token_perm;    /* [T] */
+  int32_t* seg_indptr;    /* [T + 1] */
+  int32_t* seg_adapter;   /* [T] */
+  int32_t* meta;          /* [8] */
+  int32_t* short_units;   /* [T] */
+  int32_t* long_units;    /* [2 * max_long_units] */
+  int32_t* scratch;       /* [4 * T + 8]: run starts, run ends, run ids, run positions */
+} lora_segments_t;
+
+/** Bytes of the device buffer lora_segments_carve needs for T tokens (T >= 0). */
+size_t lora_segments_buffer_bytes(int32_t T);
+
+/**
+ * Point the arrays of *out into a caller-owned device buffer (no device access).
+ * buf must be 16-byte aligned and hold lora_segments_buffer_bytes(T) bytes.
+ * Returns LORA_ERR_WORKSPACE if it is too small, LORA_ERR_INVALID_ARG on a
+ * null or misaligned pointer or T < 0.
+ */
+lora_status_t lora_segments_carve(void* buf, size_t bytes, int32_t T, lora_segments_t* out);
+
+/**
+ * Group the batch's tokens by adapter ("Multi-LoRA serving: ...", section
+ * "SGMV: the kernel that holds it all up": SGMV segments the batch's tokens by
+ * adapter; "Multi-LoRA Serving in Production", section "Punica and Segmented
+ * Gather Matrix-Vector Multiplication (SGMV)": contiguous segments whose tokens
+ * share an adapter id).  token_adapter: device int32 [T], -1 = no adapter.
+ * mode: LORA_SEG_GROUP or LORA_SEG_CONTIGUOUS.  Tokens with id -1 belong to no
+ * segment; ids outside [-1, n_adapters) set LORA_DERR_BAD_ADAPTER and are
+ * dropped.  1 <= n_adapters <= LORA_MAX_ADAPTERS.  Output is bit-exact and
+ * deterministic.  T = 0 is a no-op that still writes empty segments.
+ */
+lora_status_t lora_segments_build(const int32_t* token_adapter, int32_t T, int32_t n_adapters,
+                                  int32_t mode, const lora_segments_t* seg, int32_t* dev_err,
+                                  lora_stream_t stream);
+
+/**
+ * Shrink stage ("Multi-LoRA Serving in Production", section "Punica and
+ * Segmented Gather Matrix-Vector Multiplication (SGMV)", "Shrink Stage"):
+ *     h[t, j] = sum_k x[t, k] * A_i[j, k]     for j < r_i, unscaled,
+ * for every token of the segments.  x: device bf16 [T, ldx] (ldx >= d_in,
+ * ldx % 8 == 0, 16-byte aligned).  h: device fp32 [T, ldh], ldh >= max_rank,
+ * ldh % 4 == 0, 16-byte aligned; columns >= r_i and rows of tokens in no
+ * segment are not written.
+ */
+lora_status_t lora_sgmv_shrink(const void* x, int64_t ldx, float* h, int64_t ldh,
+                               const lora_segments_t* seg, const lora_pool_view_t* view,
+                               int32_t* dev_err, lora_stream_t stream);
+
+/**
+ * Expand stage (same section, "Expand Stage"): scale and accumulate into the
+ * base output,
+ *     y[t, n] = bf16( y[t, n] + sum_j (s_i * h[t, j]) * B_i[j, n] ).
+ * h: device fp32 [T, ldh] as written by lora_sgmv_shrink.  y: device bf16
+ * [T, ldy] in place (ldy >= d_out, ldy % 8 == 0, 16-byte aligned).
+ */
+lora_status_t lora_sgmv_expand(const float* h, int64_t ldh, void* y, int64_t ldy,
+                               const lora_segments_t* seg, const lora_pool_view_t* view,
+                               int32_t* dev_err, lora_stream_t stream);
+
+/**
+ * Fused shrink -> scale -> expand over the segments; h never leaves the chip
+ * ("Multi-LoRA serving: ...", TL;DR: Y += sum_i X_i A_i B_i in a single pass).
+ *     y[t, n] = bf16( y[t, n] + sum_j (s_i * sum_k x[t,k] A_i[j,k]) * B_i[j, n] ).
+ * x must not overlap y.
+ */
+lora_status_t lora_apply(const void* x, int64_t ldx, void* y, int64_t ldy,
+                         const lora_segments_t* seg, const lora_pool_view_t* view,
+                         int32_t* dev_err, lora_stream_t stream);
+
+/**
+ * Decode form without segments: each token t gathers its own adapter
+ * token_adapter[t] (device int32 [T], -1 = no adapter), one token per request
+ * (the batched gather path for size-1 segments of "Multi-LoRA serving: ...",
+ * section "SGMV: the kernel that holds it all up"; MBGMV in "Multi-LoRA
+ * Serving in Production", section "S-LoRA: MBGMV and MBGMM Kernels").
+ * Same result as lora_apply.
+ */
+lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy,
+                        const int32_t* token_adapter, int32_t T, const lora_pool_view_t* view,
+                        int32_t* dev_err, lora_stream_t stream);
+
+/**
+ * Pages one adapter of rank r occupies in a pool of page_elems-element pages:
+ * ceil(r * d_in / page_elems) + ceil(r * d_out / page_elems) (bytes per matrix
+ * pair (d_in * r + r * d_out) * 2 before rounding to pages: "Multi-LoRA
+ * serving: ...", section "The maths that matters").  Returns -1 on bad input.
+ */
+int64_t lora_pool_pages_needed(int32_t rank, int32_t d_in, int32_t d_out, int32_t page_elems);
+
+/** Static, human-readable text for a status code. */
+const char* lora_status_string(lora_status_t status);
+
+/** ABI version of this header (bumped on any incompatible change). */
+#define LORA_ABI_VERSION 1
+int32_t lora_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_SGMV_H */

@@ -1,0 +1,257 @@
+"""Thin Python binding of liblora_sgmv.so (the C ABI in include/lora_sgmv.h).
+
+Argument marshalling only: every step of the LoRA path runs in the library's
+CUDA kernels.  PyTorch supplies device memory and the current stream.  There is
+no fallback: if the library cannot be built or loaded, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+# ---------------------------------------------------------------- C structs --
+
+LORA_OK = 0
+LORA_ERR_INVALID_ARG = -1
+LORA_ERR_UNSUPPORTED = -2
+LORA_ERR_CUDA = -3
+LORA_ERR_WORKSPACE = -4
+LORA_DERR_BAD_ADAPTER = 1
+LORA_DERR_BAD_PAGE = 2
+LORA_DERR_BAD_RANK = 4
+LORA_DERR_TIMEOUT = 8
+LORA_MAX_RANK = 64
+LORA_MAX_ADAPTERS = 32768
+LORA_SHORT_MAX_TOKENS = 8
+LORA_TILE_M = 128
+LORA_SEG_GROUP = 0
+LORA_SEG_CONTIGUOUS = 1
+
+EXPORTED = (
+    "lora_segments_buffer_bytes",
+    "lora_segments_carve",
+    "lora_segments_build",
+    "lora_sgmv_shrink",
+    "lora_sgmv_expand",
+    "lora_apply",
+    "lora_bgmv",
+    "lora_pool_pages_needed",
+    "lora_status_string",
+    "lora_abi_version",
+)
+
+
+class lora_adapter_desc_t(ctypes.Structure):
+    _fields_ = [("rank", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("a_page0", ctypes.c_int32), ("b_page0", ctypes.c_int32)]
+
+
+class lora_pool_view_t(ctypes.Structure):
+    _fields_ = [("pool", ctypes.c_void_p), ("n_pages", ctypes.c_int64),
+                ("page_list", ctypes.c_void_p), ("n_page_list", ctypes.c_int64),
+                ("adapters", ctypes.c_void_p), ("n_adapters", ctypes.c_int32),
+                ("page_elems", ctypes.c_int32), ("max_rank", ctypes.c_int32),
+                ("d_in", ctypes.c_int32), ("d_out", ctypes.c_int32)]
+
+
+class lora_segments_t(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("max_long_units", ctypes.c_int32),
+                ("token_perm", ctypes.c_void_p), ("seg_indptr", ctypes.c_void_p),
+                ("seg_adapter", ctypes.c_void_p), ("meta", ctypes.c_void_p),
+                ("short_units", ctypes.c_void_p), ("long_units", ctypes.c_void_p),
+                ("scratch", ctypes.c_void_p)]
+
+
+class LoraError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
+        self.status = status
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (built in-tree first if its sources are newer)."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        L.lora_segments_buffer_bytes.restype = sz
+        L.lora_segments_buffer_bytes.argtypes = [i32]
+        L.lora_segments_carve.restype = i32
+        L.lora_segments_carve.argtypes = [vp, sz, i32, ctypes.POINTER(lora_segments_t)]
+        L.lora_segments_build.restype = i32
+        L.lora_segments_build.argtypes = [vp, i32, i32, i32, ctypes.POINTER(lora_segments_t), vp, vp]
+        seg_p = ctypes.POINTER(lora_segments_t)
+        view_p = ctypes.POINTER(lora_pool_view_t)
+        L.lora_sgmv_shrink.restype = i32
+        L.lora_sgmv_shrink.argtypes = [vp, i64, vp, i64, seg_p, view_p, vp, vp]
+        L.lora_sgmv_expand.restype = i32
+        L.lora_sgmv_expand.argtypes = [vp, i64, vp, i64, seg_p, view_p, vp, vp]
+        L.lora_apply.restype = i32
+        L.lora_apply.argtypes = [vp, i64, vp, i64, seg_p, view_p, vp, vp]
+        L.lora_bgmv.restype = i32
+        L.lora_bgmv.argtypes = [vp, i64, vp, i64, vp, i32, view_p, vp, vp]
+        L.lora_pool_pages_needed.restype = i64
+        L.lora_pool_pages_needed.argtypes = [i32, i32, i32, i32]
+        L.lora_status_string.restype = ctypes.c_char_p
+        L.lora_status_string.argtypes = [i32]
+        L.lora_abi_version.restype = i32
+        L.lora_abi_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def status_string(status: int) -> str:
+    return lib().lora_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != LORA_OK:
+        raise LoraError(status, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _ld(t: torch.Tensor) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D row-major tensor with unit column stride")
+    return int(t.stride(0))
+
+
+# ------------------------------------------------------------ device views --
+
+class PoolView:
+    """A projection's paged adapter pool on the device plus its C view."""
+
+    def __init__(self, pool: torch.Tensor, page_list: torch.Tensor, adapters: torch.Tensor,
+                 page_elems: int, max_rank: int, d_in: int, d_out: int):
+        self.pool = pool  # bf16 (or int16 bits) [n_pages, page_elems]
+        self.page_list = page_list  # int32
+        self.adapters = adapters  # uint8 [n_adapters * 16] or int32 [n_adapters, 4]
+        self.c = lora_pool_view_t(
+            pool.data_ptr(), pool.numel() // page_elems, page_list.data_ptr(), page_list.numel(),
+            adapters.data_ptr(), adapters.numel() * adapters.element_size() // 16, page_elems,
+            max_rank, d_in, d_out)
+
+    @classmethod
+    def from_host(cls, host_pool, device="cuda"):
+        """Upload a workloads.AdapterPool."""
+        pool = torch.from_numpy(host_pool.pool.view(np.int16)).to(device).view(torch.bfloat16)
+        pl = torch.from_numpy(np.ascontiguousarray(host_pool.page_list, dtype=np.int32)).to(device)
+        desc = torch.from_numpy(np.ascontiguousarray(host_pool.desc).view(np.uint8)).to(device)
+        return cls(pool, pl, desc, host_pool.page_elems, host_pool.max_rank, host_pool.d_in,
+                   host_pool.d_out)
+
+    @property
+    def d_in(self):
+        return self.c.d_in
+
+    @property
+    def d_out(self):
+        return self.c.d_out
+
+
+class Segments:
+    """A device buffer carved into the segment arrays for T tokens."""
+
+    def __init__(self, T: int, device="cuda"):
+        nbytes = int(lib().lora_segments_buffer_bytes(T))
+        self.buf = torch.zeros(max(nbytes, 16) // 4 + 4, dtype=torch.int32, device=device)
+        self.c = lora_segments_t()
+        _check(lib().lora_segments_carve(_ptr(self.buf), self.buf.numel() * 4, T, ctypes.byref(self.c)),
+               "lora_segments_carve")
+        self.T = T
+
+    def _view(self, ptr_field: str, n: int) -> torch.Tensor:
+        off = (getattr(self.c, ptr_field) - self.buf.data_ptr()) // 4
+        return self.buf[off: off + n]
+
+    @property
+    def meta(self) -> torch.Tensor:
+        return self._view("meta", 8)
+
+    def host(self):
+        """(perm, indptr, seg_adapter, n_tokens, short_units, long_units [n, 2]) on the host."""
+        meta = self.meta.cpu().numpy()
+        n_segs, n_tok, n_short, n_long = (int(v) for v in meta[:4])
+        perm = self._view("token_perm", n_tok).cpu().numpy()
+        indptr = self._view("seg_indptr", n_segs + 1).cpu().numpy()
+        seg_ad = self._view("seg_adapter", n_segs).cpu().numpy()
+        short = self._view("short_units", n_short).cpu().numpy()
+        long_ = self._view("long_units", 2 * n_long).cpu().numpy().reshape(-1, 2)
+        return perm, indptr, seg_ad, n_tok, short, long_
+
+
+# ------------------------------------------------------------ entry points --
+
+def lora_segments_buffer_bytes(T: int) -> int:
+    return int(lib().lora_segments_buffer_bytes(T))
+
+
+def lora_pool_pages_needed(rank: int, d_in: int, d_out: int, page_elems: int) -> int:
+    return int(lib().lora_pool_pages_needed(rank, d_in, d_out, page_elems))
+
+
+def lora_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def lora_abi_version() -> int:
+    return int(lib().lora_abi_version())
+
+
+def lora_segments_build(token_adapter: torch.Tensor, n_adapters: int, seg: Segments,
+                        mode: int = LORA_SEG_GROUP, err: Optional[torch.Tensor] = None, stream=None):
+    T = int(token_adapter.numel())
+    _check(lib().lora_segments_build(_ptr(token_adapter), T, n_adapters, mode, ctypes.byref(seg.c),
+                                     _ptr(err), _stream(stream)), "lora_segments_build")
+
+
+def lora_sgmv_shrink(x: torch.Tensor, h: torch.Tensor, seg: Segments, view: PoolView,
+                     err: Optional[torch.Tensor] = None, stream=None):
+    _check(lib().lora_sgmv_shrink(_ptr(x), _ld(x), _ptr(h), _ld(h), ctypes.byref(seg.c),
+                                  ctypes.byref(view.c), _ptr(err), _stream(stream)),
+           "lora_sgmv_shrink")
+
+
+def lora_sgmv_expand(h: torch.Tensor, y: torch.Tensor, seg: Segments, view: PoolView,
+                     err: Optional[torch.Tensor] = None, stream=None):
+    _check(lib().lora_sgmv_expand(_ptr(h), _ld(h), _ptr(y), _ld(y), ctypes.byref(seg.c),
+                                  ctypes.byref(view.c), _ptr(err), _stream(stream)),
+           "lora_sgmv_expand")
+
+
+def lora_apply(x: torch.Tensor, y: torch.Tensor, seg: Segments, view: PoolView,
+               err: Optional[torch.Tensor] = None, stream=None):
+    _check(lib().lora_apply(_ptr(x), _ld(x), _ptr(y), _ld(y), ctypes.byref(seg.c),
+                            ctypes.byref(view.c), _ptr(err), _stream(stream)), "lora_apply")
+
+
+def lora_bgmv(x: torch.Tensor, y: torch.Tensor, token_adapter: torch.Tensor, view: PoolView,
+              err: Optional[torch.Tensor] = None, stream=None):
+    T = int(token_adapter.numel())
+    _check(lib().lora_bgmv(_ptr(x), _ld(x), _ptr(y), _ld(y), _ptr(token_adapter), T,
+                           ctypes.byref(view.c), _ptr(err), _stream(stream)), "lora_bgmv")

@@ -1,0 +1,261 @@
+// C ABI entry points: host-side argument checks, then launches on the caller's
+// stream.  Nothing here allocates device memory or synchronises.
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace lora {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_pow2(long long v) { return v > 0 && (v & (v - 1)) == 0; }
+
+int log2i(long long v) {
+  int s = 0;
+  while ((1LL << s) < v) ++s;
+  return s;
+}
+
+lora_status_t check_view(const lora_pool_view_t* v) {
+  if (v == nullptr) return LORA_ERR_INVALID_ARG;
+  if (v->pool == nullptr || v->page_list == nullptr || v->adapters == nullptr) return LORA_ERR_INVALID_ARG;
+  if (!aligned16(v->pool)) return LORA_ERR_INVALID_ARG;
+  if (v->n_pages < 1 || v->n_page_list < 1 || v->n_adapters < 1) return LORA_ERR_INVALID_ARG;
+  if (v->page_elems < 8 || v->page_elems % 8 != 0) return LORA_ERR_INVALID_ARG;
+  if (!is_pow2(v->page_elems) || v->page_elems < 64 || v->page_elems > (1 << 30)) return LORA_ERR_UNSUPPORTED;
+  if (v->d_in < 8 || v->d_out < 8 || v->d_in % 8 != 0 || v->d_out % 8 != 0) return LORA_ERR_INVALID_ARG;
+  if (v->max_rank < 1) return LORA_ERR_INVALID_ARG;
+  if (v->max_rank > LORA_MAX_RANK) return LORA_ERR_UNSUPPORTED;
+  if (v->n_pages > (1LL << 40) / v->page_elems) return LORA_ERR_UNSUPPORTED;
+  return LORA_OK;
+}
+
+lora_status_t check_seg(const lora_segments_t* s) {
+  if (s == nullptr) return LORA_ERR_INVALID_ARG;
+  if (s->T < 0) return LORA_ERR_INVALID_ARG;
+  if (s->T == 0) return LORA_OK;
+  if (!s->token_perm || !s->seg_indptr || !s->seg_adapter || !s->meta || !s->short_units ||
+      !s->long_units || !s->scratch)
+    return LORA_ERR_INVALID_ARG;
+  const long long need = (long long)s->T / LORA_TILE_M + (long long)s->T / (LORA_SHORT_MAX_TOKENS + 1) + 1;
+  if (s->max_long_units < need) return LORA_ERR_WORKSPACE;
+  return LORA_OK;
+}
+
+// An activation matrix [T, ld] of bf16 with `width` used columns.
+lora_status_t check_act(const void* p, long long ld, int width, int T) {
+  if (T == 0) return LORA_OK;
+  if (p == nullptr || !aligned16(p)) return LORA_ERR_INVALID_ARG;
+  if (ld < width || ld % 8 != 0) return LORA_ERR_INVALID_ARG;
+  return LORA_OK;
+}
+
+bool overlap(const void* a, long long abytes, const void* b, long long bbytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + (uintptr_t)bbytes && b0 < a0 + (uintptr_t)abytes;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void* func, size_t bytes) {
+  // A few kernels, each raised once per device to its largest request.
+  static std::atomic<size_t> cache[8][kMaxDevices];
+  static std::atomic<const void*> funcs[8];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  int slot = -1;
+  for (int i = 0; i < 8; ++i) {
+    const void* f = funcs[i].load();
+    if (f == func) { slot = i; break; }
+    if (f == nullptr) {
+      const void* expected = nullptr;
+      if (funcs[i].compare_exchange_strong(expected, func) || expected == func) { slot = i; break; }
+    }
+  }
+  if (slot >= 0 && cache[slot][dev].load() >= bytes) return cudaSuccess;
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && slot >= 0) {
+    size_t cur = cache[slot][dev].load();
+    while (cur < bytes && !cache[slot][dev].compare_exchange_weak(cur, bytes)) {}
+  }
+  return e;
+}
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < kMaxDevices) {
+    int c = g_sm_count[dev].load();
+    if (c > 0) return c;
+  }
+  int c = 1;
+  if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c < 1) c = 1;
+  if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(c);
+  return c;
+}
+
+void make_dev_view(const lora_pool_view_t* v, DevView* out) {
+  out->pool = static_cast<const uint16_t*>(v->pool);
+  out->page_list = v->page_list;
+  out->adapters = v->adapters;
+  out->n_pages = v->n_pages;
+  out->n_page_list = v->n_page_list;
+  out->n_adapters = v->n_adapters;
+  out->page_shift = log2i(v->page_elems);
+  out->max_rank = v->max_rank;
+  out->d_in = v->d_in;
+  out->d_out = v->d_out;
+}
+
+}  // namespace lora
+
+using namespace lora;
+
+extern "C" {
+
+int32_t lora_abi_version(void) { return LORA_ABI_VERSION; }
+
+const char* lora_status_string(lora_status_t s) {
+  switch (s) {
+    case LORA_OK: return "ok";
+    case LORA_ERR_INVALID_ARG: return "invalid argument";
+    case LORA_ERR_UNSUPPORTED: return "unsupported by this build";
+    case LORA_ERR_CUDA: return "CUDA runtime error";
+    case LORA_ERR_WORKSPACE: return "segment buffer too small";
+    default: return "unknown status";
+  }
+}
+
+int64_t lora_pool_pages_needed(int32_t rank, int32_t d_in, int32_t d_out, int32_t page_elems) {
+  if (rank < 0 || d_in < 0 || d_out < 0 || page_elems < 1) return -1;
+  const int64_t a = (int64_t)rank * d_in, b = (int64_t)rank * d_out;
+  return (a + page_elems - 1) / page_elems + (b + page_elems - 1) / page_elems;
+}
+
+static size_t seg_layout(int32_t T, size_t* off) {
+  // token_perm, seg_indptr, seg_adapter, meta, short_units, long_units, scratch
+  const size_t t = (size_t)(T > 0 ? T : 0);
+  const size_t n_long = t / LORA_TILE_M + t / (LORA_SHORT_MAX_TOKENS + 1) + 1;
+  const size_t sizes[7] = {t, t + 1, t, 8, t, 2 * n_long, 4 * t + 8};
+  size_t cur = 0;
+  for (int i = 0; i < 7; ++i) {
+    if (off) off[i] = cur;
+    cur = align_up(cur + sizes[i] * sizeof(int32_t), 16);
+  }
+  return cur;
+}
+
+size_t lora_segments_buffer_bytes(int32_t T) {
+  if (T < 0) return 0;
+  return seg_layout(T, nullptr);
+}
+
+lora_status_t lora_segments_carve(void* buf, size_t bytes, int32_t T, lora_segments_t* out) {
+  if (out == nullptr || T < 0) return LORA_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  if (buf == nullptr || !aligned16(buf)) return LORA_ERR_INVALID_ARG;
+  size_t off[7];
+  const size_t need = seg_layout(T, off);
+  if (bytes < need) return LORA_ERR_WORKSPACE;
+  char* b = static_cast<char*>(buf);
+  out->T = T;
+  out->max_long_units = (int32_t)(T / LORA_TILE_M + T / (LORA_SHORT_MAX_TOKENS + 1) + 1);
+  out->token_perm = reinterpret_cast<int32_t*>(b + off[0]);
+  out->seg_indptr = reinterpret_cast<int32_t*>(b + off[1]);
+  out->seg_adapter = reinterpret_cast<int32_t*>(b + off[2]);
+  out->meta = reinterpret_cast<int32_t*>(b + off[3]);
+  out->short_units = reinterpret_cast<int32_t*>(b + off[4]);
+  out->long_units = reinterpret_cast<int32_t*>(b + off[5]);
+  out->scratch = reinterpret_cast<int32_t*>(b + off[6]);
+  return LORA_OK;
+}
+
+lora_status_t lora_segments_build(const int32_t* token_adapter, int32_t T, int32_t n_adapters,
+                                  int32_t mode, const lora_segments_t* seg, int32_t* dev_err,
+                                  lora_stream_t stream) {
+  if (seg == nullptr || T < 0 || T != seg->T) return LORA_ERR_INVALID_ARG;
+  if (mode != LORA_SEG_GROUP && mode != LORA_SEG_CONTIGUOUS) return LORA_ERR_INVALID_ARG;
+  if (n_adapters < 1) return LORA_ERR_INVALID_ARG;
+  if (n_adapters > LORA_MAX_ADAPTERS) return LORA_ERR_UNSUPPORTED;
+  if (seg->meta == nullptr || seg->seg_indptr == nullptr) return LORA_ERR_INVALID_ARG;
+  if (T > 0 && token_adapter == nullptr) return LORA_ERR_INVALID_ARG;
+  lora_status_t st = check_seg(seg);
+  if (st != LORA_OK) return st;
+  return launch_segments(token_adapter, T, n_adapters, mode, seg, dev_err, (cudaStream_t)stream);
+}
+
+static lora_status_t run_segmented(int mode, const void* x, long long ldx, void* y, long long ldy,
+                                   float* h, long long ldh, const lora_segments_t* seg,
+                                   const lora_pool_view_t* view, int32_t* dev_err, cudaStream_t s) {
+  return launch_gather(mode, kSrcSegments, x, ldx, y, ldy, h, ldh, seg, nullptr, 0, view, dev_err, s);
+}
+
+lora_status_t lora_sgmv_shrink(const void* x, int64_t ldx, float* h, int64_t ldh,
+                               const lora_segments_t* seg, const lora_pool_view_t* view,
+                               int32_t* dev_err, lora_stream_t stream) {
+  lora_status_t st = check_view(view);
+  if (st != LORA_OK) return st;
+  if ((st = check_seg(seg)) != LORA_OK) return st;
+  const int T = seg->T;
+  if ((st = check_act(x, ldx, view->d_in, T)) != LORA_OK) return st;
+  if (T > 0 && (h == nullptr || !aligned16(h) || ldh < view->max_rank || ldh % 4 != 0)) return LORA_ERR_INVALID_ARG;
+  if (T == 0) return LORA_OK;
+  return run_segmented(kModeShrink, x, ldx, nullptr, 0, h, ldh, seg, view, dev_err, (cudaStream_t)stream);
+}
+
+lora_status_t lora_sgmv_expand(const float* h, int64_t ldh, void* y, int64_t ldy,
+                               const lora_segments_t* seg, const lora_pool_view_t* view,
+                               int32_t* dev_err, lora_stream_t stream) {
+  lora_status_t st = check_view(view);
+  if (st != LORA_OK) return st;
+  if ((st = check_seg(seg)) != LORA_OK) return st;
+  const int T = seg->T;
+  if ((st = check_act(y, ldy, view->d_out, T)) != LORA_OK) return st;
+  if (T > 0 && (h == nullptr || !aligned16(h) || ldh < view->max_rank || ldh % 4 != 0)) return LORA_ERR_INVALID_ARG;
+  if (T > 0 && overlap(h, (long long)T * ldh * 4, y, (long long)T * ldy * 2)) return LORA_ERR_INVALID_ARG;
+  if (T == 0) return LORA_OK;
+  return run_segmented(kModeExpand, nullptr, 0, y, ldy, const_cast<float*>(h), ldh, seg, view, dev_err,
+                       (cudaStream_t)stream);
+}
+
+lora_status_t lora_apply(const void* x, int64_t ldx, void* y, int64_t ldy, const lora_segments_t* seg,
+                         const lora_pool_view_t* view, int32_t* dev_err, lora_stream_t stream) {
+  lora_status_t st = check_view(view);
+  if (st != LORA_OK) return st;
+  if ((st = check_seg(seg)) != LORA_OK) return st;
+  const int T = seg->T;
+  if ((st = check_act(x, ldx, view->d_in, T)) != LORA_OK) return st;
+  if ((st = check_act(y, ldy, view->d_out, T)) != LORA_OK) return st;
+  if (T > 0 && overlap(x, (long long)T * ldx * 2, y, (long long)T * ldy * 2)) return LORA_ERR_INVALID_ARG;
+  if (T == 0) return LORA_OK;
+  return run_segmented(kModeApply, x, ldx, y, ldy, nullptr, 0, seg, view, dev_err, (cudaStream_t)stream);
+}
+
+lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy, const int32_t* token_adapter,
+                        int32_t T, const lora_pool_view_t* view, int32_t* dev_err, lora_stream_t stream) {
+  lora_status_t st = check_view(view);
+  if (st != LORA_OK) return st;
+  if (T < 0) return LORA_ERR_INVALID_ARG;
+  if ((st = check_act(x, ldx, view->d_in, T)) != LORA_OK) return st;
+  if ((st = check_act(y, ldy, view->d_out, T)) != LORA_OK) return st;
+  if (T > 0 && token_adapter == nullptr) return LORA_ERR_INVALID_ARG;
+  if (T > 0 && overlap(x, (long long)T * ldx * 2, y, (long long)T * ldy * 2)) return LORA_ERR_INVALID_ARG;
+  if (T == 0) return LORA_OK;
+  return launch_gather(kModeApply, kSrcTokens, x, ldx, y, ldy, nullptr, 0, nullptr, token_adapter, T, view,
+                       dev_err, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,36 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lora_sgmv.h"
+
+namespace lora {
+
+struct DevView;
+
+// Raise a kernel's dynamic shared-memory limit on the current device (once per
+// device and size).
+cudaError_t ensure_smem_attr(const void* func, size_t bytes);
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
+
+// Fill a DevView from a validated host view.
+void make_dev_view(const lora_pool_view_t* v, DevView* out);
+
+lora_status_t launch_segments(const int32_t* ids, int T, int n_adapters, int mode,
+                              const lora_segments_t* seg, int32_t* err, cudaStream_t stream);
+
+enum GatherMode { kModeApply = 0, kModeShrink = 1, kModeExpand = 2 };
+enum GatherSrc { kSrcSegments = 0, kSrcTokens = 1 };
+
+// CUDA-core gather kernel over the segments' work lists (short units, then
+// long tiles) or over one-token units.
+lora_status_t launch_gather(int mode, int src, const void* x, long long ldx, void* y,
+                            long long ldy, float* h, long long ldh, const lora_segments_t* seg,
+                            const int32_t* token_adapter, int T, const lora_pool_view_t* view,
+                            int32_t* err, cudaStream_t stream);
+
+}  // namespace lora

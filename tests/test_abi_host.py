@@ -1,0 +1,150 @@
+"""The C-ABI library on the host: it loads, exports every symbol include/lora_sgmv.h
+declares, and rejects bad arguments before launching anything (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from segmented_gather_gemm_lora_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lora_sgmv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lora_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    L = B.lib()
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(B.EXPORTED) == set(names)
+
+
+def test_abi_version_and_status_strings():
+    assert B.lora_abi_version() == 1
+    assert B.lora_status_string(0) == "ok"
+    assert "invalid" in B.lora_status_string(-1)
+    assert "unsupported" in B.lora_status_string(-2)
+    assert B.lora_status_string(-99) == "unknown status"
+
+
+def test_struct_sizes_match_c_layout():
+    assert ctypes.sizeof(B.lora_adapter_desc_t) == 16
+    assert ctypes.sizeof(B.lora_pool_view_t) == 64
+    assert ctypes.sizeof(B.lora_segments_t) == 8 + 7 * 8
+
+
+@pytest.mark.parametrize("rank,d_in,d_out,P", [(16, 8192, 8192, 4096), (13, 5120, 11008, 4096),
+                                                (64, 13824, 5120, 4096), (1, 8, 8, 64)])
+def test_pages_needed_matches_oracle(rank, d_in, d_out, P):
+    assert B.lora_pool_pages_needed(rank, d_in, d_out, P) == oracle.pages_needed(rank, d_in, d_out, P)
+
+
+def test_carve_layout():
+    L = B.lib()
+    for T in (0, 1, 16, 64, 129, 9216):
+        n = B.lora_segments_buffer_bytes(T)
+        assert n % 16 == 0 and n >= 4 * (4 * T + 8)
+        buf = (ctypes.c_uint8 * (n + 16))()
+        base = (ctypes.addressof(buf) + 15) // 16 * 16
+        s = B.lora_segments_t()
+        assert L.lora_segments_carve(ctypes.c_void_p(base), n, T, ctypes.byref(s)) == 0
+        assert s.T == T
+        assert s.max_long_units == T // 128 + T // 9 + 1
+        ptrs = [s.token_perm, s.seg_indptr, s.seg_adapter, s.meta, s.short_units, s.long_units, s.scratch]
+        assert all(p % 16 == 0 for p in ptrs)
+        assert ptrs == sorted(ptrs) and ptrs[0] == base
+        assert L.lora_segments_carve(ctypes.c_void_p(base), n - 16, T, ctypes.byref(s)) == B.LORA_ERR_WORKSPACE
+        assert L.lora_segments_carve(ctypes.c_void_p(base + 4), n, T, ctypes.byref(s)) == B.LORA_ERR_INVALID_ARG
+
+
+def fake_view(**kw):
+    v = dict(pool=0x10000, n_pages=10, page_list=0x20000, n_page_list=10, adapters=0x30000,
+             n_adapters=4, page_elems=4096, max_rank=16, d_in=256, d_out=256)
+    v.update(kw)
+    return B.lora_pool_view_t(v["pool"], v["n_pages"], v["page_list"], v["n_page_list"], v["adapters"],
+                              v["n_adapters"], v["page_elems"], v["max_rank"], v["d_in"], v["d_out"])
+
+
+def fake_seg(T=16):
+    s = B.lora_segments_t()
+    s.T = T
+    s.max_long_units = T // 128 + T // 9 + 1
+    for i, f in enumerate(("token_perm", "seg_indptr", "seg_adapter", "meta", "short_units",
+                           "long_units", "scratch")):
+        setattr(s, f, 0x100000 + 0x1000 * i)
+    return s
+
+
+@pytest.mark.parametrize("bad,want", [
+    (dict(pool=0x10008), B.LORA_ERR_INVALID_ARG),  # misaligned pool
+    (dict(pool=0), B.LORA_ERR_INVALID_ARG),
+    (dict(d_in=250), B.LORA_ERR_INVALID_ARG),  # not a multiple of 8
+    (dict(d_out=0), B.LORA_ERR_INVALID_ARG),
+    (dict(max_rank=0), B.LORA_ERR_INVALID_ARG),
+    (dict(max_rank=65), B.LORA_ERR_UNSUPPORTED),
+    (dict(page_elems=4004), B.LORA_ERR_INVALID_ARG),  # not a multiple of 8
+    (dict(page_elems=3072), B.LORA_ERR_UNSUPPORTED),  # not a power of two
+    (dict(page_elems=32), B.LORA_ERR_UNSUPPORTED),
+    (dict(n_adapters=0), B.LORA_ERR_INVALID_ARG),
+])
+def test_apply_rejects_bad_views_without_launch(bad, want):
+    L = B.lib()
+    seg = fake_seg()
+    v = fake_view(**bad)
+    rc = L.lora_apply(ctypes.c_void_p(0x400000), 256, ctypes.c_void_p(0x800000), 256, ctypes.byref(seg),
+                      ctypes.byref(v), None, None)
+    assert rc == want
+
+
+def test_apply_rejects_bad_activations_without_launch():
+    L = B.lib()
+    seg = fake_seg(16)
+    v = fake_view()
+    x, y = ctypes.c_void_p(0x400000), ctypes.c_void_p(0x800000)
+    # misaligned, short stride, stride not a multiple of 8, x overlapping y
+    assert L.lora_apply(ctypes.c_void_p(0x400002), 256, y, 256, ctypes.byref(seg), ctypes.byref(v), None, None) == -1
+    assert L.lora_apply(x, 128, y, 256, ctypes.byref(seg), ctypes.byref(v), None, None) == -1
+    assert L.lora_apply(x, 260, y, 256, ctypes.byref(seg), ctypes.byref(v), None, None) == -1
+    assert L.lora_apply(x, 256, ctypes.c_void_p(0x400000 + 512 * 8), 256, ctypes.byref(seg),
+                        ctypes.byref(v), None, None) == -1
+    assert L.lora_apply(x, 256, y, 256, None, ctypes.byref(v), None, None) == -1
+    # a segment buffer carved for more tokens than it can hold
+    small = fake_seg(16)
+    small.max_long_units = 1
+    assert L.lora_apply(x, 256, y, 256, ctypes.byref(small), ctypes.byref(v), None, None) == B.LORA_ERR_WORKSPACE
+
+
+def test_other_entry_points_reject_bad_arguments():
+    L = B.lib()
+    seg = fake_seg(16)
+    v = fake_view()
+    x, y, h = ctypes.c_void_p(0x400000), ctypes.c_void_p(0x800000), ctypes.c_void_p(0xC00000)
+    assert L.lora_sgmv_shrink(x, 256, h, 8, ctypes.byref(seg), ctypes.byref(v), None, None) == -1  # ldh < max_rank
+    assert L.lora_sgmv_shrink(x, 256, h, 18, ctypes.byref(seg), ctypes.byref(v), None, None) == -1  # ldh % 4
+    assert L.lora_sgmv_expand(h, 16, y, 100, ctypes.byref(seg), ctypes.byref(v), None, None) == -1
+    assert L.lora_bgmv(x, 256, y, 256, None, 4, ctypes.byref(v), None, None) == -1
+    assert L.lora_bgmv(x, 256, y, 256, ctypes.c_void_p(0x900000), -1, ctypes.byref(v), None, None) == -1
+    assert L.lora_segments_build(ctypes.c_void_p(0x900000), 16, 4, 2, ctypes.byref(seg), None, None) == -1
+    assert L.lora_segments_build(ctypes.c_void_p(0x900000), 16, 0, 0, ctypes.byref(seg), None, None) == -1
+    assert L.lora_segments_build(ctypes.c_void_p(0x900000), 16, 40000, 0, ctypes.byref(seg), None, None) == -2
+    assert L.lora_segments_build(ctypes.c_void_p(0x900000), 17, 4, 0, ctypes.byref(seg), None, None) == -1
+
+
+def test_empty_batches_are_noops_without_launch():
+    L = B.lib()
+    seg = fake_seg(0)
+    v = fake_view()
+    assert L.lora_apply(None, 256, None, 256, ctypes.byref(seg), ctypes.byref(v), None, None) == 0
+    assert L.lora_bgmv(None, 256, None, 256, None, 0, ctypes.byref(v), None, None) == 0
+    assert L.lora_sgmv_shrink(None, 256, None, 16, ctypes.byref(seg), ctypes.byref(v), None, None) == 0

@@ -1,0 +1,362 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the same
+seeded inputs -- bit-exact for segments and work lists, within the stated tolerance
+for the LoRA outputs -- plus the invariants that must hold on the GPU too."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from segmented_gather_gemm_lora_gb300 import binding as B
+from segmented_gather_gemm_lora_gb300 import workloads as W
+from gpu_util import (compare_bf16, cuda_or_skip, ids_dev, new_err, run_apply, run_bgmv,
+                      to_dev_bits, to_host_bits)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    cuda_or_skip()
+
+
+def f64(bits):
+    return W.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+# ------------------------------------------------------------------ segments --
+
+def segment_cases():
+    rng = np.random.default_rng(100)
+    cases = [
+        ("empty", np.array([], dtype=np.int32), 4),
+        ("all_none", np.full(33, -1, dtype=np.int32), 4),
+        ("one_adapter", np.zeros(300, dtype=np.int32), 1),
+        ("all_distinct", np.arange(1500, dtype=np.int32)[::-1].copy(), 1500),
+        ("max_id", np.full(40, 999, dtype=np.int32), 1000),
+        ("runs_broken", np.array([3, 3, 1, 1, 3, -1, 3, 0, 0, 3, 3, 3], dtype=np.int32), 4),
+        ("tile_edges", np.repeat(np.arange(6, dtype=np.int32), [8, 9, 127, 128, 129, 1024]), 6),
+    ]
+    for i in range(12):
+        T = int(rng.integers(1, 5000))
+        n = int(rng.integers(1, 2000))
+        cases.append(("rand%d" % i, rng.integers(-1, n, size=T).astype(np.int32), n))
+        k = int(rng.integers(1, 60))
+        runs = np.repeat(rng.integers(-1, n, size=k), rng.integers(1, 400, size=k)).astype(np.int32)
+        cases.append(("runs%d" % i, runs, n))
+    cases.append(("decode", W.decode(0).batch.ids, 100))
+    cases.append(("prefill", W.prefill(0).batch.ids, 200))
+    cases.append(("hetero", W.hetero(0, which="up").batch.ids, 500))
+    rng2 = np.random.default_rng(0)
+    W.mixed13b_ranks(rng2)
+    cases.append(("mixed13b", W.mixed13b_ids(rng2), 1000))
+    cases.append(("big_catalogue", rng.integers(0, 32768, size=3000).astype(np.int32), 32768))
+    cases.append(("long_batch", np.repeat(rng.integers(0, 50, size=40), 1200).astype(np.int32), 50))
+    return cases
+
+
+@pytest.mark.parametrize("mode", [B.LORA_SEG_GROUP, B.LORA_SEG_CONTIGUOUS])
+def test_segments_bit_exact(mode):
+    for name, ids, n_ad in segment_cases():
+        seg = B.Segments(len(ids))
+        err = new_err()
+        B.lora_segments_build(ids_dev(ids), n_ad, seg, mode=mode, err=err)
+        torch.cuda.synchronize()
+        perm, indptr, seg_ad, n_tok, short, long_ = seg.host()
+        o_perm, o_indptr, o_ad, o_ntok, o_err = oracle.segments_build(ids, n_ad, mode)
+        o_short, o_long = oracle.work_lists(o_indptr, B.LORA_SHORT_MAX_TOKENS, B.LORA_TILE_M)
+        assert n_tok == o_ntok, name
+        assert np.array_equal(perm, o_perm), name
+        assert np.array_equal(indptr, o_indptr), name
+        assert np.array_equal(seg_ad, o_ad), name
+        assert np.array_equal(short, o_short), name
+        assert np.array_equal(long_, o_long), name
+        assert int(err.item()) == o_err, name
+
+
+def test_segments_flag_bad_ids():
+    ids = np.array([0, 7, -5, 1, 1, 2], dtype=np.int32)
+    seg = B.Segments(len(ids))
+    err = new_err()
+    B.lora_segments_build(ids_dev(ids), 3, seg, err=err)
+    torch.cuda.synchronize()
+    perm, indptr, seg_ad, n_tok, _, _ = seg.host()
+    assert int(err.item()) == B.LORA_DERR_BAD_ADAPTER
+    assert perm.tolist() == [0, 3, 4, 5]
+    assert seg_ad.tolist() == [0, 1, 2]
+
+
+# -------------------------------------------------------------------- apply --
+
+def check_untouched(y_bits, batch, pool, rows):
+    """Rows in `rows` and every guard column must equal y0 bit for bit."""
+    assert np.array_equal(y_bits[rows], batch.y0[rows])
+    assert np.array_equal(y_bits[:, pool.d_out:], batch.y0[:, pool.d_out:])
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_apply_tiny(seed):
+    wl = W.tiny(seed)
+    pool = wl.pools[0]
+    y, err, _ = run_apply(wl.batch, pool, wl.mode, wl.n_adapters)
+    ref, oerr = oracle.lora_apply(wl.batch.x, wl.batch.y0, wl.batch.ids, pool)
+    assert err == oerr == 0
+    compare_bf16(y[:, : pool.d_out], ref, "tiny seed %d" % seed)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_apply_decode(seed):
+    wl = W.decode(seed)
+    pool = wl.pools[0]
+    y, err, _ = run_apply(wl.batch, pool, wl.mode, wl.n_adapters)
+    ref, _ = oracle.lora_apply(wl.batch.x, wl.batch.y0, wl.batch.ids, pool)
+    assert err == 0
+    compare_bf16(y, ref, "decode seed %d" % seed)
+
+
+@pytest.mark.parametrize("mode", [B.LORA_SEG_CONTIGUOUS, B.LORA_SEG_GROUP])
+def test_apply_prefill_small(mode):
+    wl = W.prefill(1, n_requests=5)
+    pool = wl.pools[0]
+    y, err, _ = run_apply(wl.batch, pool, mode, wl.n_adapters)
+    ref, _ = oracle.lora_apply(wl.batch.x, wl.batch.y0, wl.batch.ids, pool)
+    assert err == 0
+    compare_bf16(y, ref, "prefill(5 requests)")
+
+
+@pytest.mark.parametrize("which", ["up", "down"])
+def test_apply_hetero(which):
+    wl = W.hetero(0, which=which)
+    pool = wl.pools[0]
+    rng = np.random.default_rng(7)
+    batch = W.make_batch(rng, wl.batch.ids, pool.d_in, pool.d_out, ldx=pool.d_in + 16,
+                         ldy=pool.d_out + 8)
+    y, err, _ = run_apply(batch, pool, wl.mode, wl.n_adapters)
+    ref, _ = oracle.lora_apply(batch.x, batch.y0, batch.ids, pool)
+    assert err == 0
+    compare_bf16(y[:, : pool.d_out], ref, "hetero " + which)
+    check_untouched(y, batch, pool, np.where(batch.ids < 0)[0])
+
+
+def test_apply_odd_shapes_and_ranks():
+    """Ranks that divide nothing, widths that are not multiples of the page, rows that
+    straddle pages, segment lengths around the dispatch thresholds, and -1 tokens."""
+    rng = np.random.default_rng(11)
+    ranks = [1, 7, 13, 33, 64, 8, 16]
+    pool = W.build_pool(rng, 5120, 1000, ranks, page_elems=4096, max_rank=64)
+    lens = [1, 2, 7, 8, 9, 127, 128, 129, 300]
+    ids = np.concatenate([np.full(n, i % len(ranks), dtype=np.int32) for i, n in enumerate(lens)])
+    ids[rng.choice(ids.size, 20, replace=False)] = -1
+    batch = W.make_batch(rng, ids, 5120, 1000, ldx=5128, ldy=1016)
+    for mode in (B.LORA_SEG_GROUP, B.LORA_SEG_CONTIGUOUS):
+        y, err, _ = run_apply(batch, pool, mode, len(ranks))
+        ref, _ = oracle.lora_apply(batch.x, batch.y0, ids, pool)
+        assert err == 0
+        compare_bf16(y[:, :1000], ref, "odd shapes mode %d" % mode)
+        check_untouched(y, batch, pool, np.where(ids < 0)[0])
+
+
+def test_apply_small_pages():
+    rng = np.random.default_rng(12)
+    pool = W.build_pool(rng, 256, 512, [8, 24, 64], page_elems=64, max_rank=64)
+    ids = rng.integers(-1, 3, size=200).astype(np.int32)
+    batch = W.make_batch(rng, ids, 256, 512)
+    y, err, _ = run_apply(batch, pool, B.LORA_SEG_GROUP, 3)
+    ref, _ = oracle.lora_apply(batch.x, batch.y0, ids, pool)
+    assert err == 0
+    compare_bf16(y, ref, "64-element pages")
+
+
+def test_apply_mixed13b_layer_sampled():
+    """13B-shaped mixed batch, one layer's seven projections, full T = 4224; the oracle
+    checks a sample of 160 rows (all decode rows' adapters are represented)."""
+    wl = W.mixed13b(0, layers=(0,))
+    rng = np.random.default_rng(13)
+    ids = wl.batch.ids
+    rows = np.sort(np.concatenate([rng.choice(4096, 96, replace=False), 4096 + rng.choice(128, 64, replace=False)]))
+    for pool in wl.pools:
+        batch = W.make_batch(rng, ids, pool.d_in, pool.d_out)
+        y, err, _ = run_apply(batch, pool, wl.mode, wl.n_adapters)
+        assert err == 0
+        ref, _ = oracle.lora_apply(batch.x[rows], batch.y0[rows], ids[rows], pool)
+        compare_bf16(y[rows], ref, "13B %dx%d" % (pool.d_in, pool.d_out))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode", [B.LORA_SEG_CONTIGUOUS, B.LORA_SEG_GROUP])
+def test_apply_prefill_full_sampled(mode):
+    wl = W.prefill(0)
+    pool = wl.pools[0]
+    y, err, _ = run_apply(wl.batch, pool, mode, wl.n_adapters)
+    assert err == 0
+    rng = np.random.default_rng(14)
+    rows = np.sort(rng.choice(wl.batch.T, 256, replace=False))
+    ref, _ = oracle.lora_apply(wl.batch.x[rows], wl.batch.y0[rows], wl.batch.ids[rows], pool)
+    compare_bf16(y[rows], ref, "prefill full")
+
+
+# --------------------------------------------------------------------- bgmv --
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "hetero"])
+def test_bgmv_parity(name):
+    wl = {"tiny": W.tiny, "decode": W.decode, "hetero": lambda s: W.hetero(s, which="up")}[name](0)
+    pool = wl.pools[0]
+    ids = wl.batch.ids.copy()
+    ids[::7] = -1
+    y, err = run_bgmv(wl.batch, pool, ids=ids)
+    ref, _ = oracle.lora_apply(wl.batch.x, wl.batch.y0, ids, pool)
+    assert err == 0
+    compare_bf16(y[:, : pool.d_out], ref, "bgmv " + name)
+    assert np.array_equal(y[ids < 0], wl.batch.y0[ids < 0])
+
+
+def test_bgmv_equals_apply_bitwise():
+    wl = W.decode(1)
+    pool = wl.pools[0]
+    yb, _ = run_bgmv(wl.batch, pool)
+    ya, _, _ = run_apply(wl.batch, pool, B.LORA_SEG_GROUP, wl.n_adapters)
+    assert np.array_equal(ya, yb)
+
+
+# ------------------------------------------------------------ shrink/expand --
+
+def test_shrink_parity_and_chain_equals_apply():
+    wl = W.hetero(1, which="down")
+    pool = wl.pools[0]
+    rng = np.random.default_rng(15)
+    batch = W.make_batch(rng, wl.batch.ids, pool.d_in, pool.d_out)
+    view = B.PoolView.from_host(pool)
+    x = to_dev_bits(batch.x)
+    y = to_dev_bits(batch.y0)
+    seg = B.Segments(batch.T)
+    err = new_err()
+    B.lora_segments_build(ids_dev(batch.ids), wl.n_adapters, seg, err=err)
+    ldh = 64
+    h = torch.full((batch.T, ldh), 7.0, dtype=torch.float32, device="cuda")
+    B.lora_sgmv_shrink(x, h, seg, view, err=err)
+    B.lora_sgmv_expand(h, y, seg, view, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    hh = h.cpu().numpy()
+    href, _ = oracle.shrink(batch.x, batch.ids, pool, h_init=np.full((batch.T, ldh), 7.0), ldh=ldh)
+    np.testing.assert_allclose(hh, href, rtol=1e-4, atol=1e-4)
+    ya, _, _ = run_apply(batch, pool, B.LORA_SEG_GROUP, wl.n_adapters, view=view)
+    assert np.array_equal(to_host_bits(y), ya)
+
+
+def test_expand_parity_random_h():
+    wl = W.hetero(2, which="up")
+    pool = wl.pools[0]
+    rng = np.random.default_rng(16)
+    batch = W.make_batch(rng, wl.batch.ids, pool.d_in, pool.d_out)
+    hin = rng.standard_normal((batch.T, 64), dtype=np.float32)
+    view = B.PoolView.from_host(pool)
+    y = to_dev_bits(batch.y0)
+    seg = B.Segments(batch.T)
+    err = new_err()
+    B.lora_segments_build(ids_dev(batch.ids), wl.n_adapters, seg, err=err)
+    B.lora_sgmv_expand(torch.from_numpy(hin).cuda(), y, seg, view, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref, _ = oracle.expand(hin, batch.y0, batch.ids, pool)
+    compare_bf16(to_host_bits(y), ref, "expand")
+
+
+# --------------------------------------------------------------- invariants --
+
+def test_zero_B_leaves_y0():
+    rng = np.random.default_rng(17)
+    pool = W.build_pool(rng, 4096, 4096, [16] * 20, zero_B=True)
+    ids = rng.integers(-1, 20, size=300).astype(np.int32)
+    batch = W.make_batch(rng, ids, 4096, 4096)
+    y, err, _ = run_apply(batch, pool, B.LORA_SEG_GROUP, 20)
+    assert err == 0
+    assert np.array_equal(W.bf16_bits_to_f32(y), W.bf16_bits_to_f32(batch.y0))
+
+
+def test_zero_padded_rank_equals_unpadded():
+    rng = np.random.default_rng(18)
+    d_in, d_out = 4096, 2048
+    base = W.build_pool(rng, d_in, d_out, [8, 16, 5], max_rank=64)
+    A, Bm, ranks = [], [], []
+    for i, r in enumerate(base.ranks):
+        rp = int(r) + 24
+        a = np.zeros((rp, d_in), dtype=np.uint16)
+        b = np.zeros((rp, d_out), dtype=np.uint16)
+        a[:r] = base.A[i]
+        b[:r] = base.B[i]
+        A.append(a)
+        Bm.append(b)
+        ranks.append(rp)
+    padded = W.pack_pool(A, Bm, np.array(ranks), d_in, d_out, rng, scales=base.scales, max_rank=64)
+    ids = np.repeat(rng.integers(0, 3, size=30), rng.integers(1, 40, size=30)).astype(np.int32)
+    batch = W.make_batch(rng, ids, d_in, d_out)
+    y1, e1, _ = run_apply(batch, base, B.LORA_SEG_GROUP, 3)
+    y2, e2, _ = run_apply(batch, padded, B.LORA_SEG_GROUP, 3)
+    assert e1 == e2 == 0
+    assert np.array_equal(W.bf16_bits_to_f32(y1), W.bf16_bits_to_f32(y2))
+
+
+def test_request_order_invariance_bitwise():
+    wl = W.prefill(3, n_requests=6)
+    pool = wl.pools[0]
+    ids = wl.batch.ids
+    # split into requests (runs) and reverse their order
+    starts = np.flatnonzero(np.r_[True, ids[1:] != ids[:-1]])
+    ends = np.r_[starts[1:], ids.size]
+    order = np.concatenate([np.arange(s, e) for s, e in list(zip(starts, ends))[::-1]])
+    b2 = W.Batch(x=wl.batch.x[order], y0=wl.batch.y0[order], ids=ids[order], d_in=4096, d_out=4096)
+    for mode in (B.LORA_SEG_GROUP, B.LORA_SEG_CONTIGUOUS):
+        y1, _, _ = run_apply(wl.batch, pool, mode, wl.n_adapters)
+        y2, _, _ = run_apply(b2, pool, mode, wl.n_adapters)
+        assert np.array_equal(y1[order], y2)
+
+
+def test_group_equals_contiguous_bitwise():
+    wl = W.prefill(4, n_requests=8)
+    pool = wl.pools[0]
+    y1, _, _ = run_apply(wl.batch, pool, B.LORA_SEG_GROUP, wl.n_adapters)
+    y2, _, _ = run_apply(wl.batch, pool, B.LORA_SEG_CONTIGUOUS, wl.n_adapters)
+    assert np.array_equal(y1, y2)
+
+
+# ---------------------------------------------------------------- error paths --
+
+def test_device_errors_flag_and_skip():
+    rng = np.random.default_rng(19)
+    pool = W.build_pool(rng, 1024, 1024, [16, 16, 16, 16], max_rank=16)
+    pool.desc[1]["rank"] = 32  # above max_rank
+    pool.page_list[int(pool.desc[2]["b_page0"]) + 1] = pool.n_pages + 3  # page outside the pool
+    pool.desc[3]["rank"] = 0  # not resident
+    ids = np.array([0, 1, 2, 3, 0, -1, 1, 0], dtype=np.int32)
+    batch = W.make_batch(rng, ids, 1024, 1024)
+    ref, oerr = oracle.lora_apply(batch.x, batch.y0, ids, pool)
+    y, err, _ = run_apply(batch, pool, B.LORA_SEG_GROUP, 4)
+    assert err == oerr == B.LORA_DERR_BAD_RANK | B.LORA_DERR_BAD_PAGE
+    good = ids == 0
+    compare_bf16(y[good], ref[good], "good rows next to bad ones")
+    assert np.array_equal(y[~good], batch.y0[~good])
+    yb, errb = run_bgmv(batch, pool)
+    assert errb == oerr
+    assert np.array_equal(yb[~good], batch.y0[~good])
+    ids2 = ids.copy()
+    ids2[2] = 9
+    yc, errc = run_bgmv(batch, pool, ids=ids2)
+    assert errc & B.LORA_DERR_BAD_ADAPTER
+    assert np.array_equal(yc[2], batch.y0[2])
+
+
+def test_empty_batch_is_noop():
+    wl = W.tiny(0)
+    view = B.PoolView.from_host(wl.pools[0])
+    seg = B.Segments(0)
+    err = new_err()
+    empty = torch.zeros(0, dtype=torch.int32, device="cuda")
+    B.lora_segments_build(empty, 4, seg, err=err)
+    x = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
+    B.lora_apply(x, y, seg, view, err=err)
+    B.lora_bgmv(x, y, empty, view, err=err)
+    torch.cuda.synchronize()
+    assert int(seg.meta[0].item()) == 0
+    assert int(err.item()) == 0
