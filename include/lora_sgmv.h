@@ -129,6 +129,8 @@ typedef struct {
   int32_t* short_units;   /* [T] */
   int32_t* long_units;    /* [2 * max_long_units] */
   int32_t* scratch;       /* [4 * T + 8]: run starts, run ends, run ids, run positions */
+  float* h_scratch;       /* [T * LORA_MAX_RANK]: lora_apply's rank-r intermediate of
+                             tokens on the tensor-core path, by segment position */
 } lora_segments_t;
 
 /** Bytes of the device buffer lora_segments_carve needs for T tokens (T >= 0). */

@@ -43,7 +43,7 @@ lora_status_t check_seg(const lora_segments_t* s) {
   if (s->T < 0) return LORA_ERR_INVALID_ARG;
   if (s->T == 0) return LORA_OK;
   if (!s->token_perm || !s->seg_indptr || !s->seg_adapter || !s->meta || !s->short_units ||
-      !s->long_units || !s->scratch)
+      !s->long_units || !s->scratch || !s->h_scratch)
     return LORA_ERR_INVALID_ARG;
   const long long need = (long long)s->T / LORA_TILE_M + (long long)s->T / (LORA_SHORT_MAX_TOKENS + 1) + 1;
   if (s->max_long_units < need) return LORA_ERR_WORKSPACE;
@@ -146,12 +146,12 @@ int64_t lora_pool_pages_needed(int32_t rank, int32_t d_in, int32_t d_out, int32_
 }
 
 static size_t seg_layout(int32_t T, size_t* off) {
-  // token_perm, seg_indptr, seg_adapter, meta, short_units, long_units, scratch
+  // token_perm, seg_indptr, seg_adapter, meta, short_units, long_units, scratch, h_scratch
   const size_t t = (size_t)(T > 0 ? T : 0);
   const size_t n_long = t / LORA_TILE_M + t / (LORA_SHORT_MAX_TOKENS + 1) + 1;
-  const size_t sizes[7] = {t, t + 1, t, 8, t, 2 * n_long, 4 * t + 8};
+  const size_t sizes[8] = {t, t + 1, t, 8, t, 2 * n_long, 4 * t + 8, t * LORA_MAX_RANK};
   size_t cur = 0;
-  for (int i = 0; i < 7; ++i) {
+  for (int i = 0; i < 8; ++i) {
     if (off) off[i] = cur;
     cur = align_up(cur + sizes[i] * sizeof(int32_t), 16);
   }
@@ -167,7 +167,7 @@ lora_status_t lora_segments_carve(void* buf, size_t bytes, int32_t T, lora_segme
   if (out == nullptr || T < 0) return LORA_ERR_INVALID_ARG;
   std::memset(out, 0, sizeof(*out));
   if (buf == nullptr || !aligned16(buf)) return LORA_ERR_INVALID_ARG;
-  size_t off[7];
+  size_t off[8];
   const size_t need = seg_layout(T, off);
   if (bytes < need) return LORA_ERR_WORKSPACE;
   char* b = static_cast<char*>(buf);
@@ -180,6 +180,7 @@ lora_status_t lora_segments_carve(void* buf, size_t bytes, int32_t T, lora_segme
   out->short_units = reinterpret_cast<int32_t*>(b + off[4]);
   out->long_units = reinterpret_cast<int32_t*>(b + off[5]);
   out->scratch = reinterpret_cast<int32_t*>(b + off[6]);
+  out->h_scratch = reinterpret_cast<float*>(b + off[7]);
   return LORA_OK;
 }
 
@@ -200,7 +201,21 @@ lora_status_t lora_segments_build(const int32_t* token_adapter, int32_t T, int32
 static lora_status_t run_segmented(int mode, const void* x, long long ldx, void* y, long long ldy,
                                    float* h, long long ldh, const lora_segments_t* seg,
                                    const lora_pool_view_t* view, int32_t* dev_err, cudaStream_t s) {
-  return launch_gather(mode, kSrcSegments, x, ldx, y, ldy, h, ldh, seg, nullptr, 0, view, dev_err, s);
+  // Long tiles go to the tensor-core kernels when the shapes allow it.
+  bool tc;
+  if (mode == kModeApply) tc = tc_shrink_ok(view) && tc_expand_ok(view);
+  else if (mode == kModeShrink) tc = tc_shrink_ok(view);
+  else tc = tc_expand_ok(view);
+  lora_status_t st = launch_gather(mode, kSrcSegments, tc ? 1 : 0, x, ldx, y, ldy, h, ldh, seg, nullptr, 0, view,
+                                   dev_err, s);
+  if (st != LORA_OK || !tc) return st;
+  if (mode == kModeApply) {
+    st = launch_shrink_tc(x, ldx, seg->h_scratch, LORA_MAX_RANK, 0, seg, view, dev_err, s);
+    if (st != LORA_OK) return st;
+    return launch_expand_tc(seg->h_scratch, LORA_MAX_RANK, 0, y, ldy, seg, view, dev_err, s);
+  }
+  if (mode == kModeShrink) return launch_shrink_tc(x, ldx, h, ldh, 1, seg, view, dev_err, s);
+  return launch_expand_tc(h, ldh, 1, y, ldy, seg, view, dev_err, s);
 }
 
 lora_status_t lora_sgmv_shrink(const void* x, int64_t ldx, float* h, int64_t ldh,
@@ -254,7 +269,7 @@ lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy, const 
   if (T > 0 && token_adapter == nullptr) return LORA_ERR_INVALID_ARG;
   if (T > 0 && overlap(x, (long long)T * ldx * 2, y, (long long)T * ldy * 2)) return LORA_ERR_INVALID_ARG;
   if (T == 0) return LORA_OK;
-  return launch_gather(kModeApply, kSrcTokens, x, ldx, y, ldy, nullptr, 0, nullptr, token_adapter, T, view,
+  return launch_gather(kModeApply, kSrcTokens, 0, x, ldx, y, ldy, nullptr, 0, nullptr, token_adapter, T, view,
                        dev_err, (cudaStream_t)stream);
 }
 

@@ -56,6 +56,7 @@ struct GatherArgs {
   int32_t* err;
   int mode;
   int src;
+  int short_only;
 };
 
 constexpr size_t kOffBars = (size_t)kStages * kStageBytes;
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
 
   // kSrcSegments walks the short units, then the long tiles, in one launch.
   const int n_short = a.src == kSrcSegments ? a.meta[2] : 0;
-  const int n_units = a.src == kSrcTokens ? a.T : a.meta[2] + a.meta[3];
+  const int n_units = a.src == kSrcTokens ? a.T : a.meta[2] + (a.short_only ? 0 : a.meta[3]);
   const int kc = ((v.d_in + (int)ncta - 1) / (int)ncta + 7) & ~7;
   const int nc = ((v.d_out + (int)ncta - 1) / (int)ncta + 7) & ~7;
   const int k0 = min(v.d_in, (int)crank * kc), k1 = min(v.d_in, k0 + kc);
@@ -343,7 +344,7 @@ static int cluster_size_for(const lora_pool_view_t* view) {
   return cl;
 }
 
-lora_status_t launch_gather(int mode, int src, const void* x, long long ldx, void* y, long long ldy,
+lora_status_t launch_gather(int mode, int src, int short_only, const void* x, long long ldx, void* y, long long ldy,
                             float* h, long long ldh, const lora_segments_t* seg,
                             const int32_t* token_adapter, int T, const lora_pool_view_t* view,
                             int32_t* err, cudaStream_t stream) {
@@ -366,8 +367,9 @@ lora_status_t launch_gather(int mode, int src, const void* x, long long ldx, voi
   a.err = err;
   a.mode = mode;
   a.src = src;
+  a.short_only = short_only;
 
-  const int upper = src == kSrcTokens ? T : seg->T + seg->max_long_units;
+  const int upper = src == kSrcTokens ? T : seg->T + (short_only ? 0 : seg->max_long_units);
   if (upper <= 0) return LORA_OK;
   const int cl = cluster_size_for(view);
   int cap = sm_count() * 3 / cl;

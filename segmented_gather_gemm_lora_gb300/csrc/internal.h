@@ -28,9 +28,21 @@ enum GatherSrc { kSrcSegments = 0, kSrcTokens = 1 };
 
 // CUDA-core gather kernel over the segments' work lists (short units, then
 // long tiles) or over one-token units.
-lora_status_t launch_gather(int mode, int src, const void* x, long long ldx, void* y,
+// long tiles too unless short_only (then the tensor-core kernels take them).
+lora_status_t launch_gather(int mode, int src, int short_only, const void* x, long long ldx, void* y,
                             long long ldy, float* h, long long ldh, const lora_segments_t* seg,
                             const int32_t* token_adapter, int T, const lora_pool_view_t* view,
                             int32_t* err, cudaStream_t stream);
+
+// Tensor-core path for long tiles.  Eligibility: d_in % 64 == 0 (shrink),
+// d_out % 128 == 0 (expand), pages of at least 128 elements.
+bool tc_shrink_ok(const lora_pool_view_t* v);
+bool tc_expand_ok(const lora_pool_view_t* v);
+lora_status_t launch_shrink_tc(const void* x, long long ldx, float* h, long long ldh, int h_by_token,
+                               const lora_segments_t* seg, const lora_pool_view_t* view, int32_t* err,
+                               cudaStream_t stream);
+lora_status_t launch_expand_tc(const float* h, long long ldh, int h_by_token, void* y, long long ldy,
+                               const lora_segments_t* seg, const lora_pool_view_t* view, int32_t* err,
+                               cudaStream_t stream);
 
 }  // namespace lora

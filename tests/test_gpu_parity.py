@@ -360,3 +360,90 @@ def test_empty_batch_is_noop():
     torch.cuda.synchronize()
     assert int(seg.meta[0].item()) == 0
     assert int(err.item()) == 0
+
+
+# ------------------------------------------------------ tensor-core long path --
+
+def long_segment_batch(seed, ranks, lens, d_in, d_out, page_elems=4096):
+    rng = np.random.default_rng(seed)
+    pool = W.build_pool(rng, d_in, d_out, ranks, page_elems=page_elems, max_rank=64)
+    ids = np.concatenate([np.full(n, i % len(ranks), dtype=np.int32) for i, n in enumerate(lens)])
+    batch = W.make_batch(rng, ids, d_in, d_out, ldx=d_in + 64, ldy=d_out + 8)
+    return pool, batch
+
+
+@pytest.mark.parametrize("mode", [B.LORA_SEG_GROUP, B.LORA_SEG_CONTIGUOUS])
+def test_tc_odd_ranks_and_tile_edges(mode):
+    """Long segments on the tensor cores with ranks that are not multiples of 16 and
+    segment lengths around the 128-token tile."""
+    ranks = [1, 7, 13, 33, 64, 16, 48]
+    lens = [9, 127, 128, 129, 256, 300, 40, 1, 3]
+    pool, batch = long_segment_batch(21, ranks, lens, 4096, 1024)
+    y, err, _ = run_apply(batch, pool, mode, len(ranks))
+    ref, _ = oracle.lora_apply(batch.x, batch.y0, batch.ids, pool)
+    assert err == 0
+    compare_bf16(y[:, :1024], ref, "tensor-core tiles mode %d" % mode)
+    check_untouched(y, batch, pool, np.array([], dtype=int))
+
+
+def test_tc_wide_shapes():
+    """d_in = 13824 (27 chunks per CTA) and d_out = 13824 (108 column chunks), rank 64."""
+    for d_in, d_out in ((13824, 5120), (5120, 13824)):
+        pool, batch = long_segment_batch(22, [64, 32], [200, 140], d_in, d_out)
+        y, err, _ = run_apply(batch, pool, B.LORA_SEG_GROUP, 2)
+        ref, _ = oracle.lora_apply(batch.x, batch.y0, batch.ids, pool)
+        assert err == 0
+        compare_bf16(y[:, :d_out], ref, "tensor-core %dx%d" % (d_in, d_out))
+
+
+def test_tc_shrink_expand_chain_equals_apply():
+    wl = W.prefill(5, n_requests=6)
+    pool = wl.pools[0]
+    batch = wl.batch
+    view = B.PoolView.from_host(pool)
+    x = to_dev_bits(batch.x)
+    y = to_dev_bits(batch.y0)
+    seg = B.Segments(batch.T)
+    err = new_err()
+    B.lora_segments_build(ids_dev(batch.ids), wl.n_adapters, seg, mode=B.LORA_SEG_GROUP, err=err)
+    h = torch.full((batch.T, 64), 3.0, dtype=torch.float32, device="cuda")
+    B.lora_sgmv_shrink(x, h, seg, view, err=err)
+    B.lora_sgmv_expand(h, y, seg, view, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    href, _ = oracle.shrink(batch.x, batch.ids, pool, h_init=np.full((batch.T, 64), 3.0), ldh=64)
+    np.testing.assert_allclose(h.cpu().numpy(), href, rtol=1e-4, atol=1e-4)
+    ya, _, _ = run_apply(batch, pool, B.LORA_SEG_GROUP, wl.n_adapters, view=view)
+    assert np.array_equal(to_host_bits(y), ya)
+
+
+def test_tc_expand_parity_random_h():
+    pool, batch = long_segment_batch(23, [16, 64, 5], [150, 200, 64], 2048, 4096)
+    rng = np.random.default_rng(24)
+    hin = rng.standard_normal((batch.T, 64), dtype=np.float32)
+    view = B.PoolView.from_host(pool)
+    y = to_dev_bits(batch.y0)
+    seg = B.Segments(batch.T)
+    err = new_err()
+    B.lora_segments_build(ids_dev(batch.ids), 3, seg, err=err)
+    B.lora_sgmv_expand(torch.from_numpy(hin).cuda(), y, seg, view, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref, _ = oracle.expand(hin, batch.y0, batch.ids, pool)
+    compare_bf16(to_host_bits(y)[:, :4096], ref, "tensor-core expand")
+
+
+def test_tc_device_errors_in_long_tiles():
+    rng = np.random.default_rng(25)
+    pool = W.build_pool(rng, 2048, 2048, [16, 16, 16], max_rank=16)
+    pool.desc[1]["rank"] = 32
+    pool.page_list[int(pool.desc[2]["a_page0"]) + 3] = -7
+    ids = np.repeat(np.array([0, 1, 2, 0], dtype=np.int32), [150, 140, 130, 20])
+    batch = W.make_batch(rng, ids, 2048, 2048)
+    ref, oerr = oracle.lora_apply(batch.x, batch.y0, ids, pool)
+    for mode in (B.LORA_SEG_GROUP, B.LORA_SEG_CONTIGUOUS):
+        y, err, _ = run_apply(batch, pool, mode, 3)
+        assert err == oerr == B.LORA_DERR_BAD_RANK | B.LORA_DERR_BAD_PAGE
+        good = ids == 0
+        compare_bf16(y[good], ref[good], "long tiles next to bad ones")
+        assert np.array_equal(y[~good], batch.y0[~good])
