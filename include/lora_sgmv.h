@@ -117,7 +117,7 @@ typedef struct {
  * units, meta[3] = long work units.  short_units lists the segments of at most
  * LORA_SHORT_MAX_TOKENS tokens; long_units lists (segment, offset) pairs, one
  * per LORA_TILE_M-token tile of every longer segment, both in segment order.
- * The remaining arrays are the build's scratch.
+ * scratch belongs to lora_segments_build, h_scratch to lora_apply.
  */
 typedef struct {
   int32_t T;              /* tokens the buffer was carved for */
