@@ -206,6 +206,34 @@ lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy,
                         int32_t* dev_err, lora_stream_t stream);
 
 /**
+ * lora_apply for callers that cannot allocate device memory.  (The pages have
+ * no counterpart: this is a deployment convenience of this library.)
+ *
+ * lora_apply keeps the rank-r intermediate of long segments in seg->h_scratch,
+ * a workspace the caller sizes and allocates.  Callers whose device memory is
+ * planned once by a host runtime, and who can therefore neither size nor
+ * request an extra workspace per call, use this entry point instead: the
+ * intermediate goes to a fixed array of LORA_FIXED_SCRATCH_MAX_TOKENS x
+ * LORA_MAX_RANK fp32 values (4 MiB) that is part of the library's device image
+ * (every GPU that loads the library holds it until the process exits).  It
+ * allocates nothing.
+ *
+ * Arguments, results and errors are those of lora_apply; seg->h_scratch is not
+ * used and may be NULL.  Returns LORA_ERR_UNSUPPORTED if seg->T exceeds
+ * LORA_FIXED_SCRATCH_MAX_TOKENS.  The first call on a device looks up the
+ * array's device address (once per device, on the current device); make that
+ * first call before any stream capture.  Every call shares the one array: calls
+ * that may run at the same time on the GPU (other streams, other host threads)
+ * race on it and must be serialised by the caller.  The array keeps the last
+ * call's contents; nothing in it needs to start at zero, because every value a
+ * call reads was written earlier in the same call.
+ */
+#define LORA_FIXED_SCRATCH_MAX_TOKENS 16384
+lora_status_t lora_apply_fixed_scratch(const void* x, int64_t ldx, void* y, int64_t ldy,
+                                       const lora_segments_t* seg, const lora_pool_view_t* view,
+                                       int32_t* dev_err, lora_stream_t stream);
+
+/**
  * Pages one adapter of rank r occupies in a pool of page_elems-element pages:
  * ceil(r * d_in / page_elems) + ceil(r * d_out / page_elems) (bytes per matrix
  * pair (d_in * r + r * d_out) * 2 before rounding to pages: "Multi-LoRA

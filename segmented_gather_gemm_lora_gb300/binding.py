@@ -32,6 +32,7 @@ LORA_SHORT_MAX_TOKENS = 8
 LORA_TILE_M = 128
 LORA_SEG_GROUP = 0
 LORA_SEG_CONTIGUOUS = 1
+LORA_FIXED_SCRATCH_MAX_TOKENS = 16384
 
 EXPORTED = (
     "lora_segments_buffer_bytes",
@@ -40,6 +41,7 @@ EXPORTED = (
     "lora_sgmv_shrink",
     "lora_sgmv_expand",
     "lora_apply",
+    "lora_apply_fixed_scratch",
     "lora_bgmv",
     "lora_pool_pages_needed",
     "lora_status_string",
@@ -98,6 +100,8 @@ def lib():
         L.lora_sgmv_expand.argtypes = [vp, i64, vp, i64, seg_p, view_p, vp, vp]
         L.lora_apply.restype = i32
         L.lora_apply.argtypes = [vp, i64, vp, i64, seg_p, view_p, vp, vp]
+        L.lora_apply_fixed_scratch.restype = i32
+        L.lora_apply_fixed_scratch.argtypes = [vp, i64, vp, i64, seg_p, view_p, vp, vp]
         L.lora_bgmv.restype = i32
         L.lora_bgmv.argtypes = [vp, i64, vp, i64, vp, i32, view_p, vp, vp]
         L.lora_pool_pages_needed.restype = i64
@@ -248,6 +252,16 @@ def lora_apply(x: torch.Tensor, y: torch.Tensor, seg: Segments, view: PoolView,
                err: Optional[torch.Tensor] = None, stream=None):
     _check(lib().lora_apply(_ptr(x), _ld(x), _ptr(y), _ld(y), ctypes.byref(seg.c),
                             ctypes.byref(view.c), _ptr(err), _stream(stream)), "lora_apply")
+
+
+def lora_apply_fixed_scratch(x: torch.Tensor, y: torch.Tensor, seg: Segments, view: PoolView,
+                             err: Optional[torch.Tensor] = None, stream=None):
+    """lora_apply with its intermediate in the library's fixed device array: for callers
+    that cannot allocate a workspace (see include/lora_sgmv.h).  Calls that may overlap on
+    the GPU share that array and must be serialised by the caller."""
+    _check(lib().lora_apply_fixed_scratch(_ptr(x), _ld(x), _ptr(y), _ld(y), ctypes.byref(seg.c),
+                                          ctypes.byref(view.c), _ptr(err), _stream(stream)),
+           "lora_apply_fixed_scratch")
 
 
 def lora_bgmv(x: torch.Tensor, y: torch.Tensor, token_adapter: torch.Tensor, view: PoolView,

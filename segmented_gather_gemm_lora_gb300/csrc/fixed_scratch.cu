@@ -1,0 +1,56 @@
+// lora_apply_fixed_scratch: lora_apply whose scratch lives in the library.
+//
+// lora_apply keeps the rank-r intermediate of tokens on the tensor-core path
+// in seg->h_scratch, memory the caller sized and allocated.  Some callers can
+// neither size nor request such a workspace: their device memory is planned
+// once, at start-up, by a host runtime that hands the library only the
+// activation, weight and segment buffers, and they cannot call cudaMalloc
+// afterwards.  For them this entry point takes the intermediate from a
+// fixed-size array that is part of the library's own device image: it is
+// created when the library is loaded onto a GPU and stays there until the
+// process exits.  Nothing is allocated per call.
+#include <mutex>
+
+#include "internal.h"
+
+namespace {
+
+// Scratch for LORA_FIXED_SCRATCH_MAX_TOKENS tokens x LORA_MAX_RANK fp32 values
+// (4 MiB).  In host code `g_fixed_h` only stands in for the symbol: its device
+// address comes from cudaGetSymbolAddress on each device.
+static __device__ __align__(256) float g_fixed_h[(size_t)LORA_FIXED_SCRATCH_MAX_TOKENS * LORA_MAX_RANK];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+float* g_fixed_h_addr[kMaxDevices];  // per device; null until that device's first call
+
+// Device address of g_fixed_h on the current device, looked up once per device.
+lora_status_t fixed_scratch_address(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return LORA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_fixed_h_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fixed_h) != cudaSuccess || p == nullptr) return LORA_ERR_CUDA;
+    g_fixed_h_addr[dev] = static_cast<float*>(p);
+  }
+  *out = g_fixed_h_addr[dev];
+  return LORA_OK;
+}
+
+}  // namespace
+
+extern "C" lora_status_t lora_apply_fixed_scratch(const void* x, int64_t ldx, void* y, int64_t ldy,
+                                                   const lora_segments_t* seg, const lora_pool_view_t* view,
+                                                   int32_t* dev_err, lora_stream_t stream) {
+  if (seg == nullptr) return LORA_ERR_INVALID_ARG;
+  if (seg->T > LORA_FIXED_SCRATCH_MAX_TOKENS) return LORA_ERR_UNSUPPORTED;
+  float* h = nullptr;
+  const lora_status_t st = fixed_scratch_address(&h);
+  if (st != LORA_OK) return st;
+  // Same arguments, same kernels as lora_apply; only the intermediate's home differs.
+  lora_segments_t local = *seg;
+  local.h_scratch = h;
+  return lora_apply(x, ldx, y, ldy, &local, view, dev_err, stream);
+}
