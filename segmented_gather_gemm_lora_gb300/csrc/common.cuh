@@ -51,14 +51,18 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Test for completion of the phase with the given parity.  A waiting thread
+// is suspended in hardware (woken when the phase completes, or after at most
+// about a millisecond) instead of spinning, so waiting warps leave the issue
+// slots and the shared-memory pipe to the warps doing the work.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(1000000u)
       : "memory");
   return done != 0;
 }
@@ -131,6 +135,18 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
   return v;
+}
+
+// ------------------------------------------------- programmatic dependent launch --
+
+// Wait until the grids this one depends on have completed and their memory is
+// visible, then let the next grid in the stream start its prologue.  Every
+// kernel of the library calls this before its first global-memory access, so
+// a kernel launched early (programmatic stream serialization) never reads or
+// writes anything its predecessor still touches.
+__device__ __forceinline__ void pdl_wait_then_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ------------------------------------------------------------------- bf16 --

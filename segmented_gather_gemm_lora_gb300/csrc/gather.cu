@@ -20,11 +20,10 @@
 //
 // Data movement.  Adapter rows (translated page by page through the page
 // table, "Multi-LoRA Serving in Production", section "Unified Paged Memory")
-// and token rows are staged in shared memory by bulk asynchronous copies
-// (cp.async.bulk, the TMA engine's non-tensor form) into a ring of stages
-// completed through mbarrier transaction counts; the expand's B and y0 chunks
-// are issued before the shrink's arithmetic finishes, so both phases' bytes
-// are in flight together.
+// and token rows are staged in shared memory by 16-byte asynchronous copies
+// from every thread into a ring of stages, each completed through an mbarrier;
+// the expand's B and y0 chunks are issued before the shrink's arithmetic
+// finishes, so both phases' bytes are in flight together.
 #include "common.cuh"
 #include "internal.h"
 
@@ -63,7 +62,9 @@ constexpr size_t kOffBars = (size_t)kStages * kStageBytes;
 constexpr size_t kOffHp = kOffBars + kStages * 8;
 constexpr size_t kOffHs = kOffHp + 2 * kNT * kHMax * sizeof(float);
 constexpr size_t kOffTok = kOffHs + kNT * kHMax * sizeof(float);
-constexpr size_t kGatherSmem = kOffTok + kNT * sizeof(int) + 64;
+constexpr int kMaxPgSlots = 1024;  // page-list slots of one adapter cached in shared memory
+constexpr size_t kOffPgt = kOffTok + kNT * sizeof(int) + 64;
+constexpr size_t kGatherSmem = kOffPgt + kMaxPgSlots * sizeof(int);
 
 // Elements per row of one stage: the stage holds up to max_rank adapter rows
 // and up to kNT token rows.  A function of the view's max_rank alone, so a
@@ -77,12 +78,17 @@ __device__ __forceinline__ int chunk_width(int r) {
 struct ChunkPlan {
   int r, ntok, nkc, nnc, wk, wn, k0, k1, n0, n1;
   int a_page0, b_page0;
+  int na;          // page-list slots of A_i (B_i's follow in the cached table)
+  const int* pgt;  // cached physical pages of A_i then B_i, or null
 };
 
-// Issue the bulk copies of chunk c (shrink chunks first, then expand chunks)
-// into stage st.  Called by all 32 lanes of one warp.
+// Stage chunk c (shrink chunks first, then expand chunks) into `stage`: every
+// thread of the CTA copies 16-byte pieces with cp.async (the load/store units
+// issue these in parallel; one TMA bulk copy per row costs tens of
+// nanoseconds of issue each, far too slow for rows of a few hundred bytes)
+// and then arrives on `bar` when its own pieces have landed.
 __device__ __forceinline__ void issue_chunk(const GatherArgs& a, const ChunkPlan& p, const int* tok,
-                                            int c, uint8_t* stage, uint32_t bar, int lane) {
+                                            int c, uint8_t* stage, uint32_t bar, int tid) {
   const bool shrink = c < p.nkc;
   const int stride = shrink ? p.wk : p.wn;
   const int cols = shrink ? p.k0 + c * p.wk : p.n0 + (c - p.nkc) * p.wn;
@@ -93,26 +99,63 @@ __device__ __forceinline__ void issue_chunk(const GatherArgs& a, const ChunkPlan
   const long long ld = shrink ? a.ldx : a.ldy;
   const int shift = a.v.page_shift;
   const long long pmask = (1LL << shift) - 1;
-  if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)((p.r + p.ntok) * w * 2));
-  __syncwarp();
   const uint32_t sbase = smem_u32(stage);
-  for (int item = lane; item < p.r + p.ntok; item += 32) {
-    uint32_t dst = sbase + (uint32_t)(item * stride * 2);
+  const int nq = w >> 3;  // 16-byte pieces per row
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int item = warp; item < p.r + p.ntok; item += kGThreads / 32) {
+    const uint32_t drow = sbase + (uint32_t)(item * stride * 2);
     if (item < p.r) {
-      long long e0 = (long long)item * rowlen + cols;
-      const long long e1 = e0 + w;
-      while (e0 < e1) {
-        const long long slot = page0 + (e0 >> shift);
-        const long long off = e0 & pmask;
-        const long long n = min(e1 - e0, (pmask + 1) - off);
-        const uint16_t* src = a.v.pool + ((long long)a.v.page_list[slot] << shift) + off;
-        bulk_g2s(dst, src, (uint32_t)(n * 2), bar);
-        dst += (uint32_t)(n * 2);
-        e0 += n;
+      const long long e0 = (long long)item * rowlen + cols;  // first element of the row piece
+      for (int q = lane; q < nq; q += 32) {
+        const long long e = e0 + 8 * q;
+        const long long idx = e >> shift;
+        const long long page = p.pgt ? p.pgt[(shrink ? 0 : p.na) + idx] : a.v.page_list[page0 + idx];
+        const uint16_t* src = a.v.pool + (page << shift) + (e & pmask);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(drow + 16 * q), "l"(src) : "memory");
       }
     } else {
-      const uint16_t* src = act + (long long)tok[item - p.r] * ld + cols;
-      bulk_g2s(dst, src, (uint32_t)(w * 2), bar);
+      const uint16_t* src0 = act + (long long)tok[item - p.r] * ld + cols;
+      for (int q = lane; q < nq; q += 32)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(drow + 16 * q), "l"(src0 + 8 * q) : "memory");
+    }
+  }
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Partial shrink of one staged chunk for NT tokens: warp w takes rank rows
+// j = w, w + 8, ...; its lanes take 8-element vectors of the chunk; the row's
+// dot products with every token are reduced over the warp and added to the
+// CTA's partial h.  Instantiated per token count so that a one-token decode
+// unit executes only its own arithmetic.
+template <int NT>
+__device__ __forceinline__ void shrink_chunk(const uint8_t* sb, const ChunkPlan& p, int nvec, float* hpb, int warp,
+                                             int lane) {
+  for (int j = warp; j < p.r; j += kGThreads / 32) {
+    float acc[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+    const uint4* arow = reinterpret_cast<const uint4*>(sb + (size_t)j * p.wk * 2);
+    const uint4* xrow = reinterpret_cast<const uint4*>(sb + (size_t)p.r * p.wk * 2);
+    const int xstride = p.wk / 8;  // uint4 per staged row
+    for (int vv = lane; vv < nvec; vv += 32) {
+      float af[8];
+      unpack8(arow[vv], af);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        float xf[8];
+        unpack8(xrow[t * xstride + vv], xf);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[t] = fmaf(af[q], xf[q], acc[t]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) hpb[t * kHMax + j] += acc[t];
     }
   }
 }
@@ -130,10 +173,11 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
   const DevView& v = a.v;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars[s]), kGThreads);
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait_then_release();
 
   // kSrcSegments walks the short units, then the long tiles, in one launch.
   const int n_short = a.src == kSrcSegments ? a.meta[2] : 0;
@@ -145,6 +189,7 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
   uint32_t parity = 0;  // bit s: parity of stage s's next phase
   int gbuf = 0;
 
+  int* pgt = reinterpret_cast<int*>(sm + kOffPgt);
   for (int u = (int)cid; u < n_units; u += (int)ncl) {
     int ad, tb = 0, cnt;
     if (a.src == kSrcTokens) {
@@ -167,25 +212,33 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
       tb = a.indptr[s] + m0;
       cnt = min(LORA_TILE_M, a.indptr[s + 1] - tb);
     }
+    // The first group's token indices do not depend on the adapter: load them
+    // alongside its descriptor.
+    const int first_tok = tid < min(kNT, cnt) ? (a.src == kSrcTokens ? u : a.perm[tb + tid]) : -1;
     const lora_adapter_desc_t d = v.adapters[ad];
-    // Every CTA checks the whole adapter, so all reach the same verdict
-    // without talking to each other.
+    // Every CTA checks the whole adapter, so all reach the same verdict without
+    // talking to each other; the same pass caches the physical pages.
     int bad = 0;
+    long long na = 0, nb = 0;
+    bool cached = false;
     if (d.rank < 1 || d.rank > v.max_rank || d.rank > kHMax) {
       bad = LORA_DERR_BAD_RANK;
     } else {
       const long long P = 1LL << v.page_shift;
-      const long long na = ((long long)d.rank * v.d_in + P - 1) >> v.page_shift;
-      const long long nb = ((long long)d.rank * v.d_out + P - 1) >> v.page_shift;
+      na = ((long long)d.rank * v.d_in + P - 1) >> v.page_shift;
+      nb = ((long long)d.rank * v.d_out + P - 1) >> v.page_shift;
+      cached = na + nb <= kMaxPgSlots;
       int mine = 0;
       for (long long i = tid; i < na + nb; i += kGThreads) {
         const long long slot = i < na ? d.a_page0 + i : d.b_page0 + (i - na);
+        long long pg = -1;
         if (slot < 0 || slot >= v.n_page_list) {
           mine = 1;
         } else {
-          const long long pg = v.page_list[slot];
+          pg = v.page_list[slot];
           if (pg < 0 || pg >= v.n_pages) mine = 1;
         }
+        if (cached) pgt[i] = (int)pg;
       }
       if (__syncthreads_or(mine)) bad = LORA_DERR_BAD_PAGE;
     }
@@ -203,21 +256,21 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
     p.nnc = (a.mode != kModeShrink && n1 > n0) ? (n1 - n0 + p.wn - 1) / p.wn : 0;
     p.a_page0 = d.a_page0;
     p.b_page0 = d.b_page0;
+    p.na = (int)na;
+    p.pgt = cached ? pgt : nullptr;
     const float sc = d.scale;
 
     for (int g0 = 0; g0 < cnt; g0 += kNT) {
       p.ntok = min(kNT, cnt - g0);
       const int ntok = p.ntok;
-      if (tid < ntok) tok[tid] = a.src == kSrcTokens ? u : a.perm[tb + g0 + tid];
+      if (tid < ntok) tok[tid] = g0 == 0 ? first_tok : a.perm[tb + g0 + tid];
       float* hpb = hp + gbuf * kNT * kHMax;
       for (int i = tid; i < kNT * kHMax; i += kGThreads) hpb[i] = 0.f;
       __syncthreads();
 
       const int nch = p.nkc + p.nnc;
-      if (warp == 0) {
-        for (int c = 0; c < min(kStages, nch); ++c)
-          issue_chunk(a, p, tok, c, sm + (size_t)c * kStageBytes, smem_u32(&bars[c]), lane);
-      }
+      for (int c = 0; c < min(kStages, nch); ++c)
+        issue_chunk(a, p, tok, c, sm + (size_t)c * kStageBytes, smem_u32(&bars[c]), tid);
       bool ok = true;
 
       // ---- shrink: partial h over this CTA's d_in slice ----
@@ -229,41 +282,19 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
         const int cols = p.k0 + c * p.wk;
         const int w = min(p.wk, p.k1 - cols);
         const int nvec = w >> 3;
-        for (int j = warp; j < p.r; j += kGThreads / 32) {
-          float acc[kNT];
-#pragma unroll
-          for (int t = 0; t < kNT; ++t) acc[t] = 0.f;
-          const uint4* arow = reinterpret_cast<const uint4*>(sb + (size_t)j * p.wk * 2);
-          for (int vv = lane; vv < nvec; vv += 32) {
-            float af[8];
-            unpack8(arow[vv], af);
-#pragma unroll
-            for (int t = 0; t < kNT; ++t) {
-              if (t < ntok) {
-                const uint4* xr = reinterpret_cast<const uint4*>(sb + (size_t)(p.r + t) * p.wk * 2);
-                float xf[8];
-                unpack8(xr[vv], xf);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc[t] = fmaf(af[q], xf[q], acc[t]);
-              }
-            }
-          }
-#pragma unroll
-          for (int t = 0; t < kNT; ++t) {
-            if (t < ntok) {
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
-            }
-          }
-          if (lane == 0) {
-#pragma unroll
-            for (int t = 0; t < kNT; ++t)
-              if (t < ntok) hpb[t * kHMax + j] += acc[t];
-          }
+        switch (ntok) {
+          case 1: shrink_chunk<1>(sb, p, nvec, hpb, warp, lane); break;
+          case 2: shrink_chunk<2>(sb, p, nvec, hpb, warp, lane); break;
+          case 3: shrink_chunk<3>(sb, p, nvec, hpb, warp, lane); break;
+          case 4: shrink_chunk<4>(sb, p, nvec, hpb, warp, lane); break;
+          case 5: shrink_chunk<5>(sb, p, nvec, hpb, warp, lane); break;
+          case 6: shrink_chunk<6>(sb, p, nvec, hpb, warp, lane); break;
+          case 7: shrink_chunk<7>(sb, p, nvec, hpb, warp, lane); break;
+          default: shrink_chunk<8>(sb, p, nvec, hpb, warp, lane); break;
         }
         __syncthreads();
-        if (warp == 0 && c + kStages < nch)
-          issue_chunk(a, p, tok, c + kStages, sm + (size_t)st * kStageBytes, smem_u32(&bars[st]), lane);
+        if (c + kStages < nch)
+          issue_chunk(a, p, tok, c + kStages, sm + (size_t)st * kStageBytes, smem_u32(&bars[st]), tid);
       }
 
       // ---- h: cluster reduction (apply / shrink) or load (expand) ----
@@ -273,8 +304,15 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
         for (int i = tid; i < ntok * p.r; i += kGThreads) {
           const int t = i / p.r, j = i - t * p.r;
           const uint32_t off = (uint32_t)((t * kHMax + j) * sizeof(float));
+          // all peers' loads in flight first, then the sum in fixed CTA order
+          float part[kMaxCluster];
+#pragma unroll
+          for (int c = 0; c < kMaxCluster; ++c)
+            part[c] = (uint32_t)c < ncta ? ld_dsmem_f32(mapa(hp_addr + off, (uint32_t)c)) : 0.f;
           float sum = 0.f;
-          for (uint32_t c = 0; c < ncta; ++c) sum += ld_dsmem_f32(mapa(hp_addr + off, c));
+#pragma unroll
+          for (int c = 0; c < kMaxCluster; ++c)
+            if ((uint32_t)c < ncta) sum += part[c];
           hs[t * kHMax + j] = a.mode == kModeApply ? sc * sum : sum;
         }
         __syncthreads();
@@ -301,19 +339,34 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
         const int cols = p.n0 + (c - p.nkc) * p.wn;
         const int w = min(p.wn, p.n1 - cols);
         const int nvec = w >> 3;
-        if (ok) {
-          for (int it = tid; it < ntok * nvec; it += kGThreads) {
-            const int t = it / nvec, vv = it - t * nvec;
-            float o[8];
+        // Eight consecutive lanes share one (token, 8-column vector); lane jq
+        // sums rank rows j = jq, jq + 8, ... in ascending order and the eight
+        // partial sums meet in a fixed butterfly.  The order depends neither on
+        // the unit's token count nor on the adapter's rank.
+        const int items = ntok * nvec * 8;
+        for (int base = 0; base < items; base += kGThreads) {
+          const int it = base + tid;
+          const bool act = it < items;
+          const int jq = it & 7, tv = it >> 3;
+          const int t = act ? tv / nvec : 0, vv = act ? tv - t * nvec : 0;
+          float o[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) o[q] = 0.f;
-            for (int j = 0; j < p.r; ++j) {
+          for (int q = 0; q < 8; ++q) o[q] = 0.f;
+          if (act) {
+            for (int j = jq; j < p.r; j += 8) {
               const float hj = hs[t * kHMax + j];
               float bf[8];
               unpack8(reinterpret_cast<const uint4*>(sb + (size_t)j * p.wn * 2)[vv], bf);
 #pragma unroll
               for (int q = 0; q < 8; ++q) o[q] = fmaf(hj, bf[q], o[q]);
             }
+          }
+#pragma unroll
+          for (int m = 1; m < 8; m <<= 1) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) o[q] += __shfl_xor_sync(0xffffffffu, o[q], m);
+          }
+          if (act && jq == 0 && ok) {
             float yf[8];
             unpack8(reinterpret_cast<const uint4*>(sb + (size_t)(p.r + t) * p.wn * 2)[vv], yf);
             uint4 out;
@@ -325,8 +378,8 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
           }
         }
         __syncthreads();
-        if (warp == 0 && c + kStages < nch)
-          issue_chunk(a, p, tok, c + kStages, sm + (size_t)st * kStageBytes, smem_u32(&bars[st]), lane);
+        if (c + kStages < nch)
+          issue_chunk(a, p, tok, c + kStages, sm + (size_t)st * kStageBytes, smem_u32(&bars[st]), tid);
       }
       if (!ok && tid == 0) report(a.err, LORA_DERR_TIMEOUT);
       gbuf ^= 1;
@@ -377,20 +430,10 @@ lora_status_t launch_gather(int mode, int src, int short_only, const void* x, lo
   const int n_clusters = upper < cap ? upper : cap;
 
   if (ensure_smem_attr((const void*)gather_kernel, kGatherSmem) != cudaSuccess) return LORA_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(n_clusters * cl), 1, 1);
-  cfg.blockDim = dim3(kGThreads, 1, 1);
-  cfg.dynamicSmemBytes = kGatherSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)cl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gather_kernel, a);
-  return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+  return launch_pdl((const void*)gather_kernel, dim3((unsigned)(n_clusters * cl)), dim3(kGThreads), kGatherSmem,
+                    stream, cl, &a) == cudaSuccess
+             ? LORA_OK
+             : LORA_ERR_CUDA;
 }
 
 }  // namespace lora

@@ -14,6 +14,13 @@ struct DevView;
 // device and size).
 cudaError_t ensure_smem_attr(const void* func, size_t bytes);
 
+// Launch `func` (whose only parameter is the struct at `args`) with a cluster
+// of `cluster_x` CTAs (0 = launched without clusters) and programmatic stream serialization,
+// so it may start while its predecessor in the stream finishes; the kernel
+// itself waits for the predecessor before touching global memory.
+cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, int cluster_x,
+                       void* args);
+
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 

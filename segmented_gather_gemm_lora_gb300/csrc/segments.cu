@@ -8,19 +8,22 @@
 // Matrix-Vector Multiplication (SGMV)": contiguous segments whose tokens share
 // one adapter id -- CONTIGUOUS mode: one segment per maximal run.
 //
-// One CTA of 1024 threads does the whole job (the batch is at most a few
-// thousand tokens):
-//   1. run-length pass: maximal runs of equal, valid ids (block-wide scan of
-//      run heads); serving batches are runs (a prefill request is one run), so
-//      the sort below works on runs, not tokens;
+// One CTA does the whole job (a batch is at most some thousands of tokens),
+// sized to the batch so that its barriers stay cheap for small decode batches.
+// Each thread owns a span of up to 16 consecutive tokens, loaded with all its
+// loads in flight at once:
+//   1. run-length pass: maximal runs of equal, valid ids; one block scan of the
+//      per-thread run counts numbers the runs.  Serving batches are runs (a
+//      prefill request is one run), so the grouping below works on runs;
 //   2. GROUP: per-adapter token counts (shared-memory atomics on run lengths,
-//      an exact integer sum), exclusive scan -> segment starts; one warp then
-//      walks the runs in order and hands each its position inside its
-//      adapter's segment (warp match + in-order prefix), which keeps the sort
-//      stable;  CONTIGUOUS: segments are the runs, starts by a scan;
+//      an exact integer sum); one block scan over adapters gives segment
+//      starts, segment numbers and both work lists at once; one warp then walks
+//      the runs in token order and hands each its place inside its adapter's
+//      segment (warp match + in-order prefix), which keeps the grouping
+//      stable.  CONTIGUOUS: segments are the runs, one scan over runs;
 //   3. scatter of token indices to their positions;
-//   4. the work lists of the compute kernels (segments of at most
-//      LORA_SHORT_MAX_TOKENS tokens; LORA_TILE_M-token tiles of longer ones).
+//   work lists: segments of at most LORA_SHORT_MAX_TOKENS tokens are short
+//   units; longer ones are cut into LORA_TILE_M-token tiles.
 // Everything is integer arithmetic with a fixed order: the output is
 // bit-exact and deterministic.
 #include <climits>
@@ -30,35 +33,39 @@
 
 namespace lora {
 
-constexpr int kSegThreads = 1024;
+constexpr int kSpan = 16;          // tokens per thread per pass
+constexpr int kSegMaxThreads = 1024;
 
-// Exclusive scan over the CTA; *total receives the sum.  ws: 33 ints of smem.
-__device__ __forceinline__ int block_scan_ex(int v, int* total, int* ws) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
+// Exclusive scan of four counters at once over the CTA; *total receives the
+// sums.  ws: 33 int4 of shared memory.
+__device__ __forceinline__ int4 block_scan4(int4 v, int4* total, int4* ws) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  int4 inc = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += n;
+    const int a = __shfl_up_sync(0xffffffffu, inc.x, o), b = __shfl_up_sync(0xffffffffu, inc.y, o);
+    const int c = __shfl_up_sync(0xffffffffu, inc.z, o), d = __shfl_up_sync(0xffffffffu, inc.w, o);
+    if (lane >= o) { inc.x += a; inc.y += b; inc.z += c; inc.w += d; }
   }
-  if (lane == 31) ws[warp] = incl;
+  if (lane == 31) ws[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    int w = (lane < (int)(blockDim.x >> 5)) ? ws[lane] : 0;
-    int wi = w;
+    const int4 w = lane < nw ? ws[lane] : make_int4(0, 0, 0, 0);
+    int4 wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int n = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += n;
+      const int a = __shfl_up_sync(0xffffffffu, wi.x, o), b = __shfl_up_sync(0xffffffffu, wi.y, o);
+      const int c = __shfl_up_sync(0xffffffffu, wi.z, o), d = __shfl_up_sync(0xffffffffu, wi.w, o);
+      if (lane >= o) { wi.x += a; wi.y += b; wi.z += c; wi.w += d; }
     }
-    ws[lane] = wi - w;
+    ws[lane] = make_int4(wi.x - w.x, wi.y - w.y, wi.z - w.z, wi.w - w.w);
     if (lane == 31) ws[32] = wi;
   }
   __syncthreads();
-  int ex = ws[warp] + incl - v;
+  const int4 base = ws[warp];
   *total = ws[32];
   __syncthreads();
-  return ex;
+  return make_int4(base.x + inc.x - v.x, base.y + inc.y - v.y, base.z + inc.z - v.z, base.w + inc.w - v.w);
 }
 
 struct SegKernelArgs {
@@ -77,11 +84,27 @@ struct SegKernelArgs {
   int32_t* err;
 };
 
-__global__ void __launch_bounds__(kSegThreads, 1) segments_kernel(const __grid_constant__ SegKernelArgs a) {
+// Short / long classification of a segment of `len` tokens: (short, tiles).
+__device__ __forceinline__ int2 unit_counts(int len) {
+  if (len <= 0) return make_int2(0, 0);
+  if (len <= LORA_SHORT_MAX_TOKENS) return make_int2(1, 0);
+  return make_int2(0, (len + LORA_TILE_M - 1) / LORA_TILE_M);
+}
+
+__device__ __forceinline__ void emit_units(const SegKernelArgs& a, int s, int2 uc, int short_at, int long_at) {
+  if (uc.x) a.short_units[short_at] = s;
+  for (int i = 0; i < uc.y; ++i) {
+    a.long_units[2 * (long_at + i)] = s;
+    a.long_units[2 * (long_at + i) + 1] = i * LORA_TILE_M;
+  }
+}
+
+__global__ void __launch_bounds__(kSegMaxThreads, 1) segments_kernel(const __grid_constant__ SegKernelArgs a) {
   extern __shared__ __align__(16) int dyn[];
-  __shared__ int ws[33];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ int4 ws[33];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
   const int T = a.T, NA = a.n_adapters;
+  pdl_wait_then_release();
 
   int* counts = dyn;  // [NA] (GROUP)
   int* runs = a.runs_in_smem ? dyn + ((a.mode == LORA_SEG_GROUP ? NA : 0) + 3) / 4 * 4 : a.scratch;
@@ -89,52 +112,68 @@ __global__ void __launch_bounds__(kSegThreads, 1) segments_kernel(const __grid_c
   int* run_end = runs + T;
   int* run_id = runs + 2 * T;
   int* run_pos = runs + 3 * T;
+  const int per_pass = nthr * kSpan;
 
   // 1. runs of equal valid ids.
   int bad = 0, R = 0;
-  for (int base = 0; base < T; base += kSegThreads) {
-    const int t = base + tid;
-    const int id = t < T ? a.ids[t] : -1;
-    const bool valid = t < T && id >= 0 && id < NA;
-    if (t < T && (id < -1 || id >= NA)) bad = 1;
-    const int prev = (t > 0 && t < T) ? a.ids[t - 1] : INT_MIN;
-    const int next = (t + 1 < T) ? a.ids[t + 1] : INT_MIN;
-    const bool head = valid && (t == 0 || prev != id);
-    const bool tail = valid && (t == T - 1 || next != id);
-    int total;
-    const int ex = block_scan_ex(head ? 1 : 0, &total, ws);
-    const int rho = R + ex + (head ? 1 : 0) - 1;
-    if (head) {
-      run_start[rho] = t;
-      run_id[rho] = id;
+  for (int base = 0; base < T; base += per_pass) {
+    const int t0 = base + tid * kSpan;
+    int v[kSpan];
+#pragma unroll
+    for (int k = 0; k < kSpan; ++k) v[k] = (t0 + k < T) ? a.ids[t0 + k] : INT_MIN;
+    const int prev = (t0 > 0 && t0 < T) ? a.ids[t0 - 1] : INT_MIN;
+    const int next = (t0 + kSpan < T) ? a.ids[t0 + kSpan] : INT_MIN;
+    int heads = 0;
+#pragma unroll
+    for (int k = 0; k < kSpan; ++k) {
+      const bool valid = v[k] >= 0 && v[k] < NA;
+      if (t0 + k < T && (v[k] < -1 || v[k] >= NA)) bad = 1;
+      const int before = k == 0 ? prev : v[k - 1];
+      heads += (valid && before != v[k]) ? 1 : 0;
     }
-    if (tail) run_end[rho] = t + 1;
-    R += total;
+    int4 tot;
+    const int4 ex = block_scan4(make_int4(heads, 0, 0, 0), &tot, ws);
+    int rho = R + ex.x - 1;
+#pragma unroll
+    for (int k = 0; k < kSpan; ++k) {
+      const bool valid = v[k] >= 0 && v[k] < NA;
+      const int before = k == 0 ? prev : v[k - 1];
+      const int after = k == kSpan - 1 ? next : v[k + 1];
+      if (valid && before != v[k]) {
+        ++rho;
+        run_start[rho] = t0 + k;
+        run_id[rho] = v[k];
+      }
+      if (valid && after != v[k]) run_end[rho] = t0 + k + 1;
+    }
+    R += tot.x;
   }
   __syncthreads();
 
-  // 2. segment starts and every run's position.
-  int n_segs = 0, n_tok = 0;
+  // 2. segments, their starts and the work lists; every run's position.
+  int n_segs = 0, n_tok = 0, n_short = 0, n_long = 0;
   if (a.mode == LORA_SEG_GROUP) {
-    for (int i = tid; i < NA; i += kSegThreads) counts[i] = 0;
+    for (int i = tid; i < NA; i += nthr) counts[i] = 0;
     __syncthreads();
-    for (int rho = tid; rho < R; rho += kSegThreads)
-      atomicAdd(&counts[run_id[rho]], run_end[rho] - run_start[rho]);
+    for (int rho = tid; rho < R; rho += nthr) atomicAdd(&counts[run_id[rho]], run_end[rho] - run_start[rho]);
     __syncthreads();
-    for (int base = 0; base < NA; base += kSegThreads) {
+    for (int base = 0; base < NA; base += nthr) {
       const int ad = base + tid;
       const int c = ad < NA ? counts[ad] : 0;
-      const int ne = c > 0 ? 1 : 0;
-      int tc, tn;
-      const int exc = block_scan_ex(c, &tc, ws);
-      const int exn = block_scan_ex(ne, &tn, ws);
-      if (ne) {
-        a.indptr[n_segs + exn] = n_tok + exc;
-        a.seg_adapter[n_segs + exn] = ad;
+      const int2 uc = unit_counts(c);
+      int4 tot;
+      const int4 ex = block_scan4(make_int4(c, c > 0 ? 1 : 0, uc.x, uc.y), &tot, ws);
+      if (c > 0) {
+        const int sidx = n_segs + ex.y;
+        a.indptr[sidx] = n_tok + ex.x;
+        a.seg_adapter[sidx] = ad;
+        emit_units(a, sidx, uc, n_short + ex.z, n_long + ex.w);
       }
-      if (ad < NA) counts[ad] = n_tok + exc;  // becomes the adapter's fill cursor
-      n_tok += tc;
-      n_segs += tn;
+      if (ad < NA) counts[ad] = n_tok + ex.x;  // becomes the adapter's fill cursor
+      n_tok += tot.x;
+      n_segs += tot.y;
+      n_short += tot.z;
+      n_long += tot.w;
     }
     __syncthreads();
     if (warp == 0) {  // stable: runs take their places in token order
@@ -160,65 +199,65 @@ __global__ void __launch_bounds__(kSegThreads, 1) segments_kernel(const __grid_c
       }
     }
   } else {
-    for (int base = 0; base < R; base += kSegThreads) {
+    for (int base = 0; base < R; base += nthr) {
       const int rho = base + tid;
       const int len = rho < R ? run_end[rho] - run_start[rho] : 0;
-      int tot;
-      const int ex = block_scan_ex(len, &tot, ws);
+      const int2 uc = unit_counts(len);
+      int4 tot;
+      const int4 ex = block_scan4(make_int4(len, 0, uc.x, uc.y), &tot, ws);
       if (rho < R) {
-        a.indptr[rho] = n_tok + ex;
+        a.indptr[rho] = n_tok + ex.x;
         a.seg_adapter[rho] = run_id[rho];
-        run_pos[rho] = n_tok + ex;
+        run_pos[rho] = n_tok + ex.x;
+        emit_units(a, rho, uc, n_short + ex.z, n_long + ex.w);
       }
-      n_tok += tot;
+      n_tok += tot.x;
+      n_short += tot.z;
+      n_long += tot.w;
     }
     n_segs = R;
   }
   if (tid == 0) a.indptr[n_segs] = n_tok;
   __syncthreads();
 
-  // 3. token indices to their positions.
+  // 3. token indices to their positions (the runs are renumbered exactly as in 1).
   int rbase = 0;
-  for (int base = 0; base < T; base += kSegThreads) {
-    const int t = base + tid;
-    const int id = t < T ? a.ids[t] : -1;
-    const bool valid = t < T && id >= 0 && id < NA;
-    const int prev = (t > 0 && t < T) ? a.ids[t - 1] : INT_MIN;
-    const bool head = valid && (t == 0 || prev != id);
-    int total;
-    const int ex = block_scan_ex(head ? 1 : 0, &total, ws);
-    if (valid) {
-      const int rho = rbase + ex + (head ? 1 : 0) - 1;
-      a.perm[run_pos[rho] + (t - run_start[rho])] = t;
+  for (int base = 0; base < T; base += per_pass) {
+    const int t0 = base + tid * kSpan;
+    int v[kSpan];
+#pragma unroll
+    for (int k = 0; k < kSpan; ++k) v[k] = (t0 + k < T) ? a.ids[t0 + k] : INT_MIN;
+    const int prev = (t0 > 0 && t0 < T) ? a.ids[t0 - 1] : INT_MIN;
+    int heads = 0;
+#pragma unroll
+    for (int k = 0; k < kSpan; ++k) {
+      const int before = k == 0 ? prev : v[k - 1];
+      heads += (v[k] >= 0 && v[k] < NA && before != v[k]) ? 1 : 0;
     }
-    rbase += total;
+    int4 tot;
+    const int4 ex = block_scan4(make_int4(heads, 0, 0, 0), &tot, ws);
+    int rho = rbase + ex.x - 1;
+    int pos = 0;
+#pragma unroll
+    for (int k = 0; k < kSpan; ++k) {
+      const bool valid = v[k] >= 0 && v[k] < NA;
+      const int before = k == 0 ? prev : v[k - 1];
+      if (valid && before != v[k]) {
+        ++rho;
+        pos = run_pos[rho];
+      } else if (valid && k == 0) {
+        pos = run_pos[rho] + (t0 - run_start[rho]);  // a run that began in an earlier span
+      }
+      if (valid) a.perm[pos++] = t0 + k;
+    }
+    rbase += tot.x;
   }
-  __syncthreads();
 
-  // 4. work lists.
-  int ns = 0, nl = 0;
-  for (int base = 0; base < n_segs; base += kSegThreads) {
-    const int s = base + tid;
-    const bool act = s < n_segs;
-    const int len = act ? a.indptr[s + 1] - a.indptr[s] : 0;
-    const int sh = (act && len <= LORA_SHORT_MAX_TOKENS) ? 1 : 0;
-    const int tiles = (act && !sh) ? (len + LORA_TILE_M - 1) / LORA_TILE_M : 0;
-    int ts, tl;
-    const int exs = block_scan_ex(sh, &ts, ws);
-    const int exl = block_scan_ex(tiles, &tl, ws);
-    if (sh) a.short_units[ns + exs] = s;
-    for (int i = 0; i < tiles; ++i) {
-      a.long_units[2 * (nl + exl + i)] = s;
-      a.long_units[2 * (nl + exl + i) + 1] = i * LORA_TILE_M;
-    }
-    ns += ts;
-    nl += tl;
-  }
   if (tid == 0) {
     a.meta[0] = n_segs;
     a.meta[1] = n_tok;
-    a.meta[2] = ns;
-    a.meta[3] = nl;
+    a.meta[2] = n_short;
+    a.meta[3] = n_long;
     a.meta[4] = R;
     a.meta[5] = 0;
     a.meta[6] = 0;
@@ -236,6 +275,12 @@ lora_status_t launch_segments(const int32_t* ids, int T, int n_adapters, int mod
   const size_t dyn = counts_bytes + (runs_in_smem ? runs_bytes : 0);
   if (dyn > smem_cap) return LORA_ERR_UNSUPPORTED;
   if (ensure_smem_attr((const void*)segments_kernel, dyn) != cudaSuccess) return LORA_ERR_CUDA;
+  // Enough threads for the token spans and for one pass over the adapters.
+  int want = (T + kSpan - 1) / kSpan;
+  if (mode == LORA_SEG_GROUP && n_adapters > want) want = n_adapters;
+  int nthr = (want + 31) / 32 * 32;
+  if (nthr < 64) nthr = 64;
+  if (nthr > kSegMaxThreads) nthr = kSegMaxThreads;
   SegKernelArgs a;
   a.ids = ids;
   a.T = T;
@@ -250,8 +295,9 @@ lora_status_t launch_segments(const int32_t* ids, int T, int n_adapters, int mod
   a.long_units = seg->long_units;
   a.scratch = seg->scratch;
   a.err = err;
-  segments_kernel<<<1, kSegThreads, dyn, stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+  return launch_pdl((const void*)segments_kernel, dim3(1), dim3(nthr), dyn, stream, 0, &a) == cudaSuccess
+             ? LORA_OK
+             : LORA_ERR_CUDA;
 }
 
 }  // namespace lora

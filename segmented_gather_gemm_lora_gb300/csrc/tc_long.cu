@@ -26,8 +26,9 @@
 //             same fp32 tensor-memory columns), which keeps the rank-r
 //             intermediate at about fp32 accuracy on bf16 tensor cores.  B_i
 //             rows are MN-major operands (r_i rows of d_out contiguous
-//             elements, as stored).  y0 rows arrive and y rows leave by bulk
-//             asynchronous copies (the TMA engine), one per row.
+//             elements, as stored).  y0 rows arrive by 16-byte asynchronous
+//             copies and y rows leave by coalesced 16-byte stores, both through
+//             a padded staging tile in shared memory.
 #include "internal.h"
 #include "tc.cuh"
 
@@ -117,6 +118,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) shrink_tc_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait_then_release();
 
   // This CTA's slice of d_in, in whole 64-column chunks.
   const int kc = (((v.d_in + (int)ncta - 1) / (int)ncta) + 63) & ~63;
@@ -270,13 +272,8 @@ constexpr size_t kEOffPg = kEOffTok + kTM * 4;
 constexpr size_t kEOffBars = kEOffPg + 64 * 4;
 constexpr size_t kExpandSmem = kEOffBars + 8 * 8 + 1024;
 
-__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Barrier among the 128 loader / epilogue threads (warps 0-3) only.
+__device__ __forceinline__ void named_sync_128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kTcThreads, 2) expand_tc_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -289,7 +286,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) expand_tc_kernel(const __grid_c
   int* pgb = reinterpret_cast<int*>(sm + kEOffPg);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kEOffBars);
   uint64_t* bar_b = bars;       // 128 producer arrivals: B tile and H operand in place
-  uint64_t* bar_y = bars + 1;   // 128 arrivals + y0 transaction bytes
   uint64_t* acc_full = bars + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3);
 
@@ -297,7 +293,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) expand_tc_kernel(const __grid_c
   const DevView& v = a.v;
   if (tid == 0) {
     mbar_init(smem_u32(bar_b), 128);
-    mbar_init(smem_u32(bar_y), 128);
     mbar_init(smem_u32(acc_full), 1);
     fence_mbar_init();
   }
@@ -306,6 +301,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) expand_tc_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait_then_release();
 
   const int n_nc = v.d_out / kENC;
   const long long n_work = (long long)a.meta[3] * n_nc;
@@ -369,14 +365,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) expand_tc_kernel(const __grid_c
     __syncthreads();
 
     if (warp < 4) {
-      const int m = tid;
-      // y0 row m by one bulk copy (after this row's previous store has read it)
-      bulk_wait_read0();
-      if (m < cnt) {
-        mbar_arrive_expect_tx(smem_u32(bar_y), kENC * 2);
-        bulk_g2s(smem_u32(ys + m * kEYRow), a.y + (long long)tok[m] * a.ldy + n0, kENC * 2, smem_u32(bar_y));
-      } else {
-        mbar_arrive(smem_u32(bar_y));
+      // y0 rows: 16-byte pieces, 16 consecutive threads per 256-byte row
+      for (int i = tid; i < kTM * (kENC / 8); i += 128) {
+        const int m = i / (kENC / 8), q = i % (kENC / 8);
+        if (m < cnt)
+          cp_async16(smem_u32(ys + m * kEYRow + q * 16), a.y + (long long)tok[m] * a.ldy + n0 + 8 * q);
       }
       // B rows: MN-major operand, 2 atoms of 64 columns, 8 rank rows per
       // 1024-byte group, 128-byte swizzle; zero beyond r.
@@ -393,6 +386,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) expand_tc_kernel(const __grid_c
       cp_async_commit();
       cp_async_wait<0>();
       fence_proxy_async_smem();
+      named_sync_128();  // every loader's y0 pieces visible to every epilogue thread
       tc_fence_before();
       mbar_arrive(smem_u32(bar_b));
     } else if (lane == 0) {
@@ -417,7 +411,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) expand_tc_kernel(const __grid_c
 
     if (warp < 4) {
       const int m = tid;
-      if (!mbar_wait(smem_u32(bar_y), nunit & 1)) ok = false;
       if (!mbar_wait(smem_u32(acc_full), nunit & 1)) ok = false;
       tc_fence_after();
       uint8_t* yrow = ys + m * kEYRow;
@@ -442,16 +435,19 @@ __global__ void __launch_bounds__(kTcThreads, 2) expand_tc_kernel(const __grid_c
         p[1] = o1;
       }
       tc_fence_before();
-      fence_proxy_async_smem();
-      if (m < cnt && ok) {
-        bulk_s2g(a.y + (long long)tok[m] * a.ldy + n0, smem_u32(yrow), kENC * 2);
-        bulk_commit();
+      named_sync_128();
+      // y rows: 16 consecutive threads store one 256-byte row
+      if (ok) {
+        for (int i = tid; i < cnt * (kENC / 8); i += 128) {
+          const int mm = i / (kENC / 8), q = i % (kENC / 8);
+          *reinterpret_cast<uint4*>(a.y + (long long)tok[mm] * a.ldy + n0 + 8 * q) =
+              *reinterpret_cast<const uint4*>(ys + mm * kEYRow + q * 16);
+        }
       }
     }
     ++nunit;
     __syncthreads();
   }
-  if (warp < 4) bulk_wait0();
   if (!ok && tid == 0) report(a.err, LORA_DERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();
@@ -497,19 +493,10 @@ lora_status_t launch_shrink_tc(const void* x, long long ldx, float* h, long long
   const int n_clusters = seg->max_long_units < cap ? seg->max_long_units : cap;
   if (n_clusters <= 0) return LORA_OK;
   if (ensure_smem_attr((const void*)shrink_tc_kernel, kShrinkSmem) != cudaSuccess) return LORA_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(n_clusters * cl), 1, 1);
-  cfg.blockDim = dim3(kTcThreads, 1, 1);
-  cfg.dynamicSmemBytes = kShrinkSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)cl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, shrink_tc_kernel, a) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+  return launch_pdl((const void*)shrink_tc_kernel, dim3((unsigned)(n_clusters * cl)), dim3(kTcThreads),
+                    kShrinkSmem, stream, cl, &a) == cudaSuccess
+             ? LORA_OK
+             : LORA_ERR_CUDA;
 }
 
 lora_status_t launch_expand_tc(const float* h, long long ldh, int h_by_token, void* y, long long ldy,
@@ -522,8 +509,10 @@ lora_status_t launch_expand_tc(const float* h, long long ldh, int h_by_token, vo
   if (upper < grid) grid = upper;
   if (grid <= 0) return LORA_OK;
   if (ensure_smem_attr((const void*)expand_tc_kernel, kExpandSmem) != cudaSuccess) return LORA_ERR_CUDA;
-  expand_tc_kernel<<<(unsigned)grid, kTcThreads, kExpandSmem, stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+  return launch_pdl((const void*)expand_tc_kernel, dim3((unsigned)grid), dim3(kTcThreads), kExpandSmem, stream,
+                    0, &a) == cudaSuccess
+             ? LORA_OK
+             : LORA_ERR_CUDA;
 }
 
 }  // namespace lora
