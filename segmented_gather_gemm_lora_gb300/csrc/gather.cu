@@ -18,23 +18,46 @@
 //   expand  y[t, n] = bf16(y0[t, n] + sum_j h[t, j] * B_i[j, n]),  n in slice c
 // The rank-r intermediate never leaves the chip.
 //
-// Data movement.  Adapter rows (translated page by page through the page
-// table, "Multi-LoRA Serving in Production", section "Unified Paged Memory")
-// and token rows are staged in shared memory by 16-byte asynchronous copies
-// from every thread into a ring of stages, each completed through an mbarrier;
-// the expand's B and y0 chunks are issued before the shrink's arithmetic
-// finishes, so both phases' bytes are in flight together.
+// Data movement.  A slice is cut into sub-slices of 512 columns and each
+// sub-slice into chunks of 16 adapter rows, so every staged row is a 1 KB run
+// (translated 16 bytes at a time through the page table, "Multi-LoRA Serving
+// in Production", section "Unified Paged Memory"), staged together with the
+// unit's token rows for the same columns.  Every thread copies 16-byte pieces
+// with cp.async, one warp per row (512 bytes per instruction), into a ring of
+// two stages, each completed through an mbarrier; expand chunks are issued as
+// soon as stages free up, so the two phases' bytes overlap.  Rows of 1 KB are
+// what keeps a streaming multiprocessor near its share of HBM bandwidth;
+// rows of a few hundred bytes fall to a half or less.
+//
+// Summation order.  Each rank row's shrink dot product over a sub-slice and
+// each output's expand sum over a 16-row chunk are fixed functions of column
+// and row positions, and partial results combine in sub-slice / chunk order.
+// A token's result therefore depends neither on how many tokens share its unit
+// nor on its adapter's rank: zero-padding an adapter or moving a token between
+// units changes no bit of its output.
 #include "common.cuh"
 #include "internal.h"
 
 namespace lora {
 
 constexpr int kGThreads = 256;
-constexpr int kStages = 4;
-constexpr int kStageBytes = 16384;
 constexpr int kNT = LORA_SHORT_MAX_TOKENS;  // tokens per group
 constexpr int kHMax = LORA_MAX_RANK;
 constexpr int kMaxCluster = 8;
+constexpr int kSub = 512;                      // columns per sub-slice (one 1 KB row)
+constexpr int kChunkRows = 16;                 // adapter rows per chunk
+constexpr int kRowBytes = kSub * 2;
+constexpr int kStages = 2;
+constexpr int kStageBytes = (kChunkRows + kNT) * kRowBytes;  // 24 KB
+constexpr int kMaxPgSlots = 512;  // page-list slots of one adapter cached in shared memory
+
+constexpr size_t kOffBars = (size_t)kStages * kStageBytes;
+constexpr size_t kOffEacc = kOffBars + 64;                                  // fp32 [kNT][kSub]
+constexpr size_t kOffHp = kOffEacc + (size_t)kNT * kSub * sizeof(float);    // fp32 [2][kNT][kHMax]
+constexpr size_t kOffHs = kOffHp + 2 * kNT * kHMax * sizeof(float);         // fp32 [kNT][kHMax]
+constexpr size_t kOffTok = kOffHs + kNT * kHMax * sizeof(float);
+constexpr size_t kOffPgt = kOffTok + kNT * sizeof(int) + 32;
+constexpr size_t kGatherSmem = kOffPgt + kMaxPgSlots * sizeof(int);
 
 struct GatherArgs {
   const uint16_t* x;
@@ -58,41 +81,31 @@ struct GatherArgs {
   int short_only;
 };
 
-constexpr size_t kOffBars = (size_t)kStages * kStageBytes;
-constexpr size_t kOffHp = kOffBars + kStages * 8;
-constexpr size_t kOffHs = kOffHp + 2 * kNT * kHMax * sizeof(float);
-constexpr size_t kOffTok = kOffHs + kNT * kHMax * sizeof(float);
-constexpr int kMaxPgSlots = 1024;  // page-list slots of one adapter cached in shared memory
-constexpr size_t kOffPgt = kOffTok + kNT * sizeof(int) + 64;
-constexpr size_t kGatherSmem = kOffPgt + kMaxPgSlots * sizeof(int);
-
-// Elements per row of one stage: the stage holds up to max_rank adapter rows
-// and up to kNT token rows.  A function of the view's max_rank alone, so a
-// token's arithmetic depends neither on how many tokens share its unit nor on
-// its adapter's rank (zero-padding an adapter does not change its result).
-__device__ __forceinline__ int chunk_width(int r) {
-  int w = ((kStageBytes / 2) / (r + kNT)) & ~7;
-  return w < 8 ? 8 : w;
-}
-
+// One unit's chunk schedule: shrink chunks (sub-slice ks, row block jb) first,
+// then expand chunks (sub-slice ns, row block jb).
 struct ChunkPlan {
-  int r, ntok, nkc, nnc, wk, wn, k0, k1, n0, n1;
+  int r, ntok, njb;  // rank, tokens, row blocks of kChunkRows
+  int nks, nns;      // sub-slices of the d_in / d_out slices (0 if the phase is skipped)
+  int k0, k1, n0, n1;
   int a_page0, b_page0;
-  int na;          // page-list slots of A_i (B_i's follow in the cached table)
-  const int* pgt;  // cached physical pages of A_i then B_i, or null
+  int na;            // page-list slots of A_i (B_i's follow in the cached table)
+  const int* pgt;    // cached physical pages of A_i then B_i, or null
 };
 
-// Stage chunk c (shrink chunks first, then expand chunks) into `stage`: every
-// thread of the CTA copies 16-byte pieces with cp.async (the load/store units
-// issue these in parallel; one TMA bulk copy per row costs tens of
-// nanoseconds of issue each, far too slow for rows of a few hundred bytes)
-// and then arrives on `bar` when its own pieces have landed.
-__device__ __forceinline__ void issue_chunk(const GatherArgs& a, const ChunkPlan& p, const int* tok,
-                                            int c, uint8_t* stage, uint32_t bar, int tid) {
-  const bool shrink = c < p.nkc;
-  const int stride = shrink ? p.wk : p.wn;
-  const int cols = shrink ? p.k0 + c * p.wk : p.n0 + (c - p.nkc) * p.wn;
-  const int w = shrink ? min(p.wk, p.k1 - cols) : min(p.wn, p.n1 - cols);
+// Stage chunk c into `stage`: adapter rows [16 jb, 16 jb + 16) of the chunk's
+// sub-slice at rows 0..15, then the unit's token rows (x for the shrink, y0
+// for the expand) of the same columns at rows 16..23.  One warp per row,
+// 16-byte pieces per lane; every thread then arrives on `bar` once its own
+// pieces have landed.
+__device__ __forceinline__ void issue_chunk(const GatherArgs& a, const ChunkPlan& p, const int* tok, int c,
+                                            uint8_t* stage, uint32_t bar, int tid) {
+  const int nsh = p.nks * p.njb;
+  const bool shrink = c < nsh;
+  const int cc = shrink ? c : c - nsh;
+  const int sub = cc / p.njb, jb = cc - sub * p.njb;
+  const int col0 = shrink ? p.k0 + sub * kSub : p.n0 + sub * kSub;
+  const int w = shrink ? min(kSub, p.k1 - col0) : min(kSub, p.n1 - col0);
+  const int j0 = jb * kChunkRows, nrows = min(kChunkRows, p.r - j0);
   const long long rowlen = shrink ? a.v.d_in : a.v.d_out;
   const long long page0 = shrink ? p.a_page0 : p.b_page0;
   const uint16_t* act = shrink ? a.x : a.y;
@@ -102,10 +115,11 @@ __device__ __forceinline__ void issue_chunk(const GatherArgs& a, const ChunkPlan
   const uint32_t sbase = smem_u32(stage);
   const int nq = w >> 3;  // 16-byte pieces per row
   const int warp = tid >> 5, lane = tid & 31;
-  for (int item = warp; item < p.r + p.ntok; item += kGThreads / 32) {
-    const uint32_t drow = sbase + (uint32_t)(item * stride * 2);
-    if (item < p.r) {
-      const long long e0 = (long long)item * rowlen + cols;  // first element of the row piece
+  for (int item = warp; item < nrows + p.ntok; item += kGThreads / 32) {
+    const bool adapter_row = item < nrows;
+    const uint32_t drow = sbase + (uint32_t)((adapter_row ? item : kChunkRows + item - nrows) * kRowBytes);
+    if (adapter_row) {
+      const long long e0 = (long long)(j0 + item) * rowlen + col0;
       for (int q = lane; q < nq; q += 32) {
         const long long e = e0 + 8 * q;
         const long long idx = e >> shift;
@@ -114,7 +128,7 @@ __device__ __forceinline__ void issue_chunk(const GatherArgs& a, const ChunkPlan
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(drow + 16 * q), "l"(src) : "memory");
       }
     } else {
-      const uint16_t* src0 = act + (long long)tok[item - p.r] * ld + cols;
+      const uint16_t* src0 = act + (long long)tok[item - nrows] * ld + col0;
       for (int q = lane; q < nq; q += 32)
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(drow + 16 * q), "l"(src0 + 8 * q) : "memory");
     }
@@ -122,40 +136,111 @@ __device__ __forceinline__ void issue_chunk(const GatherArgs& a, const ChunkPlan
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Partial shrink of one staged chunk for NT tokens: warp w takes rank rows
-// j = w, w + 8, ...; its lanes take 8-element vectors of the chunk; the row's
-// dot products with every token are reduced over the warp and added to the
-// CTA's partial h.  Instantiated per token count so that a one-token decode
-// unit executes only its own arithmetic.
+// Shrink of one staged chunk for NT tokens: warp w takes the chunk's rows w
+// and w + 8 together (one unpack of each token vector serves both); its lanes
+// take fixed 8-column vectors of the sub-slice; each row's dot product with
+// every token is reduced over the warp and added to the CTA's partial h
+// (sub-slices in order).  Instantiated per token count so that a one-token
+// decode unit executes only its own arithmetic.
 template <int NT>
-__device__ __forceinline__ void shrink_chunk(const uint8_t* sb, const ChunkPlan& p, int nvec, float* hpb, int warp,
-                                             int lane) {
-  for (int j = warp; j < p.r; j += kGThreads / 32) {
-    float acc[NT];
+__device__ __forceinline__ void shrink_chunk(const uint8_t* sb, int j0, int nrows, int nvec, float* hpb,
+                                             int warp, int lane) {
+  const uint4* xrow = reinterpret_cast<const uint4*>(sb + kChunkRows * kRowBytes);
+  const int i0 = warp, i1 = warp + kGThreads / 32;  // the warp's two rows (16-row chunks)
+  const bool has0 = i0 < nrows, has1 = i1 < nrows;
+  if (!has0) return;
+  float acc0[NT], acc1[NT];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-    const uint4* arow = reinterpret_cast<const uint4*>(sb + (size_t)j * p.wk * 2);
-    const uint4* xrow = reinterpret_cast<const uint4*>(sb + (size_t)p.r * p.wk * 2);
-    const int xstride = p.wk / 8;  // uint4 per staged row
-    for (int vv = lane; vv < nvec; vv += 32) {
-      float af[8];
-      unpack8(arow[vv], af);
+  for (int t = 0; t < NT; ++t) acc0[t] = acc1[t] = 0.f;
+  const uint4* arow0 = reinterpret_cast<const uint4*>(sb + i0 * kRowBytes);
+  const uint4* arow1 = reinterpret_cast<const uint4*>(sb + (has1 ? i1 : i0) * kRowBytes);
+  for (int vv = lane; vv < nvec; vv += 32) {
+    float a0[8], a1[8];
+    unpack8(arow0[vv], a0);
+    unpack8(arow1[vv], a1);
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        float xf[8];
-        unpack8(xrow[t * xstride + vv], xf);
+    for (int t = 0; t < NT; ++t) {
+      float xf[8];
+      unpack8(xrow[t * (kRowBytes / 16) + vv], xf);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[t] = fmaf(af[q], xf[q], acc[t]);
+      for (int q = 0; q < 8; ++q) {
+        acc0[t] = fmaf(a0[q], xf[q], acc0[t]);
+        acc1[t] = fmaf(a1[q], xf[q], acc1[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      acc0[t] += __shfl_xor_sync(0xffffffffu, acc0[t], o);
+      acc1[t] += __shfl_xor_sync(0xffffffffu, acc1[t], o);
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      hpb[t * kHMax + j0 + i0] += acc0[t];
+      if (has1) hpb[t * kHMax + j0 + i1] += acc1[t];
+    }
+  }
+}
+
+// Expand of one staged chunk.  A warp takes one (token, block of 8 output
+// vectors): lane = 8 g + u handles vector u of the block for the chunk's rows
+// 4 g .. 4 g + 3 (ascending), so each group of 8 lanes reads 128 contiguous
+// bytes of one row (no bank conflicts); the four row-quarter sums meet in a
+// fixed two-step butterfly, and chunk sums accumulate in chunk order in eacc.
+// The sub-slice's last chunk adds y0 and writes y.
+__device__ __forceinline__ void expand_chunk(const GatherArgs& a, const uint8_t* sb, const float* hs, float* eacc,
+                                             const int* tok, int ntok, int nvec, int j0, int nrows, bool first,
+                                             bool last, int col0, bool ok, int warp, int lane) {
+  const int nblk = (nvec + 7) >> 3;
+  const int g = lane >> 3, u = lane & 7;
+  for (int wi = warp; wi < ntok * nblk; wi += kGThreads / 32) {
+    const int t = wi / nblk, vv = (wi - t * nblk) * 8 + u;
+    const bool act = vv < nvec;
+    float o[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) o[q] = 0.f;
+    if (act) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = 4 * g + k;
+        if (i < nrows) {
+          const float hj = hs[t * kHMax + j0 + i];
+          float bf[8];
+          unpack8(reinterpret_cast<const uint4*>(sb + i * kRowBytes)[vv], bf);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) o[q] = fmaf(hj, bf[q], o[q]);
+        }
       }
     }
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
+    for (int m = 8; m < 32; m <<= 1) {
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+      for (int q = 0; q < 8; ++q) o[q] += __shfl_xor_sync(0xffffffffu, o[q], m);
     }
-    if (lane == 0) {
-#pragma unroll
-      for (int t = 0; t < NT; ++t) hpb[t * kHMax + j] += acc[t];
+    if (act && g == 0) {
+      float4* ea = reinterpret_cast<float4*>(eacc + (t * kSub + vv * 8));
+      if (!first) {
+        const float4 e0 = ea[0], e1 = ea[1];
+        o[0] = e0.x + o[0]; o[1] = e0.y + o[1]; o[2] = e0.z + o[2]; o[3] = e0.w + o[3];
+        o[4] = e1.x + o[4]; o[5] = e1.y + o[5]; o[6] = e1.z + o[6]; o[7] = e1.w + o[7];
+      }
+      if (!last) {
+        ea[0] = make_float4(o[0], o[1], o[2], o[3]);
+        ea[1] = make_float4(o[4], o[5], o[6], o[7]);
+      } else if (ok) {
+        float yf[8];
+        unpack8(reinterpret_cast<const uint4*>(sb + (kChunkRows + t) * kRowBytes)[vv], yf);
+        uint4 out;
+        out.x = pack_bf16x2(yf[0] + o[0], yf[1] + o[1]);
+        out.y = pack_bf16x2(yf[2] + o[2], yf[3] + o[3]);
+        out.z = pack_bf16x2(yf[4] + o[4], yf[5] + o[5]);
+        out.w = pack_bf16x2(yf[6] + o[6], yf[7] + o[7]);
+        *reinterpret_cast<uint4*>(a.y + (long long)tok[t] * a.ldy + col0 + vv * 8) = out;
+      }
     }
   }
 }
@@ -163,9 +248,11 @@ __device__ __forceinline__ void shrink_chunk(const uint8_t* sb, const ChunkPlan&
 __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_constant__ GatherArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBars);
+  float* eacc = reinterpret_cast<float*>(sm + kOffEacc);
   float* hp = reinterpret_cast<float*>(sm + kOffHp);
   float* hs = reinterpret_cast<float*>(sm + kOffHs);
   int* tok = reinterpret_cast<int*>(sm + kOffTok);
+  int* pgt = reinterpret_cast<int*>(sm + kOffPgt);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t crank = cluster_ctarank(), ncta = cluster_nctarank();
@@ -189,7 +276,6 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
   uint32_t parity = 0;  // bit s: parity of stage s's next phase
   int gbuf = 0;
 
-  int* pgt = reinterpret_cast<int*>(sm + kOffPgt);
   for (int u = (int)cid; u < n_units; u += (int)ncl) {
     int ad, tb = 0, cnt;
     if (a.src == kSrcTokens) {
@@ -249,16 +335,17 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
 
     ChunkPlan p;
     p.r = d.rank;
-    p.wk = chunk_width(v.max_rank);
-    p.wn = p.wk;
+    p.njb = (p.r + kChunkRows - 1) / kChunkRows;
     p.k0 = k0; p.k1 = k1; p.n0 = n0; p.n1 = n1;
-    p.nkc = (a.mode != kModeExpand && k1 > k0) ? (k1 - k0 + p.wk - 1) / p.wk : 0;
-    p.nnc = (a.mode != kModeShrink && n1 > n0) ? (n1 - n0 + p.wn - 1) / p.wn : 0;
+    p.nks = (a.mode != kModeExpand && k1 > k0) ? (k1 - k0 + kSub - 1) / kSub : 0;
+    p.nns = (a.mode != kModeShrink && n1 > n0) ? (n1 - n0 + kSub - 1) / kSub : 0;
     p.a_page0 = d.a_page0;
     p.b_page0 = d.b_page0;
     p.na = (int)na;
     p.pgt = cached ? pgt : nullptr;
     const float sc = d.scale;
+    const int nsh = p.nks * p.njb;
+    const int nch = nsh + p.nns * p.njb;
 
     for (int g0 = 0; g0 < cnt; g0 += kNT) {
       p.ntok = min(kNT, cnt - g0);
@@ -268,29 +355,28 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
       for (int i = tid; i < kNT * kHMax; i += kGThreads) hpb[i] = 0.f;
       __syncthreads();
 
-      const int nch = p.nkc + p.nnc;
       for (int c = 0; c < min(kStages, nch); ++c)
         issue_chunk(a, p, tok, c, sm + (size_t)c * kStageBytes, smem_u32(&bars[c]), tid);
       bool ok = true;
 
       // ---- shrink: partial h over this CTA's d_in slice ----
-      for (int c = 0; c < p.nkc; ++c) {
+      for (int c = 0; c < nsh; ++c) {
         const int st = c % kStages;
         if (!mbar_wait(smem_u32(&bars[st]), (parity >> st) & 1u)) ok = false;
         parity ^= 1u << st;
         const uint8_t* sb = sm + (size_t)st * kStageBytes;
-        const int cols = p.k0 + c * p.wk;
-        const int w = min(p.wk, p.k1 - cols);
-        const int nvec = w >> 3;
+        const int ks = c / p.njb, jb = c - ks * p.njb;
+        const int nvec = min(kSub, p.k1 - (p.k0 + ks * kSub)) >> 3;
+        const int j0 = jb * kChunkRows, nrows = min(kChunkRows, p.r - j0);
         switch (ntok) {
-          case 1: shrink_chunk<1>(sb, p, nvec, hpb, warp, lane); break;
-          case 2: shrink_chunk<2>(sb, p, nvec, hpb, warp, lane); break;
-          case 3: shrink_chunk<3>(sb, p, nvec, hpb, warp, lane); break;
-          case 4: shrink_chunk<4>(sb, p, nvec, hpb, warp, lane); break;
-          case 5: shrink_chunk<5>(sb, p, nvec, hpb, warp, lane); break;
-          case 6: shrink_chunk<6>(sb, p, nvec, hpb, warp, lane); break;
-          case 7: shrink_chunk<7>(sb, p, nvec, hpb, warp, lane); break;
-          default: shrink_chunk<8>(sb, p, nvec, hpb, warp, lane); break;
+          case 1: shrink_chunk<1>(sb, j0, nrows, nvec, hpb, warp, lane); break;
+          case 2: shrink_chunk<2>(sb, j0, nrows, nvec, hpb, warp, lane); break;
+          case 3: shrink_chunk<3>(sb, j0, nrows, nvec, hpb, warp, lane); break;
+          case 4: shrink_chunk<4>(sb, j0, nrows, nvec, hpb, warp, lane); break;
+          case 5: shrink_chunk<5>(sb, j0, nrows, nvec, hpb, warp, lane); break;
+          case 6: shrink_chunk<6>(sb, j0, nrows, nvec, hpb, warp, lane); break;
+          case 7: shrink_chunk<7>(sb, j0, nrows, nvec, hpb, warp, lane); break;
+          default: shrink_chunk<8>(sb, j0, nrows, nvec, hpb, warp, lane); break;
         }
         __syncthreads();
         if (c + kStages < nch)
@@ -331,52 +417,16 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
       }
 
       // ---- expand: y over this CTA's d_out slice ----
-      for (int c = p.nkc; c < nch; ++c) {
+      for (int c = nsh; c < nch; ++c) {
         const int st = c % kStages;
         if (!mbar_wait(smem_u32(&bars[st]), (parity >> st) & 1u)) ok = false;
         parity ^= 1u << st;
         const uint8_t* sb = sm + (size_t)st * kStageBytes;
-        const int cols = p.n0 + (c - p.nkc) * p.wn;
-        const int w = min(p.wn, p.n1 - cols);
-        const int nvec = w >> 3;
-        // Eight consecutive lanes share one (token, 8-column vector); lane jq
-        // sums rank rows j = jq, jq + 8, ... in ascending order and the eight
-        // partial sums meet in a fixed butterfly.  The order depends neither on
-        // the unit's token count nor on the adapter's rank.
-        const int items = ntok * nvec * 8;
-        for (int base = 0; base < items; base += kGThreads) {
-          const int it = base + tid;
-          const bool act = it < items;
-          const int jq = it & 7, tv = it >> 3;
-          const int t = act ? tv / nvec : 0, vv = act ? tv - t * nvec : 0;
-          float o[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) o[q] = 0.f;
-          if (act) {
-            for (int j = jq; j < p.r; j += 8) {
-              const float hj = hs[t * kHMax + j];
-              float bf[8];
-              unpack8(reinterpret_cast<const uint4*>(sb + (size_t)j * p.wn * 2)[vv], bf);
-#pragma unroll
-              for (int q = 0; q < 8; ++q) o[q] = fmaf(hj, bf[q], o[q]);
-            }
-          }
-#pragma unroll
-          for (int m = 1; m < 8; m <<= 1) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) o[q] += __shfl_xor_sync(0xffffffffu, o[q], m);
-          }
-          if (act && jq == 0 && ok) {
-            float yf[8];
-            unpack8(reinterpret_cast<const uint4*>(sb + (size_t)(p.r + t) * p.wn * 2)[vv], yf);
-            uint4 out;
-            out.x = pack_bf16x2(yf[0] + o[0], yf[1] + o[1]);
-            out.y = pack_bf16x2(yf[2] + o[2], yf[3] + o[3]);
-            out.z = pack_bf16x2(yf[4] + o[4], yf[5] + o[5]);
-            out.w = pack_bf16x2(yf[6] + o[6], yf[7] + o[7]);
-            *reinterpret_cast<uint4*>(a.y + (long long)tok[t] * a.ldy + cols + vv * 8) = out;
-          }
-        }
+        const int ns = (c - nsh) / p.njb, jb = (c - nsh) - ns * p.njb;
+        const int col0 = p.n0 + ns * kSub;
+        const int nvec = min(kSub, p.n1 - col0) >> 3;
+        const int j0 = jb * kChunkRows, nrows = min(kChunkRows, p.r - j0);
+        expand_chunk(a, sb, hs, eacc, tok, ntok, nvec, j0, nrows, jb == 0, jb == p.njb - 1, col0, ok, warp, lane);
         __syncthreads();
         if (c + kStages < nch)
           issue_chunk(a, p, tok, c + kStages, sm + (size_t)st * kStageBytes, smem_u32(&bars[st]), tid);

@@ -148,6 +148,7 @@ def build_pool(
     zero_B: bool = False,
     zero_A: bool = False,
     scales: Optional[Sequence[float]] = None,
+    shuffle_pages: bool = True,
 ) -> AdapterPool:
     """Draw adapters of the given ranks (0 = not resident) and pack them into pages."""
     n = len(ranks)
@@ -169,7 +170,8 @@ def build_pool(
         A.append(a)
         B.append(b)
     return pack_pool(A, B, ranks, d_in, d_out, rng, alpha=alpha, page_elems=page_elems,
-                     max_rank=max_rank, spare_pages=spare_pages, scales=scales)
+                     max_rank=max_rank, spare_pages=spare_pages, scales=scales,
+                     shuffle_pages=shuffle_pages)
 
 
 def pack_pool(
@@ -185,8 +187,10 @@ def pack_pool(
     max_rank: Optional[int] = None,
     spare_pages: int = 3,
     scales: Optional[Sequence[float]] = None,
+    shuffle_pages: bool = True,
 ) -> AdapterPool:
-    """Lay logical adapter matrices out on randomly permuted physical pages."""
+    """Lay logical adapter matrices out on physical pages: a random permutation of the
+    pool (default), or in order when shuffle_pages is False."""
     P = int(page_elems)
     n = len(ranks)
     desc = np.zeros(n, dtype=DESC_DTYPE)
@@ -198,7 +202,7 @@ def pack_pool(
         counts.append((na, nb))
     n_list = sum(na + nb for na, nb in counts)
     n_pages = n_list + spare_pages
-    phys = rng.permutation(n_pages).astype(np.int32)
+    phys = rng.permutation(n_pages).astype(np.int32) if shuffle_pages else np.arange(n_pages, dtype=np.int32)
     page_list = phys[:n_list].copy()
     pool = np.full((n_pages, P), BF16_NAN, dtype=np.uint16)
     flat = pool.reshape(-1)
