@@ -8,7 +8,7 @@
 // "S-LoRA: MBGMV and MBGMM Kernels"), and for the shrink / expand stages alone.
 //
 // Work decomposition.  One thread-block cluster of CL CTAs (CL <= 8) takes one
-// work unit (an adapter and up to 8 of its tokens) at a time.  CTA c of the
+// work unit (an adapter and up to 8 of its tokens, in groups of 4) at a time.  CTA c of the
 // cluster owns the c-th slice of d_in for the shrink and the c-th slice of
 // d_out for the expand, so every adapter byte and every activation byte is
 // read once per unit:
@@ -24,8 +24,8 @@
 // in Production", section "Unified Paged Memory"), staged together with the
 // unit's token rows for the same columns.  Every thread copies 16-byte pieces
 // with cp.async, one warp per row (512 bytes per instruction), into a ring of
-// two stages, each completed through an mbarrier; expand chunks are issued as
-// soon as stages free up, so the two phases' bytes overlap.  Rows of 1 KB are
+// three stages, each completed through an mbarrier; expand chunks are issued
+// as soon as stages free up, so the two phases' bytes overlap.  Rows of 1 KB are
 // what keeps a streaming multiprocessor near its share of HBM bandwidth;
 // rows of a few hundred bytes fall to a half or less.
 //
@@ -41,14 +41,14 @@
 namespace lora {
 
 constexpr int kGThreads = 256;
-constexpr int kNT = LORA_SHORT_MAX_TOKENS;  // tokens per group
+constexpr int kNT = 4;  // tokens per group (a unit of up to 8 tokens runs in two groups)
 constexpr int kHMax = LORA_MAX_RANK;
 constexpr int kMaxCluster = 8;
 constexpr int kSub = 512;                      // columns per sub-slice (one 1 KB row)
 constexpr int kChunkRows = 16;                 // adapter rows per chunk
 constexpr int kRowBytes = kSub * 2;
-constexpr int kStages = 2;
-constexpr int kStageBytes = (kChunkRows + kNT) * kRowBytes;  // 24 KB
+constexpr int kStages = 3;
+constexpr int kStageBytes = (kChunkRows + kNT) * kRowBytes;  // 20 KB
 constexpr int kMaxPgSlots = 512;  // page-list slots of one adapter cached in shared memory
 
 constexpr size_t kOffBars = (size_t)kStages * kStageBytes;
@@ -372,11 +372,7 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
           case 1: shrink_chunk<1>(sb, j0, nrows, nvec, hpb, warp, lane); break;
           case 2: shrink_chunk<2>(sb, j0, nrows, nvec, hpb, warp, lane); break;
           case 3: shrink_chunk<3>(sb, j0, nrows, nvec, hpb, warp, lane); break;
-          case 4: shrink_chunk<4>(sb, j0, nrows, nvec, hpb, warp, lane); break;
-          case 5: shrink_chunk<5>(sb, j0, nrows, nvec, hpb, warp, lane); break;
-          case 6: shrink_chunk<6>(sb, j0, nrows, nvec, hpb, warp, lane); break;
-          case 7: shrink_chunk<7>(sb, j0, nrows, nvec, hpb, warp, lane); break;
-          default: shrink_chunk<8>(sb, j0, nrows, nvec, hpb, warp, lane); break;
+          default: shrink_chunk<4>(sb, j0, nrows, nvec, hpb, warp, lane); break;
         }
         __syncthreads();
         if (c + kStages < nch)
