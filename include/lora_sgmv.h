@@ -117,7 +117,8 @@ typedef struct {
  * units, meta[3] = long work units.  short_units lists the segments of at most
  * LORA_SHORT_MAX_TOKENS tokens; long_units lists (segment, offset) pairs, one
  * per LORA_TILE_M-token tile of every longer segment, both in segment order.
- * scratch belongs to lora_segments_build, h_scratch to lora_apply.
+ * scratch belongs to lora_segments_build; h_scratch, k_partials and tickets
+ * to the compute calls.
  */
 typedef struct {
   int32_t T;              /* tokens the buffer was carved for */
@@ -131,7 +132,14 @@ typedef struct {
   int32_t* scratch;       /* [4 * T + 8]: run starts, run ends, run ids, run positions */
   float* h_scratch;       /* [T * LORA_MAX_RANK]: lora_apply's rank-r intermediate of
                              tokens on the tensor-core path, by segment position */
+  float* k_partials;      /* [LORA_KSPLIT_MAX * T * LORA_MAX_RANK]: partial shrink sums of
+                             the tensor-core path, one slab per slice of d_in */
+  int32_t* tickets;       /* [max_long_units]: per-tile completion counters (zeroed by
+                             lora_segments_build, left at zero by every call) */
 } lora_segments_t;
+
+/** Slices of d_in the tensor-core shrink splits a tile into, at most. */
+#define LORA_KSPLIT_MAX 8
 
 /** Bytes of the device buffer lora_segments_carve needs for T tokens (T >= 0). */
 size_t lora_segments_buffer_bytes(int32_t T);

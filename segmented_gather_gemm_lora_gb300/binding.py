@@ -67,7 +67,8 @@ class lora_segments_t(ctypes.Structure):
                 ("token_perm", ctypes.c_void_p), ("seg_indptr", ctypes.c_void_p),
                 ("seg_adapter", ctypes.c_void_p), ("meta", ctypes.c_void_p),
                 ("short_units", ctypes.c_void_p), ("long_units", ctypes.c_void_p),
-                ("scratch", ctypes.c_void_p), ("h_scratch", ctypes.c_void_p)]
+                ("scratch", ctypes.c_void_p), ("h_scratch", ctypes.c_void_p),
+                ("k_partials", ctypes.c_void_p), ("tickets", ctypes.c_void_p)]
 
 
 class LoraError(RuntimeError):

@@ -41,7 +41,7 @@ def test_abi_version_and_status_strings():
 def test_struct_sizes_match_c_layout():
     assert ctypes.sizeof(B.lora_adapter_desc_t) == 16
     assert ctypes.sizeof(B.lora_pool_view_t) == 64
-    assert ctypes.sizeof(B.lora_segments_t) == 8 + 8 * 8
+    assert ctypes.sizeof(B.lora_segments_t) == 8 + 10 * 8
 
 
 @pytest.mark.parametrize("rank,d_in,d_out,P", [(16, 8192, 8192, 4096), (13, 5120, 11008, 4096),
@@ -54,7 +54,7 @@ def test_carve_layout():
     L = B.lib()
     for T in (0, 1, 16, 64, 129, 9216):
         n = B.lora_segments_buffer_bytes(T)
-        assert n % 16 == 0 and n >= 4 * (4 * T + 8) + 4 * 64 * T
+        assert n % 16 == 0 and n >= 4 * (4 * T + 8) + 4 * 64 * T * (1 + 8)
         buf = (ctypes.c_uint8 * (n + 16))()
         base = (ctypes.addressof(buf) + 15) // 16 * 16
         s = B.lora_segments_t()
@@ -62,7 +62,7 @@ def test_carve_layout():
         assert s.T == T
         assert s.max_long_units == T // 128 + T // 9 + 1
         ptrs = [s.token_perm, s.seg_indptr, s.seg_adapter, s.meta, s.short_units, s.long_units, s.scratch,
-                s.h_scratch]
+                s.h_scratch, s.k_partials, s.tickets]
         assert all(p % 16 == 0 for p in ptrs)
         assert ptrs == sorted(ptrs) and ptrs[0] == base
         assert L.lora_segments_carve(ctypes.c_void_p(base), n - 16, T, ctypes.byref(s)) == B.LORA_ERR_WORKSPACE
@@ -82,7 +82,7 @@ def fake_seg(T=16):
     s.T = T
     s.max_long_units = T // 128 + T // 9 + 1
     for i, f in enumerate(("token_perm", "seg_indptr", "seg_adapter", "meta", "short_units",
-                           "long_units", "scratch", "h_scratch")):
+                           "long_units", "scratch", "h_scratch", "k_partials", "tickets")):
         setattr(s, f, 0x100000 + 0x1000 * i)
     return s
 

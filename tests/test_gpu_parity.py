@@ -447,3 +447,93 @@ def test_tc_device_errors_in_long_tiles():
         good = ids == 0
         compare_bf16(y[good], ref[good], "long tiles next to bad ones")
         assert np.array_equal(y[~good], batch.y0[~good])
+
+
+def test_tc_segments_reused_across_calls_and_shapes():
+    """One segment buffer serves several projections of different d_in in a row (the
+    per-tile tickets of the split d_in reduction must be back at zero after each
+    call); every result equals a fresh run bit for bit."""
+    rng = np.random.default_rng(26)
+    ranks = [16, 64, 7]
+    lens = [256, 300, 129]
+    ids = np.concatenate([np.full(n, i, dtype=np.int32) for i, n in enumerate(lens)])
+    seg = B.Segments(ids.size)
+    err = new_err()
+    B.lora_segments_build(ids_dev(ids), len(ranks), seg, mode=B.LORA_SEG_GROUP, err=err)
+    for d_in, d_out in ((4096, 1024), (1024, 2048), (8192, 1024), (4096, 1024)):
+        pool = W.build_pool(rng, d_in, d_out, ranks, max_rank=64)
+        batch = W.make_batch(rng, ids, d_in, d_out)
+        view = B.PoolView.from_host(pool)
+        outs = []
+        for _ in range(2):
+            y = to_dev_bits(batch.y0)
+            B.lora_apply(to_dev_bits(batch.x), y, seg, view, err=err)
+            torch.cuda.synchronize()
+            outs.append(to_host_bits(y))
+        assert int(err.item()) == 0
+        fresh, e2, _ = run_apply(batch, pool, B.LORA_SEG_GROUP, len(ranks), view=view)
+        assert e2 == 0
+        assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], fresh)
+        ref, _ = oracle.lora_apply(batch.x, batch.y0, ids, pool)
+        compare_bf16(fresh, ref, "reused segments %dx%d" % (d_in, d_out))
+
+
+@pytest.mark.parametrize("d_in", [1024, 4096])
+def test_tc_shrink_caller_h_odd_stride_and_ranks(d_in):
+    """Caller's h with a row stride of 72 and ranks that are not multiples of 4, with
+    d_in in one slice (h written straight from tensor memory) and in four slices
+    (partials summed by the tile's last slice)."""
+    pool, batch = long_segment_batch(27, [7, 13, 33, 64], [200, 150, 130, 300], d_in, 1024)
+    view = B.PoolView.from_host(pool)
+    seg = B.Segments(batch.T)
+    err = new_err()
+    B.lora_segments_build(ids_dev(batch.ids), 4, seg, err=err)
+    hbuf = torch.full((batch.T, 72), -5.0, dtype=torch.float32, device="cuda")
+    B.lora_sgmv_shrink(to_dev_bits(batch.x), hbuf, seg, view, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    href, _ = oracle.shrink(batch.x, batch.ids, pool, h_init=np.full((batch.T, 72), -5.0), ldh=72)
+    got = hbuf.cpu().numpy().astype(np.float64)
+    scale = np.abs(href).max()
+    np.testing.assert_allclose(got, href, rtol=1e-4, atol=1e-5 * scale)
+
+
+def test_tc_interleaved_tokens_full_tiles():
+    """Segments of 300 tokens whose rows are interleaved in x (every third row), so full
+    tiles take the row-by-row copies, next to a run of 256 consecutive tokens."""
+    rng = np.random.default_rng(28)
+    ranks = [32, 8, 64, 16]
+    ids = np.concatenate([np.arange(900, dtype=np.int32) % 3, np.full(256, 3, dtype=np.int32)])
+    pool = W.build_pool(rng, 2048, 4096, ranks, max_rank=64)
+    batch = W.make_batch(rng, ids, 2048, 4096, ldx=2048 + 8, ldy=4096 + 64)
+    for mode in (B.LORA_SEG_GROUP, B.LORA_SEG_CONTIGUOUS):
+        y, err, _ = run_apply(batch, pool, mode, len(ranks))
+        ref, _ = oracle.lora_apply(batch.x, batch.y0, ids, pool)
+        assert err == 0
+        compare_bf16(y[:, :4096], ref, "interleaved tiles mode %d" % mode)
+
+
+def test_tc_expand_caller_h_odd_stride():
+    pool, batch = long_segment_batch(29, [5, 13, 64], [130, 256, 140], 1024, 2048)
+    rng = np.random.default_rng(30)
+    hin = rng.standard_normal((batch.T, 68), dtype=np.float32)
+    view = B.PoolView.from_host(pool)
+    y = to_dev_bits(batch.y0)
+    seg = B.Segments(batch.T)
+    err = new_err()
+    B.lora_segments_build(ids_dev(batch.ids), 3, seg, err=err)
+    B.lora_sgmv_expand(torch.from_numpy(hin).cuda(), y, seg, view, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref, _ = oracle.expand(hin, batch.y0, batch.ids, pool)
+    compare_bf16(to_host_bits(y)[:, :2048], ref, "tensor-core expand, h stride 68")
+
+
+def test_tc_single_full_tile():
+    """T = 128, one adapter: the tile is the whole of x and y."""
+    pool, batch = long_segment_batch(31, [64], [128], 4096, 4096)
+    for mode in (B.LORA_SEG_GROUP, B.LORA_SEG_CONTIGUOUS):
+        y, err, _ = run_apply(batch, pool, mode, 1)
+        ref, _ = oracle.lora_apply(batch.x, batch.y0, batch.ids, pool)
+        assert err == 0
+        compare_bf16(y[:, :4096], ref, "single tile mode %d" % mode)
