@@ -114,11 +114,13 @@ typedef struct {
  * token_perm lists the segments' tokens in segment order; segment s covers
  * token_perm[seg_indptr[s] .. seg_indptr[s+1]) and uses adapter seg_adapter[s].
  * meta[0] = number of segments, meta[1] = tokens placed, meta[2] = short work
- * units, meta[3] = long work units.  short_units lists the segments of at most
+ * units, meta[3] = long work units, meta[5] and meta[6] = work counters of the
+ * tensor-core kernels (zeroed by lora_segments_build, left at zero by every call).  short_units lists the segments of at most
  * LORA_SHORT_MAX_TOKENS tokens; long_units lists (segment, offset) pairs, one
  * per LORA_TILE_M-token tile of every longer segment, both in segment order.
- * scratch belongs to lora_segments_build; h_scratch, k_partials and tickets
- * to the compute calls.
+ * scratch belongs to lora_segments_build; h_scratch, k_partials and the work
+ * counters to the compute calls, so calls that share a segment buffer
+ * must be ordered on one stream.
  */
 typedef struct {
   int32_t T;              /* tokens the buffer was carved for */
@@ -134,8 +136,6 @@ typedef struct {
                              tokens on the tensor-core path, by segment position */
   float* k_partials;      /* [LORA_KSPLIT_MAX * T * LORA_MAX_RANK]: partial shrink sums of
                              the tensor-core path, one slab per slice of d_in */
-  int32_t* tickets;       /* [max_long_units]: per-tile completion counters (zeroed by
-                             lora_segments_build, left at zero by every call) */
 } lora_segments_t;
 
 /** Slices of d_in the tensor-core shrink splits a tile into, at most. */

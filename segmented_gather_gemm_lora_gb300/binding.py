@@ -68,7 +68,7 @@ class lora_segments_t(ctypes.Structure):
                 ("seg_adapter", ctypes.c_void_p), ("meta", ctypes.c_void_p),
                 ("short_units", ctypes.c_void_p), ("long_units", ctypes.c_void_p),
                 ("scratch", ctypes.c_void_p), ("h_scratch", ctypes.c_void_p),
-                ("k_partials", ctypes.c_void_p), ("tickets", ctypes.c_void_p)]
+                ("k_partials", ctypes.c_void_p)]
 
 
 class LoraError(RuntimeError):

@@ -43,7 +43,7 @@ lora_status_t check_seg(const lora_segments_t* s) {
   if (s->T < 0) return LORA_ERR_INVALID_ARG;
   if (s->T == 0) return LORA_OK;
   if (!s->token_perm || !s->seg_indptr || !s->seg_adapter || !s->meta || !s->short_units ||
-      !s->long_units || !s->scratch || !s->h_scratch || !s->k_partials || !s->tickets)
+      !s->long_units || !s->scratch || !s->h_scratch || !s->k_partials)
     return LORA_ERR_INVALID_ARG;
   const long long need = (long long)s->T / LORA_TILE_M + (long long)s->T / (LORA_SHORT_MAX_TOKENS + 1) + 1;
   if (s->max_long_units < need) return LORA_ERR_WORKSPACE;
@@ -172,13 +172,13 @@ int64_t lora_pool_pages_needed(int32_t rank, int32_t d_in, int32_t d_out, int32_
 
 static size_t seg_layout(int32_t T, size_t* off) {
   // token_perm, seg_indptr, seg_adapter, meta, short_units, long_units, scratch, h_scratch,
-  // k_partials, tickets
+  // k_partials
   const size_t t = (size_t)(T > 0 ? T : 0);
   const size_t n_long = t / LORA_TILE_M + t / (LORA_SHORT_MAX_TOKENS + 1) + 1;
-  const size_t sizes[10] = {t, t + 1, t, 8, t, 2 * n_long, 4 * t + 8, t * LORA_MAX_RANK,
-                            (size_t)LORA_KSPLIT_MAX * t * LORA_MAX_RANK, n_long};
+  const size_t sizes[9] = {t, t + 1, t, 8, t, 2 * n_long, 4 * t + 8, t * LORA_MAX_RANK,
+                           (size_t)LORA_KSPLIT_MAX * t * LORA_MAX_RANK};
   size_t cur = 0;
-  for (int i = 0; i < 10; ++i) {
+  for (int i = 0; i < 9; ++i) {
     if (off) off[i] = cur;
     cur = align_up(cur + sizes[i] * sizeof(int32_t), 16);
   }
@@ -194,7 +194,7 @@ lora_status_t lora_segments_carve(void* buf, size_t bytes, int32_t T, lora_segme
   if (out == nullptr || T < 0) return LORA_ERR_INVALID_ARG;
   std::memset(out, 0, sizeof(*out));
   if (buf == nullptr || !aligned16(buf)) return LORA_ERR_INVALID_ARG;
-  size_t off[10];
+  size_t off[9];
   const size_t need = seg_layout(T, off);
   if (bytes < need) return LORA_ERR_WORKSPACE;
   char* b = static_cast<char*>(buf);
@@ -209,7 +209,6 @@ lora_status_t lora_segments_carve(void* buf, size_t bytes, int32_t T, lora_segme
   out->scratch = reinterpret_cast<int32_t*>(b + off[6]);
   out->h_scratch = reinterpret_cast<float*>(b + off[7]);
   out->k_partials = reinterpret_cast<float*>(b + off[8]);
-  out->tickets = reinterpret_cast<int32_t*>(b + off[9]);
   return LORA_OK;
 }
 

@@ -81,7 +81,6 @@ struct SegKernelArgs {
   int32_t* short_units;
   int32_t* long_units;
   int32_t* scratch;  // global run arrays when they do not fit in shared memory
-  int32_t* tickets;  // per-tile counters of the tensor-core shrink, zeroed here
   int32_t* err;
 };
 
@@ -254,7 +253,6 @@ __global__ void __launch_bounds__(kSegMaxThreads, 1) segments_kernel(const __gri
     rbase += tot.x;
   }
 
-  for (int i = tid; i < n_long; i += nthr) a.tickets[i] = 0;
   if (tid == 0) {
     a.meta[0] = n_segs;
     a.meta[1] = n_tok;
@@ -296,7 +294,6 @@ lora_status_t launch_segments(const int32_t* ids, int T, int n_adapters, int mod
   a.short_units = seg->short_units;
   a.long_units = seg->long_units;
   a.scratch = seg->scratch;
-  a.tickets = seg->tickets;
   a.err = err;
   return launch_pdl((const void*)segments_kernel, dim3(1), dim3(nthr), dyn, stream, 0, &a) == cudaSuccess
              ? LORA_OK

@@ -18,24 +18,22 @@
 // accumulators let one unit's epilogue overlap the next unit's loads and MMAs.
 //
 //  shrink_tc  H[128, r] = X[128, d_in] . A_i^T.  A unit is (tile, slice of
-//             d_in).  64-column chunks of x and of A_i stream through two
-//             3-stage rings in 128-byte-swizzle K-major form into tcgen05.mma
-//             M = 128, N = r padded to 16.  x arrives as one TMA tensor copy
-//             per chunk when the tile is 128 consecutive tokens, as 16-byte
-//             asynchronous copies of the listed rows otherwise; A_i page by
-//             page.  With one slice per tile the epilogue writes h directly;
-//             otherwise each unit writes an fp32 partial and the unit that
-//             finishes its tile last (a per-tile ticket) sums the partials in
-//             slice order, so the result does not depend on timing.
+//             about 512 columns of d_in).  64-column chunks of x and of A_i
+//             stream through a 6-stage ring in 128-byte-swizzle K-major form
+//             into tcgen05.mma M = 128, N = r padded to 16.  With one slice per
+//             tile the epilogue writes h; otherwise each unit writes an fp32
+//             partial and reduce_partials sums a tile's partials in slice order,
+//             so the result does not depend on timing.
 //  expand_tc  Y[128, n0:n0+128] = bf16(Y0 + (s_i H) . B_i[:, n0:n0+128]).
 //             A unit is (tile, 128-column chunk), so the expand, which carries
 //             two thirds of the bytes, spreads over every SM.  s_i H is split
 //             into bf16 hi + lo parts (two MMAs accumulating into the same fp32
 //             columns), keeping the rank-r intermediate at about fp32
 //             accuracy.  B_i rows are MN-major operands (r_i rows of d_out
-//             contiguous elements, as stored).  y0 arrives and y leaves by TMA
-//             tensor copies for tiles of 128 consecutive tokens, by 16-byte
-//             pieces otherwise.
+//             contiguous elements, as stored).  y0's first 64 columns arrive
+//             by a TMA tensor copy for tiles of 128 consecutive tokens, the
+//             rest by 16-byte asynchronous copies; y leaves by coalesced
+//             16-byte stores.
 //
 // Tokens of one segment are listed in increasing order (the segment builder's
 // order is stable), so a tile whose first and last tokens are 127 apart is the
@@ -48,19 +46,6 @@
 namespace lora {
 
 constexpr int kTM = LORA_TILE_M;  // 128
-
-__device__ __forceinline__ void named_sync_epi() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// Barrier of the four epilogue warps that also ANDs `v` over their threads.
-__device__ __forceinline__ bool named_and_epi(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v)
-      : "memory");
-  return r != 0;
-}
 
 // One long tile: rows p0 .. p0 + cnt - 1 of the segment order, all on adapter ad.
 struct TileInfo {
@@ -118,33 +103,50 @@ __device__ __forceinline__ void drain_ring(uint64_t* ring, uint32_t issued, uint
 }
 
 // ---------------------------------------------------------------- shrink_tc --
+//
+// Warp roles: 0-1 schedule (each claims units from a counter in the segment
+// buffer and resolves tile, adapter and pages), 2-5 load, 6 issues MMAs, 7-10
+// epilogue.  Units pass from the schedulers to the loaders through a 4-slot
+// queue in shared memory (scheduler s fills slots s and s + 2), chunks from the
+// loaders to the MMA warp through a 6-stage ring whose stages carry a record
+// of their chunk, and finished units from the MMA warp to the epilogue with
+// their accumulator.  Only the schedulers read the segment and adapter tables.
+//
+// A TMA tensor copy moves 128-byte box rows at a fixed rate per SM, so of a
+// full tile's 128 x rows per chunk the first 64 come by TMA and the rest, with
+// the adapter rows, by the four loader warps' 16-byte asynchronous copies; the
+// two engines run side by side.
 
-constexpr int kSThreads = 224;  // warps 0-1 load (alternate units), warp 2 MMA, warps 3-6 epilogue
-constexpr int kSRings = 2;      // one stage ring per loader warp
-constexpr int kSStages = 3;     // stages per ring
+constexpr int kSThreads = 352;
+constexpr int kSSched = 2, kSLoad = 4;
+constexpr int kSWarpLoad0 = 2, kSWarpMma = 6;  // epilogue: warps 7-10
+constexpr int kSStages = 6;
 constexpr int kSXBytes = kTM * 128;  // x tile: 128 rows x 64 bf16
 constexpr int kSABytes = 64 * 128;   // A tile: up to 64 rank rows x 64 bf16
 constexpr int kSStageBytes = kSXBytes + kSABytes;
+constexpr int kSTmaRows = 64;    // x rows of a full tile that come by TMA
 constexpr int kSMaxChunks = 32;  // 64-column chunks per unit
-constexpr int kRecSkip = 1, kRecEnd = 2;
+constexpr int kRecEnd = 1, kRecTma = 2, kRecNewTile = 4;
 
-// What a loader tells the MMA warp about the chunk in a stage.
-struct SRec {
+struct SUnit {  // scheduler -> loaders
+  int tile, q, r, rpad, nch, kbeg, p0, cnt, row0, flags;
+};
+struct SRec {  // loaders -> MMA warp, one per stage
   int tile, q, r, rpad, c, nch, p0, cnt, flags;
 };
-// What the MMA warp tells the epilogue about the unit in an accumulator.
-struct ARec {
+struct ARec {  // MMA warp -> epilogue, one per accumulator
   int tile, q, r, rpad, p0, cnt, flags;
 };
 
-constexpr size_t kSOffPg = (size_t)kSRings * kSStages * kSStageBytes;
-constexpr size_t kSOffRec = kSOffPg + (size_t)kSRings * 64 * kSMaxChunks * 4;
-constexpr size_t kSOffARec = kSOffRec + (size_t)kSRings * kSStages * 64;
+constexpr int kSSlotBytes = 64 + kTM * 4 + 64 * kSMaxChunks * 4;  // record, x rows, A pages
+constexpr size_t kSOffQ = (size_t)kSStages * kSStageBytes;
+constexpr size_t kSOffRec = kSOffQ + 4 * (size_t)kSSlotBytes;
+constexpr size_t kSOffARec = kSOffRec + (size_t)kSStages * 64;
 constexpr size_t kSOffBars = kSOffARec + 2 * 64;
 constexpr size_t kShrinkSmem = kSOffBars + 64 * 8 + 1024;  // + alignment slack
 
 struct ShrinkArgs {
-  CUtensorMap xmap;  // x as [T rows, d_in columns], 128 x 64 boxes, 128-byte swizzle
+  CUtensorMap xmap;  // x as [T rows, d_in columns], 64 x 64 boxes, 128-byte swizzle
   const uint16_t* x;
   long long ldx;
   float* h;
@@ -152,7 +154,7 @@ struct ShrinkArgs {
   int h_by_token;  // h rows by token (caller's h) or by segment position (scratch)
   int use_tma;
   float* part;  // [ksplit][T][LORA_MAX_RANK] partial sums by segment position
-  int32_t* tickets;
+  int32_t* counter;  // work counter (zero between calls)
   DevView v;
   const int32_t* perm;
   const int32_t* indptr;
@@ -165,37 +167,37 @@ struct ShrinkArgs {
   int klen;    // columns per slice (a multiple of 64)
 };
 
-// Units of this CTA are w_k = blockIdx.x + k * gridDim.x, k = 0, 1, ...  Loader
-// warp k % 2 stages unit k into ring k % 2, so one loader resolves its next
-// unit's tile, adapter and pages while the other's unit streams.  Only the
-// loaders read the segment and adapter tables: every stage carries a record of
-// its chunk, and the MMA warp takes the rings in unit order (a unit's last chunk,
-// or a skipped unit, hands over to the other ring) and passes each unit's
-// record on to the epilogue with its accumulator.
+__device__ __forceinline__ void named_sync_load() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
 __global__ void __launch_bounds__(kSThreads, 1) shrink_tc_kernel(const __grid_constant__ ShrinkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  // stage records [ring * stages + stage] and accumulator records [2], 64-byte slots
-  auto srec_at = [&](int s) { return reinterpret_cast<SRec*>(sm + kSOffRec + (size_t)s * 64); };
-  auto arec_at = [&](int b) { return reinterpret_cast<ARec*>(sm + kSOffARec + (size_t)b * 64); };
+  auto slot_at = [&](int q) { return sm + kSOffQ + (size_t)q * kSSlotBytes; };
+  auto srec_at = [&](uint32_t s) { return reinterpret_cast<SRec*>(sm + kSOffRec + (size_t)s * 64); };
+  auto arec_at = [&](uint32_t b) { return reinterpret_cast<ARec*>(sm + kSOffARec + (size_t)b * 64); };
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSOffBars);
-  uint64_t* full_tma = bars;                           // [ring][stage] 1 arrival (+ TMA bytes)
-  uint64_t* full_cp = bars + kSRings * kSStages;       // [ring][stage] 32 loader lanes' copies landed
-  uint64_t* empty = bars + 2 * kSRings * kSStages;     // [ring][stage] MMA done with the stage
-  uint64_t* acc_full = bars + 3 * kSRings * kSStages;  // [2] MMAs of the unit done
-  uint64_t* acc_empty = acc_full + 2;                  // [2] 4 epilogue warps done
-  uint64_t* rec_full = acc_empty + 2;                  // [2] unit record written
+  uint64_t* full_tma = bars;                // [stages] lead loader (+ TMA bytes)
+  uint64_t* full_cp = bars + kSStages;      // [stages] 128 loader threads' copies landed
+  uint64_t* empty = bars + 2 * kSStages;    // [stages] MMA done with the stage
+  uint64_t* uq_full = bars + 3 * kSStages;  // [4] 32 scheduler lanes
+  uint64_t* uq_empty = uq_full + 4;         // [4] 4 loader warps
+  uint64_t* acc_full = uq_empty + 4;        // [2] MMAs of the unit done
+  uint64_t* acc_empty = acc_full + 2;       // [2] 4 epilogue warps done
+  uint64_t* rec_full = acc_empty + 2;       // [2] unit record written
   uint64_t* mma_done = rec_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
-  int* flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const DevView& v = a.v;
   if (tid == 0) {
-    for (int s = 0; s < kSRings * kSStages; ++s) {
+    for (int s = 0; s < kSStages; ++s) {
       mbar_init(smem_u32(&full_tma[s]), 1);
-      mbar_init(smem_u32(&full_cp[s]), 32);
+      mbar_init(smem_u32(&full_cp[s]), 32 * kSLoad);
       mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(smem_u32(&uq_full[q]), 32);
+      mbar_init(smem_u32(&uq_empty[q]), kSLoad);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&acc_full[b]), 1);
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(kSThreads, 1) shrink_tc_kernel(const __grid_co
     mbar_init(smem_u32(mma_done), 1);
     fence_mbar_init();
   }
-  if (warp == 2) tmem_alloc(smem_u32(tmem_slot), 128);
+  if (warp == kSWarpMma) tmem_alloc(smem_u32(tmem_slot), 128);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -215,131 +217,199 @@ __global__ void __launch_bounds__(kSThreads, 1) shrink_tc_kernel(const __grid_co
   const int ks = a.ksplit;
   bool ok = true;
 
-  if (warp < kSRings) {
-    // ---------------- loaders ----------------
-    const int ring = warp;
+  if (warp < kSSched) {
+    // ---------------- schedulers ----------------
+    const int sid = warp;
     const int n_work = a.meta[3] * ks;
     const int shift = v.page_shift;
+    // Claims: unit sid * grid + block first, then units 2 * grid + counter.  Every
+    // scheduler over-claims the counter exactly once; the last claim of all
+    // puts it back to zero for the next call.
+    const int g2 = kSSched * (int)gridDim.x;
+    const int n_dyn = max(0, n_work - g2);
+    int u = sid * (int)gridDim.x + (int)blockIdx.x;
+    int claim = 0;  // the counter's answer in flight (lane 0)
+    if (lane == 0) claim = atomicAdd(a.counter, 1);
+    auto advance = [&]() {
+      const int c = __shfl_sync(0xffffffffu, claim, 0);
+      if (c < n_dyn) {
+        u = g2 + c;
+        if (lane == 0) claim = atomicAdd(a.counter, 1);
+      } else {
+        u = n_work;
+      }
+    };
+    for (uint32_t k = 0;;) {
+      const bool end = u >= n_work;
+      if (end && lane == 0 && claim == n_dyn + g2 - 1) *a.counter = 0;
+      TileInfo ti{};
+      lora_adapter_desc_t d{};
+      int tile = 0, q = 0;
+      if (!end) {
+        tile = u / ks;
+        q = u - tile * ks;
+        ti = load_tile(a.long_units, a.seg_adapter, a.indptr, a.perm, tile, a.use_tma);
+        d = v.adapters[ti.ad];
+        const int bad = check_adapter_warp(v, d, lane);
+        if (bad) {
+          if (lane == 0 && q == 0) report(a.err, bad);
+          advance();
+          continue;
+        }
+      }
+      const int qs = sid + 2 * (k & 1);
+      if (k >= 2 && !mbar_wait(smem_u32(&uq_empty[qs]), ((k >> 1) - 1) & 1)) ok = false;
+      uint8_t* slot = slot_at(qs);
+      SUnit* su = reinterpret_cast<SUnit*>(slot);
+      if (end) {
+        if (lane == 0) su->flags = kRecEnd;
+      } else {
+        const int r = d.rank;
+        const int kbeg = q * a.klen, nch = (min(v.d_in, kbeg + a.klen) - kbeg) / 64;
+        if (lane == 0) {
+          su->tile = tile;
+          su->q = q;
+          su->r = r;
+          su->rpad = (r + 15) & ~15;
+          su->nch = nch;
+          su->kbeg = kbeg;
+          su->p0 = ti.p0;
+          su->cnt = ti.cnt;
+          su->row0 = ti.row0;
+          su->flags = ti.tma ? kRecTma : 0;
+        }
+        int* rows = reinterpret_cast<int*>(slot + 64);  // x row of each tile row, -1 past the tile
+        for (int m = lane; m < kTM; m += 32)
+          rows[m] = m >= ti.cnt ? -1 : ti.tma ? ti.row0 + m : a.perm[ti.p0 + m];
+        int* pg = reinterpret_cast<int*>(slot + 64 + kTM * 4);  // [64][kSMaxChunks]
+        for (int i = lane; i < r * nch; i += 32) {
+          const int jr = i / nch, c = i - jr * nch;
+          const long long e = (long long)jr * v.d_in + kbeg + 64 * c;
+          pg[jr * kSMaxChunks + c] = v.page_list[d.a_page0 + (e >> shift)];
+        }
+      }
+      mbar_arrive(smem_u32(&uq_full[qs]));  // each lane after its own writes
+      ++k;
+      if (end) break;
+      advance();
+    }
+    if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
+  } else if (warp < kSWarpMma) {
+    // ---------------- loaders ----------------
+    const int lw = warp - kSWarpLoad0;  // 0 leads: records, stage barrier, TMA
+    const bool lead = lw == 0 && lane == 0;
+    const int shift = v.page_shift;
     const long long pmask = (1LL << shift) - 1;
-    uint8_t* rsm = sm + (size_t)ring * kSStages * kSStageBytes;
-    int* pgtab = reinterpret_cast<int*>(sm + kSOffPg) + ring * 64 * kSMaxChunks;  // [64][kSMaxChunks]
-    uint64_t* rf_tma = full_tma + ring * kSStages;
-    uint64_t* rf_cp = full_cp + ring * kSStages;
-    uint64_t* rempty = empty + ring * kSStages;
-    if (lane == 0 && a.use_tma) prefetch_tensormap(&a.xmap);
-    uint32_t g = 0;
-    // next free stage of this ring (waits for the MMA warp to release it)
+    if (lead && a.use_tma) prefetch_tensormap(&a.xmap);
+    uint32_t g = 0, n0 = 0, n1 = 0;  // stages used; units read from each scheduler
+    bool done0 = false, done1 = false;
     auto take_stage = [&]() -> uint32_t {
       const uint32_t st = g % kSStages;
-      if (g >= kSStages && !mbar_wait(smem_u32(&rempty[st]), ((g / kSStages) - 1) & 1)) ok = false;
+      if (g >= kSStages && !mbar_wait(smem_u32(&empty[st]), ((g / kSStages) - 1) & 1)) ok = false;
       return st;
     };
-    // a record with no data: every lane and the record's writer arrive by hand
-    auto post_flag = [&](int flags) {
-      const uint32_t st = take_stage();
-      if (lane == 0) {
-        srec_at(ring * kSStages + st)->flags = flags;
-        mbar_arrive(smem_u32(&rf_tma[st]));
-      }
-      mbar_arrive(smem_u32(&rf_cp[st]));
-      ++g;
-    };
-    for (int w = blockIdx.x + ring * gridDim.x; w < n_work && ok; w += kSRings * gridDim.x) {
-      const int tile = w / ks, q = w - tile * ks;
-      const TileInfo ti = load_tile(a.long_units, a.seg_adapter, a.indptr, a.perm, tile, a.use_tma);
-      const lora_adapter_desc_t d = v.adapters[ti.ad];
-      const int bad = check_adapter_warp(v, d, lane);
-      if (bad) {
-        if (lane == 0 && q == 0) report(a.err, bad);
-        post_flag(kRecSkip);
+    for (int s = 0; !(done0 && done1); s ^= 1) {
+      if (s ? done1 : done0) continue;
+      const uint32_t ns = s ? n1 : n0;
+      const int qs = s + 2 * (ns & 1);
+      if (!mbar_wait(smem_u32(&uq_full[qs]), (ns >> 1) & 1)) ok = false;
+      if (s) ++n1; else ++n0;
+      const uint8_t* slot = slot_at(qs);
+      const SUnit su = *reinterpret_cast<const SUnit*>(slot);
+      if (su.flags & kRecEnd) {
+        if (s) done1 = true; else done0 = true;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&uq_empty[qs]));
         continue;
       }
-      const int r = d.rank, rpad = (r + 15) & ~15;
-      const int kbeg = q * a.klen, nch = (min(v.d_in, kbeg + a.klen) - kbeg) / 64;
-      int toks[4];
+      const bool tma = su.flags & kRecTma;
+      const int* rows = reinterpret_cast<const int*>(slot + 64);
+      const int* pg = reinterpret_cast<const int*>(slot + 64 + kTM * 4);
+      // x rows of this thread: m = base + (lane >> 3) + 4 t, 16-byte piece lane & 7
+      const int p = lane & 7;
+      const int xbase = tma ? kSTmaRows + 16 * lw : 32 * lw;
+      const int xcnt = tma ? 4 : 8;
+      const uint16_t* xsrc[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int m = lane + 32 * i;
-        toks[i] = (!ti.tma && m < ti.cnt) ? a.perm[ti.p0 + m] : -1;
+      for (int t = 0; t < 8; ++t) {
+        const int rw = t < xcnt ? rows[xbase + (lane >> 3) + 4 * t] : -1;
+        xsrc[t] = rw < 0 ? nullptr : a.x + (long long)rw * a.ldx + su.kbeg + 8 * p;
       }
-      __syncwarp();
-      for (int i = lane; i < r * nch; i += 32) {
-        const int j = i / nch, c = i - j * nch;
-        const long long e = (long long)j * v.d_in + kbeg + 64 * c;
-        pgtab[j * kSMaxChunks + c] = v.page_list[d.a_page0 + (e >> shift)];
-      }
-      __syncwarp();
-      for (int c = 0; c < nch; ++c, ++g) {
+      for (int c = 0; c < su.nch; ++c, ++g) {
         const uint32_t st = take_stage();
-        const uint32_t xs = smem_u32(rsm + st * kSStageBytes);
+        const uint32_t xs = smem_u32(sm + st * kSStageBytes);
         const uint32_t as = xs + kSXBytes;
-        const int kcol = kbeg + 64 * c;
-        if (lane == 0) {
-          SRec* rc = srec_at(ring * kSStages + st);
-          rc->tile = tile;
-          rc->q = q;
-          rc->r = r;
-          rc->rpad = rpad;
+        const int kcol = su.kbeg + 64 * c;
+        if (lead) {
+          SRec* rc = srec_at(st);
+          rc->tile = su.tile;
+          rc->q = su.q;
+          rc->r = su.r;
+          rc->rpad = su.rpad;
           rc->c = c;
-          rc->nch = nch;
-          rc->p0 = ti.p0;
-          rc->cnt = ti.cnt;
+          rc->nch = su.nch;
+          rc->p0 = su.p0;
+          rc->cnt = su.cnt;
           rc->flags = 0;
-        }
-        if (ti.tma) {
-          if (lane == 0) {
-            mbar_arrive_expect_tx(smem_u32(&rf_tma[st]), kSXBytes);
-            tma_load_2d(xs, &a.xmap, kcol, ti.row0, smem_u32(&rf_tma[st]));
-          }
-        } else {
-          if (lane == 0) mbar_arrive(smem_u32(&rf_tma[st]));
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int m = lane + 32 * i;
-            const uint16_t* src = a.x + (long long)(toks[i] < 0 ? 0 : toks[i]) * a.ldx + kcol;
-#pragma unroll
-            for (int p = 0; p < 8; ++p) cp_async16(xs + sw128_offset(m, p), src + 8 * p, toks[i] >= 0);
+          if (tma) {
+            mbar_arrive_expect_tx(smem_u32(&full_tma[st]), kSTmaRows * 128);
+            tma_load_2d(xs, &a.xmap, kcol, su.row0, smem_u32(&full_tma[st]));
+          } else {
+            mbar_arrive(smem_u32(&full_tma[st]));
           }
         }
-        for (int i = lane; i < rpad * 8; i += 32) {
-          const int j = i >> 3, p = i & 7;
-          const bool real = j < r;
-          const long long e = real ? ((long long)j * v.d_in + kcol) : 0;
-          const uint16_t* src =
-              real ? v.pool + ((long long)pgtab[j * kSMaxChunks + c] << shift) + (e & pmask) + 8 * p : v.pool;
-          cp_async16(as + sw128_offset(j, p), src, real);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          if (t < xcnt) {
+            const int m = xbase + (lane >> 3) + 4 * t;
+            cp_async16(xs + sw128_offset(m, p), xsrc[t] ? xsrc[t] + 64 * c : a.x, xsrc[t] != nullptr);
+          }
         }
-        cp_async_arrive_noinc(smem_u32(&rf_cp[st]));
+        // adapter rows j = 4 ((lane >> 3) + 4 t) + lw, piece lane & 7
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int jr = 4 * ((lane >> 3) + 4 * t) + lw;
+          if (jr < su.rpad) {
+            const bool real = jr < su.r;
+            const long long e = real ? ((long long)jr * v.d_in + kcol) : 0;
+            const uint16_t* src =
+                real ? v.pool + ((long long)pg[jr * kSMaxChunks + c] << shift) + (e & pmask) + 8 * p : v.pool;
+            cp_async16(as + sw128_offset(jr, p), src, real);
+          }
+        }
+        cp_async_arrive_noinc(smem_u32(&full_cp[st]));
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&uq_empty[qs]));
     }
-    post_flag(kRecEnd);
+    {  // the end, for the MMA warp: a record with no data on the next stage
+      const uint32_t st = take_stage();  // every loader thread, so no arrival runs ahead of the stage
+      if (lead) {
+        srec_at(st)->flags = kRecEnd;
+        mbar_arrive(smem_u32(&full_tma[st]));
+      }
+      mbar_arrive(smem_u32(&full_cp[st]));
+      ++g;
+    }
     // nothing may still be landing in shared memory when the CTA ends
     cp_async_wait<0>();
-    if (lane == 0) {
-      drain_ring(rf_tma, g, kSStages);
-      drain_ring(rf_cp, g, kSStages);
-      if (!ok) report(a.err, LORA_DERR_TIMEOUT);
+    if (lead) {
+      drain_ring(full_tma, g, kSStages);
+      drain_ring(full_cp, g, kSStages);
     }
-  } else if (warp == 2) {
+    if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
+  } else if (warp == kSWarpMma) {
     // ---------------- MMA issue ----------------
     if (lane == 0) {
-      uint32_t g0 = 0, g1 = 0, nunit = 0;  // stages taken per ring, units started
-      int ring = 0;
-      for (;;) {
-        const uint32_t g = ring ? g1 : g0, st = g % kSStages, ph = (g / kSStages) & 1;
-        const int s = ring * kSStages + st;
-        if (!mbar_wait(smem_u32(&full_tma[s]), ph) || !mbar_wait(smem_u32(&full_cp[s]), ph)) {
+      uint32_t nunit = 0;
+      for (uint32_t g = 0;; ++g) {
+        const uint32_t st = g % kSStages, ph = (g / kSStages) & 1;
+        if (!mbar_wait(smem_u32(&full_tma[st]), ph) || !mbar_wait(smem_u32(&full_cp[st]), ph)) {
           ok = false;
           break;
         }
-        if (ring) ++g1; else ++g0;
-        const SRec rc = *srec_at(s);
+        const SRec rc = *srec_at(st);
         if (rc.flags & kRecEnd) break;
-        if (rc.flags & kRecSkip) {
-          mbar_arrive(smem_u32(&empty[s]));
-          ring ^= 1;
-          continue;
-        }
         const uint32_t b = nunit & 1, k = nunit >> 1;
         if (rc.c == 0) {
           if (k >= 1 && !mbar_wait(smem_u32(&acc_empty[b]), (k - 1) & 1)) ok = false;
@@ -355,18 +425,17 @@ __global__ void __launch_bounds__(kSThreads, 1) shrink_tc_kernel(const __grid_co
         }
         fence_proxy_async_smem();  // asynchronous-copy writes, seen here, before the tensor cores read them
         tc_fence_after();
-        const uint32_t xs = smem_u32(sm + (size_t)s * kSStageBytes);
+        const uint32_t xs = smem_u32(sm + st * kSStageBytes);
         const uint32_t as = xs + kSXBytes;
         const uint32_t idesc = idesc_bf16(kTM, rc.rpad, 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_bf16(tmem + b * 64, sdesc_sw128(xs + 32 * kk, 16, 1024), sdesc_sw128(as + 32 * kk, 16, 1024), idesc,
                    (rc.c | kk) != 0);
-        mma_commit(smem_u32(&empty[s]));
+        mma_commit(smem_u32(&empty[st]));
         if (rc.c == rc.nch - 1) {
           mma_commit(smem_u32(&acc_full[b]));
           ++nunit;
-          ring ^= 1;
         }
       }
       // the end, passed on through the next accumulator record
@@ -382,15 +451,12 @@ __global__ void __launch_bounds__(kSThreads, 1) shrink_tc_kernel(const __grid_co
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue: h or a partial H, then the tile's reduction ----------------
-    const int etid = tid - 96;
+    // ---------------- epilogue: h, or this slice's partial H ----------------
     const int quarter = warp & 3;  // tensor-memory lanes this warp may read
     const int m = quarter * 32 + lane;
     for (uint32_t nunit = 0;; ++nunit) {
       const uint32_t b = nunit & 1, k = nunit >> 1;
-      bool got = mbar_wait(smem_u32(&rec_full[b]), k & 1);
-      if (ks > 1) got = named_and_epi(got);  // leave together: the reduction below uses barriers
-      if (!got) {
+      if (!mbar_wait(smem_u32(&rec_full[b]), k & 1)) {
         ok = false;
         break;
       }
@@ -418,61 +484,49 @@ __global__ void __launch_bounds__(kSThreads, 1) shrink_tc_kernel(const __grid_co
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));  // accumulator and record both free
-      if (ks == 1) continue;
-      __threadfence();
-      ok = named_and_epi(ok);  // the same verdict in every epilogue thread before the next barrier
-      if (etid == 0) *flag = atomicAdd(&a.tickets[ar.tile], 1) == ks - 1 ? 1 : 0;
-      named_sync_epi();
-      if (*flag) {  // the tile's last slice to finish: sum the partials in slice order
-        __threadfence();
-        if (mine) {
-          float* hrow = a.h + (long long)(a.h_by_token ? a.perm[ar.p0 + m] : ar.p0 + m) * a.ldh;
-          for (int j = 0; j < r; j += 4) {
-            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int qq = 0; qq < ks; ++qq) {
-              const float4 p4 = __ldcg(
-                  reinterpret_cast<const float4*>(a.part + ((long long)qq * a.T + ar.p0 + m) * LORA_MAX_RANK + j));
-              s4.x += p4.x;
-              s4.y += p4.y;
-              s4.z += p4.z;
-              s4.w += p4.w;
-            }
-            store_h4(hrow, j, r, s4.x, s4.y, s4.z, s4.w);
-          }
-        }
-        if (etid == 0) a.tickets[ar.tile] = 0;  // ready for the next call on these segments
-      }
     }
     if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) tmem_dealloc(tmem, 128);
+  if (warp == kSWarpMma) tmem_dealloc(tmem, 128);
 }
 
 // ---------------------------------------------------------------- expand_tc --
+//
+// Warp roles: 0 schedules (claims groups of kEGroup consecutive units, resolves
+// tile, adapter and B pages, and builds each new tile's H operand, s_i h as
+// bf16 hi + lo, into one of two buffers), 1-4 load, 5 issues MMAs, 6-13
+// epilogue.  Units pass from the scheduler to the loaders through a 4-slot
+// queue; the loaders' 3-stage ring carries a record of each unit to the MMA
+// warp and the epilogue.  A unit's first 64 y0 columns come by one TMA tensor
+// copy when the tile is 128 consecutive tokens, the rest by the loader warps'
+// 16-byte asynchronous copies.
 
-constexpr int kEThreads = 320;  // warp 0 loads, warp 1 MMA, warps 2-9 epilogue
-constexpr int kEEpiWarps = 8;   // (tensor-memory lane quarter, 64-column half) each
-constexpr int kENC = 128;       // output columns per unit
-constexpr int kEStages = 4;
+constexpr int kEThreads = 448;
+constexpr int kELoad = 4;
+constexpr int kEWarpLoad0 = 1, kEWarpMma = 5, kEWarpEpi0 = 6;
+constexpr int kEEpiWarps = 8;  // (tensor-memory lane quarter, 64-column half) each
+constexpr int kENC = 128;      // output columns per unit
+constexpr int kEGroup = 4;     // units per claim
+constexpr int kEStages = 3;
+constexpr int kEQ = 4;                    // unit queue slots
 constexpr int kEYBytes = kTM * kENC * 2;  // y0 / y tile: 2 atoms of 128 rows x 64 columns
 constexpr int kEAtom = kTM * 128;         // one 128 x 64 bf16 atom column
 constexpr int kEBBytes = 64 * kENC * 2;   // B tile: up to 64 rank rows x 128 columns
 constexpr int kEStageBytes = kEYBytes + kEBBytes;
-constexpr int kRecTma = 4, kRecNewTile = 8;
+constexpr int kEHBytes = 2 * kTM * 128;  // one H operand: hi then lo
 
-// What the loader tells the MMA warp and the epilogue about the unit in a stage.
-struct ERec {
-  int tile, n0, r, rpad, p0, cnt, row0, flags;
-  float scale;
+struct EUnit {  // scheduler -> loaders -> MMA warp and epilogue
+  int tile, n0, r, rpad, p0, cnt, row0, flags, hbuf;
 };
-
-constexpr size_t kEOffH = (size_t)kEStages * kEStageBytes;  // H hi, then lo: 2 x 16 KB
-constexpr size_t kEOffPg = kEOffH + 2 * kTM * 128;
-constexpr size_t kEOffRec = kEOffPg + 64 * 4;
-constexpr size_t kEOffBars = kEOffRec + (size_t)kEStages * 64;
-constexpr size_t kExpandSmem = kEOffBars + 32 * 8 + 1024;
+constexpr int kERecBytes = 64 + kTM * 4;          // record, y row of each tile row
+constexpr int kESlotBytes = kERecBytes + 64 * 4;  // record, rows, B pages
+constexpr size_t kEOffH = (size_t)kEStages * kEStageBytes;
+constexpr size_t kEOffQ = kEOffH + 2 * (size_t)kEHBytes;
+constexpr size_t kEOffRec = kEOffQ + (size_t)kEQ * kESlotBytes;
+constexpr size_t kEOffBars = kEOffRec + (size_t)kEStages * kERecBytes;
+constexpr size_t kExpandSmem = kEOffBars + 64 * 8 + 1024;
 
 struct ExpandArgs {
   CUtensorMap ymap;  // y as [T rows, d_out columns], 128 x 64 boxes, 128-byte swizzle
@@ -482,6 +536,7 @@ struct ExpandArgs {
   long long ldh;
   int h_by_token;
   int use_tma;
+  int32_t* counter;  // work counter (zero between calls)
   DevView v;
   const int32_t* perm;
   const int32_t* indptr;
@@ -491,25 +546,23 @@ struct ExpandArgs {
   int32_t* err;
 };
 
-// Units of this CTA are a contiguous range of (tile, column chunk), so
-// consecutive units mostly share a tile and its H operand.  Only the loader
-// reads the segment and adapter tables; every stage carries a record of its
-// unit, and a record with the end flag closes the ring.
 __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_constant__ ExpandArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* hhi = sm + kEOffH;
-  uint8_t* hlo = hhi + kTM * 128;
-  int* pgb = reinterpret_cast<int*>(sm + kEOffPg);
-  auto erec_at = [&](uint32_t st) { return reinterpret_cast<ERec*>(sm + kEOffRec + (size_t)st * 64); };
+  auto hbuf_at = [&](int hb) { return sm + kEOffH + (size_t)hb * kEHBytes; };
+  auto slot_at = [&](uint32_t q) { return sm + kEOffQ + (size_t)q * kESlotBytes; };
+  auto rec_at = [&](uint32_t st) { return sm + kEOffRec + (size_t)st * kERecBytes; };
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kEOffBars);
-  uint64_t* full_tma = bars;                 // [stages] 1 arrival (+ TMA bytes of y0)
-  uint64_t* full_cp = bars + kEStages;       // [stages] 32 loader lanes' copies landed
-  uint64_t* empty = bars + 2 * kEStages;     // [stages] MMA commit + 8 epilogue warps
-  uint64_t* acc_full = bars + 3 * kEStages;  // [2]
-  uint64_t* acc_empty = acc_full + 2;        // [2] 8 epilogue warps
-  uint64_t* h_ready = acc_empty + 2;         // 256 epilogue threads per tile's H operand
-  uint64_t* mma_done = h_ready + 1;
+  uint64_t* full_tma = bars;                // [stages] lead loader (+ TMA bytes of y0)
+  uint64_t* full_cp = bars + kEStages;      // [stages] 128 loader threads' copies landed
+  uint64_t* empty = bars + 2 * kEStages;    // [stages] MMA commit + 8 epilogue warps
+  uint64_t* uq_full = bars + 3 * kEStages;  // [kEQ] 32 scheduler lanes
+  uint64_t* uq_empty = uq_full + kEQ;       // [kEQ] 4 loader warps
+  uint64_t* acc_full = uq_empty + kEQ;      // [2]
+  uint64_t* acc_empty = acc_full + 2;       // [2] 8 epilogue warps
+  uint64_t* h_ready = acc_empty + 2;        // [2] 32 scheduler lanes
+  uint64_t* h_free = h_ready + 2;           // [2] MMA commit when it leaves the buffer's tile
+  uint64_t* mma_done = h_free + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -517,18 +570,23 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
   if (tid == 0) {
     for (int s = 0; s < kEStages; ++s) {
       mbar_init(smem_u32(&full_tma[s]), 1);
-      mbar_init(smem_u32(&full_cp[s]), 32);
+      mbar_init(smem_u32(&full_cp[s]), 32 * kELoad);
       mbar_init(smem_u32(&empty[s]), 1 + kEEpiWarps);
+    }
+    for (int q = 0; q < kEQ; ++q) {
+      mbar_init(smem_u32(&uq_full[q]), 32);
+      mbar_init(smem_u32(&uq_empty[q]), kELoad);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&acc_full[b]), 1);
       mbar_init(smem_u32(&acc_empty[b]), kEEpiWarps);
+      mbar_init(smem_u32(&h_ready[b]), 32);
+      mbar_init(smem_u32(&h_free[b]), 1);
     }
-    mbar_init(smem_u32(h_ready), 32 * kEEpiWarps);
     mbar_init(smem_u32(mma_done), 1);
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 256);
+  if (warp == kEWarpMma) tmem_alloc(smem_u32(tmem_slot), 256);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -537,133 +595,237 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
   bool ok = true;
 
   if (warp == 0) {
-    // ---------------- loader ----------------
+    // ---------------- scheduler ----------------
     const int n_nc = v.d_out / kENC;
-    const long long n_work = (long long)a.meta[3] * n_nc;
-    const long long w0 = n_work * blockIdx.x / gridDim.x, w1 = n_work * (blockIdx.x + 1) / gridDim.x;
+    const int n_work = a.meta[3] * n_nc;
+    const int n_claims = (n_work + kEGroup - 1) / kEGroup;
+    const int shift = v.page_shift;
+    uint32_t j = 0, tcount = 0;
+    int cur = -1, bad = 0;
+    TileInfo ti{};
+    lora_adapter_desc_t d{};
+    int rows[4] = {-1, -1, -1, -1};
+    bool new_tile = false;
+    auto take_slot = [&]() -> uint8_t* {
+      const uint32_t qs = j % kEQ;
+      if (j >= kEQ && !mbar_wait(smem_u32(&uq_empty[qs]), ((j / kEQ) - 1) & 1)) ok = false;
+      return slot_at(qs);
+    };
+    // Claims: group blockIdx.x first, then groups grid + counter.  The scheduler
+    // over-claims the counter exactly once; the last claim of all puts it back
+    // to zero for the next call.
+    const int n_dyn = max(0, n_claims - (int)gridDim.x);
+    int c = blockIdx.x;
+    int claim = 0;  // the counter's answer in flight (lane 0)
+    if (lane == 0) claim = atomicAdd(a.counter, 1);
+    for (;;) {
+      if (c >= n_claims) {
+        if (lane == 0 && claim == n_dyn + (int)gridDim.x - 1) *a.counter = 0;
+        uint8_t* slot = take_slot();
+        if (lane == 0) reinterpret_cast<EUnit*>(slot)->flags = kRecEnd;
+        mbar_arrive(smem_u32(&uq_full[j % kEQ]));
+        ++j;
+        break;
+      }
+      for (int w = c * kEGroup; w < min(n_work, (c + 1) * kEGroup); ++w) {
+        const int tile = w / n_nc, n0 = (w - tile * n_nc) * kENC;
+        if (tile != cur) {
+          cur = tile;
+          ti = load_tile(a.long_units, a.seg_adapter, a.indptr, a.perm, tile, a.use_tma);
+          d = v.adapters[ti.ad];
+          bad = check_adapter_warp(v, d, lane);
+          if (bad && lane == 0 && n0 == 0) report(a.err, bad);
+          if (!bad) {
+            new_tile = true;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int m = lane + 32 * i;
+              rows[i] = m >= ti.cnt ? -1 : ti.tma ? ti.row0 + m : a.perm[ti.p0 + m];
+            }
+            // H operand of the tile: s * h in two bf16 parts, K-major, 128-byte
+            // swizzle, one atom; zero beyond r and beyond the tile's rows.
+            const int hb = tcount & 1;
+            if (tcount >= 2 && !mbar_wait(smem_u32(&h_free[hb]), ((tcount >> 1) - 1) & 1)) ok = false;
+            uint8_t* hhi = hbuf_at(hb);
+            uint8_t* hlo = hhi + kTM * 128;
+            const int r = d.rank, rpad = (r + 15) & ~15;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int m = lane + 32 * i;
+              const bool mine = m < ti.cnt;
+              const long long hr = !mine ? 0 : a.h_by_token ? (ti.tma ? (long long)(ti.row0 + m) : (long long)rows[i])
+                                                             : (long long)(ti.p0 + m);
+              const float* hrow = a.h + hr * a.ldh;
+              for (int qq = 0; qq < rpad / 8; ++qq) {
+                float hv[8];
+#pragma unroll
+                for (int e4 = 0; e4 < 2; ++e4) {
+                  const int jj = qq * 8 + 4 * e4;
+                  if (mine && jj + 3 < r) {
+                    const float4 f = *reinterpret_cast<const float4*>(hrow + jj);
+                    hv[4 * e4] = f.x;
+                    hv[4 * e4 + 1] = f.y;
+                    hv[4 * e4 + 2] = f.z;
+                    hv[4 * e4 + 3] = f.w;
+                  } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) hv[4 * e4 + e] = (mine && jj + e < r) ? hrow[jj + e] : 0.f;
+                  }
+                }
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float s0 = d.scale * hv[2 * e], s1 = d.scale * hv[2 * e + 1];
+                  hi[e] = pack_bf16x2(s0, s1);
+                  lo[e] = pack_bf16x2(s0 - bf_lo(hi[e]), s1 - bf_hi(hi[e]));
+                }
+                *reinterpret_cast<uint4*>(hhi + sw128_offset(m, qq)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(hlo + sw128_offset(m, qq)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+              }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&h_ready[hb]));
+            ++tcount;
+          }
+        }
+        if (bad) continue;
+        uint8_t* slot = take_slot();
+        if (lane == 0) {
+          EUnit* eu = reinterpret_cast<EUnit*>(slot);
+          eu->tile = tile;
+          eu->n0 = n0;
+          eu->r = d.rank;
+          eu->rpad = (d.rank + 15) & ~15;
+          eu->p0 = ti.p0;
+          eu->cnt = ti.cnt;
+          eu->row0 = ti.row0;
+          eu->flags = (ti.tma ? kRecTma : 0) | (new_tile ? kRecNewTile : 0);
+          eu->hbuf = (tcount - 1) & 1;
+        }
+        new_tile = false;
+        int* srows = reinterpret_cast<int*>(slot + 64);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) srows[lane + 32 * i] = rows[i];
+        int* pgb = reinterpret_cast<int*>(slot + kERecBytes);
+        for (int jr = lane; jr < d.rank; jr += 32)
+          pgb[jr] = v.page_list[d.b_page0 + (((long long)jr * v.d_out + n0) >> shift)];
+        mbar_arrive(smem_u32(&uq_full[j % kEQ]));  // each lane after its own writes
+        ++j;
+      }
+      const int cn = __shfl_sync(0xffffffffu, claim, 0);
+      if (cn < n_dyn) {
+        c = (int)gridDim.x + cn;
+        if (lane == 0) claim = atomicAdd(a.counter, 1);
+      } else {
+        c = n_claims;
+      }
+    }
+    if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
+  } else if (warp < kEWarpMma) {
+    // ---------------- loaders ----------------
+    const int lw = warp - kEWarpLoad0;  // 0 leads: record, stage barrier, TMA
+    const bool lead = lw == 0 && lane == 0;
+    const int ltid = tid - 32 * kEWarpLoad0;
     const int shift = v.page_shift;
     const long long pmask = (1LL << shift) - 1;
-    if (lane == 0 && a.use_tma) prefetch_tensormap(&a.ymap);
+    if (lead && a.use_tma) prefetch_tensormap(&a.ymap);
     uint32_t g = 0;
-    int cur = -1, bad = 0, r = 0, rpad = 16;
-    bool new_tile = false;
-    TileInfo ti;
-    lora_adapter_desc_t d;
-    int toks[4];
-    auto take_stage = [&]() -> uint32_t {
+    const int p = lane & 7;
+    for (uint32_t j = 0;; ++j, ++g) {
+      const uint32_t qs = j % kEQ;
+      if (!mbar_wait(smem_u32(&uq_full[qs]), (j / kEQ) & 1)) ok = false;
+      const uint8_t* slot = slot_at(qs);
+      const EUnit eu = *reinterpret_cast<const EUnit*>(slot);
       const uint32_t st = g % kEStages;
       if (g >= kEStages && !mbar_wait(smem_u32(&empty[st]), ((g / kEStages) - 1) & 1)) ok = false;
-      return st;
-    };
-    for (long long w = w0; w < w1 && ok; ++w) {
-      const int tile = (int)(w / n_nc), n0 = (int)(w - (long long)tile * n_nc) * kENC;
-      if (tile != cur) {
-        cur = tile;
-        ti = load_tile(a.long_units, a.seg_adapter, a.indptr, a.perm, tile, a.use_tma);
-        d = v.adapters[ti.ad];
-        bad = check_adapter_warp(v, d, lane);
-        if (bad && lane == 0 && n0 == 0) report(a.err, bad);
-        r = d.rank;
-        rpad = (r + 15) & ~15;
-        new_tile = true;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int m = lane + 32 * i;
-          toks[i] = (!ti.tma && m < ti.cnt) ? a.perm[ti.p0 + m] : -1;
+      uint8_t* rec = rec_at(st);
+      // the unit's record and y rows travel with the stage
+      if (lead) *reinterpret_cast<EUnit*>(rec) = eu;
+      const int* srows = reinterpret_cast<const int*>(slot + 64);
+      reinterpret_cast<int*>(rec + 64)[ltid] = srows[ltid];
+      named_sync_load();  // every loader's writes before the lead's arrival publishes them
+      const bool tma = eu.flags & kRecTma;
+      if (lead) {
+        if (tma && !(eu.flags & kRecEnd)) {
+          mbar_arrive_expect_tx(smem_u32(&full_tma[st]), kEAtom);
+          tma_load_2d(smem_u32(sm + st * kEStageBytes), &a.ymap, eu.n0, eu.row0, smem_u32(&full_tma[st]));
+        } else {
+          mbar_arrive(smem_u32(&full_tma[st]));
         }
       }
-      if (bad) continue;
-      __syncwarp();
-      for (int j = lane; j < r; j += 32) pgb[j] = v.page_list[d.b_page0 + (((long long)j * v.d_out + n0) >> shift)];
-      __syncwarp();
-      const uint32_t st = take_stage();
+      if (eu.flags & kRecEnd) {
+        mbar_arrive(smem_u32(&full_cp[st]));
+        ++g;
+        break;
+      }
       const uint32_t ys = smem_u32(sm + st * kEStageBytes);
       const uint32_t bs = ys + kEYBytes;
-      if (lane == 0) {
-        ERec* rc = erec_at(st);
-        rc->tile = tile;
-        rc->n0 = n0;
-        rc->r = r;
-        rc->rpad = rpad;
-        rc->p0 = ti.p0;
-        rc->cnt = ti.cnt;
-        rc->row0 = ti.row0;
-        rc->flags = (ti.tma ? kRecTma : 0) | (new_tile ? kRecNewTile : 0);
-        rc->scale = d.scale;
-      }
-      new_tile = false;
-      if (ti.tma) {
-        if (lane == 0) {
-          mbar_arrive_expect_tx(smem_u32(&full_tma[st]), kEYBytes);
-          tma_load_2d(ys, &a.ymap, n0, ti.row0, smem_u32(&full_tma[st]));
-          tma_load_2d(ys + kEAtom, &a.ymap, n0 + 64, ti.row0, smem_u32(&full_tma[st]));
-        }
-      } else {
-        if (lane == 0) mbar_arrive(smem_u32(&full_tma[st]));
+      // y0 rows m = 32 lw + (lane >> 3) + 4 t, piece lane & 7 of each 64-column atom
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (toks[i] < 0) continue;
-          const int m = lane + 32 * i;
-          const uint16_t* src = a.y + (long long)toks[i] * a.ldy + n0;
-#pragma unroll
-          for (int p = 0; p < 16; ++p) cp_async16(ys + (p >> 3) * kEAtom + sw128_offset(m, p & 7), src + 8 * p);
-        }
+      for (int t = 0; t < 8; ++t) {
+        const int m = 32 * lw + (lane >> 3) + 4 * t;
+        const int rw = srows[m];
+        if (rw < 0) continue;
+        const uint16_t* src = a.y + (long long)rw * a.ldy + eu.n0 + 8 * p;
+        if (!tma) cp_async16(ys + sw128_offset(m, p), src);
+        cp_async16(ys + kEAtom + sw128_offset(m, p), src + 64);
       }
-      // B rows: MN-major operand, 2 atoms of 64 columns, 8 rank rows per
-      // 1024-byte group, 128-byte swizzle; zero beyond r.
-      const int kg = rpad / 8;
-      for (int i = lane; i < rpad * 16; i += 32) {
-        const int j = i >> 4, p = i & 15;
-        const bool real = j < r;
-        const long long e = real ? ((long long)j * v.d_out + n0) : 0;
-        const uint16_t* src = real ? v.pool + ((long long)pgb[j] << shift) + (e & pmask) + 8 * p : v.pool;
-        cp_async16(bs + (uint32_t)((((p >> 3) * kg) + (j >> 3)) * 1024) + sw128_offset(j & 7, p & 7), src, real);
+      // B rows j = 4 ((lane >> 4) + 2 t) + lw: MN-major operand, 2 atoms of 64
+      // columns, 8 rank rows per 1024-byte group, 128-byte swizzle; zero beyond r
+      const int* pgb = reinterpret_cast<const int*>(slot + kERecBytes);
+      const int kg = eu.rpad / 8, p16 = lane & 15;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int jr = 4 * ((lane >> 4) + 2 * t) + lw;
+        if (jr < eu.rpad) {
+          const bool real = jr < eu.r;
+          const long long e = real ? ((long long)jr * v.d_out + eu.n0) : 0;
+          const uint16_t* src = real ? v.pool + ((long long)pgb[jr] << shift) + (e & pmask) + 8 * p16 : v.pool;
+          cp_async16(bs + (uint32_t)((((p16 >> 3) * kg) + (jr >> 3)) * 1024) + sw128_offset(jr & 7, p16 & 7), src,
+                     real);
+        }
       }
       cp_async_arrive_noinc(smem_u32(&full_cp[st]));
-      ++g;
-    }
-    {  // the end record
-      const uint32_t st = take_stage();
-      if (lane == 0) {
-        erec_at(st)->flags = kRecEnd;
-        mbar_arrive(smem_u32(&full_tma[st]));
-      }
-      mbar_arrive(smem_u32(&full_cp[st]));
-      ++g;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&uq_empty[qs]));
     }
     cp_async_wait<0>();
-    if (lane == 0) {
+    if (lead) {
       drain_ring(full_tma, g, kEStages);
       drain_ring(full_cp, g, kEStages);
-      if (!ok) report(a.err, LORA_DERR_TIMEOUT);
     }
-  } else if (warp == 1) {
+    if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
+  } else if (warp == kEWarpMma) {
     // ---------------- MMA issue ----------------
     if (lane == 0) {
-      uint32_t g = 0, uc = 0, tc = 0;
-      for (;; ++g) {
+      uint32_t uc = 0, tcount = 0;
+      int hb = 0;
+      for (uint32_t g = 0;; ++g) {
         const uint32_t st = g % kEStages, ph = (g / kEStages) & 1;
         if (!mbar_wait(smem_u32(&full_tma[st]), ph) || !mbar_wait(smem_u32(&full_cp[st]), ph)) {
           ok = false;
           break;
         }
-        const ERec rc = *erec_at(st);
+        const EUnit rc = *reinterpret_cast<const EUnit*>(rec_at(st));
         if (rc.flags & kRecEnd) break;
         const uint32_t b = uc & 1, k = uc >> 1;
         if (rc.flags & kRecNewTile) {
-          ++tc;
-          if (!mbar_wait(smem_u32(h_ready), (tc - 1) & 1)) ok = false;
+          if (tcount > 0) mma_commit(smem_u32(&h_free[hb]));  // the previous tile's H is free once its MMAs end
+          hb = rc.hbuf;
+          if (!mbar_wait(smem_u32(&h_ready[hb]), (tcount >> 1) & 1)) ok = false;
+          ++tcount;
         }
         if (k >= 1 && !mbar_wait(smem_u32(&acc_empty[b]), (k - 1) & 1)) ok = false;
         fence_proxy_async_smem();  // asynchronous-copy writes, seen here, before the tensor cores read them
         tc_fence_after();
         const uint32_t idesc = idesc_bf16(kTM, 64, 1);
         const uint32_t bs = smem_u32(sm + st * kEStageBytes) + kEYBytes;
+        const uint32_t hhi = smem_u32(hbuf_at(hb)), hlo = hhi + kTM * 128;
         const int kg = rc.rpad / 8;
         for (int na = 0; na < kENC / 64; ++na) {
           int first = 1;
           for (int part = 0; part < 2; ++part) {
-            const uint32_t abase = smem_u32(part ? hlo : hhi);
+            const uint32_t abase = part ? hlo : hhi;
             for (int kk = 0; kk < rc.rpad / 16; ++kk) {
               mma_bf16(tmem + b * 128 + (uint32_t)(na * 64), sdesc_sw128(abase + 32 * kk, 16, 1024),
                        sdesc_sw128(bs + (uint32_t)((na * kg) * 1024 + kk * 2048), 0, 1024), idesc, first ? 0u : 1u);
@@ -683,56 +845,20 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue: H operand per tile, y per unit ----------------
-    const int quarter = warp & 3;      // tensor-memory lanes this warp may read
-    const int half = (warp - 2) >> 2;  // 64-column half of the unit (one swizzle atom)
-    const int m = quarter * 32 + lane;  // tile row
-    int tok_m = -1;
+    // ---------------- epilogue: y = y0 + accumulator, per unit ----------------
+    const int quarter = warp & 3;                 // tensor-memory lanes this warp may read
+    const int half = (warp - kEWarpEpi0) >> 2;    // 64-column half of the unit (one swizzle atom)
+    const int m = quarter * 32 + lane;            // tile row
     for (uint32_t g = 0, uc = 0;; ++g, ++uc) {
       const uint32_t st = g % kEStages, ph = (g / kEStages) & 1;
       if (!mbar_wait(smem_u32(&full_tma[st]), ph) || !mbar_wait(smem_u32(&full_cp[st]), ph)) {
         ok = false;
         break;
       }
-      const ERec rc = *erec_at(st);
+      const uint8_t* rec = rec_at(st);
+      const EUnit rc = *reinterpret_cast<const EUnit*>(rec);
       if (rc.flags & kRecEnd) break;
-      const bool mine = m < rc.cnt;
-      if (rc.flags & kRecNewTile) {
-        tok_m = !mine ? -1 : (rc.flags & kRecTma) ? rc.row0 + m : a.perm[rc.p0 + m];
-        // s * h as two bf16 parts, K-major, 128-byte swizzle, one atom; zero
-        // beyond r and beyond the tile's rows.  This thread builds 16-byte
-        // chunks half * 4 .. half * 4 + 3 of row m.  The previous tile's MMAs
-        // have completed: its last accumulator was read below.
-        const float* hrow = a.h + (mine ? (a.h_by_token ? (long long)tok_m : (long long)(rc.p0 + m)) : 0) * a.ldh;
-        for (int qq = half * 4; qq < min(rc.rpad / 8, half * 4 + 4); ++qq) {
-          float hv[8];
-#pragma unroll
-          for (int e4 = 0; e4 < 2; ++e4) {
-            const int j = qq * 8 + 4 * e4;
-            if (mine && j + 3 < rc.r) {
-              const float4 f = *reinterpret_cast<const float4*>(hrow + j);
-              hv[4 * e4] = f.x;
-              hv[4 * e4 + 1] = f.y;
-              hv[4 * e4 + 2] = f.z;
-              hv[4 * e4 + 3] = f.w;
-            } else {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) hv[4 * e4 + e] = (mine && j + e < rc.r) ? hrow[j + e] : 0.f;
-            }
-          }
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float s0 = rc.scale * hv[2 * e], s1 = rc.scale * hv[2 * e + 1];
-            hi[e] = pack_bf16x2(s0, s1);
-            lo[e] = pack_bf16x2(s0 - bf_lo(hi[e]), s1 - bf_hi(hi[e]));
-          }
-          *reinterpret_cast<uint4*>(hhi + sw128_offset(m, qq)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(hlo + sw128_offset(m, qq)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(h_ready));
-      }
+      const int tok_m = reinterpret_cast<const int*>(rec + 64)[m];
       const uint32_t b = uc & 1, k = uc >> 1;
       if (!mbar_wait(smem_u32(&acc_full[b]), k & 1)) ok = false;
       tc_fence_after();
@@ -764,11 +890,11 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
       if (ok) {
 #pragma unroll
         for (int rr = 0; rr < 32; rr += 4) {
-          const int sub = rr + (lane >> 3), mr = quarter * 32 + sub, p = lane & 7;
+          const int sub = rr + (lane >> 3), mr = quarter * 32 + sub, pp = lane & 7;
           const int tk = __shfl_sync(0xffffffffu, tok_m, sub);
           if (mr < rc.cnt)
-            *reinterpret_cast<uint4*>(a.y + (long long)tk * a.ldy + rc.n0 + half * 64 + 8 * p) =
-                *reinterpret_cast<const uint4*>(atom + sw128_offset(mr, p));
+            *reinterpret_cast<uint4*>(a.y + (long long)tk * a.ldy + rc.n0 + half * 64 + 8 * pp) =
+                *reinterpret_cast<const uint4*>(atom + sw128_offset(mr, pp));
         }
       }
       __syncwarp();
@@ -778,7 +904,88 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (warp == kEWarpMma) tmem_dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------- reduce_partials --
+//
+// h of a tile split over several slices of d_in: the sum of the slices'
+// partials in slice order (the order does not depend on which CTA finished
+// first).  One CTA per tile at a time; (row, 4-column group) pairs spread over
+// the threads, every slice's load in flight before the sums.
+
+constexpr int kRThreads = 256;
+
+struct ReduceArgs {
+  const float* part;
+  float* h;
+  long long ldh;
+  int h_by_token;
+  int T;
+  int ks;
+  DevView v;
+  const int32_t* perm;
+  const int32_t* indptr;
+  const int32_t* seg_adapter;
+  const int32_t* long_units;
+  const int32_t* meta;
+};
+
+__global__ void __launch_bounds__(kRThreads) reduce_partials_kernel(const __grid_constant__ ReduceArgs a) {
+  __shared__ int info[4];  // p0, cnt, rank, skip
+  pdl_wait_then_release();
+  const int n_tiles = a.meta[3];
+  const int tid = threadIdx.x;
+  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    if (tid < 32) {
+      const int s = a.long_units[2 * tile], m0 = a.long_units[2 * tile + 1];
+      const lora_adapter_desc_t d = a.v.adapters[a.seg_adapter[s]];
+      const int bad = check_adapter_warp(a.v, d, tid);  // the tiles the shrink skipped
+      if (tid == 0) {
+        info[0] = a.indptr[s] + m0;
+        info[1] = min(kTM, a.indptr[s + 1] - info[0]);
+        info[2] = d.rank;
+        info[3] = bad;
+      }
+    }
+    __syncthreads();
+    const int p0 = info[0], cnt = info[1], r = info[2], skip = info[3];
+    __syncthreads();
+    if (skip) continue;
+    const int nq4 = (r + 3) / 4, npairs = cnt * nq4;
+    for (int i0 = tid; i0 < npairs; i0 += 2 * kRThreads) {
+      float4 pv[LORA_KSPLIT_MAX][2];
+      long long hrow[2];
+#pragma unroll
+      for (int b2 = 0; b2 < 2; ++b2) {
+        const int i = i0 + kRThreads * b2;
+        const int row = i / nq4, j = (i - row * nq4) * 4;
+        hrow[b2] = i < npairs ? (a.h_by_token ? (long long)a.perm[p0 + row] : (long long)(p0 + row)) : 0;
+#pragma unroll
+        for (int qq = 0; qq < LORA_KSPLIT_MAX; ++qq)
+          pv[qq][b2] = (qq < a.ks && i < npairs)
+                           ? __ldcg(reinterpret_cast<const float4*>(
+                                 a.part + ((long long)qq * a.T + p0 + row) * LORA_MAX_RANK + j))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int b2 = 0; b2 < 2; ++b2) {
+        const int i = i0 + kRThreads * b2;
+        if (i >= npairs) continue;
+        float4 s4 = pv[0][b2];
+#pragma unroll
+        for (int qq = 1; qq < LORA_KSPLIT_MAX; ++qq) {
+          if (qq < a.ks) {
+            s4.x += pv[qq][b2].x;
+            s4.y += pv[qq][b2].y;
+            s4.z += pv[qq][b2].z;
+            s4.w += pv[qq][b2].w;
+          }
+        }
+        store_h4(a.h + hrow[b2] * a.ldh, (i % nq4) * 4, r, s4.x, s4.y, s4.z, s4.w);
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------- launchers --
@@ -856,19 +1063,38 @@ lora_status_t launch_shrink_tc(const void* x, long long ldx, float* h, long long
   long long grid = sm_count();
   if (upper < grid) grid = upper;
   if (grid <= 0) return LORA_OK;
-  a.use_tma = make_act_map(&a.xmap, x, seg->T, view->d_in, ldx, kTM) ? 1 : 0;
+  a.use_tma = make_act_map(&a.xmap, x, seg->T, view->d_in, ldx, kSTmaRows) ? 1 : 0;
   a.x = static_cast<const uint16_t*>(x);
   a.ldx = ldx;
   a.h = h;
   a.ldh = ldh;
   a.h_by_token = h_by_token;
   a.part = seg->k_partials;
-  a.tickets = seg->tickets;
+  a.counter = seg->meta + 5;
   a.T = seg->T;
   fill_common(&a, seg, view, err);
   if (ensure_smem_attr((const void*)shrink_tc_kernel, kShrinkSmem) != cudaSuccess) return LORA_ERR_CUDA;
-  return launch_pdl((const void*)shrink_tc_kernel, dim3((unsigned)grid), dim3(kSThreads), kShrinkSmem, stream, 0,
-                    &a) == cudaSuccess
+  if (launch_pdl((const void*)shrink_tc_kernel, dim3((unsigned)grid), dim3(kSThreads), kShrinkSmem, stream, 0, &a) !=
+      cudaSuccess)
+    return LORA_ERR_CUDA;
+  if (a.ksplit == 1) return LORA_OK;
+  ReduceArgs ra;
+  ra.part = a.part;
+  ra.h = h;
+  ra.ldh = ldh;
+  ra.h_by_token = h_by_token;
+  ra.T = a.T;
+  ra.ks = a.ksplit;
+  ra.v = a.v;
+  ra.perm = a.perm;
+  ra.indptr = a.indptr;
+  ra.seg_adapter = a.seg_adapter;
+  ra.long_units = a.long_units;
+  ra.meta = a.meta;
+  long long rgrid = (long long)sm_count() * 4;
+  if (seg->max_long_units < rgrid) rgrid = seg->max_long_units;
+  return launch_pdl((const void*)reduce_partials_kernel, dim3((unsigned)rgrid), dim3(kRThreads), 0, stream, 0,
+                    &ra) == cudaSuccess
              ? LORA_OK
              : LORA_ERR_CUDA;
 }
@@ -882,6 +1108,7 @@ lora_status_t launch_expand_tc(const float* h, long long ldh, int h_by_token, vo
   if (upper < grid) grid = upper;
   if (grid <= 0) return LORA_OK;
   a.use_tma = make_act_map(&a.ymap, y, seg->T, view->d_out, ldy, kTM) ? 1 : 0;
+  a.counter = seg->meta + 6;
   a.y = static_cast<uint16_t*>(y);
   a.ldy = ldy;
   a.h = h;

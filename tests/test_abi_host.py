@@ -41,7 +41,7 @@ def test_abi_version_and_status_strings():
 def test_struct_sizes_match_c_layout():
     assert ctypes.sizeof(B.lora_adapter_desc_t) == 16
     assert ctypes.sizeof(B.lora_pool_view_t) == 64
-    assert ctypes.sizeof(B.lora_segments_t) == 8 + 10 * 8
+    assert ctypes.sizeof(B.lora_segments_t) == 8 + 9 * 8
 
 
 @pytest.mark.parametrize("rank,d_in,d_out,P", [(16, 8192, 8192, 4096), (13, 5120, 11008, 4096),
@@ -62,7 +62,7 @@ def test_carve_layout():
         assert s.T == T
         assert s.max_long_units == T // 128 + T // 9 + 1
         ptrs = [s.token_perm, s.seg_indptr, s.seg_adapter, s.meta, s.short_units, s.long_units, s.scratch,
-                s.h_scratch, s.k_partials, s.tickets]
+                s.h_scratch, s.k_partials]
         assert all(p % 16 == 0 for p in ptrs)
         assert ptrs == sorted(ptrs) and ptrs[0] == base
         assert L.lora_segments_carve(ctypes.c_void_p(base), n - 16, T, ctypes.byref(s)) == B.LORA_ERR_WORKSPACE
@@ -82,7 +82,7 @@ def fake_seg(T=16):
     s.T = T
     s.max_long_units = T // 128 + T // 9 + 1
     for i, f in enumerate(("token_perm", "seg_indptr", "seg_adapter", "meta", "short_units",
-                           "long_units", "scratch", "h_scratch", "k_partials", "tickets")):
+                           "long_units", "scratch", "h_scratch", "k_partials")):
         setattr(s, f, 0x100000 + 0x1000 * i)
     return s
 

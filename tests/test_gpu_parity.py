@@ -451,8 +451,8 @@ def test_tc_device_errors_in_long_tiles():
 
 def test_tc_segments_reused_across_calls_and_shapes():
     """One segment buffer serves several projections of different d_in in a row (the
-    per-tile tickets of the split d_in reduction must be back at zero after each
-    call); every result equals a fresh run bit for bit."""
+    tensor-core kernels' work counters must be back at zero after each call);
+    every result equals a fresh run bit for bit."""
     rng = np.random.default_rng(26)
     ranks = [16, 64, 7]
     lens = [256, 300, 129]
