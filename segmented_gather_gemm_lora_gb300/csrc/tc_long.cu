@@ -30,10 +30,10 @@
 //             into bf16 hi + lo parts (two MMAs accumulating into the same fp32
 //             columns), keeping the rank-r intermediate at about fp32
 //             accuracy.  B_i rows are MN-major operands (r_i rows of d_out
-//             contiguous elements, as stored).  y0's first 64 columns arrive
-//             by a TMA tensor copy for tiles of 128 consecutive tokens, the
-//             rest by 16-byte asynchronous copies; y leaves by coalesced
-//             16-byte stores.
+//             contiguous elements, as stored).  y0 arrives by TMA tensor
+//             copies for tiles of 128 consecutive tokens, by 16-byte
+//             asynchronous copies otherwise; y leaves by coalesced 16-byte
+//             stores.
 //
 // Tokens of one segment are listed in increasing order (the segment builder's
 // order is stable), so a tile whose first and last tokens are 127 apart is the
@@ -495,15 +495,17 @@ __global__ void __launch_bounds__(kSThreads, 1) shrink_tc_kernel(const __grid_co
 // ---------------------------------------------------------------- expand_tc --
 //
 // Warp roles: 0 schedules (claims groups of kEGroup consecutive units, resolves
-// tile, adapter and B pages, and builds each new tile's H operand, s_i h as
-// bf16 hi + lo, into one of two buffers), 1-4 load, 5 issues MMAs, 6-13
-// epilogue.  Units pass from the scheduler to the loaders through a 4-slot
+// tile, adapter and B pages), 1-4 load, 5 issues MMAs, 6-13 epilogue, 14
+// builds each new tile's H operand, s_i h as bf16 hi + lo, into one of two
+// buffers, a tile ahead of the MMAs.  Units pass from the scheduler to the loaders through a 4-slot
 // queue; the loaders' 3-stage ring carries a record of each unit to the MMA
-// warp and the epilogue.  A unit's first 64 y0 columns come by one TMA tensor
-// copy when the tile is 128 consecutive tokens, the rest by the loader warps'
-// 16-byte asynchronous copies.
+// warp and the epilogue.  A unit's y0 comes by two TMA tensor copies when the
+// tile is 128 consecutive tokens (the y stores and the B rows keep the load /
+// store units busy meanwhile), by the loader warps' 16-byte asynchronous copies
+// otherwise.
 
-constexpr int kEThreads = 448;
+constexpr int kEThreads = 480;
+constexpr int kEWarpH = 14;
 constexpr int kELoad = 4;
 constexpr int kEWarpLoad0 = 1, kEWarpMma = 5, kEWarpEpi0 = 6;
 constexpr int kEEpiWarps = 8;  // (tensor-memory lane quarter, 64-column half) each
@@ -525,7 +527,12 @@ constexpr int kESlotBytes = kERecBytes + 64 * 4;  // record, rows, B pages
 constexpr size_t kEOffH = (size_t)kEStages * kEStageBytes;
 constexpr size_t kEOffQ = kEOffH + 2 * (size_t)kEHBytes;
 constexpr size_t kEOffRec = kEOffQ + (size_t)kEQ * kESlotBytes;
-constexpr size_t kEOffBars = kEOffRec + (size_t)kEStages * kERecBytes;
+struct HReq {  // scheduler -> H builder, one per tile
+  int p0, cnt, r, flags;
+  float scale;
+};
+constexpr size_t kEOffHq = kEOffRec + (size_t)kEStages * kERecBytes;  // 2 requests: record, h rows
+constexpr size_t kEOffBars = kEOffHq + 2 * (size_t)kERecBytes;
 constexpr size_t kExpandSmem = kEOffBars + 64 * 8 + 1024;
 
 struct ExpandArgs {
@@ -552,6 +559,7 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
   auto hbuf_at = [&](int hb) { return sm + kEOffH + (size_t)hb * kEHBytes; };
   auto slot_at = [&](uint32_t q) { return sm + kEOffQ + (size_t)q * kESlotBytes; };
   auto rec_at = [&](uint32_t st) { return sm + kEOffRec + (size_t)st * kERecBytes; };
+  auto hq_at = [&](uint32_t q) { return sm + kEOffHq + (size_t)q * kERecBytes; };
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kEOffBars);
   uint64_t* full_tma = bars;                // [stages] lead loader (+ TMA bytes of y0)
   uint64_t* full_cp = bars + kEStages;      // [stages] 128 loader threads' copies landed
@@ -562,7 +570,9 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
   uint64_t* acc_empty = acc_full + 2;       // [2] 8 epilogue warps
   uint64_t* h_ready = acc_empty + 2;        // [2] 32 scheduler lanes
   uint64_t* h_free = h_ready + 2;           // [2] MMA commit when it leaves the buffer's tile
-  uint64_t* mma_done = h_free + 2;
+  uint64_t* hq_full = h_free + 2;           // [2] 32 scheduler lanes
+  uint64_t* hq_empty = hq_full + 2;         // [2] H builder
+  uint64_t* mma_done = hq_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -582,6 +592,8 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
       mbar_init(smem_u32(&acc_empty[b]), kEEpiWarps);
       mbar_init(smem_u32(&h_ready[b]), 32);
       mbar_init(smem_u32(&h_free[b]), 1);
+      mbar_init(smem_u32(&hq_full[b]), 32);
+      mbar_init(smem_u32(&hq_empty[b]), 1);
     }
     mbar_init(smem_u32(mma_done), 1);
     fence_mbar_init();
@@ -625,6 +637,10 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
         if (lane == 0) reinterpret_cast<EUnit*>(slot)->flags = kRecEnd;
         mbar_arrive(smem_u32(&uq_full[j % kEQ]));
         ++j;
+        const int hq = tcount & 1;  // and the H builder's end
+        if (tcount >= 2 && !mbar_wait(smem_u32(&hq_empty[hq]), ((tcount >> 1) - 1) & 1)) ok = false;
+        if (lane == 0) reinterpret_cast<HReq*>(hq_at(hq))->flags = kRecEnd;
+        mbar_arrive(smem_u32(&hq_full[hq]));
         break;
       }
       for (int w = c * kEGroup; w < min(n_work, (c + 1) * kEGroup); ++w) {
@@ -642,49 +658,21 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
               const int m = lane + 32 * i;
               rows[i] = m >= ti.cnt ? -1 : ti.tma ? ti.row0 + m : a.perm[ti.p0 + m];
             }
-            // H operand of the tile: s * h in two bf16 parts, K-major, 128-byte
-            // swizzle, one atom; zero beyond r and beyond the tile's rows.
-            const int hb = tcount & 1;
-            if (tcount >= 2 && !mbar_wait(smem_u32(&h_free[hb]), ((tcount >> 1) - 1) & 1)) ok = false;
-            uint8_t* hhi = hbuf_at(hb);
-            uint8_t* hlo = hhi + kTM * 128;
-            const int r = d.rank, rpad = (r + 15) & ~15;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int m = lane + 32 * i;
-              const bool mine = m < ti.cnt;
-              const long long hr = !mine ? 0 : a.h_by_token ? (ti.tma ? (long long)(ti.row0 + m) : (long long)rows[i])
-                                                             : (long long)(ti.p0 + m);
-              const float* hrow = a.h + hr * a.ldh;
-              for (int qq = 0; qq < rpad / 8; ++qq) {
-                float hv[8];
-#pragma unroll
-                for (int e4 = 0; e4 < 2; ++e4) {
-                  const int jj = qq * 8 + 4 * e4;
-                  if (mine && jj + 3 < r) {
-                    const float4 f = *reinterpret_cast<const float4*>(hrow + jj);
-                    hv[4 * e4] = f.x;
-                    hv[4 * e4 + 1] = f.y;
-                    hv[4 * e4 + 2] = f.z;
-                    hv[4 * e4 + 3] = f.w;
-                  } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) hv[4 * e4 + e] = (mine && jj + e < r) ? hrow[jj + e] : 0.f;
-                  }
-                }
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float s0 = d.scale * hv[2 * e], s1 = d.scale * hv[2 * e + 1];
-                  hi[e] = pack_bf16x2(s0, s1);
-                  lo[e] = pack_bf16x2(s0 - bf_lo(hi[e]), s1 - bf_hi(hi[e]));
-                }
-                *reinterpret_cast<uint4*>(hhi + sw128_offset(m, qq)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(hlo + sw128_offset(m, qq)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-              }
+            // the tile's H operand, built by the H warp into buffer tcount & 1
+            const int hq = tcount & 1;
+            if (tcount >= 2 && !mbar_wait(smem_u32(&hq_empty[hq]), ((tcount >> 1) - 1) & 1)) ok = false;
+            uint8_t* req = hq_at(hq);
+            if (lane == 0) {
+              HReq* hr = reinterpret_cast<HReq*>(req);
+              hr->p0 = ti.p0;
+              hr->cnt = ti.cnt;
+              hr->r = d.rank;
+              hr->flags = 0;
+              hr->scale = d.scale;
             }
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&h_ready[hb]));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) reinterpret_cast<int*>(req + 64)[lane + 32 * i] = rows[i];
+            mbar_arrive(smem_u32(&hq_full[hq]));  // each lane after its own writes
             ++tcount;
           }
         }
@@ -747,8 +735,10 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
       const bool tma = eu.flags & kRecTma;
       if (lead) {
         if (tma && !(eu.flags & kRecEnd)) {
-          mbar_arrive_expect_tx(smem_u32(&full_tma[st]), kEAtom);
+          mbar_arrive_expect_tx(smem_u32(&full_tma[st]), kEYBytes);
           tma_load_2d(smem_u32(sm + st * kEStageBytes), &a.ymap, eu.n0, eu.row0, smem_u32(&full_tma[st]));
+          tma_load_2d(smem_u32(sm + st * kEStageBytes) + kEAtom, &a.ymap, eu.n0 + 64, eu.row0,
+                      smem_u32(&full_tma[st]));
         } else {
           mbar_arrive(smem_u32(&full_tma[st]));
         }
@@ -760,15 +750,17 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
       }
       const uint32_t ys = smem_u32(sm + st * kEStageBytes);
       const uint32_t bs = ys + kEYBytes;
-      // y0 rows m = 32 lw + (lane >> 3) + 4 t, piece lane & 7 of each 64-column atom
+      // y0 rows of other tiles: m = 32 lw + (lane >> 3) + 4 t, piece lane & 7 of each 64-column atom
+      if (!tma) {
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int m = 32 * lw + (lane >> 3) + 4 * t;
-        const int rw = srows[m];
-        if (rw < 0) continue;
-        const uint16_t* src = a.y + (long long)rw * a.ldy + eu.n0 + 8 * p;
-        if (!tma) cp_async16(ys + sw128_offset(m, p), src);
-        cp_async16(ys + kEAtom + sw128_offset(m, p), src + 64);
+        for (int t = 0; t < 8; ++t) {
+          const int m = 32 * lw + (lane >> 3) + 4 * t;
+          const int rw = srows[m];
+          if (rw < 0) continue;
+          const uint16_t* src = a.y + (long long)rw * a.ldy + eu.n0 + 8 * p;
+          cp_async16(ys + sw128_offset(m, p), src);
+          cp_async16(ys + kEAtom + sw128_offset(m, p), src + 64);
+        }
       }
       // B rows j = 4 ((lane >> 4) + 2 t) + lw: MN-major operand, 2 atoms of 64
       // columns, 8 rank rows per 1024-byte group, 128-byte swizzle; zero beyond r
@@ -844,6 +836,77 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
       if (!ok) report(a.err, LORA_DERR_TIMEOUT);
     }
     __syncwarp();
+  } else if (warp == kEWarpH) {
+    // ---------------- H builder ----------------
+    // Tile t's H into buffer t & 1 once the MMA warp has left tile t - 2: s * h
+    // in two bf16 parts, K-major, 128-byte swizzle, one atom; zero beyond r
+    // and beyond the tile's rows.  Lane l builds rows l + 32 i; every load of
+    // a batch of eight 8-column chunks is in flight before the batch's stores.
+    for (uint32_t t = 0;; ++t) {
+      const int hq = t & 1;
+      if (!mbar_wait(smem_u32(&hq_full[hq]), (t >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* req = hq_at(hq);
+      const HReq hr = *reinterpret_cast<const HReq*>(req);
+      if (hr.flags & kRecEnd) break;
+      if (t >= 2 && !mbar_wait(smem_u32(&h_free[hq]), ((t >> 1) - 1) & 1)) ok = false;
+      uint8_t* hhi = hbuf_at(hq);
+      uint8_t* hlo = hhi + kTM * 128;
+      const int r = hr.r, nq8 = ((r + 15) & ~15) / 8, npair = 4 * nq8;
+      const float* hrows[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int m = lane + 32 * i;
+        const long long row = m >= hr.cnt ? -1
+                              : a.h_by_token ? (long long)reinterpret_cast<const int*>(req + 64)[m]
+                                             : (long long)(hr.p0 + m);
+        hrows[i] = row < 0 ? nullptr : a.h + row * a.ldh;
+      }
+      for (int t0 = 0; t0 < npair; t0 += 8) {
+        float hv[8][8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          const int tp = t0 + b, i = tp / nq8, qq = tp - i * nq8;
+          const float* hrow = tp >= npair ? nullptr : i == 0 ? hrows[0] : i == 1 ? hrows[1] : i == 2 ? hrows[2] : hrows[3];
+#pragma unroll
+          for (int e4 = 0; e4 < 2; ++e4) {
+            const int jj = qq * 8 + 4 * e4;
+            if (hrow != nullptr && jj + 3 < r) {
+              const float4 f = *reinterpret_cast<const float4*>(hrow + jj);
+              hv[b][4 * e4] = f.x;
+              hv[b][4 * e4 + 1] = f.y;
+              hv[b][4 * e4 + 2] = f.z;
+              hv[b][4 * e4 + 3] = f.w;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) hv[b][4 * e4 + e] = (hrow != nullptr && jj + e < r) ? hrow[jj + e] : 0.f;
+            }
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          const int tp = t0 + b, i = tp / nq8, qq = tp - i * nq8;
+          if (tp >= npair) continue;
+          const int m = lane + 32 * i;
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float s0 = hr.scale * hv[b][2 * e], s1 = hr.scale * hv[b][2 * e + 1];
+            hi[e] = pack_bf16x2(s0, s1);
+            lo[e] = pack_bf16x2(s0 - bf_lo(hi[e]), s1 - bf_hi(hi[e]));
+          }
+          *reinterpret_cast<uint4*>(hhi + sw128_offset(m, qq)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(hlo + sw128_offset(m, qq)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&h_ready[hq]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&hq_empty[hq]));
+    }
+    if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
   } else {
     // ---------------- epilogue: y = y0 + accumulator, per unit ----------------
     const int quarter = warp & 3;                 // tensor-memory lanes this warp may read
