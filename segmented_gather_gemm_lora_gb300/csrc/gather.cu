@@ -8,9 +8,9 @@
 // "S-LoRA: MBGMV and MBGMM Kernels"), and for the shrink / expand stages alone.
 //
 // Work decomposition.  One thread-block cluster of CL CTAs (CL <= 8) takes one
-// work unit (an adapter and up to 8 of its tokens, in groups of 4) at a time.  CTA c of the
-// cluster owns the c-th slice of d_in for the shrink and the c-th slice of
-// d_out for the expand, so every adapter byte and every activation byte is
+// work unit (an adapter and its tokens, in groups of up to 4) at a time.  CTA c
+// of the cluster owns the c-th slice of d_in for the shrink and the c-th slice
+// of d_out for the expand, so every adapter byte and every activation byte is
 // read once per unit:
 //   shrink  partial_c[t, j] = sum_{k in slice c} x[t, k] * A_i[j, k]
 //   reduce  h[t, j] = s_i * sum_c partial_c[t, j]   through distributed shared
@@ -18,16 +18,17 @@
 //   expand  y[t, n] = bf16(y0[t, n] + sum_j h[t, j] * B_i[j, n]),  n in slice c
 // The rank-r intermediate never leaves the chip.
 //
-// Data movement.  A slice is cut into sub-slices of 512 columns and each
-// sub-slice into chunks of 16 adapter rows, so every staged row is a 1 KB run
-// (translated 16 bytes at a time through the page table, "Multi-LoRA Serving
-// in Production", section "Unified Paged Memory"), staged together with the
-// unit's token rows for the same columns.  Every thread copies 16-byte pieces
-// with cp.async, one warp per row (512 bytes per instruction), into a ring of
-// three stages, each completed through an mbarrier; expand chunks are issued
-// as soon as stages free up, so the two phases' bytes overlap.  Rows of 1 KB are
-// what keeps a streaming multiprocessor near its share of HBM bandwidth;
-// rows of a few hundred bytes fall to a half or less.
+// Warp roles.  Warp 8 of every CTA produces: it resolves each unit's adapter
+// and pages and stages 16-row chunks of the adapter (1 KB row runs, translated
+// 16 bytes at a time through the page table, "Multi-LoRA Serving in
+// Production", section "Unified Paged Memory"; one bulk copy per row run and
+// page) with the unit's token rows for the same columns into a 4-stage ring;
+// every stage carries a record of what it holds.  Warps 0-7 consume the ring.  Between a group's shrink and expand the
+// consumers of the cluster's CTAs exchange partial h through distributed shared
+// memory, signalled by mbarrier arrivals on the peers, so the producer keeps
+// streaming the expand rows and the next unit meanwhile.  Units are claimed
+// from a counter (CTA 0 of a cluster claims, and hands the claim to its peers)
+// when the segments give one; one-token units go round-robin.
 //
 // Summation order.  Each rank row's shrink dot product over a sub-slice and
 // each output's expand sum over a 16-row chunk are fixed functions of column
@@ -37,27 +38,54 @@
 // units changes no bit of its output.
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace lora {
 
-constexpr int kGThreads = 256;
-constexpr int kNT = 4;  // tokens per group (a unit of up to 8 tokens runs in two groups)
+constexpr int kGCons = 8;       // consumer warps
+constexpr int kGProd = kGCons;  // the producer warp
+constexpr int kGThreads = 32 * (kGCons + 1);
+constexpr int kGConsThreads = 32 * kGCons;
+constexpr int kNT = 4;  // tokens per group
 constexpr int kHMax = LORA_MAX_RANK;
 constexpr int kMaxCluster = 8;
-constexpr int kSub = 512;                      // columns per sub-slice (one 1 KB row)
-constexpr int kChunkRows = 16;                 // adapter rows per chunk
+constexpr int kSub = 512;       // columns per sub-slice (one 1 KB row)
+constexpr int kChunkRows = 16;  // adapter rows per chunk
 constexpr int kRowBytes = kSub * 2;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kStageBytes = (kChunkRows + kNT) * kRowBytes;  // 20 KB
 constexpr int kMaxPgSlots = 512;  // page-list slots of one adapter cached in shared memory
 
-constexpr size_t kOffBars = (size_t)kStages * kStageBytes;
-constexpr size_t kOffEacc = kOffBars + 64;                                  // fp32 [kNT][kSub]
-constexpr size_t kOffHp = kOffEacc + (size_t)kNT * kSub * sizeof(float);    // fp32 [2][kNT][kHMax]
-constexpr size_t kOffHs = kOffHp + 2 * kNT * kHMax * sizeof(float);         // fp32 [kNT][kHMax]
-constexpr size_t kOffTok = kOffHs + kNT * kHMax * sizeof(float);
-constexpr size_t kOffPgt = kOffTok + kNT * sizeof(int) + 32;
-constexpr size_t kGatherSmem = kOffPgt + kMaxPgSlots * sizeof(int);
+enum GKind { kGShrink = 0, kGExpand = 1, kGReduce = 2, kGEnd = 3 };
+
+// What the producer tells the consumers about a stage.
+struct GRec {
+  int kind;
+  int ntok;    // tokens of the group
+  int j0;      // first adapter row of the chunk
+  int nrows;   // adapter rows of the chunk
+  int nvec;    // 16-byte pieces per row of the sub-slice
+  int col0;    // first column of the sub-slice
+  int first;   // shrink: first sub-slice (store, not add); expand: first row block of the sub-slice
+  int last;    // expand: last row block of the sub-slice (adds y0, writes y; token rows staged)
+  int gfirst;  // first record of the group: the partial-h buffer is reused once peers are done
+  int r;       // rank
+  float sc;    // scale
+  int no_k;    // reduce: this CTA has no d_in slice (its partial is zero)
+  int tok[kNT];
+};
+static_assert(sizeof(GRec) <= 64, "record slot");
+static_assert(kSub / 64 <= kGCons, "one warp per block of 8 output vectors");
+
+constexpr size_t kOffRec = (size_t)kStages * kStageBytes;
+constexpr size_t kOffEacc = kOffRec + (size_t)kStages * 64;               // fp32 [kNT][kSub]
+constexpr size_t kOffHp = kOffEacc + (size_t)kNT * kSub * sizeof(float);  // fp32 [2][kNT][kHMax]
+constexpr size_t kOffHs = kOffHp + 2 * kNT * kHMax * sizeof(float);       // fp32 [kNT][kHMax]
+constexpr size_t kOffPgt = kOffHs + kNT * kHMax * sizeof(float);          // int [kMaxPgSlots]
+constexpr size_t kOffClaim = kOffPgt + kMaxPgSlots * sizeof(int);         // int [2]
+constexpr size_t kOffBars = kOffClaim + 16;
+constexpr int kNBars = 2 * kStages + 2 + 2 + 2 + 2 + 1;
+constexpr size_t kGatherSmem = kOffBars + kNBars * 8;
 
 struct GatherArgs {
   const uint16_t* x;
@@ -73,6 +101,7 @@ struct GatherArgs {
   const int32_t* short_units;
   const int32_t* long_units;
   const int32_t* meta;
+  int32_t* counter;  // unit claims (segments); zero between calls
   const int32_t* token_adapter;
   int T;
   int32_t* err;
@@ -81,72 +110,16 @@ struct GatherArgs {
   int short_only;
 };
 
-// One unit's chunk schedule: shrink chunks (sub-slice ks, row block jb) first,
-// then expand chunks (sub-slice ns, row block jb).
-struct ChunkPlan {
-  int r, ntok, njb;  // rank, tokens, row blocks of kChunkRows
-  int nks, nns;      // sub-slices of the d_in / d_out slices (0 if the phase is skipped)
-  int k0, k1, n0, n1;
-  int a_page0, b_page0;
-  int na;            // page-list slots of A_i (B_i's follow in the cached table)
-  const int* pgt;    // cached physical pages of A_i then B_i, or null
-};
-
-// Stage chunk c into `stage`: adapter rows [16 jb, 16 jb + 16) of the chunk's
-// sub-slice at rows 0..15, then the unit's token rows (x for the shrink, y0
-// for the expand) of the same columns at rows 16..23.  One warp per row,
-// 16-byte pieces per lane; every thread then arrives on `bar` once its own
-// pieces have landed.
-__device__ __forceinline__ void issue_chunk(const GatherArgs& a, const ChunkPlan& p, const int* tok, int c,
-                                            uint8_t* stage, uint32_t bar, int tid) {
-  const int nsh = p.nks * p.njb;
-  const bool shrink = c < nsh;
-  const int cc = shrink ? c : c - nsh;
-  const int sub = cc / p.njb, jb = cc - sub * p.njb;
-  const int col0 = shrink ? p.k0 + sub * kSub : p.n0 + sub * kSub;
-  const int w = shrink ? min(kSub, p.k1 - col0) : min(kSub, p.n1 - col0);
-  const int j0 = jb * kChunkRows, nrows = min(kChunkRows, p.r - j0);
-  const long long rowlen = shrink ? a.v.d_in : a.v.d_out;
-  const long long page0 = shrink ? p.a_page0 : p.b_page0;
-  const uint16_t* act = shrink ? a.x : a.y;
-  const long long ld = shrink ? a.ldx : a.ldy;
-  const int shift = a.v.page_shift;
-  const long long pmask = (1LL << shift) - 1;
-  const uint32_t sbase = smem_u32(stage);
-  const int nq = w >> 3;  // 16-byte pieces per row
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int item = warp; item < nrows + p.ntok; item += kGThreads / 32) {
-    const bool adapter_row = item < nrows;
-    const uint32_t drow = sbase + (uint32_t)((adapter_row ? item : kChunkRows + item - nrows) * kRowBytes);
-    if (adapter_row) {
-      const long long e0 = (long long)(j0 + item) * rowlen + col0;
-      for (int q = lane; q < nq; q += 32) {
-        const long long e = e0 + 8 * q;
-        const long long idx = e >> shift;
-        const long long page = p.pgt ? p.pgt[(shrink ? 0 : p.na) + idx] : a.v.page_list[page0 + idx];
-        const uint16_t* src = a.v.pool + (page << shift) + (e & pmask);
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(drow + 16 * q), "l"(src) : "memory");
-      }
-    } else {
-      const uint16_t* src0 = act + (long long)tok[item - nrows] * ld + col0;
-      for (int q = lane; q < nq; q += 32)
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(drow + 16 * q), "l"(src0 + 8 * q) : "memory");
-    }
-  }
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// Shrink of one staged chunk for NT tokens: warp w takes the chunk's rows w
-// and w + 8 together (one unpack of each token vector serves both); its lanes
-// take fixed 8-column vectors of the sub-slice; each row's dot product with
-// every token is reduced over the warp and added to the CTA's partial h
-// (sub-slices in order).  Instantiated per token count so that a one-token
-// decode unit executes only its own arithmetic.
+// Shrink of one staged chunk for NT tokens: consumer warp w takes the chunk's
+// rows w and w + 8 together (one unpack of each token vector serves both); its
+// lanes take fixed 8-column vectors of the sub-slice; each row's dot product
+// with every token is reduced over the warp and stored (first sub-slice) or
+// added to the CTA's partial h (sub-slices in order).
 template <int NT>
-__device__ __forceinline__ void shrink_chunk(const uint8_t* sb, int j0, int nrows, int nvec, float* hpb,
+__device__ __forceinline__ void shrink_chunk(const uint8_t* sb, int j0, int nrows, int nvec, bool store, float* hpb,
                                              int warp, int lane) {
   const uint4* xrow = reinterpret_cast<const uint4*>(sb + kChunkRows * kRowBytes);
-  const int i0 = warp, i1 = warp + kGThreads / 32;  // the warp's two rows (16-row chunks)
+  const int i0 = warp, i1 = warp + kGCons;  // the warp's two rows (16-row chunks)
   const bool has0 = i0 < nrows, has1 = i1 < nrows;
   if (!has0) return;
   float acc0[NT], acc1[NT];
@@ -180,26 +153,33 @@ __device__ __forceinline__ void shrink_chunk(const uint8_t* sb, int j0, int nrow
   if (lane == 0) {
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      hpb[t * kHMax + j0 + i0] += acc0[t];
-      if (has1) hpb[t * kHMax + j0 + i1] += acc1[t];
+      float* p0 = hpb + t * kHMax + j0 + i0;
+      *p0 = store ? acc0[t] : *p0 + acc0[t];
+      if (has1) {
+        float* p1 = hpb + t * kHMax + j0 + i1;
+        *p1 = store ? acc1[t] : *p1 + acc1[t];
+      }
     }
   }
 }
 
-// Expand of one staged chunk.  A warp takes one (token, block of 8 output
-// vectors): lane = 8 g + u handles vector u of the block for the chunk's rows
-// 4 g .. 4 g + 3 (ascending), so each group of 8 lanes reads 128 contiguous
-// bytes of one row (no bank conflicts); the four row-quarter sums meet in a
-// fixed two-step butterfly, and chunk sums accumulate in chunk order in eacc.
-// The sub-slice's last chunk adds y0 and writes y.
+// Expand of one staged chunk.  Warp w takes block w of 8 output vectors (a
+// sub-slice has at most 8 blocks) for every token, whatever the sub-slice's
+// width, so each eacc entry always belongs to the same warp and consecutive
+// chunks need no barrier between the warps.  Lane = 8 g + u handles vector u of
+// the block for the chunk's rows 4 g .. 4 g + 3 (ascending), so each group of 8
+// lanes reads 128 contiguous bytes of one row (no bank conflicts); the four
+// row-quarter sums meet in a fixed two-step butterfly, and chunk sums
+// accumulate in chunk order in eacc.  The sub-slice's last chunk adds y0 and
+// writes y.
 __device__ __forceinline__ void expand_chunk(const GatherArgs& a, const uint8_t* sb, const float* hs, float* eacc,
-                                             const int* tok, int ntok, int nvec, int j0, int nrows, bool first,
-                                             bool last, int col0, bool ok, int warp, int lane) {
-  const int nblk = (nvec + 7) >> 3;
+                                             const GRec& rc, bool ok, int warp, int lane) {
+  const int nblk = (rc.nvec + 7) >> 3;
+  if (warp >= nblk) return;
   const int g = lane >> 3, u = lane & 7;
-  for (int wi = warp; wi < ntok * nblk; wi += kGThreads / 32) {
-    const int t = wi / nblk, vv = (wi - t * nblk) * 8 + u;
-    const bool act = vv < nvec;
+  for (int t = 0; t < rc.ntok; ++t) {
+    const int vv = warp * 8 + u;
+    const bool act = vv < rc.nvec;
     float o[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) o[q] = 0.f;
@@ -207,8 +187,8 @@ __device__ __forceinline__ void expand_chunk(const GatherArgs& a, const uint8_t*
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int i = 4 * g + k;
-        if (i < nrows) {
-          const float hj = hs[t * kHMax + j0 + i];
+        if (i < rc.nrows) {
+          const float hj = hs[t * kHMax + rc.j0 + i];
           float bf[8];
           unpack8(reinterpret_cast<const uint4*>(sb + i * kRowBytes)[vv], bf);
 #pragma unroll
@@ -223,12 +203,12 @@ __device__ __forceinline__ void expand_chunk(const GatherArgs& a, const uint8_t*
     }
     if (act && g == 0) {
       float4* ea = reinterpret_cast<float4*>(eacc + (t * kSub + vv * 8));
-      if (!first) {
+      if (!rc.first) {
         const float4 e0 = ea[0], e1 = ea[1];
         o[0] = e0.x + o[0]; o[1] = e0.y + o[1]; o[2] = e0.z + o[2]; o[3] = e0.w + o[3];
         o[4] = e1.x + o[4]; o[5] = e1.y + o[5]; o[6] = e1.z + o[6]; o[7] = e1.w + o[7];
       }
-      if (!last) {
+      if (!rc.last) {
         ea[0] = make_float4(o[0], o[1], o[2], o[3]);
         ea[1] = make_float4(o[4], o[5], o[6], o[7]);
       } else if (ok) {
@@ -239,154 +219,314 @@ __device__ __forceinline__ void expand_chunk(const GatherArgs& a, const uint8_t*
         out.y = pack_bf16x2(yf[2] + o[2], yf[3] + o[3]);
         out.z = pack_bf16x2(yf[4] + o[4], yf[5] + o[5]);
         out.w = pack_bf16x2(yf[6] + o[6], yf[7] + o[7]);
-        *reinterpret_cast<uint4*>(a.y + (long long)tok[t] * a.ldy + col0 + vv * 8) = out;
+        *reinterpret_cast<uint4*>(a.y + (long long)rc.tok[t] * a.ldy + rc.col0 + vv * 8) = out;
       }
     }
   }
 }
 
-__global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_constant__ GatherArgs a) {
+__global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_constant__ GatherArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBars);
+  GRec* recs = reinterpret_cast<GRec*>(sm + kOffRec);  // 64-byte slots
   float* eacc = reinterpret_cast<float*>(sm + kOffEacc);
   float* hp = reinterpret_cast<float*>(sm + kOffHp);
   float* hs = reinterpret_cast<float*>(sm + kOffHs);
-  int* tok = reinterpret_cast<int*>(sm + kOffTok);
   int* pgt = reinterpret_cast<int*>(sm + kOffPgt);
+  int* claim_val = reinterpret_cast<int*>(sm + kOffClaim);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBars);
+  uint64_t* full = bars;                   // [stages] the record writer (+ the copies' bytes)
+  uint64_t* empty = bars + kStages;        // [stages] 8 consumer warps
+  uint64_t* hp_ready = bars + 2 * kStages;  // [2] one arrival per CTA of the cluster
+  uint64_t* hp_free = hp_ready + 2;        // [2] one arrival per CTA of the cluster
+  uint64_t* claim_full = hp_free + 2;      // [2] CTA 0's producer
+  uint64_t* claim_empty = claim_full + 2;  // [2] (CTA 0 only) one arrival per CTA
+  uint64_t* cons = claim_empty + 2;        // 8 consumer warps, twice per group
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t crank = cluster_ctarank(), ncta = cluster_nctarank();
   const uint32_t cid = cluster_id_x(), ncl = ncluster_x();
   const DevView& v = a.v;
+  const bool dynamic = a.src == kSrcSegments;
+  const bool reduce_h = a.mode != kModeExpand;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars[s]), kGThreads);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), kGCons);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&hp_ready[b]), ncta);
+      mbar_init(smem_u32(&hp_free[b]), ncta);
+      mbar_init(smem_u32(&claim_full[b]), 1);
+      mbar_init(smem_u32(&claim_empty[b]), ncta);
+    }
+    mbar_init(smem_u32(cons), kGCons);
     fence_mbar_init();
   }
-  __syncthreads();
+  // every barrier of every CTA initialised before any peer arrives on it
+  cluster_sync();
   pdl_wait_then_release();
 
-  // kSrcSegments walks the short units, then the long tiles, in one launch.
-  const int n_short = a.src == kSrcSegments ? a.meta[2] : 0;
-  const int n_units = a.src == kSrcTokens ? a.T : a.meta[2] + (a.short_only ? 0 : a.meta[3]);
   const int kc = ((v.d_in + (int)ncta - 1) / (int)ncta + 7) & ~7;
   const int nc = ((v.d_out + (int)ncta - 1) / (int)ncta + 7) & ~7;
   const int k0 = min(v.d_in, (int)crank * kc), k1 = min(v.d_in, k0 + kc);
   const int n0 = min(v.d_out, (int)crank * nc), n1 = min(v.d_out, n0 + nc);
-  uint32_t parity = 0;  // bit s: parity of stage s's next phase
-  int gbuf = 0;
+  const int nks = (a.mode != kModeExpand && k1 > k0) ? (k1 - k0 + kSub - 1) / kSub : 0;
+  const int nns = (a.mode != kModeShrink && n1 > n0) ? (n1 - n0 + kSub - 1) / kSub : 0;
+  bool ok = true;
 
-  for (int u = (int)cid; u < n_units; u += (int)ncl) {
-    int ad, tb = 0, cnt;
-    if (a.src == kSrcTokens) {
-      ad = a.token_adapter[u];
-      cnt = 1;
-      if (ad == -1) continue;
-      if (ad < -1 || ad >= v.n_adapters) {
-        if (crank == 0 && tid == 0) report(a.err, LORA_DERR_BAD_ADAPTER);
+  if (warp == kGProd) {
+    // ---------------- producer ----------------
+    const int n_short = a.src == kSrcSegments ? a.meta[2] : 0;
+    const int n_units = a.src == kSrcTokens ? a.T : a.meta[2] + (a.short_only ? 0 : a.meta[3]);
+    const int shift = v.page_shift;
+    const long long pmask = (1LL << shift) - 1;
+    uint32_t g = 0;  // stages posted
+    auto take_stage = [&]() -> uint32_t {
+      const uint32_t st = g % kStages;
+      if (g >= kStages && !mbar_wait(smem_u32(&empty[st]), ((g / kStages) - 1) & 1)) ok = false;
+      return st;
+    };
+    // a record without data
+    auto post_record = [&](const GRec& rc) {
+      const uint32_t st = take_stage();
+      if (lane == 0) {
+        recs[st] = rc;
+        mbar_arrive(smem_u32(&full[st]));
+      }
+      ++g;
+    };
+    // Claims: unit cid first, then units ncl + counter, CTA 0 claiming for the
+    // cluster.  Each cluster over-claims the counter exactly once; the last
+    // claim of all puts it back to zero for the next call.
+    const int n_dyn = max(0, n_units - (int)ncl);
+    int u = (int)cid;
+    int claim = 0;  // CTA 0, lane 0: the counter's answer in flight
+    if (dynamic && crank == 0 && lane == 0) claim = atomicAdd(a.counter, 1);
+    uint32_t nclaim = 0;
+    auto next_unit = [&]() {
+      if (!dynamic) {
+        u += (int)ncl;
+        return;
+      }
+      const int q = nclaim & 1;
+      if (crank == 0 && lane == 0) {
+        if (nclaim >= 2 && !mbar_wait_cluster(smem_u32(&claim_empty[q]), ((nclaim >> 1) - 1) & 1)) ok = false;
+        const int c = claim;
+        int nu;
+        if (c < n_dyn) {
+          nu = (int)ncl + c;
+          claim = atomicAdd(a.counter, 1);
+        } else {
+          nu = n_units;  // the over-claim stays in `claim`
+        }
+        for (uint32_t p = 0; p < ncta; ++p) {
+          st_dsmem_u32(mapa(smem_u32(&claim_val[q]), p), (uint32_t)nu);
+          mbar_arrive_cluster(mapa(smem_u32(&claim_full[q]), p));
+        }
+      }
+      if (!mbar_wait_cluster(smem_u32(&claim_full[q]), (nclaim >> 1) & 1)) ok = false;
+      u = claim_val[q];
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa(smem_u32(&claim_empty[q]), 0));
+      ++nclaim;
+    };
+
+    for (; u < n_units && ok; next_unit()) {
+      int ad, tb = 0, cnt;
+      if (a.src == kSrcTokens) {
+        ad = a.token_adapter[u];
+        cnt = 1;
+        if (ad == -1) continue;
+        if (ad < -1 || ad >= v.n_adapters) {
+          if (crank == 0 && lane == 0) report(a.err, LORA_DERR_BAD_ADAPTER);
+          continue;
+        }
+      } else if (u < n_short) {
+        const int s = a.short_units[u];
+        ad = a.seg_adapter[s];
+        tb = a.indptr[s];
+        cnt = a.indptr[s + 1] - tb;
+      } else {
+        const int s = a.long_units[2 * (u - n_short)];
+        const int m0 = a.long_units[2 * (u - n_short) + 1];
+        ad = a.seg_adapter[s];
+        tb = a.indptr[s] + m0;
+        cnt = min(LORA_TILE_M, a.indptr[s + 1] - tb);
+      }
+      // The first group's tokens do not depend on the adapter: load them
+      // alongside its descriptor.
+      const int first_tok = lane < min(kNT, cnt) ? (a.src == kSrcTokens ? u : a.perm[tb + lane]) : -1;
+      const lora_adapter_desc_t d = v.adapters[ad];
+      // Every CTA checks the whole adapter, so all reach the same verdict
+      // without talking to each other; the same pass caches the physical pages.
+      int bad = 0;
+      long long na = 0, nb = 0;
+      bool cached = false;
+      if (d.rank < 1 || d.rank > v.max_rank || d.rank > kHMax) {
+        bad = LORA_DERR_BAD_RANK;
+      } else {
+        const long long P = 1LL << shift;
+        na = ((long long)d.rank * v.d_in + P - 1) >> shift;
+        nb = ((long long)d.rank * v.d_out + P - 1) >> shift;
+        cached = na + nb <= kMaxPgSlots;
+        __syncwarp();  // the previous unit's page reads are done
+        int mine = 0;
+        for (long long i = lane; i < na + nb; i += 32) {
+          const long long slot = i < na ? d.a_page0 + i : d.b_page0 + (i - na);
+          long long pg = -1;
+          if (slot < 0 || slot >= v.n_page_list) {
+            mine = 1;
+          } else {
+            pg = v.page_list[slot];
+            if (pg < 0 || pg >= v.n_pages) mine = 1;
+          }
+          if (cached) pgt[i] = (int)pg;
+        }
+        if (__any_sync(0xffffffffu, mine)) bad = LORA_DERR_BAD_PAGE;
+        __syncwarp();
+      }
+      if (bad) {
+        if (crank == 0 && lane == 0) report(a.err, bad);
         continue;
       }
-    } else if (u < n_short) {
-      const int s = a.short_units[u];
-      ad = a.seg_adapter[s];
-      tb = a.indptr[s];
-      cnt = a.indptr[s + 1] - tb;
-    } else {
-      const int s = a.long_units[2 * (u - n_short)];
-      const int m0 = a.long_units[2 * (u - n_short) + 1];
-      ad = a.seg_adapter[s];
-      tb = a.indptr[s] + m0;
-      cnt = min(LORA_TILE_M, a.indptr[s + 1] - tb);
-    }
-    // The first group's token indices do not depend on the adapter: load them
-    // alongside its descriptor.
-    const int first_tok = tid < min(kNT, cnt) ? (a.src == kSrcTokens ? u : a.perm[tb + tid]) : -1;
-    const lora_adapter_desc_t d = v.adapters[ad];
-    // Every CTA checks the whole adapter, so all reach the same verdict without
-    // talking to each other; the same pass caches the physical pages.
-    int bad = 0;
-    long long na = 0, nb = 0;
-    bool cached = false;
-    if (d.rank < 1 || d.rank > v.max_rank || d.rank > kHMax) {
-      bad = LORA_DERR_BAD_RANK;
-    } else {
-      const long long P = 1LL << v.page_shift;
-      na = ((long long)d.rank * v.d_in + P - 1) >> v.page_shift;
-      nb = ((long long)d.rank * v.d_out + P - 1) >> v.page_shift;
-      cached = na + nb <= kMaxPgSlots;
-      int mine = 0;
-      for (long long i = tid; i < na + nb; i += kGThreads) {
-        const long long slot = i < na ? d.a_page0 + i : d.b_page0 + (i - na);
-        long long pg = -1;
-        if (slot < 0 || slot >= v.n_page_list) {
-          mine = 1;
-        } else {
-          pg = v.page_list[slot];
-          if (pg < 0 || pg >= v.n_pages) mine = 1;
+      const int r = d.rank;
+      const int njb = (r + kChunkRows - 1) / kChunkRows;
+      for (int g0 = 0; g0 < cnt; g0 += kNT) {
+        const int ntok = min(kNT, cnt - g0);
+        const int mytok = g0 == 0 ? first_tok : (lane < ntok ? a.perm[tb + g0 + lane] : -1);
+        GRec rc{};
+        rc.ntok = ntok;
+        rc.r = r;
+        rc.sc = d.scale;
+#pragma unroll
+        for (int t = 0; t < kNT; ++t) rc.tok[t] = __shfl_sync(0xffffffffu, mytok, t);
+        // One chunk: adapter rows [j0, j0 + nrows) of the sub-slice at col0,
+        // with the group's x (shrink) or y0 (expand) rows of the same columns
+        // when `tokens`.  Lane i copies row i as one bulk copy per page the
+        // row run touches; the copies complete as transaction bytes on the
+        // stage barrier.
+        auto post_chunk = [&](int kind, int col0, int w, int j0, int nrows, bool tokens, int first, int last,
+                              int gfirst) {
+          const uint32_t st = take_stage();
+          const uint32_t sbase = smem_u32(sm + (size_t)st * kStageBytes);
+          const uint32_t bar = smem_u32(&full[st]);
+          const bool shrink = kind == kGShrink;
+          const int ntr = tokens ? ntok : 0;
+          const uint32_t rowb = (uint32_t)w * 2;
+          if (lane == 0) {
+            GRec r2 = rc;
+            r2.kind = kind;
+            r2.j0 = j0;
+            r2.nrows = nrows;
+            r2.nvec = w >> 3;
+            r2.col0 = col0;
+            r2.first = first;
+            r2.last = last;
+            r2.gfirst = gfirst;
+            recs[st] = r2;
+            mbar_arrive_expect_tx(bar, (uint32_t)(nrows + ntr) * rowb);
+          }
+          __syncwarp();
+          const int tk = __shfl_sync(0xffffffffu, mytok, (lane - nrows) & (kNT - 1));
+          if (lane < nrows) {
+            const long long rowlen = shrink ? v.d_in : v.d_out;
+            const long long page0 = shrink ? d.a_page0 : d.b_page0;
+            const int pbase = shrink ? 0 : (int)na;
+            long long e = (long long)(j0 + lane) * rowlen + col0;
+            uint32_t dst = sbase + (uint32_t)(lane * kRowBytes);
+            for (int rem = w; rem > 0;) {
+              const long long idx = e >> shift, off = e & pmask;
+              const long long page = cached ? pgt[pbase + idx] : v.page_list[page0 + idx];
+              const int n = (int)min((long long)rem, (1LL << shift) - off);
+              bulk_g2s(dst, v.pool + (page << shift) + off, (uint32_t)n * 2, bar);
+              e += n;
+              dst += (uint32_t)n * 2;
+              rem -= n;
+            }
+          } else if (lane < nrows + ntr) {
+            const uint16_t* src = (shrink ? a.x + (long long)tk * a.ldx : a.y + (long long)tk * a.ldy) + col0;
+            bulk_g2s(sbase + (uint32_t)((kChunkRows + lane - nrows) * kRowBytes), src, rowb, bar);
+          }
+          ++g;
+        };
+        bool gfirst = true;
+        for (int ks = 0; ks < nks; ++ks) {
+          const int col0 = k0 + ks * kSub, w = min(kSub, k1 - col0);
+          for (int jb = 0; jb < njb; ++jb) {
+            post_chunk(kGShrink, col0, w, jb * kChunkRows, min(kChunkRows, r - jb * kChunkRows), true, ks == 0, 0,
+                       gfirst);
+            gfirst = false;
+          }
         }
-        if (cached) pgt[i] = (int)pg;
-      }
-      if (__syncthreads_or(mine)) bad = LORA_DERR_BAD_PAGE;
-    }
-    if (bad) {
-      if (crank == 0 && tid == 0) report(a.err, bad);
-      continue;
-    }
-
-    ChunkPlan p;
-    p.r = d.rank;
-    p.njb = (p.r + kChunkRows - 1) / kChunkRows;
-    p.k0 = k0; p.k1 = k1; p.n0 = n0; p.n1 = n1;
-    p.nks = (a.mode != kModeExpand && k1 > k0) ? (k1 - k0 + kSub - 1) / kSub : 0;
-    p.nns = (a.mode != kModeShrink && n1 > n0) ? (n1 - n0 + kSub - 1) / kSub : 0;
-    p.a_page0 = d.a_page0;
-    p.b_page0 = d.b_page0;
-    p.na = (int)na;
-    p.pgt = cached ? pgt : nullptr;
-    const float sc = d.scale;
-    const int nsh = p.nks * p.njb;
-    const int nch = nsh + p.nns * p.njb;
-
-    for (int g0 = 0; g0 < cnt; g0 += kNT) {
-      p.ntok = min(kNT, cnt - g0);
-      const int ntok = p.ntok;
-      if (tid < ntok) tok[tid] = g0 == 0 ? first_tok : a.perm[tb + g0 + tid];
-      float* hpb = hp + gbuf * kNT * kHMax;
-      for (int i = tid; i < kNT * kHMax; i += kGThreads) hpb[i] = 0.f;
-      __syncthreads();
-
-      for (int c = 0; c < min(kStages, nch); ++c)
-        issue_chunk(a, p, tok, c, sm + (size_t)c * kStageBytes, smem_u32(&bars[c]), tid);
-      bool ok = true;
-
-      // ---- shrink: partial h over this CTA's d_in slice ----
-      for (int c = 0; c < nsh; ++c) {
-        const int st = c % kStages;
-        if (!mbar_wait(smem_u32(&bars[st]), (parity >> st) & 1u)) ok = false;
-        parity ^= 1u << st;
-        const uint8_t* sb = sm + (size_t)st * kStageBytes;
-        const int ks = c / p.njb, jb = c - ks * p.njb;
-        const int nvec = min(kSub, p.k1 - (p.k0 + ks * kSub)) >> 3;
-        const int j0 = jb * kChunkRows, nrows = min(kChunkRows, p.r - j0);
-        switch (ntok) {
-          case 1: shrink_chunk<1>(sb, j0, nrows, nvec, hpb, warp, lane); break;
-          case 2: shrink_chunk<2>(sb, j0, nrows, nvec, hpb, warp, lane); break;
-          case 3: shrink_chunk<3>(sb, j0, nrows, nvec, hpb, warp, lane); break;
-          default: shrink_chunk<4>(sb, j0, nrows, nvec, hpb, warp, lane); break;
+        GRec red = rc;
+        red.kind = kGReduce;
+        red.no_k = nks == 0;
+        red.gfirst = gfirst;
+        post_record(red);
+        for (int ns = 0; ns < nns; ++ns) {
+          const int col0 = n0 + ns * kSub, w = min(kSub, n1 - col0);
+          for (int jb = 0; jb < njb; ++jb) {
+            const bool last = jb == njb - 1;
+            post_chunk(kGExpand, col0, w, jb * kChunkRows, min(kChunkRows, r - jb * kChunkRows), last, jb == 0, last,
+                       0);
+          }
         }
-        __syncthreads();
-        if (c + kStages < nch)
-          issue_chunk(a, p, tok, c + kStages, sm + (size_t)st * kStageBytes, smem_u32(&bars[st]), tid);
       }
-
-      // ---- h: cluster reduction (apply / shrink) or load (expand) ----
-      if (a.mode != kModeExpand) {
-        cluster_sync();
+    }
+    // `claim` holds this cluster's over-claim now; the last of all resets the counter
+    if (dynamic && crank == 0 && lane == 0 && claim == n_dyn + (int)ncl - 1) *a.counter = 0;
+    {
+      GRec end{};
+      end.kind = kGEnd;
+      post_record(end);
+    }
+    if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
+  } else {
+    // ---------------- consumers ----------------
+    const int ctid = tid;  // 0 .. 255
+    uint32_t ngroup = 0, ncons = 0;
+    auto cons_sync = [&]() {  // the 8 consumer warps, bounded
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(cons));
+      if (!mbar_wait(smem_u32(cons), ncons & 1)) ok = false;
+      ++ncons;
+    };
+    for (uint32_t g = 0;; ++g) {
+      const uint32_t st = g % kStages;
+      if (!mbar_wait(smem_u32(&full[st]), (g / kStages) & 1)) {
+        ok = false;
+        break;
+      }
+      const GRec& rc = recs[st];  // stable until this stage is released
+      if (rc.kind == kGEnd) break;
+      const uint8_t* sb = sm + (size_t)st * kStageBytes;
+      const int b = ngroup & 1;
+      float* hpb = hp + b * kNT * kHMax;
+      if (rc.gfirst && reduce_h && ngroup >= 2 &&
+          !mbar_wait_cluster(smem_u32(&hp_free[b]), ((ngroup >> 1) - 1) & 1))
+        ok = false;
+      if (rc.kind == kGShrink) {
+        switch (rc.ntok) {
+          case 1: shrink_chunk<1>(sb, rc.j0, rc.nrows, rc.nvec, rc.first, hpb, warp, lane); break;
+          case 2: shrink_chunk<2>(sb, rc.j0, rc.nrows, rc.nvec, rc.first, hpb, warp, lane); break;
+          case 3: shrink_chunk<3>(sb, rc.j0, rc.nrows, rc.nvec, rc.first, hpb, warp, lane); break;
+          default: shrink_chunk<4>(sb, rc.j0, rc.nrows, rc.nvec, rc.first, hpb, warp, lane); break;
+        }
+      } else if (rc.kind == kGExpand) {
+        expand_chunk(a, sb, hs, eacc, rc, ok, warp, lane);
+      } else if (reduce_h) {  // kGReduce: h of the group from the cluster's partials
+        if (rc.no_k)
+          for (int i = ctid; i < rc.ntok * rc.r; i += kGConsThreads) hpb[(i / rc.r) * kHMax + i % rc.r] = 0.f;
+        cons_sync();  // this CTA's partial is complete
+        if (ctid == 0)
+          for (uint32_t p = 0; p < ncta; ++p) mbar_arrive_cluster(mapa(smem_u32(&hp_ready[b]), p));
+        if (!mbar_wait_cluster(smem_u32(&hp_ready[b]), (ngroup >> 1) & 1)) ok = false;
         const uint32_t hp_addr = smem_u32(hpb);
-        for (int i = tid; i < ntok * p.r; i += kGThreads) {
-          const int t = i / p.r, j = i - t * p.r;
+        for (int i = ctid; i < rc.ntok * rc.r; i += kGConsThreads) {
+          const int t = i / rc.r, j = i - t * rc.r;
           const uint32_t off = (uint32_t)((t * kHMax + j) * sizeof(float));
-          // all peers' loads in flight first, then the sum in fixed CTA order
+          // every peer's load in flight first, then the sum in fixed CTA order
           float part[kMaxCluster];
 #pragma unroll
           for (int c = 0; c < kMaxCluster; ++c)
@@ -395,43 +535,28 @@ __global__ void __launch_bounds__(kGThreads, 3) gather_kernel(const __grid_const
 #pragma unroll
           for (int c = 0; c < kMaxCluster; ++c)
             if ((uint32_t)c < ncta) sum += part[c];
-          hs[t * kHMax + j] = a.mode == kModeApply ? sc * sum : sum;
+          hs[t * kHMax + j] = a.mode == kModeApply ? rc.sc * sum : sum;
+          if (a.mode == kModeShrink && ok && (uint32_t)t % ncta == crank) a.h[(long long)rc.tok[t] * a.ldh + j] = sum;
         }
-        __syncthreads();
-        if (a.mode == kModeShrink && ok) {
-          for (int i = tid; i < ntok * p.r; i += kGThreads) {
-            const int t = i / p.r, j = i - t * p.r;
-            if ((uint32_t)t % ncta == crank) a.h[(long long)tok[t] * a.ldh + j] = hs[t * kHMax + j];
-          }
+        cons_sync();  // h complete here; this CTA is done reading the peers' partials
+        if (ctid == 0)
+          for (uint32_t p = 0; p < ncta; ++p) mbar_arrive_cluster(mapa(smem_u32(&hp_free[b]), p));
+        ++ngroup;
+      } else {  // kGReduce: h of the group from the caller
+        cons_sync();  // every warp is done with the previous group's h
+        for (int i = ctid; i < rc.ntok * rc.r; i += kGConsThreads) {
+          const int t = i / rc.r, j = i - t * rc.r;
+          hs[t * kHMax + j] = rc.sc * a.h[(long long)rc.tok[t] * a.ldh + j];
         }
-      } else {
-        for (int i = tid; i < ntok * p.r; i += kGThreads) {
-          const int t = i / p.r, j = i - t * p.r;
-          hs[t * kHMax + j] = sc * a.h[(long long)tok[t] * a.ldh + j];
-        }
-        __syncthreads();
+        cons_sync();
       }
-
-      // ---- expand: y over this CTA's d_out slice ----
-      for (int c = nsh; c < nch; ++c) {
-        const int st = c % kStages;
-        if (!mbar_wait(smem_u32(&bars[st]), (parity >> st) & 1u)) ok = false;
-        parity ^= 1u << st;
-        const uint8_t* sb = sm + (size_t)st * kStageBytes;
-        const int ns = (c - nsh) / p.njb, jb = (c - nsh) - ns * p.njb;
-        const int col0 = p.n0 + ns * kSub;
-        const int nvec = min(kSub, p.n1 - col0) >> 3;
-        const int j0 = jb * kChunkRows, nrows = min(kChunkRows, p.r - j0);
-        expand_chunk(a, sb, hs, eacc, tok, ntok, nvec, j0, nrows, jb == 0, jb == p.njb - 1, col0, ok, warp, lane);
-        __syncthreads();
-        if (c + kStages < nch)
-          issue_chunk(a, p, tok, c + kStages, sm + (size_t)st * kStageBytes, smem_u32(&bars[st]), tid);
-      }
-      if (!ok && tid == 0) report(a.err, LORA_DERR_TIMEOUT);
-      gbuf ^= 1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
     }
+    if (!ok && ctid == 0) report(a.err, LORA_DERR_TIMEOUT);
   }
-  // No CTA may leave while a peer can still read its partials.
+  // No CTA may leave while a peer can still read its partials or arrive on
+  // its barriers.
   cluster_sync();
 }
 
@@ -461,6 +586,7 @@ lora_status_t launch_gather(int mode, int src, int short_only, const void* x, lo
   a.short_units = seg ? seg->short_units : nullptr;
   a.long_units = seg ? seg->long_units : nullptr;
   a.meta = seg ? seg->meta : nullptr;
+  a.counter = seg ? seg->meta + 7 : nullptr;
   a.token_adapter = token_adapter;
   a.T = T;
   a.err = err;
@@ -470,8 +596,17 @@ lora_status_t launch_gather(int mode, int src, int short_only, const void* x, lo
 
   const int upper = src == kSrcTokens ? T : seg->T + (short_only ? 0 : seg->max_long_units);
   if (upper <= 0) return LORA_OK;
-  const int cl = cluster_size_for(view);
-  int cap = sm_count() * 3 / cl;
+  // The widest cluster whose clusters take every unit at once (halving from the
+  // width the slices want); if none does, the full width.
+  const int cl0 = cluster_size_for(view);
+  int cl = cl0;
+  for (int c = cl0; c >= 2; c /= 2) {
+    if (upper <= sm_count() * 2 / c) {
+      cl = c;
+      break;
+    }
+  }
+  int cap = sm_count() * 2 / cl;
   if (cap < 1) cap = 1;
   const int n_clusters = upper < cap ? upper : cap;
 

@@ -537,3 +537,25 @@ def test_tc_single_full_tile():
         ref, _ = oracle.lora_apply(batch.x, batch.y0, batch.ids, pool)
         assert err == 0
         compare_bf16(y[:, :4096], ref, "single tile mode %d" % mode)
+
+
+def test_gather_multi_token_units_mixed_subslice_widths():
+    """d = 5120 gives every CTA of an 8-CTA cluster a 512- and a 128-column sub-slice;
+    units of 2..8 tokens with ranks 32 and 64 use the expand accumulator across both.
+    Repeated runs: the warps of a CTA meet at no barrier between chunks, so a warp
+    that owned another warp's accumulator entries would show up as a varying error."""
+    rng = np.random.default_rng(32)
+    ranks = [32, 64, 48, 32, 64, 16, 40]
+    counts = [3, 2, 4, 5, 8, 3, 7]
+    ids = np.concatenate([np.full(n, i, dtype=np.int32) for i, n in enumerate(counts)])
+    ids = ids[rng.permutation(ids.size)]
+    pool = W.build_pool(rng, 5120, 5120, ranks, max_rank=64)
+    batch = W.make_batch(rng, ids, 5120, 5120)
+    ref, _ = oracle.lora_apply(batch.x, batch.y0, ids, pool)
+    first = None
+    for rep in range(4):
+        y, err, _ = run_apply(batch, pool, B.LORA_SEG_GROUP, len(ranks))
+        assert err == 0
+        compare_bf16(y, ref, "gather 5120x5120, run %d" % rep)
+        first = y if first is None else first
+        assert np.array_equal(y, first)
