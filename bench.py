@@ -1,11 +1,13 @@
 #!/usr/bin/env python
 """Benchmark of the multi-adapter LoRA path on one GB300 (or N, one process each).
 
-A step is one pass of the whole path over one batch: lora_segments_build (grouping
-the batch's tokens by adapter, work lists) followed by lora_apply (gather + shrink
-+ scale + expand through the page table, in place in y).  The default workload is
-the decode batch: 64 tokens (one per request), q_proj 4096 -> 4096, 100 rank-16
-adapters, uniformly random adapter per token.
+A step is one pass of the whole path over one batch.  For the decode batch (one
+token per request) that is lora_bgmv: every token gathers its own adapter through
+the page table, shrink + scale + expand in place in y, one kernel.  For batches
+with segments it is lora_segments_build (grouping the batch's tokens by adapter,
+work lists) followed by lora_apply.  The default workload is the decode batch: 64
+tokens, q_proj 4096 -> 4096, 100 rank-16 adapters, uniformly random adapter per
+token.
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU fp64 oracle on the
 same workload instead (the reference arm of this build: there is no runnable
@@ -167,19 +169,20 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
-def profile_traffic(kernel_key: str, workload: str, current_hash: str):
-    """DRAM bytes per launch from the committed ncu summary, or None if absent or if the
-    kernel's sources changed since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+def profile_traffic(call: str, workload: str, current_hash: str):
+    """DRAM bytes (read + write) per call from the table in profiles/traffic.md (rows
+    `| call | workload | kernel sources hash | bytes | ...`), or None if there is no row
+    or the kernel sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
     try:
         with open(path) as f:
-            d = json.load(f)
-        e = d[kernel_key][workload]
-        if e.get("source_hash") != current_hash:
-            return None
-        return float(e["dram_bytes_per_launch"])
-    except Exception:
+            for line in f:
+                cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
+                if len(cells) >= 4 and cells[0] == call and cells[1] == workload:
+                    return float(cells[3]) if cells[2] == current_hash else None
+    except (OSError, ValueError):
         return None
+    return None
 
 
 # --------------------------------------------------------------- workloads --
@@ -244,10 +247,15 @@ def run_ours(args, world, rank, local):
     mode = sets[0]["wl"].mode
     n_ad = sets[0]["wl"].n_adapters
 
+    bgmv = args.workload == "decode"
+
     def step(k):
         S = sets[k % n_sets]
-        B.lora_segments_build(S["ids"], n_ad, S["seg"], mode=mode, err=err)
-        B.lora_apply(S["x"], S["y"], S["seg"], S["view"], err=err)
+        if bgmv:
+            B.lora_bgmv(S["x"], S["y"], S["ids"], S["view"], err=err)
+        else:
+            B.lora_segments_build(S["ids"], n_ad, S["seg"], mode=mode, err=err)
+            B.lora_apply(S["x"], S["y"], S["seg"], S["view"], err=err)
 
     # warm-up (eager), then a CUDA graph of one pass over all sets.
     for k in range(max(args.warmup, 3)):
@@ -256,9 +264,11 @@ def run_ours(args, world, rank, local):
     g_steps = n_sets * max(1, 64 // n_sets)
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream(device=dev)
+    launches0 = B.launch_count()
     with torch.cuda.graph(graph, stream=cap):
         for k in range(g_steps):
             step(k)
+    launches_per_step = (B.launch_count() - launches0) / g_steps
     rem = args.steps % g_steps
     graph_rem = None
     if rem:
@@ -304,29 +314,46 @@ def run_ours(args, world, rank, local):
     total_tokens = sum_over_ranks(tokens_timed, world)
     value = total_tokens / (ms / 1e3)
 
-    # ---- per-launch duration of the dominant kernel (the fused apply) ----
-    # The stream is held by a sleep kernel while the host queues every launch, so
-    # the events bracket GPU execution only.
-    n_k = min(args.steps, 4 * g_steps)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_k)]
-    torch.cuda.synchronize()
-    torch.cuda._sleep(int(2e8))
-    for k in range(n_k):
+    # ---- per-call duration of the dominant call (lora_bgmv / lora_apply) ----
+    # A CUDA graph of that call alone (segments built beforehand for every set),
+    # replayed back to back and bracketed by CUDA events on the launching stream.
+    if not bgmv:
+        for S in sets:
+            B.lora_segments_build(S["ids"], n_ad, S["seg"], mode=mode, err=err)
+        torch.cuda.synchronize()
+
+    def one_call(k):
         S = sets[k % n_sets]
-        B.lora_segments_build(S["ids"], n_ad, S["seg"], mode=mode, err=err)
-        evs[k][0].record()
-        B.lora_apply(S["x"], S["y"], S["seg"], S["view"], err=err)
-        evs[k][1].record()
+        if bgmv:
+            B.lora_bgmv(S["x"], S["y"], S["ids"], S["view"], err=err)
+        else:
+            B.lora_apply(S["x"], S["y"], S["seg"], S["view"], err=err)
+
+    call_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(call_graph, stream=cap):
+        for k in range(g_steps):
+            one_call(k)
+    call_graph.replay()
     torch.cuda.synchronize()
-    apply_ms = [a.elapsed_time(b) for a, b in evs]
+    call_reps = max(1, min(reps, int(0.2 / max(ms / args.steps / 1e3 * g_steps, 1e-9))))
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record()
+    for _ in range(call_reps):
+        call_graph.replay()
+    c1.record()
+    torch.cuda.synchronize()
+    n_k = call_reps * g_steps
+    apply_ms = [c0.elapsed_time(c1) / n_k]
     apply_avg_s = statistics.fmean(apply_ms) / 1e3
-    bytes_avg = statistics.fmean(sets[k % n_sets]["bytes"] for k in range(n_k))
-    flops_avg = statistics.fmean(sets[k % n_sets]["flops"] for k in range(n_k))
+    bytes_avg = statistics.fmean(sets[k % n_sets]["bytes"] for k in range(g_steps))
+    flops_avg = statistics.fmean(sets[k % n_sets]["flops"] for k in range(g_steps))
     hbm_peak, tc_peak, peak_kind = read_peaks()
     achieved_gbs = bytes_avg / apply_avg_s / 1e9
     csrc = os.path.join(ROOT, "segmented_gather_gemm_lora_gb300", "csrc")
     kernel_hash = source_hash([os.path.join(csrc, f) for f in sorted(os.listdir(csrc))])
-    traffic = profile_traffic("lora_apply", args.workload, kernel_hash)
+    call = "lora_bgmv" if bgmv else "lora_apply"
+    traffic = profile_traffic(call, args.workload, kernel_hash)
 
     # ---- end to end: host buffers in, result out, through the public API ----
     S0 = sets[0]
@@ -343,8 +370,11 @@ def run_ours(args, world, rank, local):
         dx.copy_(hx, non_blocking=True)
         dy.copy_(hy0, non_blocking=True)
         S0["ids"].copy_(hids, non_blocking=True)
-        B.lora_segments_build(S0["ids"], n_ad, S0["seg"], mode=mode, err=err)
-        B.lora_apply(S0["x"], S0["y"], S0["seg"], S0["view"], err=err)
+        if bgmv:
+            B.lora_bgmv(S0["x"], S0["y"], S0["ids"], S0["view"], err=err)
+        else:
+            B.lora_segments_build(S0["ids"], n_ad, S0["seg"], mode=mode, err=err)
+            B.lora_apply(S0["x"], S0["y"], S0["seg"], S0["view"], err=err)
         hy.copy_(dy, non_blocking=True)
 
     for _ in range(3):
@@ -376,15 +406,15 @@ def run_ours(args, world, rank, local):
         "config": {
             "workload": WORKLOAD_TEXT[args.workload],
             "tokens_per_step": tokens_per_step,
-            "segments": "GROUP" if mode == 0 else "CONTIGUOUS",
-            "step": "lora_segments_build + lora_apply",
+            "segments": "none (one token per request)" if bgmv else ("GROUP" if mode == 0 else "CONTIGUOUS"),
+            "step": "lora_bgmv" if bgmv else "lora_segments_build + lora_apply",
             "l2": "inputs larger than L2: %d rotating input sets (%.0f MB in all, L2 %.0f MB)"
                   % (n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
             "timing": "CUDA graph of %d steps replayed; CUDA events on the launching stream" % g_steps,
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "lora_apply (gather_kernel)",
+            "kernel": "lora_bgmv (gather_kernel)" if bgmv else "lora_apply (gather, shrink_tc, reduce_partials, expand_tc)",
             "achieved": achieved_gbs,
             "peak": hbm_peak,
             "unit": "GB/s",
@@ -396,7 +426,7 @@ def run_ours(args, world, rank, local):
             "tflops": flops_avg / apply_avg_s / 1e12,
         },
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": int(round(launches_per_step * args.steps)),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
     }

@@ -242,6 +242,14 @@ lora_status_t lora_apply_fixed_scratch(const void* x, int64_t ldx, void* y, int6
                                        int32_t* dev_err, lora_stream_t stream);
 
 /**
+ * Kernels this library has launched in this process so far, on every device
+ * and stream (a host-side count, incremented at each launch; a launch recorded
+ * into a CUDA graph counts once, when it is recorded).  Diagnostic only: lets a
+ * caller check how many kernels one call issues.
+ */
+uint64_t lora_launch_count(void);
+
+/**
  * Pages one adapter of rank r occupies in a pool of page_elems-element pages:
  * ceil(r * d_in / page_elems) + ceil(r * d_out / page_elems) (bytes per matrix
  * pair (d_in * r + r * d_out) * 2 before rounding to pages: "Multi-LoRA

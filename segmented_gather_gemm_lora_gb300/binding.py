@@ -46,6 +46,7 @@ EXPORTED = (
     "lora_pool_pages_needed",
     "lora_status_string",
     "lora_abi_version",
+    "lora_launch_count",
 )
 
 
@@ -87,6 +88,8 @@ def lib():
         path = _build.build()
         L = ctypes.CDLL(path)
         vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        L.lora_launch_count.restype = ctypes.c_uint64
+        L.lora_launch_count.argtypes = []
         L.lora_segments_buffer_bytes.restype = sz
         L.lora_segments_buffer_bytes.argtypes = [i32]
         L.lora_segments_carve.restype = i32
@@ -263,6 +266,11 @@ def lora_apply_fixed_scratch(x: torch.Tensor, y: torch.Tensor, seg: Segments, vi
     _check(lib().lora_apply_fixed_scratch(_ptr(x), _ld(x), _ptr(y), _ld(y), ctypes.byref(seg.c),
                                           ctypes.byref(view.c), _ptr(err), _stream(stream)),
            "lora_apply_fixed_scratch")
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process (a recorded graph counts once)."""
+    return int(lib().lora_launch_count())
 
 
 def lora_bgmv(x: torch.Tensor, y: torch.Tensor, token_adapter: torch.Tensor, view: PoolView,

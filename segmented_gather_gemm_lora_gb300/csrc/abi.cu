@@ -2,6 +2,7 @@
 // stream.  Nothing here allocates device memory or synchronises.
 #include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -94,6 +95,47 @@ cudaError_t ensure_smem_attr(const void* func, size_t bytes) {
   return e;
 }
 
+std::atomic<uint64_t> g_launches{0};
+
+int max_active_clusters(const void* func, int block, size_t smem, int cluster_x) {
+  struct Entry {
+    int dev;
+    const void* func;
+    int block;
+    size_t smem;
+    int cluster_x;
+    int n;
+  };
+  static std::mutex mu;
+  static Entry cache[32];
+  static int n_cache = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_cache; ++i) {
+    const Entry& e = cache[i];
+    if (e.dev == dev && e.func == func && e.block == block && e.smem == smem && e.cluster_x == cluster_x) return e.n;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cluster_x);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)cluster_x;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 1;
+  }
+  if (n_cache < 32) cache[n_cache++] = Entry{dev, func, block, smem, cluster_x, n};
+  return n;
+}
+
 cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, int cluster_x,
                        void* args) {
   cudaLaunchConfig_t cfg = {};
@@ -116,7 +158,9 @@ cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cud
   cfg.attrs = attr;
   cfg.numAttrs = n;
   void* params[1] = {args};
-  return cudaLaunchKernelExC(&cfg, func, params);
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, func, params);
+  if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return e;
 }
 
 int sm_count() {
@@ -302,3 +346,5 @@ lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy, const 
 }
 
 }  // extern "C"
+
+extern "C" uint64_t lora_launch_count(void) { return lora::g_launches.load(std::memory_order_relaxed); }

@@ -57,21 +57,28 @@ constexpr int kStageBytes = (kChunkRows + kNT) * kRowBytes;  // 20 KB
 constexpr int kMaxPgSlots = 512;  // page-list slots of one adapter cached in shared memory
 
 enum GKind { kGShrink = 0, kGExpand = 1, kGReduce = 2, kGEnd = 3 };
+enum GFlag {
+  kFFirst = 1,   // shrink: first sub-slice (store, not add); expand: first row block of the sub-slice
+  kFLast = 2,    // expand: last row block of the sub-slice (adds y0, writes y; token rows staged)
+  kFGFirst = 4,  // first record of the group: the partial-h buffer is reused once peers are done
+  kFRed = 8,     // after this record: h of the group from the cluster's partials
+  kFHLoad = 16,  // before this record: h of the group from the caller
+  kFNoK = 32     // this CTA has no d_in slice (its partial is zero)
+};
 
-// What the producer tells the consumers about a stage.
+// What the producer tells the consumers about a stage.  The group's reduction
+// rides on its last shrink chunk, so only a CTA without a d_in slice spends a
+// stage on a record without data.
 struct GRec {
   int kind;
-  int ntok;    // tokens of the group
-  int j0;      // first adapter row of the chunk
-  int nrows;   // adapter rows of the chunk
-  int nvec;    // 16-byte pieces per row of the sub-slice
-  int col0;    // first column of the sub-slice
-  int first;   // shrink: first sub-slice (store, not add); expand: first row block of the sub-slice
-  int last;    // expand: last row block of the sub-slice (adds y0, writes y; token rows staged)
-  int gfirst;  // first record of the group: the partial-h buffer is reused once peers are done
-  int r;       // rank
-  float sc;    // scale
-  int no_k;    // reduce: this CTA has no d_in slice (its partial is zero)
+  int ntok;   // tokens of the group
+  int j0;     // first adapter row of the chunk
+  int nrows;  // adapter rows of the chunk
+  int nvec;   // 16-byte pieces per row of the sub-slice
+  int col0;   // first column of the sub-slice
+  int flags;  // GFlag bits
+  int r;      // rank
+  float sc;   // scale
   int tok[kNT];
 };
 static_assert(sizeof(GRec) <= 64, "record slot");
@@ -203,12 +210,12 @@ __device__ __forceinline__ void expand_chunk(const GatherArgs& a, const uint8_t*
     }
     if (act && g == 0) {
       float4* ea = reinterpret_cast<float4*>(eacc + (t * kSub + vv * 8));
-      if (!rc.first) {
+      if (!(rc.flags & kFFirst)) {
         const float4 e0 = ea[0], e1 = ea[1];
         o[0] = e0.x + o[0]; o[1] = e0.y + o[1]; o[2] = e0.z + o[2]; o[3] = e0.w + o[3];
         o[4] = e1.x + o[4]; o[5] = e1.y + o[5]; o[6] = e1.z + o[6]; o[7] = e1.w + o[7];
       }
-      if (!rc.last) {
+      if (!(rc.flags & kFLast)) {
         ea[0] = make_float4(o[0], o[1], o[2], o[3]);
         ea[1] = make_float4(o[4], o[5], o[6], o[7]);
       } else if (ok) {
@@ -406,8 +413,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         // when `tokens`.  Lane i copies row i as one bulk copy per page the
         // row run touches; the copies complete as transaction bytes on the
         // stage barrier.
-        auto post_chunk = [&](int kind, int col0, int w, int j0, int nrows, bool tokens, int first, int last,
-                              int gfirst) {
+        auto post_chunk = [&](int kind, int col0, int w, int j0, int nrows, bool tokens, int flags) {
           const uint32_t st = take_stage();
           const uint32_t sbase = smem_u32(sm + (size_t)st * kStageBytes);
           const uint32_t bar = smem_u32(&full[st]);
@@ -421,9 +427,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
             r2.nrows = nrows;
             r2.nvec = w >> 3;
             r2.col0 = col0;
-            r2.first = first;
-            r2.last = last;
-            r2.gfirst = gfirst;
+            r2.flags = flags;
             recs[st] = r2;
             mbar_arrive_expect_tx(bar, (uint32_t)(nrows + ntr) * rowb);
           }
@@ -450,26 +454,26 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
           }
           ++g;
         };
-        bool gfirst = true;
         for (int ks = 0; ks < nks; ++ks) {
           const int col0 = k0 + ks * kSub, w = min(kSub, k1 - col0);
           for (int jb = 0; jb < njb; ++jb) {
-            post_chunk(kGShrink, col0, w, jb * kChunkRows, min(kChunkRows, r - jb * kChunkRows), true, ks == 0, 0,
-                       gfirst);
-            gfirst = false;
+            const int f = (ks == 0 ? kFFirst : 0) | (ks == 0 && jb == 0 ? kFGFirst : 0) |
+                          (ks == nks - 1 && jb == njb - 1 ? kFRed : 0);
+            post_chunk(kGShrink, col0, w, jb * kChunkRows, min(kChunkRows, r - jb * kChunkRows), true, f);
           }
         }
-        GRec red = rc;
-        red.kind = kGReduce;
-        red.no_k = nks == 0;
-        red.gfirst = gfirst;
-        post_record(red);
+        if (reduce_h && nks == 0) {
+          GRec red = rc;
+          red.kind = kGReduce;
+          red.flags = kFGFirst | kFRed | kFNoK;
+          post_record(red);
+        }
         for (int ns = 0; ns < nns; ++ns) {
           const int col0 = n0 + ns * kSub, w = min(kSub, n1 - col0);
           for (int jb = 0; jb < njb; ++jb) {
             const bool last = jb == njb - 1;
-            post_chunk(kGExpand, col0, w, jb * kChunkRows, min(kChunkRows, r - jb * kChunkRows), last, jb == 0, last,
-                       0);
+            const int f = (jb == 0 ? kFFirst : 0) | (last ? kFLast : 0) | (!reduce_h && ns == 0 && jb == 0 ? kFHLoad : 0);
+            post_chunk(kGExpand, col0, w, jb * kChunkRows, min(kChunkRows, r - jb * kChunkRows), last, f);
           }
         }
       }
@@ -503,22 +507,22 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       const uint8_t* sb = sm + (size_t)st * kStageBytes;
       const int b = ngroup & 1;
       float* hpb = hp + b * kNT * kHMax;
-      if (rc.gfirst && reduce_h && ngroup >= 2 &&
+      if ((rc.flags & kFGFirst) && reduce_h && ngroup >= 2 &&
           !mbar_wait_cluster(smem_u32(&hp_free[b]), ((ngroup >> 1) - 1) & 1))
         ok = false;
       if (rc.kind == kGShrink) {
+        const bool store = rc.flags & kFFirst;
         switch (rc.ntok) {
-          case 1: shrink_chunk<1>(sb, rc.j0, rc.nrows, rc.nvec, rc.first, hpb, warp, lane); break;
-          case 2: shrink_chunk<2>(sb, rc.j0, rc.nrows, rc.nvec, rc.first, hpb, warp, lane); break;
-          case 3: shrink_chunk<3>(sb, rc.j0, rc.nrows, rc.nvec, rc.first, hpb, warp, lane); break;
-          default: shrink_chunk<4>(sb, rc.j0, rc.nrows, rc.nvec, rc.first, hpb, warp, lane); break;
+          case 1: shrink_chunk<1>(sb, rc.j0, rc.nrows, rc.nvec, store, hpb, warp, lane); break;
+          case 2: shrink_chunk<2>(sb, rc.j0, rc.nrows, rc.nvec, store, hpb, warp, lane); break;
+          case 3: shrink_chunk<3>(sb, rc.j0, rc.nrows, rc.nvec, store, hpb, warp, lane); break;
+          default: shrink_chunk<4>(sb, rc.j0, rc.nrows, rc.nvec, store, hpb, warp, lane); break;
         }
-      } else if (rc.kind == kGExpand) {
-        expand_chunk(a, sb, hs, eacc, rc, ok, warp, lane);
-      } else if (reduce_h) {  // kGReduce: h of the group from the cluster's partials
-        if (rc.no_k)
+      }
+      if (rc.flags & kFRed) {  // h of the group from the cluster's partials
+        if (rc.flags & kFNoK)
           for (int i = ctid; i < rc.ntok * rc.r; i += kGConsThreads) hpb[(i / rc.r) * kHMax + i % rc.r] = 0.f;
-        cons_sync();  // this CTA's partial is complete
+        cons_sync();  // this CTA's partial is complete, and every warp is done with the previous h
         if (ctid == 0)
           for (uint32_t p = 0; p < ncta; ++p) mbar_arrive_cluster(mapa(smem_u32(&hp_ready[b]), p));
         if (!mbar_wait_cluster(smem_u32(&hp_ready[b]), (ngroup >> 1) & 1)) ok = false;
@@ -542,7 +546,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         if (ctid == 0)
           for (uint32_t p = 0; p < ncta; ++p) mbar_arrive_cluster(mapa(smem_u32(&hp_free[b]), p));
         ++ngroup;
-      } else {  // kGReduce: h of the group from the caller
+      }
+      if (rc.flags & kFHLoad) {  // h of the group from the caller
         cons_sync();  // every warp is done with the previous group's h
         for (int i = ctid; i < rc.ntok * rc.r; i += kGConsThreads) {
           const int t = i / rc.r, j = i - t * rc.r;
@@ -550,6 +555,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         }
         cons_sync();
       }
+      if (rc.kind == kGExpand) expand_chunk(a, sb, hs, eacc, rc, ok, warp, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
     }
@@ -596,21 +602,19 @@ lora_status_t launch_gather(int mode, int src, int short_only, const void* x, lo
 
   const int upper = src == kSrcTokens ? T : seg->T + (short_only ? 0 : seg->max_long_units);
   if (upper <= 0) return LORA_OK;
-  // The widest cluster whose clusters take every unit at once (halving from the
-  // width the slices want); if none does, the full width.
+  if (ensure_smem_attr((const void*)gather_kernel, kGatherSmem) != cudaSuccess) return LORA_ERR_CUDA;
+  // The widest cluster whose resident clusters take every unit at once
+  // (halving from the width the slices want); if none does, the full width.
   const int cl0 = cluster_size_for(view);
   int cl = cl0;
   for (int c = cl0; c >= 2; c /= 2) {
-    if (upper <= sm_count() * 2 / c) {
+    if (upper <= max_active_clusters((const void*)gather_kernel, kGThreads, kGatherSmem, c)) {
       cl = c;
       break;
     }
   }
-  int cap = sm_count() * 2 / cl;
-  if (cap < 1) cap = 1;
+  const int cap = max_active_clusters((const void*)gather_kernel, kGThreads, kGatherSmem, cl);
   const int n_clusters = upper < cap ? upper : cap;
-
-  if (ensure_smem_attr((const void*)gather_kernel, kGatherSmem) != cudaSuccess) return LORA_ERR_CUDA;
   return launch_pdl((const void*)gather_kernel, dim3((unsigned)(n_clusters * cl)), dim3(kGThreads), kGatherSmem,
                     stream, cl, &a) == cudaSuccess
              ? LORA_OK

@@ -24,6 +24,11 @@ cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cud
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
+// Clusters of `cluster_x` CTAs of `func` (block threads, smem dynamic bytes,
+// its shared-memory attribute already raised) that the current device holds
+// at once (cached).
+int max_active_clusters(const void* func, int block, size_t smem, int cluster_x);
+
 // Fill a DevView from a validated host view.
 void make_dev_view(const lora_pool_view_t* v, DevView* out);
 
