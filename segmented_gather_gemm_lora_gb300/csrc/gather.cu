@@ -317,19 +317,24 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         return;
       }
       const int q = nclaim & 1;
-      if (crank == 0 && lane == 0) {
-        if (nclaim >= 2 && !mbar_wait_cluster(smem_u32(&claim_empty[q]), ((nclaim >> 1) - 1) & 1)) ok = false;
-        const int c = claim;
-        int nu;
-        if (c < n_dyn) {
-          nu = (int)ncl + c;
-          claim = atomicAdd(a.counter, 1);
-        } else {
-          nu = n_units;  // the over-claim stays in `claim`
+      if (crank == 0) {
+        int nu = 0;
+        if (lane == 0) {
+          if (nclaim >= 2 && !mbar_wait_cluster(smem_u32(&claim_empty[q]), ((nclaim >> 1) - 1) & 1)) ok = false;
+          const int c = claim;
+          if (c < n_dyn) {
+            nu = (int)ncl + c;
+            claim = atomicAdd(a.counter, 1);
+          } else {
+            nu = n_units;  // the over-claim stays in `claim`
+          }
         }
-        for (uint32_t p = 0; p < ncta; ++p) {
-          st_dsmem_u32(mapa(smem_u32(&claim_val[q]), p), (uint32_t)nu);
-          mbar_arrive_cluster(mapa(smem_u32(&claim_full[q]), p));
+        nu = __shfl_sync(0xffffffffu, nu, 0);
+        __syncwarp();  // lane 0 saw every CTA done with this slot before any lane rewrites it
+        // lane p hands the claim to CTA p
+        if (lane < (int)ncta) {
+          st_dsmem_u32(mapa(smem_u32(&claim_val[q]), (uint32_t)lane), (uint32_t)nu);
+          mbar_arrive_cluster(mapa(smem_u32(&claim_full[q]), (uint32_t)lane));
         }
       }
       if (!mbar_wait_cluster(smem_u32(&claim_full[q]), (nclaim >> 1) & 1)) ok = false;
@@ -523,8 +528,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         if (rc.flags & kFNoK)
           for (int i = ctid; i < rc.ntok * rc.r; i += kGConsThreads) hpb[(i / rc.r) * kHMax + i % rc.r] = 0.f;
         cons_sync();  // this CTA's partial is complete, and every warp is done with the previous h
-        if (ctid == 0)
-          for (uint32_t p = 0; p < ncta; ++p) mbar_arrive_cluster(mapa(smem_u32(&hp_ready[b]), p));
+        // lane p of warp 0 signals CTA p: the cluster-scope releases run side by side
+        if (ctid < (int)ncta) mbar_arrive_cluster(mapa(smem_u32(&hp_ready[b]), (uint32_t)ctid));
         if (!mbar_wait_cluster(smem_u32(&hp_ready[b]), (ngroup >> 1) & 1)) ok = false;
         const uint32_t hp_addr = smem_u32(hpb);
         for (int i = ctid; i < rc.ntok * rc.r; i += kGConsThreads) {
@@ -543,8 +548,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
           if (a.mode == kModeShrink && ok && (uint32_t)t % ncta == crank) a.h[(long long)rc.tok[t] * a.ldh + j] = sum;
         }
         cons_sync();  // h complete here; this CTA is done reading the peers' partials
-        if (ctid == 0)
-          for (uint32_t p = 0; p < ncta; ++p) mbar_arrive_cluster(mapa(smem_u32(&hp_free[b]), p));
+        if (ctid < (int)ncta) mbar_arrive_cluster(mapa(smem_u32(&hp_free[b]), (uint32_t)ctid));
         ++ngroup;
       }
       if (rc.flags & kFHLoad) {  // h of the group from the caller
