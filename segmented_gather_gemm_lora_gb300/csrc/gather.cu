@@ -179,12 +179,14 @@ __device__ __forceinline__ void shrink_chunk(const uint8_t* sb, int j0, int nrow
 // row-quarter sums meet in a fixed two-step butterfly, and chunk sums
 // accumulate in chunk order in eacc.  The sub-slice's last chunk adds y0 and
 // writes y.
-__device__ __forceinline__ void expand_chunk(const GatherArgs& a, const uint8_t* sb, const float* hs, float* eacc,
-                                             const GRec& rc, bool ok, int warp, int lane) {
+__device__ __forceinline__ void expand_chunk(uint16_t* ybase, long long ldy, const uint8_t* sb, const float* hs,
+                                             float* eacc, const GRec& rc, bool ok, int warp, int lane) {
   const int nblk = (rc.nvec + 7) >> 3;
   if (warp >= nblk) return;
   const int g = lane >> 3, u = lane & 7;
-  for (int t = 0; t < rc.ntok; ++t) {
+#pragma unroll
+  for (int t = 0; t < kNT; ++t) {
+    if (t >= rc.ntok) break;
     const int vv = warp * 8 + u;
     const bool act = vv < rc.nvec;
     float o[8];
@@ -226,7 +228,7 @@ __device__ __forceinline__ void expand_chunk(const GatherArgs& a, const uint8_t*
         out.y = pack_bf16x2(yf[2] + o[2], yf[3] + o[3]);
         out.z = pack_bf16x2(yf[4] + o[4], yf[5] + o[5]);
         out.w = pack_bf16x2(yf[6] + o[6], yf[7] + o[7]);
-        *reinterpret_cast<uint4*>(a.y + (long long)rc.tok[t] * a.ldy + rc.col0 + vv * 8) = out;
+        *reinterpret_cast<uint4*>(ybase + (long long)rc.tok[t] * ldy + rc.col0 + vv * 8) = out;
       }
     }
   }
@@ -494,6 +496,11 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   } else {
     // ---------------- consumers ----------------
     const int ctid = tid;  // 0 .. 255
+    uint16_t* const ybase = a.y;  // parameters the loop needs, read once up front
+    const long long ldy = a.ldy;
+    float* const hout = a.h;
+    const long long ldh = a.ldh;
+    const int mode = a.mode;
     uint32_t ngroup = 0, ncons = 0;
     auto cons_sync = [&]() {  // the 8 consumer warps, bounded
       __syncwarp();
@@ -507,7 +514,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         ok = false;
         break;
       }
-      const GRec& rc = recs[st];  // stable until this stage is released
+      const GRec rc = recs[st];  // in registers: every field is used below
       if (rc.kind == kGEnd) break;
       const uint8_t* sb = sm + (size_t)st * kStageBytes;
       const int b = ngroup & 1;
@@ -544,8 +551,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
 #pragma unroll
           for (int c = 0; c < kMaxCluster; ++c)
             if ((uint32_t)c < ncta) sum += part[c];
-          hs[t * kHMax + j] = a.mode == kModeApply ? rc.sc * sum : sum;
-          if (a.mode == kModeShrink && ok && (uint32_t)t % ncta == crank) a.h[(long long)rc.tok[t] * a.ldh + j] = sum;
+          hs[t * kHMax + j] = mode == kModeApply ? rc.sc * sum : sum;
+          if (mode == kModeShrink && ok && (uint32_t)t % ncta == crank) hout[(long long)recs[st].tok[t] * ldh + j] = sum;
         }
         cons_sync();  // h complete here; this CTA is done reading the peers' partials
         if (ctid < (int)ncta) mbar_arrive_cluster(mapa(smem_u32(&hp_free[b]), (uint32_t)ctid));
@@ -555,11 +562,11 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         cons_sync();  // every warp is done with the previous group's h
         for (int i = ctid; i < rc.ntok * rc.r; i += kGConsThreads) {
           const int t = i / rc.r, j = i - t * rc.r;
-          hs[t * kHMax + j] = rc.sc * a.h[(long long)rc.tok[t] * a.ldh + j];
+          hs[t * kHMax + j] = rc.sc * hout[(long long)recs[st].tok[t] * ldh + j];
         }
         cons_sync();
       }
-      if (rc.kind == kGExpand) expand_chunk(a, sb, hs, eacc, rc, ok, warp, lane);
+      if (rc.kind == kGExpand) expand_chunk(ybase, ldy, sb, hs, eacc, rc, ok, warp, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
     }

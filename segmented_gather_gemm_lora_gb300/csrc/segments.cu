@@ -114,7 +114,10 @@ __global__ void __launch_bounds__(kSegMaxThreads, 1) segments_kernel(const __gri
   int* run_pos = runs + 3 * T;
   const int per_pass = nthr * kSpan;
 
-  // 1. runs of equal valid ids.
+  // 1. runs of equal valid ids.  A batch that fits one pass keeps its ids, its
+  // predecessor id and its run numbering for step 3.
+  const bool one_pass = T <= per_pass;
+  int keep_v[kSpan], keep_prev = INT_MIN, keep_ex = 0;
   int bad = 0, R = 0;
   for (int base = 0; base < T; base += per_pass) {
     const int t0 = base + tid * kSpan;
@@ -133,6 +136,12 @@ __global__ void __launch_bounds__(kSegMaxThreads, 1) segments_kernel(const __gri
     }
     int4 tot;
     const int4 ex = block_scan4(make_int4(heads, 0, 0, 0), &tot, ws);
+    if (one_pass) {
+#pragma unroll
+      for (int k = 0; k < kSpan; ++k) keep_v[k] = v[k];
+      keep_prev = prev;
+      keep_ex = ex.x;
+    }
     int rho = R + ex.x - 1;
 #pragma unroll
     for (int k = 0; k < kSpan; ++k) {
@@ -181,15 +190,15 @@ __global__ void __launch_bounds__(kSegMaxThreads, 1) segments_kernel(const __gri
         const int rho = base + lane;
         const bool act = rho < R;
         const int ad = act ? run_id[rho] : -(lane + 2);
-        const int len = act ? run_end[rho] - run_start[rho] : 0;
         const unsigned peers = __match_any_sync(0xffffffffu, ad);
+        // lengths of this batch's runs with the same adapter: earlier ones and all
+        // (a run's peers are few: each adapter's runs inside 32 consecutive runs)
         int pre = 0, tot = 0;
-        for (int i = 0; i < 32; ++i) {
-          const int li = __shfl_sync(0xffffffffu, len, i);
-          if ((peers >> i) & 1u) {
-            tot += li;
-            if (i < lane) pre += li;
-          }
+        for (unsigned m = act ? peers : 0u; m != 0; m &= m - 1) {  // an inactive lane's only peer is itself
+          const int i = __ffs(m) - 1;
+          const int li = run_end[base + i] - run_start[base + i];
+          tot += li;
+          if (i < lane) pre += li;
         }
         const int cur = act ? counts[ad] : 0;
         __syncwarp();
@@ -225,18 +234,29 @@ __global__ void __launch_bounds__(kSegMaxThreads, 1) segments_kernel(const __gri
   for (int base = 0; base < T; base += per_pass) {
     const int t0 = base + tid * kSpan;
     int v[kSpan];
+    int prev, exx, totx;
+    if (one_pass) {
 #pragma unroll
-    for (int k = 0; k < kSpan; ++k) v[k] = (t0 + k < T) ? a.ids[t0 + k] : INT_MIN;
-    const int prev = (t0 > 0 && t0 < T) ? a.ids[t0 - 1] : INT_MIN;
-    int heads = 0;
+      for (int k = 0; k < kSpan; ++k) v[k] = keep_v[k];
+      prev = keep_prev;
+      exx = keep_ex;
+      totx = R;
+    } else {
 #pragma unroll
-    for (int k = 0; k < kSpan; ++k) {
-      const int before = k == 0 ? prev : v[k - 1];
-      heads += (v[k] >= 0 && v[k] < NA && before != v[k]) ? 1 : 0;
+      for (int k = 0; k < kSpan; ++k) v[k] = (t0 + k < T) ? a.ids[t0 + k] : INT_MIN;
+      prev = (t0 > 0 && t0 < T) ? a.ids[t0 - 1] : INT_MIN;
+      int heads = 0;
+#pragma unroll
+      for (int k = 0; k < kSpan; ++k) {
+        const int before = k == 0 ? prev : v[k - 1];
+        heads += (v[k] >= 0 && v[k] < NA && before != v[k]) ? 1 : 0;
+      }
+      int4 tot;
+      const int4 ex = block_scan4(make_int4(heads, 0, 0, 0), &tot, ws);
+      exx = ex.x;
+      totx = tot.x;
     }
-    int4 tot;
-    const int4 ex = block_scan4(make_int4(heads, 0, 0, 0), &tot, ws);
-    int rho = rbase + ex.x - 1;
+    int rho = rbase + exx - 1;
     int pos = 0;
 #pragma unroll
     for (int k = 0; k < kSpan; ++k) {
@@ -250,7 +270,7 @@ __global__ void __launch_bounds__(kSegMaxThreads, 1) segments_kernel(const __gri
       }
       if (valid) a.perm[pos++] = t0 + k;
     }
-    rbase += tot.x;
+    rbase += totx;
   }
 
   if (tid == 0) {
