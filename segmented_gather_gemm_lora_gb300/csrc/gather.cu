@@ -18,17 +18,19 @@
 //   expand  y[t, n] = bf16(y0[t, n] + sum_j h[t, j] * B_i[j, n]),  n in slice c
 // The rank-r intermediate never leaves the chip.
 //
-// Warp roles.  Warp 8 of every CTA produces: it resolves each unit's adapter
-// and pages and stages 16-row chunks of the adapter (1 KB row runs, translated
-// 16 bytes at a time through the page table, "Multi-LoRA Serving in
-// Production", section "Unified Paged Memory"; one bulk copy per row run and
-// page) with the unit's token rows for the same columns into a 4-stage ring;
-// every stage carries a record of what it holds.  Warps 0-7 consume the ring.  Between a group's shrink and expand the
-// consumers of the cluster's CTAs exchange partial h through distributed shared
-// memory, signalled by mbarrier arrivals on the peers, so the producer keeps
-// streaming the expand rows and the next unit meanwhile.  Units are claimed
-// from a counter (CTA 0 of a cluster claims, and hands the claim to its peers)
-// when the segments give one; one-token units go round-robin.
+// Warp roles.  Warp 9 of every CTA schedules: it claims units (from a counter,
+// CTA 0 of a cluster claiming and handing the claim to its peers, when the
+// segments give one; one-token units go round-robin), resolves each unit's
+// tokens and adapter, checks every page slot of the adapter and caches its
+// physical pages, one unit ahead of the producer.  Warp 8 produces: it stages
+// 16-row chunks of the adapter (1 KB row runs, translated through the page
+// table, "Multi-LoRA Serving in Production", section "Unified Paged Memory";
+// one bulk copy per row run and page) with the unit's token rows for the same
+// columns into a 4-stage ring; every stage carries a record of what it holds.
+// Warps 0-7 consume the ring.  Between a group's shrink and expand the
+// consumers of the cluster's CTAs exchange partial h through distributed
+// shared memory, signalled by mbarrier arrivals on the peers, so the producer
+// keeps streaming the expand rows and the next unit meanwhile.
 //
 // Summation order.  Each rank row's shrink dot product over a sub-slice and
 // each output's expand sum over a 16-row chunk are fixed functions of column
@@ -42,9 +44,10 @@
 
 namespace lora {
 
-constexpr int kGCons = 8;       // consumer warps
-constexpr int kGProd = kGCons;  // the producer warp
-constexpr int kGThreads = 32 * (kGCons + 1);
+constexpr int kGCons = 8;            // consumer warps
+constexpr int kGProd = kGCons;       // the producer warp
+constexpr int kGSched = kGCons + 1;  // the scheduler warp
+constexpr int kGThreads = 32 * (kGCons + 2);
 constexpr int kGConsThreads = 32 * kGCons;
 constexpr int kNT = 4;  // tokens per group
 constexpr int kHMax = LORA_MAX_RANK;
@@ -58,9 +61,9 @@ constexpr int kMaxPgSlots = 512;  // page-list slots of one adapter cached in sh
 
 enum GKind { kGShrink = 0, kGExpand = 1, kGReduce = 2, kGEnd = 3 };
 enum GFlag {
-  kFFirst = 1,   // shrink: first sub-slice (store, not add); expand: first row block of the sub-slice
-  kFLast = 2,    // expand: last row block of the sub-slice (adds y0, writes y; token rows staged)
-  kFGFirst = 4,  // first record of the group: the partial-h buffer is reused once peers are done
+  kFFirst = 1,   // shrink: first sub-slice of the row block; expand: first row block of the sub-slice
+  kFLast = 2,    // shrink: last sub-slice of the row block (partials to the warp's h);
+                 // expand: last row block of the sub-slice (adds y0, writes y; token rows staged)
   kFRed = 8,     // after this record: h of the group from the cluster's partials
   kFHLoad = 16,  // before this record: h of the group from the caller
   kFNoK = 32     // this CTA has no d_in slice (its partial is zero)
@@ -82,16 +85,33 @@ struct GRec {
   int tok[kNT];
 };
 static_assert(sizeof(GRec) <= 64, "record slot");
+
+// What the scheduler tells the producer about a unit it has resolved: the
+// adapter's rank, scale and page-list origin, the unit's tokens, and whether
+// its page slots sit checked in the unit's page cache.
+struct GUnit {
+  int end;       // 1: no more units
+  int r;         // rank
+  float sc;      // scale
+  int tb;        // first position of the unit in token order (segments)
+  int cnt;       // tokens of the unit
+  int na;        // page slots of A_i; B_i's follow them in the cache
+  int cached;    // 1: every page slot of the adapter is in the cache
+  int tok[kNT];  // the first group's tokens
+  long long a_page0, b_page0;
+};
+static_assert(sizeof(GUnit) <= 64, "unit slot");
 static_assert(kSub / 64 <= kGCons, "one warp per block of 8 output vectors");
 
 constexpr size_t kOffRec = (size_t)kStages * kStageBytes;
-constexpr size_t kOffEacc = kOffRec + (size_t)kStages * 64;               // fp32 [kNT][kSub]
-constexpr size_t kOffHp = kOffEacc + (size_t)kNT * kSub * sizeof(float);  // fp32 [2][kNT][kHMax]
+constexpr size_t kOffPw = kOffRec + (size_t)kStages * 64;                     // fp32 [kGCons][kNT][kHMax]
+constexpr size_t kOffHp = kOffPw + (size_t)kGCons * kNT * kHMax * sizeof(float);  // fp32 [2][kNT][kHMax]
 constexpr size_t kOffHs = kOffHp + 2 * kNT * kHMax * sizeof(float);       // fp32 [kNT][kHMax]
-constexpr size_t kOffPgt = kOffHs + kNT * kHMax * sizeof(float);          // int [kMaxPgSlots]
-constexpr size_t kOffClaim = kOffPgt + kMaxPgSlots * sizeof(int);         // int [2]
+constexpr size_t kOffPgt = kOffHs + kNT * kHMax * sizeof(float);          // int [2][kMaxPgSlots]
+constexpr size_t kOffUnit = kOffPgt + 2 * kMaxPgSlots * sizeof(int);      // GUnit [2], 64-byte slots
+constexpr size_t kOffClaim = kOffUnit + 2 * 64;                           // int [2]
 constexpr size_t kOffBars = kOffClaim + 16;
-constexpr int kNBars = 2 * kStages + 2 + 2 + 2 + 2 + 1;
+constexpr int kNBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 2 + 1;
 constexpr size_t kGatherSmem = kOffBars + kNBars * 8;
 
 struct GatherArgs {
@@ -117,119 +137,92 @@ struct GatherArgs {
   int short_only;
 };
 
-// Shrink of one staged chunk for NT tokens: consumer warp w takes the chunk's
-// rows w and w + 8 together (one unpack of each token vector serves both); its
-// lanes take fixed 8-column vectors of the sub-slice; each row's dot product
-// with every token is reduced over the warp and stored (first sub-slice) or
-// added to the CTA's partial h (sub-slices in order).
+// Shrink of one staged chunk for NT tokens.  Warp w owns 8-column vectors
+// 8w .. 8w + 7 of every sub-slice; lane = 2 i + half takes chunk row i and four
+// of those vectors (half 0 the first four, half 1 the last four), visiting them
+// in an order rotated by the row so that one load instruction of the warp
+// touches every bank four times.  The lane's dot products accumulate in
+// registers over the row block's sub-slices (in order); the two halves of a
+// row meet when the block's last sub-slice is done.
 template <int NT>
-__device__ __forceinline__ void shrink_chunk(const uint8_t* sb, int j0, int nrows, int nvec, bool store, float* hpb,
-                                             int warp, int lane) {
+__device__ __forceinline__ void shrink_chunk(const uint8_t* sb, int nrows, int nvec, float (&acc)[kNT], int warp,
+                                             int lane) {
+  const int i = lane >> 1;
+  if (i >= nrows) return;
+  const int v0 = warp * 8 + (lane & 1) * 4;
+  const uint4* arow = reinterpret_cast<const uint4*>(sb + i * kRowBytes);
   const uint4* xrow = reinterpret_cast<const uint4*>(sb + kChunkRows * kRowBytes);
-  const int i0 = warp, i1 = warp + kGCons;  // the warp's two rows (16-row chunks)
-  const bool has0 = i0 < nrows, has1 = i1 < nrows;
-  if (!has0) return;
-  float acc0[NT], acc1[NT];
+  uint4 av[4];
 #pragma unroll
-  for (int t = 0; t < NT; ++t) acc0[t] = acc1[t] = 0.f;
-  const uint4* arow0 = reinterpret_cast<const uint4*>(sb + i0 * kRowBytes);
-  const uint4* arow1 = reinterpret_cast<const uint4*>(sb + (has1 ? i1 : i0) * kRowBytes);
-  for (int vv = lane; vv < nvec; vv += 32) {
-    float a0[8], a1[8];
-    unpack8(arow0[vv], a0);
-    unpack8(arow1[vv], a1);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      float xf[8];
-      unpack8(xrow[t * (kRowBytes / 16) + vv], xf);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        acc0[t] = fmaf(a0[q], xf[q], acc0[t]);
-        acc1[t] = fmaf(a1[q], xf[q], acc1[t]);
-      }
-    }
+  for (int k = 0; k < 4; ++k) {
+    const int vv = v0 + ((k + i) & 3);
+    av[k] = vv < nvec ? arow[vv] : make_uint4(0u, 0u, 0u, 0u);
   }
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
+    float s = acc[t];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      acc0[t] += __shfl_xor_sync(0xffffffffu, acc0[t], o);
-      acc1[t] += __shfl_xor_sync(0xffffffffu, acc1[t], o);
-    }
-  }
-  if (lane == 0) {
+    for (int k = 0; k < 4; ++k) {
+      const int vv = v0 + ((k + i) & 3);
+      if (vv < nvec) {
+        float af[8], xf[8];
+        unpack8(av[k], af);
+        unpack8(xrow[t * (kRowBytes / 16) + vv], xf);
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      float* p0 = hpb + t * kHMax + j0 + i0;
-      *p0 = store ? acc0[t] : *p0 + acc0[t];
-      if (has1) {
-        float* p1 = hpb + t * kHMax + j0 + i1;
-        *p1 = store ? acc1[t] : *p1 + acc1[t];
+        for (int q = 0; q < 8; ++q) s = fmaf(af[q], xf[q], s);
       }
     }
+    acc[t] = s;
   }
 }
 
-// Expand of one staged chunk.  Warp w takes block w of 8 output vectors (a
-// sub-slice has at most 8 blocks) for every token, whatever the sub-slice's
-// width, so each eacc entry always belongs to the same warp and consecutive
-// chunks need no barrier between the warps.  Lane = 8 g + u handles vector u of
-// the block for the chunk's rows 4 g .. 4 g + 3 (ascending), so each group of 8
-// lanes reads 128 contiguous bytes of one row (no bank conflicts); the four
-// row-quarter sums meet in a fixed two-step butterfly, and chunk sums
-// accumulate in chunk order in eacc.  The sub-slice's last chunk adds y0 and
-// writes y.
+// Expand of one staged chunk.  Lane l of warp w owns the two output columns
+// of 32-bit word 32 w + l of the sub-slice, for every token, so the sum over
+// the adapter's rows runs in the lane's registers from the sub-slice's first
+// row block to its last, in row order, with no exchange between lanes; one
+// load instruction of the warp reads 128 contiguous bytes of a row.  The
+// sub-slice's last chunk adds y0 and writes y.
 __device__ __forceinline__ void expand_chunk(uint16_t* ybase, long long ldy, const uint8_t* sb, const float* hs,
-                                             float* eacc, const GRec& rc, bool ok, int warp, int lane) {
-  const int nblk = (rc.nvec + 7) >> 3;
-  if (warp >= nblk) return;
-  const int g = lane >> 3, u = lane & 7;
+                                             float (&acc)[kNT][2], const GRec& rc, bool ok, int warp, int lane) {
+  const int m = warp * 32 + lane;
+  if (m >= rc.nvec * 4) return;
+  if (rc.flags & kFFirst) {
+#pragma unroll
+    for (int t = 0; t < kNT; ++t) acc[t][0] = acc[t][1] = 0.f;
+  }
+  uint32_t bw[kChunkRows];
+#pragma unroll
+  for (int i = 0; i < kChunkRows; ++i)
+    bw[i] = i < rc.nrows ? *reinterpret_cast<const uint32_t*>(sb + i * kRowBytes + 4 * m) : 0u;
 #pragma unroll
   for (int t = 0; t < kNT; ++t) {
     if (t >= rc.ntok) break;
-    const int vv = warp * 8 + u;
-    const bool act = vv < rc.nvec;
-    float o[8];
+    const float4* h4 = reinterpret_cast<const float4*>(hs + t * kHMax + rc.j0);
+    float s0 = acc[t][0], s1 = acc[t][1];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) o[q] = 0.f;
-    if (act) {
+    for (int i4 = 0; i4 < kChunkRows / 4; ++i4) {
+      if (4 * i4 >= rc.nrows) break;
+      const float4 hv = h4[i4];
+      const float he[4] = {hv.x, hv.y, hv.z, hv.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int i = 4 * g + k;
+      for (int e = 0; e < 4; ++e) {
+        const int i = 4 * i4 + e;
         if (i < rc.nrows) {
-          const float hj = hs[t * kHMax + rc.j0 + i];
-          float bf[8];
-          unpack8(reinterpret_cast<const uint4*>(sb + i * kRowBytes)[vv], bf);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) o[q] = fmaf(hj, bf[q], o[q]);
+          s0 = fmaf(he[e], bf_lo(bw[i]), s0);
+          s1 = fmaf(he[e], bf_hi(bw[i]), s1);
         }
       }
     }
+    acc[t][0] = s0;
+    acc[t][1] = s1;
+  }
+  if ((rc.flags & kFLast) && ok) {
 #pragma unroll
-    for (int m = 8; m < 32; m <<= 1) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q) o[q] += __shfl_xor_sync(0xffffffffu, o[q], m);
-    }
-    if (act && g == 0) {
-      float4* ea = reinterpret_cast<float4*>(eacc + (t * kSub + vv * 8));
-      if (!(rc.flags & kFFirst)) {
-        const float4 e0 = ea[0], e1 = ea[1];
-        o[0] = e0.x + o[0]; o[1] = e0.y + o[1]; o[2] = e0.z + o[2]; o[3] = e0.w + o[3];
-        o[4] = e1.x + o[4]; o[5] = e1.y + o[5]; o[6] = e1.z + o[6]; o[7] = e1.w + o[7];
-      }
-      if (!(rc.flags & kFLast)) {
-        ea[0] = make_float4(o[0], o[1], o[2], o[3]);
-        ea[1] = make_float4(o[4], o[5], o[6], o[7]);
-      } else if (ok) {
-        float yf[8];
-        unpack8(reinterpret_cast<const uint4*>(sb + (kChunkRows + t) * kRowBytes)[vv], yf);
-        uint4 out;
-        out.x = pack_bf16x2(yf[0] + o[0], yf[1] + o[1]);
-        out.y = pack_bf16x2(yf[2] + o[2], yf[3] + o[3]);
-        out.z = pack_bf16x2(yf[4] + o[4], yf[5] + o[5]);
-        out.w = pack_bf16x2(yf[6] + o[6], yf[7] + o[7]);
-        *reinterpret_cast<uint4*>(ybase + (long long)rc.tok[t] * ldy + rc.col0 + vv * 8) = out;
-      }
+    for (int t = 0; t < kNT; ++t) {
+      if (t >= rc.ntok) break;
+      const uint32_t y0 = *reinterpret_cast<const uint32_t*>(sb + (kChunkRows + t) * kRowBytes + 4 * m);
+      *reinterpret_cast<uint32_t*>(ybase + (long long)rc.tok[t] * ldy + rc.col0 + 2 * m) =
+          pack_bf16x2(bf_lo(y0) + acc[t][0], bf_hi(y0) + acc[t][1]);
     }
   }
 }
@@ -237,19 +230,22 @@ __device__ __forceinline__ void expand_chunk(uint16_t* ybase, long long ldy, con
 __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_constant__ GatherArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   GRec* recs = reinterpret_cast<GRec*>(sm + kOffRec);  // 64-byte slots
-  float* eacc = reinterpret_cast<float*>(sm + kOffEacc);
+  float* pw = reinterpret_cast<float*>(sm + kOffPw);  // each warp's partial h of the group
   float* hp = reinterpret_cast<float*>(sm + kOffHp);
   float* hs = reinterpret_cast<float*>(sm + kOffHs);
   int* pgt = reinterpret_cast<int*>(sm + kOffPgt);
+  GUnit* units = reinterpret_cast<GUnit*>(sm + kOffUnit);
   int* claim_val = reinterpret_cast<int*>(sm + kOffClaim);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBars);
   uint64_t* full = bars;                   // [stages] the record writer (+ the copies' bytes)
   uint64_t* empty = bars + kStages;        // [stages] 8 consumer warps
   uint64_t* hp_ready = bars + 2 * kStages;  // [2] one arrival per CTA of the cluster
   uint64_t* hp_free = hp_ready + 2;        // [2] one arrival per CTA of the cluster
-  uint64_t* claim_full = hp_free + 2;      // [2] CTA 0's producer
+  uint64_t* claim_full = hp_free + 2;      // [2] CTA 0's scheduler
   uint64_t* claim_empty = claim_full + 2;  // [2] (CTA 0 only) one arrival per CTA
-  uint64_t* cons = claim_empty + 2;        // 8 consumer warps, twice per group
+  uint64_t* unit_full = claim_empty + 2;   // [2] the scheduler
+  uint64_t* unit_empty = unit_full + 2;    // [2] the producer
+  uint64_t* cons = unit_empty + 2;         // 8 consumer warps, twice per group
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t crank = cluster_ctarank(), ncta = cluster_nctarank();
@@ -268,6 +264,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       mbar_init(smem_u32(&hp_free[b]), ncta);
       mbar_init(smem_u32(&claim_full[b]), 1);
       mbar_init(smem_u32(&claim_empty[b]), ncta);
+      mbar_init(smem_u32(&unit_full[b]), 1);
+      mbar_init(smem_u32(&unit_empty[b]), 1);
     }
     mbar_init(smem_u32(cons), kGCons);
     fence_mbar_init();
@@ -284,27 +282,14 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   const int nns = (a.mode != kModeShrink && n1 > n0) ? (n1 - n0 + kSub - 1) / kSub : 0;
   bool ok = true;
 
-  if (warp == kGProd) {
-    // ---------------- producer ----------------
+  if (warp == kGSched) {
+    // ---------------- scheduler ----------------
+    // Claims a unit, resolves its segment, tokens and adapter, checks every
+    // page slot of the adapter and caches the physical pages, a unit ahead of
+    // the producer (two unit slots).
     const int n_short = a.src == kSrcSegments ? a.meta[2] : 0;
     const int n_units = a.src == kSrcTokens ? a.T : a.meta[2] + (a.short_only ? 0 : a.meta[3]);
     const int shift = v.page_shift;
-    const long long pmask = (1LL << shift) - 1;
-    uint32_t g = 0;  // stages posted
-    auto take_stage = [&]() -> uint32_t {
-      const uint32_t st = g % kStages;
-      if (g >= kStages && !mbar_wait(smem_u32(&empty[st]), ((g / kStages) - 1) & 1)) ok = false;
-      return st;
-    };
-    // a record without data
-    auto post_record = [&](const GRec& rc) {
-      const uint32_t st = take_stage();
-      if (lane == 0) {
-        recs[st] = rc;
-        mbar_arrive(smem_u32(&full[st]));
-      }
-      ++g;
-    };
     // Claims: unit cid first, then units ncl + counter, CTA 0 claiming for the
     // cluster.  Each cluster over-claims the counter exactly once; the last
     // claim of all puts it back to zero for the next call.
@@ -345,11 +330,18 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       if (lane == 0) mbar_arrive_cluster(mapa(smem_u32(&claim_empty[q]), 0));
       ++nclaim;
     };
-
+    uint32_t nposted = 0;  // units handed to the producer
+    // the slot of the next unit, once the producer is done with its last use
+    auto take_slot = [&]() -> uint32_t {
+      const uint32_t q = nposted & 1;
+      if (nposted >= 2 && !mbar_wait(smem_u32(&unit_empty[q]), ((nposted >> 1) - 1) & 1)) ok = false;
+      return q;
+    };
     for (; u < n_units && ok; next_unit()) {
       int ad, tb = 0, cnt;
       if (a.src == kSrcTokens) {
         ad = a.token_adapter[u];
+        tb = u;
         cnt = 1;
         if (ad == -1) continue;
         if (ad < -1 || ad >= v.n_adapters) {
@@ -372,47 +364,110 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       // alongside its descriptor.
       const int first_tok = lane < min(kNT, cnt) ? (a.src == kSrcTokens ? u : a.perm[tb + lane]) : -1;
       const lora_adapter_desc_t d = v.adapters[ad];
-      // Every CTA checks the whole adapter, so all reach the same verdict
-      // without talking to each other; the same pass caches the physical pages.
-      int bad = 0;
-      long long na = 0, nb = 0;
-      bool cached = false;
       if (d.rank < 1 || d.rank > v.max_rank || d.rank > kHMax) {
-        bad = LORA_DERR_BAD_RANK;
-      } else {
-        const long long P = 1LL << shift;
-        na = ((long long)d.rank * v.d_in + P - 1) >> shift;
-        nb = ((long long)d.rank * v.d_out + P - 1) >> shift;
-        cached = na + nb <= kMaxPgSlots;
-        __syncwarp();  // the previous unit's page reads are done
-        int mine = 0;
-        for (long long i = lane; i < na + nb; i += 32) {
-          const long long slot = i < na ? d.a_page0 + i : d.b_page0 + (i - na);
-          long long pg = -1;
-          if (slot < 0 || slot >= v.n_page_list) {
-            mine = 1;
-          } else {
-            pg = v.page_list[slot];
-            if (pg < 0 || pg >= v.n_pages) mine = 1;
-          }
-          if (cached) pgt[i] = (int)pg;
-        }
-        if (__any_sync(0xffffffffu, mine)) bad = LORA_DERR_BAD_PAGE;
-        __syncwarp();
-      }
-      if (bad) {
-        if (crank == 0 && lane == 0) report(a.err, bad);
+        if (crank == 0 && lane == 0) report(a.err, LORA_DERR_BAD_RANK);
         continue;
       }
-      const int r = d.rank;
+      // Every CTA checks the whole adapter, so all reach the same verdict
+      // without talking to each other; the same pass caches the physical
+      // pages.  Each lane has up to 8 page-list reads in flight at once.
+      const long long P = 1LL << shift;
+      const long long na = ((long long)d.rank * v.d_in + P - 1) >> shift;
+      const long long nb = ((long long)d.rank * v.d_out + P - 1) >> shift;
+      const bool cached = na + nb <= kMaxPgSlots;
+      const uint32_t q = take_slot();
+      int* pc = pgt + q * kMaxPgSlots;
+      int mine = 0;
+      for (long long i0 = 0; i0 < na + nb; i0 += 32 * 8) {
+        int pv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const long long i = i0 + k * 32 + lane;
+          const long long slot = i < na ? d.a_page0 + i : d.b_page0 + (i - na);
+          pv[k] = 0;
+          if (i < na + nb) pv[k] = (slot < 0 || slot >= v.n_page_list) ? -1 : v.page_list[slot];
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const long long i = i0 + k * 32 + lane;
+          if (i < na + nb) {
+            if (pv[k] < 0 || pv[k] >= v.n_pages) mine = 1;
+            if (cached) pc[i] = pv[k];
+          }
+        }
+      }
+      if (__any_sync(0xffffffffu, mine)) {
+        if (crank == 0 && lane == 0) report(a.err, LORA_DERR_BAD_PAGE);
+        continue;  // the slot stays free
+      }
+      GUnit un;
+      un.end = 0;
+      un.r = d.rank;
+      un.sc = d.scale;
+      un.tb = tb;
+      un.cnt = cnt;
+      un.na = (int)na;
+      un.cached = cached ? 1 : 0;
+#pragma unroll
+      for (int t = 0; t < kNT; ++t) un.tok[t] = __shfl_sync(0xffffffffu, first_tok, t);
+      un.a_page0 = d.a_page0;
+      un.b_page0 = d.b_page0;
+      __syncwarp();  // every lane's cache writes before the hand-over
+      if (lane == 0) {
+        units[q] = un;
+        mbar_arrive(smem_u32(&unit_full[q]));
+      }
+      ++nposted;
+    }
+    // `claim` holds this cluster's over-claim now; the last of all resets the counter
+    if (dynamic && crank == 0 && lane == 0 && claim == n_dyn + (int)ncl - 1) *a.counter = 0;
+    {
+      const uint32_t q = take_slot();
+      if (lane == 0) {
+        units[q].end = 1;
+        mbar_arrive(smem_u32(&unit_full[q]));
+      }
+    }
+    if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
+  } else if (warp == kGProd) {
+    // ---------------- producer ----------------
+    const int shift = v.page_shift;
+    const long long pmask = (1LL << shift) - 1;
+    uint32_t g = 0;  // stages posted
+    auto take_stage = [&]() -> uint32_t {
+      const uint32_t st = g % kStages;
+      if (g >= kStages && !mbar_wait(smem_u32(&empty[st]), ((g / kStages) - 1) & 1)) ok = false;
+      return st;
+    };
+    // a record without data
+    auto post_record = [&](const GRec& rc) {
+      const uint32_t st = take_stage();
+      if (lane == 0) {
+        recs[st] = rc;
+        mbar_arrive(smem_u32(&full[st]));
+      }
+      ++g;
+    };
+    for (uint32_t nu = 0; ok; ++nu) {
+      const uint32_t q = nu & 1;
+      if (!mbar_wait(smem_u32(&unit_full[q]), (nu >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const GUnit un = units[q];
+      if (un.end) break;
+      const int* pc = pgt + q * kMaxPgSlots;
+      const int r = un.r, cnt = un.cnt;
+      const long long na = un.na;
       const int njb = (r + kChunkRows - 1) / kChunkRows;
       for (int g0 = 0; g0 < cnt; g0 += kNT) {
         const int ntok = min(kNT, cnt - g0);
-        const int mytok = g0 == 0 ? first_tok : (lane < ntok ? a.perm[tb + g0 + lane] : -1);
+        const int mytok = g0 == 0 ? (lane < kNT ? units[q].tok[lane] : -1)
+                                  : (lane < ntok ? a.perm[un.tb + g0 + lane] : -1);
         GRec rc{};
         rc.ntok = ntok;
         rc.r = r;
-        rc.sc = d.scale;
+        rc.sc = un.sc;
 #pragma unroll
         for (int t = 0; t < kNT; ++t) rc.tok[t] = __shfl_sync(0xffffffffu, mytok, t);
         // One chunk: adapter rows [j0, j0 + nrows) of the sub-slice at col0,
@@ -442,13 +497,13 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
           const int tk = __shfl_sync(0xffffffffu, mytok, (lane - nrows) & (kNT - 1));
           if (lane < nrows) {
             const long long rowlen = shrink ? v.d_in : v.d_out;
-            const long long page0 = shrink ? d.a_page0 : d.b_page0;
+            const long long page0 = shrink ? un.a_page0 : un.b_page0;
             const int pbase = shrink ? 0 : (int)na;
             long long e = (long long)(j0 + lane) * rowlen + col0;
             uint32_t dst = sbase + (uint32_t)(lane * kRowBytes);
             for (int rem = w; rem > 0;) {
               const long long idx = e >> shift, off = e & pmask;
-              const long long page = cached ? pgt[pbase + idx] : v.page_list[page0 + idx];
+              const long long page = un.cached ? pc[pbase + idx] : v.page_list[page0 + idx];
               const int n = (int)min((long long)rem, (1LL << shift) - off);
               bulk_g2s(dst, v.pool + (page << shift) + off, (uint32_t)n * 2, bar);
               e += n;
@@ -461,10 +516,10 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
           }
           ++g;
         };
-        for (int ks = 0; ks < nks; ++ks) {
-          const int col0 = k0 + ks * kSub, w = min(kSub, k1 - col0);
-          for (int jb = 0; jb < njb; ++jb) {
-            const int f = (ks == 0 ? kFFirst : 0) | (ks == 0 && jb == 0 ? kFGFirst : 0) |
+        for (int jb = 0; jb < njb; ++jb) {
+          for (int ks = 0; ks < nks; ++ks) {
+            const int col0 = k0 + ks * kSub, w = min(kSub, k1 - col0);
+            const int f = (ks == 0 ? kFFirst : 0) | (ks == nks - 1 ? kFLast : 0) |
                           (ks == nks - 1 && jb == njb - 1 ? kFRed : 0);
             post_chunk(kGShrink, col0, w, jb * kChunkRows, min(kChunkRows, r - jb * kChunkRows), true, f);
           }
@@ -472,7 +527,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         if (reduce_h && nks == 0) {
           GRec red = rc;
           red.kind = kGReduce;
-          red.flags = kFGFirst | kFRed | kFNoK;
+          red.flags = kFRed | kFNoK;
           post_record(red);
         }
         for (int ns = 0; ns < nns; ++ns) {
@@ -484,9 +539,9 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
           }
         }
       }
+      __syncwarp();  // every lane's last page-cache read is done
+      if (lane == 0) mbar_arrive(smem_u32(&unit_empty[q]));
     }
-    // `claim` holds this cluster's over-claim now; the last of all resets the counter
-    if (dynamic && crank == 0 && lane == 0 && claim == n_dyn + (int)ncl - 1) *a.counter = 0;
     {
       GRec end{};
       end.kind = kGEnd;
@@ -502,6 +557,10 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
     const long long ldh = a.ldh;
     const int mode = a.mode;
     uint32_t ngroup = 0, ncons = 0;
+    float sacc[kNT];     // shrink: the lane's row partials over a row block's sub-slices
+    float eacc[kNT][2];  // expand: the lane's two outputs over a sub-slice's row blocks
+#pragma unroll
+    for (int t = 0; t < kNT; ++t) sacc[t] = eacc[t][0] = eacc[t][1] = 0.f;
     auto cons_sync = [&]() {  // the 8 consumer warps, bounded
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(cons));
@@ -519,22 +578,41 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       const uint8_t* sb = sm + (size_t)st * kStageBytes;
       const int b = ngroup & 1;
       float* hpb = hp + b * kNT * kHMax;
-      if ((rc.flags & kFGFirst) && reduce_h && ngroup >= 2 &&
-          !mbar_wait_cluster(smem_u32(&hp_free[b]), ((ngroup >> 1) - 1) & 1))
-        ok = false;
       if (rc.kind == kGShrink) {
-        const bool store = rc.flags & kFFirst;
+        if (rc.flags & kFFirst) {
+#pragma unroll
+          for (int t = 0; t < kNT; ++t) sacc[t] = 0.f;
+        }
         switch (rc.ntok) {
-          case 1: shrink_chunk<1>(sb, rc.j0, rc.nrows, rc.nvec, store, hpb, warp, lane); break;
-          case 2: shrink_chunk<2>(sb, rc.j0, rc.nrows, rc.nvec, store, hpb, warp, lane); break;
-          case 3: shrink_chunk<3>(sb, rc.j0, rc.nrows, rc.nvec, store, hpb, warp, lane); break;
-          default: shrink_chunk<4>(sb, rc.j0, rc.nrows, rc.nvec, store, hpb, warp, lane); break;
+          case 1: shrink_chunk<1>(sb, rc.nrows, rc.nvec, sacc, warp, lane); break;
+          case 2: shrink_chunk<2>(sb, rc.nrows, rc.nvec, sacc, warp, lane); break;
+          case 3: shrink_chunk<3>(sb, rc.nrows, rc.nvec, sacc, warp, lane); break;
+          default: shrink_chunk<4>(sb, rc.nrows, rc.nvec, sacc, warp, lane); break;
+        }
+        if (rc.flags & kFLast) {  // the row block is done: its two halves meet in the warp's partial
+          const int i = lane >> 1;
+#pragma unroll
+          for (int t = 0; t < kNT; ++t) {
+            const float v = sacc[t] + __shfl_xor_sync(0xffffffffu, sacc[t], 1);
+            if ((lane & 1) == 0 && i < rc.nrows && t < rc.ntok) pw[(warp * kNT + t) * kHMax + rc.j0 + i] = v;
+          }
         }
       }
       if (rc.flags & kFRed) {  // h of the group from the cluster's partials
-        if (rc.flags & kFNoK)
-          for (int i = ctid; i < rc.ntok * rc.r; i += kGConsThreads) hpb[(i / rc.r) * kHMax + i % rc.r] = 0.f;
-        cons_sync();  // this CTA's partial is complete, and every warp is done with the previous h
+        cons_sync();  // every warp's partial is in, and every warp is done with the previous h
+        // the peers are done reading this buffer's partial of two groups ago
+        if (ngroup >= 2 && !mbar_wait_cluster(smem_u32(&hp_free[b]), ((ngroup >> 1) - 1) & 1)) ok = false;
+        // this CTA's partial: the warps' partials in warp order
+        for (int i = ctid; i < rc.ntok * rc.r; i += kGConsThreads) {
+          const int t = i / rc.r, j = i - t * rc.r;
+          float sum = 0.f;
+          if (!(rc.flags & kFNoK)) {
+#pragma unroll
+            for (int w = 0; w < kGCons; ++w) sum += pw[(w * kNT + t) * kHMax + j];
+          }
+          hpb[t * kHMax + j] = sum;
+        }
+        cons_sync();  // this CTA's partial is complete
         // lane p of warp 0 signals CTA p: the cluster-scope releases run side by side
         if (ctid < (int)ncta) mbar_arrive_cluster(mapa(smem_u32(&hp_ready[b]), (uint32_t)ctid));
         if (!mbar_wait_cluster(smem_u32(&hp_ready[b]), (ngroup >> 1) & 1)) ok = false;
