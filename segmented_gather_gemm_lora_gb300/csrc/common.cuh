@@ -161,10 +161,15 @@ __device__ __forceinline__ void st_dsmem_u32(uint32_t cluster_addr, uint32_t v) 
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
-  return v;
+// Asynchronous 16-byte store into the shared memory of a CTA of the cluster
+// (possibly this one); its bytes complete as transaction bytes on the
+// mbarrier at `cluster_bar`, which sits in the same CTA as the destination.
+// Whoever waits on that barrier sees the data once the phase completes.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, const float4& v, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   cluster_addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(cluster_bar)
+               : "memory");
 }
 
 // ------------------------------------------------- programmatic dependent launch --

@@ -105,13 +105,13 @@ static_assert(kSub / 64 <= kGCons, "one warp per block of 8 output vectors");
 
 constexpr size_t kOffRec = (size_t)kStages * kStageBytes;
 constexpr size_t kOffPw = kOffRec + (size_t)kStages * 64;                     // fp32 [kGCons][kNT][kHMax]
-constexpr size_t kOffHp = kOffPw + (size_t)kGCons * kNT * kHMax * sizeof(float);  // fp32 [2][kNT][kHMax]
-constexpr size_t kOffHs = kOffHp + 2 * kNT * kHMax * sizeof(float);       // fp32 [kNT][kHMax]
+constexpr size_t kOffRecv = kOffPw + (size_t)kGCons * kNT * kHMax * sizeof(float);  // fp32 [2][kMaxCluster][kNT][kHMax]
+constexpr size_t kOffHs = kOffRecv + 2 * (size_t)kMaxCluster * kNT * kHMax * sizeof(float);  // fp32 [kNT][kHMax]
 constexpr size_t kOffPgt = kOffHs + kNT * kHMax * sizeof(float);          // int [2][kMaxPgSlots]
 constexpr size_t kOffUnit = kOffPgt + 2 * kMaxPgSlots * sizeof(int);      // GUnit [2], 64-byte slots
 constexpr size_t kOffClaim = kOffUnit + 2 * 64;                           // int [2]
 constexpr size_t kOffBars = kOffClaim + 16;
-constexpr int kNBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 2 + 1;
+constexpr int kNBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1;
 constexpr size_t kGatherSmem = kOffBars + kNBars * 8;
 
 struct GatherArgs {
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   extern __shared__ __align__(128) uint8_t sm[];
   GRec* recs = reinterpret_cast<GRec*>(sm + kOffRec);  // 64-byte slots
   float* pw = reinterpret_cast<float*>(sm + kOffPw);  // each warp's partial h of the group
-  float* hp = reinterpret_cast<float*>(sm + kOffHp);
+  float* recv = reinterpret_cast<float*>(sm + kOffRecv);  // the cluster's partials, by CTA
   float* hs = reinterpret_cast<float*>(sm + kOffHs);
   int* pgt = reinterpret_cast<int*>(sm + kOffPgt);
   GUnit* units = reinterpret_cast<GUnit*>(sm + kOffUnit);
@@ -239,9 +239,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBars);
   uint64_t* full = bars;                   // [stages] the record writer (+ the copies' bytes)
   uint64_t* empty = bars + kStages;        // [stages] 8 consumer warps
-  uint64_t* hp_ready = bars + 2 * kStages;  // [2] one arrival per CTA of the cluster
-  uint64_t* hp_free = hp_ready + 2;        // [2] one arrival per CTA of the cluster
-  uint64_t* claim_full = hp_free + 2;      // [2] CTA 0's scheduler
+  uint64_t* recv_full = bars + 2 * kStages;  // [2] this CTA's arrival + every CTA's partial bytes
+  uint64_t* claim_full = recv_full + 2;     // [2] CTA 0's scheduler
   uint64_t* claim_empty = claim_full + 2;  // [2] (CTA 0 only) one arrival per CTA
   uint64_t* unit_full = claim_empty + 2;   // [2] the scheduler
   uint64_t* unit_empty = unit_full + 2;    // [2] the producer
@@ -260,8 +259,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       mbar_init(smem_u32(&empty[s]), kGCons);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&hp_ready[b]), ncta);
-      mbar_init(smem_u32(&hp_free[b]), ncta);
+      mbar_init(smem_u32(&recv_full[b]), 1);
       mbar_init(smem_u32(&claim_full[b]), 1);
       mbar_init(smem_u32(&claim_empty[b]), ncta);
       mbar_init(smem_u32(&unit_full[b]), 1);
@@ -292,11 +290,13 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
     const int shift = v.page_shift;
     // Claims: unit cid first, then units ncl + counter, CTA 0 claiming for the
     // cluster.  Each cluster over-claims the counter exactly once; the last
-    // claim of all puts it back to zero for the next call.
+    // claim of all puts it back to zero for the next call.  A unit is claimed
+    // only once the producer has started on the previous one, so that when
+    // the units run out no cluster holds more than one in reserve.
     const int n_dyn = max(0, n_units - (int)ncl);
     int u = (int)cid;
-    int claim = 0;  // CTA 0, lane 0: the counter's answer in flight
-    if (dynamic && crank == 0 && lane == 0) claim = atomicAdd(a.counter, 1);
+    int claim = 0;      // CTA 0, lane 0: the counter's last answer
+    bool over = false;  // CTA 0, lane 0: this cluster's over-claim is made
     uint32_t nclaim = 0;
     auto next_unit = [&]() {
       if (!dynamic) {
@@ -308,12 +308,12 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         int nu = 0;
         if (lane == 0) {
           if (nclaim >= 2 && !mbar_wait_cluster(smem_u32(&claim_empty[q]), ((nclaim >> 1) - 1) & 1)) ok = false;
-          const int c = claim;
-          if (c < n_dyn) {
-            nu = (int)ncl + c;
-            claim = atomicAdd(a.counter, 1);
+          claim = atomicAdd(a.counter, 1);
+          if (claim < n_dyn) {
+            nu = (int)ncl + claim;
           } else {
-            nu = n_units;  // the over-claim stays in `claim`
+            nu = n_units;
+            over = true;
           }
         }
         nu = __shfl_sync(0xffffffffu, nu, 0);
@@ -332,12 +332,16 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
     };
     uint32_t nposted = 0;  // units handed to the producer
     // the slot of the next unit, once the producer is done with its last use
+    // (it has then started on the previous unit)
     auto take_slot = [&]() -> uint32_t {
       const uint32_t q = nposted & 1;
       if (nposted >= 2 && !mbar_wait(smem_u32(&unit_empty[q]), ((nposted >> 1) - 1) & 1)) ok = false;
       return q;
     };
-    for (; u < n_units && ok; next_unit()) {
+    for (uint32_t k = 0; ok; ++k) {
+      const uint32_t q = take_slot();
+      if (k > 0) next_unit();
+      if (u >= n_units) break;
       int ad, tb = 0, cnt;
       if (a.src == kSrcTokens) {
         ad = a.token_adapter[u];
@@ -375,7 +379,6 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       const long long na = ((long long)d.rank * v.d_in + P - 1) >> shift;
       const long long nb = ((long long)d.rank * v.d_out + P - 1) >> shift;
       const bool cached = na + nb <= kMaxPgSlots;
-      const uint32_t q = take_slot();
       int* pc = pgt + q * kMaxPgSlots;
       int mine = 0;
       for (long long i0 = 0; i0 < na + nb; i0 += 32 * 8) {
@@ -419,8 +422,11 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       }
       ++nposted;
     }
-    // `claim` holds this cluster's over-claim now; the last of all resets the counter
-    if (dynamic && crank == 0 && lane == 0 && claim == n_dyn + (int)ncl - 1) *a.counter = 0;
+    if (dynamic && crank == 0 && lane == 0) {
+      if (!over) claim = atomicAdd(a.counter, 1);  // no unit was claimed (cid >= n_units)
+      // `claim` holds this cluster's over-claim now; the last of all resets the counter
+      if (claim == n_dyn + (int)ncl - 1) *a.counter = 0;
+    }
     {
       const uint32_t q = take_slot();
       if (lane == 0) {
@@ -577,7 +583,6 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       if (rc.kind == kGEnd) break;
       const uint8_t* sb = sm + (size_t)st * kStageBytes;
       const int b = ngroup & 1;
-      float* hpb = hp + b * kNT * kHMax;
       if (rc.kind == kGShrink) {
         if (rc.flags & kFFirst) {
 #pragma unroll
@@ -599,41 +604,41 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         }
       }
       if (rc.flags & kFRed) {  // h of the group from the cluster's partials
+        // Buffer b last held group ngroup - 2, which this CTA read before it
+        // sent group ngroup - 1; no peer sends group ngroup before receiving that.
         cons_sync();  // every warp's partial is in, and every warp is done with the previous h
-        // the peers are done reading this buffer's partial of two groups ago
-        if (ngroup >= 2 && !mbar_wait_cluster(smem_u32(&hp_free[b]), ((ngroup >> 1) - 1) & 1)) ok = false;
-        // this CTA's partial: the warps' partials in warp order
-        for (int i = ctid; i < rc.ntok * rc.r; i += kGConsThreads) {
-          const int t = i / rc.r, j = i - t * rc.r;
-          float sum = 0.f;
+        const int q4 = (rc.r + 3) >> 2;  // 16-byte pieces of one token's partial
+        const int nq = rc.ntok * q4;
+        float* rb = recv + b * kMaxCluster * kNT * kHMax;
+        const uint32_t bar = smem_u32(&recv_full[b]);
+        if (ctid == 0) mbar_arrive_expect_tx(bar, (uint32_t)(ncta * nq * 16));
+        if (ctid < nq) {
+          // this CTA's partial (the warps' partials in warp order), pushed to
+          // every CTA of the cluster, this one included
+          const int t = ctid / q4, j = (ctid - t * q4) * 4;
+          float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
           if (!(rc.flags & kFNoK)) {
 #pragma unroll
-            for (int w = 0; w < kGCons; ++w) sum += pw[(w * kNT + t) * kHMax + j];
+            for (int w = 0; w < kGCons; ++w) {
+              const float4 p = *reinterpret_cast<const float4*>(pw + (w * kNT + t) * kHMax + j);
+              sum.x += p.x;
+              sum.y += p.y;
+              sum.z += p.z;
+              sum.w += p.w;
+            }
           }
-          hpb[t * kHMax + j] = sum;
+          const uint32_t dst = smem_u32(rb + (crank * kNT + t) * kHMax + j);
+          for (uint32_t c = 0; c < ncta; ++c) st_async_v4(mapa(dst, c), sum, mapa(bar, c));
         }
-        cons_sync();  // this CTA's partial is complete
-        // lane p of warp 0 signals CTA p: the cluster-scope releases run side by side
-        if (ctid < (int)ncta) mbar_arrive_cluster(mapa(smem_u32(&hp_ready[b]), (uint32_t)ctid));
-        if (!mbar_wait_cluster(smem_u32(&hp_ready[b]), (ngroup >> 1) & 1)) ok = false;
-        const uint32_t hp_addr = smem_u32(hpb);
+        if (!mbar_wait(bar, (ngroup >> 1) & 1)) ok = false;
         for (int i = ctid; i < rc.ntok * rc.r; i += kGConsThreads) {
           const int t = i / rc.r, j = i - t * rc.r;
-          const uint32_t off = (uint32_t)((t * kHMax + j) * sizeof(float));
-          // every peer's load in flight first, then the sum in fixed CTA order
-          float part[kMaxCluster];
-#pragma unroll
-          for (int c = 0; c < kMaxCluster; ++c)
-            part[c] = (uint32_t)c < ncta ? ld_dsmem_f32(mapa(hp_addr + off, (uint32_t)c)) : 0.f;
-          float sum = 0.f;
-#pragma unroll
-          for (int c = 0; c < kMaxCluster; ++c)
-            if ((uint32_t)c < ncta) sum += part[c];
+          float sum = 0.f;  // in fixed CTA order
+          for (uint32_t c = 0; c < ncta; ++c) sum += rb[(c * kNT + t) * kHMax + j];
           hs[t * kHMax + j] = mode == kModeApply ? rc.sc * sum : sum;
           if (mode == kModeShrink && ok && (uint32_t)t % ncta == crank) hout[(long long)recs[st].tok[t] * ldh + j] = sum;
         }
-        cons_sync();  // h complete here; this CTA is done reading the peers' partials
-        if (ctid < (int)ncta) mbar_arrive_cluster(mapa(smem_u32(&hp_free[b]), (uint32_t)ctid));
+        cons_sync();  // h complete here
         ++ngroup;
       }
       if (rc.flags & kFHLoad) {  // h of the group from the caller
