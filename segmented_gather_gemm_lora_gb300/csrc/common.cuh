@@ -202,6 +202,14 @@ __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
   f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
 }
 
+// The descriptor of adapter `ad`; a zero one (rank 0) when `ad` is outside
+// [0, n_adapters) of the view, so nothing outside the descriptor array is read.
+__device__ __forceinline__ lora_adapter_desc_t adapter_desc(const DevView& v, int ad) {
+  lora_adapter_desc_t d{};
+  if (ad >= 0 && ad < v.n_adapters) d = v.adapters[ad];
+  return d;
+}
+
 __device__ __forceinline__ void report(int32_t* err, int bits) {
   if (err != nullptr && bits) atomicOr(err, bits);
 }

@@ -367,6 +367,10 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       // The first group's tokens do not depend on the adapter: load them
       // alongside its descriptor.
       const int first_tok = lane < min(kNT, cnt) ? (a.src == kSrcTokens ? u : a.perm[tb + lane]) : -1;
+      if (ad < 0 || ad >= v.n_adapters) {  // segments built for more adapters than the view has
+        if (crank == 0 && lane == 0) report(a.err, LORA_DERR_BAD_ADAPTER);
+        continue;
+      }
       const lora_adapter_desc_t d = v.adapters[ad];
       if (d.rank < 1 || d.rank > v.max_rank || d.rank > kHMax) {
         if (crank == 0 && lane == 0) report(a.err, LORA_DERR_BAD_RANK);

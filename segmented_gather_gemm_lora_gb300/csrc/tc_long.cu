@@ -66,9 +66,11 @@ __device__ __forceinline__ TileInfo load_tile(const int32_t* long_units, const i
   return t;
 }
 
-// Rank, every page-list slot and page of A_i and B_i, checked by one warp;
-// returns 0 or LORA_DERR_* bits (the same in every lane).
-__device__ __forceinline__ int check_adapter_warp(const DevView& v, const lora_adapter_desc_t& d, int lane) {
+// Adapter id, rank, every page-list slot and page of A_i and B_i, checked by
+// one warp; returns 0 or LORA_DERR_* bits (the same in every lane).  `d` is
+// adapter_desc(v, ad).
+__device__ __forceinline__ int check_adapter_warp(const DevView& v, int ad, const lora_adapter_desc_t& d, int lane) {
+  if (ad < 0 || ad >= v.n_adapters) return LORA_DERR_BAD_ADAPTER;
   if (d.rank < 1 || d.rank > v.max_rank || d.rank > LORA_MAX_RANK) return LORA_DERR_BAD_RANK;
   const long long na = ((long long)d.rank * v.d_in + (1LL << v.page_shift) - 1) >> v.page_shift;
   const long long nb = ((long long)d.rank * v.d_out + (1LL << v.page_shift) - 1) >> v.page_shift;
@@ -249,8 +251,8 @@ __global__ void __launch_bounds__(kSThreads, 1) shrink_tc_kernel(const __grid_co
         tile = u / ks;
         q = u - tile * ks;
         ti = load_tile(a.long_units, a.seg_adapter, a.indptr, a.perm, tile, a.use_tma);
-        d = v.adapters[ti.ad];
-        const int bad = check_adapter_warp(v, d, lane);
+        d = adapter_desc(v, ti.ad);
+        const int bad = check_adapter_warp(v, ti.ad, d, lane);
         if (bad) {
           if (lane == 0 && q == 0) report(a.err, bad);
           advance();
@@ -648,8 +650,8 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
         if (tile != cur) {
           cur = tile;
           ti = load_tile(a.long_units, a.seg_adapter, a.indptr, a.perm, tile, a.use_tma);
-          d = v.adapters[ti.ad];
-          bad = check_adapter_warp(v, d, lane);
+          d = adapter_desc(v, ti.ad);
+          bad = check_adapter_warp(v, ti.ad, d, lane);
           if (bad && lane == 0 && n0 == 0) report(a.err, bad);
           if (!bad) {
             new_tile = true;
@@ -1002,8 +1004,9 @@ __global__ void __launch_bounds__(kRThreads) reduce_partials_kernel(const __grid
   for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
     if (tid < 32) {
       const int s = a.long_units[2 * tile], m0 = a.long_units[2 * tile + 1];
-      const lora_adapter_desc_t d = a.v.adapters[a.seg_adapter[s]];
-      const int bad = check_adapter_warp(a.v, d, tid);  // the tiles the shrink skipped
+      const int ad = a.seg_adapter[s];
+      const lora_adapter_desc_t d = adapter_desc(a.v, ad);
+      const int bad = check_adapter_warp(a.v, ad, d, tid);  // the tiles the shrink skipped
       if (tid == 0) {
         info[0] = a.indptr[s] + m0;
         info[1] = min(kTM, a.indptr[s + 1] - info[0]);

@@ -346,6 +346,24 @@ def test_device_errors_flag_and_skip():
     assert np.array_equal(yc[2], batch.y0[2])
 
 
+def test_segment_ids_beyond_the_view_flag_and_skip():
+    """Segments built for more adapters than the pool view holds: the compute calls
+    check every segment's adapter id against the view (short segments on the gather
+    path, long ones on the tensor-core path) and skip those outside it."""
+    rng = np.random.default_rng(31)
+    pool = W.build_pool(rng, 2048, 2048, [16, 16, 16], max_rank=16)
+    ids = np.repeat(np.array([5, 0, 7, 1, 2, 6], dtype=np.int32), [3, 20, 150, 4, 140, 1])
+    batch = W.make_batch(rng, ids, 2048, 2048)
+    bad = ids >= 3
+    ref, oerr = oracle.lora_apply(batch.x, batch.y0, np.where(bad, -1, ids).astype(np.int32), pool)
+    assert oerr == 0
+    for mode in (B.LORA_SEG_GROUP, B.LORA_SEG_CONTIGUOUS):
+        y, err, _ = run_apply(batch, pool, mode, 8)
+        assert err == B.LORA_DERR_BAD_ADAPTER
+        compare_bf16(y[~bad], ref[~bad], "rows next to out-of-view adapters")
+        assert np.array_equal(y[bad], batch.y0[bad])
+
+
 def test_empty_batch_is_noop():
     wl = W.tiny(0)
     view = B.PoolView.from_host(wl.pools[0])
