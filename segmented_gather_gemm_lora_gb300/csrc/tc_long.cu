@@ -75,14 +75,18 @@ __device__ __forceinline__ int check_adapter_warp(const DevView& v, int ad, cons
   const long long na = ((long long)d.rank * v.d_in + (1LL << v.page_shift) - 1) >> v.page_shift;
   const long long nb = ((long long)d.rank * v.d_out + (1LL << v.page_shift) - 1) >> v.page_shift;
   int mine = 0;
-  for (long long i = lane; i < na + nb; i += 32) {
-    const long long slot = i < na ? d.a_page0 + i : d.b_page0 + (i - na);
-    if (slot < 0 || slot >= v.n_page_list) {
-      mine = 1;
-    } else {
-      const long long pg = v.page_list[slot];
-      if (pg < 0 || pg >= v.n_pages) mine = 1;
+  for (long long i0 = 0; i0 < na + nb; i0 += 32 * 8) {  // eight page-list reads in flight per lane
+    int pv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const long long i = i0 + 32 * k + lane;
+      const long long slot = i < na ? d.a_page0 + i : d.b_page0 + (i - na);
+      pv[k] = 0;
+      if (i < na + nb) pv[k] = (slot < 0 || slot >= v.n_page_list) ? -1 : v.page_list[slot];
     }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (pv[k] < 0 || pv[k] >= v.n_pages) mine = 1;
   }
   return __any_sync(0xffffffffu, mine) ? LORA_DERR_BAD_PAGE : 0;
 }
@@ -127,6 +131,7 @@ constexpr int kSXBytes = kTM * 128;  // x tile: 128 rows x 64 bf16
 constexpr int kSABytes = 64 * 128;   // A tile: up to 64 rank rows x 64 bf16
 constexpr int kSStageBytes = kSXBytes + kSABytes;
 constexpr int kSTmaRows = 64;    // x rows of a full tile that come by TMA
+static_assert(kSTmaRows % 16 == 0 && kSTmaRows <= kTM, "x rows split between TMA and the loader warps");
 constexpr int kSMaxChunks = 32;  // 64-column chunks per unit
 constexpr int kRecEnd = 1, kRecTma = 2, kRecNewTile = 4;
 
@@ -226,24 +231,31 @@ __global__ void __launch_bounds__(kSThreads, 1) shrink_tc_kernel(const __grid_co
     const int shift = v.page_shift;
     // Claims: unit sid * grid + block first, then units 2 * grid + counter.  Every
     // scheduler over-claims the counter exactly once; the last claim of all
-    // puts it back to zero for the next call.
+    // puts it back to zero for the next call.  A scheduler claims its next unit
+    // only once the loaders are done with its previous one (they meanwhile
+    // load the other scheduler's unit), so when the units run out no CTA holds
+    // more than one in reserve.
     const int g2 = kSSched * (int)gridDim.x;
     const int n_dyn = max(0, n_work - g2);
     int u = sid * (int)gridDim.x + (int)blockIdx.x;
-    int claim = 0;  // the counter's answer in flight (lane 0)
-    if (lane == 0) claim = atomicAdd(a.counter, 1);
+    int claim = 0;      // lane 0: the counter's last answer
+    bool over = false;  // lane 0: this scheduler's over-claim is made
     auto advance = [&]() {
-      const int c = __shfl_sync(0xffffffffu, claim, 0);
-      if (c < n_dyn) {
-        u = g2 + c;
-        if (lane == 0) claim = atomicAdd(a.counter, 1);
-      } else {
-        u = n_work;
+      int c = 0;
+      if (lane == 0) {
+        claim = atomicAdd(a.counter, 1);
+        c = claim;
+        over = c >= n_dyn;
       }
+      c = __shfl_sync(0xffffffffu, c, 0);
+      u = c < n_dyn ? g2 + c : n_work;
     };
     for (uint32_t k = 0;;) {
       const bool end = u >= n_work;
-      if (end && lane == 0 && claim == n_dyn + g2 - 1) *a.counter = 0;
+      if (end && lane == 0) {
+        if (!over) claim = atomicAdd(a.counter, 1);  // the first unit was already past the end
+        if (claim == n_dyn + g2 - 1) *a.counter = 0;
+      }
       TileInfo ti{};
       lora_adapter_desc_t d{};
       int tile = 0, q = 0;
@@ -281,18 +293,34 @@ __global__ void __launch_bounds__(kSThreads, 1) shrink_tc_kernel(const __grid_co
           su->flags = ti.tma ? kRecTma : 0;
         }
         int* rows = reinterpret_cast<int*>(slot + 64);  // x row of each tile row, -1 past the tile
-        for (int m = lane; m < kTM; m += 32)
-          rows[m] = m >= ti.cnt ? -1 : ti.tma ? ti.row0 + m : a.perm[ti.p0 + m];
+        int rv[kTM / 32];  // every lane's loads in flight before the stores
+#pragma unroll
+        for (int i = 0; i < kTM / 32; ++i) {
+          const int m = lane + 32 * i;
+          rv[i] = m >= ti.cnt ? -1 : ti.tma ? ti.row0 + m : a.perm[ti.p0 + m];
+        }
+#pragma unroll
+        for (int i = 0; i < kTM / 32; ++i) rows[lane + 32 * i] = rv[i];
         int* pg = reinterpret_cast<int*>(slot + 64 + kTM * 4);  // [64][kSMaxChunks]
-        for (int i = lane; i < r * nch; i += 32) {
-          const int jr = i / nch, c = i - jr * nch;
-          const long long e = (long long)jr * v.d_in + kbeg + 64 * c;
-          pg[jr * kSMaxChunks + c] = v.page_list[d.a_page0 + (e >> shift)];
+        for (int i0 = 0; i0 < r * nch; i0 += 32 * 8) {  // eight page-list reads in flight per lane
+          int pv[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int i = i0 + 32 * k + lane, jr = i / nch, c = i - jr * nch;
+            const long long e = (long long)jr * v.d_in + kbeg + 64 * c;
+            pv[k] = i < r * nch ? v.page_list[d.a_page0 + (e >> shift)] : 0;
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int i = i0 + 32 * k + lane, jr = i / nch, c = i - jr * nch;
+            if (i < r * nch) pg[jr * kSMaxChunks + c] = pv[k];
+          }
         }
       }
       mbar_arrive(smem_u32(&uq_full[qs]));  // each lane after its own writes
       ++k;
       if (end) break;
+      if (!mbar_wait(smem_u32(&uq_empty[qs]), ((k - 1) >> 1) & 1)) ok = false;  // the loaders are done with it
       advance();
     }
     if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
@@ -329,8 +357,9 @@ __global__ void __launch_bounds__(kSThreads, 1) shrink_tc_kernel(const __grid_co
       const int* pg = reinterpret_cast<const int*>(slot + 64 + kTM * 4);
       // x rows of this thread: m = base + (lane >> 3) + 4 t, 16-byte piece lane & 7
       const int p = lane & 7;
-      const int xbase = tma ? kSTmaRows + 16 * lw : 32 * lw;
-      const int xcnt = tma ? 4 : 8;
+      constexpr int kXPer = (kTM - kSTmaRows) / kSLoad;  // cp.async x rows per loader warp, TMA tiles
+      const int xbase = tma ? kSTmaRows + kXPer * lw : 32 * lw;
+      const int xcnt = tma ? kXPer / 4 : 8;
       const uint16_t* xsrc[8];
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
@@ -627,14 +656,19 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
     };
     // Claims: group blockIdx.x first, then groups grid + counter.  The scheduler
     // over-claims the counter exactly once; the last claim of all puts it back
-    // to zero for the next call.
+    // to zero for the next call.  The next group is claimed once the loaders
+    // are done with all but the last two units of this one, so that when the
+    // groups run out no CTA holds much more than the group it is on.
     const int n_dyn = max(0, n_claims - (int)gridDim.x);
     int c = blockIdx.x;
-    int claim = 0;  // the counter's answer in flight (lane 0)
-    if (lane == 0) claim = atomicAdd(a.counter, 1);
+    int claim = 0;      // lane 0: the counter's last answer
+    bool over = false;  // lane 0: the over-claim is made
     for (;;) {
       if (c >= n_claims) {
-        if (lane == 0 && claim == n_dyn + (int)gridDim.x - 1) *a.counter = 0;
+        if (lane == 0) {
+          if (!over) claim = atomicAdd(a.counter, 1);  // the first group was already past the end
+          if (claim == n_dyn + (int)gridDim.x - 1) *a.counter = 0;
+        }
         uint8_t* slot = take_slot();
         if (lane == 0) reinterpret_cast<EUnit*>(slot)->flags = kRecEnd;
         mbar_arrive(smem_u32(&uq_full[j % kEQ]));
@@ -697,18 +731,30 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
 #pragma unroll
         for (int i = 0; i < 4; ++i) srows[lane + 32 * i] = rows[i];
         int* pgb = reinterpret_cast<int*>(slot + kERecBytes);
-        for (int jr = lane; jr < d.rank; jr += 32)
-          pgb[jr] = v.page_list[d.b_page0 + (((long long)jr * v.d_out + n0) >> shift)];
+        int pv[LORA_MAX_RANK / 32];  // both reads in flight before the stores
+#pragma unroll
+        for (int i = 0; i < LORA_MAX_RANK / 32; ++i) {
+          const int jr = lane + 32 * i;
+          pv[i] = jr < d.rank ? v.page_list[d.b_page0 + (((long long)jr * v.d_out + n0) >> shift)] : 0;
+        }
+#pragma unroll
+        for (int i = 0; i < LORA_MAX_RANK / 32; ++i)
+          if (lane + 32 * i < d.rank) pgb[lane + 32 * i] = pv[i];
         mbar_arrive(smem_u32(&uq_full[j % kEQ]));  // each lane after its own writes
         ++j;
       }
-      const int cn = __shfl_sync(0xffffffffu, claim, 0);
-      if (cn < n_dyn) {
-        c = (int)gridDim.x + cn;
-        if (lane == 0) claim = atomicAdd(a.counter, 1);
-      } else {
-        c = n_claims;
+      if (j >= 2) {
+        const uint32_t jd = j - 2;
+        if (!mbar_wait(smem_u32(&uq_empty[jd % kEQ]), (jd / kEQ) & 1)) ok = false;
       }
+      int cn = 0;
+      if (lane == 0) {
+        claim = atomicAdd(a.counter, 1);
+        cn = claim;
+        over = cn >= n_dyn;
+      }
+      cn = __shfl_sync(0xffffffffu, cn, 0);
+      c = cn < n_dyn ? (int)gridDim.x + cn : n_claims;
     }
     if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
   } else if (warp < kEWarpMma) {
