@@ -72,7 +72,7 @@ enum GFlag {
 // What the producer tells the consumers about a stage.  The group's reduction
 // rides on its last shrink chunk, so only a CTA without a d_in slice spends a
 // stage on a record without data.
-struct GRec {
+struct __align__(16) GRec {
   int kind;
   int ntok;   // tokens of the group
   int j0;     // first adapter row of the chunk
@@ -84,7 +84,19 @@ struct GRec {
   float sc;   // scale
   int tok[kNT];
 };
-static_assert(sizeof(GRec) <= 64, "record slot");
+static_assert(sizeof(GRec) <= 64 && sizeof(GRec) % 16 == 0, "record slot, read as 16-byte pieces");
+
+// A stage's record, by 16-byte shared-memory loads (one per piece, all in
+// flight together) rather than one load per field.
+__device__ __forceinline__ GRec load_rec(const GRec* p) {
+  union {
+    GRec r;
+    uint4 v[sizeof(GRec) / 16];
+  } u;
+#pragma unroll
+  for (int i = 0; i < (int)(sizeof(GRec) / 16); ++i) u.v[i] = reinterpret_cast<const uint4*>(p)[i];
+  return u.r;
+}
 
 // What the scheduler tells the producer about a unit it has resolved: the
 // adapter's rank, scale and page-list origin, the unit's tokens, and whether
@@ -141,9 +153,10 @@ struct GatherArgs {
 // 8w .. 8w + 7 of every sub-slice; lane = 2 i + half takes chunk row i and four
 // of those vectors (half 0 the first four, half 1 the last four), visiting them
 // in an order rotated by the row so that one load instruction of the warp
-// touches every bank four times.  The lane's dot products accumulate in
-// registers over the row block's sub-slices (in order); the two halves of a
-// row meet when the block's last sub-slice is done.
+// touches every bank four times.  Per chunk each vector's 8-term dot product
+// is its own chain and the four meet as (v0 + v1) + (v2 + v3); the lane's sums
+// accumulate in registers over the row block's sub-slices (in order); the two
+// halves of a row meet when the block's last sub-slice is done.
 template <int NT>
 __device__ __forceinline__ void shrink_chunk(const uint8_t* sb, int nrows, int nvec, float (&acc)[kNT], int warp,
                                              int lane) {
@@ -160,28 +173,30 @@ __device__ __forceinline__ void shrink_chunk(const uint8_t* sb, int nrows, int n
   }
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
-    float s = acc[t];
+    float p[4];  // one partial per vector (independent chains), then a fixed combination
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int vv = v0 + ((k + i) & 3);
+      p[k] = 0.f;
       if (vv < nvec) {
         float af[8], xf[8];
         unpack8(av[k], af);
         unpack8(xrow[t * (kRowBytes / 16) + vv], xf);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) s = fmaf(af[q], xf[q], s);
+        for (int q = 0; q < 8; ++q) p[k] = fmaf(af[q], xf[q], p[k]);
       }
     }
-    acc[t] = s;
+    acc[t] += (p[0] + p[1]) + (p[2] + p[3]);
   }
 }
 
 // Expand of one staged chunk.  Lane l of warp w owns the two output columns
 // of 32-bit word 32 w + l of the sub-slice, for every token, so the sum over
 // the adapter's rows runs in the lane's registers from the sub-slice's first
-// row block to its last, in row order, with no exchange between lanes; one
-// load instruction of the warp reads 128 contiguous bytes of a row.  The
-// sub-slice's last chunk adds y0 and writes y.
+// row block to its last, with no exchange between lanes: per chunk, even and
+// odd rows in two chains (rows ascending) whose sum is added to the running
+// total.  One load instruction of the warp reads 128 contiguous bytes of a
+// row.  The sub-slice's last chunk adds y0 and writes y.
 __device__ __forceinline__ void expand_chunk(uint16_t* ybase, long long ldy, const uint8_t* sb, const float* hs,
                                              float (&acc)[kNT][2], const GRec& rc, bool ok, int warp, int lane) {
   const int m = warp * 32 + lane;
@@ -198,23 +213,30 @@ __device__ __forceinline__ void expand_chunk(uint16_t* ybase, long long ldy, con
   for (int t = 0; t < kNT; ++t) {
     if (t >= rc.ntok) break;
     const float4* h4 = reinterpret_cast<const float4*>(hs + t * kHMax + rc.j0);
-    float s0 = acc[t][0], s1 = acc[t][1];
+    float4 hv[kChunkRows / 4];
+#pragma unroll
+    for (int i4 = 0; i4 < kChunkRows / 4; ++i4) hv[i4] = h4[i4];  // rows past nrows are read, not used
+    // even and odd rows in separate chains, combined in a fixed order
+    float e0 = 0.f, e1 = 0.f, o0 = 0.f, o1 = 0.f;
 #pragma unroll
     for (int i4 = 0; i4 < kChunkRows / 4; ++i4) {
-      if (4 * i4 >= rc.nrows) break;
-      const float4 hv = h4[i4];
-      const float he[4] = {hv.x, hv.y, hv.z, hv.w};
+      const float he[4] = {hv[i4].x, hv[i4].y, hv[i4].z, hv[i4].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = 4 * i4 + e;
         if (i < rc.nrows) {
-          s0 = fmaf(he[e], bf_lo(bw[i]), s0);
-          s1 = fmaf(he[e], bf_hi(bw[i]), s1);
+          if (e & 1) {
+            o0 = fmaf(he[e], bf_lo(bw[i]), o0);
+            o1 = fmaf(he[e], bf_hi(bw[i]), o1);
+          } else {
+            e0 = fmaf(he[e], bf_lo(bw[i]), e0);
+            e1 = fmaf(he[e], bf_hi(bw[i]), e1);
+          }
         }
       }
     }
-    acc[t][0] = s0;
-    acc[t][1] = s1;
+    acc[t][0] += e0 + o0;
+    acc[t][1] += e1 + o1;
   }
   if ((rc.flags & kFLast) && ok) {
 #pragma unroll
@@ -583,7 +605,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         ok = false;
         break;
       }
-      const GRec rc = recs[st];  // in registers: every field is used below
+      const GRec rc = load_rec(&recs[st]);  // in registers: every field is used below
       if (rc.kind == kGEnd) break;
       const uint8_t* sb = sm + (size_t)st * kStageBytes;
       const int b = ngroup & 1;
