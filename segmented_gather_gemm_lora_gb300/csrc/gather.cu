@@ -122,8 +122,9 @@ constexpr size_t kOffHs = kOffRecv + 2 * (size_t)kMaxCluster * kNT * kHMax * siz
 constexpr size_t kOffPgt = kOffHs + kNT * kHMax * sizeof(float);          // int [2][kMaxPgSlots]
 constexpr size_t kOffUnit = kOffPgt + 2 * kMaxPgSlots * sizeof(int);      // GUnit [2], 64-byte slots
 constexpr size_t kOffClaim = kOffUnit + 2 * 64;                           // int [2]
-constexpr size_t kOffBars = kOffClaim + 16;
-constexpr int kNBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1;
+constexpr size_t kOffCls = kOffClaim + 16;                                // uint32 [3][32] unit classes
+constexpr size_t kOffBars = kOffCls + 3 * 32 * sizeof(uint32_t);
+constexpr int kNBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1 + 1;
 constexpr size_t kGatherSmem = kOffBars + kNBars * 8;
 
 struct GatherArgs {
@@ -258,6 +259,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   int* pgt = reinterpret_cast<int*>(sm + kOffPgt);
   GUnit* units = reinterpret_cast<GUnit*>(sm + kOffUnit);
   int* claim_val = reinterpret_cast<int*>(sm + kOffClaim);
+  uint32_t* cls = reinterpret_cast<uint32_t*>(sm + kOffCls);  // CTA 0: claimable units by class
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBars);
   uint64_t* full = bars;                   // [stages] the record writer (+ the copies' bytes)
   uint64_t* empty = bars + kStages;        // [stages] 8 consumer warps
@@ -267,6 +269,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   uint64_t* unit_full = claim_empty + 2;   // [2] the scheduler
   uint64_t* unit_empty = unit_full + 2;    // [2] the producer
   uint64_t* cons = unit_empty + 2;         // 8 consumer warps, twice per group
+  uint64_t* cls_ready = cons + 1;          // 8 consumer warps, once
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t crank = cluster_ctarank(), ncta = cluster_nctarank();
@@ -288,8 +291,10 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       mbar_init(smem_u32(&unit_empty[b]), 1);
     }
     mbar_init(smem_u32(cons), kGCons);
+    mbar_init(smem_u32(cls_ready), kGCons);
     fence_mbar_init();
   }
+  if (tid < 3 * 32) cls[tid] = 0u;
   // every barrier of every CTA initialised before any peer arrives on it
   cluster_sync();
   pdl_wait_then_release();
@@ -301,25 +306,66 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   const int nks = (a.mode != kModeExpand && k1 > k0) ? (k1 - k0 + kSub - 1) / kSub : 0;
   const int nns = (a.mode != kModeShrink && n1 > n0) ? (n1 - n0 + kSub - 1) / kSub : 0;
   bool ok = true;
+  const int n_short = a.src == kSrcSegments ? a.meta[2] : 0;
+  const int n_units = a.src == kSrcTokens ? a.T : a.meta[2] + (a.short_only ? 0 : a.meta[3]);
+  const int n_dyn = max(0, n_units - (int)ncl);  // units claimed from the counter
+  // Order of the claimed units: largest first.  A unit's time grows with its
+  // adapter's row blocks, and a cluster that draws a large unit last keeps the
+  // call waiting; so CTA 0's consumer warps, idle until the first chunk lands,
+  // classify the claimable units (more than two row blocks, two, one) into bit
+  // masks (word L holds units ncl + 32 L + b), and CTA 0's scheduler maps
+  // counter value c to the c-th unit of that order (segment order within a
+  // class).  Up to 1024 claimable units; beyond, segment order.
+  const bool ordered = dynamic && crank == 0 && n_dyn <= 32 * 32;
 
   if (warp == kGSched) {
     // ---------------- scheduler ----------------
     // Claims a unit, resolves its segment, tokens and adapter, checks every
     // page slot of the adapter and caches the physical pages, a unit ahead of
     // the producer (two unit slots).
-    const int n_short = a.src == kSrcSegments ? a.meta[2] : 0;
-    const int n_units = a.src == kSrcTokens ? a.T : a.meta[2] + (a.short_only ? 0 : a.meta[3]);
     const int shift = v.page_shift;
     // Claims: unit cid first, then units ncl + counter, CTA 0 claiming for the
     // cluster.  Each cluster over-claims the counter exactly once; the last
     // claim of all puts it back to zero for the next call.  A unit is claimed
     // only once the producer has started on the previous one, so that when
     // the units run out no cluster holds more than one in reserve.
-    const int n_dyn = max(0, n_units - (int)ncl);
     int u = (int)cid;
     int claim = 0;      // CTA 0, lane 0: the counter's last answer
     bool over = false;  // CTA 0, lane 0: this cluster's over-claim is made
     uint32_t nclaim = 0;
+    uint32_t cmask[3] = {0u, 0u, 0u};  // CTA 0: this lane's units of each class
+    int cpre[3] = {0, 0, 0};           // CTA 0: units of the class in lower lanes
+    int ctot[3] = {0, 0, 0};           // CTA 0: units of the class
+    auto classify = [&]() {  // the consumers' masks, then each class's prefix over the lanes
+      if (!mbar_wait(smem_u32(cls_ready), 0)) ok = false;
+#pragma unroll
+      for (int c = 0; c < 3; ++c) cmask[c] = cls[c * 32 + lane];
+#pragma unroll
+      for (int c = 0; c < 3; ++c) {
+        const int n = __popc(cmask[c]);
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        cpre[c] = incl - n;
+        ctot[c] = __shfl_sync(0xffffffffu, incl, 31);
+      }
+    };
+    // the unit of the c-th claim, c < n_dyn (every lane of CTA 0's warp)
+    auto ordered_unit = [&](int c) -> int {
+      const int k = c < ctot[0] ? 0 : c < ctot[0] + ctot[1] ? 1 : 2;
+      const int n = c - (k > 0 ? ctot[0] : 0) - (k > 1 ? ctot[1] : 0);
+      const uint32_t m = k == 0 ? cmask[0] : k == 1 ? cmask[1] : cmask[2];
+      const int pre = k == 0 ? cpre[0] : k == 1 ? cpre[1] : cpre[2];
+      const uint32_t hit = __ballot_sync(0xffffffffu, pre <= n && n < pre + __popc(m));
+      const int owner = __ffs(hit) - 1;
+      uint32_t mm = m;  // the (n - pre)-th set bit of the owner's mask
+      for (int j = 0; j < n - pre && j < 32; ++j) mm &= mm - 1;
+      const int bit = __ffs(mm) - 1;
+      return (int)ncl + 32 * owner + __shfl_sync(0xffffffffu, bit, owner);
+    };
     auto next_unit = [&]() {
       if (!dynamic) {
         u += (int)ncl;
@@ -327,6 +373,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       }
       const int q = nclaim & 1;
       if (crank == 0) {
+        if (ordered && nclaim == 0) classify();
         int nu = 0;
         if (lane == 0) {
           if (nclaim >= 2 && !mbar_wait_cluster(smem_u32(&claim_empty[q]), ((nclaim >> 1) - 1) & 1)) ok = false;
@@ -339,6 +386,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
           }
         }
         nu = __shfl_sync(0xffffffffu, nu, 0);
+        if (ordered && nu < n_units) nu = ordered_unit(nu - (int)ncl);
         __syncwarp();  // lane 0 saw every CTA done with this slot before any lane rewrites it
         // lane p hands the claim to CTA p
         if (lane < (int)ncta) {
@@ -593,6 +641,28 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
     float eacc[kNT][2];  // expand: the lane's two outputs over a sub-slice's row blocks
 #pragma unroll
     for (int t = 0; t < kNT; ++t) sacc[t] = eacc[t][0] = eacc[t][1] = 0.f;
+    if (ordered) {  // classify the claimable units: four per thread, every load in flight
+      int val[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = ctid + kGConsThreads * k, uu = (int)ncl + i;
+        val[k] = i >= n_dyn ? -1 : uu < n_short ? a.short_units[uu] : a.long_units[2 * (uu - n_short)];
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) val[k] = val[k] < 0 ? -1 : a.seg_adapter[val[k]];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) val[k] = val[k] < 0 || val[k] >= v.n_adapters ? 0 : v.adapters[val[k]].rank;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = ctid + kGConsThreads * k;
+        if (i < n_dyn) {
+          const int nb = (val[k] + kChunkRows - 1) / kChunkRows;  // a bad adapter falls in the last class
+          atomicOr(&cls[(nb > 2 ? 0 : nb == 2 ? 1 : 2) * 32 + (i >> 5)], 1u << (i & 31));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(cls_ready));
+    }
     auto cons_sync = [&]() {  // the 8 consumer warps, bounded
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(cons));
