@@ -1026,6 +1026,8 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
 // the threads, every slice's load in flight before the sums.
 
 constexpr int kRThreads = 256;
+constexpr int kRRows = 32;              // rows of a tile per work item
+constexpr int kRGroups = kTM / kRRows;  // work items per tile
 
 struct ReduceArgs {
   const float* part;
@@ -1047,7 +1049,10 @@ __global__ void __launch_bounds__(kRThreads) reduce_partials_kernel(const __grid
   pdl_wait_then_release();
   const int n_tiles = a.meta[3];
   const int tid = threadIdx.x;
-  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+  // work item: (tile, group of kRRows rows), so a batch of few tiles still spreads
+  // over many CTAs
+  for (int w = blockIdx.x; w < n_tiles * kRGroups; w += gridDim.x) {
+    const int tile = w / kRGroups, rg = w - tile * kRGroups;
     if (tid < 32) {
       const int s = a.long_units[2 * tile], m0 = a.long_units[2 * tile + 1];
       const int ad = a.seg_adapter[s];
@@ -1063,15 +1068,15 @@ __global__ void __launch_bounds__(kRThreads) reduce_partials_kernel(const __grid
     __syncthreads();
     const int p0 = info[0], cnt = info[1], r = info[2], skip = info[3];
     __syncthreads();
-    if (skip) continue;
-    const int nq4 = (r + 3) / 4, npairs = cnt * nq4;
+    if (skip || rg * kRRows >= cnt) continue;
+    const int rbase = rg * kRRows, nq4 = (r + 3) / 4, npairs = min(kRRows, cnt - rbase) * nq4;
     for (int i0 = tid; i0 < npairs; i0 += 2 * kRThreads) {
       float4 pv[LORA_KSPLIT_MAX][2];
       long long hrow[2];
 #pragma unroll
       for (int b2 = 0; b2 < 2; ++b2) {
         const int i = i0 + kRThreads * b2;
-        const int row = i / nq4, j = (i - row * nq4) * 4;
+        const int row = rbase + i / nq4, j = (i % nq4) * 4;
         hrow[b2] = i < npairs ? (a.h_by_token ? (long long)a.perm[p0 + row] : (long long)(p0 + row)) : 0;
 #pragma unroll
         for (int qq = 0; qq < LORA_KSPLIT_MAX; ++qq)
@@ -1204,7 +1209,7 @@ lora_status_t launch_shrink_tc(const void* x, long long ldx, float* h, long long
   ra.long_units = a.long_units;
   ra.meta = a.meta;
   long long rgrid = (long long)sm_count() * 4;
-  if (seg->max_long_units < rgrid) rgrid = seg->max_long_units;
+  if ((long long)seg->max_long_units * kRGroups < rgrid) rgrid = (long long)seg->max_long_units * kRGroups;
   return launch_pdl((const void*)reduce_partials_kernel, dim3((unsigned)rgrid), dim3(kRThreads), 0, stream, 0,
                     &ra) == cudaSuccess
              ? LORA_OK
