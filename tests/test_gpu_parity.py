@@ -138,6 +138,24 @@ def test_apply_hetero(which):
     check_untouched(y, batch, pool, np.where(batch.ids < 0)[0])
 
 
+@pytest.mark.parametrize("n_units", [600, 1500])
+def test_gather_claim_order_many_units_mixed_ranks(n_units):
+    """Short segments of mixed ranks: with a few hundred units the gather kernel claims them
+    largest adapter first; beyond 1024 claimable units it claims them in segment order.
+    Either way every token's output matches the oracle, and every unit runs once."""
+    rng = np.random.default_rng(40 + n_units)
+    ranks = rng.choice(np.array([1, 8, 16, 17, 32, 33, 48, 64], dtype=np.int32), size=n_units)
+    pool = W.build_pool(rng, 512, 768, ranks, max_rank=64)
+    ids = rng.permutation(np.repeat(np.arange(n_units, dtype=np.int32), rng.integers(1, 3, size=n_units)))
+    ids[rng.random(ids.size) < 0.05] = -1
+    batch = W.make_batch(rng, ids, 512, 768)
+    ref, oerr = oracle.lora_apply(batch.x, batch.y0, ids, pool)
+    y, err, _ = run_apply(batch, pool, B.LORA_SEG_GROUP, n_units)
+    assert err == oerr == 0
+    compare_bf16(y, ref, "claim order, %d units" % n_units)
+    assert np.array_equal(y[ids < 0], batch.y0[ids < 0])
+
+
 def test_apply_odd_shapes_and_ranks():
     """Ranks that divide nothing, widths that are not multiples of the page, rows that
     straddle pages, segment lengths around the dispatch thresholds, and -1 tokens."""
