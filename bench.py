@@ -444,6 +444,33 @@ def run_ours(args, world, rank, local):
     c1.record()
     torch.cuda.synchronize()
     calls_avg_s = c0.elapsed_time(c1) / (call_reps * g_steps) / 1e3
+
+    # single-call latency (one eager call group on an idle GPU, not graph-amortised) and
+    # the same calls with a warm L2 (one input set, back to back in a graph)
+    lat = []
+    for i in range(20):
+        torch.cuda.synchronize()
+        c0.record()
+        calls_of(sets[i % n_sets])
+        c1.record()
+        torch.cuda.synchronize()
+        lat.append(c0.elapsed_time(c1) * 1e3)
+    single_us = statistics.median(lat)
+    hot_us = None
+    if args.workload != "mixed13b":
+        hot_graph = torch.cuda.CUDAGraph()
+        n_hot = max(1, 64 // n_calls)
+        with torch.cuda.graph(hot_graph, stream=cap):
+            for _ in range(n_hot):
+                calls_of(sets[0])
+        hot_graph.replay()
+        torch.cuda.synchronize()
+        c0.record()
+        for _ in range(5):
+            hot_graph.replay()
+        c1.record()
+        torch.cuda.synchronize()
+        hot_us = c0.elapsed_time(c1) * 1e3 / (5 * n_hot)
     bytes_avg = statistics.fmean(sum(c["bytes"] for c in sets[k % n_sets]["calls"]) for k in range(g_steps))
     flops_avg = statistics.fmean(sum(c["flops"] for c in sets[k % n_sets]["calls"]) for k in range(g_steps))
     hbm_peak, tc_peak, peak_kind = read_peaks()
@@ -555,6 +582,9 @@ def run_ours(args, world, rank, local):
             "tflops": flops_avg / calls_avg_s / 1e12,
         },
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "call_timing": {"graph_us": calls_avg_s * 1e6, "single_launch_us": single_us, "hot_l2_us": hot_us,
+                        "note": "the step's projection calls: graph-amortised over rotating sets (cold L2), "
+                                "one eager launch group on an idle GPU, and one set repeated (warm L2)"},
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
