@@ -281,12 +281,14 @@ static lora_status_t run_segmented(int mode, const void* x, long long ldx, void*
   lora_status_t st = launch_gather(mode, kSrcSegments, tc ? 1 : 0, x, ldx, y, ldy, h, ldh, seg, nullptr, 0, view,
                                    dev_err, s);
   if (st != LORA_OK || !tc) return st;
+  // the gather kernel was launched iff the buffer has tokens (its short-only bound is T)
+  const int after_gather = seg->T > 0 ? 1 : 0;
   if (mode == kModeApply) {
-    st = launch_shrink_tc(x, ldx, seg->h_scratch, LORA_MAX_RANK, 0, seg, view, dev_err, s);
+    st = launch_shrink_tc(x, ldx, seg->h_scratch, LORA_MAX_RANK, 0, after_gather, seg, view, dev_err, s);
     if (st != LORA_OK) return st;
     return launch_expand_tc(seg->h_scratch, LORA_MAX_RANK, 0, y, ldy, seg, view, dev_err, s);
   }
-  if (mode == kModeShrink) return launch_shrink_tc(x, ldx, h, ldh, 1, seg, view, dev_err, s);
+  if (mode == kModeShrink) return launch_shrink_tc(x, ldx, h, ldh, 1, after_gather, seg, view, dev_err, s);
   return launch_expand_tc(h, ldh, 1, y, ldy, seg, view, dev_err, s);
 }
 

@@ -184,6 +184,16 @@ __device__ __forceinline__ void pdl_wait_then_release() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// The same, or, when `after_independent` is set, only the release: for a grid
+// launched right after a library kernel that itself waited for everything
+// before it (its CTAs release their dependents only after that wait) and that
+// touches none of this grid's data.  Everything this grid reads was then
+// complete before it started.
+__device__ __forceinline__ void pdl_enter(bool after_independent) {
+  if (!after_independent) asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- bf16 --
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }

@@ -50,7 +50,9 @@ lora_status_t launch_gather(int mode, int src, int short_only, const void* x, lo
 // d_out % 128 == 0 (expand), pages of at least 128 elements.
 bool tc_shrink_ok(const lora_pool_view_t* v);
 bool tc_expand_ok(const lora_pool_view_t* v);
-lora_status_t launch_shrink_tc(const void* x, long long ldx, float* h, long long ldh, int h_by_token,
+// after_gather: the gather kernel of the same call was launched just before
+// (the two touch disjoint data), so this grid need not wait for it.
+lora_status_t launch_shrink_tc(const void* x, long long ldx, float* h, long long ldh, int h_by_token, int after_gather,
                                const lora_segments_t* seg, const lora_pool_view_t* view, int32_t* err,
                                cudaStream_t stream);
 lora_status_t launch_expand_tc(const float* h, long long ldh, int h_by_token, void* y, long long ldy,

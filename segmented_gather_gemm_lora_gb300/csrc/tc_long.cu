@@ -160,6 +160,10 @@ struct ShrinkArgs {
   long long ldh;
   int h_by_token;  // h rows by token (caller's h) or by segment position (scratch)
   int use_tma;
+  // Launched right after this call's gather kernel, which waited for every earlier
+  // grid before releasing this one and writes only y / h rows of short segments
+  // and its own counter: nothing to wait for.
+  int after_gather;
   float* part;  // [ksplit][T][LORA_MAX_RANK] partial sums by segment position
   int32_t* counter;  // work counter (zero between calls)
   DevView v;
@@ -219,7 +223,7 @@ __global__ void __launch_bounds__(kSThreads, 1) shrink_tc_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait_then_release();
+  pdl_enter(a.after_gather != 0);
 
   const int ks = a.ksplit;
   bool ok = true;
@@ -1171,7 +1175,7 @@ bool tc_shrink_ok(const lora_pool_view_t* v) {
 
 bool tc_expand_ok(const lora_pool_view_t* v) { return v->d_out % kENC == 0 && v->page_elems >= kENC; }
 
-lora_status_t launch_shrink_tc(const void* x, long long ldx, float* h, long long ldh, int h_by_token,
+lora_status_t launch_shrink_tc(const void* x, long long ldx, float* h, long long ldh, int h_by_token, int after_gather,
                                const lora_segments_t* seg, const lora_pool_view_t* view, int32_t* err,
                                cudaStream_t stream) {
   ShrinkArgs a;
@@ -1186,6 +1190,7 @@ lora_status_t launch_shrink_tc(const void* x, long long ldx, float* h, long long
   a.h = h;
   a.ldh = ldh;
   a.h_by_token = h_by_token;
+  a.after_gather = after_gather;
   a.part = seg->k_partials;
   a.counter = seg->meta + 5;
   a.T = seg->T;
