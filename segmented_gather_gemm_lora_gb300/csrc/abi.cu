@@ -286,10 +286,10 @@ static lora_status_t run_segmented(int mode, const void* x, long long ldx, void*
   if (mode == kModeApply) {
     st = launch_shrink_tc(x, ldx, seg->h_scratch, LORA_MAX_RANK, 0, after_gather, seg, view, dev_err, s);
     if (st != LORA_OK) return st;
-    return launch_expand_tc(seg->h_scratch, LORA_MAX_RANK, 0, y, ldy, seg, view, dev_err, s);
+    return launch_expand_tc(seg->h_scratch, LORA_MAX_RANK, 0, 0, y, ldy, seg, view, dev_err, s);
   }
   if (mode == kModeShrink) return launch_shrink_tc(x, ldx, h, ldh, 1, after_gather, seg, view, dev_err, s);
-  return launch_expand_tc(h, ldh, 1, y, ldy, seg, view, dev_err, s);
+  return launch_expand_tc(h, ldh, 1, after_gather, y, ldy, seg, view, dev_err, s);
 }
 
 lora_status_t lora_sgmv_shrink(const void* x, int64_t ldx, float* h, int64_t ldh,

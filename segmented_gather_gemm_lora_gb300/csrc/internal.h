@@ -55,7 +55,9 @@ bool tc_expand_ok(const lora_pool_view_t* v);
 lora_status_t launch_shrink_tc(const void* x, long long ldx, float* h, long long ldh, int h_by_token, int after_gather,
                                const lora_segments_t* seg, const lora_pool_view_t* view, int32_t* err,
                                cudaStream_t stream);
-lora_status_t launch_expand_tc(const float* h, long long ldh, int h_by_token, void* y, long long ldy,
+// after_gather: as for launch_shrink_tc; only in expand-only calls (lora_apply's
+// expand reads the h its shrink wrote and waits).
+lora_status_t launch_expand_tc(const float* h, long long ldh, int h_by_token, int after_gather, void* y, long long ldy,
                                const lora_segments_t* seg, const lora_pool_view_t* view, int32_t* err,
                                cudaStream_t stream);
 

@@ -578,6 +578,7 @@ struct ExpandArgs {
   long long ldh;
   int h_by_token;
   int use_tma;
+  int after_gather;  // expand-only call, launched right after its gather kernel: no wait
   int32_t* counter;  // work counter (zero between calls)
   DevView v;
   const int32_t* perm;
@@ -638,7 +639,7 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait_then_release();
+  pdl_enter(a.after_gather != 0);
   bool ok = true;
 
   if (warp == 0) {
@@ -1221,7 +1222,7 @@ lora_status_t launch_shrink_tc(const void* x, long long ldx, float* h, long long
              : LORA_ERR_CUDA;
 }
 
-lora_status_t launch_expand_tc(const float* h, long long ldh, int h_by_token, void* y, long long ldy,
+lora_status_t launch_expand_tc(const float* h, long long ldh, int h_by_token, int after_gather, void* y, long long ldy,
                                const lora_segments_t* seg, const lora_pool_view_t* view, int32_t* err,
                                cudaStream_t stream) {
   ExpandArgs a;
@@ -1236,6 +1237,7 @@ lora_status_t launch_expand_tc(const float* h, long long ldh, int h_by_token, vo
   a.h = h;
   a.ldh = ldh;
   a.h_by_token = h_by_token;
+  a.after_gather = after_gather;
   fill_common(&a, seg, view, err);
   if (ensure_smem_attr((const void*)expand_tc_kernel, kExpandSmem) != cudaSuccess) return LORA_ERR_CUDA;
   return launch_pdl((const void*)expand_tc_kernel, dim3((unsigned)grid), dim3(kEThreads), kExpandSmem, stream, 0,
