@@ -188,10 +188,19 @@ __device__ __forceinline__ void pdl_wait_then_release() {
 // launched right after a library kernel that itself waited for everything
 // before it (its CTAs release their dependents only after that wait) and that
 // touches none of this grid's data.  Everything this grid reads was then
-// complete before it started.
+// complete before it started.  Such a grid calls pdl_exit before it ends.
 __device__ __forceinline__ void pdl_enter(bool after_independent) {
   if (!after_independent) asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// For a grid that entered with pdl_enter(true): wait for the predecessor before
+// ending, so that this grid's completion still implies its predecessor's and the
+// grids after it (which wait only for this one) see every earlier write.  The
+// predecessor's CTAs are all resident by then (they released this grid), so
+// the wait cannot hold up their progress.
+__device__ __forceinline__ void pdl_exit(bool after_independent) {
+  if (after_independent) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------------- bf16 --

@@ -525,6 +525,7 @@ __global__ void __launch_bounds__(kSThreads, 1) shrink_tc_kernel(const __grid_co
   tc_fence_before();
   __syncthreads();
   if (warp == kSWarpMma) tmem_dealloc(tmem, 128);
+  pdl_exit(a.after_gather != 0);
 }
 
 // ---------------------------------------------------------------- expand_tc --
@@ -1021,6 +1022,7 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
   tc_fence_before();
   __syncthreads();
   if (warp == kEWarpMma) tmem_dealloc(tmem, 256);
+  pdl_exit(a.after_gather != 0);
 }
 
 // ---------------------------------------------------------- reduce_partials --
