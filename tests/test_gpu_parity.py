@@ -382,6 +382,54 @@ def test_segment_ids_beyond_the_view_flag_and_skip():
         assert np.array_equal(y[bad], batch.y0[bad])
 
 
+def test_graph_chain_sees_every_row_of_the_previous_call():
+    """Two lora_apply calls in one CUDA graph, the second reading the first's y as its x,
+    over a batch with both short segments (gather kernel) and long ones (tensor-core
+    kernels), replayed many times: every replay equals the chain run call by call with
+    a synchronisation in between, bit for bit.  The tensor-core shrink starts without
+    waiting for the same call's gather kernel, so this checks that the next call still
+    sees the gather's rows."""
+    rng = np.random.default_rng(53)
+    d = 1024
+    pool = W.build_pool(rng, d, d, [16, 32, 8, 64] * 8, max_rank=64)
+    ids = np.concatenate([np.full(300, 3, dtype=np.int32), rng.permutation(np.arange(4, 32, dtype=np.int32)),
+                          np.full(140, 1, dtype=np.int32), np.arange(4, 12, dtype=np.int32)])
+    ids = rng.permutation(ids).astype(np.int32)
+    batch = W.make_batch(rng, ids, d, d)
+    view = B.PoolView.from_host(pool)
+    x0 = to_dev_bits(batch.x)
+    y0 = to_dev_bits(batch.y0)
+    idt = ids_dev(ids)
+    seg = B.Segments(len(ids))
+    err = new_err()
+    y1 = torch.empty_like(y0)
+    y2 = torch.empty_like(y0)
+
+    def chain(sync):
+        y1.copy_(y0)
+        y2.copy_(y0)
+        B.lora_segments_build(idt, 32, seg, mode=B.LORA_SEG_GROUP, err=err)
+        B.lora_apply(x0, y1, seg, view, err=err)
+        if sync:
+            torch.cuda.synchronize()
+        B.lora_apply(y1, y2, seg, view, err=err)
+
+    chain(True)
+    torch.cuda.synchronize()
+    want = y2.clone()
+    assert int(err.item()) == 0
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        chain(False)
+    for _ in range(40):
+        y2.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y2.view(torch.int16), want.view(torch.int16))
+    assert int(err.item()) == 0
+
+
 def test_empty_batch_is_noop():
     wl = W.tiny(0)
     view = B.PoolView.from_host(wl.pools[0])
