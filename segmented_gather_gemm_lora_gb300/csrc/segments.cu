@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(kSegMaxThreads, 1) segments_kernel(const __gri
   int* run_id = runs + 2 * T;
   int* run_pos = runs + 3 * T;
   const int per_pass = nthr * kSpan;
+  const bool ids_vec = (reinterpret_cast<uintptr_t>(a.ids) & 15) == 0;  // spans start at multiples of 16 ids
 
   // 1. runs of equal valid ids.  A batch that fits one pass keeps its ids, its
   // predecessor id and its run numbering for step 3.
@@ -122,8 +123,19 @@ __global__ void __launch_bounds__(kSegMaxThreads, 1) segments_kernel(const __gri
   for (int base = 0; base < T; base += per_pass) {
     const int t0 = base + tid * kSpan;
     int v[kSpan];
+    if (ids_vec && t0 + kSpan <= T) {  // a whole span: four 16-byte loads
 #pragma unroll
-    for (int k = 0; k < kSpan; ++k) v[k] = (t0 + k < T) ? a.ids[t0 + k] : INT_MIN;
+      for (int q = 0; q < kSpan / 4; ++q) {
+        const int4 w = reinterpret_cast<const int4*>(a.ids + t0)[q];
+        v[4 * q] = w.x;
+        v[4 * q + 1] = w.y;
+        v[4 * q + 2] = w.z;
+        v[4 * q + 3] = w.w;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < kSpan; ++k) v[k] = (t0 + k < T) ? a.ids[t0 + k] : INT_MIN;
+    }
     const int prev = (t0 > 0 && t0 < T) ? a.ids[t0 - 1] : INT_MIN;
     const int next = (t0 + kSpan < T) ? a.ids[t0 + kSpan] : INT_MIN;
     int heads = 0;
@@ -230,6 +242,9 @@ __global__ void __launch_bounds__(kSegMaxThreads, 1) segments_kernel(const __gri
   __syncthreads();
 
   // 3. token indices to their positions (the runs are renumbered exactly as in 1).
+  // With the runs in shared memory, the positions are staged there (over the run
+  // ends, which step 2 was the last to read) and leave in coalesced 16-byte stores.
+  int* stage = a.runs_in_smem ? run_end : nullptr;
   int rbase = 0;
   for (int base = 0; base < T; base += per_pass) {
     const int t0 = base + tid * kSpan;
@@ -268,9 +283,19 @@ __global__ void __launch_bounds__(kSegMaxThreads, 1) segments_kernel(const __gri
       } else if (valid && k == 0) {
         pos = run_pos[rho] + (t0 - run_start[rho]);  // a run that began in an earlier span
       }
-      if (valid) a.perm[pos++] = t0 + k;
+      if (valid) {
+        if (stage) stage[pos++] = t0 + k;
+        else a.perm[pos++] = t0 + k;
+      }
     }
     rbase += totx;
+  }
+  if (stage) {
+    __syncthreads();
+    const int n4 = (reinterpret_cast<uintptr_t>(a.perm) & 15) == 0 ? n_tok / 4 : 0;  // carved buffers are aligned
+    for (int i = tid; i < n4; i += nthr)
+      reinterpret_cast<int4*>(a.perm)[i] = make_int4(stage[4 * i], stage[4 * i + 1], stage[4 * i + 2], stage[4 * i + 3]);
+    for (int i = 4 * n4 + tid; i < n_tok; i += nthr) a.perm[i] = stage[i];
   }
 
   if (tid == 0) {
