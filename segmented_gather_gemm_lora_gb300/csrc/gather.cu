@@ -27,10 +27,10 @@
 // table, "Multi-LoRA Serving in Production", section "Unified Paged Memory";
 // one bulk copy per row run and page) with the unit's token rows for the same
 // columns into a 4-stage ring; every stage carries a record of what it holds.
-// Warps 0-7 consume the ring.  Between a group's shrink and expand the
-// consumers of the cluster's CTAs exchange partial h through distributed
-// shared memory, signalled by mbarrier arrivals on the peers, so the producer
-// keeps streaming the expand rows and the next unit meanwhile.
+// Warps 0-7 consume the ring.  Between a group's shrink and expand each CTA
+// pushes its partial h into every peer's shared memory (asynchronous stores
+// whose bytes complete on the peer's own mbarrier) and sums what it received
+// in CTA order; the producer keeps streaming the expand rows meanwhile.
 //
 // Summation order.  Each rank row's shrink dot product over a sub-slice and
 // each output's expand sum over a 16-row chunk are fixed functions of column
