@@ -114,8 +114,10 @@ typedef struct {
  * token_perm lists the segments' tokens in segment order; segment s covers
  * token_perm[seg_indptr[s] .. seg_indptr[s+1]) and uses adapter seg_adapter[s].
  * meta[0] = number of segments, meta[1] = tokens placed, meta[2] = short work
- * units, meta[3] = long work units, meta[5] and meta[6] = work counters of the
- * tensor-core kernels (zeroed by lora_segments_build, left at zero by every call).  short_units lists the segments of at most
+ * units, meta[3] = long work units, meta[4] = runs of equal ids, meta[5],
+ * meta[6] and meta[7] = work counters of the tensor-core shrink, the tensor-core
+ * expand and the gather kernel (zeroed by lora_segments_build, left at zero by
+ * every call).  short_units lists the segments of at most
  * LORA_SHORT_MAX_TOKENS tokens; long_units lists (segment, offset) pairs, one
  * per LORA_TILE_M-token tile of every longer segment, both in segment order.
  * scratch belongs to lora_segments_build; h_scratch, k_partials and the work
