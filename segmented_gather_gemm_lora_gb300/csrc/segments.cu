@@ -245,8 +245,15 @@ __global__ void __launch_bounds__(kSegMaxThreads, 1) segments_kernel(const __gri
   // With the runs in shared memory, the positions are staged there (over the run
   // ends, which step 2 was the last to read) and leave in coalesced 16-byte stores.
   int* stage = a.runs_in_smem ? run_end : nullptr;
+  // Maximal runs with every token valid keep token order: the identity.
+  const bool identity = a.mode == LORA_SEG_CONTIGUOUS && n_tok == T;
+  if (identity) {
+    const int n4 = (reinterpret_cast<uintptr_t>(a.perm) & 15) == 0 ? T / 4 : 0;
+    for (int i = tid; i < n4; i += nthr) reinterpret_cast<int4*>(a.perm)[i] = make_int4(4 * i, 4 * i + 1, 4 * i + 2, 4 * i + 3);
+    for (int i = 4 * n4 + tid; i < T; i += nthr) a.perm[i] = i;
+  }
   int rbase = 0;
-  for (int base = 0; base < T; base += per_pass) {
+  for (int base = identity ? T : 0; base < T; base += per_pass) {
     const int t0 = base + tid * kSpan;
     int v[kSpan];
     int prev, exx, totx;
@@ -290,7 +297,7 @@ __global__ void __launch_bounds__(kSegMaxThreads, 1) segments_kernel(const __gri
     }
     rbase += totx;
   }
-  if (stage) {
+  if (stage && !identity) {
     __syncthreads();
     const int n4 = (reinterpret_cast<uintptr_t>(a.perm) & 15) == 0 ? n_tok / 4 : 0;  // carved buffers are aligned
     for (int i = tid; i < n4; i += nthr)

@@ -52,6 +52,8 @@ def segment_cases():
     cases.append(("mixed13b", W.mixed13b_ids(rng2), 1000))
     cases.append(("big_catalogue", rng.integers(0, 32768, size=3000).astype(np.int32), 32768))
     cases.append(("long_batch", np.repeat(rng.integers(0, 50, size=40), 1200).astype(np.int32), 50))
+    for T in (1, 2, 3, 5, 4097, 9999):  # every id valid (the identity order of maximal runs)
+        cases.append(("valid%d" % T, np.sort(rng.integers(0, 30, size=T)).astype(np.int32)[::-1].copy(), 30))
     return cases
 
 
