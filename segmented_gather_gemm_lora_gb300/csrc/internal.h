@@ -39,8 +39,8 @@ enum GatherMode { kModeApply = 0, kModeShrink = 1, kModeExpand = 2 };
 enum GatherSrc { kSrcSegments = 0, kSrcTokens = 1 };
 
 // CUDA-core gather kernel over the segments' work lists (short units, then
-// long tiles) or over one-token units.
-// long tiles too unless short_only (then the tensor-core kernels take them).
+// long tiles unless short_only, when the tensor-core kernels take them) or over
+// one-token units.
 lora_status_t launch_gather(int mode, int src, int short_only, const void* x, long long ldx, void* y,
                             long long ldy, float* h, long long ldh, const lora_segments_t* seg,
                             const int32_t* token_adapter, int T, const lora_pool_view_t* view,

@@ -30,6 +30,16 @@ def test_every_declared_symbol_is_exported():
     assert set(B.EXPORTED) == set(names)
 
 
+def test_header_constants_match_the_binding():
+    text = open(HEADER).read()
+    defs = re.findall(r"#define\s+(LORA_[A-Z0-9_]+)\s+\(?(-?\d+)u?\)?", text)
+    assert len(defs) >= 17
+    for name, value in defs:
+        if name in ("LORA_ABI_VERSION", "LORA_KSPLIT_MAX"):
+            continue
+        assert getattr(B, name) == int(value), name
+
+
 def test_abi_version_and_status_strings():
     assert B.lora_abi_version() == 1
     assert B.lora_status_string(0) == "ok"
