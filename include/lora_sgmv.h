@@ -62,7 +62,7 @@ typedef int32_t lora_status_t;
 #define LORA_ERR_INVALID_ARG (-1) /* null/misaligned pointer, bad size or stride, aliasing */
 #define LORA_ERR_UNSUPPORTED (-2) /* valid but outside what this build handles */
 #define LORA_ERR_CUDA (-3)        /* a CUDA runtime call or launch failed */
-#define LORA_ERR_WORKSPACE (-4)   /* the segment buffer is too small */
+#define LORA_ERR_WORKSPACE (-4)   /* the segment buffer or the adapter pool is too small */
 
 /* Bits OR-ed into the caller's device error word. */
 #define LORA_DERR_BAD_ADAPTER 1 /* adapter id outside [-1, n_adapters) */

@@ -1,4 +1,5 @@
-"""Thin Python binding of liblora_sgmv.so (the C ABI in include/lora_sgmv.h).
+"""Thin Python binding of liblora_sgmv.so (the C ABI in include/lora_sgmv.h and
+include/lora_pool.h).
 
 Argument marshalling only: every step of the LoRA path runs in the library's
 CUDA kernels.  PyTorch supplies device memory and the current stream.  There is
@@ -47,6 +48,17 @@ EXPORTED = (
     "lora_status_string",
     "lora_abi_version",
     "lora_launch_count",
+    "lora_pool_mgr_create",
+    "lora_pool_mgr_destroy",
+    "lora_pool_mgr_page_list_len",
+    "lora_pool_mgr_free_pages",
+    "lora_pool_resident_rank",
+    "lora_pool_pin",
+    "lora_pool_unpin",
+    "lora_pool_mgr_reserve",
+    "lora_pool_mgr_release",
+    "lora_pool_load",
+    "lora_pool_evict",
 )
 
 
@@ -114,6 +126,29 @@ def lib():
         L.lora_status_string.argtypes = [i32]
         L.lora_abi_version.restype = i32
         L.lora_abi_version.argtypes = []
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        L.lora_pool_mgr_create.restype = i32
+        L.lora_pool_mgr_create.argtypes = [i64, i32, i32, i32, i32, i32, ctypes.POINTER(vp)]
+        L.lora_pool_mgr_destroy.restype = None
+        L.lora_pool_mgr_destroy.argtypes = [vp]
+        L.lora_pool_mgr_page_list_len.restype = i64
+        L.lora_pool_mgr_page_list_len.argtypes = [vp]
+        L.lora_pool_mgr_free_pages.restype = i64
+        L.lora_pool_mgr_free_pages.argtypes = [vp]
+        L.lora_pool_resident_rank.restype = i32
+        L.lora_pool_resident_rank.argtypes = [vp, i32]
+        L.lora_pool_pin.restype = i32
+        L.lora_pool_pin.argtypes = [vp, i32]
+        L.lora_pool_unpin.restype = i32
+        L.lora_pool_unpin.argtypes = [vp, i32]
+        L.lora_pool_mgr_reserve.restype = i32
+        L.lora_pool_mgr_reserve.argtypes = [vp, i32, i32, i32p, i32, i32p, i32p, i32, i32p]
+        L.lora_pool_mgr_release.restype = i32
+        L.lora_pool_mgr_release.argtypes = [vp, i32]
+        L.lora_pool_load.restype = i32
+        L.lora_pool_load.argtypes = [vp, i32, i32, ctypes.c_float, vp, vp, view_p, vp]
+        L.lora_pool_evict.restype = i32
+        L.lora_pool_evict.argtypes = [vp, i32, view_p, vp]
         _lib = L
     return _lib
 
@@ -278,3 +313,143 @@ def lora_bgmv(x: torch.Tensor, y: torch.Tensor, token_adapter: torch.Tensor, vie
     T = int(token_adapter.numel())
     _check(lib().lora_bgmv(_ptr(x), _ld(x), _ptr(y), _ld(y), _ptr(token_adapter), T,
                            ctypes.byref(view.c), _ptr(err), _stream(stream)), "lora_bgmv")
+
+
+# ---------------------------------------------------------- pool residency --
+
+def _host_bits(m, rows: int, cols: int) -> tuple:
+    """(pointer, owner) of a host bf16 matrix [rows, cols]: a contiguous CPU tensor of
+    bfloat16 / int16 / uint16 or a numpy uint16 / int16 array."""
+    if isinstance(m, torch.Tensor):
+        if m.device.type != "cpu" or m.element_size() != 2 or not m.is_contiguous():
+            raise ValueError("expected a contiguous 2-byte CPU tensor")
+        if m.numel() != rows * cols:
+            raise ValueError("expected %d x %d elements" % (rows, cols))
+        return ctypes.c_void_p(m.data_ptr()), m
+    a = np.ascontiguousarray(m)
+    if a.dtype.itemsize != 2 or a.size != rows * cols:
+        raise ValueError("expected a %d x %d array of 2-byte elements" % (rows, cols))
+    return ctypes.c_void_p(a.ctypes.data), a
+
+
+def lora_pool_mgr_create(n_pages: int, page_elems: int, n_adapters: int, max_rank: int,
+                         d_in: int, d_out: int) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    _check(lib().lora_pool_mgr_create(n_pages, page_elems, n_adapters, max_rank, d_in, d_out,
+                                      ctypes.byref(h)), "lora_pool_mgr_create")
+    return h
+
+
+def lora_pool_mgr_destroy(mgr: ctypes.c_void_p) -> None:
+    lib().lora_pool_mgr_destroy(mgr)
+
+
+def lora_pool_mgr_page_list_len(mgr) -> int:
+    return int(lib().lora_pool_mgr_page_list_len(mgr))
+
+
+def lora_pool_mgr_free_pages(mgr) -> int:
+    return int(lib().lora_pool_mgr_free_pages(mgr))
+
+
+def lora_pool_resident_rank(mgr, adapter: int) -> int:
+    return int(lib().lora_pool_resident_rank(mgr, adapter))
+
+
+def lora_pool_pin(mgr, adapter: int) -> None:
+    _check(lib().lora_pool_pin(mgr, adapter), "lora_pool_pin")
+
+
+def lora_pool_unpin(mgr, adapter: int) -> None:
+    _check(lib().lora_pool_unpin(mgr, adapter), "lora_pool_unpin")
+
+
+def lora_pool_mgr_reserve(mgr, adapter: int, rank: int, pages_cap: int, evicted_cap: int):
+    """(pages, evicted) as int32 arrays: the pages the adapter now holds (empty if it was
+    already resident with this rank) and the adapters evicted for them, in order."""
+    pages = (ctypes.c_int32 * max(1, pages_cap))()
+    evicted = (ctypes.c_int32 * max(1, evicted_cap))()
+    n_p, n_e = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib().lora_pool_mgr_reserve(mgr, adapter, rank, pages, pages_cap, ctypes.byref(n_p), evicted,
+                                       evicted_cap, ctypes.byref(n_e)), "lora_pool_mgr_reserve")
+    return (np.frombuffer(pages, dtype=np.int32)[: n_p.value].copy(),
+            np.frombuffer(evicted, dtype=np.int32)[: n_e.value].copy())
+
+
+def lora_pool_mgr_release(mgr, adapter: int) -> None:
+    _check(lib().lora_pool_mgr_release(mgr, adapter), "lora_pool_mgr_release")
+
+
+def lora_pool_load(mgr, adapter: int, rank: int, scale: float, A, B, view: PoolView, stream=None):
+    """A: host bf16 [rank, d_in], B: host bf16 [rank, d_out] (tensors or uint16 arrays).  A
+    pinned tensor is copied asynchronously: keep it unchanged until the stream passes."""
+    pa, _ = _host_bits(A, rank, view.d_in)
+    pb, _ = _host_bits(B, rank, view.d_out)
+    _check(lib().lora_pool_load(mgr, adapter, rank, float(scale), pa, pb, ctypes.byref(view.c),
+                                _stream(stream)), "lora_pool_load")
+
+
+def lora_pool_evict(mgr, adapter: int, view: PoolView, stream=None) -> None:
+    _check(lib().lora_pool_evict(mgr, adapter, ctypes.byref(view.c), _stream(stream)), "lora_pool_evict")
+
+
+class PoolManager:
+    """One projection's pool residency (include/lora_pool.h): a host-side manager plus,
+    from device_view(), the device pool, page list and descriptors it fills."""
+
+    def __init__(self, n_pages: int, page_elems: int, n_adapters: int, max_rank: int,
+                 d_in: int, d_out: int):
+        self.h = lora_pool_mgr_create(n_pages, page_elems, n_adapters, max_rank, d_in, d_out)
+        self.n_pages, self.page_elems, self.n_adapters = n_pages, page_elems, n_adapters
+        self.max_rank, self.d_in, self.d_out = max_rank, d_in, d_out
+
+    def close(self):
+        if self.h is not None and self.h.value:
+            lora_pool_mgr_destroy(self.h)
+        self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def page_list_len(self) -> int:
+        return lora_pool_mgr_page_list_len(self.h)
+
+    @property
+    def slots_per_adapter(self) -> int:
+        return self.page_list_len // self.n_adapters
+
+    @property
+    def free_pages(self) -> int:
+        return lora_pool_mgr_free_pages(self.h)
+
+    def resident_rank(self, adapter: int) -> int:
+        return lora_pool_resident_rank(self.h, adapter)
+
+    def pin(self, adapter: int):
+        lora_pool_pin(self.h, adapter)
+
+    def unpin(self, adapter: int):
+        lora_pool_unpin(self.h, adapter)
+
+    def reserve(self, adapter: int, rank: int):
+        return lora_pool_mgr_reserve(self.h, adapter, rank, self.slots_per_adapter, self.n_adapters)
+
+    def release(self, adapter: int):
+        lora_pool_mgr_release(self.h, adapter)
+
+    def device_view(self, device="cuda") -> PoolView:
+        """A zeroed device pool, page list and descriptor array of this manager's geometry."""
+        pool = torch.zeros(self.n_pages, self.page_elems, dtype=torch.bfloat16, device=device)
+        pl = torch.zeros(self.page_list_len, dtype=torch.int32, device=device)
+        desc = torch.zeros(self.n_adapters * 16, dtype=torch.uint8, device=device)
+        return PoolView(pool, pl, desc, self.page_elems, self.max_rank, self.d_in, self.d_out)
+
+    def load(self, adapter: int, rank: int, scale: float, A, B, view: PoolView, stream=None):
+        lora_pool_load(self.h, adapter, rank, scale, A, B, view, stream)
+
+    def evict(self, adapter: int, view: PoolView, stream=None):
+        lora_pool_evict(self.h, adapter, view, stream)

@@ -176,6 +176,10 @@ int sm_count() {
   return c;
 }
 
+lora_status_t validate_view(const lora_pool_view_t* v) { return check_view(v); }
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 void make_dev_view(const lora_pool_view_t* v, DevView* out) {
   out->pool = static_cast<const uint16_t*>(v->pool);
   out->page_list = v->page_list;
@@ -203,7 +207,7 @@ const char* lora_status_string(lora_status_t s) {
     case LORA_ERR_INVALID_ARG: return "invalid argument";
     case LORA_ERR_UNSUPPORTED: return "unsupported by this build";
     case LORA_ERR_CUDA: return "CUDA runtime error";
-    case LORA_ERR_WORKSPACE: return "segment buffer too small";
+    case LORA_ERR_WORKSPACE: return "segment buffer or adapter pool too small";
     default: return "unknown status";
   }
 }

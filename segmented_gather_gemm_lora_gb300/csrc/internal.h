@@ -32,6 +32,12 @@ int max_active_clusters(const void* func, int block, size_t smem, int cluster_x)
 // Fill a DevView from a validated host view.
 void make_dev_view(const lora_pool_view_t* v, DevView* out);
 
+// The checks every compute call makes on a view (LORA_OK if it passes).
+lora_status_t validate_view(const lora_pool_view_t* v);
+
+// Count one kernel launch made without launch_pdl (lora_launch_count).
+void count_launch();
+
 lora_status_t launch_segments(const int32_t* ids, int T, int n_adapters, int mode,
                               const lora_segments_t* seg, int32_t* err, cudaStream_t stream);
 

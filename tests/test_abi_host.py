@@ -1,7 +1,8 @@
-"""The C-ABI library on the host: it loads, exports every symbol include/lora_sgmv.h
+"""The C-ABI library on the host: it loads, exports every symbol include/*.h
 declares, and rejects bad arguments before launching anything (no GPU needed)."""
 
 import ctypes
+import glob
 import os
 import re
 
@@ -12,11 +13,11 @@ import oracle
 from segmented_gather_gemm_lora_gb300 import binding as B
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "lora_sgmv.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(lora_[a-z0-9_]+)\s*\(", text)))
 
@@ -31,7 +32,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_header_constants_match_the_binding():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     defs = re.findall(r"#define\s+(LORA_[A-Z0-9_]+)\s+\(?(-?\d+)u?\)?", text)
     assert len(defs) >= 17
     for name, value in defs:
