@@ -233,13 +233,18 @@ lora_status_t lora_pool_mgr_create(int64_t n_pages, int32_t page_elems, int32_t 
   m->n_free = n_pages;
   m->hint = 0;
   const size_t words = (size_t)ceil_div(n_pages, 64);
-  m->used.assign(words, 0ull);
+  try {
+    m->used.assign(words, 0ull);
+    m->rank.assign((size_t)n_adapters, 0);
+    m->pins.assign((size_t)n_adapters, 0);
+    m->pages.resize((size_t)n_adapters);
+    m->prev.assign((size_t)n_adapters, -1);
+    m->next.assign((size_t)n_adapters, -1);
+  } catch (const std::bad_alloc&) {  // no exception crosses the C ABI
+    delete m;
+    return LORA_ERR_INVALID_ARG;
+  }
   if (n_pages % 64 != 0) m->used[words - 1] = ~0ull << (n_pages % 64);  // beyond the pool: never free
-  m->rank.assign((size_t)n_adapters, 0);
-  m->pins.assign((size_t)n_adapters, 0);
-  m->pages.resize((size_t)n_adapters);
-  m->prev.assign((size_t)n_adapters, -1);
-  m->next.assign((size_t)n_adapters, -1);
   *out = m;
   return LORA_OK;
 }
