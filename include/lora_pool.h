@@ -86,8 +86,9 @@ lora_status_t lora_pool_unpin(lora_pool_mgr_t* mgr, int32_t adapter);
  * released first) it takes ceil(rank * d_in / page_elems) +
  * ceil(rank * d_out / page_elems) free pages, lowest page numbers first (A's
  * pages, then B's, in logical order, into pages_out), evicting the least
- * recently used unpinned adapters (into evicted_out, in eviction order) until
- * enough pages are free, and becomes resident and the most recently used.
+ * recently used unpinned adapters (into evicted_out, in eviction order, after
+ * the adapter itself when its rank changed) until enough pages are free, and
+ * becomes resident and the most recently used.
  * Nothing changes if the pages cannot be found: LORA_ERR_WORKSPACE when even
  * evicting every unpinned adapter would not free enough, LORA_ERR_INVALID_ARG
  * for a bad id or rank, a pinned adapter of another rank, or capacities below
