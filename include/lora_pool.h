@@ -70,6 +70,20 @@ int64_t lora_pool_mgr_free_pages(const lora_pool_mgr_t* mgr);
 /** Rank of a resident adapter, 0 if it is not resident, -1 on a bad argument. */
 int32_t lora_pool_resident_rank(const lora_pool_mgr_t* mgr, int32_t adapter);
 
+/** Counters of a manager since its creation (host only). */
+typedef struct {
+  int64_t hits;         /* reserves of an adapter already resident with that rank */
+  int64_t loads;        /* reserves that handed out pages */
+  int64_t refused;      /* reserves refused for want of unpinned pages (LORA_ERR_WORKSPACE) */
+  int64_t evictions;    /* adapters released to make room, their own release on a rank change included */
+  int64_t pages_loaded; /* pages handed out by those loads */
+  int32_t resident;     /* adapters resident now */
+  int32_t pinned;       /* of which pinned */
+} lora_pool_stats_t;
+
+/** Fill *out (LORA_ERR_INVALID_ARG if mgr or out is null). */
+lora_status_t lora_pool_mgr_stats(const lora_pool_mgr_t* mgr, lora_pool_stats_t* out);
+
 /** Pin counts: a pinned adapter (count > 0) is never evicted.  lora_pool_pin
  *  needs a resident adapter; lora_pool_unpin one with a count above zero
  *  (LORA_ERR_INVALID_ARG otherwise). */

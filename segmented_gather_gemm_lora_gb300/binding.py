@@ -59,6 +59,7 @@ EXPORTED = (
     "lora_pool_mgr_release",
     "lora_pool_load",
     "lora_pool_evict",
+    "lora_pool_mgr_stats",
 )
 
 
@@ -73,6 +74,12 @@ class lora_pool_view_t(ctypes.Structure):
                 ("adapters", ctypes.c_void_p), ("n_adapters", ctypes.c_int32),
                 ("page_elems", ctypes.c_int32), ("max_rank", ctypes.c_int32),
                 ("d_in", ctypes.c_int32), ("d_out", ctypes.c_int32)]
+
+
+class lora_pool_stats_t(ctypes.Structure):
+    _fields_ = [("hits", ctypes.c_int64), ("loads", ctypes.c_int64), ("refused", ctypes.c_int64),
+                ("evictions", ctypes.c_int64), ("pages_loaded", ctypes.c_int64),
+                ("resident", ctypes.c_int32), ("pinned", ctypes.c_int32)]
 
 
 class lora_segments_t(ctypes.Structure):
@@ -149,6 +156,8 @@ def lib():
         L.lora_pool_load.argtypes = [vp, i32, i32, ctypes.c_float, vp, vp, view_p, vp]
         L.lora_pool_evict.restype = i32
         L.lora_pool_evict.argtypes = [vp, i32, view_p, vp]
+        L.lora_pool_mgr_stats.restype = i32
+        L.lora_pool_mgr_stats.argtypes = [vp, ctypes.POINTER(lora_pool_stats_t)]
         _lib = L
     return _lib
 
@@ -389,6 +398,12 @@ def lora_pool_load(mgr, adapter: int, rank: int, scale: float, A, B, view: PoolV
                                 _stream(stream)), "lora_pool_load")
 
 
+def lora_pool_mgr_stats(mgr) -> dict:
+    st = lora_pool_stats_t()
+    _check(lib().lora_pool_mgr_stats(mgr, ctypes.byref(st)), "lora_pool_mgr_stats")
+    return {name: int(getattr(st, name)) for name, _ in lora_pool_stats_t._fields_}
+
+
 def lora_pool_evict(mgr, adapter: int, view: PoolView, stream=None) -> None:
     _check(lib().lora_pool_evict(mgr, adapter, ctypes.byref(view.c), _stream(stream)), "lora_pool_evict")
 
@@ -425,6 +440,10 @@ class PoolManager:
     @property
     def free_pages(self) -> int:
         return lora_pool_mgr_free_pages(self.h)
+
+    def stats(self) -> dict:
+        """hits, loads, refused, evictions, pages_loaded, resident, pinned."""
+        return lora_pool_mgr_stats(self.h)
 
     def resident_rank(self, adapter: int) -> int:
         return lora_pool_resident_rank(self.h, adapter)

@@ -32,6 +32,7 @@ struct lora_pool_mgr {
   std::vector<std::vector<int32_t>> pages;  // a resident adapter's pages: A's, then B's
   std::vector<int32_t> prev, next;          // list of resident adapters, least recent first
   int32_t head = -1, tail = -1;
+  lora_pool_stats_t stats{};    // resident and pinned are counted when asked for
   mutable std::mutex mu;
 };
 
@@ -135,6 +136,7 @@ lora_status_t reserve_locked(lora_pool_mgr* m, int a, int r, std::vector<int32_t
   if (m->rank[a] == r) {
     lru_unlink(m, a);
     lru_push_back(m, a);
+    ++m->stats.hits;
     return LORA_OK;
   }
   const bool again = m->rank[a] != 0;  // resident with another rank: released first
@@ -149,12 +151,16 @@ lora_status_t reserve_locked(lora_pool_mgr* m, int a, int r, std::vector<int32_t
   }
   if (avail < need) {
     evicted->clear();
+    ++m->stats.refused;
     return LORA_ERR_WORKSPACE;
   }
   for (const int e : *evicted) release_locked(m, e);
   take_pages(m, need, &m->pages[a]);
   m->rank[a] = r;
   lru_push_back(m, a);
+  ++m->stats.loads;
+  m->stats.evictions += (int64_t)evicted->size();
+  m->stats.pages_loaded += need;
   *fresh = true;
   return LORA_OK;
 }
@@ -265,6 +271,19 @@ int32_t lora_pool_resident_rank(const lora_pool_mgr_t* mgr, int32_t adapter) {
   if (mgr == nullptr || adapter < 0 || adapter >= mgr->n_adapters) return -1;
   std::lock_guard<std::mutex> lock(mgr->mu);
   return mgr->rank[adapter];
+}
+
+lora_status_t lora_pool_mgr_stats(const lora_pool_mgr_t* mgr, lora_pool_stats_t* out) {
+  if (mgr == nullptr || out == nullptr) return LORA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(mgr->mu);
+  *out = mgr->stats;
+  out->resident = 0;
+  out->pinned = 0;
+  for (int32_t a = 0; a < mgr->n_adapters; ++a) {
+    out->resident += mgr->rank[a] != 0 ? 1 : 0;
+    out->pinned += mgr->pins[a] > 0 ? 1 : 0;
+  }
+  return LORA_OK;
 }
 
 lora_status_t lora_pool_pin(lora_pool_mgr_t* mgr, int32_t adapter) {

@@ -29,6 +29,7 @@ class Model:
         self.pages = {}
         self.pins = {}
         self.order = []  # least recent first
+        self.counts = dict(hits=0, loads=0, refused=0, evictions=0, pages_loaded=0)
 
     def need(self, r):
         return ceil_div(r * self.d_in, self.P) + ceil_div(r * self.d_out, self.P)
@@ -44,6 +45,7 @@ class Model:
         if self.rank.get(a) == r:
             self.order.remove(a)
             self.order.append(a)
+            self.counts["hits"] += 1
             return "ok", [], []
         again = a in self.rank
         if again and self.pins.get(a, 0) > 0:
@@ -58,6 +60,7 @@ class Model:
             avail += len(self.pages[e])
             ev.append(e)
         if avail < self.need(r):
+            self.counts["refused"] += 1
             return "workspace", None, None
         for e in ev:
             self._release(e)
@@ -66,6 +69,9 @@ class Model:
         self.pages[a] = got
         self.rank[a] = r
         self.order.append(a)
+        self.counts["loads"] += 1
+        self.counts["evictions"] += len(ev)
+        self.counts["pages_loaded"] += len(got)
         return "ok", got, ev
 
     def pin(self, a):
@@ -170,6 +176,9 @@ def test_policy_matches_the_model_under_random_traffic(seed):
             check_invariants(m, model)
     check_invariants(m, model)
     assert evictions > 20 and workspace > 0  # the traffic reached both paths
+    want = dict(model.counts, resident=len(model.rank),
+                pinned=sum(1 for a in model.rank if model.pins.get(a, 0) > 0))
+    assert m.stats() == want
     m.close()
 
 
