@@ -32,8 +32,9 @@
  * Ownership and threading.  The caller owns every buffer (x, y, h, pool, page
  * list, descriptors, segment buffer, error word); all device buffers are plain
  * device pointers from any allocator.  The library allocates no device memory,
- * keeps no per-call state, and its entry points may be called from several
- * host threads.  Every compute entry point is asynchronous on the given CUDA
+ * keeps no per-call state (the pool managers of lora_pool.h are host objects
+ * the caller creates and destroys), and its entry points may be called from
+ * several host threads.  Every compute entry point is asynchronous on the given CUDA
  * stream (NULL = the legacy default stream) and does not synchronise.
  *
  * Errors.  Argument errors found on the host are returned before anything is
