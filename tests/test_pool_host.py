@@ -271,3 +271,24 @@ def test_device_calls_reject_bad_arguments_before_any_launch():
     assert L.lora_pool_mgr_page_list_len(None) == -1 and L.lora_pool_mgr_free_pages(None) == -1
     assert L.lora_pool_resident_rank(m.h, 8) == -1
     m.close()
+
+
+def test_reserve_rejects_short_output_buffers_and_nulls():
+    m = B.PoolManager(64, 4096, 8, 16, 1024, 1024)
+    L = B.lib()
+    S = m.slots_per_adapter
+    pages = (ctypes.c_int32 * S)()
+    ev = (ctypes.c_int32 * 8)()
+    n_p, n_e = ctypes.c_int32(-7), ctypes.c_int32(-7)
+    args = lambda pcap, ecap: (m.h, 1, 16, pages, pcap, ctypes.byref(n_p), ev, ecap, ctypes.byref(n_e))
+    assert L.lora_pool_mgr_reserve(*args(S - 1, 8)) == B.LORA_ERR_INVALID_ARG
+    assert L.lora_pool_mgr_reserve(*args(S, 7)) == B.LORA_ERR_INVALID_ARG
+    assert L.lora_pool_mgr_reserve(m.h, 1, 16, None, S, ctypes.byref(n_p), ev, 8, ctypes.byref(n_e)) == -1
+    assert L.lora_pool_mgr_reserve(m.h, 1, 16, pages, S, None, ev, 8, ctypes.byref(n_e)) == -1
+    assert L.lora_pool_mgr_reserve(None, 1, 16, pages, S, ctypes.byref(n_p), ev, 8, ctypes.byref(n_e)) == -1
+    assert (n_p.value, n_e.value) == (-7, -7) and m.free_pages == 64  # nothing written, nothing taken
+    assert L.lora_pool_mgr_reserve(*args(S, 8)) == B.LORA_OK and (n_p.value, n_e.value) == (8, 0)
+    assert list(pages[:8]) == list(range(8))
+    assert L.lora_pool_pin(None, 1) == -1 and L.lora_pool_unpin(m.h, 99) == -1
+    assert L.lora_pool_mgr_stats(m.h, None) == -1 and L.lora_pool_mgr_release(m.h, -1) == -1
+    m.close()
