@@ -1,23 +1,27 @@
 #!/usr/bin/env python
 """Benchmark of the multi-adapter LoRA path on one GB300 (or N, one process each).
 
-A step is one pass of the whole path over one batch.  For the decode batch (one
-token per request) that is lora_bgmv: every token gathers its own adapter through
-the page table, shrink + scale + expand in place in y, one kernel.  For batches
-with segments it is lora_segments_build (grouping the batch's tokens by adapter,
-work lists) followed by lora_apply.  The default workload is the decode batch: 64
-tokens, q_proj 4096 -> 4096, 100 rank-16 adapters, uniformly random adapter per
-token.
+A step is one pass of the whole path over one batch of one configuration:
 
-Prints one JSON line (rank 0).  `--impl reference` times the CPU fp64 oracle on the
-same workload instead (the reference arm of this build: there is no runnable
-upstream implementation).
+* tiny, prefill, hetero: lora_segments_build (grouping the batch's tokens by adapter,
+  work lists) followed by the step's lora_apply call(s);
+* decode (one token per request): lora_bgmv, every token gathering its own adapter
+  through the page table, shrink + scale + expand in place in y, one kernel;
+* mixed13b (the headline, the largest configuration that fits one GPU): one forward of
+  the 13B-shaped mixed batch, one segment build and 40 layers x 7 projections.
+
+By default the printed JSON line is the 13B forward, with every other configuration
+timed in the same process under "per_config" (each with its own roofline, CPU
+baseline, end-to-end figure and parity sample).  `--workload NAME` times one
+configuration alone.  `--impl reference` times the CPU fp64 oracle on the same
+workload instead (the reference arm of this build: there is no runnable upstream
+implementation).
 """
 
 from __future__ import annotations
 
 import argparse
-import hashlib
+import gc
 import json
 import math
 import os
@@ -35,6 +39,8 @@ if ROOT not in sys.path:
 
 METRIC = "SGMV/BGMV adapter-path tokens/s and achieved HBM GB/s (% of roofline), 1×GB300"
 UNIT = "tokens/s"
+HEADLINE = "mixed13b"
+OTHERS = ("tiny", "decode", "prefill", "hetero")
 
 WORKLOAD_TEXT = {
     "decode": "decode BGMV: 64 tokens (1 per request), q_proj 4096->4096, 100 adapters rank 16, "
@@ -51,28 +57,38 @@ WORKLOAD_TEXT = {
     "tiny": "tiny SGMV: d=256, 4 adapters rank 8, 16 tokens in segments [3,5,1,7]",
 }
 
+# timed steps of the configurations timed beside the headline (each well under a second)
+OTHER_STEPS = {"tiny": 20000, "decode": 20000, "prefill": 2000, "hetero": 2000}
+
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=None,
-                   help="timed steps (default 20000; 20 for the 13B forward)")
-    p.add_argument("--warmup", type=int, default=20)
+                   help="timed steps of the headline (default 20 forwards of the 13B batch; "
+                        "20000 for a small configuration timed alone)")
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="decode")
-    p.add_argument("--cpu-seconds", type=float, default=10.0,
-                   help="bounded CPU work for the oracle baseline (0 disables it)")
+    p.add_argument("--workload", choices=["all"] + sorted(WORKLOAD_TEXT), default="all",
+                   help="all (default): the 13B forward as the headline, every other "
+                        "configuration under per_config; or one configuration alone")
+    p.add_argument("--cpu-seconds", type=float, default=5.0,
+                   help="bounded CPU work per configuration for the oracle baseline (0 disables it)")
     p.add_argument("--e2e-steps", type=int, default=None,
-                   help="end-to-end steps (default 2000; 5 for the 13B forward)")
-    p.add_argument("--soak-seconds", type=float, default=1.0,
-                   help="untimed steady load before the timed region while clocks are sampled")
+                   help="end-to-end steps (default 500; 5 for the 13B forward)")
+    p.add_argument("--soak-seconds", type=float, default=0.5,
+                   help="untimed steady load before each timed region while clocks are sampled")
     args = p.parse_args(argv)
-    big = args.workload == "mixed13b"
+    head = HEADLINE if args.workload == "all" else args.workload
     if args.steps is None:
-        args.steps = 20 if big else 20000
-    if args.e2e_steps is None:
-        args.e2e_steps = 5 if big else 2000
+        args.steps = 20 if head == "mixed13b" else 20000
     return args
+
+
+def default_e2e_steps(name: str, args) -> int:
+    if args.e2e_steps is not None:
+        return args.e2e_steps
+    return 5 if name == "mixed13b" else 500
 
 
 # ------------------------------------------------------------------ helpers --
@@ -176,30 +192,6 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def source_hash(paths):
-    h = hashlib.sha256()
-    for p in paths:
-        with open(p, "rb") as f:
-            h.update(f.read())
-    return h.hexdigest()[:16]
-
-
-def profile_traffic(call: str, workload: str, current_hash: str):
-    """DRAM bytes (read + write) per call from the table in profiles/traffic.md (rows
-    `| call | workload | kernel sources hash | bytes | ...`), or None if there is no row
-    or the kernel sources changed since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "traffic.md")
-    try:
-        with open(path) as f:
-            for line in f:
-                cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
-                if len(cells) >= 4 and cells[0] == call and cells[1] == workload:
-                    return float(cells[3]) if cells[2] == current_hash else None
-    except (OSError, ValueError):
-        return None
-    return None
-
-
 # --------------------------------------------------------------- workloads --
 
 def make_workload(name: str, seed: int):
@@ -207,7 +199,7 @@ def make_workload(name: str, seed: int):
 
     if name == "hetero":
         wl = W.hetero(seed, which="both")
-    elif name == "mixed13b":  # one (layer, projection) on the host: the CPU samples
+    elif name == "mixed13b":  # one (layer, projection) on the host: the CPU sample
         wl = W.mixed13b(seed, layers=(0,), projections=("q",))
     else:
         wl = W.WORKLOADS[name](seed)
@@ -281,7 +273,7 @@ def algorithmic_flops(batch, pool) -> int:
 
 # -------------------------------------------------------------- our arm --
 
-def build_sets(args, rank, dev, l2, torch, B):
+def build_sets(name, rank, dev, l2, torch, B):
     """Input sets of the workload on the device.  Each set is one step's batch: its ids,
     segment buffer and projection calls (view, x, y and their algorithmic bytes / flops);
     sets rotate so that a pass over them exceeds 2x L2."""
@@ -290,7 +282,7 @@ def build_sets(args, rank, dev, l2, torch, B):
     def up(a):  # host bf16 bits -> device bf16
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
-    if args.workload == "mixed13b":
+    if name == "mixed13b":
         # One forward of 40 layers x 7 projections; adapters and activations drawn on the
         # device (about 20 GB of adapter pages and 33 GB of activations, so nothing stays
         # in L2 between calls).
@@ -303,26 +295,26 @@ def build_sets(args, rank, dev, l2, torch, B):
         T = len(ids)
         calls = []
         for layer in range(40):
-            for pi, (name, d_in, d_out) in enumerate(W.PROJ_13B):
+            for pi, (pname, d_in, d_out) in enumerate(W.PROJ_13B):
                 prng = np.random.default_rng([1000 * rank, 1 + layer, 1 + pi])
                 view, shape = device_pool(B, torch, dev, prng, resident, d_in, d_out)
                 x = torch.randn(T, d_in, device=dev).to(torch.bfloat16)
                 y = torch.randn(T, d_out, device=dev).to(torch.bfloat16)
                 bt = W.Batch(x=None, y0=None, ids=ids, d_in=d_in, d_out=d_out)
                 calls.append(dict(view=view, x=x, y=y, bytes=algorithmic_bytes(bt, shape),
-                                  flops=algorithmic_flops(bt, shape), layer=layer, name=name))
+                                  flops=algorithmic_flops(bt, shape), layer=layer, name=pname))
         S = dict(calls=calls, ids=torch.from_numpy(ids).to(dev), seg=B.Segments(T, device=dev),
                  T=int((ids >= 0).sum()), host_ids=ids, wl=None, mode=0, n_ad=1000)
         set_bytes = sum(c["view"].pool.numel() * 2 + c["x"].numel() * 2 + c["y"].numel() * 2 for c in calls)
         return [S], set_bytes
 
-    wl0 = make_workload(args.workload, 1000 * rank)
+    wl0 = make_workload(name, 1000 * rank)
     set_bytes = sum(p.pool.nbytes + b.x.nbytes + b.y0.nbytes for p, b in host_calls(wl0, 1000 * rank))
     n_sets = max(2, math.ceil(2 * l2 / max(set_bytes, 1)) + 1)
     sets = []
     for s in range(n_sets):
         seed = 1000 * rank + s
-        wl = wl0 if s == 0 else make_workload(args.workload, seed)
+        wl = wl0 if s == 0 else make_workload(name, seed)
         calls = []
         for pool, b in host_calls(wl, seed):
             calls.append(dict(view=B.PoolView.from_host(pool, device=dev), x=up(b.x), y=up(b.y0),
@@ -334,24 +326,33 @@ def build_sets(args, rank, dev, l2, torch, B):
     return sets, set_bytes
 
 
-def run_ours(args, world, rank, local):
+def gpu_id_of(props) -> str:
+    gpu_id = str(getattr(props, "uuid", "") or "")
+    if gpu_id and not gpu_id.startswith("GPU-"):
+        gpu_id = "GPU-" + gpu_id
+    return gpu_id
+
+
+def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, local):
+    """Time `steps` steps of one configuration (inputs resident in HBM), the step's
+    projection calls alone, and the same step end to end from host buffers; returns the
+    JSON fields of the configuration."""
     import torch
 
     from segmented_gather_gemm_lora_gb300 import binding as B
 
-    torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
 
-    sets, set_bytes = build_sets(args, rank, dev, l2, torch, B)
+    sets, set_bytes = build_sets(name, rank, dev, l2, torch, B)
     n_sets = len(sets)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     mode = sets[0]["mode"]
     n_ad = sets[0]["n_ad"]
     n_calls = len(sets[0]["calls"])
 
-    bgmv = args.workload == "decode"
+    bgmv = name == "decode"
 
     def calls_of(S):
         for c in S["calls"]:
@@ -367,7 +368,7 @@ def run_ours(args, world, rank, local):
         calls_of(S)
 
     # warm-up (eager), then a CUDA graph of one pass over all sets.
-    for k in range(max(args.warmup, 3)):
+    for k in range(max(warmup, 3)):
         step(k)
     torch.cuda.synchronize()
     g_steps = n_sets * max(1, 64 // (n_sets * n_calls))
@@ -378,28 +379,25 @@ def run_ours(args, world, rank, local):
         for k in range(g_steps):
             step(k)
     launches_per_step = (B.launch_count() - launches0) / g_steps
-    rem = args.steps % g_steps
+    rem = steps % g_steps
     graph_rem = None
     if rem:
         graph_rem = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph_rem, stream=cap):
             for k in range(rem):
                 step(k)
-    reps = args.steps // g_steps
+    reps = steps // g_steps
     graph.replay()
     torch.cuda.synchronize()
 
     # clocks: steady load before and during the timed region
-    gpu_id = str(getattr(props, "uuid", "") or "")
-    if gpu_id and not gpu_id.startswith("GPU-"):
-        gpu_id = "GPU-" + gpu_id
-    sampler = ClockSampler(gpu_id)
-    t_end = time.perf_counter() + args.soak_seconds
+    sampler = ClockSampler(gpu_id_of(props))
+    t_end = time.perf_counter() + soak_seconds
     while time.perf_counter() < t_end:
         graph.replay()
         torch.cuda.synchronize()
 
-    # ---- timed region: exactly K steps ----
+    # ---- timed region: exactly `steps` steps ----
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -437,7 +435,7 @@ def run_ours(args, world, rank, local):
             calls_of(sets[k % n_sets])
     call_graph.replay()
     torch.cuda.synchronize()
-    call_reps = max(1, min(reps, int(0.2 / max(ms / args.steps / 1e3 * g_steps, 1e-9))))
+    call_reps = max(1, min(max(reps, 1), int(0.2 / max(ms / steps / 1e3 * g_steps, 1e-9))))
     c0 = torch.cuda.Event(enable_timing=True)
     c1 = torch.cuda.Event(enable_timing=True)
     c0.record()
@@ -459,7 +457,7 @@ def run_ours(args, world, rank, local):
         lat.append(c0.elapsed_time(c1) * 1e3)
     single_us = statistics.median(lat)
     hot_us = None
-    if args.workload != "mixed13b":
+    if name != "mixed13b":
         hot_graph = torch.cuda.CUDAGraph()
         n_hot = max(1, 64 // n_calls)
         with torch.cuda.graph(hot_graph, stream=cap):
@@ -477,10 +475,6 @@ def run_ours(args, world, rank, local):
     flops_avg = statistics.fmean(sum(c["flops"] for c in sets[k % n_sets]["calls"]) for k in range(g_steps))
     hbm_peak, tc_peak, peak_kind = read_peaks()
     achieved_gbs = bytes_avg / calls_avg_s / 1e9
-    csrc = os.path.join(ROOT, "segmented_gather_gemm_lora_gb300", "csrc")
-    kernel_hash = source_hash([os.path.join(csrc, f) for f in sorted(os.listdir(csrc))])
-    call = "lora_bgmv" if bgmv else "lora_apply"
-    traffic = profile_traffic(call, args.workload, kernel_hash)
 
     # ---- end to end: host buffers in, result out, through the public API ----
     # Every step copies the ids and the projection calls' x and y0 from one pinned host
@@ -488,7 +482,7 @@ def run_ours(args, world, rank, local):
     # it, and reads the y back (one copy).  The 13B forward stages layer 0's seven x / y0
     # in and reads layer 39's seven y out.
     S0 = sets[0]
-    if args.workload == "mixed13b":
+    if name == "mixed13b":
         ins = [c for c in S0["calls"] if c["layer"] == 0]
         outs_extra = [c for c in S0["calls"] if c["layer"] == 39]
     else:
@@ -509,14 +503,14 @@ def run_ours(args, world, rank, local):
     views = [dstage[o:o + t.numel() * 2].view(torch.bfloat16).view(t.shape) for t, o in zip(pieces, offs)]
     n_in = len(ins)
     e_calls = [dict(c, x=views[i], y=views[n_in + i]) for i, c in enumerate(ins)]
-    if args.workload == "mixed13b":
+    if name == "mixed13b":
         e_calls = e_calls + [c for c in S0["calls"] if c["layer"] != 0]
     e_ids = dstage[ids_off:ids_off + S0["ids"].numel() * 4].view(torch.int32)
     y_lo, y_hi = offs[n_in], offs[-1] + pieces[-1].numel() * 2  # the staged y, contiguous
     hy = torch.empty(y_hi - y_lo, dtype=torch.uint8).pin_memory()
     hout = [(c["y"], torch.empty(c["y"].shape, dtype=torch.bfloat16).pin_memory()) for c in outs_extra]
     e_seg = S0["seg"]
-    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    e2e_steps = max(1, min(e2e_steps, steps))
 
     def e2e_step():
         dstage.copy_(hstage, non_blocking=True)
@@ -546,22 +540,16 @@ def run_ours(args, world, rank, local):
     h2d = cur
     d2h = sum(h.numel() * 2 for _, h in hout) if outs_extra else y_hi - y_lo
 
-    kernels = "gather_kernel" if bgmv else "gather, shrink_tc, reduce_partials, expand_tc"
+    call = "lora_bgmv" if bgmv else "lora_apply"
+    kernels = "gather_kernel" if bgmv else ", ".join(B.apply_kernel_names())
     out = {
-        "metric": METRIC,
         "value": value,
         "unit": UNIT,
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": ms / args.steps,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic",
+        "steps": steps,
+        "warmup": warmup,
+        "ms_per_step": ms / steps,
         "config": {
-            "workload": WORKLOAD_TEXT[args.workload],
+            "workload": WORKLOAD_TEXT[name],
             "tokens_per_step": tokens_per_step,
             "segments": "none (one token per request)" if bgmv else ("GROUP" if mode == 0 else "CONTIGUOUS"),
             "step": ("%d x lora_bgmv" if bgmv else "lora_segments_build + %d x lora_apply") % n_calls,
@@ -576,24 +564,93 @@ def run_ours(args, world, rank, local):
             "peak": hbm_peak,
             "unit": "GB/s",
             "frac": achieved_gbs / hbm_peak,
-            "peak_kind": peak_kind,
-            "traffic": traffic,
+            "peak_kind": peak_kind + " (copy bandwidth, MEASURED_PEAKS.json)" if peak_kind == "measured"
+            else peak_kind,
+            "traffic": None,
+            "traffic_note": "not measured in this run; DRAM bytes per call from ncu are summarised "
+                            "under profiles/",
             "algorithmic_bytes_per_launch": bytes_avg,
             "avg_launch_us": calls_avg_s * 1e6,
             "calls_per_step": n_calls,
             "tflops": flops_avg / calls_avg_s / 1e12,
+            "tensor_frac_of_bf16_peak": flops_avg / calls_avg_s / 1e12 / tc_peak,
         },
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "call_timing": {"graph_us": calls_avg_s * 1e6, "single_launch_us": single_us, "hot_l2_us": hot_us,
                         "note": "the step's projection calls: graph-amortised over rotating sets (cold L2), "
                                 "one eager launch group on an idle GPU, and one set repeated (warm L2)"},
-        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "gpu_launches": int(round(launches_per_step * steps)),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
     }
-    if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        out["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    del sets, graph, graph_rem, call_graph, dstage, hstage
+    gc.collect()
+    torch.cuda.empty_cache()
     return out
+
+
+def gpu_sample(name: str, local: int):
+    """The CPU sample's projection calls on the GPU, from fresh copies of the same host
+    inputs: y through lora_apply (bf16, in place) and through lora_apply_f32y (fp32)."""
+    import torch
+
+    from segmented_gather_gemm_lora_gb300 import binding as B
+
+    dev = torch.device("cuda", local)
+    wl, calls, _ = oracle_sample(name)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ids = torch.from_numpy(wl.batch.ids).to(dev)
+    seg = B.Segments(wl.batch.T, device=dev)
+    B.lora_segments_build(ids, wl.n_adapters, seg, mode=wl.mode, err=err)
+    outs = []
+    for pool, b in calls:
+        view = B.PoolView.from_host(pool, device=dev)
+        x = up(b.x)
+        y = up(b.y0)
+        yf = torch.empty(y.shape, dtype=torch.float32, device=dev)
+        if name == "decode":
+            B.lora_bgmv(x, y, ids, view, err=err)
+        else:
+            B.lora_apply(x, y, seg, view, err=err)
+        B.lora_apply_f32y(x, up(b.y0), yf, seg, view, err=err)
+        torch.cuda.synchronize()
+        outs.append((y.view(torch.int16).cpu().numpy().view(np.uint16), yf.cpu().numpy()))
+    assert int(err.item()) == 0, "device error word %d" % int(err.item())
+    return outs
+
+
+def parity_report(gpu_outs, oracle_ys, d_outs):
+    """Raw max |err| and relative L2 of the GPU outputs against the oracle's, for the bf16
+    output (gate: 2e-2 plus half a bf16 ulp of the oracle value) and the fp32 output
+    (literal 2e-2)."""
+    from segmented_gather_gemm_lora_gb300 import workloads as W
+
+    mx16 = mx32 = 0.0
+    num16 = num32 = den = 0.0
+    gate_ok = True
+    for (ybits, yf), ref, d_out in zip(gpu_outs, oracle_ys, d_outs):
+        g16 = W.bf16_bits_to_f32(ybits[:, :d_out]).astype(np.float64)
+        g32 = yf[:, :d_out].astype(np.float64)
+        e16 = np.abs(g16 - ref)
+        e32 = np.abs(g32 - ref)
+        half_ulp = 0.5 * np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 7)
+        gate_ok = gate_ok and bool((e16 <= 2e-2 + half_ulp).all())
+        mx16 = max(mx16, float(e16.max(initial=0.0)))
+        mx32 = max(mx32, float(e32.max(initial=0.0)))
+        num16 += float((e16 ** 2).sum())
+        num32 += float((e32 ** 2).sum())
+        den += float((ref ** 2).sum())
+    rel16 = math.sqrt(num16 / den) if den > 0 else 0.0
+    rel32 = math.sqrt(num32 / den) if den > 0 else 0.0
+    return {"bf16_y": {"max_abs_err": mx16, "rel_l2": rel16, "gate": "max|err| <= 2e-2 + half a bf16 ulp; "
+                       "rel L2 <= 5e-3", "pass": gate_ok and rel16 <= 5e-3},
+            "f32_y": {"max_abs_err": mx32, "rel_l2": rel32, "gate": "max|err| <= 2e-2; rel L2 <= 5e-3",
+                      "pass": mx32 <= 2e-2 and rel32 <= 5e-3},
+            "against": "the CPU fp64 oracle on the CPU baseline's sample"}
 
 
 # ------------------------------------------------------------ CPU oracle --
@@ -607,8 +664,7 @@ def oracle_sample(workload: str):
 
 
 def oracle_pass(oracle, calls):
-    for pool, b in calls:
-        oracle.lora_apply(b.x, b.y0, b.ids, pool)
+    return [oracle.lora_apply(b.x, b.y0, b.ids, pool)[0] for pool, b in calls]
 
 
 def sample_text(wl, calls, scale, reps):
@@ -661,7 +717,8 @@ def oracle_all_cores(workload: str, seconds: float):
 
 def cpu_baseline(workload: str, seconds: float):
     """The fp64 oracle as it stands, single-threaded, on the step's calls repeated for a
-    bounded time; tokens/s.  Also the same oracle on every host core."""
+    bounded time; tokens/s.  Also the same oracle on every host core.  Returns the
+    baseline and the oracle's outputs of one pass (for the parity sample)."""
     import oracle
 
     wl, calls, scale = oracle_sample(workload)
@@ -669,23 +726,25 @@ def cpu_baseline(workload: str, seconds: float):
     n_tok = int((b.ids >= 0).sum())
     oracle.lora_apply(b.x[:1], b.y0[:1], b.ids[:1], calls[0][0])  # load/compile outside the clock
     reps = 0
+    ys = None
     t0 = time.perf_counter()
     while True:
-        oracle_pass(oracle, calls)
+        out = oracle_pass(oracle, calls)
+        ys = out if ys is None else ys
         reps += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    out = {"value": reps * n_tok / dt / scale, "unit": UNIT, "cores": 1, "kind": "oracle",
+    res = {"value": reps * n_tok / dt / scale, "unit": UNIT, "cores": 1, "kind": "oracle",
            "sample": sample_text(wl, calls, scale, reps) + ", %.1f s" % dt}
     try:
         v, n = oracle_all_cores(workload, seconds)
-        out["all_cores"] = {"value": v / scale, "cores": n,
+        res["all_cores"] = {"value": v / scale, "cores": n,
                             "sample": "the same calls split by token over %d spawned processes, %.0f s each"
                                       % (n, seconds)}
     except (OSError, RuntimeError, EOFError) as e:  # a host without process support
-        out["all_cores"] = {"unavailable": str(e)[:200]}
-    return out
+        res["all_cores"] = {"unavailable": str(e)[:200]}
+    return res, ys, [pool.d_out for pool, _ in calls]
 
 
 def run_reference(args, world, rank):
@@ -694,7 +753,8 @@ def run_reference(args, world, rank):
     for about K steps' worth of work, bounded to a minute; the single-core rate alongside."""
     import oracle
 
-    wl, calls, scale = oracle_sample(args.workload)
+    name = HEADLINE if args.workload == "all" else args.workload
+    wl, calls, scale = oracle_sample(name)
     b = wl.batch
     n_tok = int((b.ids >= 0).sum())
     oracle_pass(oracle, calls)  # load outside the clock
@@ -705,13 +765,13 @@ def run_reference(args, world, rank):
     try:
         n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
         seconds = min(60.0, max(5.0, args.steps * one / max(n, 1)))
-        value, n = oracle_all_cores(args.workload, seconds)
+        value, n = oracle_all_cores(name, seconds)
         value /= scale
         how = "the step's calls split by token over %d spawned processes, %.0f s" % (n, seconds)
     except (OSError, RuntimeError, EOFError):  # a host without process support: one core
         n, value, seconds = 1, single, one
         how = "one pass of the step's calls on one core"
-    ms = b.T / value * 1e3 / 1.0
+    ms = b.T / value * 1e3 if name != "mixed13b" else 4224 / value * 1e3
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -726,12 +786,24 @@ def run_reference(args, world, rank):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload],
+        "config": {"workload": WORKLOAD_TEXT[name],
                    "step": "the CPU fp64 oracle over the step's projection calls"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": n, "kind": "oracle",
                          "sample": how + "; one core: %.4g tokens/s (%s)" % (single, sample_text(wl, calls, scale, 1))},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+# ------------------------------------------------------------------- main --
+
+def config_line(name, args, world, rank, local, steps):
+    out = run_workload(name, steps, args.warmup, default_e2e_steps(name, args), args.soak_seconds,
+                       world, rank, local)
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        base, ys, d_outs = cpu_baseline(name, args.cpu_seconds)
+        out["cpu_baseline"] = base
+        out["parity"] = parity_report(gpu_sample(name, local), ys, d_outs)
+    return out
 
 
 def main(argv=None):
@@ -741,12 +813,39 @@ def main(argv=None):
         if rank == 0:
             print(json.dumps(run_reference(args, world, rank)), flush=True)
         return 0
+    import torch
+
     if world > 1:
-        import torch
         import torch.distributed as dist
 
         dist.init_process_group(backend="nccl")
-    out = run_ours(args, world, rank, local)
+    torch.cuda.set_device(local)
+    head = HEADLINE if args.workload == "all" else args.workload
+    per_config = {}
+    if args.workload == "all":
+        for name in OTHERS:
+            per_config[name] = config_line(name, args, world, rank, local, OTHER_STEPS[name])
+    h = config_line(head, args, world, rank, local, args.steps)
+    out = {
+        "metric": METRIC,
+        "value": h["value"],
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": h["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+    }
+    for k in ("config", "roofline", "e2e", "call_timing", "gpu_launches", "clocks", "cpu_baseline", "parity"):
+        if k in h:
+            out[k] = h[k]
+    if per_config:
+        out["per_config"] = per_config
+        out["gpu_launches_all_configs"] = h["gpu_launches"] + sum(c["gpu_launches"] for c in per_config.values())
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

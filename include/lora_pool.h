@@ -139,7 +139,11 @@ lora_status_t lora_pool_mgr_release(lora_pool_mgr_t* mgr, int32_t adapter);
  * written, though the view declares them const).  Errors as
  * lora_pool_mgr_reserve, plus LORA_ERR_INVALID_ARG for a mismatched view or a
  * null host pointer and LORA_ERR_CUDA if a copy or the launch fails (the
- * adapter is then not resident).
+ * adapter is then not resident).  If the kernel that zeroes the evicted
+ * adapters' descriptors fails to launch, the device may still address pages
+ * the manager now counts as free; the manager then refuses every later
+ * lora_pool_mgr_reserve, lora_pool_mgr_release, lora_pool_load and
+ * lora_pool_evict with LORA_ERR_CUDA (destroy it and rebuild the pool).
  */
 lora_status_t lora_pool_load(lora_pool_mgr_t* mgr, int32_t adapter, int32_t rank, float scale,
                              const void* host_A, const void* host_B, const lora_pool_view_t* view,
@@ -147,7 +151,8 @@ lora_status_t lora_pool_load(lora_pool_mgr_t* mgr, int32_t adapter, int32_t rank
 
 /** lora_pool_mgr_release, then the adapter's descriptor set to rank 0 on
  *  `stream` (one small kernel).  Errors as lora_pool_mgr_release and
- *  lora_pool_load. */
+ *  lora_pool_load; a failed launch of that kernel leaves the manager refusing
+ *  later calls, as in lora_pool_load. */
 lora_status_t lora_pool_evict(lora_pool_mgr_t* mgr, int32_t adapter, const lora_pool_view_t* view,
                               lora_stream_t stream);
 

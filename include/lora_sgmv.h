@@ -205,6 +205,24 @@ lora_status_t lora_apply(const void* x, int64_t ldx, void* y, int64_t ldy,
                          int32_t* dev_err, lora_stream_t stream);
 
 /**
+ * lora_apply with an fp32 output, for checking accuracy: the same kernels and
+ * the same sums, but the result float(y0[t, n]) + delta is written as fp32
+ * into yf instead of being rounded to bf16 in place, so a comparison against
+ * an exact reference sees the accumulation error alone (the bf16 rounding of
+ * the output, half an ulp, hides it otherwise; "Multi-LoRA Serving in
+ * Production", section "Mathematical Formulation and the Batching Challenge",
+ * defines the result this approximates).
+ *     yf[t, n] = float(y0[t, n]) + sum_j (s_i * sum_k x[t,k] A_i[j,k]) * B_i[j, n].
+ * y0: device bf16 [T, ldy0], read only.  yf: device fp32 [T, ldyf], ldyf >=
+ * d_out, ldyf % 4 == 0, 16-byte aligned, overlapping neither x nor y0; rows of
+ * tokens in no segment (and of tokens whose adapter is flagged on the device)
+ * and columns >= d_out are not written.
+ */
+lora_status_t lora_apply_f32y(const void* x, int64_t ldx, const void* y0, int64_t ldy0, float* yf,
+                              int64_t ldyf, const lora_segments_t* seg, const lora_pool_view_t* view,
+                              int32_t* dev_err, lora_stream_t stream);
+
+/**
  * Decode form without segments: each token t gathers its own adapter
  * token_adapter[t] (device int32 [T], -1 = no adapter), one token per request
  * (the batched gather path for size-1 segments of "Multi-LoRA serving: ...",
@@ -229,15 +247,19 @@ lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy,
  * (every GPU that loads the library holds it until the process exits).  It
  * allocates nothing.
  *
- * Arguments, results and errors are those of lora_apply; seg->h_scratch is not
- * used and may be NULL.  Returns LORA_ERR_UNSUPPORTED if seg->T exceeds
- * LORA_FIXED_SCRATCH_MAX_TOKENS.  The first call on a device looks up the
- * array's device address (once per device, on the current device); make that
- * first call before any stream capture.  Every call shares the one array: calls
- * that may run at the same time on the GPU (other streams, other host threads)
- * race on it and must be serialised by the caller.  The array keeps the last
- * call's contents; nothing in it needs to start at zero, because every value a
- * call reads was written earlier in the same call.
+ * Arguments, results and errors are those of lora_apply.  Only seg->h_scratch
+ * moves into the library's array (it is not read and may be NULL); every other
+ * array of the segment buffer, k_partials (the tensor-core path's partial
+ * sums, LORA_KSPLIT_MAX x T x LORA_MAX_RANK fp32) included, is still the
+ * caller's, carved as for lora_apply.  Returns LORA_ERR_UNSUPPORTED if seg->T
+ * exceeds LORA_FIXED_SCRATCH_MAX_TOKENS.  Each call looks up the array's
+ * device address on the current device (a host query; the first call on a
+ * device may also load the library's device code there, so make it before any
+ * stream capture).  Every call shares the one array: calls that may run at the
+ * same time on the GPU (other streams, other host threads) race on it and must
+ * be serialised by the caller.  The array keeps the last call's contents;
+ * nothing in it needs to start at zero, because every value a call reads was
+ * written earlier in the same call.
  */
 #define LORA_FIXED_SCRATCH_MAX_TOKENS 16384
 lora_status_t lora_apply_fixed_scratch(const void* x, int64_t ldx, void* y, int64_t ldy,

@@ -42,6 +42,7 @@ EXPORTED = (
     "lora_sgmv_shrink",
     "lora_sgmv_expand",
     "lora_apply",
+    "lora_apply_f32y",
     "lora_apply_fixed_scratch",
     "lora_bgmv",
     "lora_pool_pages_needed",
@@ -123,6 +124,8 @@ def lib():
         L.lora_sgmv_expand.argtypes = [vp, i64, vp, i64, seg_p, view_p, vp, vp]
         L.lora_apply.restype = i32
         L.lora_apply.argtypes = [vp, i64, vp, i64, seg_p, view_p, vp, vp]
+        L.lora_apply_f32y.restype = i32
+        L.lora_apply_f32y.argtypes = [vp, i64, vp, i64, vp, i64, seg_p, view_p, vp, vp]
         L.lora_apply_fixed_scratch.restype = i32
         L.lora_apply_fixed_scratch.argtypes = [vp, i64, vp, i64, seg_p, view_p, vp, vp]
         L.lora_bgmv.restype = i32
@@ -300,6 +303,19 @@ def lora_apply(x: torch.Tensor, y: torch.Tensor, seg: Segments, view: PoolView,
                err: Optional[torch.Tensor] = None, stream=None):
     _check(lib().lora_apply(_ptr(x), _ld(x), _ptr(y), _ld(y), ctypes.byref(seg.c),
                             ctypes.byref(view.c), _ptr(err), _stream(stream)), "lora_apply")
+
+
+def lora_apply_f32y(x: torch.Tensor, y0: torch.Tensor, yf: torch.Tensor, seg: Segments, view: PoolView,
+                    err: Optional[torch.Tensor] = None, stream=None):
+    """lora_apply with the result written as fp32 into yf (y0 bf16 is only read)."""
+    _check(lib().lora_apply_f32y(_ptr(x), _ld(x), _ptr(y0), _ld(y0), _ptr(yf), _ld(yf),
+                                 ctypes.byref(seg.c), ctypes.byref(view.c), _ptr(err), _stream(stream)),
+           "lora_apply_f32y")
+
+
+def apply_kernel_names():
+    """Names of the kernels one lora_apply call may launch, in launch order."""
+    return ["gather_kernel", "shrink_tc_kernel", "reduce_partials_kernel", "expand_tc_kernel"]
 
 
 def lora_apply_fixed_scratch(x: torch.Tensor, y: torch.Tensor, seg: Segments, view: PoolView,

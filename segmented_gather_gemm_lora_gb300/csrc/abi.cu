@@ -276,21 +276,22 @@ lora_status_t lora_segments_build(const int32_t* token_adapter, int32_t T, int32
 
 static lora_status_t run_segmented(int mode, const void* x, long long ldx, void* y, long long ldy,
                                    float* h, long long ldh, const lora_segments_t* seg,
-                                   const lora_pool_view_t* view, int32_t* dev_err, cudaStream_t s) {
+                                   const lora_pool_view_t* view, int32_t* dev_err, cudaStream_t s,
+                                   float* yf = nullptr, long long ldyf = 0) {
   // Long tiles go to the tensor-core kernels when the shapes allow it.
   bool tc;
   if (mode == kModeApply) tc = tc_shrink_ok(view) && tc_expand_ok(view);
   else if (mode == kModeShrink) tc = tc_shrink_ok(view);
   else tc = tc_expand_ok(view);
   lora_status_t st = launch_gather(mode, kSrcSegments, tc ? 1 : 0, x, ldx, y, ldy, h, ldh, seg, nullptr, 0, view,
-                                   dev_err, s);
+                                   dev_err, s, yf, ldyf);
   if (st != LORA_OK || !tc) return st;
   // the gather kernel was launched iff the buffer has tokens (its short-only bound is T)
   const int after_gather = seg->T > 0 ? 1 : 0;
   if (mode == kModeApply) {
     st = launch_shrink_tc(x, ldx, seg->h_scratch, LORA_MAX_RANK, 0, after_gather, seg, view, dev_err, s);
     if (st != LORA_OK) return st;
-    return launch_expand_tc(seg->h_scratch, LORA_MAX_RANK, 0, 0, y, ldy, seg, view, dev_err, s);
+    return launch_expand_tc(seg->h_scratch, LORA_MAX_RANK, 0, 0, y, ldy, seg, view, dev_err, s, yf, ldyf);
   }
   if (mode == kModeShrink) return launch_shrink_tc(x, ldx, h, ldh, 1, after_gather, seg, view, dev_err, s);
   return launch_expand_tc(h, ldh, 1, after_gather, y, ldy, seg, view, dev_err, s);
@@ -335,6 +336,24 @@ lora_status_t lora_apply(const void* x, int64_t ldx, void* y, int64_t ldy, const
   if (T > 0 && overlap(x, (long long)T * ldx * 2, y, (long long)T * ldy * 2)) return LORA_ERR_INVALID_ARG;
   if (T == 0) return LORA_OK;
   return run_segmented(kModeApply, x, ldx, y, ldy, nullptr, 0, seg, view, dev_err, (cudaStream_t)stream);
+}
+
+lora_status_t lora_apply_f32y(const void* x, int64_t ldx, const void* y0, int64_t ldy0, float* yf, int64_t ldyf,
+                              const lora_segments_t* seg, const lora_pool_view_t* view, int32_t* dev_err,
+                              lora_stream_t stream) {
+  lora_status_t st = check_view(view);
+  if (st != LORA_OK) return st;
+  if ((st = check_seg(seg)) != LORA_OK) return st;
+  const int T = seg->T;
+  if ((st = check_act(x, ldx, view->d_in, T)) != LORA_OK) return st;
+  if ((st = check_act(y0, ldy0, view->d_out, T)) != LORA_OK) return st;
+  if (T > 0 && (yf == nullptr || !aligned16(yf) || ldyf < view->d_out || ldyf % 4 != 0)) return LORA_ERR_INVALID_ARG;
+  if (T > 0 && (overlap(yf, (long long)T * ldyf * 4, x, (long long)T * ldx * 2) ||
+                overlap(yf, (long long)T * ldyf * 4, y0, (long long)T * ldy0 * 2)))
+    return LORA_ERR_INVALID_ARG;
+  if (T == 0) return LORA_OK;
+  return run_segmented(kModeApply, x, ldx, const_cast<void*>(y0), ldy0, nullptr, 0, seg, view, dev_err,
+                       (cudaStream_t)stream, yf, ldyf);
 }
 
 lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy, const int32_t* token_adapter,

@@ -9,33 +9,25 @@
 // fixed-size array that is part of the library's own device image: it is
 // created when the library is loaded onto a GPU and stays there until the
 // process exits.  Nothing is allocated per call.
-#include <mutex>
-
 #include "internal.h"
 
 namespace {
 
 // Scratch for LORA_FIXED_SCRATCH_MAX_TOKENS tokens x LORA_MAX_RANK fp32 values
 // (4 MiB).  In host code `g_fixed_h` only stands in for the symbol: its device
-// address comes from cudaGetSymbolAddress on each device.
+// address comes from cudaGetSymbolAddress on the current device.
 static __device__ __align__(256) float g_fixed_h[(size_t)LORA_FIXED_SCRATCH_MAX_TOKENS * LORA_MAX_RANK];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-float* g_fixed_h_addr[kMaxDevices];  // per device; null until that device's first call
-
-// Device address of g_fixed_h on the current device, looked up once per device.
+// Device address of g_fixed_h on the current device and context.  Looked up on
+// every call (a host-side query, no device work): a cached address could be
+// stale after a device reset or under another context.
 lora_status_t fixed_scratch_address(float** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return LORA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_fixed_h_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_fixed_h) != cudaSuccess || p == nullptr) return LORA_ERR_CUDA;
-    g_fixed_h_addr[dev] = static_cast<float*>(p);
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_fixed_h) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return LORA_ERR_CUDA;
   }
-  *out = g_fixed_h_addr[dev];
+  *out = static_cast<float*>(p);
   return LORA_OK;
 }
 

@@ -134,6 +134,8 @@ struct GatherArgs {
   long long ldy;
   float* h;
   long long ldh;
+  float* yf;  // non-null: fp32 output rows (y is then read only, for y0)
+  long long ldyf;
   DevView v;
   const int32_t* perm;
   const int32_t* indptr;
@@ -198,8 +200,9 @@ __device__ __forceinline__ void shrink_chunk(const uint8_t* sb, int nrows, int n
 // odd rows in two chains (rows ascending) whose sum is added to the running
 // total.  One load instruction of the warp reads 128 contiguous bytes of a
 // row.  The sub-slice's last chunk adds y0 and writes y.
-__device__ __forceinline__ void expand_chunk(uint16_t* ybase, long long ldy, const uint8_t* sb, const float* hs,
-                                             float (&acc)[kNT][2], const GRec& rc, bool ok, int warp, int lane) {
+__device__ __forceinline__ void expand_chunk(uint16_t* ybase, long long ldy, float* yf, long long ldyf,
+                                             const uint8_t* sb, const float* hs, float (&acc)[kNT][2],
+                                             const GRec& rc, bool ok, int warp, int lane) {
   const int m = warp * 32 + lane;
   if (m >= rc.nvec * 4) return;
   if (rc.flags & kFFirst) {
@@ -244,8 +247,12 @@ __device__ __forceinline__ void expand_chunk(uint16_t* ybase, long long ldy, con
     for (int t = 0; t < kNT; ++t) {
       if (t >= rc.ntok) break;
       const uint32_t y0 = *reinterpret_cast<const uint32_t*>(sb + (kChunkRows + t) * kRowBytes + 4 * m);
-      *reinterpret_cast<uint32_t*>(ybase + (long long)rc.tok[t] * ldy + rc.col0 + 2 * m) =
-          pack_bf16x2(bf_lo(y0) + acc[t][0], bf_hi(y0) + acc[t][1]);
+      if (yf != nullptr)  // fp32 output (diagnostic form): the same sums, not rounded to bf16
+        *reinterpret_cast<float2*>(yf + (long long)rc.tok[t] * ldyf + rc.col0 + 2 * m) =
+            make_float2(bf_lo(y0) + acc[t][0], bf_hi(y0) + acc[t][1]);
+      else
+        *reinterpret_cast<uint32_t*>(ybase + (long long)rc.tok[t] * ldy + rc.col0 + 2 * m) =
+            pack_bf16x2(bf_lo(y0) + acc[t][0], bf_hi(y0) + acc[t][1]);
     }
   }
 }
@@ -633,6 +640,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
     const int ctid = tid;  // 0 .. 255
     uint16_t* const ybase = a.y;  // parameters the loop needs, read once up front
     const long long ldy = a.ldy;
+    float* const yf = a.yf;
+    const long long ldyf = a.ldyf;
     float* const hout = a.h;
     const long long ldh = a.ldh;
     const int mode = a.mode;
@@ -745,7 +754,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         }
         cons_sync();
       }
-      if (rc.kind == kGExpand) expand_chunk(ybase, ldy, sb, hs, eacc, rc, ok, warp, lane);
+      if (rc.kind == kGExpand) expand_chunk(ybase, ldy, yf, ldyf, sb, hs, eacc, rc, ok, warp, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
     }
@@ -767,7 +776,7 @@ static int cluster_size_for(const lora_pool_view_t* view) {
 lora_status_t launch_gather(int mode, int src, int short_only, const void* x, long long ldx, void* y, long long ldy,
                             float* h, long long ldh, const lora_segments_t* seg,
                             const int32_t* token_adapter, int T, const lora_pool_view_t* view,
-                            int32_t* err, cudaStream_t stream) {
+                            int32_t* err, cudaStream_t stream, float* yf, long long ldyf) {
   GatherArgs a;
   a.x = static_cast<const uint16_t*>(x);
   a.ldx = ldx;
@@ -775,6 +784,8 @@ lora_status_t launch_gather(int mode, int src, int short_only, const void* x, lo
   a.ldy = ldy;
   a.h = h;
   a.ldh = ldh;
+  a.yf = yf;
+  a.ldyf = ldyf;
   make_dev_view(view, &a.v);
   a.perm = seg ? seg->token_perm : nullptr;
   a.indptr = seg ? seg->seg_indptr : nullptr;

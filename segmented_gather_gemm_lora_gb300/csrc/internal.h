@@ -47,10 +47,12 @@ enum GatherSrc { kSrcSegments = 0, kSrcTokens = 1 };
 // CUDA-core gather kernel over the segments' work lists (short units, then
 // long tiles unless short_only, when the tensor-core kernels take them) or over
 // one-token units.
+// yf (apply mode only): when non-null, outputs go to yf as fp32 [T, ldyf] and y
+// is only read (for y0).
 lora_status_t launch_gather(int mode, int src, int short_only, const void* x, long long ldx, void* y,
                             long long ldy, float* h, long long ldh, const lora_segments_t* seg,
                             const int32_t* token_adapter, int T, const lora_pool_view_t* view,
-                            int32_t* err, cudaStream_t stream);
+                            int32_t* err, cudaStream_t stream, float* yf = nullptr, long long ldyf = 0);
 
 // Tensor-core path for long tiles.  Eligibility: d_in % 64 == 0 (shrink),
 // d_out % 128 == 0 (expand), pages of at least 128 elements.
@@ -63,8 +65,9 @@ lora_status_t launch_shrink_tc(const void* x, long long ldx, float* h, long long
                                cudaStream_t stream);
 // after_gather: as for launch_shrink_tc; only in expand-only calls (lora_apply's
 // expand reads the h its shrink wrote and waits).
+// yf: as for launch_gather.
 lora_status_t launch_expand_tc(const float* h, long long ldh, int h_by_token, int after_gather, void* y, long long ldy,
                                const lora_segments_t* seg, const lora_pool_view_t* view, int32_t* err,
-                               cudaStream_t stream);
+                               cudaStream_t stream, float* yf = nullptr, long long ldyf = 0);
 
 }  // namespace lora

@@ -33,6 +33,10 @@ struct lora_pool_mgr {
   std::vector<int32_t> prev, next;          // list of resident adapters, least recent first
   int32_t head = -1, tail = -1;
   lora_pool_stats_t stats{};    // resident and pinned are counted when asked for
+  // Set when zeroing an evicted adapter's descriptor failed to launch: the device
+  // may still address pages the host now counts as free, so every later call
+  // that hands out or frees pages returns LORA_ERR_CUDA.
+  bool broken = false;
   mutable std::mutex mu;
 };
 
@@ -309,6 +313,7 @@ lora_status_t lora_pool_mgr_reserve(lora_pool_mgr_t* mgr, int32_t adapter, int32
   if (pages_out == nullptr || pages_cap < mgr->slots_per) return LORA_ERR_INVALID_ARG;
   if (evicted_out == nullptr || evicted_cap < mgr->n_adapters) return LORA_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(mgr->mu);
+  if (mgr->broken) return LORA_ERR_CUDA;
   std::vector<int32_t> evicted;
   bool fresh = false;
   const lora_status_t st = reserve_locked(mgr, adapter, rank, &evicted, &fresh);
@@ -325,6 +330,7 @@ lora_status_t lora_pool_mgr_reserve(lora_pool_mgr_t* mgr, int32_t adapter, int32
 lora_status_t lora_pool_mgr_release(lora_pool_mgr_t* mgr, int32_t adapter) {
   if (mgr == nullptr || adapter < 0 || adapter >= mgr->n_adapters) return LORA_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(mgr->mu);
+  if (mgr->broken) return LORA_ERR_CUDA;
   if (mgr->rank[adapter] == 0) return LORA_OK;
   if (mgr->pins[adapter] > 0) return LORA_ERR_INVALID_ARG;
   release_locked(mgr, adapter);
@@ -337,6 +343,7 @@ lora_status_t lora_pool_load(lora_pool_mgr_t* mgr, int32_t adapter, int32_t rank
   lora_status_t st = check_mgr_view(mgr, view);
   if (st != LORA_OK) return st;
   std::lock_guard<std::mutex> lock(mgr->mu);
+  if (mgr->broken) return LORA_ERR_CUDA;
   std::vector<int32_t> evicted;
   bool fresh = false;
   st = reserve_locked(mgr, adapter, rank, &evicted, &fresh);
@@ -345,6 +352,12 @@ lora_status_t lora_pool_load(lora_pool_mgr_t* mgr, int32_t adapter, int32_t rank
   const int64_t na = pages_a(mgr, rank), nb = pages_b(mgr, rank);
   const std::vector<int32_t>& pg = mgr->pages[adapter];
   cudaError_t e = zero_descs(evicted, view, s);
+  if (e != cudaSuccess) {
+    // The evicted adapters' pages are free on the host but their descriptors may
+    // still point at them on the device: nothing may hand those pages out again.
+    mgr->broken = true;
+    return LORA_ERR_CUDA;
+  }
   if (e == cudaSuccess)
     e = copy_matrix(mgr, pg.data(), na, (int64_t)rank * mgr->d_in, static_cast<const uint16_t*>(host_A), view, s);
   if (e == cudaSuccess)
@@ -381,11 +394,15 @@ lora_status_t lora_pool_evict(lora_pool_mgr_t* mgr, int32_t adapter, const lora_
   lora_status_t st = check_mgr_view(mgr, view);
   if (st != LORA_OK) return st;
   std::lock_guard<std::mutex> lock(mgr->mu);
+  if (mgr->broken) return LORA_ERR_CUDA;
   if (mgr->rank[adapter] == 0) return LORA_OK;
   if (mgr->pins[adapter] > 0) return LORA_ERR_INVALID_ARG;
   release_locked(mgr, adapter);
-  return zero_descs(std::vector<int32_t>{adapter}, view, (cudaStream_t)stream) == cudaSuccess ? LORA_OK
-                                                                                               : LORA_ERR_CUDA;
+  if (zero_descs(std::vector<int32_t>{adapter}, view, (cudaStream_t)stream) != cudaSuccess) {
+    mgr->broken = true;  // as in lora_pool_load: the device may still address the freed pages
+    return LORA_ERR_CUDA;
+  }
+  return LORA_OK;
 }
 
 }  // extern "C"

@@ -575,6 +575,8 @@ struct ExpandArgs {
   CUtensorMap ymap;  // y as [T rows, d_out columns], 128 x 64 boxes, 128-byte swizzle
   uint16_t* y;
   long long ldy;
+  float* yf;  // non-null: fp32 output rows (y is then read only, for y0)
+  long long ldyf;
   const float* h;
   long long ldh;
   int h_by_token;
@@ -988,6 +990,24 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
+      if (a.yf != nullptr) {  // fp32 output (diagnostic form): the same sums, not rounded to bf16
+        if (ok && m < rc.cnt) {
+          float* frow = a.yf + (long long)tok_m * a.ldyf + rc.n0 + half * 64;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            float y0[8];
+            unpack8(*reinterpret_cast<const uint4*>(atom + sw128_offset(m, cc)), y0);
+            float4* o4 = reinterpret_cast<float4*>(frow + 8 * cc);
+            o4[0] = make_float4(y0[0] + __uint_as_float(acc[8 * cc]), y0[1] + __uint_as_float(acc[8 * cc + 1]),
+                                y0[2] + __uint_as_float(acc[8 * cc + 2]), y0[3] + __uint_as_float(acc[8 * cc + 3]));
+            o4[1] = make_float4(y0[4] + __uint_as_float(acc[8 * cc + 4]), y0[5] + __uint_as_float(acc[8 * cc + 5]),
+                                y0[6] + __uint_as_float(acc[8 * cc + 6]), y0[7] + __uint_as_float(acc[8 * cc + 7]));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
+        continue;
+      }
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
         uint4* qp = reinterpret_cast<uint4*>(atom + sw128_offset(m, cc));
@@ -1226,8 +1246,10 @@ lora_status_t launch_shrink_tc(const void* x, long long ldx, float* h, long long
 
 lora_status_t launch_expand_tc(const float* h, long long ldh, int h_by_token, int after_gather, void* y, long long ldy,
                                const lora_segments_t* seg, const lora_pool_view_t* view, int32_t* err,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, float* yf, long long ldyf) {
   ExpandArgs a;
+  a.yf = yf;
+  a.ldyf = ldyf;
   const long long upper = (long long)seg->max_long_units * (view->d_out / kENC);
   long long grid = sm_count();
   if (upper < grid) grid = upper;

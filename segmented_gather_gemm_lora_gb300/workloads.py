@@ -352,14 +352,34 @@ def mixed13b(seed: int = 0, layers: Sequence[int] = (0,), projections: Sequence[
     referenced[np.unique(ids)] = True
     resident = np.where(referenced, ranks, 0).astype(np.int32)
     names = [p[0] for p in PROJ_13B] if projections is None else list(projections)
-    pools = []
-    for layer in layers:
-        for name in names:
-            d_in, d_out = {p[0]: (p[1], p[2]) for p in PROJ_13B}[name]
-            prng = np.random.default_rng([seed, 1 + int(layer), 1 + names.index(name)])
-            pools.append(build_pool(prng, d_in, d_out, resident, max_rank=64))
+    pools = [mixed13b_pool(seed, resident, layer, name) for layer in layers for name in names]
     batch = make_batch(rng, ids, 5120, 5120)
     return Workload("mixed13b", batch, pools, mode=0, n_adapters=1000)
+
+
+def mixed13b_pool(seed: int, resident: np.ndarray, layer: int, name: str) -> AdapterPool:
+    """One (layer, projection) pool of the 13B-shaped batch; its draws depend only on the
+    seed, the layer and the projection's place in the layer."""
+    order = [p[0] for p in PROJ_13B]
+    _, d_in, d_out = PROJ_13B[order.index(name)]
+    prng = np.random.default_rng([seed, 1 + int(layer), 1 + order.index(name)])
+    return build_pool(prng, d_in, d_out, resident, max_rank=64)
+
+
+def mixed13b_projection(seed: int, layer: int, name: str):
+    """(pool, batch, n_adapters) of one (layer, projection) call of the 13B-shaped batch:
+    the pool as mixed13b draws it and a batch of that projection's shape on the batch's
+    ids (x and y0 drawn from the seed, the layer and the projection)."""
+    rng = np.random.default_rng(seed)
+    ranks = mixed13b_ranks(rng)
+    ids = mixed13b_ids(rng)
+    resident = np.zeros(1000, dtype=np.int32)
+    used = np.unique(ids)
+    resident[used] = ranks[used]
+    pool = mixed13b_pool(seed, resident, layer, name)
+    order = [p[0] for p in PROJ_13B]
+    brng = np.random.default_rng([seed, 101 + int(layer), 1 + order.index(name)])
+    return pool, make_batch(brng, ids, pool.d_in, pool.d_out), 1000
 
 
 WORKLOADS = {

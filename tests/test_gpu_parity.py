@@ -9,8 +9,8 @@ import torch
 import oracle
 from segmented_gather_gemm_lora_gb300 import binding as B
 from segmented_gather_gemm_lora_gb300 import workloads as W
-from gpu_util import (compare_bf16, cuda_or_skip, ids_dev, new_err, run_apply, run_bgmv,
-                      to_dev_bits, to_host_bits)
+from gpu_util import (compare_bf16, compare_f32, cuda_or_skip, ids_dev, new_err, oracle_apply, run_apply,
+                      run_apply_f32y, run_bgmv, to_dev_bits, to_host_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -187,32 +187,110 @@ def test_apply_small_pages():
     compare_bf16(y, ref, "64-element pages")
 
 
-def test_apply_mixed13b_layer_sampled():
-    """13B-shaped mixed batch, one layer's seven projections, full T = 4224; the oracle
-    checks a sample of 160 rows (all decode rows' adapters are represented)."""
-    wl = W.mixed13b(0, layers=(0,))
-    rng = np.random.default_rng(13)
-    ids = wl.batch.ids
-    rows = np.sort(np.concatenate([rng.choice(4096, 96, replace=False), 4096 + rng.choice(128, 64, replace=False)]))
-    for pool in wl.pools:
-        batch = W.make_batch(rng, ids, pool.d_in, pool.d_out)
-        y, err, _ = run_apply(batch, pool, wl.mode, wl.n_adapters)
-        assert err == 0
-        ref, _ = oracle.lora_apply(batch.x[rows], batch.y0[rows], ids[rows], pool)
-        compare_bf16(y[rows], ref, "13B %dx%d" % (pool.d_in, pool.d_out))
+MIXED13B_PROJ = [p[0] for p in W.PROJ_13B]
 
 
-@pytest.mark.slow
-@pytest.mark.parametrize("mode", [B.LORA_SEG_CONTIGUOUS, B.LORA_SEG_GROUP])
-def test_apply_prefill_full_sampled(mode):
-    wl = W.prefill(0)
-    pool = wl.pools[0]
-    y, err, _ = run_apply(wl.batch, pool, mode, wl.n_adapters)
+def mixed13b_cases():
+    """(layer, projection, all rows?) pairs of the 13B-shaped check: every projection of
+    layers 0, 19 and 39 (one projection per layer on all 4224 rows, the rest on a sample)
+    plus eight random (layer, projection) pairs."""
+    full = {0: "q", 19: "gate", 39: "down"}
+    cases = [(layer, name, full[layer] == name) for layer in (0, 19, 39) for name in MIXED13B_PROJ]
+    rng = np.random.default_rng(1313)
+    for _ in range(8):
+        cases.append((int(rng.integers(0, 40)), MIXED13B_PROJ[int(rng.integers(0, 7))], False))
+    return cases
+
+
+@pytest.mark.parametrize("layer,name,all_rows", mixed13b_cases())
+def test_apply_mixed13b(layer, name, all_rows):
+    """13B-shaped mixed batch (4 prefill requests of 1024 tokens + 128 decode tokens, GROUP
+    segments, T = 4224), one (layer, projection) call at full size.  The oracle checks
+    every row, or all 128 decode rows plus 160 prefill rows; rows of the full case are
+    also checked through lora_apply_f32y against the literal bounds."""
+    pool, batch, n_ad = W.mixed13b_projection(0, layer, name)
+    ids = batch.ids
+    view = B.PoolView.from_host(pool)
+    y, err, _ = run_apply(batch, pool, B.LORA_SEG_GROUP, n_ad, view=view)
     assert err == 0
-    rng = np.random.default_rng(14)
-    rows = np.sort(rng.choice(wl.batch.T, 256, replace=False))
-    ref, _ = oracle.lora_apply(wl.batch.x[rows], wl.batch.y0[rows], wl.batch.ids[rows], pool)
-    compare_bf16(y[rows], ref, "prefill full")
+    if all_rows:
+        rows = np.arange(batch.T)
+    else:
+        rng = np.random.default_rng([layer, MIXED13B_PROJ.index(name)])
+        rows = np.sort(np.concatenate([rng.choice(4096, 160, replace=False), 4096 + np.arange(128)]))
+    ref, oerr = oracle_apply(batch.x[rows], batch.y0[rows], ids[rows], pool)
+    assert oerr == 0
+    compare_bf16(y[rows], ref, "13B layer %d %s" % (layer, name))
+    if all_rows:
+        yf, errf = run_apply_f32y(batch, pool, B.LORA_SEG_GROUP, n_ad, view=view)
+        assert errf == 0
+        compare_f32(yf, ref, "13B f32y layer %d %s" % (layer, name))
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_apply_prefill_full(seed):
+    """The prefill configuration at full size (32 requests of 64..512 tokens), every row,
+    CONTIGUOUS segments as the configuration states (and GROUP for seed 0)."""
+    wl = W.prefill(seed)
+    pool = wl.pools[0]
+    ref, _ = oracle_apply(wl.batch.x, wl.batch.y0, wl.batch.ids, pool)
+    for mode in ([B.LORA_SEG_CONTIGUOUS, B.LORA_SEG_GROUP] if seed == 0 else [B.LORA_SEG_CONTIGUOUS]):
+        y, err, _ = run_apply(wl.batch, pool, mode, wl.n_adapters)
+        assert err == 0
+        compare_bf16(y, ref, "prefill seed %d mode %d" % (seed, mode))
+
+
+@pytest.mark.parametrize("seed", range(5))
+@pytest.mark.parametrize("which", ["up", "down"])
+def test_apply_hetero_seeds(seed, which):
+    """Heterogeneous ranks at full size (256 decode tokens, 500 adapters of rank 8..64,
+    MLP up 4096 -> 11008 or down 11008 -> 4096), every row, seeds 0-4."""
+    wl = W.hetero(seed, which=which)
+    pool = wl.pools[0]
+    batch = W.make_batch(np.random.default_rng([seed, 7]), wl.batch.ids, pool.d_in, pool.d_out)
+    y, err, _ = run_apply(batch, pool, wl.mode, wl.n_adapters)
+    assert err == 0
+    ref, _ = oracle_apply(batch.x, batch.y0, batch.ids, pool)
+    compare_bf16(y, ref, "hetero %s seed %d" % (which, seed))
+
+
+def f32y_cases():
+    cases = []
+    for seed in range(5):
+        cases += [("tiny", seed), ("decode", seed), ("prefill", seed), ("hetero_up", seed), ("hetero_down", seed)]
+    return cases
+
+
+@pytest.mark.parametrize("name,seed", f32y_cases())
+def test_f32y_literal_bounds(name, seed):
+    """Every configuration through lora_apply_f32y (the same kernels as lora_apply, fp32
+    output): max |err| <= 2e-2 and relative L2 <= 5e-3 against the oracle, with no
+    allowance for output rounding; rows of tokens without an adapter stay unwritten.
+    The bf16 outputs of lora_apply equal the fp32 ones rounded to nearest even."""
+    if name.startswith("hetero"):
+        which = name.split("_")[1]
+        wl = W.hetero(seed, which=which)
+        pool = wl.pools[0]
+        ids = wl.batch.ids.copy()
+        ids[::11] = -1
+        batch = W.make_batch(np.random.default_rng([seed, 7]), ids, pool.d_in, pool.d_out)
+    else:
+        wl = W.WORKLOADS[name](seed)
+        pool = wl.pools[0]
+        batch = wl.batch
+        if name == "decode":
+            batch.ids[::9] = -1
+    view = B.PoolView.from_host(pool)
+    yf, err = run_apply_f32y(batch, pool, wl.mode, wl.n_adapters, view=view)
+    assert err == 0
+    ref, _ = oracle_apply(batch.x, batch.y0, batch.ids, pool)
+    on = batch.ids >= 0
+    compare_f32(yf[on], ref[on], "f32y %s seed %d" % (name, seed))
+    assert np.isnan(yf[~on]).all()
+    y, err2, _ = run_apply(batch, pool, wl.mode, wl.n_adapters, view=view)
+    assert err2 == 0
+    rounded = W.f32_to_bf16_bits(yf[on])
+    assert np.array_equal(y[on][:, : pool.d_out], rounded)
 
 
 # --------------------------------------------------------------------- bgmv --

@@ -1,8 +1,9 @@
 """lora_apply_fixed_scratch: the entry point for callers that cannot allocate device
 memory (their device memory is planned once by a host runtime, so they cannot size
 or request the workspace lora_apply keeps its intermediate in).  It must give the
-same outputs as lora_apply, call after call, although every call reuses the one
-fixed array inside the library.
+same outputs as lora_apply, bit for bit, call after call, although every call reuses
+the one fixed array inside the library, and it must not touch the caller's
+h_scratch (passed as NULL here, so a call that still used it would fail).
 
 This file is collected last on purpose: if it fails, a run that stops at the first
 failure has already run every other test.
@@ -16,7 +17,7 @@ import torch
 
 from segmented_gather_gemm_lora_gb300 import binding as B
 from segmented_gather_gemm_lora_gb300 import workloads as W
-from gpu_util import compare_bf16, cuda_or_skip, ids_dev, new_err, to_dev_bits, to_host_bits
+from gpu_util import compare_bf16, cuda_or_skip, ids_dev, new_err, oracle_apply, to_dev_bits, to_host_bits
 
 
 def batch_with_long_and_short_segments(seed):
@@ -31,12 +32,14 @@ def batch_with_long_and_short_segments(seed):
     return pool, batch
 
 
-def run(entry, pool, batch, view):
+def run(entry, pool, batch, view, no_h_scratch=False):
     x = to_dev_bits(batch.x)
     y = to_dev_bits(batch.y0)
     seg = B.Segments(batch.T)
     err = new_err()
     B.lora_segments_build(ids_dev(batch.ids), pool.n_adapters, seg, mode=B.LORA_SEG_GROUP, err=err)
+    if no_h_scratch:
+        seg.c.h_scratch = None  # the fixed-scratch call must not read or write it
     entry(x, y, seg, view, err=err)
     torch.cuda.synchronize()
     return to_host_bits(y), int(err.item())
@@ -48,12 +51,15 @@ def test_fixed_scratch_matches_lora_apply_on_two_calls_in_a_row():
     cases = [batch_with_long_and_short_segments(s) for s in (1, 2)]
     views = [B.PoolView.from_host(pool) for pool, _ in cases]
     # two calls of the fixed-scratch entry point back to back, then the reference calls
-    fixed = [run(B.lora_apply_fixed_scratch, pool, batch, view) for (pool, batch), view in zip(cases, views)]
+    fixed = [run(B.lora_apply_fixed_scratch, pool, batch, view, no_h_scratch=True)
+             for (pool, batch), view in zip(cases, views)]
     for ((pool, batch), view), (y_fixed, e_fixed) in zip(zip(cases, views), fixed):
         y_ref, e_ref = run(B.lora_apply, pool, batch, view)
         assert e_fixed == e_ref == 0
-        ref = W.bf16_bits_to_f32(y_ref).astype(np.float64)
-        compare_bf16(y_fixed, ref, "fixed scratch vs lora_apply")
+        assert np.array_equal(y_fixed, y_ref), "fixed scratch differs from lora_apply"
+        ref, oerr = oracle_apply(batch.x, batch.y0, batch.ids, pool)
+        assert oerr == 0
+        compare_bf16(y_fixed, ref, "fixed scratch vs oracle")
 
 
 def test_fixed_scratch_rejects_batches_above_its_limit():
