@@ -204,6 +204,36 @@ lora_status_t lora_apply(const void* x, int64_t ldx, void* y, int64_t ldy,
                          const lora_segments_t* seg, const lora_pool_view_t* view,
                          int32_t* dev_err, lora_stream_t stream);
 
+/** Projections one lora_apply_multi call takes, at most. */
+#define LORA_MAX_PROJ 4
+
+/** One projection of a lora_apply_multi call (host struct, device pointers). */
+typedef struct {
+  const void* x;          /* device bf16 [T, ldx]; may be shared with other projections */
+  int64_t ldx;
+  void* y;                /* device bf16 [T, ldy], updated in place */
+  int64_t ldy;
+  lora_pool_view_t view;  /* the projection's adapters */
+} lora_proj_t;
+
+/**
+ * Several projections of one layer that share a batch in one grouped call:
+ * the q, k and v projections of attention (one input x), or the gate and up
+ * projections of an MLP ("Multi-LoRA Serving in Production", section "Ragged
+ * Batching and FlashInfer Grouped GEMM": the adapters of every projection in a
+ * single fused invocation).  The result is that of n_proj lora_apply calls,
+ * one per projection, on the same segments: bit for bit for tokens on the
+ * tensor-core path; tokens of short segments may be summed in another order,
+ * within the stated tolerance, when the grouped call gives the gather kernel
+ * narrower clusters.  The work units of all projections share each launch, a
+ * tile's units for every projection side by side, so x rows that several
+ * projections read come from DRAM once.
+ * 1 <= n_proj <= LORA_MAX_PROJ.  Every view must have the same d_in; each
+ * projection's x and y as for lora_apply; no y may overlap another y or any x.
+ */
+lora_status_t lora_apply_multi(const lora_proj_t* projs, int32_t n_proj, const lora_segments_t* seg,
+                               int32_t* dev_err, lora_stream_t stream);
+
 /**
  * lora_apply with an fp32 output, for checking accuracy: the same kernels and
  * the same sums, but the result float(y0[t, n]) + delta is written as fp32

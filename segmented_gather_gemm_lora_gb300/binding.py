@@ -34,6 +34,7 @@ LORA_TILE_M = 128
 LORA_SEG_GROUP = 0
 LORA_SEG_CONTIGUOUS = 1
 LORA_FIXED_SCRATCH_MAX_TOKENS = 16384
+LORA_MAX_PROJ = 4
 
 EXPORTED = (
     "lora_segments_buffer_bytes",
@@ -43,6 +44,7 @@ EXPORTED = (
     "lora_sgmv_expand",
     "lora_apply",
     "lora_apply_f32y",
+    "lora_apply_multi",
     "lora_apply_fixed_scratch",
     "lora_bgmv",
     "lora_pool_pages_needed",
@@ -75,6 +77,11 @@ class lora_pool_view_t(ctypes.Structure):
                 ("adapters", ctypes.c_void_p), ("n_adapters", ctypes.c_int32),
                 ("page_elems", ctypes.c_int32), ("max_rank", ctypes.c_int32),
                 ("d_in", ctypes.c_int32), ("d_out", ctypes.c_int32)]
+
+
+class lora_proj_t(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("ldx", ctypes.c_int64), ("y", ctypes.c_void_p),
+                ("ldy", ctypes.c_int64), ("view", lora_pool_view_t)]
 
 
 class lora_pool_stats_t(ctypes.Structure):
@@ -126,6 +133,8 @@ def lib():
         L.lora_apply.argtypes = [vp, i64, vp, i64, seg_p, view_p, vp, vp]
         L.lora_apply_f32y.restype = i32
         L.lora_apply_f32y.argtypes = [vp, i64, vp, i64, vp, i64, seg_p, view_p, vp, vp]
+        L.lora_apply_multi.restype = i32
+        L.lora_apply_multi.argtypes = [ctypes.POINTER(lora_proj_t), i32, seg_p, vp, vp]
         L.lora_apply_fixed_scratch.restype = i32
         L.lora_apply_fixed_scratch.argtypes = [vp, i64, vp, i64, seg_p, view_p, vp, vp]
         L.lora_bgmv.restype = i32
@@ -313,9 +322,23 @@ def lora_apply_f32y(x: torch.Tensor, y0: torch.Tensor, yf: torch.Tensor, seg: Se
            "lora_apply_f32y")
 
 
+def lora_apply_multi(calls, seg: Segments, err: Optional[torch.Tensor] = None, stream=None):
+    """Several projections on one batch in one grouped call: `calls` is a list of
+    (x, y, view) with the same d_in; projections may share x."""
+    arr = (lora_proj_t * len(calls))()
+    for i, (x, y, view) in enumerate(calls):
+        arr[i].x = _ptr(x).value
+        arr[i].ldx = _ld(x)
+        arr[i].y = _ptr(y).value
+        arr[i].ldy = _ld(y)
+        arr[i].view = view.c
+    _check(lib().lora_apply_multi(arr, len(calls), ctypes.byref(seg.c), _ptr(err), _stream(stream)),
+           "lora_apply_multi")
+
+
 def apply_kernel_names():
     """Names of the kernels one lora_apply call may launch, in launch order."""
-    return ["gather_kernel", "shrink_tc_kernel", "reduce_partials_kernel", "expand_tc_kernel"]
+    return ["gather_kernel", "fused_tc_kernel"]
 
 
 def lora_apply_fixed_scratch(x: torch.Tensor, y: torch.Tensor, seg: Segments, view: PoolView,

@@ -277,10 +277,11 @@ lora_status_t lora_segments_build(const int32_t* token_adapter, int32_t T, int32
 static lora_status_t run_segmented(int mode, const void* x, long long ldx, void* y, long long ldy,
                                    float* h, long long ldh, const lora_segments_t* seg,
                                    const lora_pool_view_t* view, int32_t* dev_err, cudaStream_t s,
-                                   float* yf = nullptr, long long ldyf = 0) {
-  // Long tiles go to the tensor-core kernels when the shapes allow it.
+                                   float* yf = nullptr, long long ldyf = 0, bool staged = false) {
+  // Long tiles go to the tensor-core kernels when the shapes allow it: the fused
+  // kernel for lora_apply, the staged ones for the separate stages.
   bool tc;
-  if (mode == kModeApply) tc = tc_shrink_ok(view) && tc_expand_ok(view);
+  if (mode == kModeApply) tc = staged ? tc_shrink_ok(view) && tc_expand_ok(view) : tc_fused_ok(view);
   else if (mode == kModeShrink) tc = tc_shrink_ok(view);
   else tc = tc_expand_ok(view);
   lora_status_t st = launch_gather(mode, kSrcSegments, tc ? 1 : 0, x, ldx, y, ldy, h, ldh, seg, nullptr, 0, view,
@@ -288,6 +289,10 @@ static lora_status_t run_segmented(int mode, const void* x, long long ldx, void*
   if (st != LORA_OK || !tc) return st;
   // the gather kernel was launched iff the buffer has tokens (its short-only bound is T)
   const int after_gather = seg->T > 0 ? 1 : 0;
+  if (mode == kModeApply && !staged) {
+    const ProjCall p{x, ldx, y, ldy, yf, ldyf, view};
+    return launch_fused_tc(1, &p, seg, after_gather, dev_err, s);
+  }
   if (mode == kModeApply) {
     st = launch_shrink_tc(x, ldx, seg->h_scratch, LORA_MAX_RANK, 0, after_gather, seg, view, dev_err, s);
     if (st != LORA_OK) return st;
@@ -295,6 +300,19 @@ static lora_status_t run_segmented(int mode, const void* x, long long ldx, void*
   }
   if (mode == kModeShrink) return launch_shrink_tc(x, ldx, h, ldh, 1, after_gather, seg, view, dev_err, s);
   return launch_expand_tc(h, ldh, 1, after_gather, y, ldy, seg, view, dev_err, s);
+}
+
+// The checks of lora_apply.
+static lora_status_t check_apply(const void* x, long long ldx, void* y, long long ldy, const lora_segments_t* seg,
+                                 const lora_pool_view_t* view) {
+  lora_status_t st = check_view(view);
+  if (st != LORA_OK) return st;
+  if ((st = check_seg(seg)) != LORA_OK) return st;
+  const int T = seg->T;
+  if ((st = check_act(x, ldx, view->d_in, T)) != LORA_OK) return st;
+  if ((st = check_act(y, ldy, view->d_out, T)) != LORA_OK) return st;
+  if (T > 0 && overlap(x, (long long)T * ldx * 2, y, (long long)T * ldy * 2)) return LORA_ERR_INVALID_ARG;
+  return LORA_OK;
 }
 
 lora_status_t lora_sgmv_shrink(const void* x, int64_t ldx, float* h, int64_t ldh,
@@ -327,15 +345,42 @@ lora_status_t lora_sgmv_expand(const float* h, int64_t ldh, void* y, int64_t ldy
 
 lora_status_t lora_apply(const void* x, int64_t ldx, void* y, int64_t ldy, const lora_segments_t* seg,
                          const lora_pool_view_t* view, int32_t* dev_err, lora_stream_t stream) {
-  lora_status_t st = check_view(view);
-  if (st != LORA_OK) return st;
-  if ((st = check_seg(seg)) != LORA_OK) return st;
-  const int T = seg->T;
-  if ((st = check_act(x, ldx, view->d_in, T)) != LORA_OK) return st;
-  if ((st = check_act(y, ldy, view->d_out, T)) != LORA_OK) return st;
-  if (T > 0 && overlap(x, (long long)T * ldx * 2, y, (long long)T * ldy * 2)) return LORA_ERR_INVALID_ARG;
-  if (T == 0) return LORA_OK;
+  const lora_status_t st = check_apply(x, ldx, y, ldy, seg, view);
+  if (st != LORA_OK || seg->T == 0) return st;
   return run_segmented(kModeApply, x, ldx, y, ldy, nullptr, 0, seg, view, dev_err, (cudaStream_t)stream);
+}
+
+lora_status_t lora_apply_multi(const lora_proj_t* projs, int32_t n_proj, const lora_segments_t* seg,
+                               int32_t* dev_err, lora_stream_t stream) {
+  if (projs == nullptr || n_proj < 1) return LORA_ERR_INVALID_ARG;
+  if (n_proj > LORA_MAX_PROJ) return LORA_ERR_UNSUPPORTED;
+  lora_status_t st = check_seg(seg);
+  if (st != LORA_OK) return st;
+  const int T = seg->T;
+  ProjCall calls[LORA_MAX_PROJ];
+  bool tc = true;
+  for (int g = 0; g < n_proj; ++g) {
+    const lora_proj_t& p = projs[g];
+    if ((st = check_view(&p.view)) != LORA_OK) return st;
+    if (p.view.d_in != projs[0].view.d_in) return LORA_ERR_INVALID_ARG;
+    if ((st = check_act(p.x, p.ldx, p.view.d_in, T)) != LORA_OK) return st;
+    if ((st = check_act(p.y, p.ldy, p.view.d_out, T)) != LORA_OK) return st;
+    calls[g] = ProjCall{p.x, p.ldx, p.y, p.ldy, nullptr, 0, &p.view};
+    tc = tc && tc_fused_ok(&p.view);
+  }
+  if (T == 0) return LORA_OK;
+  for (int g = 0; g < n_proj; ++g)  // no output overlaps an input or another output
+    for (int k = 0; k < n_proj; ++k) {
+      const lora_proj_t &pg = projs[g], &pk = projs[k];
+      if (overlap(pg.y, (long long)T * pg.ldy * 2, pk.x, (long long)T * pk.ldx * 2)) return LORA_ERR_INVALID_ARG;
+      if (k != g && overlap(pg.y, (long long)T * pg.ldy * 2, pk.y, (long long)T * pk.ldy * 2))
+        return LORA_ERR_INVALID_ARG;
+    }
+  const cudaStream_t s = (cudaStream_t)stream;
+  st = launch_gather_multi(kModeApply, kSrcSegments, tc ? 1 : 0, n_proj, calls, nullptr, 0, seg, nullptr, 0,
+                           dev_err, s);
+  if (st != LORA_OK || !tc) return st;
+  return launch_fused_tc(n_proj, calls, seg, 1, dev_err, s);
 }
 
 lora_status_t lora_apply_f32y(const void* x, int64_t ldx, const void* y0, int64_t ldy0, float* yf, int64_t ldyf,
@@ -373,3 +418,16 @@ lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy, const 
 }  // extern "C"
 
 extern "C" uint64_t lora_launch_count(void) { return lora::g_launches.load(std::memory_order_relaxed); }
+
+namespace lora {
+
+// Defined here, outside the C linkage block, so it can reach run_segmented.
+lora_status_t apply_staged(const void* x, long long ldx, void* y, long long ldy, const lora_segments_t* seg,
+                           const lora_pool_view_t* view, int32_t* err, cudaStream_t stream) {
+  const lora_status_t st = check_apply(x, ldx, y, ldy, seg, view);
+  if (st != LORA_OK || seg->T == 0) return st;
+  return run_segmented(kModeApply, x, ldx, y, ldy, nullptr, 0, seg, view, err, stream, nullptr, 0, true);
+}
+
+}  // namespace lora
+

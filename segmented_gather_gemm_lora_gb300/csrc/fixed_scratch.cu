@@ -41,8 +41,10 @@ extern "C" lora_status_t lora_apply_fixed_scratch(const void* x, int64_t ldx, vo
   float* h = nullptr;
   const lora_status_t st = fixed_scratch_address(&h);
   if (st != LORA_OK) return st;
-  // Same arguments, same kernels as lora_apply; only the intermediate's home differs.
+  // Same arguments and results as lora_apply, through the staged kernels, which
+  // keep the intermediate in global memory between the shrink and the expand:
+  // here in the library's array instead of the caller's h_scratch.
   lora_segments_t local = *seg;
   local.h_scratch = h;
-  return lora_apply(x, ldx, y, ldy, &local, view, dev_err, stream);
+  return lora::apply_staged(x, ldx, y, ldy, &local, view, dev_err, (cudaStream_t)stream);
 }

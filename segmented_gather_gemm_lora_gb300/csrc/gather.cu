@@ -38,6 +38,9 @@
 // A token's result therefore depends neither on how many tokens share its unit
 // nor on its adapter's rank: zero-padding an adapter or moving a token between
 // units changes no bit of its output.
+#include <algorithm>
+#include <cstring>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -82,6 +85,7 @@ struct __align__(16) GRec {
   int flags;  // GFlag bits
   int r;      // rank
   float sc;   // scale
+  int g;      // projection
   int tok[kNT];
 };
 static_assert(sizeof(GRec) <= 64 && sizeof(GRec) % 16 == 0, "record slot, read as 16-byte pieces");
@@ -109,6 +113,7 @@ struct GUnit {
   int cnt;       // tokens of the unit
   int na;        // page slots of A_i; B_i's follow them in the cache
   int cached;    // 1: every page slot of the adapter is in the cache
+  int g;         // projection
   int tok[kNT];  // the first group's tokens
   long long a_page0, b_page0;
 };
@@ -127,16 +132,22 @@ constexpr size_t kOffBars = kOffCls + 3 * 32 * sizeof(uint32_t);
 constexpr int kNBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1 + 1;
 constexpr size_t kGatherSmem = kOffBars + kNBars * 8;
 
-struct GatherArgs {
+// One projection of the call: its activations and its view of the adapter pool.
+struct GProj {
   const uint16_t* x;
   long long ldx;
   uint16_t* y;
   long long ldy;
-  float* h;
-  long long ldh;
-  float* yf;  // non-null: fp32 output rows (y is then read only, for y0)
-  long long ldyf;
   DevView v;
+};
+
+struct GatherArgs {
+  GProj proj[kMaxFusedProj];
+  int n_proj;  // projections sharing the segments (apply mode); unit u is (u / n_proj, projection u % n_proj)
+  float* h;    // shrink / expand modes (one projection)
+  long long ldh;
+  float* yf;  // non-null: fp32 output rows (y is then read only, for y0; one projection)
+  long long ldyf;
   const int32_t* perm;
   const int32_t* indptr;
   const int32_t* seg_adapter;
@@ -281,8 +292,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t crank = cluster_ctarank(), ncta = cluster_nctarank();
   const uint32_t cid = cluster_id_x(), ncl = ncluster_x();
-  const DevView& v = a.v;
   const bool dynamic = a.src == kSrcSegments;
+  const int G = a.n_proj;
   const bool reduce_h = a.mode != kModeExpand;
 
   if (tid == 0) {
@@ -306,15 +317,11 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   cluster_sync();
   pdl_wait_then_release();
 
-  const int kc = ((v.d_in + (int)ncta - 1) / (int)ncta + 7) & ~7;
-  const int nc = ((v.d_out + (int)ncta - 1) / (int)ncta + 7) & ~7;
-  const int k0 = min(v.d_in, (int)crank * kc), k1 = min(v.d_in, k0 + kc);
-  const int n0 = min(v.d_out, (int)crank * nc), n1 = min(v.d_out, n0 + nc);
-  const int nks = (a.mode != kModeExpand && k1 > k0) ? (k1 - k0 + kSub - 1) / kSub : 0;
-  const int nns = (a.mode != kModeShrink && n1 > n0) ? (n1 - n0 + kSub - 1) / kSub : 0;
   bool ok = true;
   const int n_short = a.src == kSrcSegments ? a.meta[2] : 0;
-  const int n_units = a.src == kSrcTokens ? a.T : a.meta[2] + (a.short_only ? 0 : a.meta[3]);
+  // units of one projection (a segment's group of tokens, or a token), times the projections
+  const int n_base = a.src == kSrcTokens ? a.T : a.meta[2] + (a.short_only ? 0 : a.meta[3]);
+  const int n_units = n_base * G;
   const int n_dyn = max(0, n_units - (int)ncl);  // units claimed from the counter
   // Order of the claimed units: largest first.  A unit's time grows with its
   // adapter's row blocks, and a cluster that draws a large unit last keeps the
@@ -330,7 +337,6 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
     // Claims a unit, resolves its segment, tokens and adapter, checks every
     // page slot of the adapter and caches the physical pages, a unit ahead of
     // the producer (two unit slots).
-    const int shift = v.page_shift;
     // Claims: unit cid first, then units ncl + counter, CTA 0 claiming for the
     // cluster.  Each cluster over-claims the counter exactly once; the last
     // claim of all puts it back to zero for the next call.  A unit is claimed
@@ -419,31 +425,34 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       const uint32_t q = take_slot();
       if (k > 0) next_unit();
       if (u >= n_units) break;
+      const int ub = u / G, g = u - ub * G;  // the unit of its projection, the projection
+      const DevView& v = a.proj[g].v;
+      const int shift = v.page_shift;
       int ad, tb = 0, cnt;
       if (a.src == kSrcTokens) {
-        ad = a.token_adapter[u];
-        tb = u;
+        ad = a.token_adapter[ub];
+        tb = ub;
         cnt = 1;
         if (ad == -1) continue;
         if (ad < -1 || ad >= v.n_adapters) {
           if (crank == 0 && lane == 0) report(a.err, LORA_DERR_BAD_ADAPTER);
           continue;
         }
-      } else if (u < n_short) {
-        const int s = a.short_units[u];
+      } else if (ub < n_short) {
+        const int s = a.short_units[ub];
         ad = a.seg_adapter[s];
         tb = a.indptr[s];
         cnt = a.indptr[s + 1] - tb;
       } else {
-        const int s = a.long_units[2 * (u - n_short)];
-        const int m0 = a.long_units[2 * (u - n_short) + 1];
+        const int s = a.long_units[2 * (ub - n_short)];
+        const int m0 = a.long_units[2 * (ub - n_short) + 1];
         ad = a.seg_adapter[s];
         tb = a.indptr[s] + m0;
         cnt = min(LORA_TILE_M, a.indptr[s + 1] - tb);
       }
       // The first group's tokens do not depend on the adapter: load them
       // alongside its descriptor.
-      const int first_tok = lane < min(kNT, cnt) ? (a.src == kSrcTokens ? u : a.perm[tb + lane]) : -1;
+      const int first_tok = lane < min(kNT, cnt) ? (a.src == kSrcTokens ? ub : a.perm[tb + lane]) : -1;
       if (ad < 0 || ad >= v.n_adapters) {  // segments built for more adapters than the view has
         if (crank == 0 && lane == 0) report(a.err, LORA_DERR_BAD_ADAPTER);
         continue;
@@ -492,6 +501,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       un.cnt = cnt;
       un.na = (int)na;
       un.cached = cached ? 1 : 0;
+      un.g = g;
 #pragma unroll
       for (int t = 0; t < kNT; ++t) un.tok[t] = __shfl_sync(0xffffffffu, first_tok, t);
       un.a_page0 = d.a_page0;
@@ -518,8 +528,6 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
     if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
   } else if (warp == kGProd) {
     // ---------------- producer ----------------
-    const int shift = v.page_shift;
-    const long long pmask = (1LL << shift) - 1;
     uint32_t g = 0;  // stages posted
     auto take_stage = [&]() -> uint32_t {
       const uint32_t st = g % kStages;
@@ -543,6 +551,17 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       }
       const GUnit un = units[q];
       if (un.end) break;
+      const GProj& P = a.proj[un.g];
+      const DevView& v = P.v;
+      const int shift = v.page_shift;
+      const long long pmask = (1LL << shift) - 1;
+      // this CTA's slices of d_in (shrink) and d_out (expand) for the unit's projection
+      const int kc = ((v.d_in + (int)ncta - 1) / (int)ncta + 7) & ~7;
+      const int nc = ((v.d_out + (int)ncta - 1) / (int)ncta + 7) & ~7;
+      const int k0 = min(v.d_in, (int)crank * kc), k1 = min(v.d_in, k0 + kc);
+      const int n0 = min(v.d_out, (int)crank * nc), n1 = min(v.d_out, n0 + nc);
+      const int nks = (a.mode != kModeExpand && k1 > k0) ? (k1 - k0 + kSub - 1) / kSub : 0;
+      const int nns = (a.mode != kModeShrink && n1 > n0) ? (n1 - n0 + kSub - 1) / kSub : 0;
       const int* pc = pgt + q * kMaxPgSlots;
       const int r = un.r, cnt = un.cnt;
       const long long na = un.na;
@@ -555,6 +574,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         rc.ntok = ntok;
         rc.r = r;
         rc.sc = un.sc;
+        rc.g = un.g;
 #pragma unroll
         for (int t = 0; t < kNT; ++t) rc.tok[t] = __shfl_sync(0xffffffffu, mytok, t);
         // One chunk: adapter rows [j0, j0 + nrows) of the sub-slice at col0,
@@ -598,7 +618,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
               rem -= n;
             }
           } else if (lane < nrows + ntr) {
-            const uint16_t* src = (shrink ? a.x + (long long)tk * a.ldx : a.y + (long long)tk * a.ldy) + col0;
+            const uint16_t* src = (shrink ? P.x + (long long)tk * P.ldx : P.y + (long long)tk * P.ldy) + col0;
             bulk_g2s(sbase + (uint32_t)((kChunkRows + lane - nrows) * kRowBytes), src, rowb, bar);
           }
           ++g;
@@ -638,9 +658,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   } else {
     // ---------------- consumers ----------------
     const int ctid = tid;  // 0 .. 255
-    uint16_t* const ybase = a.y;  // parameters the loop needs, read once up front
-    const long long ldy = a.ldy;
-    float* const yf = a.yf;
+    float* const yf = a.yf;  // parameters the loop needs, read once up front
     const long long ldyf = a.ldyf;
     float* const hout = a.h;
     const long long ldh = a.ldh;
@@ -653,14 +671,21 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
     if (ordered) {  // classify the claimable units: four per thread, every load in flight
       int val[4];
 #pragma unroll
+      int gk[4];
+#pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int i = ctid + kGConsThreads * k, uu = (int)ncl + i;
-        val[k] = i >= n_dyn ? -1 : uu < n_short ? a.short_units[uu] : a.long_units[2 * (uu - n_short)];
+        const int ub = uu / G;
+        gk[k] = uu - ub * G;
+        val[k] = i >= n_dyn ? -1 : ub < n_short ? a.short_units[ub] : a.long_units[2 * (ub - n_short)];
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) val[k] = val[k] < 0 ? -1 : a.seg_adapter[val[k]];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) val[k] = val[k] < 0 || val[k] >= v.n_adapters ? 0 : v.adapters[val[k]].rank;
+      for (int k = 0; k < 4; ++k) {
+        const DevView& vk = a.proj[gk[k]].v;
+        val[k] = val[k] < 0 || val[k] >= vk.n_adapters ? 0 : vk.adapters[val[k]].rank;
+      }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int i = ctid + kGConsThreads * k;
@@ -754,7 +779,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         }
         cons_sync();
       }
-      if (rc.kind == kGExpand) expand_chunk(ybase, ldy, yf, ldyf, sb, hs, eacc, rc, ok, warp, lane);
+      if (rc.kind == kGExpand)
+        expand_chunk(a.proj[rc.g].y, a.proj[rc.g].ldy, yf, ldyf, sb, hs, eacc, rc, ok, warp, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
     }
@@ -765,28 +791,35 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   cluster_sync();
 }
 
-static int cluster_size_for(const lora_pool_view_t* view) {
-  const int d = view->d_in > view->d_out ? view->d_in : view->d_out;
+static int cluster_size_for(const lora_pool_view_t* const* views, int n) {
+  int d = 0;
+  for (int g = 0; g < n; ++g) d = std::max(d, std::max(views[g]->d_in, views[g]->d_out));
   int cl = (d + 511) / 512;
   if (cl < 1) cl = 1;
   if (cl > kMaxCluster) cl = kMaxCluster;
   return cl;
 }
 
-lora_status_t launch_gather(int mode, int src, int short_only, const void* x, long long ldx, void* y, long long ldy,
-                            float* h, long long ldh, const lora_segments_t* seg,
-                            const int32_t* token_adapter, int T, const lora_pool_view_t* view,
-                            int32_t* err, cudaStream_t stream, float* yf, long long ldyf) {
+lora_status_t launch_gather_multi(int mode, int src, int short_only, int n_proj, const ProjCall* projs, float* h,
+                                  long long ldh, const lora_segments_t* seg, const int32_t* token_adapter, int T,
+                                  int32_t* err, cudaStream_t stream) {
+  if (n_proj < 1 || n_proj > kMaxFusedProj) return LORA_ERR_INVALID_ARG;
   GatherArgs a;
-  a.x = static_cast<const uint16_t*>(x);
-  a.ldx = ldx;
-  a.y = static_cast<uint16_t*>(y);
-  a.ldy = ldy;
+  memset(&a, 0, sizeof(a));
+  const lora_pool_view_t* views[kMaxFusedProj];
+  for (int g = 0; g < n_proj; ++g) {
+    a.proj[g].x = static_cast<const uint16_t*>(projs[g].x);
+    a.proj[g].ldx = projs[g].ldx;
+    a.proj[g].y = static_cast<uint16_t*>(projs[g].y);
+    a.proj[g].ldy = projs[g].ldy;
+    make_dev_view(projs[g].view, &a.proj[g].v);
+    views[g] = projs[g].view;
+  }
+  a.n_proj = n_proj;
   a.h = h;
   a.ldh = ldh;
-  a.yf = yf;
-  a.ldyf = ldyf;
-  make_dev_view(view, &a.v);
+  a.yf = projs[0].yf;
+  a.ldyf = projs[0].ldyf;
   a.perm = seg ? seg->token_perm : nullptr;
   a.indptr = seg ? seg->seg_indptr : nullptr;
   a.seg_adapter = seg ? seg->seg_adapter : nullptr;
@@ -801,12 +834,12 @@ lora_status_t launch_gather(int mode, int src, int short_only, const void* x, lo
   a.src = src;
   a.short_only = short_only;
 
-  const int upper = src == kSrcTokens ? T : seg->T + (short_only ? 0 : seg->max_long_units);
+  const int upper = (src == kSrcTokens ? T : seg->T + (short_only ? 0 : seg->max_long_units)) * n_proj;
   if (upper <= 0) return LORA_OK;
   if (ensure_smem_attr((const void*)gather_kernel, kGatherSmem) != cudaSuccess) return LORA_ERR_CUDA;
   // The widest cluster whose resident clusters take every unit at once
   // (halving from the width the slices want); if none does, the full width.
-  const int cl0 = cluster_size_for(view);
+  const int cl0 = cluster_size_for(views, n_proj);
   int cl = cl0;
   for (int c = cl0; c >= 2; c /= 2) {
     if (upper <= max_active_clusters((const void*)gather_kernel, kGThreads, kGatherSmem, c)) {
@@ -820,6 +853,14 @@ lora_status_t launch_gather(int mode, int src, int short_only, const void* x, lo
                     stream, cl, &a) == cudaSuccess
              ? LORA_OK
              : LORA_ERR_CUDA;
+}
+
+lora_status_t launch_gather(int mode, int src, int short_only, const void* x, long long ldx, void* y, long long ldy,
+                            float* h, long long ldh, const lora_segments_t* seg,
+                            const int32_t* token_adapter, int T, const lora_pool_view_t* view,
+                            int32_t* err, cudaStream_t stream, float* yf, long long ldyf) {
+  const ProjCall p{x, ldx, y, ldy, yf, ldyf, view};
+  return launch_gather_multi(mode, src, short_only, 1, &p, h, ldh, seg, token_adapter, T, err, stream);
 }
 
 }  // namespace lora

@@ -41,12 +41,31 @@ void count_launch();
 lora_status_t launch_segments(const int32_t* ids, int T, int n_adapters, int mode,
                               const lora_segments_t* seg, int32_t* err, cudaStream_t stream);
 
+// One projection of a call: its activations, optional fp32 output and view.
+constexpr int kMaxFusedProj = LORA_MAX_PROJ;
+struct ProjCall {
+  const void* x;
+  long long ldx;
+  void* y;  // bf16 y, updated in place (or only read, for y0, when yf is set)
+  long long ldy;
+  float* yf;  // optional fp32 output
+  long long ldyf;
+  const lora_pool_view_t* view;
+};
+
 enum GatherMode { kModeApply = 0, kModeShrink = 1, kModeExpand = 2 };
 enum GatherSrc { kSrcSegments = 0, kSrcTokens = 1 };
 
 // CUDA-core gather kernel over the segments' work lists (short units, then
 // long tiles unless short_only, when the tensor-core kernels take them) or over
 // one-token units.
+// The gather kernel over n_proj projections that share the segments (apply
+// mode): a unit is (segment or token, projection), projections fastest.  h, and
+// projs[0].yf, only with one projection.
+lora_status_t launch_gather_multi(int mode, int src, int short_only, int n_proj, const ProjCall* projs, float* h,
+                                  long long ldh, const lora_segments_t* seg, const int32_t* token_adapter, int T,
+                                  int32_t* err, cudaStream_t stream);
+
 // yf (apply mode only): when non-null, outputs go to yf as fp32 [T, ldyf] and y
 // is only read (for y0).
 lora_status_t launch_gather(int mode, int src, int short_only, const void* x, long long ldx, void* y,
@@ -54,10 +73,32 @@ lora_status_t launch_gather(int mode, int src, int short_only, const void* x, lo
                             const int32_t* token_adapter, int T, const lora_pool_view_t* view,
                             int32_t* err, cudaStream_t stream, float* yf = nullptr, long long ldyf = 0);
 
+// Slices of d_in the tensor-core shrink splits a tile into (ks, each of klen
+// columns, a multiple of 64; the last may be shorter): about 512 columns each,
+// at most kMaxKSplit.  A function of d_in alone, so a token's h does not depend
+// on the rest of the batch; the staged and the fused tensor-core paths use the
+// same slices and so compute the same h bit for bit.
+constexpr int kMaxKSplit = 4;
+void shrink_split(int d_in, int* ks, int* klen);
+
 // Tensor-core path for long tiles.  Eligibility: d_in % 64 == 0 (shrink),
 // d_out % 128 == 0 (expand), pages of at least 128 elements.
 bool tc_shrink_ok(const lora_pool_view_t* v);
 bool tc_expand_ok(const lora_pool_view_t* v);
+// Fused tensor-core path (tc_fused.cu): shrink, exchange of the intermediate
+// between the CTAs of a cluster and expand of each long tile in one kernel, for
+// up to kMaxFusedProj projections that share the segments and d_in.
+// Eligibility: d_in % 64 == 0, d_out % 64 == 0.
+bool tc_fused_ok(const lora_pool_view_t* v);
+lora_status_t launch_fused_tc(int n_proj, const ProjCall* projs, const lora_segments_t* seg, int after_gather,
+                              int32_t* err, cudaStream_t stream);
+
+// lora_apply through the staged tensor-core kernels (shrink_tc, reduce_partials,
+// expand_tc) with the intermediate in seg->h_scratch; arguments checked as for
+// lora_apply.  Same results as lora_apply, bit for bit.
+lora_status_t apply_staged(const void* x, long long ldx, void* y, long long ldy, const lora_segments_t* seg,
+                           const lora_pool_view_t* view, int32_t* err, cudaStream_t stream);
+
 // after_gather: the gather kernel of the same call was launched just before
 // (the two touch disjoint data), so this grid need not wait for it.
 lora_status_t launch_shrink_tc(const void* x, long long ldx, float* h, long long ldh, int h_by_token, int after_gather,

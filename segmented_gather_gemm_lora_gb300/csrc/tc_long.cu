@@ -45,52 +45,6 @@
 
 namespace lora {
 
-constexpr int kTM = LORA_TILE_M;  // 128
-
-// One long tile: rows p0 .. p0 + cnt - 1 of the segment order, all on adapter ad.
-struct TileInfo {
-  int ad, p0, cnt;
-  int row0;  // token of the first row
-  bool tma;  // 128 consecutive tokens and tensor maps available
-};
-
-__device__ __forceinline__ TileInfo load_tile(const int32_t* long_units, const int32_t* seg_adapter,
-                                              const int32_t* indptr, const int32_t* perm, int tile, int use_tma) {
-  TileInfo t;
-  const int s = long_units[2 * tile], m0 = long_units[2 * tile + 1];
-  t.ad = seg_adapter[s];
-  t.p0 = indptr[s] + m0;
-  t.cnt = min(kTM, indptr[s + 1] - t.p0);
-  t.row0 = perm[t.p0];
-  t.tma = use_tma && t.cnt == kTM && perm[t.p0 + kTM - 1] - t.row0 == kTM - 1;
-  return t;
-}
-
-// Adapter id, rank, every page-list slot and page of A_i and B_i, checked by
-// one warp; returns 0 or LORA_DERR_* bits (the same in every lane).  `d` is
-// adapter_desc(v, ad).
-__device__ __forceinline__ int check_adapter_warp(const DevView& v, int ad, const lora_adapter_desc_t& d, int lane) {
-  if (ad < 0 || ad >= v.n_adapters) return LORA_DERR_BAD_ADAPTER;
-  if (d.rank < 1 || d.rank > v.max_rank || d.rank > LORA_MAX_RANK) return LORA_DERR_BAD_RANK;
-  const long long na = ((long long)d.rank * v.d_in + (1LL << v.page_shift) - 1) >> v.page_shift;
-  const long long nb = ((long long)d.rank * v.d_out + (1LL << v.page_shift) - 1) >> v.page_shift;
-  int mine = 0;
-  for (long long i0 = 0; i0 < na + nb; i0 += 32 * 8) {  // eight page-list reads in flight per lane
-    int pv[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const long long i = i0 + 32 * k + lane;
-      const long long slot = i < na ? d.a_page0 + i : d.b_page0 + (i - na);
-      pv[k] = 0;
-      if (i < na + nb) pv[k] = (slot < 0 || slot >= v.n_page_list) ? -1 : v.page_list[slot];
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (pv[k] < 0 || pv[k] >= v.n_pages) mine = 1;
-  }
-  return __any_sync(0xffffffffu, mine) ? LORA_DERR_BAD_PAGE : 0;
-}
-
 // Four consecutive fp32 values to h[j .. j + 3], only those below r.
 __device__ __forceinline__ void store_h4(float* hrow, int j, int r, float a, float b, float c, float d) {
   if (j + 3 < r) {
@@ -132,7 +86,7 @@ constexpr int kSABytes = 64 * 128;   // A tile: up to 64 rank rows x 64 bf16
 constexpr int kSStageBytes = kSXBytes + kSABytes;
 constexpr int kSTmaRows = 64;    // x rows of a full tile that come by TMA
 static_assert(kSTmaRows % 16 == 0 && kSTmaRows <= kTM, "x rows split between TMA and the loader warps");
-constexpr int kSMaxChunks = 32;  // 64-column chunks per unit
+constexpr int kSMaxChunks = 64;  // 64-column chunks per unit
 constexpr int kRecEnd = 1, kRecTma = 2, kRecNewTile = 4;
 
 struct SUnit {  // scheduler -> loaders
@@ -1151,9 +1105,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 matrix [rows, cols] with a row stride of `ld` elements as a tensor map
-// of box_rows x 64 boxes with 128-byte swizzle.  False when the driver offers
-// no encoder or rejects the map; the kernels then copy every tile row by row.
+}  // namespace
+
 bool make_act_map(CUtensorMap* m, const void* base, long long rows, long long cols, long long ld, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (fn == nullptr) return false;
@@ -1166,6 +1119,8 @@ bool make_act_map(CUtensorMap* m, const void* base, long long rows, long long co
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+
 template <typename Args>
 void fill_common(Args* a, const lora_segments_t* seg, const lora_pool_view_t* view, int32_t* err) {
   make_dev_view(view, &a->v);
@@ -1177,18 +1132,16 @@ void fill_common(Args* a, const lora_segments_t* seg, const lora_pool_view_t* vi
   a->err = err;
 }
 
-// Slices of d_in per tile: about 512 columns each, at most LORA_KSPLIT_MAX.  A
-// function of d_in alone, so a token's h does not depend on the rest of the batch.
+}  // namespace
+
 void shrink_split(int d_in, int* ks, int* klen) {
   int k = d_in / 512;
   if (k < 1) k = 1;
-  if (k > LORA_KSPLIT_MAX) k = LORA_KSPLIT_MAX;
+  if (k > kMaxKSplit) k = kMaxKSplit;
   const int len = ((d_in + k - 1) / k + 63) / 64 * 64;
   *klen = len;
   *ks = (d_in + len - 1) / len;
 }
-
-}  // namespace
 
 bool tc_shrink_ok(const lora_pool_view_t* v) {
   int ks, klen;

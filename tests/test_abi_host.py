@@ -160,3 +160,25 @@ def test_empty_batches_are_noops_without_launch():
     assert L.lora_apply(None, 256, None, 256, ctypes.byref(seg), ctypes.byref(v), None, None) == 0
     assert L.lora_bgmv(None, 256, None, 256, None, 0, ctypes.byref(v), None, None) == 0
     assert L.lora_sgmv_shrink(None, 256, None, 16, ctypes.byref(seg), ctypes.byref(v), None, None) == 0
+
+
+def test_apply_multi_rejects_bad_groups_on_the_host():
+    """Argument checks of lora_apply_multi happen before any launch (no GPU needed)."""
+    L = B.lib()
+    seg = B.lora_segments_t()
+    seg.T = 0  # nothing to launch even when the arguments pass
+    projs = (B.lora_proj_t * 2)()
+    for i in range(2):
+        v = projs[i].view
+        v.pool, v.n_pages, v.page_list, v.n_page_list = 0x100000, 4, 0x200000, 8
+        v.adapters, v.n_adapters, v.page_elems, v.max_rank = 0x300000, 2, 4096, 16
+        v.d_in, v.d_out = 4096, 1024
+        projs[i].x, projs[i].ldx, projs[i].y, projs[i].ldy = 0x400000, 4096, 0x800000 + i * 0x100000, 1024
+    assert L.lora_apply_multi(projs, 2, ctypes.byref(seg), None, None) == B.LORA_OK
+    assert L.lora_apply_multi(projs, 0, ctypes.byref(seg), None, None) == B.LORA_ERR_INVALID_ARG
+    assert L.lora_apply_multi(projs, B.LORA_MAX_PROJ + 1, ctypes.byref(seg), None, None) == B.LORA_ERR_UNSUPPORTED
+    projs[1].view.d_in = 2048
+    assert L.lora_apply_multi(projs, 2, ctypes.byref(seg), None, None) == B.LORA_ERR_INVALID_ARG
+    projs[1].view.d_in = 4096
+    projs[1].view.max_rank = 65
+    assert L.lora_apply_multi(projs, 2, ctypes.byref(seg), None, None) == B.LORA_ERR_UNSUPPORTED

@@ -723,3 +723,78 @@ def test_gather_multi_token_units_mixed_subslice_widths():
         compare_bf16(y, ref, "gather 5120x5120, run %d" % rep)
         first = y if first is None else first
         assert np.array_equal(y, first)
+
+
+# ------------------------------------------------------ multi-projection call --
+
+def multi_case(seed, d_in, d_outs, n_long=3, n_short=20):
+    """Projections on one batch (shared x, one pool per projection, mixed ranks) with long
+    segments (tensor-core path) and short ones (gather path)."""
+    rng = np.random.default_rng(seed)
+    n_ad = 12
+    ranks = rng.choice(np.array([8, 16, 32, 64], dtype=np.int32), size=n_ad)
+    lens = list(rng.integers(129, 400, size=n_long)) + list(rng.integers(1, 8, size=n_short))
+    ids = np.concatenate([np.full(n, i % n_ad, dtype=np.int32) for i, n in enumerate(lens)])
+    ids = ids[rng.permutation(ids.size)]
+    ids[rng.random(ids.size) < 0.03] = -1
+    T = ids.size
+    x = W._normal_bf16(rng, (T, d_in), 1.0)
+    pools, y0s = [], []
+    for d_out in d_outs:
+        pools.append(W.build_pool(rng, d_in, d_out, ranks, max_rank=64))
+        y0s.append(W._normal_bf16(rng, (T, d_out), 1.0))
+    return ids, x, pools, y0s, n_ad
+
+
+@pytest.mark.parametrize("d_in,d_outs", [(5120, (5120, 5120, 5120)), (4096, (1024, 2048)),
+                                         (1024, (4096, 4096, 512, 1536))])
+def test_apply_multi_matches_separate_calls_and_oracle(d_in, d_outs):
+    ids, x, pools, y0s, n_ad = multi_case(41, d_in, d_outs)
+    seg = B.Segments(ids.size)
+    err = new_err()
+    B.lora_segments_build(ids_dev(ids), n_ad, seg, mode=B.LORA_SEG_GROUP, err=err)
+    views = [B.PoolView.from_host(p) for p in pools]
+    xd = to_dev_bits(x)
+    ys = [to_dev_bits(y0) for y0 in y0s]
+    B.lora_apply_multi([(xd, y, v) for y, v in zip(ys, views)], seg, err=err)
+    sep = []
+    for y0, v in zip(y0s, views):
+        y = to_dev_bits(y0)
+        B.lora_apply(xd, y, seg, v, err=err)
+        sep.append(y)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    perm, indptr, seg_ad, n_tok, short, long_ = seg.host()
+    long_tok = np.zeros(ids.size, dtype=bool)
+    for s_, m0 in long_:
+        lo = indptr[s_] + m0
+        long_tok[perm[lo:min(lo + 128, indptr[s_ + 1])]] = True
+    for g, (pool, y0) in enumerate(zip(pools, y0s)):
+        got, want = to_host_bits(ys[g]), to_host_bits(sep[g])
+        assert np.array_equal(got[long_tok], want[long_tok]), "projection %d, tensor-core rows" % g
+        ref, _ = oracle_apply(x, y0, ids, pool)
+        compare_bf16(got, ref, "multi projection %d" % g)
+        assert np.array_equal(got[ids < 0], y0[ids < 0])
+
+
+def test_apply_multi_mixed13b_qkv_and_gate_up():
+    """The 13B-shaped batch's q, k, v (one x) and gate, up (one x) as two grouped calls on
+    one segment build, every row against the oracle for v and up, sampled rows otherwise."""
+    rng = np.random.default_rng(77)
+    for names in (("q", "k", "v"), ("gate", "up")):
+        parts = [W.mixed13b_projection(0, 5, n) for n in names]
+        ids = parts[0][1].ids
+        x = parts[0][1].x  # one input for the group
+        seg = B.Segments(ids.size)
+        err = new_err()
+        B.lora_segments_build(ids_dev(ids), 1000, seg, mode=B.LORA_SEG_GROUP, err=err)
+        xd = to_dev_bits(x)
+        ys = [to_dev_bits(b.y0) for _, b, _ in parts]
+        B.lora_apply_multi([(xd, y, B.PoolView.from_host(p)) for (p, _, _), y in zip(parts, ys)], seg, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        for k, ((pool, b, _), y) in enumerate(zip(parts, ys)):
+            rows = np.arange(ids.size) if k == len(parts) - 1 else \
+                np.sort(np.concatenate([rng.choice(4096, 128, replace=False), 4096 + np.arange(128)]))
+            ref, _ = oracle_apply(x[rows], b.y0[rows], ids[rows], pool)
+            compare_bf16(to_host_bits(y)[rows], ref, "13B grouped %s" % names[k])
