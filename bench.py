@@ -8,7 +8,9 @@ A step is one pass of the whole path over one batch of one configuration:
 * decode (one token per request): lora_bgmv, every token gathering its own adapter
   through the page table, shrink + scale + expand in place in y, one kernel;
 * mixed13b (the headline, the largest configuration that fits one GPU): one forward of
-  the 13B-shaped mixed batch, one segment build and 40 layers x 7 projections.
+  the 13B-shaped mixed batch, one segment build and 40 layers x 7 projections, in four
+  grouped calls per layer (lora_apply_multi for q, k, v on their shared input and for
+  gate, up on theirs; lora_apply for o and down).
 
 By default the printed JSON line is the 13B forward, with every other configuration
 timed in the same process under "per_config" (each with its own roofline, CPU
@@ -53,7 +55,8 @@ WORKLOAD_TEXT = {
     "mixed13b": "13B-shaped mixed batch: 4 prefill requests of 1024 tokens + 128 decode tokens, "
                 "d=5120, 40 layers x (q,k,v,o 5120->5120, gate,up 5120->13824, down 13824->5120), "
                 "1000 adapters r in {16,32,64} Zipf(1.1)-popular, referenced ones resident in "
-                "paged pools; a step is one forward: 280 lora_apply calls on one segment build",
+                "paged pools; a step is one forward: one segment build and 40 layers x 4 grouped "
+                "calls ([q,k,v] on one x, [o], [gate,up] on one x, [down]) = 280 projections",
     "tiny": "tiny SGMV: d=256, 4 adapters rank 8, 16 tokens in segments [3,5,1,7]",
 }
 
@@ -253,16 +256,17 @@ def device_pool(B, torch, dev, rng, ranks, d_in, d_out, page_elems=4096, alpha=1
     return B.PoolView(pool, pl, dsc, P, 64, d_in, d_out), _Shape(ranks, d_in, d_out)
 
 
-def algorithmic_bytes(batch, pool) -> int:
+def algorithmic_bytes(batch, pool, x_read: bool = True) -> int:
     """Bytes the fused apply must move at least once: every distinct adapter used (A and B
-    at its own rank, no padding), x read, y read and written (bf16)."""
+    at its own rank, no padding), x read (unless another projection of the same grouped
+    call already counts it), y read and written (bf16)."""
     ids = batch.ids
     valid = ids >= 0
     distinct = np.unique(ids[valid])
     ranks = pool.ranks[distinct].astype(np.int64)
     adapters = int((ranks * (pool.d_in + pool.d_out)).sum()) * 2
     n = int(valid.sum())
-    return adapters + n * pool.d_in * 2 + n * pool.d_out * 2 * 2
+    return adapters + (n * pool.d_in * 2 if x_read else 0) + n * pool.d_out * 2 * 2
 
 
 def algorithmic_flops(batch, pool) -> int:
@@ -283,9 +287,10 @@ def build_sets(name, rank, dev, l2, torch, B):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
     if name == "mixed13b":
-        # One forward of 40 layers x 7 projections; adapters and activations drawn on the
-        # device (about 20 GB of adapter pages and 33 GB of activations, so nothing stays
-        # in L2 between calls).
+        # One forward of 40 layers x 7 projections in 4 grouped calls per layer (q, k, v share
+        # their input, as gate and up do); adapters and activations drawn on the device
+        # (about 20 GB of adapter pages and 25 GB of activations, so nothing stays in L2
+        # between calls).
         rng = np.random.default_rng(1000 * rank)
         ranks = W.mixed13b_ranks(rng)
         ids = W.mixed13b_ids(rng)
@@ -293,19 +298,28 @@ def build_sets(name, rank, dev, l2, torch, B):
         used = np.unique(ids)
         resident[used] = ranks[used]
         T = len(ids)
+        proj = {p[0]: (i, p[1], p[2]) for i, p in enumerate(W.PROJ_13B)}
         calls = []
         for layer in range(40):
-            for pi, (pname, d_in, d_out) in enumerate(W.PROJ_13B):
-                prng = np.random.default_rng([1000 * rank, 1 + layer, 1 + pi])
-                view, shape = device_pool(B, torch, dev, prng, resident, d_in, d_out)
+            for group in (("q", "k", "v"), ("o",), ("gate", "up"), ("down",)):
+                d_in = proj[group[0]][1]
                 x = torch.randn(T, d_in, device=dev).to(torch.bfloat16)
-                y = torch.randn(T, d_out, device=dev).to(torch.bfloat16)
-                bt = W.Batch(x=None, y0=None, ids=ids, d_in=d_in, d_out=d_out)
-                calls.append(dict(view=view, x=x, y=y, bytes=algorithmic_bytes(bt, shape),
-                                  flops=algorithmic_flops(bt, shape), layer=layer, name=pname))
+                views, ys, nbytes, nflops = [], [], 0, 0
+                for k, pname in enumerate(group):
+                    pi, _, d_out = proj[pname]
+                    prng = np.random.default_rng([1000 * rank, 1 + layer, 1 + pi])
+                    view, shape = device_pool(B, torch, dev, prng, resident, d_in, d_out)
+                    bt = W.Batch(x=None, y0=None, ids=ids, d_in=d_in, d_out=d_out)
+                    views.append(view)
+                    ys.append(torch.randn(T, d_out, device=dev).to(torch.bfloat16))
+                    nbytes += algorithmic_bytes(bt, shape, x_read=k == 0)
+                    nflops += algorithmic_flops(bt, shape)
+                calls.append(dict(views=views, x=x, ys=ys, bytes=nbytes, flops=nflops, layer=layer,
+                                  name="+".join(group)))
         S = dict(calls=calls, ids=torch.from_numpy(ids).to(dev), seg=B.Segments(T, device=dev),
                  T=int((ids >= 0).sum()), host_ids=ids, wl=None, mode=0, n_ad=1000)
-        set_bytes = sum(c["view"].pool.numel() * 2 + c["x"].numel() * 2 + c["y"].numel() * 2 for c in calls)
+        set_bytes = sum(sum(v.pool.numel() * 2 for v in c["views"]) + c["x"].numel() * 2 +
+                        sum(y.numel() * 2 for y in c["ys"]) for c in calls)
         return [S], set_bytes
 
     wl0 = make_workload(name, 1000 * rank)
@@ -317,7 +331,7 @@ def build_sets(name, rank, dev, l2, torch, B):
         wl = wl0 if s == 0 else make_workload(name, seed)
         calls = []
         for pool, b in host_calls(wl, seed):
-            calls.append(dict(view=B.PoolView.from_host(pool, device=dev), x=up(b.x), y=up(b.y0),
+            calls.append(dict(views=[B.PoolView.from_host(pool, device=dev)], x=up(b.x), ys=[up(b.y0)],
                               bytes=algorithmic_bytes(b, pool), flops=algorithmic_flops(b, pool),
                               hx=b.x, hy0=b.y0))
         sets.append(dict(calls=calls, ids=torch.from_numpy(wl.batch.ids).to(dev),
@@ -354,12 +368,17 @@ def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, loca
 
     bgmv = name == "decode"
 
+    def run_call(c, ids, seg):
+        if bgmv:
+            B.lora_bgmv(c["x"], c["ys"][0], ids, c["views"][0], err=err)
+        elif len(c["views"]) == 1:
+            B.lora_apply(c["x"], c["ys"][0], seg, c["views"][0], err=err)
+        else:
+            B.lora_apply_multi(list(zip([c["x"]] * len(c["ys"]), c["ys"], c["views"])), seg, err=err)
+
     def calls_of(S):
         for c in S["calls"]:
-            if bgmv:
-                B.lora_bgmv(c["x"], c["y"], S["ids"], c["view"], err=err)
-            else:
-                B.lora_apply(c["x"], c["y"], S["seg"], c["view"], err=err)
+            run_call(c, S["ids"], S["seg"])
 
     def step(k):
         S = sets[k % n_sets]
@@ -488,7 +507,7 @@ def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, loca
     else:
         ins = S0["calls"]
         outs_extra = []
-    pieces = [c["x"] for c in ins] + [c["y"] for c in ins]
+    pieces = [c["x"] for c in ins] + [y for c in ins for y in c["ys"]]
     offs, cur = [], 0
     for t in pieces:
         offs.append(cur)
@@ -502,13 +521,16 @@ def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, loca
     hstage[ids_off:ids_off + S0["ids"].numel() * 4].copy_(S0["ids"].view(torch.uint8).cpu())
     views = [dstage[o:o + t.numel() * 2].view(torch.bfloat16).view(t.shape) for t, o in zip(pieces, offs)]
     n_in = len(ins)
-    e_calls = [dict(c, x=views[i], y=views[n_in + i]) for i, c in enumerate(ins)]
+    e_calls, k = [], n_in
+    for i, c in enumerate(ins):
+        e_calls.append(dict(c, x=views[i], ys=views[k:k + len(c["ys"])]))
+        k += len(c["ys"])
     if name == "mixed13b":
         e_calls = e_calls + [c for c in S0["calls"] if c["layer"] != 0]
     e_ids = dstage[ids_off:ids_off + S0["ids"].numel() * 4].view(torch.int32)
     y_lo, y_hi = offs[n_in], offs[-1] + pieces[-1].numel() * 2  # the staged y, contiguous
     hy = torch.empty(y_hi - y_lo, dtype=torch.uint8).pin_memory()
-    hout = [(c["y"], torch.empty(c["y"].shape, dtype=torch.bfloat16).pin_memory()) for c in outs_extra]
+    hout = [(y, torch.empty(y.shape, dtype=torch.bfloat16).pin_memory()) for c in outs_extra for y in c["ys"]]
     e_seg = S0["seg"]
     e2e_steps = max(1, min(e2e_steps, steps))
 
@@ -517,10 +539,7 @@ def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, loca
         if not bgmv:
             B.lora_segments_build(e_ids, n_ad, e_seg, mode=mode, err=err)
         for c in e_calls:
-            if bgmv:
-                B.lora_bgmv(c["x"], c["y"], e_ids, c["view"], err=err)
-            else:
-                B.lora_apply(c["x"], c["y"], e_seg, c["view"], err=err)
+            run_call(c, e_ids, e_seg)
         if outs_extra:
             for d, h in hout:
                 h.copy_(d, non_blocking=True)
@@ -540,8 +559,10 @@ def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, loca
     h2d = cur
     d2h = sum(h.numel() * 2 for _, h in hout) if outs_extra else y_hi - y_lo
 
-    call = "lora_bgmv" if bgmv else "lora_apply"
+    grouped = any(len(c["views"]) > 1 for c in sets[0]["calls"])
+    call = "lora_bgmv" if bgmv else ("lora_apply / lora_apply_multi" if grouped else "lora_apply")
     kernels = "gather_kernel" if bgmv else ", ".join(B.apply_kernel_names())
+    n_proj = sum(len(c["views"]) for c in sets[0]["calls"])
     out = {
         "value": value,
         "unit": UNIT,
@@ -552,7 +573,9 @@ def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, loca
             "workload": WORKLOAD_TEXT[name],
             "tokens_per_step": tokens_per_step,
             "segments": "none (one token per request)" if bgmv else ("GROUP" if mode == 0 else "CONTIGUOUS"),
-            "step": ("%d x lora_bgmv" if bgmv else "lora_segments_build + %d x lora_apply") % n_calls,
+            "step": ("%d x lora_bgmv" % n_calls) if bgmv else
+                    ("lora_segments_build + %d grouped calls over %d projections" % (n_calls, n_proj) if grouped
+                     else "lora_segments_build + %d x lora_apply" % n_calls),
             "l2": "inputs larger than L2: %d rotating input sets (%.0f MB in all, L2 %.0f MB)"
                   % (n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
             "timing": "CUDA graph of %d steps replayed; CUDA events on the launching stream" % g_steps,

@@ -322,7 +322,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   // units of one projection (a segment's group of tokens, or a token), times the projections
   const int n_base = a.src == kSrcTokens ? a.T : a.meta[2] + (a.short_only ? 0 : a.meta[3]);
   const int n_units = n_base * G;
-  const int n_dyn = max(0, n_units - (int)ncl);  // units claimed from the counter
+  const int ncl_eff = (int)ncl;  // clusters that take part
+  const int n_dyn = max(0, n_units - ncl_eff);  // units claimed from the counter
   // Order of the claimed units: largest first.  A unit's time grows with its
   // adapter's row blocks, and a cluster that draws a large unit last keeps the
   // call waiting; so CTA 0's consumer warps, idle until the first chunk lands,
@@ -377,11 +378,11 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       uint32_t mm = m;  // the (n - pre)-th set bit of the owner's mask
       for (int j = 0; j < n - pre && j < 32; ++j) mm &= mm - 1;
       const int bit = __ffs(mm) - 1;
-      return (int)ncl + 32 * owner + __shfl_sync(0xffffffffu, bit, owner);
+      return ncl_eff + 32 * owner + __shfl_sync(0xffffffffu, bit, owner);
     };
     auto next_unit = [&]() {
       if (!dynamic) {
-        u += (int)ncl;
+        u += ncl_eff;
         return;
       }
       const int q = nclaim & 1;
@@ -392,14 +393,14 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
           if (nclaim >= 2 && !mbar_wait_cluster(smem_u32(&claim_empty[q]), ((nclaim >> 1) - 1) & 1)) ok = false;
           claim = atomicAdd(a.counter, 1);
           if (claim < n_dyn) {
-            nu = (int)ncl + claim;
+            nu = ncl_eff + claim;
           } else {
             nu = n_units;
             over = true;
           }
         }
         nu = __shfl_sync(0xffffffffu, nu, 0);
-        if (ordered && nu < n_units) nu = ordered_unit(nu - (int)ncl);
+        if (ordered && nu < n_units) nu = ordered_unit(nu - ncl_eff);
         __syncwarp();  // lane 0 saw every CTA done with this slot before any lane rewrites it
         // lane p hands the claim to CTA p
         if (lane < (int)ncta) {
@@ -516,7 +517,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
     if (dynamic && crank == 0 && lane == 0) {
       if (!over) claim = atomicAdd(a.counter, 1);  // no unit was claimed (cid >= n_units)
       // `claim` holds this cluster's over-claim now; the last of all resets the counter
-      if (claim == n_dyn + (int)ncl - 1) *a.counter = 0;
+      if (claim == n_dyn + ncl_eff - 1) *a.counter = 0;
     }
     {
       const uint32_t q = take_slot();
@@ -674,7 +675,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       int gk[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int i = ctid + kGConsThreads * k, uu = (int)ncl + i;
+        const int i = ctid + kGConsThreads * k, uu = ncl_eff + i;
         const int ub = uu / G;
         gk[k] = uu - ub * G;
         val[k] = i >= n_dyn ? -1 : ub < n_short ? a.short_units[ub] : a.long_units[2 * (ub - n_short)];

@@ -33,9 +33,11 @@
 // the shrink, y0 for the expand) when the tile's tokens are consecutive, else
 // 16-byte asynchronous copies of each token row, plus the adapter's rows of
 // that stage (16-byte copies through the page table, zero past the rank).
-// Warp 5 issues the MMAs.  Warps 6-9 run the epilogues: the shrink partial out
-// of tensor memory and its exchange, the owner's reduction, and per expand
-// stage y = y0 + accumulator stored to global memory.
+// Warp 5 issues the MMAs.  Warps 6-13 run the epilogues in two groups of four
+// (one warp per tensor-memory lane quarter): group 0 takes the shrink partial out
+// of tensor memory, exchanges it and runs the owner's reduction; the two groups
+// take alternate expand stages (each with its own accumulator), y = y0 +
+// accumulator written back into the stage and stored by one TMA copy per warp.
 #include <cudaTypedefs.h>
 
 #include <cstring>
@@ -45,7 +47,8 @@
 
 namespace lora {
 
-constexpr int kFThreads = 320;
+constexpr int kFThreads = 448;
+constexpr int kFEpiGroups = 2;
 constexpr int kFWarpLoad0 = 1, kFLoad = 4, kFWarpMma = 5, kFWarpEpi0 = 6;
 constexpr int kFLoadThreads = 32 * kFLoad;
 constexpr int kFStages = 6;
@@ -61,8 +64,9 @@ constexpr size_t kFOffH = (size_t)kFStages * kFStageBytes;
 constexpr size_t kFOffRecv = kFOffH + kFHBytes;
 constexpr size_t kFOffSlot = kFOffRecv + kFRecvBytes;
 constexpr size_t kFOffBars = kFOffSlot + (size_t)kFSlots * kFSlotBytes;
-constexpr int kFNBars = 2 * kFStages + 2 * kFSlots + 4 + 4 + 2 + 1;
-constexpr size_t kFusedSmem = kFOffBars + kFNBars * 8 + 16 + 4 * kFStages + 1024;  // + tensor-memory slot, release counters, alignment slack
+constexpr int kFNBars = 2 * kFStages + 3 * kFSlots + 4 + 4 + 2 + 1 + 2 + 2;
+// + tensor-memory slot, release counters, claim mailbox, alignment slack
+constexpr size_t kFusedSmem = kFOffBars + kFNBars * 8 + 16 + 4 * kFStages + 16 + 1024;
 
 constexpr int kFRecEnd = 1, kFRecTma = 2;
 
@@ -81,14 +85,15 @@ struct FUnit {  // scheduler -> loaders, MMA warp, epilogue
 static_assert(sizeof(FUnit) <= 128, "unit record slot");
 
 struct FProj {
-  CUtensorMap xmap;  // x as [T rows, d_in columns], 64 x 128 boxes, 128-byte swizzle
-  CUtensorMap ymap;  // y (y0) as [T rows, d_out columns], the same boxes
+  CUtensorMap xmap;    // x as [T rows, d_in columns], 64 x 128 boxes, 128-byte swizzle
+  CUtensorMap ymap;    // y (y0) as [T rows, d_out columns], the same boxes
+  CUtensorMap ystore;  // y as [T rows, d_out columns], 64 x 32 boxes (one epilogue warp's rows)
   const uint16_t* x;
   uint16_t* y;
   float* yf;  // non-null: fp32 output rows (y is then read only, for y0)
   long long ldx, ldy, ldyf;
   DevView v;
-  int tma;  // both maps valid
+  int tma;  // every map valid
 };
 
 struct FusedArgs {
@@ -98,6 +103,7 @@ struct FusedArgs {
   const int32_t* seg_adapter;
   const int32_t* long_units;
   const int32_t* meta;
+  int32_t* counter;  // unit claims; zero between calls (the last claim of a launch puts it back)
   int32_t* err;
   int n_proj;
   int klen;          // columns per d_in slice (a multiple of 64)
@@ -115,20 +121,30 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
   uint64_t* full = bars;                       // [stages] lead's expect_tx + 128 loader threads' copies
   uint64_t* empty = bars + kFStages;           // [stages] MMA commit (shrink) or the epilogue (expand)
   uint64_t* slot_full = bars + 2 * kFStages;   // [slots] 32 scheduler lanes
-  uint64_t* slot_empty = slot_full + kFSlots;  // [slots] 4 loader + 1 MMA + 4 epilogue warps
+  uint64_t* slot_empty = slot_full + kFSlots;  // [slots] 4 loader + 1 MMA + 8 epilogue warps
   uint64_t* accs_full = slot_empty + kFSlots;  // [2] MMA commit: a unit's shrink partial
   uint64_t* accs_empty = accs_full + 2;        // [2] 4 epilogue warps
   uint64_t* acce_full = accs_empty + 2;        // [2] MMA commit: one expand stage
-  uint64_t* acce_empty = acce_full + 2;        // [2] 4 epilogue warps
+  uint64_t* acce_empty = acce_full + 2;        // [2] the 4 warps of epilogue group b
   uint64_t* recv_full = acce_empty + 2;        // this CTA's rows of every CTA's partial (bytes)
   uint64_t* h_full = recv_full + 1;            // the whole H operand (bytes)
   uint64_t* mma_done = h_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* slot_taken = mma_done + 1;         // [slots] the loaders have read the unit's record
+  uint64_t* claim_full = slot_taken + kFSlots;  // [2] CTA 0's scheduler posted a claimed unit here
+  uint64_t* claim_empty = claim_full + 2;       // [2] (CTA 0 only) every CTA has read the claim
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(claim_empty + 2);
   int* rel_cnt = reinterpret_cast<int*>(tmem_slot + 4);  // [stages] epilogue warps done with an expand stage
+  int* claim_val = rel_cnt + kFStages;                    // [2]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t crank = cluster_ctarank(), ncta = cluster_nctarank();
   const uint32_t cid = cluster_id_x(), ncl = ncluster_x();
+  if (a.after_gather == 0) pdl_enter(false);  // otherwise the segments are complete already (see pdl_enter)
+  if (a.meta[3] == 0) {  // no long tile: every CTA of every cluster leaves at once
+    if (a.after_gather != 0) pdl_enter(true);
+    pdl_exit(a.after_gather != 0);
+    return;
+  }
   if (tid == 0) {
     for (int s = 0; s < kFStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1 + kFLoadThreads);
@@ -136,7 +152,12 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
     }
     for (int q = 0; q < kFSlots; ++q) {
       mbar_init(smem_u32(&slot_full[q]), 32);
-      mbar_init(smem_u32(&slot_empty[q]), kFLoad + 1 + 4);
+      mbar_init(smem_u32(&slot_empty[q]), kFLoad + 1 + 4 * kFEpiGroups);
+      mbar_init(smem_u32(&slot_taken[q]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&claim_full[b]), 1);
+      mbar_init(smem_u32(&claim_empty[b]), ncta);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&accs_full[b]), 1);
@@ -157,15 +178,61 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // shrink partials at columns 0 / 64, expand accumulators at 128 / 192
-  pdl_enter(a.after_gather != 0);
+  if (a.after_gather != 0) pdl_enter(true);
   bool ok = true;
   const int R = kTM / (int)ncta;  // rows each CTA owns in the exchange
 
   if (warp == 0) {
     // ---------------- scheduler ----------------
+    // Units: cluster cid takes unit cid first, then the units CTA 0 claims from
+    // the counter (n_clusters + claim) and hands to every CTA of the cluster, so
+    // clusters that start late, or draw small tiles, take more.  The next unit
+    // is claimed once the loaders have taken the previous one, so that when the
+    // units run out no cluster holds more than one in reserve.  Every cluster
+    // over-claims the counter exactly once; the last claim of all puts it back
+    // to zero for the next call.
     const int n_units = a.meta[3] * a.n_proj;
+    const int n_dyn = max(0, n_units - (int)ncl);
+    int claim = 0;      // CTA 0, lane 0: the counter's last answer
+    bool over = false;  // CTA 0, lane 0: this cluster's over-claim is made
+    uint32_t nclaim = 0;
+    auto next_unit = [&]() -> int {
+      const uint32_t qc = nclaim & 1;
+      if (crank == 0) {
+        int nu = 0;
+        if (lane == 0) {
+          if (nclaim >= 2 && !mbar_wait_cluster(smem_u32(&claim_empty[qc]), ((nclaim >> 1) - 1) & 1)) ok = false;
+          claim = atomicAdd(a.counter, 1);
+          if (claim < n_dyn) {
+            nu = (int)ncl + claim;
+          } else {
+            nu = n_units;
+            over = true;
+          }
+        }
+        nu = __shfl_sync(0xffffffffu, nu, 0);
+        __syncwarp();  // lane 0 saw every CTA done with this mailbox before any lane rewrites it
+        if (lane < (int)ncta) {  // lane p hands the claim to CTA p
+          st_dsmem_u32(mapa(smem_u32(&claim_val[qc]), (uint32_t)lane), (uint32_t)nu);
+          mbar_arrive_cluster(mapa(smem_u32(&claim_full[qc]), (uint32_t)lane));
+        }
+      }
+      if (!mbar_wait_cluster(smem_u32(&claim_full[qc]), (nclaim >> 1) & 1)) ok = false;
+      const int v = claim_val[qc];
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa(smem_u32(&claim_empty[qc]), 0));
+      ++nclaim;
+      return v;
+    };
     uint32_t np = 0;  // records posted
-    for (int u = (int)cid;; u += (int)ncl) {
+    for (int u = (int)cid, k = 0;; ++k) {
+      if (k > 0) {
+        // the loaders have taken the last record posted before the next claim
+        if (np > 0 && !mbar_wait(smem_u32(&slot_taken[(np - 1) % kFSlots]), ((np - 1) / kFSlots) & 1)) ok = false;
+        if (!__all_sync(0xffffffffu, ok)) break;
+        u = next_unit();
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
       const bool end = u >= n_units;
       int g = 0;
       TileInfo ti{};
@@ -250,6 +317,11 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
       mbar_arrive(smem_u32(&slot_full[q]));  // each lane after its own writes
       ++np;
     }
+    if (crank == 0 && lane == 0) {
+      if (!over) claim = atomicAdd(a.counter, 1);  // no unit was claimed (cid >= n_units, or a wait ran out)
+      // `claim` holds this cluster's over-claim now; the last of all resets the counter
+      if (claim == n_dyn + (int)ncl - 1) *a.counter = 0;
+    }
     if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
   } else if (warp < kFWarpMma) {
     // ---------------- loaders ----------------
@@ -275,6 +347,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
       const uint8_t* slot = slot_at(q);
       const FUnit U = *reinterpret_cast<const FUnit*>(slot);
       if (U.flags & kFRecEnd) break;
+      if (lead) mbar_arrive(smem_u32(&slot_taken[q]));
       const FProj& P = a.proj[U.g];
       const DevView& v = P.v;
       const bool tma = U.flags & kFRecTma;
@@ -436,16 +509,34 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
     __syncwarp();
   } else {
     // ---------------- epilogue ----------------
-    const int quarter = warp & 3;  // tensor-memory lanes this warp may read
-    const int m = quarter * 32 + lane;  // tile row
-    const int et = tid - 32 * kFWarpEpi0;  // 0..127
+    const int grp = (warp - kFWarpEpi0) >> 2;  // group: 0 also runs the exchange
+    const int quarter = warp & 3;              // tensor-memory lanes this warp may read
+    const int m = quarter * 32 + lane;         // tile row
+    const int et = tid - 32 * (kFWarpEpi0 + 4 * grp);  // 0..127 within the group
     uint32_t gs = 0, ne = 0;
     // Every wait is followed by a warp vote, so a warp stops as a whole when one
-    // of its lanes' waits ran out; the four epilogue warps meet at no blocking
-    // barrier (an expand stage is released by whichever of them is last).
+    // of its lanes' waits ran out; the epilogue warps meet at no blocking barrier
+    // (an expand stage is released by whichever of its group's warps is last).
     auto waited = [&](bool w) {
       if (!__all_sync(0xffffffffu, w)) ok = false;
       return ok;
+    };
+    // A warp's stage whose TMA store may still be reading it: released once the
+    // warp has issued its next store (or at the end of the unit).
+    int pending = -1;
+    auto release = [&](int st) {  // lane 0: this warp is done with stage st
+      __threadfence_block();
+      if (atomicAdd(&rel_cnt[st], 1) == 3) {
+        rel_cnt[st] = 0;
+        mbar_arrive(smem_u32(&empty[st]));
+      }
+    };
+    auto flush = [&]() {  // lane 0
+      if (pending >= 0) {
+        bulk_wait_read0();
+        release(pending);
+        pending = -1;
+      }
     };
     for (uint32_t np = 0; ok; ++np) {
       const uint32_t q = np % kFSlots;
@@ -456,40 +547,40 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
       const FProj& P = a.proj[U.g];
       const int tok_m = reinterpret_cast<const int*>(slot + 128)[m];
       const int rpad = U.rpad;
-      // -- shrink partial: row m out of tensor memory, to the owner of row m
-      const uint32_t ub = np & 1;
-      if (!waited(mbar_wait(smem_u32(&accs_full[ub]), (np >> 1) & 1))) break;
-      // This unit's exchange: the bytes of the partial rows this CTA owns, and of
-      // the H operand.  Armed only now: the MMA warp has waited for the previous
-      // unit's H before committing this unit's partial, so that phase is over.
-      if (et == 0) {
-        mbar_arrive_expect_tx(smem_u32(recv_full), (uint32_t)(ncta * R * rpad * 4));
-        mbar_arrive_expect_tx(smem_u32(h_full), (uint32_t)(kTM * rpad * 4));
-      }
-      tc_fence_after();
-      uint32_t pr[64];
-      const uint32_t taddr = tmem + ub * 64 + ((uint32_t)(quarter * 32) << 16);
-      tmem_ld32_nowait(taddr, pr);
-      tmem_ld32_nowait(taddr + 32, pr + 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&accs_empty[ub]));
-      {
-        const uint32_t owner = (uint32_t)(m / R);
-        const uint32_t dst = smem_u32(recv + ((size_t)crank * R + (m - (int)owner * R)) * LORA_MAX_RANK);
-        const uint32_t rbar = mapa(smem_u32(recv_full), owner);
+      if (grp == 0) {
+        // -- shrink partial: row m out of tensor memory, to the owner of row m
+        const uint32_t ub = np & 1;
+        if (!waited(mbar_wait(smem_u32(&accs_full[ub]), (np >> 1) & 1))) break;
+        // This unit's exchange: the bytes of the partial rows this CTA owns, and of
+        // the H operand.  Armed only now: the MMA warp has waited for the previous
+        // unit's H before committing this unit's partial, so that phase is over.
+        if (et == 0) {
+          mbar_arrive_expect_tx(smem_u32(recv_full), (uint32_t)(ncta * R * rpad * 4));
+          mbar_arrive_expect_tx(smem_u32(h_full), (uint32_t)(kTM * rpad * 4));
+        }
+        tc_fence_after();
+        uint32_t pr[64];
+        const uint32_t taddr = tmem + ub * 64 + ((uint32_t)(quarter * 32) << 16);
+        tmem_ld32_nowait(taddr, pr);
+        tmem_ld32_nowait(taddr + 32, pr + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&accs_empty[ub]));
+        {
+          const uint32_t owner = (uint32_t)(m / R);
+          const uint32_t dst = smem_u32(recv + ((size_t)crank * R + (m - (int)owner * R)) * LORA_MAX_RANK);
+          const uint32_t rbar = mapa(smem_u32(recv_full), owner);
 #pragma unroll
-        for (int j = 0; j < LORA_MAX_RANK; j += 4)
-          if (j < rpad)
-            st_async_v4(mapa(dst + 4 * j, owner),
-                        make_float4(__uint_as_float(pr[j]), __uint_as_float(pr[j + 1]), __uint_as_float(pr[j + 2]),
-                                    __uint_as_float(pr[j + 3])),
-                        rbar);
-      }
-      // -- owner: sum the partials of its rows in CTA order, scale, split, send H rows to every CTA
-      if (!waited(mbar_wait(smem_u32(recv_full), np & 1))) break;
-      {
+          for (int j = 0; j < LORA_MAX_RANK; j += 4)
+            if (j < rpad)
+              st_async_v4(mapa(dst + 4 * j, owner),
+                          make_float4(__uint_as_float(pr[j]), __uint_as_float(pr[j + 1]),
+                                      __uint_as_float(pr[j + 2]), __uint_as_float(pr[j + 3])),
+                          rbar);
+        }
+        // -- owner: sum the partials of its rows in CTA order, scale, split, send H rows to every CTA
+        if (!waited(mbar_wait(smem_u32(recv_full), np & 1))) break;
         const int ng = rpad / 8;  // 8-column groups of a row
         for (int gi = et; gi < R * ng; gi += 128) {
           const int rr = gi / ng, cg = gi - rr * ng;
@@ -528,11 +619,12 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
           }
         }
       }
-      // -- expand stages: y = y0 + accumulator, stored to global memory
+      // -- expand stages of this group: y = y0 + accumulator
       gs += (uint32_t)U.nk;
       for (int nc = 0; nc < U.nn; ++nc, ++gs, ++ne) {
-        const uint32_t st = gs % kFStages;
         const uint32_t eb = ne & 1;
+        if ((int)eb != grp) continue;  // the other group's stage
+        const uint32_t st = gs % kFStages;
         if (!waited(mbar_wait(smem_u32(&full[st]), (gs / kFStages) & 1) &&
                     mbar_wait(smem_u32(&acce_full[eb]), (ne >> 1) & 1)))
           break;
@@ -545,49 +637,81 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&acce_empty[eb]));
-        const uint8_t* act = stage_at(st);
-        if (ok && m < U.cnt) {
-          const int ncol = U.n0 + 64 * nc;
-          if (P.yf != nullptr) {  // fp32 output (diagnostic form): the same sums, not rounded to bf16
-            float* frow = P.yf + (long long)tok_m * P.ldyf + ncol;
+        uint8_t* act = stage_at(st);
+        const int ncol = U.n0 + 64 * nc;
+        // a warp whose 32 rows are all in a tile of consecutive tokens stores them
+        // with one TMA copy from the stage (the result overwrites the row's y0 there)
+        const bool wstore = (U.flags & kFRecTma) && P.yf == nullptr && quarter * 32 + 31 < U.cnt;
+        if (wstore) {
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-              float y0[8];
-              unpack8(*reinterpret_cast<const uint4*>(act + sw128_offset(m, cc)), y0);
-              float4* o4 = reinterpret_cast<float4*>(frow + 8 * cc);
-              o4[0] = make_float4(y0[0] + __uint_as_float(acc[8 * cc]), y0[1] + __uint_as_float(acc[8 * cc + 1]),
-                                  y0[2] + __uint_as_float(acc[8 * cc + 2]), y0[3] + __uint_as_float(acc[8 * cc + 3]));
-              o4[1] = make_float4(y0[4] + __uint_as_float(acc[8 * cc + 4]), y0[5] + __uint_as_float(acc[8 * cc + 5]),
-                                  y0[6] + __uint_as_float(acc[8 * cc + 6]), y0[7] + __uint_as_float(acc[8 * cc + 7]));
+          for (int cc = 0; cc < 8; ++cc) {
+            uint4* qp = reinterpret_cast<uint4*>(act + sw128_offset(m, cc));
+            float y0[8];
+            unpack8(*qp, y0);
+            uint4 o;
+            o.x = pack_bf16x2(y0[0] + __uint_as_float(acc[8 * cc]), y0[1] + __uint_as_float(acc[8 * cc + 1]));
+            o.y = pack_bf16x2(y0[2] + __uint_as_float(acc[8 * cc + 2]), y0[3] + __uint_as_float(acc[8 * cc + 3]));
+            o.z = pack_bf16x2(y0[4] + __uint_as_float(acc[8 * cc + 4]), y0[5] + __uint_as_float(acc[8 * cc + 5]));
+            o.w = pack_bf16x2(y0[6] + __uint_as_float(acc[8 * cc + 6]), y0[7] + __uint_as_float(acc[8 * cc + 7]));
+            *qp = o;
+          }
+          fence_proxy_async_smem();  // the rows, written here, before the TMA engine reads them
+          __syncwarp();
+          if (lane == 0) {
+            if (ok) {
+              tma_store_2d(&P.ystore, ncol, U.row0 + quarter * 32, smem_u32(act) + (uint32_t)(quarter * 32 * 128));
+              bulk_commit();
             }
-          } else {
-            uint4* yrow = reinterpret_cast<uint4*>(P.y + (long long)tok_m * P.ldy + ncol);
+            // the previous store has read its stage once at most this one is pending
+            if (pending >= 0) {
+              asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+              release(pending);
+            }
+            pending = (int)st;
+          }
+        } else {
+          if (ok && m < U.cnt) {
+            if (P.yf != nullptr) {  // fp32 output (diagnostic form): the same sums, not rounded to bf16
+              float* frow = P.yf + (long long)tok_m * P.ldyf + ncol;
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-              float y0[8];
-              unpack8(*reinterpret_cast<const uint4*>(act + sw128_offset(m, cc)), y0);
-              uint4 o;
-              o.x = pack_bf16x2(y0[0] + __uint_as_float(acc[8 * cc]), y0[1] + __uint_as_float(acc[8 * cc + 1]));
-              o.y = pack_bf16x2(y0[2] + __uint_as_float(acc[8 * cc + 2]), y0[3] + __uint_as_float(acc[8 * cc + 3]));
-              o.z = pack_bf16x2(y0[4] + __uint_as_float(acc[8 * cc + 4]), y0[5] + __uint_as_float(acc[8 * cc + 5]));
-              o.w = pack_bf16x2(y0[6] + __uint_as_float(acc[8 * cc + 6]), y0[7] + __uint_as_float(acc[8 * cc + 7]));
-              yrow[cc] = o;
+              for (int cc = 0; cc < 8; ++cc) {
+                float y0[8];
+                unpack8(*reinterpret_cast<const uint4*>(act + sw128_offset(m, cc)), y0);
+                float4* o4 = reinterpret_cast<float4*>(frow + 8 * cc);
+                o4[0] = make_float4(y0[0] + __uint_as_float(acc[8 * cc]), y0[1] + __uint_as_float(acc[8 * cc + 1]),
+                                    y0[2] + __uint_as_float(acc[8 * cc + 2]), y0[3] + __uint_as_float(acc[8 * cc + 3]));
+                o4[1] = make_float4(y0[4] + __uint_as_float(acc[8 * cc + 4]), y0[5] + __uint_as_float(acc[8 * cc + 5]),
+                                    y0[6] + __uint_as_float(acc[8 * cc + 6]), y0[7] + __uint_as_float(acc[8 * cc + 7]));
+              }
+            } else {
+              uint4* yrow = reinterpret_cast<uint4*>(P.y + (long long)tok_m * P.ldy + ncol);
+#pragma unroll
+              for (int cc = 0; cc < 8; ++cc) {
+                float y0[8];
+                unpack8(*reinterpret_cast<const uint4*>(act + sw128_offset(m, cc)), y0);
+                uint4 o;
+                o.x = pack_bf16x2(y0[0] + __uint_as_float(acc[8 * cc]), y0[1] + __uint_as_float(acc[8 * cc + 1]));
+                o.y = pack_bf16x2(y0[2] + __uint_as_float(acc[8 * cc + 2]), y0[3] + __uint_as_float(acc[8 * cc + 3]));
+                o.z = pack_bf16x2(y0[4] + __uint_as_float(acc[8 * cc + 4]), y0[5] + __uint_as_float(acc[8 * cc + 5]));
+                o.w = pack_bf16x2(y0[6] + __uint_as_float(acc[8 * cc + 6]), y0[7] + __uint_as_float(acc[8 * cc + 7]));
+                yrow[cc] = o;
+              }
             }
           }
-        }
-        // the last of the four warps to be done with the stage's y0 releases it
-        __syncwarp();
-        if (lane == 0) {
-          __threadfence_block();
-          if (atomicAdd(&rel_cnt[st], 1) == 3) {
-            rel_cnt[st] = 0;
-            mbar_arrive(smem_u32(&empty[st]));
-          }
+          __syncwarp();
+          if (lane == 0) release((int)st);  // read its y0 rows: done with the stage
         }
       }
+      // A stage held back for its store is released before the next unit: the
+      // loaders may need it to bring in that unit's shrink stages.
+      if (lane == 0) flush();
       if (!ok) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&slot_empty[q]));
+    }
+    if (lane == 0) {
+      flush();
+      bulk_wait0();  // this warp's y stores are complete before the CTA ends
     }
     if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
   }
@@ -624,7 +748,8 @@ lora_status_t launch_fused_tc(int n_proj, const ProjCall* projs, const lora_segm
     P.ldy = h.ldy;
     P.ldyf = h.ldyf;
     P.tma = make_act_map(&P.xmap, h.x, seg->T, h.view->d_in, h.ldx, kTM) &&
-                    make_act_map(&P.ymap, h.y, seg->T, h.view->d_out, h.ldy, kTM)
+                    make_act_map(&P.ymap, h.y, seg->T, h.view->d_out, h.ldy, kTM) &&
+                    make_act_map(&P.ystore, h.y, seg->T, h.view->d_out, h.ldy, 32)
                 ? 1
                 : 0;
   }
@@ -633,6 +758,7 @@ lora_status_t launch_fused_tc(int n_proj, const ProjCall* projs, const lora_segm
   a.seg_adapter = seg->seg_adapter;
   a.long_units = seg->long_units;
   a.meta = seg->meta;
+  a.counter = seg->meta + 5;
   a.err = err;
   a.n_proj = n_proj;
   a.klen = klen;
