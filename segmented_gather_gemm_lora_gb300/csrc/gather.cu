@@ -48,9 +48,11 @@
 namespace lora {
 
 constexpr int kGCons = 8;            // consumer warps
-constexpr int kGProd = kGCons;       // the producer warp
+constexpr int kGProd = kGCons;       // the first producer warp
 constexpr int kGSched = kGCons + 1;  // the scheduler warp
-constexpr int kGThreads = 32 * (kGCons + 2);
+constexpr int kGProd2 = kGCons + 2;  // the second producer warp
+constexpr int kGProds = 2;           // producer warps: a stage's copies alternate between them
+constexpr int kGThreads = 32 * (kGCons + 3);
 constexpr int kGConsThreads = 32 * kGCons;
 constexpr int kNT = 4;  // tokens per group
 constexpr int kHMax = LORA_MAX_RANK;
@@ -58,8 +60,11 @@ constexpr int kMaxCluster = 8;
 constexpr int kSub = 512;       // columns per sub-slice (one 1 KB row)
 constexpr int kChunkRows = 16;  // adapter rows per chunk
 constexpr int kRowBytes = kSub * 2;
+// Rows of a stage sit 1040 bytes apart (1 KB plus 16): the eight rows one
+// ldmatrix reads then fall in eight different bank groups.
+constexpr int kRowStride = kRowBytes + 16;
 constexpr int kStages = 4;
-constexpr int kStageBytes = (kChunkRows + kNT) * kRowBytes;  // 20 KB
+constexpr int kStageBytes = (kChunkRows + kNT) * kRowStride;  // 20.3 KB
 constexpr int kMaxPgSlots = 512;  // page-list slots of one adapter cached in shared memory
 
 enum GKind { kGShrink = 0, kGExpand = 1, kGReduce = 2, kGEnd = 3 };
@@ -120,18 +125,6 @@ struct GUnit {
 static_assert(sizeof(GUnit) <= 64, "unit slot");
 static_assert(kSub / 64 <= kGCons, "one warp per block of 8 output vectors");
 
-constexpr size_t kOffRec = (size_t)kStages * kStageBytes;
-constexpr size_t kOffPw = kOffRec + (size_t)kStages * 64;                     // fp32 [kGCons][kNT][kHMax]
-constexpr size_t kOffRecv = kOffPw + (size_t)kGCons * kNT * kHMax * sizeof(float);  // fp32 [2][kMaxCluster][kNT][kHMax]
-constexpr size_t kOffHs = kOffRecv + 2 * (size_t)kMaxCluster * kNT * kHMax * sizeof(float);  // fp32 [kNT][kHMax]
-constexpr size_t kOffPgt = kOffHs + kNT * kHMax * sizeof(float);          // int [2][kMaxPgSlots]
-constexpr size_t kOffUnit = kOffPgt + 2 * kMaxPgSlots * sizeof(int);      // GUnit [2], 64-byte slots
-constexpr size_t kOffClaim = kOffUnit + 2 * 64;                           // int [2]
-constexpr size_t kOffCls = kOffClaim + 16;                                // uint32 [3][32] unit classes
-constexpr size_t kOffBars = kOffCls + 3 * 32 * sizeof(uint32_t);
-constexpr int kNBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1 + 1;
-constexpr size_t kGatherSmem = kOffBars + kNBars * 8;
-
 // One projection of the call: its activations and its view of the adapter pool.
 struct GProj {
   const uint16_t* x;
@@ -140,6 +133,22 @@ struct GProj {
   long long ldy;
   DevView v;
 };
+
+constexpr size_t kOffRec = (size_t)kStages * kStageBytes;
+constexpr size_t kOffPw = kOffRec + (size_t)kStages * 64;                     // fp32 [kGCons][kNT][kHMax]
+constexpr size_t kOffRecv = kOffPw + (size_t)kGCons * kNT * kHMax * sizeof(float);  // fp32 [2][kMaxCluster][kNT][kHMax]
+constexpr size_t kOffHs = kOffRecv + 2 * (size_t)kMaxCluster * kNT * kHMax * sizeof(float);  // fp32 [kNT][kHMax]
+constexpr size_t kOffPgt = kOffHs + kNT * kHMax * sizeof(float);          // int [2][kMaxPgSlots]
+constexpr size_t kOffUnit = kOffPgt + 2 * kMaxPgSlots * sizeof(int);      // GUnit [2], 64-byte slots
+constexpr size_t kOffClaim = kOffUnit + 2 * 64;                           // int [2]
+constexpr size_t kOffCls = kOffClaim + 16;                                // uint32 [3][32] unit classes
+constexpr size_t kOffProj = kOffCls + 3 * 32 * sizeof(uint32_t);        // GProj [kMaxFusedProj], 16-byte slots
+constexpr size_t kOffBars = kOffProj + kMaxFusedProj * ((sizeof(GProj) + 15) / 16 * 16);
+constexpr int kNBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1 + 1;
+constexpr size_t kGatherSmem = kOffBars + kNBars * 8;
+// two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
+static_assert(kGatherSmem <= 233472 / 2 - 1024, "two gather CTAs per SM");
+
 
 struct GatherArgs {
   GProj proj[kMaxFusedProj];
@@ -163,108 +172,142 @@ struct GatherArgs {
   int short_only;
 };
 
-// Shrink of one staged chunk for NT tokens.  Warp w owns 8-column vectors
-// 8w .. 8w + 7 of every sub-slice; lane = 2 i + half takes chunk row i and four
-// of those vectors (half 0 the first four, half 1 the last four), visiting them
-// in an order rotated by the row so that one load instruction of the warp
-// touches every bank four times.  Per chunk each vector's 8-term dot product
-// is its own chain and the four meet as (v0 + v1) + (v2 + v3); the lane's sums
-// accumulate in registers over the row block's sub-slices (in order); the two
-// halves of a row meet when the block's last sub-slice is done.
-template <int NT>
-__device__ __forceinline__ void shrink_chunk(const uint8_t* sb, int nrows, int nvec, float (&acc)[kNT], int warp,
-                                             int lane) {
-  const int i = lane >> 1;
-  if (i >= nrows) return;
-  const int v0 = warp * 8 + (lane & 1) * 4;
-  const uint4* arow = reinterpret_cast<const uint4*>(sb + i * kRowBytes);
-  const uint4* xrow = reinterpret_cast<const uint4*>(sb + kChunkRows * kRowBytes);
-  uint4 av[4];
+// ------------------------------------------------ warp-level tensor-core tiles --
+//
+// The chunk arithmetic runs on mma.sync m16n8k16 (bf16 operands, fp32
+// accumulators): one instruction is 2048 multiply-adds, where a CUDA-core loop
+// spends an instruction or more per adapter element.  Operands come from the
+// staged rows with ldmatrix.
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr) : "memory");
+}
+// d (16 x 8 fp32, row-major over lanes) += a (16 x 16 bf16) . b (16 x 8 bf16)
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Shrink of one staged chunk: D[j, t] += sum_k A_i[j0 + j, k] x[t, k] over this
+// warp's 64 columns of the sub-slice (warp w owns columns 64 w .. 64 w + 63), as
+// four k16 steps in column order.  d is the lane's part of the 16 x 8 tile:
+// rows (lane / 4, lane / 4 + 8), tokens (2 (lane % 4), 2 (lane % 4) + 1).  Rows
+// past the chunk and tokens past the group give entries nobody reads; columns
+// past the sub-slice are masked to zero in both operands.  Each entry is a fixed
+// function of its own adapter row and token row.
+__device__ __forceinline__ void shrink_chunk(uint32_t sbase, int wsub, int ntok, float (&d)[4], int warp, int lane) {
+  const int kw = warp * 64;
+  if (kw >= wsub) return;
+  const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = (lane >> 4) * 8;
+  const int xrow = min(lane & 7, ntok - 1), xcol = ((lane >> 3) & 1) * 8;
+  const uint32_t abase = sbase + (uint32_t)(arow * kRowStride + (kw + acol) * 2);
+  const uint32_t xbase = sbase + (uint32_t)((kChunkRows + xrow) * kRowStride + (kw + xcol) * 2);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int vv = v0 + ((k + i) & 3);
-    av[k] = vv < nvec ? arow[vv] : make_uint4(0u, 0u, 0u, 0u);
-  }
-#pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    float p[4];  // one partial per vector (independent chains), then a fixed combination
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int vv = v0 + ((k + i) & 3);
-      p[k] = 0.f;
-      if (vv < nvec) {
-        float af[8], xf[8];
-        unpack8(av[k], af);
-        unpack8(xrow[t * (kRowBytes / 16) + vv], xf);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) p[k] = fmaf(af[q], xf[q], p[k]);
-      }
-    }
-    acc[t] += (p[0] + p[1]) + (p[2] + p[3]);
+  for (int st = 0; st < 4; ++st) {
+    const int k0 = kw + 16 * st;
+    if (k0 >= wsub) break;
+    uint32_t a0, a1, a2, a3, b0, b1;
+    ldsm_x4(abase + 32 * st, a0, a1, a2, a3);
+    ldsm_x2(xbase + 32 * st, b0, b1);
+    if (k0 + 8 >= wsub) a2 = a3 = b1 = 0u;  // columns k0 + 8 .. k0 + 15 lie past the sub-slice
+    mma16816(d, a0, a1, a2, a3, b0, b1);
   }
 }
 
-// Expand of one staged chunk.  Lane l of warp w owns the two output columns
-// of 32-bit word 32 w + l of the sub-slice, for every token, so the sum over
-// the adapter's rows runs in the lane's registers from the sub-slice's first
-// row block to its last, with no exchange between lanes: per chunk, even and
-// odd rows in two chains (rows ascending) whose sum is added to the running
-// total.  One load instruction of the warp reads 128 contiguous bytes of a
-// row.  The sub-slice's last chunk adds y0 and writes y.
+// Expand of one staged chunk: Y[n, t] += sum_j B_i[j0 + j, n] h[t, j0 + j] over
+// the chunk's rows, for this warp's 64 columns of the sub-slice (four n16
+// tiles; acc[i] is the lane's part of tile i: columns 16 i + lane / 4 (+ 8),
+// tokens 2 (lane % 4) (+ 1)).  h enters as bf16 hi + lo parts (two MMAs per
+// tile, hi first), which keeps the intermediate at about fp32 accuracy.  Rows
+// past the chunk are masked to zero in both operands.  The sub-slice's last
+// chunk adds y0 and writes y through the warp's scratch rows.
 __device__ __forceinline__ void expand_chunk(uint16_t* ybase, long long ldy, float* yf, long long ldyf,
-                                             const uint8_t* sb, const float* hs, float (&acc)[kNT][2],
-                                             const GRec& rc, bool ok, int warp, int lane) {
-  const int m = warp * 32 + lane;
-  if (m >= rc.nvec * 4) return;
+                                             uint32_t sbase, const uint8_t* sb, const float* hs, float* scr,
+                                             float (&acc)[4][4], const GRec& rc, bool ok, int warp, int lane) {
+  const int nw = warp * 64;
+  const int wsub = rc.nvec * 8;
+  if (nw >= wsub) return;
   if (rc.flags & kFFirst) {
 #pragma unroll
-    for (int t = 0; t < kNT; ++t) acc[t][0] = acc[t][1] = 0.f;
+    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
   }
-  uint32_t bw[kChunkRows];
+  const int g = lane >> 2, t = lane & 3;
+  const int nrows = rc.nrows;
+  // h fragment of token g: rows 2t, 2t + 1 (b0) and 2t + 8, 2t + 9 (b1) of the chunk
+  uint32_t bh0 = 0u, bh1 = 0u, bl0 = 0u, bl1 = 0u;
+  if (g < rc.ntok) {
+    const float* hrow = hs + g * kHMax + rc.j0;
+    float hv[4];
 #pragma unroll
-  for (int i = 0; i < kChunkRows; ++i)
-    bw[i] = i < rc.nrows ? *reinterpret_cast<const uint32_t*>(sb + i * kRowBytes + 4 * m) : 0u;
-#pragma unroll
-  for (int t = 0; t < kNT; ++t) {
-    if (t >= rc.ntok) break;
-    const float4* h4 = reinterpret_cast<const float4*>(hs + t * kHMax + rc.j0);
-    float4 hv[kChunkRows / 4];
-#pragma unroll
-    for (int i4 = 0; i4 < kChunkRows / 4; ++i4) hv[i4] = h4[i4];  // rows past nrows are read, not used
-    // even and odd rows in separate chains, combined in a fixed order
-    float e0 = 0.f, e1 = 0.f, o0 = 0.f, o1 = 0.f;
-#pragma unroll
-    for (int i4 = 0; i4 < kChunkRows / 4; ++i4) {
-      const float he[4] = {hv[i4].x, hv[i4].y, hv[i4].z, hv[i4].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = 4 * i4 + e;
-        if (i < rc.nrows) {
-          if (e & 1) {
-            o0 = fmaf(he[e], bf_lo(bw[i]), o0);
-            o1 = fmaf(he[e], bf_hi(bw[i]), o1);
-          } else {
-            e0 = fmaf(he[e], bf_lo(bw[i]), e0);
-            e1 = fmaf(he[e], bf_hi(bw[i]), e1);
-          }
-        }
-      }
+    for (int e = 0; e < 4; ++e) {
+      const int j = 2 * t + (e & 1) + 8 * (e >> 1);
+      hv[e] = j < nrows ? hrow[j] : 0.f;
     }
-    acc[t][0] += e0 + o0;
-    acc[t][1] += e1 + o1;
+    bh0 = pack_bf16x2(hv[0], hv[1]);
+    bh1 = pack_bf16x2(hv[2], hv[3]);
+    bl0 = pack_bf16x2(hv[0] - bf_lo(bh0), hv[1] - bf_hi(bh0));
+    bl1 = pack_bf16x2(hv[2] - bf_lo(bh1), hv[3] - bf_hi(bh1));
+  }
+  // rows of the lane's A entries: 2t, 2t + 1 (a0, a1) and 2t + 8, 2t + 9 (a2, a3)
+  const uint32_t m01 = (2 * t < nrows ? 0x0000ffffu : 0u) | (2 * t + 1 < nrows ? 0xffff0000u : 0u);
+  const uint32_t m23 = (2 * t + 8 < nrows ? 0x0000ffffu : 0u) | (2 * t + 9 < nrows ? 0xffff0000u : 0u);
+  const int jrow = (lane & 7) + 8 * (lane >> 4), ncol = 8 * ((lane >> 3) & 1);
+  const uint32_t bbase = sbase + (uint32_t)(jrow * kRowStride + (nw + ncol) * 2);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (nw + 16 * i >= wsub) break;
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4_t(bbase + 32 * i, a0, a1, a2, a3);
+    a0 &= m01;
+    a1 &= m01;
+    a2 &= m23;
+    a3 &= m23;
+    mma16816(acc[i], a0, a1, a2, a3, bh0, bh1);
+    mma16816(acc[i], a0, a1, a2, a3, bl0, bl1);
   }
   if ((rc.flags & kFLast) && ok) {
+    // the lane's entries into the warp's scratch [token][64 columns], then each
+    // lane writes two adjacent columns of every token
 #pragma unroll
-    for (int t = 0; t < kNT; ++t) {
-      if (t >= rc.ntok) break;
-      const uint32_t y0 = *reinterpret_cast<const uint32_t*>(sb + (kChunkRows + t) * kRowBytes + 4 * m);
-      if (yf != nullptr)  // fp32 output (diagnostic form): the same sums, not rounded to bf16
-        *reinterpret_cast<float2*>(yf + (long long)rc.tok[t] * ldyf + rc.col0 + 2 * m) =
-            make_float2(bf_lo(y0) + acc[t][0], bf_hi(y0) + acc[t][1]);
-      else
-        *reinterpret_cast<uint32_t*>(ybase + (long long)rc.tok[t] * ldy + rc.col0 + 2 * m) =
-            pack_bf16x2(bf_lo(y0) + acc[t][0], bf_hi(y0) + acc[t][1]);
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = 2 * t + (e & 1), nn = 16 * i + g + 8 * (e >> 1);
+        if (tok < rc.ntok) scr[tok * 64 + nn] = acc[i][e];
+      }
+    __syncwarp();
+    const int c2 = nw + 2 * lane;
+    if (c2 < wsub) {
+#pragma unroll
+      for (int tk = 0; tk < kNT; ++tk) {
+        if (tk >= rc.ntok) break;
+        const uint32_t y0 = *reinterpret_cast<const uint32_t*>(sb + (kChunkRows + tk) * kRowStride + 2 * c2);
+        const float v0 = scr[tk * 64 + 2 * lane], v1 = scr[tk * 64 + 2 * lane + 1];
+        if (yf != nullptr)  // fp32 output (diagnostic form): the same sums, not rounded to bf16
+          *reinterpret_cast<float2*>(yf + (long long)rc.tok[tk] * ldyf + rc.col0 + c2) =
+              make_float2(bf_lo(y0) + v0, bf_hi(y0) + v1);
+        else
+          *reinterpret_cast<uint32_t*>(ybase + (long long)rc.tok[tk] * ldy + rc.col0 + c2) =
+              pack_bf16x2(bf_lo(y0) + v0, bf_hi(y0) + v1);
+      }
     }
+    __syncwarp();
   }
 }
 
@@ -279,6 +322,9 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   int* claim_val = reinterpret_cast<int*>(sm + kOffClaim);
   uint32_t* cls = reinterpret_cast<uint32_t*>(sm + kOffCls);  // CTA 0: claimable units by class
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBars);
+  // The projections' parameters, copied once into shared memory: the loops
+  // index them by the unit's projection, which kernel parameters serve slowly.
+  GProj* projs = reinterpret_cast<GProj*>(sm + kOffProj);
   uint64_t* full = bars;                   // [stages] the record writer (+ the copies' bytes)
   uint64_t* empty = bars + kStages;        // [stages] 8 consumer warps
   uint64_t* recv_full = bars + 2 * kStages;  // [2] this CTA's arrival + every CTA's partial bytes
@@ -298,7 +344,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&full[s]), kGProds);
       mbar_init(smem_u32(&empty[s]), kGCons);
     }
     for (int b = 0; b < 2; ++b) {
@@ -306,13 +352,14 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       mbar_init(smem_u32(&claim_full[b]), 1);
       mbar_init(smem_u32(&claim_empty[b]), ncta);
       mbar_init(smem_u32(&unit_full[b]), 1);
-      mbar_init(smem_u32(&unit_empty[b]), 1);
+      mbar_init(smem_u32(&unit_empty[b]), kGProds);
     }
     mbar_init(smem_u32(cons), kGCons);
     mbar_init(smem_u32(cls_ready), kGCons);
     fence_mbar_init();
   }
   if (tid < 3 * 32) cls[tid] = 0u;
+  if (tid < a.n_proj) projs[tid] = a.proj[tid];
   // every barrier of every CTA initialised before any peer arrives on it
   cluster_sync();
   pdl_wait_then_release();
@@ -427,7 +474,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       if (k > 0) next_unit();
       if (u >= n_units) break;
       const int ub = u / G, g = u - ub * G;  // the unit of its projection, the projection
-      const DevView& v = a.proj[g].v;
+      const DevView& v = projs[g].v;
       const int shift = v.page_shift;
       int ad, tb = 0, cnt;
       if (a.src == kSrcTokens) {
@@ -527,8 +574,14 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       }
     }
     if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
-  } else if (warp == kGProd) {
-    // ---------------- producer ----------------
+  } else if (warp == kGProd || warp == kGProd2) {
+    // ---------------- producers ----------------
+    // Both producer warps walk the same units and stages; a stage's copies
+    // (adapter rows, then token rows) alternate between them, copy i going to
+    // producer i % 2, since one warp alone issues bulk copies too slowly to keep
+    // the memory system busy.  Each arrives on the stage barrier with the bytes
+    // of its own copies; producer 0 writes the stage's record.
+    const int pi = warp == kGProd ? 0 : 1;
     uint32_t g = 0;  // stages posted
     auto take_stage = [&]() -> uint32_t {
       const uint32_t st = g % kStages;
@@ -539,7 +592,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
     auto post_record = [&](const GRec& rc) {
       const uint32_t st = take_stage();
       if (lane == 0) {
-        recs[st] = rc;
+        if (pi == 0) recs[st] = rc;
         mbar_arrive(smem_u32(&full[st]));
       }
       ++g;
@@ -552,7 +605,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       }
       const GUnit un = units[q];
       if (un.end) break;
-      const GProj& P = a.proj[un.g];
+      const GProj& P = projs[un.g];
       const DevView& v = P.v;
       const int shift = v.page_shift;
       const long long pmask = (1LL << shift) - 1;
@@ -590,25 +643,29 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
           const bool shrink = kind == kGShrink;
           const int ntr = tokens ? ntok : 0;
           const uint32_t rowb = (uint32_t)w * 2;
+          const int ncopy = nrows + ntr;
           if (lane == 0) {
-            GRec r2 = rc;
-            r2.kind = kind;
-            r2.j0 = j0;
-            r2.nrows = nrows;
-            r2.nvec = w >> 3;
-            r2.col0 = col0;
-            r2.flags = flags;
-            recs[st] = r2;
-            mbar_arrive_expect_tx(bar, (uint32_t)(nrows + ntr) * rowb);
+            if (pi == 0) {
+              GRec r2 = rc;
+              r2.kind = kind;
+              r2.j0 = j0;
+              r2.nrows = nrows;
+              r2.nvec = w >> 3;
+              r2.col0 = col0;
+              r2.flags = flags;
+              recs[st] = r2;
+            }
+            mbar_arrive_expect_tx(bar, (uint32_t)((ncopy + 1 - pi) / 2) * rowb);  // copies pi, pi + 2, ...
           }
           __syncwarp();
-          const int tk = __shfl_sync(0xffffffffu, mytok, (lane - nrows) & (kNT - 1));
-          if (lane < nrows) {
+          const int idx = 2 * lane + pi;  // this lane's copy of the stage
+          const int tk = __shfl_sync(0xffffffffu, mytok, (idx - nrows) & (kNT - 1));
+          if (idx < nrows) {
             const long long rowlen = shrink ? v.d_in : v.d_out;
             const long long page0 = shrink ? un.a_page0 : un.b_page0;
             const int pbase = shrink ? 0 : (int)na;
-            long long e = (long long)(j0 + lane) * rowlen + col0;
-            uint32_t dst = sbase + (uint32_t)(lane * kRowBytes);
+            long long e = (long long)(j0 + idx) * rowlen + col0;
+            uint32_t dst = sbase + (uint32_t)(idx * kRowStride);
             for (int rem = w; rem > 0;) {
               const long long idx = e >> shift, off = e & pmask;
               const long long page = un.cached ? pc[pbase + idx] : v.page_list[page0 + idx];
@@ -618,9 +675,9 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
               dst += (uint32_t)n * 2;
               rem -= n;
             }
-          } else if (lane < nrows + ntr) {
+          } else if (idx < ncopy) {
             const uint16_t* src = (shrink ? P.x + (long long)tk * P.ldx : P.y + (long long)tk * P.ldy) + col0;
-            bulk_g2s(sbase + (uint32_t)((kChunkRows + lane - nrows) * kRowBytes), src, rowb, bar);
+            bulk_g2s(sbase + (uint32_t)((kChunkRows + idx - nrows) * kRowStride), src, rowb, bar);
           }
           ++g;
         };
@@ -665,13 +722,12 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
     const long long ldh = a.ldh;
     const int mode = a.mode;
     uint32_t ngroup = 0, ncons = 0;
-    float sacc[kNT];     // shrink: the lane's row partials over a row block's sub-slices
-    float eacc[kNT][2];  // expand: the lane's two outputs over a sub-slice's row blocks
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};  // shrink: the lane's part of the row block's 16 x 8 tile
+    float eacc[4][4];  // expand: the lane's parts of the warp's four 16 x 8 output tiles
 #pragma unroll
-    for (int t = 0; t < kNT; ++t) sacc[t] = eacc[t][0] = eacc[t][1] = 0.f;
+    for (int i = 0; i < 4; ++i) eacc[i][0] = eacc[i][1] = eacc[i][2] = eacc[i][3] = 0.f;
     if (ordered) {  // classify the claimable units: four per thread, every load in flight
       int val[4];
-#pragma unroll
       int gk[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -684,7 +740,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       for (int k = 0; k < 4; ++k) val[k] = val[k] < 0 ? -1 : a.seg_adapter[val[k]];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const DevView& vk = a.proj[gk[k]].v;
+        const DevView& vk = projs[gk[k]].v;
         val[k] = val[k] < 0 || val[k] >= vk.n_adapters ? 0 : vk.adapters[val[k]].rank;
       }
 #pragma unroll
@@ -715,22 +771,14 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       const uint8_t* sb = sm + (size_t)st * kStageBytes;
       const int b = ngroup & 1;
       if (rc.kind == kGShrink) {
-        if (rc.flags & kFFirst) {
+        if (rc.flags & kFFirst) sacc[0] = sacc[1] = sacc[2] = sacc[3] = 0.f;
+        shrink_chunk(smem_u32(sb), rc.nvec * 8, rc.ntok, sacc, warp, lane);
+        if (rc.flags & kFLast) {  // the row block is done: the warp's partial of every row and token
+          const int gr = lane >> 2, tq = lane & 3;
 #pragma unroll
-          for (int t = 0; t < kNT; ++t) sacc[t] = 0.f;
-        }
-        switch (rc.ntok) {
-          case 1: shrink_chunk<1>(sb, rc.nrows, rc.nvec, sacc, warp, lane); break;
-          case 2: shrink_chunk<2>(sb, rc.nrows, rc.nvec, sacc, warp, lane); break;
-          case 3: shrink_chunk<3>(sb, rc.nrows, rc.nvec, sacc, warp, lane); break;
-          default: shrink_chunk<4>(sb, rc.nrows, rc.nvec, sacc, warp, lane); break;
-        }
-        if (rc.flags & kFLast) {  // the row block is done: its two halves meet in the warp's partial
-          const int i = lane >> 1;
-#pragma unroll
-          for (int t = 0; t < kNT; ++t) {
-            const float v = sacc[t] + __shfl_xor_sync(0xffffffffu, sacc[t], 1);
-            if ((lane & 1) == 0 && i < rc.nrows && t < rc.ntok) pw[(warp * kNT + t) * kHMax + rc.j0 + i] = v;
+          for (int e = 0; e < 4; ++e) {
+            const int j = gr + 8 * (e >> 1), t = 2 * tq + (e & 1);
+            if (j < rc.nrows && t < rc.ntok) pw[(warp * kNT + t) * kHMax + rc.j0 + j] = sacc[e];
           }
         }
       }
@@ -781,7 +829,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         cons_sync();
       }
       if (rc.kind == kGExpand)
-        expand_chunk(a.proj[rc.g].y, a.proj[rc.g].ldy, yf, ldyf, sb, hs, eacc, rc, ok, warp, lane);
+        expand_chunk(projs[rc.g].y, projs[rc.g].ldy, yf, ldyf, smem_u32(sb), sb, hs, pw + warp * kNT * kHMax, eacc,
+                     rc, ok, warp, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
     }
