@@ -305,6 +305,18 @@ lora_status_t lora_apply_fixed_scratch(const void* x, int64_t ldx, void* y, int6
 uint64_t lora_launch_count(void);
 
 /**
+ * Test-only: exercises the kernels' timeout path without any fault.  With
+ * cycles > 0, every CTA of every compute kernel launched afterwards (in this
+ * process, on any stream) first waits, for at most `cycles` clock cycles, on a
+ * barrier of its own that nothing ever arrives on, then takes the exit of a
+ * wait that ran out: it ORs LORA_DERR_TIMEOUT into the error word, writes no
+ * output and returns.  cycles <= 0 disarms the probe.  Not for production use:
+ * while armed, every compute call fails this way.  (No passage of the pages;
+ * the bounded waits themselves are this library's failure detection.)
+ */
+void lora_debug_wait_probe(int64_t cycles);
+
+/**
  * Pages one adapter of rank r occupies in a pool of page_elems-element pages:
  * ceil(r * d_in / page_elems) + ceil(r * d_out / page_elems) (bytes per matrix
  * pair (d_in * r + r * d_out) * 2 before rounding to pages: "Multi-LoRA

@@ -51,6 +51,7 @@ EXPORTED = (
     "lora_status_string",
     "lora_abi_version",
     "lora_launch_count",
+    "lora_debug_wait_probe",
     "lora_pool_mgr_create",
     "lora_pool_mgr_destroy",
     "lora_pool_mgr_page_list_len",
@@ -117,6 +118,8 @@ def lib():
         vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
         L.lora_launch_count.restype = ctypes.c_uint64
         L.lora_launch_count.argtypes = []
+        L.lora_debug_wait_probe.restype = None
+        L.lora_debug_wait_probe.argtypes = [ctypes.c_int64]
         L.lora_segments_buffer_bytes.restype = sz
         L.lora_segments_buffer_bytes.argtypes = [i32]
         L.lora_segments_carve.restype = i32
@@ -349,6 +352,11 @@ def lora_apply_fixed_scratch(x: torch.Tensor, y: torch.Tensor, seg: Segments, vi
     _check(lib().lora_apply_fixed_scratch(_ptr(x), _ld(x), _ptr(y), _ld(y), ctypes.byref(seg.c),
                                           ctypes.byref(view.c), _ptr(err), _stream(stream)),
            "lora_apply_fixed_scratch")
+
+
+def debug_wait_probe(cycles: int) -> None:
+    """Test-only: arm (cycles > 0) or disarm the kernels' timeout probe."""
+    lib().lora_debug_wait_probe(int(cycles))
 
 
 def launch_count() -> int:

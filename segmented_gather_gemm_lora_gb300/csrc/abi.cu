@@ -96,6 +96,9 @@ cudaError_t ensure_smem_attr(const void* func, size_t bytes) {
 }
 
 std::atomic<uint64_t> g_launches{0};
+std::atomic<long long> g_wait_probe{0};
+
+long long wait_probe_cycles() { return g_wait_probe.load(std::memory_order_relaxed); }
 
 int max_active_clusters(const void* func, int block, size_t smem, int cluster_x) {
   struct Entry {
@@ -418,6 +421,10 @@ lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy, const 
 }  // extern "C"
 
 extern "C" uint64_t lora_launch_count(void) { return lora::g_launches.load(std::memory_order_relaxed); }
+
+extern "C" void lora_debug_wait_probe(int64_t cycles) {
+  lora::g_wait_probe.store(cycles > 0 ? (long long)cycles : 0, std::memory_order_relaxed);
+}
 
 namespace lora {
 

@@ -78,6 +78,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+// Bounded wait with an explicit limit in clock cycles (false when it ran out).
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, long long limit) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit) return false;
+  }
+  return true;
+}
+
+// The timeout probe of the kernels (lora_debug_wait_probe): thread 0 of the CTA
+// waits, for at most `limit` cycles, on a barrier of its own that nothing
+// arrives on, no transaction bytes are expected on and no copy or peer store
+// targets; true if the wait completed (it never does), false when it ran out.
+// The CTA's threads read the verdict after a __syncthreads.
+__device__ __forceinline__ bool wait_probe(uint64_t* bar, long long limit) {
+  mbar_init(smem_u32(bar), 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  return mbar_wait_for(smem_u32(bar), 0, limit);
+}
+
 // --------------------------------------------------- bulk copy (non-tensor TMA) --
 
 // global -> shared copy of `bytes` (a multiple of 16; both addresses 16-byte

@@ -170,6 +170,7 @@ struct GatherArgs {
   int mode;
   int src;
   int short_only;
+  long long probe;  // > 0: the timeout probe's wait limit in cycles (lora_debug_wait_probe)
 };
 
 // ------------------------------------------------ warp-level tensor-core tiles --
@@ -365,6 +366,13 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   pdl_wait_then_release();
 
   bool ok = true;
+  if (a.probe > 0) {  // the timeout probe: every CTA takes the exit of a wait that ran out
+    __shared__ uint64_t probe_bar;
+    __shared__ int probe_ok;
+    if (tid == 0) probe_ok = wait_probe(&probe_bar, a.probe) ? 1 : 0;
+    __syncthreads();
+    ok = probe_ok != 0;
+  }
   const int n_short = a.src == kSrcSegments ? a.meta[2] : 0;
   // units of one projection (a segment's group of tokens, or a token), times the projections
   const int n_base = a.src == kSrcTokens ? a.T : a.meta[2] + (a.short_only ? 0 : a.meta[3]);
@@ -883,6 +891,7 @@ lora_status_t launch_gather_multi(int mode, int src, int short_only, int n_proj,
   a.mode = mode;
   a.src = src;
   a.short_only = short_only;
+  a.probe = wait_probe_cycles();
 
   const int upper = (src == kSrcTokens ? T : seg->T + (short_only ? 0 : seg->max_long_units)) * n_proj;
   if (upper <= 0) return LORA_OK;

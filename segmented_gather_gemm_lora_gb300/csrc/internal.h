@@ -38,6 +38,10 @@ lora_status_t validate_view(const lora_pool_view_t* v);
 // Count one kernel launch made without launch_pdl (lora_launch_count).
 void count_launch();
 
+// The wait limit, in cycles, of the timeout probe lora_debug_wait_probe armed
+// (0: no probe).  The compute kernels pass it to their CTAs.
+long long wait_probe_cycles();
+
 lora_status_t launch_segments(const int32_t* ids, int T, int n_adapters, int mode,
                               const lora_segments_t* seg, int32_t* err, cudaStream_t stream);
 

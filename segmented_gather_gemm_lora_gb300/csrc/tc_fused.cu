@@ -108,6 +108,7 @@ struct FusedArgs {
   int n_proj;
   int klen;          // columns per d_in slice (a multiple of 64)
   int after_gather;  // launched right after this call's gather kernel (disjoint data): no wait at entry
+  long long probe;   // > 0: the timeout probe's wait limit in cycles (lora_debug_wait_probe)
 };
 
 __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_constant__ FusedArgs a) {
@@ -180,6 +181,13 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
   const uint32_t tmem = *tmem_slot;  // shrink partials at columns 0 / 64, expand accumulators at 128 / 192
   if (a.after_gather != 0) pdl_enter(true);
   bool ok = true;
+  if (a.probe > 0) {  // the timeout probe: every CTA takes the exit of a wait that ran out
+    __shared__ uint64_t probe_bar;
+    __shared__ int probe_ok;
+    if (tid == 0) probe_ok = wait_probe(&probe_bar, a.probe) ? 1 : 0;
+    __syncthreads();
+    ok = probe_ok != 0;
+  }
   const int R = kTM / (int)ncta;  // rows each CTA owns in the exchange
 
   if (warp == 0) {
@@ -225,7 +233,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
       return v;
     };
     uint32_t np = 0;  // records posted
-    for (int u = (int)cid, k = 0;; ++k) {
+    for (int u = ok ? (int)cid : n_units, k = 0;; ++k) {  // after a failed wait: the end record only
       if (k > 0) {
         // the loaders have taken the last record posted before the next claim
         if (np > 0 && !mbar_wait(smem_u32(&slot_taken[(np - 1) % kFSlots]), ((np - 1) / kFSlots) & 1)) ok = false;
@@ -763,6 +771,7 @@ lora_status_t launch_fused_tc(int n_proj, const ProjCall* projs, const lora_segm
   a.n_proj = n_proj;
   a.klen = klen;
   a.after_gather = after_gather;
+  a.probe = wait_probe_cycles();
   const long long upper = (long long)seg->max_long_units * n_proj;
   if (upper <= 0) return LORA_OK;
   if (ensure_smem_attr((const void*)fused_tc_kernel, kFusedSmem) != cudaSuccess) return LORA_ERR_CUDA;
