@@ -58,6 +58,9 @@ def _declare(L):
     L.oracle_expand.restype = ctypes.c_int
     L.oracle_expand.argtypes = [vp, i64, vp, i64, vp, i64, vp, vp, i64, i64, vp, i64, vp,
                                 i32, i32, i64, i64]
+    L.oracle_lora_backward.restype = ctypes.c_int
+    L.oracle_lora_backward.argtypes = [vp, i64, vp, i64, vp, vp, i64, vp, vp, i64, i64, vp, i64,
+                                       vp, i32, i32, i64, i64]
     L.oracle_segments_build.restype = i32
     L.oracle_segments_build.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp]
     L.oracle_work_lists.restype = None
@@ -150,6 +153,33 @@ def expand(h, y0, ids, pool):
                               pool.n_pages, pool.page_elems, _p(pl), pl.size, _p(desc),
                               desc.size, pool.max_rank, pool.d_in, pool.d_out)
     return y, int(err)
+
+
+def lora_backward(x, g, ids, pool, grad=None):
+    """(dx double [T, d_in], grad double [n_pages, page_elems], err): the gradients of the
+    LoRA delta given g = dL/dy (bf16 bits); dA_i and dB_i are added into `grad` (a fresh
+    zero array when None) at their elements' pool positions."""
+    x = _c(x, np.uint16)
+    g = _c(g, np.uint16)
+    ids = _c(ids, np.int32)
+    T = ids.size
+    dx = np.empty((T, pool.d_in), dtype=np.float64)
+    grad = np.zeros(pool.pool.shape, dtype=np.float64) if grad is None else _c(grad, np.float64)
+    pl, pp, desc = _pool_args(pool)
+    err = lib().oracle_lora_backward(_p(x), x.shape[1] if T else pool.d_in, _p(g),
+                                     g.shape[1] if T else pool.d_out, _p(dx), _p(grad), T, _p(ids),
+                                     _p(pp), pool.n_pages, pool.page_elems, _p(pl), pl.size,
+                                     _p(desc), desc.size, pool.max_rank, pool.d_in, pool.d_out)
+    return dx, grad, int(err)
+
+
+def unpack_grad(grad, pool, page0: int, rows: int, cols: int) -> np.ndarray:
+    """Logical rows x cols matrix of a gradient array laid out like the pool (read through
+    the page table, as unpack_matrix reads the weights)."""
+    P = pool.page_elems
+    e = np.arange(rows * cols, dtype=np.int64)
+    pos = pool.page_list[page0 + e // P].astype(np.int64) * P + e % P
+    return np.asarray(grad).reshape(-1)[pos].reshape(rows, cols)
 
 
 GROUP, CONTIGUOUS = 0, 1

@@ -29,6 +29,10 @@
  *    up").  Adapter elements are read through the page table.
  *  - oracle_shrink / oracle_expand: the two stages of that product
  *    ("Multi-LoRA Serving in Production", "Shrink Stage" / "Expand Stage").
+ *  - oracle_lora_backward: the gradients of that product for training the
+ *    adapters; the base is frozen and receives none, only A and B do ("QLoRA
+ *    and multi-LoRA at the limit on small models", section "The bare
+ *    mechanism: LoRA, and why you can train on a 4-bit base").
  *  - oracle_bf16_rne: rounding of a double to the nearest bf16, ties to even.
  *
  * Conventions (the readings this oracle takes where the pages are silent):
@@ -266,6 +270,85 @@ int oracle_expand(const float* hin, int64_t ldh, const uint16_t* y0, int64_t ldy
             for (int64_t j = 0; j < desc[i].rank; ++j)
                 acc += (double)hin[t * ldh + j] * pool_elem(&p, desc[i].b_page0, j * d_out + n, &oob);
             y[t * d_out + n] += s * acc;
+        }
+    }
+    return err;
+}
+
+/* -------------------------------------------------------- the gradients -- */
+
+/* Position of logical element e of the matrix whose pages start at page0, in
+ * the pool's layout (the gradient arrays share it); -1 if out of range. */
+static int64_t pool_pos(const orc_pool_t* p, int64_t page0, int64_t e)
+{
+    int64_t slot = page0 + e / p->page_elems;
+    if (slot < 0 || slot >= p->n_page_list) return -1;
+    int64_t page = p->page_list[slot];
+    if (page < 0 || page >= p->n_pages) return -1;
+    return page * p->page_elems + e % p->page_elems;
+}
+
+/*
+ * Gradients of a loss L through the LoRA delta, given g = dL/dy (bf16).  The
+ * base W0 is frozen and gets no gradient; only the adapters' A and B are
+ * trainable, and the adapter path is the only one the gradient flows through.
+ * Differentiating y[t,n] = y0[t,n] + s_i sum_j (sum_k x[t,k] A_i[j,k]) B_i[j,n]
+ * token by token, for every token t with a usable adapter i:
+ *     h_j        = sum_k x[t,k] A_i[j,k]
+ *     u_j        = sum_n g[t,n] B_i[j,n]
+ *     dB_i[j,n] += s_i h_j g[t,n]
+ *     dA_i[j,k] += s_i u_j x[t,k]
+ *     dx[t,k]    = s_i sum_j u_j A_i[j,k]
+ * Other tokens: dx[t,k] = 0 and no gradient.  dA_i and dB_i are added (in
+ * token order) into grad, a double array laid out like the pool: the gradient
+ * of the element at pool position q is grad[q].  dx is double [T, d_in].
+ * Returns the OR of the error bits met (as oracle_lora_apply).
+ */
+int oracle_lora_backward(const uint16_t* x, int64_t ldx, const uint16_t* g, int64_t ldg,
+                         double* dx, double* grad, int64_t T, const int32_t* ids,
+                         const uint16_t* pool, int64_t n_pages, int64_t page_elems,
+                         const int32_t* page_list, int64_t n_page_list,
+                         const void* adapters, int32_t n_adapters, int32_t max_rank,
+                         int64_t d_in, int64_t d_out)
+{
+    const orc_desc_t* desc = (const orc_desc_t*)adapters;
+    orc_pool_t p = {pool, n_pages, page_elems, page_list, n_page_list};
+    int err = 0;
+    double h[256], u[256];
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t k = 0; k < d_in; ++k) dx[t * d_in + k] = 0.0;
+        int32_t i = ids[t];
+        if (i == -1) continue;
+        if (i < -1 || i >= n_adapters) { err |= ORC_ERR_BAD_ADAPTER; continue; }
+        int bad = adapter_check(&desc[i], max_rank, &p, d_in, d_out);
+        if (bad || desc[i].rank > 256) { err |= bad ? bad : ORC_ERR_BAD_RANK; continue; }
+        int64_t r = desc[i].rank;
+        double s = (double)desc[i].scale;
+        int oob = 0;
+        for (int64_t j = 0; j < r; ++j) {            /* h = x . A_i^T */
+            double acc = 0.0;
+            for (int64_t k = 0; k < d_in; ++k)
+                acc += oracle_bf16_to_double(x[t * ldx + k]) * pool_elem(&p, desc[i].a_page0, j * d_in + k, &oob);
+            h[j] = acc;
+        }
+        for (int64_t j = 0; j < r; ++j) {            /* u = g . B_i^T */
+            double acc = 0.0;
+            for (int64_t n = 0; n < d_out; ++n)
+                acc += oracle_bf16_to_double(g[t * ldg + n]) * pool_elem(&p, desc[i].b_page0, j * d_out + n, &oob);
+            u[j] = acc;
+        }
+        for (int64_t j = 0; j < r; ++j) {            /* dB_i += s h g^T */
+            for (int64_t n = 0; n < d_out; ++n)
+                grad[pool_pos(&p, desc[i].b_page0, j * d_out + n)] += s * h[j] * oracle_bf16_to_double(g[t * ldg + n]);
+        }
+        for (int64_t j = 0; j < r; ++j) {            /* dA_i += s u x^T */
+            for (int64_t k = 0; k < d_in; ++k)
+                grad[pool_pos(&p, desc[i].a_page0, j * d_in + k)] += s * u[j] * oracle_bf16_to_double(x[t * ldx + k]);
+        }
+        for (int64_t k = 0; k < d_in; ++k) {         /* dx = s u . A_i */
+            double acc = 0.0;
+            for (int64_t j = 0; j < r; ++j) acc += u[j] * pool_elem(&p, desc[i].a_page0, j * d_in + k, &oob);
+            dx[t * d_in + k] = s * acc;
         }
     }
     return err;

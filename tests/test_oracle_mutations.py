@@ -16,8 +16,8 @@ MUTATIONS = {
                       "acc += h[j] * pool_elem(&p, desc[i].b_page0, j * d_out + n, &oob);\n            y[t * d_out + n] += acc;"),
     "expand_scale": ("(double)hin[t * ldh + j] * pool_elem(&p, desc[i].b_page0, j * d_out + n, &oob);\n            y[t * d_out + n] += s * acc;",
                      "(double)hin[t * ldh + j] * pool_elem(&p, desc[i].b_page0, j * d_out + n, &oob);\n            y[t * d_out + n] += acc;"),
-    "transposed_A": ("pool_elem(&p, desc[i].a_page0, j * d_in + k, &oob);\n            h[j] = acc;",
-                     "pool_elem(&p, desc[i].a_page0, k * r + j, &oob);\n            h[j] = acc;"),
+    "transposed_A": ("/* shrink: x . A_i (d_in -> r) */\n            double acc = 0.0;\n            for (int64_t k = 0; k < d_in; ++k)\n                acc += oracle_bf16_to_double(x[t * ldx + k]) * pool_elem(&p, desc[i].a_page0, j * d_in + k, &oob);",
+                     "/* shrink: x . A_i (d_in -> r) */\n            double acc = 0.0;\n            for (int64_t k = 0; k < d_in; ++k)\n                acc += oracle_bf16_to_double(x[t * ldx + k]) * pool_elem(&p, desc[i].a_page0, k * r + j, &oob);"),
     "transposed_B": ("acc += h[j] * pool_elem(&p, desc[i].b_page0, j * d_out + n, &oob);",
                      "acc += h[j] * pool_elem(&p, desc[i].b_page0, n * r + j, &oob);"),
     "wrong_sign": ("acc += h[j] * pool_elem", "acc -= h[j] * pool_elem"),
@@ -32,6 +32,13 @@ MUTATIONS = {
                      "return (d_in * rank + rank * d_out) * 2;"),
     "y0_dropped": ("y[t * d_out + n] = oracle_bf16_to_double(y0[t * ldy0 + n]);\n        int32_t i = ids[t];\n        if (i == -1) continue;\n        if (i < -1 || i >= n_adapters) { err |= ORC_ERR_BAD_ADAPTER; continue; }\n        int bad = adapter_check(&desc[i], max_rank, &p, d_in, d_out);\n        if (bad || desc[i].rank > 256)",
                    "y[t * d_out + n] = (ids[t] >= 0) ? 0.0 : oracle_bf16_to_double(y0[t * ldy0 + n]);\n        int32_t i = ids[t];\n        if (i == -1) continue;\n        if (i < -1 || i >= n_adapters) { err |= ORC_ERR_BAD_ADAPTER; continue; }\n        int bad = adapter_check(&desc[i], max_rank, &p, d_in, d_out);\n        if (bad || desc[i].rank > 256)"),
+    "grad_dA_scale": ("+= s * u[j] * oracle_bf16_to_double(x[t * ldx + k]);",
+                      "+= u[j] * oracle_bf16_to_double(x[t * ldx + k]);"),
+    "grad_dB_transposed": ("grad[pool_pos(&p, desc[i].b_page0, j * d_out + n)]",
+                           "grad[pool_pos(&p, desc[i].b_page0, n * r + j)]"),
+    "grad_u_from_A": ("acc += oracle_bf16_to_double(g[t * ldg + n]) * pool_elem(&p, desc[i].b_page0, j * d_out + n, &oob);",
+                      "acc += oracle_bf16_to_double(g[t * ldg + n]) * pool_elem(&p, desc[i].b_page0, n * r + j, &oob);"),
+    "grad_dx_dropped_scale": ("dx[t * d_in + k] = s * acc;", "dx[t * d_in + k] = acc;"),
 }
 
 

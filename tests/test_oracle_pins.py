@@ -376,3 +376,97 @@ def test_group_and_contiguous_give_same_outputs():
                 seen[t] += 1
                 assert ids[t] == seg_ad[s]
         assert (seen == 1).all()
+
+
+# -------------------------------------------------------------- gradients --
+#
+# The backward oracle gives dL/dA_i, dL/dB_i (added at the pool positions of A_i
+# and B_i) and dL/dx for L = sum_{t,n} g[t,n] y[t,n].  y is exactly linear in each
+# adapter element and in each x element, so a finite difference of the forward
+# oracle between two bf16 values of one element is exact up to fp64 rounding.
+
+def backward_case(seed, d_in=64, d_out=48, ranks=(3, 5, 8), T=12, page_elems=64):
+    rng = np.random.default_rng(seed)
+    pool = W.build_pool(rng, d_in, d_out, list(ranks), page_elems=page_elems, max_rank=16)
+    ids = rng.integers(-1, len(ranks), size=T).astype(np.int32)
+    ids[:len(ranks)] = np.arange(len(ranks))  # every adapter used at least once
+    batch = W.make_batch(rng, ids, d_in, d_out)
+    g = W._normal_bf16(rng, (T, d_out), 1.0)
+    return pool, batch, g
+
+
+def loss(pool, batch, g):
+    y, err = oracle.lora_apply(batch.x, batch.y0, batch.ids, pool)
+    assert err == 0
+    return float((f64(g) * y).sum())
+
+
+def with_element(bits, idx, step):
+    out = bits.copy()
+    out[idx] = np.uint16(int(out[idx]) + step)
+    return out
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_backward_matches_finite_differences(seed):
+    pool, batch, g = backward_case(seed)
+    dx, grad, err = oracle.lora_backward(batch.x, g, batch.ids, pool)
+    assert err == 0
+    L0 = loss(pool, batch, g)
+    rng = np.random.default_rng(100 + seed)
+    flat = pool.pool.reshape(-1)
+    for i in range(pool.n_adapters):
+        r = int(pool.ranks[i])
+        for page0, rows, cols in ((int(pool.desc[i]["a_page0"]), r, pool.d_in),
+                                  (int(pool.desc[i]["b_page0"]), r, pool.d_out)):
+            for _ in range(4):
+                e = int(rng.integers(0, rows * cols))
+                q = int(pool.page_list[page0 + e // pool.page_elems]) * pool.page_elems + e % pool.page_elems
+                p2 = W.AdapterPool(**{**pool.__dict__, "pool": with_element(flat, q, 37).reshape(pool.pool.shape)})
+                delta = float(f64(p2.pool.reshape(-1)[q]) - f64(flat[q]))
+                fd = (loss(p2, batch, g) - L0) / delta
+                assert fd == pytest.approx(grad.reshape(-1)[q], rel=1e-7, abs=1e-9), (i, page0, e)
+    for _ in range(6):  # dx through the adapter path (y0 is fixed)
+        t, k = int(rng.integers(0, batch.T)), int(rng.integers(0, pool.d_in))
+        b2 = W.Batch(x=with_element(batch.x, (t, k), 37), y0=batch.y0, ids=batch.ids, d_in=batch.d_in,
+                     d_out=batch.d_out)
+        delta = float(f64(b2.x[t, k]) - f64(batch.x[t, k]))
+        fd = (loss(pool, b2, g) - L0) / delta
+        assert fd == pytest.approx(dx[t, k], rel=1e-7, abs=1e-9), (t, k)
+
+
+def test_backward_single_adapter_is_dense_products():
+    """One adapter for every token: dB = s H^T G, dA = s U^T X, dx = s U A with H = X A^T,
+    U = G B^T, checked against numpy float64 matmul on the logical matrices."""
+    rng = np.random.default_rng(5)
+    pool = W.build_pool(rng, 96, 80, [8], page_elems=64, max_rank=8)
+    ids = np.zeros(20, dtype=np.int32)
+    batch = W.make_batch(rng, ids, 96, 80)
+    g = W._normal_bf16(rng, (20, 80), 1.0)
+    dx, grad, err = oracle.lora_backward(batch.x, g, ids, pool)
+    assert err == 0
+    A, Bm = f64(pool.A[0]), f64(pool.B[0])
+    X, G = f64(batch.x), f64(g)
+    s = float(pool.scales[0])
+    H, U = X @ A.T, G @ Bm.T
+    d = pool.desc[0]
+    np.testing.assert_allclose(oracle.unpack_grad(grad, pool, int(d["b_page0"]), 8, 80), s * H.T @ G, rtol=1e-12,
+                               atol=1e-12)
+    np.testing.assert_allclose(oracle.unpack_grad(grad, pool, int(d["a_page0"]), 8, 96), s * U.T @ X, rtol=1e-12,
+                               atol=1e-12)
+    np.testing.assert_allclose(dx, s * U @ A, rtol=1e-12, atol=1e-12)
+
+
+def test_backward_zero_gradient_and_untouched_tokens():
+    pool, batch, g = backward_case(3)
+    dx, grad, _ = oracle.lora_backward(batch.x, np.zeros_like(g), batch.ids, pool)
+    assert not dx.any() and not grad.any()
+    dx, grad, _ = oracle.lora_backward(batch.x, g, batch.ids, pool)
+    none = batch.ids < 0
+    assert not dx[none].any()
+    keep = ~none  # tokens without an adapter contribute nothing
+    dx2, grad2, _ = oracle.lora_backward(batch.x[keep], g[keep], batch.ids[keep], pool)
+    np.testing.assert_array_equal(grad2, grad)
+    # gradients accumulate into the array given
+    _, grad3, _ = oracle.lora_backward(batch.x, g, batch.ids, pool, grad=grad.copy())
+    np.testing.assert_allclose(grad3, 2 * grad, rtol=1e-12, atol=1e-12)
