@@ -253,6 +253,33 @@ lora_status_t lora_apply_f32y(const void* x, int64_t ldx, const void* y0, int64_
                               int32_t* dev_err, lora_stream_t stream);
 
 /**
+ * Backward pass, for training the adapters: the base stays frozen and gets no
+ * gradient; only A_i and B_i do, and the adapter is the only path the
+ * gradient flows through ("QLoRA and multi-LoRA at the limit on small
+ * models", section "The bare mechanism: LoRA, and why you can train on a
+ * 4-bit base").  Given the forward's input x and dy = dL/dy, for every token
+ * t of the segments, with i = its adapter:
+ *     h[t] = x[t] A_i^T,  u[t] = dy[t] B_i^T                 (fp32, into hu)
+ *     dB_i += s_i sum_t h[t]^T dy[t],  dA_i += s_i sum_t u[t]^T x[t]
+ *     dx[t] = bf16(dx[t] + s_i u[t] A_i)                      (if dx != NULL)
+ * x: bf16 [T, ldx]; dy: bf16 [T, lddy] (lddy >= d_out); dx: bf16 [T, lddx],
+ * updated in place, or NULL.  grad_pool: device fp32 [n_pages * page_elems],
+ * the same page layout as view->pool: the gradient of the weight at pool
+ * position q is added into grad_pool[q] (zero it to start; calls accumulate,
+ * as gradient accumulation over micro-batches does).  hu: device fp32
+ * workspace [2 * T * ldh] (h rows, then u rows, by token), ldh >= max_rank,
+ * ldh % 4 == 0.  With GROUP segments each adapter's gradient elements receive
+ * one addition per call, in a fixed order; with CONTIGUOUS segments an adapter
+ * that has several segments receives one per segment, in any order.  x, dy,
+ * dx, hu and grad_pool must not overlap.  Device errors as lora_apply: the
+ * affected tokens add nothing to any gradient and leave their dx rows alone.
+ */
+lora_status_t lora_sgmv_backward(const void* x, int64_t ldx, const void* dy, int64_t lddy, void* dx,
+                                 int64_t lddx, float* grad_pool, float* hu, int64_t ldh,
+                                 const lora_segments_t* seg, const lora_pool_view_t* view,
+                                 int32_t* dev_err, lora_stream_t stream);
+
+/**
  * Decode form without segments: each token t gathers its own adapter
  * token_adapter[t] (device int32 [T], -1 = no adapter), one token per request
  * (the batched gather path for size-1 segments of "Multi-LoRA serving: ...",

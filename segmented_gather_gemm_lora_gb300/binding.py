@@ -45,6 +45,7 @@ EXPORTED = (
     "lora_apply",
     "lora_apply_f32y",
     "lora_apply_multi",
+    "lora_sgmv_backward",
     "lora_apply_fixed_scratch",
     "lora_bgmv",
     "lora_pool_pages_needed",
@@ -136,6 +137,8 @@ def lib():
         L.lora_apply.argtypes = [vp, i64, vp, i64, seg_p, view_p, vp, vp]
         L.lora_apply_f32y.restype = i32
         L.lora_apply_f32y.argtypes = [vp, i64, vp, i64, vp, i64, seg_p, view_p, vp, vp]
+        L.lora_sgmv_backward.restype = i32
+        L.lora_sgmv_backward.argtypes = [vp, i64, vp, i64, vp, i64, vp, vp, i64, seg_p, view_p, vp, vp]
         L.lora_apply_multi.restype = i32
         L.lora_apply_multi.argtypes = [ctypes.POINTER(lora_proj_t), i32, seg_p, vp, vp]
         L.lora_apply_fixed_scratch.restype = i32
@@ -337,6 +340,18 @@ def lora_apply_multi(calls, seg: Segments, err: Optional[torch.Tensor] = None, s
         arr[i].view = view.c
     _check(lib().lora_apply_multi(arr, len(calls), ctypes.byref(seg.c), _ptr(err), _stream(stream)),
            "lora_apply_multi")
+
+
+def lora_sgmv_backward(x: torch.Tensor, dy: torch.Tensor, dx: Optional[torch.Tensor], grad_pool: torch.Tensor,
+                       hu: torch.Tensor, seg: Segments, view: PoolView, err: Optional[torch.Tensor] = None,
+                       stream=None):
+    """Adapter gradients: dA_i, dB_i added into grad_pool (fp32, the pool's page layout),
+    dx += the adapter path's contribution (bf16 in place, or None).  hu: fp32 workspace
+    [2 * T, ldh]."""
+    ldh = _ld(hu)
+    _check(lib().lora_sgmv_backward(_ptr(x), _ld(x), _ptr(dy), _ld(dy), _ptr(dx), _ld(dx) if dx is not None else 0,
+                                    _ptr(grad_pool), _ptr(hu), ldh, ctypes.byref(seg.c), ctypes.byref(view.c),
+                                    _ptr(err), _stream(stream)), "lora_sgmv_backward")
 
 
 def apply_kernel_names():

@@ -1,5 +1,6 @@
 // C ABI entry points: host-side argument checks, then launches on the caller's
 // stream.  Nothing here allocates device memory or synchronises.
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -183,7 +184,13 @@ lora_status_t validate_view(const lora_pool_view_t* v) { return check_view(v); }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+thread_local bool t_transposed = false;
+
+TransposedViews::TransposedViews() { t_transposed = true; }
+TransposedViews::~TransposedViews() { t_transposed = false; }
+
 void make_dev_view(const lora_pool_view_t* v, DevView* out) {
+  out->swap_ab = t_transposed ? 1 : 0;
   out->pool = static_cast<const uint16_t*>(v->pool);
   out->page_list = v->page_list;
   out->adapters = v->adapters;
@@ -402,6 +409,46 @@ lora_status_t lora_apply_f32y(const void* x, int64_t ldx, const void* y0, int64_
   if (T == 0) return LORA_OK;
   return run_segmented(kModeApply, x, ldx, const_cast<void*>(y0), ldy0, nullptr, 0, seg, view, dev_err,
                        (cudaStream_t)stream, yf, ldyf);
+}
+
+lora_status_t lora_sgmv_backward(const void* x, int64_t ldx, const void* dy, int64_t lddy, void* dx, int64_t lddx,
+                                 float* grad_pool, float* hu, int64_t ldh, const lora_segments_t* seg,
+                                 const lora_pool_view_t* view, int32_t* dev_err, lora_stream_t stream) {
+  lora_status_t st = check_view(view);
+  if (st != LORA_OK) return st;
+  if ((st = check_seg(seg)) != LORA_OK) return st;
+  const int T = seg->T;
+  if ((st = check_act(x, ldx, view->d_in, T)) != LORA_OK) return st;
+  if ((st = check_act(dy, lddy, view->d_out, T)) != LORA_OK) return st;
+  if (dx != nullptr && (st = check_act(dx, lddx, view->d_in, T)) != LORA_OK) return st;
+  if (T == 0) return LORA_OK;
+  if (grad_pool == nullptr || !aligned16(grad_pool)) return LORA_ERR_INVALID_ARG;
+  if (hu == nullptr || !aligned16(hu) || ldh < view->max_rank || ldh % 4 != 0) return LORA_ERR_INVALID_ARG;
+  const long long hu_bytes = 2LL * T * ldh * 4, g_bytes = view->n_pages * (long long)view->page_elems * 4;
+  if (overlap(hu, hu_bytes, x, (long long)T * ldx * 2) || overlap(hu, hu_bytes, dy, (long long)T * lddy * 2) ||
+      overlap(grad_pool, g_bytes, hu, hu_bytes) || overlap(grad_pool, g_bytes, x, (long long)T * ldx * 2) ||
+      overlap(grad_pool, g_bytes, dy, (long long)T * lddy * 2))
+    return LORA_ERR_INVALID_ARG;
+  if (dx != nullptr && (overlap(dx, (long long)T * lddx * 2, x, (long long)T * ldx * 2) ||
+                        overlap(dx, (long long)T * lddx * 2, dy, (long long)T * lddy * 2) ||
+                        overlap(dx, (long long)T * lddx * 2, hu, hu_bytes) ||
+                        overlap(dx, (long long)T * lddx * 2, grad_pool, g_bytes)))
+    return LORA_ERR_INVALID_ARG;
+  const cudaStream_t s = (cudaStream_t)stream;
+  float* h = hu;
+  float* u = hu + (long long)T * ldh;
+  // h = x A_i^T
+  if ((st = run_segmented(kModeShrink, x, ldx, nullptr, 0, h, ldh, seg, view, dev_err, s)) != LORA_OK) return st;
+  lora_pool_view_t vt = *view;  // the adapters transposed: B_i as the shrink's matrix, A_i as the expand's
+  std::swap(vt.d_in, vt.d_out);
+  {
+    TransposedViews transposed;  // u = dy B_i^T
+    if ((st = run_segmented(kModeShrink, dy, lddy, nullptr, 0, u, ldh, seg, &vt, dev_err, s)) != LORA_OK) return st;
+  }
+  if ((st = launch_grad(x, ldx, dy, lddy, h, u, ldh, grad_pool, seg, view, dev_err, s)) != LORA_OK) return st;
+  if (dx == nullptr) return LORA_OK;
+  TransposedViews transposed;  // dx += s_i u A_i
+  return run_segmented(kModeExpand, nullptr, 0, dx, lddx, u, ldh, seg, &vt, dev_err, s);
 }
 
 lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy, const int32_t* token_adapter,

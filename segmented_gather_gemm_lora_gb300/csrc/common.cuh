@@ -23,6 +23,9 @@ struct DevView {
   int max_rank;
   int d_in;
   int d_out;
+  // 1: the kernels see every adapter transposed (B_i in the role of A_i and the
+  // other way round, d_in and d_out exchanged), for the backward pass
+  int swap_ab;
 };
 
 // Roughly one second at the GB300's clocks: the bound on every spin-wait.
@@ -246,6 +249,11 @@ __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
 __device__ __forceinline__ lora_adapter_desc_t adapter_desc(const DevView& v, int ad) {
   lora_adapter_desc_t d{};
   if (ad >= 0 && ad < v.n_adapters) d = v.adapters[ad];
+  if (v.swap_ab) {
+    const int32_t t = d.a_page0;
+    d.a_page0 = d.b_page0;
+    d.b_page0 = t;
+  }
   return d;
 }
 

@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
         if (crank == 0 && lane == 0) report(a.err, LORA_DERR_BAD_ADAPTER);
         continue;
       }
-      const lora_adapter_desc_t d = v.adapters[ad];
+      const lora_adapter_desc_t d = adapter_desc(v, ad);
       if (d.rank < 1 || d.rank > v.max_rank || d.rank > kHMax) {
         if (crank == 0 && lane == 0) report(a.err, LORA_DERR_BAD_RANK);
         continue;

@@ -32,6 +32,15 @@ int max_active_clusters(const void* func, int block, size_t smem, int cluster_x)
 // Fill a DevView from a validated host view.
 void make_dev_view(const lora_pool_view_t* v, DevView* out);
 
+// While one of these lives on a host thread, the views that thread's launches
+// build see every adapter transposed: B_i in the role of A_i and A_i in the
+// role of B_i (the backward pass runs the shrink over B_i and the expand over
+// A_i); the host view given to them has d_in and d_out exchanged to match.
+struct TransposedViews {
+  TransposedViews();
+  ~TransposedViews();
+};
+
 // The checks every compute call makes on a view (LORA_OK if it passes).
 lora_status_t validate_view(const lora_pool_view_t* v);
 
@@ -84,6 +93,13 @@ lora_status_t launch_gather(int mode, int src, int short_only, const void* x, lo
 // same slices and so compute the same h bit for bit.
 constexpr int kMaxKSplit = 4;
 void shrink_split(int d_in, int* ks, int* klen);
+
+// Gradients of adapters' A and B from a batch's segments (backward.cu):
+// dB_i += s_i h^T dy and dA_i += s_i u^T x over each segment's tokens, added
+// into grad_pool at the elements' pool positions.  h and u by token, fp32.
+lora_status_t launch_grad(const void* x, long long ldx, const void* dy, long long lddy, const float* h,
+                          const float* u, long long ldh, float* grad_pool, const lora_segments_t* seg,
+                          const lora_pool_view_t* view, int32_t* err, cudaStream_t stream);
 
 // Tensor-core path for long tiles.  Eligibility: d_in % 64 == 0 (shrink),
 // d_out % 128 == 0 (expand), pages of at least 128 elements.

@@ -55,6 +55,8 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
 }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// Close this thread's current group of cp.async copies (wait_group counts groups).
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 // ----------------------------------------------------- matrix descriptors --
 

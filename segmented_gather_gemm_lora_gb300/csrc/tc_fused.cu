@@ -432,6 +432,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
       if (lane == 0) mbar_arrive(smem_u32(&slot_empty[q]));
     }
     // nothing may still be landing in shared memory when the CTA ends
+    cp_async_commit();
     cp_async_wait<0>();
     if (lead)
       for (uint32_t gg = gs > kFStages ? gs - kFStages : 0; gg < gs; ++gg)

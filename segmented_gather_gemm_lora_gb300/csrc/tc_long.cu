@@ -381,6 +381,7 @@ __global__ void __launch_bounds__(kSThreads, 1) shrink_tc_kernel(const __grid_co
       ++g;
     }
     // nothing may still be landing in shared memory when the CTA ends
+    cp_async_commit();
     cp_async_wait<0>();
     if (lead) {
       drain_ring(full_tma, g, kSStages);
@@ -791,6 +792,7 @@ __global__ void __launch_bounds__(kEThreads, 1) expand_tc_kernel(const __grid_co
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&uq_empty[qs]));
     }
+    cp_async_commit();
     cp_async_wait<0>();
     if (lead) {
       drain_ring(full_tma, g, kEStages);
