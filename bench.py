@@ -62,6 +62,7 @@ WORKLOAD_TEXT = {
 
 # timed steps of the configurations timed beside the headline (each well under a second)
 OTHER_STEPS = {"tiny": 20000, "decode": 20000, "prefill": 2000, "hetero": 2000}
+BACKWARD_STEPS = 500
 
 
 def parse_args(argv=None):
@@ -676,6 +677,124 @@ def parity_report(gpu_outs, oracle_ys, d_outs):
             "against": "the CPU fp64 oracle on the CPU baseline's sample"}
 
 
+def backward_bytes(batch, pool) -> int:
+    """Bytes one backward call must move at least once: x and dy read, dx read and
+    written (bf16), every distinct adapter's A and B read (bf16) and their fp32
+    gradients read and written."""
+    ids = batch.ids
+    valid = ids >= 0
+    n = int(valid.sum())
+    ranks = pool.ranks[np.unique(ids[valid])].astype(np.int64)
+    elems = int((ranks * (pool.d_in + pool.d_out)).sum())
+    return n * pool.d_in * 2 + n * pool.d_out * 2 + n * pool.d_in * 4 + elems * 2 + elems * 8
+
+
+def run_backward_line(steps, warmup, soak_seconds, world, rank, local):
+    """The backward pass (adapter training) on the prefill-shaped batch: a step is
+    lora_segments_build + lora_sgmv_backward (dA, dB into an fp32 gradient pool, dx
+    in place); inputs rotate over enough sets to exceed 2x L2."""
+    import torch
+
+    from segmented_gather_gemm_lora_gb300 import binding as B
+    from segmented_gather_gemm_lora_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    sets, k = [], 0
+    while True:
+        wl = W.prefill(1000 * rank + k)
+        pool, b = wl.pools[0], wl.batch
+        rng = np.random.default_rng([1000 * rank + k, 9])
+        dy = W._normal_bf16(rng, (b.T, pool.d_out), 1.0)
+        S = dict(view=B.PoolView.from_host(pool, device=dev), x=up(b.x), dy=up(dy),
+                 dx=torch.zeros((b.T, pool.d_in), dtype=torch.bfloat16, device=dev),
+                 grad=torch.zeros(pool.pool.shape, dtype=torch.float32, device=dev),
+                 hu=torch.empty((2 * b.T, 64), dtype=torch.float32, device=dev),
+                 ids=torch.from_numpy(b.ids).to(dev), seg=B.Segments(b.T, device=dev),
+                 T=int((b.ids >= 0).sum()), n_ad=wl.n_adapters,
+                 bytes=backward_bytes(b, pool), flops=3 * algorithmic_flops(b, pool))
+        sets.append(S)
+        k += 1
+        if k >= 2 and sum(x["x"].numel() * 2 + x["dy"].numel() * 2 + x["dx"].numel() * 2 for x in sets) > 2 * l2:
+            break
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(i):
+        S = sets[i % len(sets)]
+        B.lora_segments_build(S["ids"], S["n_ad"], S["seg"], mode=B.LORA_SEG_GROUP, err=err)
+        B.lora_sgmv_backward(S["x"], S["dy"], S["dx"], S["grad"], S["hu"], S["seg"], S["view"], err=err)
+
+    for i in range(max(warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    g_steps = len(sets) * max(1, 32 // len(sets))
+    cap = torch.cuda.Stream(device=dev)
+    graph = torch.cuda.CUDAGraph()
+    launches0 = B.launch_count()
+    with torch.cuda.graph(graph, stream=cap):
+        for i in range(g_steps):
+            step(i)
+    launches_per_step = (B.launch_count() - launches0) / g_steps
+    reps = max(1, steps // g_steps)
+    graph.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_id_of(props))
+    t_end = time.perf_counter() + soak_seconds
+    while time.perf_counter() < t_end:
+        graph.replay()
+        torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    assert int(err.item()) == 0, "device error word %d" % int(err.item())
+    n_steps = reps * g_steps
+    tokens = sum_over_ranks(reps * sum(sets[i % len(sets)]["T"] for i in range(g_steps)), world)
+    bytes_avg = statistics.fmean(sets[i % len(sets)]["bytes"] for i in range(g_steps))
+    flops_avg = statistics.fmean(sets[i % len(sets)]["flops"] for i in range(g_steps))
+    step_s = ms / n_steps / 1e3
+    hbm_peak, tc_peak, peak_kind = read_peaks()
+    achieved = bytes_avg / step_s / 1e9
+    out = {
+        "value": tokens / (ms / 1e3),
+        "unit": UNIT,
+        "steps": n_steps,
+        "ms_per_step": ms / n_steps,
+        "config": {"workload": "backward (adapter training) on the prefill SGMV batch: 32 requests of "
+                               "U{64..512} tokens, 4096->4096, 200 rank-16 adapters, Zipf(1.1); dA, dB into an "
+                               "fp32 gradient pool and dx in place, bf16 x and dy",
+                   "step": "lora_segments_build + lora_sgmv_backward",
+                   "l2": "inputs larger than L2: %d rotating input sets" % len(sets),
+                   "timing": "CUDA graph of %d steps replayed; CUDA events on the launching stream" % g_steps},
+        "roofline": {"bound": "hbm", "kernel": "lora_sgmv_backward (gather, shrink_tc, reduce_partials, "
+                                               "grad_kernel, expand_tc)",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "peak_kind": peak_kind, "traffic": None,
+                     "algorithmic_bytes_per_launch": bytes_avg, "avg_launch_us": step_s * 1e6,
+                     "tflops": flops_avg / step_s / 1e12},
+        "gpu_launches": int(round(launches_per_step * n_steps)),
+        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                   "reasons": clocks["reasons"], "samples": clocks["samples"]},
+    }
+    del sets, graph
+    gc.collect()
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------ CPU oracle --
 
 def oracle_sample(workload: str):
@@ -848,6 +967,8 @@ def main(argv=None):
     if args.workload == "all":
         for name in OTHERS:
             per_config[name] = config_line(name, args, world, rank, local, OTHER_STEPS[name])
+        per_config["backward"] = run_backward_line(BACKWARD_STEPS, args.warmup, args.soak_seconds, world, rank,
+                                                   local)
     h = config_line(head, args, world, rank, local, args.steps)
     out = {
         "metric": METRIC,

@@ -135,10 +135,13 @@ typedef struct {
   int32_t* short_units;   /* [T] */
   int32_t* long_units;    /* [2 * max_long_units] */
   int32_t* scratch;       /* [4 * T + 8]: run starts, run ends, run ids, run positions */
-  float* h_scratch;       /* [T * LORA_MAX_RANK]: lora_apply's rank-r intermediate of
-                             tokens on the tensor-core path, by segment position */
+  float* h_scratch;       /* [T * LORA_MAX_RANK]: the rank-r intermediate of tokens on
+                             the staged tensor-core path (lora_apply_fixed_scratch uses
+                             its own array instead), by segment position */
   float* k_partials;      /* [LORA_KSPLIT_MAX * T * LORA_MAX_RANK]: partial shrink sums of
-                             the tensor-core path, one slab per slice of d_in */
+                             the staged tensor-core path (lora_sgmv_shrink,
+                             lora_sgmv_backward, lora_apply_fixed_scratch), one slab
+                             per slice of d_in */
 } lora_segments_t;
 
 /** Slices of d_in the tensor-core shrink splits a tile into, at most. */
@@ -196,7 +199,11 @@ lora_status_t lora_sgmv_expand(const float* h, int64_t ldh, void* y, int64_t ldy
 
 /**
  * Fused shrink -> scale -> expand over the segments; h never leaves the chip
- * ("Multi-LoRA serving: ...", TL;DR: Y += sum_i X_i A_i B_i in a single pass).
+ * ("Multi-LoRA serving: ...", TL;DR: Y += sum_i X_i A_i B_i in a single pass):
+ * short segments run on the gather kernel, the 128-token tiles of long ones on
+ * the fused tensor-core kernel, which exchanges h between the CTAs of a cluster
+ * through distributed shared memory.  It uses the segment buffer's index
+ * arrays and work counter, not h_scratch or k_partials.
  *     y[t, n] = bf16( y[t, n] + sum_j (s_i * sum_k x[t,k] A_i[j,k]) * B_i[j, n] ).
  * x must not overlap y.
  */
@@ -295,11 +302,13 @@ lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy,
  * lora_apply for callers that cannot allocate device memory.  (The pages have
  * no counterpart: this is a deployment convenience of this library.)
  *
- * lora_apply keeps the rank-r intermediate of long segments in seg->h_scratch,
- * a workspace the caller sizes and allocates.  Callers whose device memory is
- * planned once by a host runtime, and who can therefore neither size nor
- * request an extra workspace per call, use this entry point instead: the
- * intermediate goes to a fixed array of LORA_FIXED_SCRATCH_MAX_TOKENS x
+ * It computes lora_apply's result, bit for bit, through the staged
+ * tensor-core kernels (a shrink grid, then an expand grid), which keep the
+ * rank-r intermediate of long segments in global memory between the two: in
+ * seg->h_scratch when the caller runs those stages itself.  Callers whose
+ * device memory is planned once by a host runtime, and who can therefore
+ * neither size nor request an extra workspace per call, use this entry point:
+ * the intermediate goes to a fixed array of LORA_FIXED_SCRATCH_MAX_TOKENS x
  * LORA_MAX_RANK fp32 values (4 MiB) that is part of the library's device image
  * (every GPU that loads the library holds it until the process exits).  It
  * allocates nothing.

@@ -1,14 +1,17 @@
 // lora_apply_fixed_scratch: lora_apply whose scratch lives in the library.
 //
-// lora_apply keeps the rank-r intermediate of tokens on the tensor-core path
-// in seg->h_scratch, memory the caller sized and allocated.  Some callers can
-// neither size nor request such a workspace: their device memory is planned
-// once, at start-up, by a host runtime that hands the library only the
-// activation, weight and segment buffers, and they cannot call cudaMalloc
-// afterwards.  For them this entry point takes the intermediate from a
-// fixed-size array that is part of the library's own device image: it is
-// created when the library is loaded onto a GPU and stays there until the
-// process exits.  Nothing is allocated per call.
+// The staged tensor-core path of lora_apply (a shrink grid, then an expand
+// grid) keeps the rank-r intermediate of long segments in global memory
+// between the two, in seg->h_scratch, memory the caller sized and allocated.
+// Some callers can neither size nor request such a workspace: their device
+// memory is planned once, at start-up, by a host runtime that hands the
+// library only the activation, weight and segment buffers, and they cannot
+// call cudaMalloc afterwards.  For them this entry point runs that staged path
+// with the intermediate in a fixed-size array that is part of the library's
+// own device image: it is created when the library is loaded onto a GPU and
+// stays there until the process exits.  Nothing is allocated per call.  The
+// result equals lora_apply's bit for bit (the staged and fused tensor-core
+// kernels split and sum the same way).
 #include "internal.h"
 
 namespace {

@@ -1,9 +1,9 @@
 """lora_apply_fixed_scratch: the entry point for callers that cannot allocate device
 memory (their device memory is planned once by a host runtime, so they cannot size
-or request the workspace lora_apply keeps its intermediate in).  It must give the
-same outputs as lora_apply, bit for bit, call after call, although every call reuses
-the one fixed array inside the library, and it must not touch the caller's
-h_scratch (passed as NULL here, so a call that still used it would fail).
+or request the workspace the staged tensor-core path keeps its intermediate in).  It
+must give the same outputs as lora_apply, bit for bit, call after call, although
+every call reuses the one fixed array inside the library, and it must not touch the
+caller's h_scratch (passed as NULL here, so a call that still used it would fail).
 
 This file is collected last on purpose: if it fails, a run that stops at the first
 failure has already run every other test.
