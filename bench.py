@@ -73,9 +73,10 @@ def parse_args(argv=None):
                         "20000 for a small configuration timed alone)")
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["all"] + sorted(WORKLOAD_TEXT), default="all",
+    p.add_argument("--workload", choices=["all", "backward"] + sorted(WORKLOAD_TEXT), default="all",
                    help="all (default): the 13B forward as the headline, every other "
-                        "configuration under per_config; or one configuration alone")
+                        "configuration under per_config; or one configuration alone "
+                        "(backward: the adapter-training backward pass on the prefill batch)")
     p.add_argument("--cpu-seconds", type=float, default=5.0,
                    help="bounded CPU work per configuration for the oracle baseline (0 disables it)")
     p.add_argument("--e2e-steps", type=int, default=None,
@@ -85,7 +86,7 @@ def parse_args(argv=None):
     args = p.parse_args(argv)
     head = HEADLINE if args.workload == "all" else args.workload
     if args.steps is None:
-        args.steps = 20 if head == "mixed13b" else 20000
+        args.steps = 20 if head == "mixed13b" else BACKWARD_STEPS if head == "backward" else 20000
     return args
 
 
@@ -969,13 +970,16 @@ def main(argv=None):
             per_config[name] = config_line(name, args, world, rank, local, OTHER_STEPS[name])
         per_config["backward"] = run_backward_line(BACKWARD_STEPS, args.warmup, args.soak_seconds, world, rank,
                                                    local)
-    h = config_line(head, args, world, rank, local, args.steps)
+    if head == "backward":
+        h = run_backward_line(args.steps, args.warmup, args.soak_seconds, world, rank, local)
+    else:
+        h = config_line(head, args, world, rank, local, args.steps)
     out = {
         "metric": METRIC,
         "value": h["value"],
         "unit": UNIT,
         "n_gpus": world,
-        "steps": args.steps,
+        "steps": h.get("steps", args.steps),
         "warmup": args.warmup,
         "ms_per_step": h["ms_per_step"],
         "higher_is_better": True,

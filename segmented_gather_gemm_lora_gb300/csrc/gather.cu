@@ -41,6 +41,7 @@
 #include <algorithm>
 #include <cstring>
 
+#include "chunk_mma.cuh"
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -54,15 +55,7 @@ constexpr int kGProd2 = kGCons + 2;  // the second producer warp
 constexpr int kGProds = 2;           // producer warps: a stage's copies alternate between them
 constexpr int kGThreads = 32 * (kGCons + 3);
 constexpr int kGConsThreads = 32 * kGCons;
-constexpr int kNT = 4;  // tokens per group
-constexpr int kHMax = LORA_MAX_RANK;
 constexpr int kMaxCluster = 8;
-constexpr int kSub = 512;       // columns per sub-slice (one 1 KB row)
-constexpr int kChunkRows = 16;  // adapter rows per chunk
-constexpr int kRowBytes = kSub * 2;
-// Rows of a stage sit 1040 bytes apart (1 KB plus 16): the eight rows one
-// ldmatrix reads then fall in eight different bank groups.
-constexpr int kRowStride = kRowBytes + 16;
 constexpr int kStages = 4;
 constexpr int kStageBytes = (kChunkRows + kNT) * kRowStride;  // 20.3 KB
 constexpr int kMaxPgSlots = 512;  // page-list slots of one adapter cached in shared memory
@@ -173,143 +166,17 @@ struct GatherArgs {
   long long probe;  // > 0: the timeout probe's wait limit in cycles (lora_debug_wait_probe)
 };
 
-// ------------------------------------------------ warp-level tensor-core tiles --
-//
-// The chunk arithmetic runs on mma.sync m16n8k16 (bf16 operands, fp32
-// accumulators): one instruction is 2048 multiply-adds, where a CUDA-core loop
-// spends an instruction or more per adapter element.  Operands come from the
-// staged rows with ldmatrix.
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr) : "memory");
-}
-// d (16 x 8 fp32, row-major over lanes) += a (16 x 16 bf16) . b (16 x 8 bf16)
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Shrink of one staged chunk: D[j, t] += sum_k A_i[j0 + j, k] x[t, k] over this
-// warp's 64 columns of the sub-slice (warp w owns columns 64 w .. 64 w + 63), as
-// four k16 steps in column order.  d is the lane's part of the 16 x 8 tile:
-// rows (lane / 4, lane / 4 + 8), tokens (2 (lane % 4), 2 (lane % 4) + 1).  Rows
-// past the chunk and tokens past the group give entries nobody reads; columns
-// past the sub-slice are masked to zero in both operands.  Each entry is a fixed
-// function of its own adapter row and token row.
-__device__ __forceinline__ void shrink_chunk(uint32_t sbase, int wsub, int ntok, float (&d)[4], int warp, int lane) {
-  const int kw = warp * 64;
-  if (kw >= wsub) return;
-  const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = (lane >> 4) * 8;
-  const int xrow = min(lane & 7, ntok - 1), xcol = ((lane >> 3) & 1) * 8;
-  const uint32_t abase = sbase + (uint32_t)(arow * kRowStride + (kw + acol) * 2);
-  const uint32_t xbase = sbase + (uint32_t)((kChunkRows + xrow) * kRowStride + (kw + xcol) * 2);
-#pragma unroll
-  for (int st = 0; st < 4; ++st) {
-    const int k0 = kw + 16 * st;
-    if (k0 >= wsub) break;
-    uint32_t a0, a1, a2, a3, b0, b1;
-    ldsm_x4(abase + 32 * st, a0, a1, a2, a3);
-    ldsm_x2(xbase + 32 * st, b0, b1);
-    if (k0 + 8 >= wsub) a2 = a3 = b1 = 0u;  // columns k0 + 8 .. k0 + 15 lie past the sub-slice
-    mma16816(d, a0, a1, a2, a3, b0, b1);
-  }
-}
-
-// Expand of one staged chunk: Y[n, t] += sum_j B_i[j0 + j, n] h[t, j0 + j] over
-// the chunk's rows, for this warp's 64 columns of the sub-slice (four n16
-// tiles; acc[i] is the lane's part of tile i: columns 16 i + lane / 4 (+ 8),
-// tokens 2 (lane % 4) (+ 1)).  h enters as bf16 hi + lo parts (two MMAs per
-// tile, hi first), which keeps the intermediate at about fp32 accuracy.  Rows
-// past the chunk are masked to zero in both operands.  The sub-slice's last
-// chunk adds y0 and writes y through the warp's scratch rows.
+// The chunk arithmetic (chunk_mma.cuh) over a stage: adapter rows first, the
+// group's token rows after the chunk's kChunkRows rows.
 __device__ __forceinline__ void expand_chunk(uint16_t* ybase, long long ldy, float* yf, long long ldyf,
                                              uint32_t sbase, const uint8_t* sb, const float* hs, float* scr,
                                              float (&acc)[4][4], const GRec& rc, bool ok, int warp, int lane) {
-  const int nw = warp * 64;
   const int wsub = rc.nvec * 8;
-  if (nw >= wsub) return;
-  if (rc.flags & kFFirst) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  }
-  const int g = lane >> 2, t = lane & 3;
-  const int nrows = rc.nrows;
-  // h fragment of token g: rows 2t, 2t + 1 (b0) and 2t + 8, 2t + 9 (b1) of the chunk
-  uint32_t bh0 = 0u, bh1 = 0u, bl0 = 0u, bl1 = 0u;
-  if (g < rc.ntok) {
-    const float* hrow = hs + g * kHMax + rc.j0;
-    float hv[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = 2 * t + (e & 1) + 8 * (e >> 1);
-      hv[e] = j < nrows ? hrow[j] : 0.f;
-    }
-    bh0 = pack_bf16x2(hv[0], hv[1]);
-    bh1 = pack_bf16x2(hv[2], hv[3]);
-    bl0 = pack_bf16x2(hv[0] - bf_lo(bh0), hv[1] - bf_hi(bh0));
-    bl1 = pack_bf16x2(hv[2] - bf_lo(bh1), hv[3] - bf_hi(bh1));
-  }
-  // rows of the lane's A entries: 2t, 2t + 1 (a0, a1) and 2t + 8, 2t + 9 (a2, a3)
-  const uint32_t m01 = (2 * t < nrows ? 0x0000ffffu : 0u) | (2 * t + 1 < nrows ? 0xffff0000u : 0u);
-  const uint32_t m23 = (2 * t + 8 < nrows ? 0x0000ffffu : 0u) | (2 * t + 9 < nrows ? 0xffff0000u : 0u);
-  const int jrow = (lane & 7) + 8 * (lane >> 4), ncol = 8 * ((lane >> 3) & 1);
-  const uint32_t bbase = sbase + (uint32_t)(jrow * kRowStride + (nw + ncol) * 2);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (nw + 16 * i >= wsub) break;
-    uint32_t a0, a1, a2, a3;
-    ldsm_x4_t(bbase + 32 * i, a0, a1, a2, a3);
-    a0 &= m01;
-    a1 &= m01;
-    a2 &= m23;
-    a3 &= m23;
-    mma16816(acc[i], a0, a1, a2, a3, bh0, bh1);
-    mma16816(acc[i], a0, a1, a2, a3, bl0, bl1);
-  }
-  if ((rc.flags & kFLast) && ok) {
-    // the lane's entries into the warp's scratch [token][64 columns], then each
-    // lane writes two adjacent columns of every token
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tok = 2 * t + (e & 1), nn = 16 * i + g + 8 * (e >> 1);
-        if (tok < rc.ntok) scr[tok * 64 + nn] = acc[i][e];
-      }
-    __syncwarp();
-    const int c2 = nw + 2 * lane;
-    if (c2 < wsub) {
-#pragma unroll
-      for (int tk = 0; tk < kNT; ++tk) {
-        if (tk >= rc.ntok) break;
-        const uint32_t y0 = *reinterpret_cast<const uint32_t*>(sb + (kChunkRows + tk) * kRowStride + 2 * c2);
-        const float v0 = scr[tk * 64 + 2 * lane], v1 = scr[tk * 64 + 2 * lane + 1];
-        if (yf != nullptr)  // fp32 output (diagnostic form): the same sums, not rounded to bf16
-          *reinterpret_cast<float2*>(yf + (long long)rc.tok[tk] * ldyf + rc.col0 + c2) =
-              make_float2(bf_lo(y0) + v0, bf_hi(y0) + v1);
-        else
-          *reinterpret_cast<uint32_t*>(ybase + (long long)rc.tok[tk] * ldy + rc.col0 + c2) =
-              pack_bf16x2(bf_lo(y0) + v0, bf_hi(y0) + v1);
-      }
-    }
-    __syncwarp();
-  }
+  if (warp * 64 >= wsub) return;
+  expand_mma(sbase, hs, rc.j0, rc.nrows, rc.ntok, wsub, (rc.flags & kFFirst) != 0, acc, warp, lane);
+  if ((rc.flags & kFLast) && ok)
+    expand_store(ybase, ldy, yf, ldyf, sb + kChunkRows * kRowStride, scr, acc, rc.ntok, rc.tok, rc.col0, wsub, warp,
+                 lane);
 }
 
 __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_constant__ GatherArgs a) {
@@ -780,7 +647,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       const int b = ngroup & 1;
       if (rc.kind == kGShrink) {
         if (rc.flags & kFFirst) sacc[0] = sacc[1] = sacc[2] = sacc[3] = 0.f;
-        shrink_chunk(smem_u32(sb), rc.nvec * 8, rc.ntok, sacc, warp, lane);
+        shrink_chunk(smem_u32(sb), smem_u32(sb) + kChunkRows * kRowStride, rc.nvec * 8, rc.ntok, sacc, warp,
+                     lane);
         if (rc.flags & kFLast) {  // the row block is done: the warp's partial of every row and token
           const int gr = lane >> 2, tq = lane & 3;
 #pragma unroll
