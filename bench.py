@@ -5,8 +5,12 @@ A step is one pass of the whole path over one batch of one configuration:
 
 * tiny, prefill, hetero: lora_segments_build (grouping the batch's tokens by adapter,
   work lists) followed by the step's lora_apply call(s);
-* decode (one token per request): lora_bgmv, every token gathering its own adapter
-  through the page table, shrink + scale + expand in place in y, one kernel;
+* decode (one token per request): lora_bgmv_ex, every token gathering its own adapter
+  through the page table, shrink + scale + expand in place in y, one kernel; the ids
+  and pools are uploaded once, so the calls pass LORA_BGMV_STATIC_ADAPTERS (a call
+  stages its adapters while the call ahead of it finishes);
+* backward (with --workload backward, and under per_config): lora_segments_build +
+  lora_sgmv_backward on the prefill batch;
 * mixed13b (the headline, the largest configuration that fits one GPU): one forward of
   the 13B-shaped mixed batch, one segment build and 40 layers x 7 projections, in four
   grouped calls per layer (lora_apply_multi for q, k, v on their shared input and for
@@ -372,7 +376,8 @@ def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, loca
 
     def run_call(c, ids, seg):
         if bgmv:
-            B.lora_bgmv(c["x"], c["ys"][0], ids, c["views"][0], err=err)
+            # the ids and the pools are uploaded once and never written by a kernel
+            B.lora_bgmv(c["x"], c["ys"][0], ids, c["views"][0], err=err, static_adapters=True)
         elif len(c["views"]) == 1:
             B.lora_apply(c["x"], c["ys"][0], seg, c["views"][0], err=err)
         else:
@@ -562,8 +567,9 @@ def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, loca
     d2h = sum(h.numel() * 2 for _, h in hout) if outs_extra else y_hi - y_lo
 
     grouped = any(len(c["views"]) > 1 for c in sets[0]["calls"])
-    call = "lora_bgmv" if bgmv else ("lora_apply / lora_apply_multi" if grouped else "lora_apply")
-    kernels = "gather_kernel" if bgmv else ", ".join(B.apply_kernel_names())
+    call = "lora_bgmv_ex (LORA_BGMV_STATIC_ADAPTERS)" if bgmv else \
+        ("lora_apply / lora_apply_multi" if grouped else "lora_apply")
+    kernels = "bgmv_kernel" if bgmv else ", ".join(B.apply_kernel_names())
     n_proj = sum(len(c["views"]) for c in sets[0]["calls"])
     out = {
         "value": value,
@@ -575,7 +581,7 @@ def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, loca
             "workload": WORKLOAD_TEXT[name],
             "tokens_per_step": tokens_per_step,
             "segments": "none (one token per request)" if bgmv else ("GROUP" if mode == 0 else "CONTIGUOUS"),
-            "step": ("%d x lora_bgmv" % n_calls) if bgmv else
+            "step": ("%d x lora_bgmv_ex (LORA_BGMV_STATIC_ADAPTERS)" % n_calls) if bgmv else
                     ("lora_segments_build + %d grouped calls over %d projections" % (n_calls, n_proj) if grouped
                      else "lora_segments_build + %d x lora_apply" % n_calls),
             "l2": "inputs larger than L2: %d rotating input sets (%.0f MB in all, L2 %.0f MB)"

@@ -292,11 +292,36 @@ lora_status_t lora_sgmv_backward(const void* x, int64_t ldx, const void* dy, int
  * (the batched gather path for size-1 segments of "Multi-LoRA serving: ...",
  * section "SGMV: the kernel that holds it all up"; MBGMV in "Multi-LoRA
  * Serving in Production", section "S-LoRA: MBGMV and MBGMM Kernels").
- * Same result as lora_apply.
+ * Same arithmetic as lora_apply's short segments: equal to lora_apply bit for
+ * bit when both run at the same cluster width (the width the projection's
+ * slices want, which lora_apply narrows only for batches with more units than
+ * resident clusters).  Views with max_rank <= 16 and d_in, d_out <= 4096 run
+ * on a decode kernel of small CTAs; other views on the gather kernel.
  */
 lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy,
                         const int32_t* token_adapter, int32_t T, const lora_pool_view_t* view,
                         int32_t* dev_err, lora_stream_t stream);
+
+/* lora_bgmv_ex flags. */
+/* token_adapter and the adapter pool (descriptors, page list, pages) were
+ * final before the kernel enqueued just ahead of this call on the stream
+ * started: nothing that kernel does writes them.  The call may then read them,
+ * and stage the adapters' rows, while that kernel is still running; x and y
+ * are still touched only after it has finished.  Host copies into those
+ * buffers, and kernels followed by at least one other kernel before the call,
+ * satisfy this; a lora_pool_load on the same stream directly ahead of the call
+ * does not (put the load on its own stream and wait for it with an event). */
+#define LORA_BGMV_STATIC_ADAPTERS 1u
+
+/**
+ * lora_bgmv with flags (LORA_BGMV_STATIC_ADAPTERS, or 0 for lora_bgmv's
+ * behaviour).  Other bits: LORA_ERR_INVALID_ARG.  The flag takes effect on
+ * the decode kernel (the views lora_bgmv runs there); the gather kernel
+ * ignores it.
+ */
+lora_status_t lora_bgmv_ex(const void* x, int64_t ldx, void* y, int64_t ldy,
+                           const int32_t* token_adapter, int32_t T, const lora_pool_view_t* view,
+                           uint32_t flags, int32_t* dev_err, lora_stream_t stream);
 
 /**
  * lora_apply for callers that cannot allocate device memory.  (The pages have

@@ -31,6 +31,7 @@ LORA_MAX_RANK = 64
 LORA_MAX_ADAPTERS = 32768
 LORA_SHORT_MAX_TOKENS = 8
 LORA_TILE_M = 128
+LORA_BGMV_STATIC_ADAPTERS = 1
 LORA_SEG_GROUP = 0
 LORA_SEG_CONTIGUOUS = 1
 LORA_FIXED_SCRATCH_MAX_TOKENS = 16384
@@ -48,6 +49,7 @@ EXPORTED = (
     "lora_sgmv_backward",
     "lora_apply_fixed_scratch",
     "lora_bgmv",
+    "lora_bgmv_ex",
     "lora_pool_pages_needed",
     "lora_status_string",
     "lora_abi_version",
@@ -145,6 +147,8 @@ def lib():
         L.lora_apply_fixed_scratch.argtypes = [vp, i64, vp, i64, seg_p, view_p, vp, vp]
         L.lora_bgmv.restype = i32
         L.lora_bgmv.argtypes = [vp, i64, vp, i64, vp, i32, view_p, vp, vp]
+        L.lora_bgmv_ex.restype = i32
+        L.lora_bgmv_ex.argtypes = [vp, i64, vp, i64, vp, i32, view_p, ctypes.c_uint32, vp, vp]
         L.lora_pool_pages_needed.restype = i64
         L.lora_pool_pages_needed.argtypes = [i32, i32, i32, i32]
         L.lora_status_string.restype = ctypes.c_char_p
@@ -380,10 +384,16 @@ def launch_count() -> int:
 
 
 def lora_bgmv(x: torch.Tensor, y: torch.Tensor, token_adapter: torch.Tensor, view: PoolView,
-              err: Optional[torch.Tensor] = None, stream=None):
+              err: Optional[torch.Tensor] = None, stream=None, static_adapters: bool = False):
+    """static_adapters: lora_bgmv_ex with LORA_BGMV_STATIC_ADAPTERS (see include/lora_sgmv.h)."""
     T = int(token_adapter.numel())
-    _check(lib().lora_bgmv(_ptr(x), _ld(x), _ptr(y), _ld(y), _ptr(token_adapter), T,
-                           ctypes.byref(view.c), _ptr(err), _stream(stream)), "lora_bgmv")
+    if static_adapters:
+        _check(lib().lora_bgmv_ex(_ptr(x), _ld(x), _ptr(y), _ld(y), _ptr(token_adapter), T, ctypes.byref(view.c),
+                                  LORA_BGMV_STATIC_ADAPTERS, _ptr(err), _stream(stream)), "lora_bgmv_ex")
+    else:
+        _check(lib().lora_bgmv(_ptr(x), _ld(x), _ptr(y), _ld(y), _ptr(token_adapter), T,
+                               ctypes.byref(view.c), _ptr(err), _stream(stream)), "lora_bgmv")
+
 
 
 # ---------------------------------------------------------- pool residency --

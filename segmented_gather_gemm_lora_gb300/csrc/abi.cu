@@ -453,6 +453,13 @@ lora_status_t lora_sgmv_backward(const void* x, int64_t ldx, const void* dy, int
 
 lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy, const int32_t* token_adapter,
                         int32_t T, const lora_pool_view_t* view, int32_t* dev_err, lora_stream_t stream) {
+  return lora_bgmv_ex(x, ldx, y, ldy, token_adapter, T, view, 0u, dev_err, stream);
+}
+
+lora_status_t lora_bgmv_ex(const void* x, int64_t ldx, void* y, int64_t ldy, const int32_t* token_adapter,
+                           int32_t T, const lora_pool_view_t* view, uint32_t flags, int32_t* dev_err,
+                           lora_stream_t stream) {
+  if (flags & ~LORA_BGMV_STATIC_ADAPTERS) return LORA_ERR_INVALID_ARG;
   lora_status_t st = check_view(view);
   if (st != LORA_OK) return st;
   if (T < 0) return LORA_ERR_INVALID_ARG;
@@ -461,6 +468,9 @@ lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy, const 
   if (T > 0 && token_adapter == nullptr) return LORA_ERR_INVALID_ARG;
   if (T > 0 && overlap(x, (long long)T * ldx * 2, y, (long long)T * ldy * 2)) return LORA_ERR_INVALID_ARG;
   if (T == 0) return LORA_OK;
+  if (bgmv_decode_ok(view, T))
+    return launch_bgmv(x, ldx, y, ldy, token_adapter, T, view, (flags & LORA_BGMV_STATIC_ADAPTERS) ? 1 : 0, dev_err,
+                       (cudaStream_t)stream);
   return launch_gather(kModeApply, kSrcTokens, 0, x, ldx, y, ldy, nullptr, 0, nullptr, token_adapter, T, view,
                        dev_err, (cudaStream_t)stream);
 }

@@ -1,0 +1,335 @@
+// Decode kernel: one token per thread-block cluster, for small adapters.
+//
+// "Multi-LoRA serving: the single translator with a thousand glossaries",
+// section "SGMV: the kernel that holds it all up" (size-one segments take a
+// batched gather path), and "Multi-LoRA Serving in Production", section
+// "S-LoRA: MBGMV and MBGMM Kernels" (the decode form: every token gathers its
+// own adapter, heterogeneous ranks unpadded).
+//
+// A decode call moves little (an adapter slice and a few KB of activations per
+// CTA), so its time is a chain of latencies: the grid's start, the token's
+// adapter id, its descriptor, its page list, the rows, the shrink, the cluster
+// exchange, the expand.  This kernel shortens that chain and lets consecutive
+// calls overlap:
+//   - small CTAs (4 warps, about 22 KB of shared memory), so that the next
+//     call's CTAs are resident, with their set-up done, while this call runs;
+//   - no record pipeline: a CTA holds its whole adapter slice, one chunk of at
+//     most 16 rows, so every copy is issued as soon as the page list is read,
+//     and B's rows are prefetched into L2 then and copied into the same buffer
+//     once the shrink is done with A's;
+//   - optionally (LORA_BGMV_STATIC_ADAPTERS) the adapter chain and A's copies
+//     run before the kernel ahead of it on the stream has finished, and only
+//     x, y0 and y wait for it.
+//
+// Work decomposition and arithmetic are those of the gather kernel at cluster
+// width C: CTA c owns slice c of d_in (shrink) and of d_out (expand), each at
+// most one 512-column sub-slice; the chunk arithmetic is chunk_mma.cuh's, the
+// eight 64-column blocks of a sub-slice taken two per warp; each CTA adds its
+// blocks' partials in block order and pushes the sum to every CTA of the
+// cluster, which add the C partials in CTA order.  So a token's output is the
+// gather kernel's at the same cluster width, bit for bit.
+#include <algorithm>
+#include <cstring>
+
+#include "chunk_mma.cuh"
+#include "common.cuh"
+#include "internal.h"
+
+namespace lora {
+
+namespace {
+
+constexpr int kDThreads = 128;
+constexpr int kDWarps = kDThreads / 32;
+constexpr int kDMaxRank = kChunkRows;  // the adapter's rows fit one chunk
+constexpr int kDMaxCluster = 8;
+constexpr int kDMaxPg = 128;  // page-list slots of one adapter cached in shared memory (A's, then B's)
+static_assert(kSubBlocks == 2 * kDWarps, "two 64-column blocks per warp");
+
+// shared memory: adapter rows (A, then B) and the token's y0 row after them;
+// the x row; page cache; the blocks' partials; the cluster's partials; h;
+// each warp's output scratch; the verdict; four mbarriers
+constexpr size_t kDOffBuf = 0;
+constexpr size_t kDOffY0 = kDOffBuf + (size_t)kChunkRows * kRowStride;
+constexpr size_t kDOffX = kDOffY0 + kRowStride;
+constexpr size_t kDOffPg = kDOffX + kRowStride;
+constexpr size_t kDOffPw = kDOffPg + kDMaxPg * sizeof(int);
+constexpr size_t kDOffRecv = kDOffPw + kSubBlocks * kDMaxRank * sizeof(float);
+constexpr size_t kDOffHs = kDOffRecv + kDMaxCluster * kDMaxRank * sizeof(float);
+constexpr size_t kDOffScr = kDOffHs + kHMax * sizeof(float);
+constexpr size_t kDOffInfo = kDOffScr + kDWarps * 64 * sizeof(float);
+constexpr size_t kDOffBars = kDOffInfo + 8 * sizeof(int);
+constexpr size_t kDSmem = kDOffBars + 4 * sizeof(uint64_t);
+static_assert(kDOffY0 % 16 == 0 && kDOffX % 16 == 0 && kDOffBars % 8 == 0, "copy destinations and barriers");
+
+struct BgmvArgs {
+  const uint16_t* x;
+  long long ldx;
+  uint16_t* y;
+  long long ldy;
+  const int32_t* ids;
+  DevView v;
+  int32_t* err;
+  int early;        // the adapter chain may run before the predecessor finishes
+  long long probe;  // > 0: the timeout probe's wait limit in cycles
+};
+
+__device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Row j's part [e, e + w) of a paged matrix whose page-list slots (relative to
+// the matrix's first) are cached in pg: one bulk copy per page the run touches,
+// into dst, completing on bar; or, with bar == 0, an L2 prefetch of the same bytes.
+__device__ __forceinline__ void copy_run(const DevView& v, const int* pg, long long e, int w, uint32_t dst,
+                                         uint32_t bar) {
+  const int shift = v.page_shift;
+  const long long pmask = (1LL << shift) - 1;
+  for (int rem = w; rem > 0;) {
+    const long long off = e & pmask;
+    const long long page = pg[e >> shift];
+    const int n = (int)min((long long)rem, (1LL << shift) - off);
+    const uint16_t* src = v.pool + (page << shift) + off;
+    if (bar != 0u) bulk_g2s(dst, src, (uint32_t)n * 2, bar);
+    else prefetch_l2(src, (uint32_t)n * 2);
+    e += n;
+    dst += (uint32_t)n * 2;
+    rem -= n;
+  }
+}
+
+__global__ void __launch_bounds__(kDThreads) bgmv_kernel(const __grid_constant__ BgmvArgs a) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  uint8_t* const buf = sm + kDOffBuf;
+  const uint8_t* const y0row = sm + kDOffY0;
+  int* const pg = reinterpret_cast<int*>(sm + kDOffPg);
+  float* const pw = reinterpret_cast<float*>(sm + kDOffPw);
+  float* const recv = reinterpret_cast<float*>(sm + kDOffRecv);
+  float* const hs = reinterpret_cast<float*>(sm + kDOffHs);
+  float* const scr = reinterpret_cast<float*>(sm + kDOffScr);
+  int* const info = reinterpret_cast<int*>(sm + kDOffInfo);
+  uint64_t* const bars = reinterpret_cast<uint64_t*>(sm + kDOffBars);
+  const uint32_t bar_xy = smem_u32(&bars[0]);    // x and y0 rows
+  const uint32_t bar_a = smem_u32(&bars[1]);     // A's rows
+  const uint32_t bar_b = smem_u32(&bars[2]);     // B's rows
+  const uint32_t bar_recv = smem_u32(&bars[3]);  // every CTA's partial h
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t crank = cluster_ctarank(), C = cluster_nctarank();
+  const int t = (int)cluster_id_x();  // the token
+  const DevView& v = a.v;
+
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    fence_mbar_init();
+    info[0] = 0;
+    info[4] = 0;
+  }
+  // every barrier of every CTA initialised before any peer stores into it
+  cluster_sync();
+  bool ok = true;
+  if (a.probe > 0) {  // the timeout probe: every CTA takes the exit of a wait that ran out
+    __shared__ uint64_t probe_bar;
+    __shared__ int probe_ok;
+    if (tid == 0) probe_ok = wait_probe(&probe_bar, a.probe) ? 1 : 0;
+    __syncthreads();
+    ok = probe_ok != 0;
+  }
+
+  // this CTA's slices, cut as the gather kernel cuts them
+  const int kc = ((v.d_in + (int)C - 1) / (int)C + 7) & ~7;
+  const int nc = ((v.d_out + (int)C - 1) / (int)C + 7) & ~7;
+  const int k0 = min(v.d_in, (int)crank * kc), k1 = min(v.d_in, k0 + kc);
+  const int n0 = min(v.d_out, (int)crank * nc), n1 = min(v.d_out, n0 + nc);
+  const int kw = k1 - k0, nw = n1 - n0;
+
+  if (!a.early) grid_wait();
+  if (warp == 0 && ok) {
+    // The token's adapter: descriptor and every page slot, checked by every CTA
+    // (so all reach the same verdict without talking), then A's rows of this
+    // CTA's slice and an L2 prefetch of B's.  Global loads through L2 only.
+    const int ad = __ldcg(a.ids + t);
+    int bits = 0, active = 0, r = 0, na = 0;
+    float sc = 0.f;
+    if (ad < -1 || ad >= v.n_adapters) {
+      bits = LORA_DERR_BAD_ADAPTER;
+    } else if (ad >= 0) {
+      // four 4-byte loads, in flight together (the descriptor array is only
+      // 4-byte aligned by its type)
+      const int* dp = reinterpret_cast<const int*>(v.adapters + ad);
+      const int d0 = __ldcg(dp), d1 = __ldcg(dp + 1), d2 = __ldcg(dp + 2), d3 = __ldcg(dp + 3);
+      r = d0;
+      sc = __int_as_float(d1);
+      const long long pa = v.swap_ab ? d3 : d2, pb = v.swap_ab ? d2 : d3;
+      if (r < 1 || r > v.max_rank || r > kDMaxRank) {
+        bits = LORA_DERR_BAD_RANK;
+      } else {
+        const long long P = 1LL << v.page_shift;
+        na = (int)(((long long)r * v.d_in + P - 1) >> v.page_shift);
+        const int nb = (int)(((long long)r * v.d_out + P - 1) >> v.page_shift);
+        int mine = 0;
+        for (int i = lane; i < na + nb; i += 32) {  // na + nb <= kDMaxPg (the host checked max_rank)
+          const long long slot = i < na ? pa + i : pb + (i - na);
+          const int p = (slot < 0 || slot >= v.n_page_list) ? -1 : __ldcg(v.page_list + slot);
+          if (p < 0 || p >= v.n_pages) mine = 1;
+          pg[i] = p;
+        }
+        if (__any_sync(0xffffffffu, mine)) bits = LORA_DERR_BAD_PAGE;
+        else active = 1;
+      }
+    }
+    if (lane == 0) info[4] = crank == 0 ? bits : 0;  // reported once the predecessor has finished
+    __syncwarp();  // the page cache, written by every lane, before any lane reads it
+    if (active) {
+      if (lane == 0) mbar_arrive_expect_tx(bar_a, (uint32_t)(r * kw * 2));
+      __syncwarp();
+      if (lane < r && kw > 0)
+        copy_run(v, pg, (long long)lane * v.d_in + k0, kw, smem_u32(buf + lane * kRowStride), bar_a);
+      if (lane < r && nw > 0) copy_run(v, pg + na, (long long)lane * v.d_out + n0, nw, 0u, 0u);
+    }
+    if (lane == 0) {
+      info[0] = active;
+      info[1] = r;
+      info[2] = __float_as_int(sc);
+      info[3] = na;
+    }
+  }
+  if (a.early) grid_wait();
+  grid_release();
+  if (tid == 0 && ok && info[4] != 0) report(a.err, info[4]);
+  if (warp == 1 && lane == 0 && ok) {  // the token's x and y0 slices; they do not depend on the adapter
+    mbar_arrive_expect_tx(bar_xy, (uint32_t)((kw + nw) * 2));
+    if (kw > 0) bulk_g2s(smem_u32(sm + kDOffX), a.x + (long long)t * a.ldx + k0, (uint32_t)kw * 2, bar_xy);
+    if (nw > 0) bulk_g2s(smem_u32(y0row), a.y + (long long)t * a.ldy + n0, (uint32_t)nw * 2, bar_xy);
+  }
+  __syncthreads();
+  const bool xy_issued = ok;
+  const bool active = ok && info[0] != 0;
+  bool b_issued = false;
+  const int r = info[1];
+  if (active) {
+    const float sc = __int_as_float(info[2]);
+    const int na = info[3];
+    ok = __syncthreads_and(mbar_wait(bar_a, 0) && mbar_wait(bar_xy, 0)) != 0;
+    if (ok) {  // shrink: 64-column blocks 2 warp and 2 warp + 1; the token is column 0 of the tile
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int b = 2 * warp + h;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        shrink_chunk(smem_u32(buf), smem_u32(sm + kDOffX), kw, 1, d, b, lane);
+        if ((lane & 3) == 0) {
+          const int g = lane >> 2;
+          if (g < r) pw[b * kDMaxRank + g] = d[0];
+          if (g + 8 < r) pw[b * kDMaxRank + g + 8] = d[2];
+        }
+      }
+    }
+    __syncthreads();  // every block's partial is in; A's rows are free
+    if (ok && warp == 0) {  // B's rows into the same buffer (mostly from L2 by now)
+      if (lane == 0) mbar_arrive_expect_tx(bar_b, (uint32_t)(r * nw * 2));
+      __syncwarp();
+      if (lane < r && nw > 0)
+        copy_run(v, pg + na, (long long)lane * v.d_out + n0, nw, smem_u32(buf + lane * kRowStride), bar_b);
+    }
+    b_issued = ok;
+    // this CTA's partial (the blocks' partials in block order), pushed to every
+    // CTA of the cluster, this one included; summed there in CTA order
+    const int q4 = (r + 3) >> 2;
+    if (ok && tid == 0) mbar_arrive_expect_tx(bar_recv, C * (uint32_t)q4 * 16u);
+    if (ok && tid < q4) {
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int b = 0; b < kSubBlocks; ++b) {
+        const float4 p = *reinterpret_cast<const float4*>(pw + b * kDMaxRank + 4 * tid);
+        sum.x += p.x;
+        sum.y += p.y;
+        sum.z += p.z;
+        sum.w += p.w;
+      }
+      const uint32_t dst = smem_u32(recv + crank * kDMaxRank + 4 * tid);
+      for (uint32_t c = 0; c < C; ++c) st_async_v4(mapa(dst, c), sum, mapa(bar_recv, c));
+    }
+    bool got = true;
+    if (ok && tid < r) {
+      got = mbar_wait(bar_recv, 0);
+      float s = 0.f;
+      for (uint32_t c = 0; c < C; ++c) s += recv[c * kDMaxRank + tid];
+      hs[tid] = sc * s;
+    }
+    ok = __syncthreads_and(ok && got) != 0;
+  }
+  // Every partial this CTA receives has landed (or it gave up): peers may leave
+  // once all have arrived here.
+  cluster_arrive();
+  if (active && ok) {
+    ok = __syncthreads_and(mbar_wait(bar_b, 0)) != 0;
+    if (ok) {
+      const int tok[kNT] = {t, t, t, t};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int b = 2 * warp + h;
+        if (b * 64 >= nw) break;
+        float acc[4][4];
+        expand_mma(smem_u32(buf), hs, 0, r, 1, nw, true, acc, b, lane);
+        expand_store(a.y, a.ldy, nullptr, 0, y0row, scr + warp * 64, acc, 1, tok, n0, nw, b, lane);
+      }
+    }
+  }
+  if (!ok) {
+    // A wait ran out: no output was written.  Copies still in flight into this
+    // CTA's shared memory get a second bounded wait before it leaves.
+    if (tid == 0) {
+      if (xy_issued) mbar_wait(bar_xy, 0);
+      if (active) mbar_wait(bar_a, 0);
+      if (b_issued) mbar_wait(bar_b, 0);
+      report(a.err, LORA_DERR_TIMEOUT);
+    }
+  }
+  cluster_wait();
+}
+
+// Cluster width of the gather kernel's slices for a view: one CTA per 512
+// columns of the wider side, at most eight.
+int slice_width(const lora_pool_view_t* v) {
+  const int d = std::max(v->d_in, v->d_out);
+  return std::min(std::max((d + kSub - 1) / kSub, 1), kDMaxCluster);
+}
+
+}  // namespace
+
+bool bgmv_decode_ok(const lora_pool_view_t* v, int T) {
+  if (T < 1 || T > (1 << 20) || v->max_rank > kDMaxRank) return false;
+  const int C = slice_width(v);
+  const int kc = ((v->d_in + C - 1) / C + 7) & ~7, nc = ((v->d_out + C - 1) / C + 7) & ~7;
+  if (kc > kSub || nc > kSub) return false;
+  const long long P = v->page_elems;
+  const long long na = ((long long)v->max_rank * v->d_in + P - 1) / P;
+  const long long nb = ((long long)v->max_rank * v->d_out + P - 1) / P;
+  return na + nb <= kDMaxPg;
+}
+
+lora_status_t launch_bgmv(const void* x, long long ldx, void* y, long long ldy, const int32_t* ids, int T,
+                          const lora_pool_view_t* view, int early, int32_t* err, cudaStream_t stream) {
+  BgmvArgs a;
+  memset(&a, 0, sizeof(a));
+  a.x = static_cast<const uint16_t*>(x);
+  a.ldx = ldx;
+  a.y = static_cast<uint16_t*>(y);
+  a.ldy = ldy;
+  a.ids = ids;
+  make_dev_view(view, &a.v);
+  a.err = err;
+  a.early = early;
+  a.probe = wait_probe_cycles();
+  const int C = slice_width(view);
+  return launch_pdl((const void*)bgmv_kernel, dim3((unsigned)(T * C)), dim3(kDThreads), kDSmem, stream, C, &a) ==
+                 cudaSuccess
+             ? LORA_OK
+             : LORA_ERR_CUDA;
+}
+
+}  // namespace lora

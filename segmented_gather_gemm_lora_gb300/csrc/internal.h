@@ -86,6 +86,14 @@ lora_status_t launch_gather(int mode, int src, int short_only, const void* x, lo
                             const int32_t* token_adapter, int T, const lora_pool_view_t* view,
                             int32_t* err, cudaStream_t stream, float* yf = nullptr, long long ldyf = 0);
 
+// Decode kernel (bgmv.cu): one token per cluster, small CTAs, for views with
+// max_rank <= 16 whose slices fit one 512-column sub-slice (d_in, d_out <=
+// 4096) and whose adapters span at most 128 page-list slots.  early: read the
+// ids and the pool before the predecessor grid finishes (LORA_BGMV_STATIC_ADAPTERS).
+bool bgmv_decode_ok(const lora_pool_view_t* v, int T);
+lora_status_t launch_bgmv(const void* x, long long ldx, void* y, long long ldy, const int32_t* ids, int T,
+                          const lora_pool_view_t* view, int early, int32_t* err, cudaStream_t stream);
+
 // Slices of d_in the tensor-core shrink splits a tile into (ks, each of klen
 // columns, a multiple of 64; the last may be shorter): about 512 columns each,
 // at most kMaxKSplit.  A function of d_in alone, so a token's h does not depend

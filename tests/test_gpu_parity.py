@@ -309,11 +309,90 @@ def test_bgmv_parity(name):
 
 
 def test_bgmv_equals_apply_bitwise():
+    """The decode kernel runs the gather kernel's arithmetic at the cluster width the
+    projection's slices want; lora_apply's gather kernel keeps that width for a batch of
+    a dozen tokens, so the two agree bit for bit (with repeated adapters and -1 ids)."""
     wl = W.decode(1)
     pool = wl.pools[0]
-    yb, _ = run_bgmv(wl.batch, pool)
-    ya, _, _ = run_apply(wl.batch, pool, B.LORA_SEG_GROUP, wl.n_adapters)
+    ids = wl.batch.ids[:12].copy()
+    ids[3] = ids[7]
+    ids[5] = -1
+    b = W.Batch(x=wl.batch.x[:12], y0=wl.batch.y0[:12], ids=ids, d_in=wl.batch.d_in, d_out=wl.batch.d_out)
+    yb, eb = run_bgmv(b, pool)
+    ya, ea, _ = run_apply(b, pool, B.LORA_SEG_GROUP, wl.n_adapters)
+    assert eb == ea == 0
     assert np.array_equal(ya, yb)
+
+
+def test_bgmv_static_adapters_chain_in_graph():
+    """With LORA_BGMV_STATIC_ADAPTERS the decode kernel reads the ids and the pool, and
+    stages the adapters, before the kernel ahead of it has finished, but x and y only
+    after.  Four calls back to back in one CUDA graph, each reading the previous call's
+    y as its x, equal the same chain run call by call without the flag and with a
+    synchronisation in between, bit for bit, replay after replay; the first call also
+    matches the oracle."""
+    rng = np.random.default_rng(83)
+    d = 4096
+    pool = W.build_pool(rng, d, d, [16, 8, 16, 4, 12, 16, 1, 16] * 3, max_rank=16)
+    ids = rng.integers(-1, pool.n_adapters, size=64).astype(np.int32)
+    batch = W.make_batch(rng, ids, d, d)
+    view = B.PoolView.from_host(pool)
+    x0 = to_dev_bits(batch.x)
+    y0 = to_dev_bits(batch.y0)
+    idt = ids_dev(ids)
+    err = new_err()
+    ys = [torch.empty_like(y0) for _ in range(4)]
+
+    def chain(static, sync):
+        for y in ys:
+            y.copy_(y0)
+        prev = x0
+        for y in ys:
+            B.lora_bgmv(prev, y, idt, view, err=err, static_adapters=static)
+            if sync:
+                torch.cuda.synchronize()
+            prev = y
+
+    chain(False, True)
+    torch.cuda.synchronize()
+    want = [y.clone() for y in ys]
+    assert int(err.item()) == 0
+    ref, oerr = oracle_apply(batch.x, batch.y0, ids, pool)
+    assert oerr == 0
+    compare_bf16(to_host_bits(want[0]), ref, "first call of the chain")
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        chain(True, False)
+    for _ in range(30):
+        for y in ys:
+            y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for y, w in zip(ys, want):
+            assert torch.equal(y.view(torch.int16), w.view(torch.int16))
+    assert int(err.item()) == 0
+
+
+def test_bgmv_decode_kernel_shapes_and_pages():
+    """The decode kernel on the shapes it takes: one CTA (d = 256), slices narrower than
+    a sub-slice, d_in != d_out, 1024-element pages, rows that cross pages (d = 1000),
+    ranks 1..16 with max_rank 16, strides wider than the rows; and a view with more page
+    slots than the kernel caches (256-element pages), which lora_bgmv runs on the gather
+    kernel.  Against the oracle; -1 rows and the guard columns untouched."""
+    for seed, (d_in, d_out, page) in enumerate([(256, 256, 4096), (1024, 2048, 4096), (4096, 1024, 1024),
+                                                (1000, 4096, 4096), (2048, 4096, 256)]):
+        rng = np.random.default_rng(900 + seed)
+        ranks = [1, 16, 3, 8, 16, 5, 12, 2]
+        pool = W.build_pool(rng, d_in, d_out, ranks, max_rank=16, page_elems=page)
+        ids = rng.integers(-1, len(ranks), size=40).astype(np.int32)
+        batch = W.make_batch(rng, ids, d_in, d_out, ldx=d_in + 16, ldy=d_out + 8)
+        y, err = run_bgmv(batch, pool)
+        ref, oerr = oracle_apply(batch.x, batch.y0, ids, pool)
+        assert err == oerr == 0
+        compare_bf16(y[:, :d_out], ref, "decode kernel %dx%d page %d" % (d_in, d_out, page))
+        assert np.array_equal(y[ids < 0], batch.y0[ids < 0])
+        assert np.array_equal(y[:, d_out:], batch.y0[:, d_out:])
 
 
 # ------------------------------------------------------------ shrink/expand --

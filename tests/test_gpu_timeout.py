@@ -63,3 +63,30 @@ def test_timeout_flags_and_leaves_outputs_then_recovers():
     assert int(err.item()) == 0
     ref, _ = oracle_apply(batch.x, batch.y0, batch.ids, pool)
     compare_bf16(to_host_bits(y), ref, "after the timeout probe")
+
+
+@pytest.mark.parametrize("static", [False, True])
+def test_timeout_on_the_decode_kernel(static):
+    """The decode kernel (small adapters, one token per cluster) takes the same exit,
+    with and without LORA_BGMV_STATIC_ADAPTERS; the next call is correct."""
+    rng = np.random.default_rng(62)
+    pool = W.build_pool(rng, 4096, 4096, [16, 8, 16, 4], max_rank=16)
+    ids = rng.integers(-1, 4, size=24).astype(np.int32)
+    batch = W.make_batch(rng, ids, 4096, 4096)
+    view = B.PoolView.from_host(pool)
+    x = to_dev_bits(batch.x)
+    idt = ids_dev(ids)
+    B.debug_wait_probe(PROBE_CYCLES)
+    y = to_dev_bits(batch.y0)
+    err = new_err()
+    B.lora_bgmv(x, y, idt, view, err=err, static_adapters=static)
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.LORA_DERR_TIMEOUT
+    assert np.array_equal(to_host_bits(y), batch.y0), "a CTA that gave up wrote output"
+    B.debug_wait_probe(0)
+    err.zero_()
+    B.lora_bgmv(x, y, idt, view, err=err, static_adapters=static)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref, _ = oracle_apply(batch.x, batch.y0, ids, pool)
+    compare_bf16(to_host_bits(y), ref, "after the timeout probe")
