@@ -292,11 +292,12 @@ lora_status_t lora_sgmv_backward(const void* x, int64_t ldx, const void* dy, int
  * (the batched gather path for size-1 segments of "Multi-LoRA serving: ...",
  * section "SGMV: the kernel that holds it all up"; MBGMV in "Multi-LoRA
  * Serving in Production", section "S-LoRA: MBGMV and MBGMM Kernels").
- * Same arithmetic as lora_apply's short segments: equal to lora_apply bit for
- * bit when both run at the same cluster width (the width the projection's
- * slices want, which lora_apply narrows only for batches with more units than
- * resident clusters).  Views with max_rank <= 16 and d_in, d_out <= 4096 run
- * on a decode kernel of small CTAs; other views on the gather kernel.
+ * Same result as lora_apply up to rounding.  Views with max_rank <= 16,
+ * d_in, d_out <= 4096 and at most 128 page-list slots per adapter run on a
+ * decode kernel of small CTAs with fp32 CUDA-core arithmetic, where a token's
+ * output depends only on its own row, its adapter and the projection's shape
+ * (not on the rest of the batch); other views run on lora_apply's gather
+ * kernel.
  */
 lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy,
                         const int32_t* token_adapter, int32_t T, const lora_pool_view_t* view,

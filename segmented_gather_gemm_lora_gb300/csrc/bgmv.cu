@@ -11,27 +11,30 @@
 // adapter id, its descriptor, its page list, the rows, the shrink, the cluster
 // exchange, the expand.  This kernel shortens that chain and lets consecutive
 // calls overlap:
-//   - small CTAs (4 warps, about 22 KB of shared memory), so that the next
+//   - small CTAs (4 warps, about 21 KB of shared memory), so that the next
 //     call's CTAs are resident, with their set-up done, while this call runs;
-//   - no record pipeline: a CTA holds its whole adapter slice, one chunk of at
-//     most 16 rows, so every copy is issued as soon as the page list is read,
-//     and B's rows are prefetched into L2 then and copied into the same buffer
-//     once the shrink is done with A's;
+//   - no record pipeline: a CTA holds its whole adapter slice, at most 16 rows,
+//     so every copy is issued as soon as the page list is read, and B's rows
+//     are prefetched into L2 then and copied into the same buffer once the
+//     shrink is done with A's;
+//   - the arithmetic of one token is a matrix-vector product, so it runs on the
+//     CUDA cores (fp32 FMA, shuffle reductions), not the tensor cores;
 //   - optionally (LORA_BGMV_STATIC_ADAPTERS) the adapter chain and A's copies
 //     run before the kernel ahead of it on the stream has finished, and only
 //     x, y0 and y wait for it.
 //
-// Work decomposition and arithmetic are those of the gather kernel at cluster
-// width C: CTA c owns slice c of d_in (shrink) and of d_out (expand), each at
-// most one 512-column sub-slice; the chunk arithmetic is chunk_mma.cuh's, the
-// eight 64-column blocks of a sub-slice taken two per warp; each CTA adds its
-// blocks' partials in block order and pushes the sum to every CTA of the
-// cluster, which add the C partials in CTA order.  So a token's output is the
-// gather kernel's at the same cluster width, bit for bit.
+// Work decomposition: the token's cluster has C CTAs, C = ceil(max(d_in,
+// d_out) / 512) (at most 8, the gather kernel's width for the projection); CTA
+// c owns slice c of d_in (shrink) and of d_out (expand), at most 512 columns
+// each.  Each CTA pushes its partial h to every CTA of the cluster through
+// distributed shared memory, and each adds the C partials in CTA order, so the
+// result is deterministic and depends only on the token's row, its adapter and
+// the projection's shape.  The sums are the exact fp32 ones (h not split into
+// bf16 parts), so they differ from lora_apply's tensor-core sums by rounding
+// only.
 #include <algorithm>
 #include <cstring>
 
-#include "chunk_mma.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -41,23 +44,24 @@ namespace {
 
 constexpr int kDThreads = 128;
 constexpr int kDWarps = kDThreads / 32;
-constexpr int kDMaxRank = kChunkRows;  // the adapter's rows fit one chunk
+constexpr int kDMaxRank = 16;    // the adapter's rows held at once
+constexpr int kDMaxCols = 512;   // columns of a CTA's slice of d_in or d_out
+constexpr int kDRowStride = kDMaxCols * 2 + 16;  // bytes between staged rows
 constexpr int kDMaxCluster = 8;
 constexpr int kDMaxPg = 128;  // page-list slots of one adapter cached in shared memory (A's, then B's)
-static_assert(kSubBlocks == 2 * kDWarps, "two 64-column blocks per warp");
+static_assert(kDMaxCols == 4 * kDThreads && kDMaxCols == 16 * 32, "column ownership of the expand and the shrink");
 
 // shared memory: adapter rows (A, then B) and the token's y0 row after them;
-// the x row; page cache; the blocks' partials; the cluster's partials; h;
-// each warp's output scratch; the verdict; four mbarriers
+// the x row; page cache; this CTA's partial h; the cluster's partials; h; the
+// verdict; four mbarriers
 constexpr size_t kDOffBuf = 0;
-constexpr size_t kDOffY0 = kDOffBuf + (size_t)kChunkRows * kRowStride;
-constexpr size_t kDOffX = kDOffY0 + kRowStride;
-constexpr size_t kDOffPg = kDOffX + kRowStride;
+constexpr size_t kDOffY0 = kDOffBuf + (size_t)kDMaxRank * kDRowStride;
+constexpr size_t kDOffX = kDOffY0 + kDRowStride;
+constexpr size_t kDOffPg = kDOffX + kDRowStride;
 constexpr size_t kDOffPw = kDOffPg + kDMaxPg * sizeof(int);
-constexpr size_t kDOffRecv = kDOffPw + kSubBlocks * kDMaxRank * sizeof(float);
+constexpr size_t kDOffRecv = kDOffPw + kDMaxRank * sizeof(float);
 constexpr size_t kDOffHs = kDOffRecv + kDMaxCluster * kDMaxRank * sizeof(float);
-constexpr size_t kDOffScr = kDOffHs + kHMax * sizeof(float);
-constexpr size_t kDOffInfo = kDOffScr + kDWarps * 64 * sizeof(float);
+constexpr size_t kDOffInfo = kDOffHs + kDMaxRank * sizeof(float);
 constexpr size_t kDOffBars = kDOffInfo + 8 * sizeof(int);
 constexpr size_t kDSmem = kDOffBars + 4 * sizeof(uint64_t);
 static_assert(kDOffY0 % 16 == 0 && kDOffX % 16 == 0 && kDOffBars % 8 == 0, "copy destinations and barriers");
@@ -76,7 +80,10 @@ struct BgmvArgs {
 
 __device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+// No release: nothing a peer reads is published through this barrier (the
+// partials complete on mbarriers), so the arrive need not wait for this
+// thread's stores to become visible.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -110,7 +117,6 @@ __global__ void __launch_bounds__(kDThreads) bgmv_kernel(const __grid_constant__
   float* const pw = reinterpret_cast<float*>(sm + kDOffPw);
   float* const recv = reinterpret_cast<float*>(sm + kDOffRecv);
   float* const hs = reinterpret_cast<float*>(sm + kDOffHs);
-  float* const scr = reinterpret_cast<float*>(sm + kDOffScr);
   int* const info = reinterpret_cast<int*>(sm + kDOffInfo);
   uint64_t* const bars = reinterpret_cast<uint64_t*>(sm + kDOffBars);
   const uint32_t bar_xy = smem_u32(&bars[0]);    // x and y0 rows
@@ -122,6 +128,13 @@ __global__ void __launch_bounds__(kDThreads) bgmv_kernel(const __grid_constant__
   const uint32_t crank = cluster_ctarank(), C = cluster_nctarank();
   const int t = (int)cluster_id_x();  // the token
   const DevView& v = a.v;
+
+  // this CTA's slices: C equal runs of d_in and of d_out, whole 16-byte pieces
+  const int kc = ((v.d_in + (int)C - 1) / (int)C + 7) & ~7;
+  const int nc = ((v.d_out + (int)C - 1) / (int)C + 7) & ~7;
+  const int k0 = min(v.d_in, (int)crank * kc), k1 = min(v.d_in, k0 + kc);
+  const int n0 = min(v.d_out, (int)crank * nc), n1 = min(v.d_out, n0 + nc);
+  const int kw = k1 - k0, nw = n1 - n0;
 
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);
@@ -140,12 +153,6 @@ __global__ void __launch_bounds__(kDThreads) bgmv_kernel(const __grid_constant__
     ok = probe_ok != 0;
   }
 
-  // this CTA's slices, cut as the gather kernel cuts them
-  const int kc = ((v.d_in + (int)C - 1) / (int)C + 7) & ~7;
-  const int nc = ((v.d_out + (int)C - 1) / (int)C + 7) & ~7;
-  const int k0 = min(v.d_in, (int)crank * kc), k1 = min(v.d_in, k0 + kc);
-  const int n0 = min(v.d_out, (int)crank * nc), n1 = min(v.d_out, n0 + nc);
-  const int kw = k1 - k0, nw = n1 - n0;
 
   if (!a.early) grid_wait();
   if (warp == 0 && ok) {
@@ -188,7 +195,7 @@ __global__ void __launch_bounds__(kDThreads) bgmv_kernel(const __grid_constant__
       if (lane == 0) mbar_arrive_expect_tx(bar_a, (uint32_t)(r * kw * 2));
       __syncwarp();
       if (lane < r && kw > 0)
-        copy_run(v, pg, (long long)lane * v.d_in + k0, kw, smem_u32(buf + lane * kRowStride), bar_a);
+        copy_run(v, pg, (long long)lane * v.d_in + k0, kw, smem_u32(buf + lane * kDRowStride), bar_a);
       if (lane < r && nw > 0) copy_run(v, pg + na, (long long)lane * v.d_out + n0, nw, 0u, 0u);
     }
     if (lane == 0) {
@@ -215,25 +222,57 @@ __global__ void __launch_bounds__(kDThreads) bgmv_kernel(const __grid_constant__
     const float sc = __int_as_float(info[2]);
     const int na = info[3];
     ok = __syncthreads_and(mbar_wait(bar_a, 0) && mbar_wait(bar_xy, 0)) != 0;
-    if (ok) {  // shrink: 64-column blocks 2 warp and 2 warp + 1; the token is column 0 of the tile
+    if (ok) {
+      // Shrink on the CUDA cores (one token: a matrix-vector product): warp w owns
+      // rows w, w + 4, w + 8, w + 12; lane l the 16-byte pieces at columns 8 l and
+      // 256 + 8 l of the slice.  Each lane sums its 16 products in column order,
+      // then a fixed butterfly of shuffles adds the lanes.
+      float xv[2][8];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int b = 2 * warp + h;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        shrink_chunk(smem_u32(buf), smem_u32(sm + kDOffX), kw, 1, d, b, lane);
-        if ((lane & 3) == 0) {
-          const int g = lane >> 2;
-          if (g < r) pw[b * kDMaxRank + g] = d[0];
-          if (g + 8 < r) pw[b * kDMaxRank + g + 8] = d[2];
+      for (int p = 0; p < 2; ++p) {
+        const int c = 8 * lane + 256 * p;
+        if (c < kw) {
+          unpack8(*reinterpret_cast<const uint4*>(sm + kDOffX + 2 * c), xv[p]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) xv[p][e] = 0.f;
         }
+      }
+      // the warp's four rows side by side, so that their loads, products and
+      // shuffles overlap
+      constexpr int kRows = kDMaxRank / kDWarps;
+      float sr[kRows];
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        const int j = warp + kDWarps * i;
+        sr[i] = 0.f;
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+          const int c = 8 * lane + 256 * p;
+          if (j < r && c < kw) {
+            float av[8];
+            unpack8(*reinterpret_cast<const uint4*>(buf + j * kDRowStride + 2 * c), av);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sr[i] = fmaf(av[e], xv[p][e], sr[i]);
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) sr[i] += __shfl_xor_sync(0xffffffffu, sr[i], o);
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < kRows; ++i)
+          if (warp + kDWarps * i < r) pw[warp + kDWarps * i] = sr[i];
       }
     }
     __syncthreads();  // every block's partial is in; A's rows are free
-    if (ok && warp == 0) {  // B's rows into the same buffer (mostly from L2 by now)
+    if (ok && warp == 1) {  // B's rows into the same buffer (mostly from L2 by now), beside warp 0's sends
       if (lane == 0) mbar_arrive_expect_tx(bar_b, (uint32_t)(r * nw * 2));
       __syncwarp();
       if (lane < r && nw > 0)
-        copy_run(v, pg + na, (long long)lane * v.d_out + n0, nw, smem_u32(buf + lane * kRowStride), bar_b);
+        copy_run(v, pg + na, (long long)lane * v.d_out + n0, nw, smem_u32(buf + lane * kDRowStride), bar_b);
     }
     b_issued = ok;
     // this CTA's partial (the blocks' partials in block order), pushed to every
@@ -241,17 +280,9 @@ __global__ void __launch_bounds__(kDThreads) bgmv_kernel(const __grid_constant__
     const int q4 = (r + 3) >> 2;
     if (ok && tid == 0) mbar_arrive_expect_tx(bar_recv, C * (uint32_t)q4 * 16u);
     if (ok && tid < q4) {
-      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int b = 0; b < kSubBlocks; ++b) {
-        const float4 p = *reinterpret_cast<const float4*>(pw + b * kDMaxRank + 4 * tid);
-        sum.x += p.x;
-        sum.y += p.y;
-        sum.z += p.z;
-        sum.w += p.w;
-      }
+      const float4 part = *reinterpret_cast<const float4*>(pw + 4 * tid);
       const uint32_t dst = smem_u32(recv + crank * kDMaxRank + 4 * tid);
-      for (uint32_t c = 0; c < C; ++c) st_async_v4(mapa(dst, c), sum, mapa(bar_recv, c));
+      for (uint32_t c = 0; c < C; ++c) st_async_v4(mapa(dst, c), part, mapa(bar_recv, c));
     }
     bool got = true;
     if (ok && tid < r) {
@@ -267,16 +298,27 @@ __global__ void __launch_bounds__(kDThreads) bgmv_kernel(const __grid_constant__
   cluster_arrive();
   if (active && ok) {
     ok = __syncthreads_and(mbar_wait(bar_b, 0)) != 0;
-    if (ok) {
-      const int tok[kNT] = {t, t, t, t};
+    const int c = 4 * tid;
+    if (ok && c < nw) {
+      // Expand on the CUDA cores: thread i owns columns 4 i .. 4 i + 3 of the
+      // slice and adds h_j B_i[j, n] over the rows in order, then y0.
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int b = 2 * warp + h;
-        if (b * 64 >= nw) break;
-        float acc[4][4];
-        expand_mma(smem_u32(buf), hs, 0, r, 1, nw, true, acc, b, lane);
-        expand_store(a.y, a.ldy, nullptr, 0, y0row, scr + warp * 64, acc, 1, tok, n0, nw, b, lane);
+      for (int j = 0; j < kDMaxRank; ++j) {
+        if (j < r) {
+          const uint2 bv = *reinterpret_cast<const uint2*>(buf + j * kDRowStride + 2 * c);
+          const float hj = hs[j];
+          acc[0] = fmaf(hj, bf_lo(bv.x), acc[0]);
+          acc[1] = fmaf(hj, bf_hi(bv.x), acc[1]);
+          acc[2] = fmaf(hj, bf_lo(bv.y), acc[2]);
+          acc[3] = fmaf(hj, bf_hi(bv.y), acc[3]);
+        }
       }
+      const uint2 y0 = *reinterpret_cast<const uint2*>(y0row + 2 * c);
+      uint2 out;
+      out.x = pack_bf16x2(bf_lo(y0.x) + acc[0], bf_hi(y0.x) + acc[1]);
+      out.y = pack_bf16x2(bf_lo(y0.y) + acc[2], bf_hi(y0.y) + acc[3]);
+      *reinterpret_cast<uint2*>(a.y + (long long)t * a.ldy + n0 + c) = out;
     }
   }
   if (!ok) {
@@ -296,7 +338,7 @@ __global__ void __launch_bounds__(kDThreads) bgmv_kernel(const __grid_constant__
 // columns of the wider side, at most eight.
 int slice_width(const lora_pool_view_t* v) {
   const int d = std::max(v->d_in, v->d_out);
-  return std::min(std::max((d + kSub - 1) / kSub, 1), kDMaxCluster);
+  return std::min(std::max((d + kDMaxCols - 1) / kDMaxCols, 1), kDMaxCluster);
 }
 
 }  // namespace
@@ -305,7 +347,7 @@ bool bgmv_decode_ok(const lora_pool_view_t* v, int T) {
   if (T < 1 || T > (1 << 20) || v->max_rank > kDMaxRank) return false;
   const int C = slice_width(v);
   const int kc = ((v->d_in + C - 1) / C + 7) & ~7, nc = ((v->d_out + C - 1) / C + 7) & ~7;
-  if (kc > kSub || nc > kSub) return false;
+  if (kc > kDMaxCols || nc > kDMaxCols) return false;
   const long long P = v->page_elems;
   const long long na = ((long long)v->max_rank * v->d_in + P - 1) / P;
   const long long nb = ((long long)v->max_rank * v->d_out + P - 1) / P;

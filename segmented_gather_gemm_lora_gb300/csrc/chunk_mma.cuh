@@ -1,5 +1,5 @@
-// Chunk arithmetic of the CUDA-core-scheduled paths (the gather kernel and the
-// decode kernel): warp-level tensor-core tiles over staged adapter rows.
+// Chunk arithmetic of the gather kernel: warp-level tensor-core tiles over
+// staged adapter rows.
 //
 // "Multi-LoRA Serving in Production", sections "Shrink Stage" and "Expand
 // Stage": the shrink contracts a token row with the adapter's rows, the expand

@@ -308,20 +308,27 @@ def test_bgmv_parity(name):
     assert np.array_equal(y[ids < 0], wl.batch.y0[ids < 0])
 
 
-def test_bgmv_equals_apply_bitwise():
-    """The decode kernel runs the gather kernel's arithmetic at the cluster width the
-    projection's slices want; lora_apply's gather kernel keeps that width for a batch of
-    a dozen tokens, so the two agree bit for bit (with repeated adapters and -1 ids)."""
+def test_bgmv_matches_apply_and_is_batch_invariant():
+    """lora_bgmv (the decode kernel's fp32 sums) and lora_apply (the gather kernel's
+    tensor-core sums) on the same batch, with a repeated adapter and a -1 id, both
+    agree with the oracle; and a token's lora_bgmv output does not depend on the other
+    tokens of its call: the batch's first dozen tokens, alone, give the same bits."""
     wl = W.decode(1)
     pool = wl.pools[0]
-    ids = wl.batch.ids[:12].copy()
+    ids = wl.batch.ids.copy()
     ids[3] = ids[7]
     ids[5] = -1
-    b = W.Batch(x=wl.batch.x[:12], y0=wl.batch.y0[:12], ids=ids, d_in=wl.batch.d_in, d_out=wl.batch.d_out)
+    b = W.Batch(x=wl.batch.x, y0=wl.batch.y0, ids=ids, d_in=wl.batch.d_in, d_out=wl.batch.d_out)
     yb, eb = run_bgmv(b, pool)
     ya, ea, _ = run_apply(b, pool, B.LORA_SEG_GROUP, wl.n_adapters)
     assert eb == ea == 0
-    assert np.array_equal(ya, yb)
+    ref, _ = oracle_apply(b.x, b.y0, ids, pool)
+    compare_bf16(yb, ref, "bgmv")
+    compare_bf16(ya, ref, "apply")
+    sub = W.Batch(x=b.x[:12], y0=b.y0[:12], ids=ids[:12], d_in=b.d_in, d_out=b.d_out)
+    ys, es = run_bgmv(sub, pool)
+    assert es == 0
+    assert np.array_equal(ys, yb[:12])
 
 
 def test_bgmv_static_adapters_chain_in_graph():
