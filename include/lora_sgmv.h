@@ -75,12 +75,13 @@ typedef int32_t lora_status_t;
 #define LORA_MAX_RANK 64
 /** Largest adapter count lora_segments_build accepts. */
 #define LORA_MAX_ADAPTERS 32768
-/** Segments of at most this many tokens take the gather (CUDA-core) path of
- *  lora_apply / lora_sgmv_*; longer ones are cut into tiles of LORA_TILE_M
- *  tokens for the tensor-core path ("Multi-LoRA serving: ...", section "SGMV:
- *  the kernel that holds it all up": large segments through tensor cores, small
- *  ones through a batched gather path). */
-#define LORA_SHORT_MAX_TOKENS 8
+/** Segments of at most this many tokens take the gather path of lora_apply /
+ *  lora_sgmv_*; longer ones are cut into tiles of LORA_TILE_M tokens for the
+ *  tensor-core path ("Multi-LoRA serving: ...", section "SGMV: the kernel that
+ *  holds it all up": large segments through tensor cores, small ones through a
+ *  batched gather path).  Chosen by measurement: with 64 segments of L tokens
+ *  (rank 16, 4096 -> 4096) the two paths take equal time near L = 24-28. */
+#define LORA_SHORT_MAX_TOKENS 24
 #define LORA_TILE_M 128
 
 /** Segmentation modes of lora_segments_build. */

@@ -29,7 +29,7 @@ LORA_DERR_BAD_RANK = 4
 LORA_DERR_TIMEOUT = 8
 LORA_MAX_RANK = 64
 LORA_MAX_ADAPTERS = 32768
-LORA_SHORT_MAX_TOKENS = 8
+LORA_SHORT_MAX_TOKENS = 24
 LORA_TILE_M = 128
 LORA_BGMV_STATIC_ADAPTERS = 1
 LORA_SEG_GROUP = 0

@@ -87,7 +87,9 @@ cudaError_t ensure_smem_attr(const void* func, size_t bytes) {
     }
   }
   if (slot >= 0 && cache[slot][dev].load() >= bytes) return cudaSuccess;
-  if (bytes <= 48 * 1024) return cudaSuccess;
+  // Raised even below 48 KB: the default limit covers dynamic and static shared
+  // memory together, so a kernel with static shared memory of its own needs the
+  // attribute for a dynamic size just under 48 KB too.
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e == cudaSuccess && slot >= 0) {
     size_t cur = cache[slot][dev].load();

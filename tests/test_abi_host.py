@@ -71,7 +71,7 @@ def test_carve_layout():
         s = B.lora_segments_t()
         assert L.lora_segments_carve(ctypes.c_void_p(base), n, T, ctypes.byref(s)) == 0
         assert s.T == T
-        assert s.max_long_units == T // 128 + T // 9 + 1
+        assert s.max_long_units == T // B.LORA_TILE_M + T // (B.LORA_SHORT_MAX_TOKENS + 1) + 1
         ptrs = [s.token_perm, s.seg_indptr, s.seg_adapter, s.meta, s.short_units, s.long_units, s.scratch,
                 s.h_scratch, s.k_partials]
         assert all(p % 16 == 0 for p in ptrs)
@@ -91,7 +91,7 @@ def fake_view(**kw):
 def fake_seg(T=16):
     s = B.lora_segments_t()
     s.T = T
-    s.max_long_units = T // 128 + T // 9 + 1
+    s.max_long_units = T // B.LORA_TILE_M + T // (B.LORA_SHORT_MAX_TOKENS + 1) + 1
     for i, f in enumerate(("token_perm", "seg_indptr", "seg_adapter", "meta", "short_units",
                            "long_units", "scratch", "h_scratch", "k_partials")):
         setattr(s, f, 0x100000 + 0x1000 * i)
@@ -133,7 +133,7 @@ def test_apply_rejects_bad_activations_without_launch():
     assert L.lora_apply(x, 256, y, 256, None, ctypes.byref(v), None, None) == -1
     # a segment buffer carved for more tokens than it can hold
     small = fake_seg(16)
-    small.max_long_units = 1
+    small.max_long_units -= 1  # one long unit fewer than 16 tokens can need
     assert L.lora_apply(x, 256, y, 256, ctypes.byref(small), ctypes.byref(v), None, None) == B.LORA_ERR_WORKSPACE
 
 

@@ -35,7 +35,7 @@ def segment_cases():
         ("all_distinct", np.arange(1500, dtype=np.int32)[::-1].copy(), 1500),
         ("max_id", np.full(40, 999, dtype=np.int32), 1000),
         ("runs_broken", np.array([3, 3, 1, 1, 3, -1, 3, 0, 0, 3, 3, 3], dtype=np.int32), 4),
-        ("tile_edges", np.repeat(np.arange(6, dtype=np.int32), [8, 9, 127, 128, 129, 1024]), 6),
+        ("tile_edges", np.repeat(np.arange(8, dtype=np.int32), [8, 9, 24, 25, 127, 128, 129, 1024]), 8),
     ]
     for i in range(12):
         T = int(rng.integers(1, 5000))
@@ -54,6 +54,10 @@ def segment_cases():
     cases.append(("long_batch", np.repeat(rng.integers(0, 50, size=40), 1200).astype(np.int32), 50))
     for T in (1, 2, 3, 5, 4097, 9999):  # every id valid (the identity order of maximal runs)
         cases.append(("valid%d" % T, np.sort(rng.integers(0, 30, size=T)).astype(np.int32)[::-1].copy(), 30))
+    # the kernel's shared memory (16 bytes a token, 4 a GROUP adapter) just under and
+    # just over 48 KB, where the launch needs the opt-in limit with its static part
+    for T, n in ((3040, 64), (3072, 64), (3073, 64), (3000, 200)):
+        cases.append(("smem%d_%d" % (T, n), np.repeat(rng.integers(-1, n, size=T // 48 + 1), 48)[:T].astype(np.int32), n))
     return cases
 
 
@@ -164,7 +168,7 @@ def test_apply_odd_shapes_and_ranks():
     rng = np.random.default_rng(11)
     ranks = [1, 7, 13, 33, 64, 8, 16]
     pool = W.build_pool(rng, 5120, 1000, ranks, page_elems=4096, max_rank=64)
-    lens = [1, 2, 7, 8, 9, 127, 128, 129, 300]
+    lens = [1, 2, 7, 8, 9, 23, 24, 25, 127, 128, 129, 300]
     ids = np.concatenate([np.full(n, i % len(ranks), dtype=np.int32) for i, n in enumerate(lens)])
     ids[rng.choice(ids.size, 20, replace=False)] = -1
     batch = W.make_batch(rng, ids, 5120, 1000, ldx=5128, ldy=1016)
@@ -627,7 +631,7 @@ def test_tc_odd_ranks_and_tile_edges(mode):
     """Long segments on the tensor cores with ranks that are not multiples of 16 and
     segment lengths around the 128-token tile."""
     ranks = [1, 7, 13, 33, 64, 16, 48]
-    lens = [9, 127, 128, 129, 256, 300, 40, 1, 3]
+    lens = [25, 127, 128, 129, 256, 300, 40, 1, 3, 24]
     pool, batch = long_segment_batch(21, ranks, lens, 4096, 1024)
     y, err, _ = run_apply(batch, pool, mode, len(ranks))
     ref, _ = oracle.lora_apply(batch.x, batch.y0, batch.ids, pool)
