@@ -58,6 +58,9 @@ def _declare(L):
     L.oracle_expand.restype = ctypes.c_int
     L.oracle_expand.argtypes = [vp, i64, vp, i64, vp, i64, vp, vp, i64, i64, vp, i64, vp,
                                 i32, i32, i64, i64]
+    L.oracle_base_apply.restype = ctypes.c_int
+    L.oracle_base_apply.argtypes = [vp, i64, vp, i64, vp, i64, vp, vp, i64, i64, vp, i64,
+                                    vp, i32, i32, i64, i64]
     L.oracle_lora_backward.restype = ctypes.c_int
     L.oracle_lora_backward.argtypes = [vp, i64, vp, i64, vp, vp, i64, vp, vp, i64, i64, vp, i64,
                                        vp, i32, i32, i64, i64]
@@ -123,6 +126,21 @@ def lora_apply(x, y0, ids, pool, d_in: int = None, d_out: int = None):
                                   y0.shape[1] if T else d_out, _p(y), T, _p(ids), _p(pp),
                                   pool.n_pages, pool.page_elems, _p(pl), pl.size, _p(desc),
                                   desc.size, pool.max_rank, d_in, d_out)
+    return y, int(err)
+
+
+def base_apply(x, w0, ids, pool):
+    """y (double [T, d_out]) and the error bits for y = x W0^T + s_i (x A_i) B_i per token;
+    w0: bf16 bits [d_out, ldw >= d_in]."""
+    x = _c(x, np.uint16)
+    w0 = _c(w0, np.uint16)
+    ids = _c(ids, np.int32)
+    T = ids.size
+    y = np.empty((T, pool.d_out), dtype=np.float64)
+    pl, pp, desc = _pool_args(pool)
+    err = lib().oracle_base_apply(_p(x), x.shape[1] if T else pool.d_in, _p(w0), w0.shape[1], _p(y), T, _p(ids),
+                                  _p(pp), pool.n_pages, pool.page_elems, _p(pl), pl.size, _p(desc),
+                                  desc.size, pool.max_rank, pool.d_in, pool.d_out)
     return y, int(err)
 
 

@@ -29,6 +29,9 @@
  *    up").  Adapter elements are read through the page table.
  *  - oracle_shrink / oracle_expand: the two stages of that product
  *    ("Multi-LoRA Serving in Production", "Shrink Stage" / "Expand Stage").
+ *  - oracle_base_apply: the base projection x W0 with that product added in
+ *    the same pass ("Multi-LoRA Serving: Many Adapters on One GPU", section
+ *    "How batching across adapters works").
  *  - oracle_lora_backward: the gradients of that product for training the
  *    adapters; the base is frozen and receives none, only A and B do ("QLoRA
  *    and multi-LoRA at the limit on small models", section "The bare
@@ -269,6 +272,63 @@ int oracle_expand(const float* hin, int64_t ldh, const uint16_t* y0, int64_t ldy
             double acc = 0.0;
             for (int64_t j = 0; j < desc[i].rank; ++j)
                 acc += (double)hin[t * ldh + j] * pool_elem(&p, desc[i].b_page0, j * d_out + n, &oob);
+            y[t * d_out + n] += s * acc;
+        }
+    }
+    return err;
+}
+
+/* ------------------------------------------- base projection and delta -- */
+
+/*
+ * The base projection with every token's adapter term in the same pass
+ * ("Multi-LoRA Serving: Many Adapters on One GPU", section "How batching
+ * across adapters works": one base product shared by the whole batch plus each
+ * token's own adapter term; "Multi-LoRA Serving in Production", section
+ * "Mathematical Formulation and the Batching Challenge": y = x W0 + (alpha/r)
+ * (x A) B):
+ *     base     = sum_k x[t,k] * W0[n,k]
+ *     h_j      = sum_k x[t,k] * A_i[j,k]                     (j < r_i)
+ *     y[t,n]   = base + s_i * sum_j h_j * B_i[j,n]
+ * W0 is bf16 [d_out, ldw]: row n holds output n's weights over the d_in inputs.
+ * Tokens with id -1, and tokens whose adapter fails the checks (their error
+ * bits are returned), get the base term alone.  y is double [T, d_out].
+ */
+int oracle_base_apply(const uint16_t* x, int64_t ldx, const uint16_t* w0, int64_t ldw, double* y,
+                      int64_t T, const int32_t* ids, const uint16_t* pool, int64_t n_pages,
+                      int64_t page_elems, const int32_t* page_list, int64_t n_page_list,
+                      const void* adapters, int32_t n_adapters, int32_t max_rank,
+                      int64_t d_in, int64_t d_out)
+{
+    const orc_desc_t* desc = (const orc_desc_t*)adapters;
+    orc_pool_t p = {pool, n_pages, page_elems, page_list, n_page_list};
+    int err = 0;
+    double h[256];
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t n = 0; n < d_out; ++n) {        /* the shared base product */
+            double base = 0.0;
+            for (int64_t k = 0; k < d_in; ++k)
+                base += oracle_bf16_to_double(x[t * ldx + k]) * oracle_bf16_to_double(w0[n * ldw + k]);
+            y[t * d_out + n] = base;
+        }
+        int32_t i = ids[t];
+        if (i == -1) continue;
+        if (i < -1 || i >= n_adapters) { err |= ORC_ERR_BAD_ADAPTER; continue; }
+        int bad = adapter_check(&desc[i], max_rank, &p, d_in, d_out);
+        if (bad || desc[i].rank > 256) { err |= bad ? bad : ORC_ERR_BAD_RANK; continue; }
+        int64_t r = desc[i].rank;
+        double s = (double)desc[i].scale;
+        int oob = 0;
+        for (int64_t j = 0; j < r; ++j) {            /* the token's shrink over A_i */
+            double acc = 0.0;
+            for (int64_t k = 0; k < d_in; ++k)
+                acc += oracle_bf16_to_double(x[t * ldx + k]) * pool_elem(&p, desc[i].a_page0, j * d_in + k, &oob);
+            h[j] = acc;
+        }
+        for (int64_t n = 0; n < d_out; ++n) {        /* its expand over B_i, onto the base */
+            double acc = 0.0;
+            for (int64_t j = 0; j < r; ++j)
+                acc += h[j] * pool_elem(&p, desc[i].b_page0, j * d_out + n, &oob);
             y[t * d_out + n] += s * acc;
         }
     }

@@ -470,3 +470,65 @@ def test_backward_zero_gradient_and_untouched_tokens():
     # gradients accumulate into the array given
     _, grad3, _ = oracle.lora_backward(batch.x, g, batch.ids, pool, grad=grad.copy())
     np.testing.assert_allclose(grad3, 2 * grad, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------ base projection and delta --
+
+def base_case(seed, d_in=72, d_out=40, ranks=(8, 1, 13, 16), T=12, ldw=None, page_elems=64):
+    rng = np.random.default_rng(seed)
+    pool = W.build_pool(rng, d_in, d_out, list(ranks), page_elems=page_elems, max_rank=16)
+    ids = rng.integers(-1, len(ranks), size=T).astype(np.int32)
+    batch = W.make_batch(rng, ids, d_in, d_out, ldx=d_in + 8)
+    ldw = d_in + 16 if ldw is None else ldw
+    w0 = W.f32_to_bf16_bits((rng.standard_normal((d_out, ldw)) / np.sqrt(d_in)).astype(np.float32))
+    return pool, batch, w0
+
+
+def test_base_apply_matches_numpy_matmul():
+    """y = X W0^T + s_i (x A_i^T) B_i per token, against numpy float64 matmuls on the logical
+    matrices (W0 read through its row stride, the pool through its pages)."""
+    pool, batch, w0 = base_case(40)
+    y, err = oracle.base_apply(batch.x, w0, batch.ids, pool)
+    assert err == 0
+    X = f64(batch.x[:, : pool.d_in])
+    ref = X @ f64(w0[:, : pool.d_in]).T
+    for t, i in enumerate(batch.ids):
+        if i >= 0:
+            ref[t] += float(pool.scales[i]) * ((X[t] @ f64(pool.A[i]).T) @ f64(pool.B[i]))
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_base_apply_merged_weight_identity():
+    """x (W0 + s A^T B)^T == x W0^T + s (x A^T) B for every token of adapter i ("Multi-LoRA
+    Serving in Production", section "Mathematical Formulation and the Batching Challenge")."""
+    pool, batch, w0 = base_case(41, d_in=64, d_out=56, ranks=(4, 16, 2))
+    y, err = oracle.base_apply(batch.x, w0, batch.ids, pool)
+    assert err == 0
+    X = f64(batch.x[:, :64])
+    W0 = f64(w0[:, :64])
+    for t, i in enumerate(batch.ids):
+        Wm = W0 if i < 0 else W0 + float(pool.scales[i]) * (f64(pool.B[i]).T @ f64(pool.A[i]))
+        np.testing.assert_allclose(y[t], X[t] @ Wm.T, rtol=1e-11, atol=1e-11)
+
+
+def test_base_apply_reduces_to_lora_apply_and_to_the_base():
+    """W0 = 0 gives lora_apply's result on y0 = 0 exactly; no adapter (every id -1) gives
+    the base product alone; a bad adapter keeps the base term and flags its bit."""
+    pool, batch, w0 = base_case(42)
+    zero = np.zeros_like(w0)
+    y, err = oracle.base_apply(batch.x, zero, batch.ids, pool)
+    y0 = np.zeros((batch.T, pool.d_out), dtype=np.uint16)
+    want, werr = oracle.lora_apply(batch.x, y0, batch.ids, pool)
+    assert err == werr == 0
+    np.testing.assert_array_equal(y, want)
+    none = np.full(batch.T, -1, dtype=np.int32)
+    yb, eb = oracle.base_apply(batch.x, w0, none, pool)
+    assert eb == 0
+    np.testing.assert_allclose(yb, f64(batch.x[:, : pool.d_in]) @ f64(w0[:, : pool.d_in]).T, rtol=1e-12,
+                               atol=1e-12)
+    bad = batch.ids.copy()
+    bad[0] = pool.n_adapters + 2
+    y2, e2 = oracle.base_apply(batch.x, w0, bad, pool)
+    assert e2 == 1  # bad adapter id
+    np.testing.assert_array_equal(y2[0], yb[0])
+    np.testing.assert_array_equal(y2[1:], oracle.base_apply(batch.x, w0, batch.ids, pool)[0][1:])
