@@ -303,7 +303,7 @@ int oracle_base_apply(const uint16_t* x, int64_t ldx, const uint16_t* w0, int64_
     const orc_desc_t* desc = (const orc_desc_t*)adapters;
     orc_pool_t p = {pool, n_pages, page_elems, page_list, n_page_list};
     int err = 0;
-    double h[256];
+    double hv[256];
     for (int64_t t = 0; t < T; ++t) {
         for (int64_t n = 0; n < d_out; ++n) {        /* the shared base product */
             double base = 0.0;
@@ -323,13 +323,13 @@ int oracle_base_apply(const uint16_t* x, int64_t ldx, const uint16_t* w0, int64_
             double acc = 0.0;
             for (int64_t k = 0; k < d_in; ++k)
                 acc += oracle_bf16_to_double(x[t * ldx + k]) * pool_elem(&p, desc[i].a_page0, j * d_in + k, &oob);
-            h[j] = acc;
+            hv[j] = acc;
         }
         for (int64_t n = 0; n < d_out; ++n) {        /* its expand over B_i, onto the base */
-            double acc = 0.0;
+            double term = 0.0;
             for (int64_t j = 0; j < r; ++j)
-                acc += h[j] * pool_elem(&p, desc[i].b_page0, j * d_out + n, &oob);
-            y[t * d_out + n] += s * acc;
+                term += hv[j] * pool_elem(&p, desc[i].b_page0, j * d_out + n, &oob);
+            y[t * d_out + n] += s * term;
         }
     }
     return err;

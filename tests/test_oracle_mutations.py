@@ -40,8 +40,7 @@ MUTATIONS = {
                       "acc += oracle_bf16_to_double(g[t * ldg + n]) * pool_elem(&p, desc[i].b_page0, n * r + j, &oob);"),
     "grad_dx_dropped_scale": ("dx[t * d_in + k] = s * acc;", "dx[t * d_in + k] = acc;"),
     "base_weight_column": ("* oracle_bf16_to_double(w0[n * ldw + k]);", "* oracle_bf16_to_double(w0[n * ldw + (k + 1) % d_in]);"),
-    "base_dropped_under_adapter": ("            y[t * d_out + n] += s * acc;\n        }\n    }\n    return err;\n}\n\n/* -------------------------------------------------------- the gradients",
-                                   "            y[t * d_out + n] = s * acc;\n        }\n    }\n    return err;\n}\n\n/* -------------------------------------------------------- the gradients"),
+    "base_dropped_under_adapter": ("y[t * d_out + n] += s * term;", "y[t * d_out + n] = s * term;"),
 }
 
 
