@@ -67,6 +67,7 @@ WORKLOAD_TEXT = {
 # timed steps of the configurations timed beside the headline (each well under a second)
 OTHER_STEPS = {"tiny": 20000, "decode": 20000, "prefill": 2000, "hetero": 2000}
 BACKWARD_STEPS = 500
+BASE_STEPS = 100
 
 
 def parse_args(argv=None):
@@ -77,7 +78,7 @@ def parse_args(argv=None):
                         "20000 for a small configuration timed alone)")
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["all", "backward"] + sorted(WORKLOAD_TEXT), default="all",
+    p.add_argument("--workload", choices=["all", "backward", "base_fused"] + sorted(WORKLOAD_TEXT), default="all",
                    help="all (default): the 13B forward as the headline, every other "
                         "configuration under per_config; or one configuration alone "
                         "(backward: the adapter-training backward pass on the prefill batch)")
@@ -90,7 +91,8 @@ def parse_args(argv=None):
     args = p.parse_args(argv)
     head = HEADLINE if args.workload == "all" else args.workload
     if args.steps is None:
-        args.steps = 20 if head == "mixed13b" else BACKWARD_STEPS if head == "backward" else 20000
+        args.steps = 20 if head == "mixed13b" else BACKWARD_STEPS if head == "backward" else \
+            BASE_STEPS if head == "base_fused" else 20000
     return args
 
 
@@ -802,6 +804,126 @@ def run_backward_line(steps, warmup, soak_seconds, world, rank, local):
     return out
 
 
+def run_base_line(steps, warmup, soak_seconds, world, rank, local):
+    """The base projection with the adapter term in its epilogue on the prefill batch: a
+    step is lora_segments_build + lora_base_apply (y = x W0^T + s_i (x A_i^T) B_i, y written
+    once) with a random 4096 x 4096 W0; timed beside cuBLAS's x W0^T followed by
+    lora_apply, the unfused way to the same y.  Two input sets rotate (each larger than L2)."""
+    import torch
+
+    from segmented_gather_gemm_lora_gb300 import binding as B
+    from segmented_gather_gemm_lora_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    sets = []
+    for k in range(2):
+        wl = W.prefill(1000 * rank + k)
+        pool, b = wl.pools[0], wl.batch
+        g = torch.Generator(device=dev)
+        g.manual_seed(1000 * rank + k)
+        w0 = (torch.randn(pool.d_out, pool.d_in, generator=g, device=dev) / float(np.sqrt(pool.d_in))).to(torch.bfloat16)
+        S = dict(view=B.PoolView.from_host(pool, device=dev), x=up(b.x), y=torch.empty((b.T, pool.d_out),
+                 dtype=torch.bfloat16, device=dev), w0=w0, ids=torch.from_numpy(b.ids).to(dev),
+                 seg=B.Segments(b.T, device=dev), T=b.T, n_ad=wl.n_adapters,
+                 flops=2 * b.T * pool.d_in * pool.d_out + algorithmic_flops(b, pool))
+        sets.append(S)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def fused(i):
+        S = sets[i % 2]
+        B.lora_segments_build(S["ids"], S["n_ad"], S["seg"], mode=B.LORA_SEG_CONTIGUOUS, err=err)
+        B.lora_base_apply(S["x"], S["w0"], S["y"], S["ids"], S["seg"], S["view"], err=err)
+
+    def unfused(i):
+        S = sets[i % 2]
+        B.lora_segments_build(S["ids"], S["n_ad"], S["seg"], mode=B.LORA_SEG_CONTIGUOUS, err=err)
+        torch.matmul(S["x"], S["w0"].t(), out=S["y"])
+        B.lora_apply(S["x"], S["y"], S["seg"], S["view"], err=err)
+
+    def graph_of(fn, n):
+        for i in range(max(warmup, 3)):
+            fn(i)
+        torch.cuda.synchronize()
+        cap = torch.cuda.Stream(device=dev)
+        gr = torch.cuda.CUDAGraph()
+        l0 = B.launch_count()
+        with torch.cuda.graph(gr, stream=cap):
+            for i in range(n):
+                fn(i)
+        return gr, (B.launch_count() - l0) / n
+
+    def timed(gr, reps, n):
+        gr.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record()
+        for _ in range(reps):
+            gr.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1), world) / (reps * n)
+
+    n = 10
+    reps = max(1, steps // n)
+    g_f, launches_per_step = graph_of(fused, n)
+    g_u, _ = graph_of(unfused, n)
+    sampler = ClockSampler(gpu_id_of(props))
+    t_end = time.perf_counter() + soak_seconds
+    while time.perf_counter() < t_end:
+        g_f.replay()
+        torch.cuda.synchronize()
+    ms_f = timed(g_f, reps, n)
+    clocks = sampler.stop()
+    ms_u = timed(g_u, reps, n)
+    assert int(err.item()) == 0, "device error word %d" % int(err.item())
+    tokens = sum_over_ranks(statistics.fmean(S["T"] for S in sets), world)
+    flops = statistics.fmean(S["flops"] for S in sets)
+    step_s = ms_f / 1e3
+    hbm_peak, tc_peak, peak_kind = read_peaks()
+    tc_sustained = tc_peak
+    try:
+        tc_sustained = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("bf16_tflops_sustained",
+                                                                                            tc_peak))
+    except Exception:
+        pass
+    achieved = flops / step_s / 1e12
+    out = {
+        "value": tokens / step_s,
+        "unit": UNIT,
+        "steps": reps * n,
+        "ms_per_step": ms_f,
+        "config": {"workload": "base projection with the adapter term in its epilogue on the prefill SGMV batch: "
+                               "32 requests of U{64..512} tokens, y = x W0^T + s_i (x A_i^T) B_i with a random "
+                               "4096 x 4096 bf16 W0, 200 rank-16 adapters, Zipf(1.1), contiguous segments",
+                   "step": "lora_segments_build + lora_base_apply (shrink, per-token scales, tcgen05 base GEMM "
+                           "with the adapter term in its epilogue; y written once)",
+                   "l2": "inputs larger than L2: 2 rotating input sets",
+                   "timing": "CUDA graph of %d steps replayed; CUDA events on the launching stream" % n,
+                   "unfused_ms_per_step": ms_u,
+                   "unfused": "lora_segments_build + cuBLAS x W0^T (torch.matmul) + lora_apply, same inputs"},
+        "roofline": {"bound": "tensor", "kernel": "lora_base_apply (base_gemm_kernel and the shrink before it)",
+                     "achieved": achieved, "peak": tc_sustained, "unit": "TFLOP/s",
+                     "frac": achieved / tc_sustained,
+                     "peak_kind": "measured sustained bf16 (cuBLAS loop, MEASURED_PEAKS.json)", "traffic": None,
+                     "flops_per_step": flops, "avg_launch_us": step_s * 1e6},
+        "gpu_launches": int(round(launches_per_step * reps * n)),
+        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                   "reasons": clocks["reasons"], "samples": clocks["samples"]},
+    }
+    del sets, g_f, g_u
+    gc.collect()
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------ CPU oracle --
 
 def oracle_sample(workload: str):
@@ -976,8 +1098,11 @@ def main(argv=None):
             per_config[name] = config_line(name, args, world, rank, local, OTHER_STEPS[name])
         per_config["backward"] = run_backward_line(BACKWARD_STEPS, args.warmup, args.soak_seconds, world, rank,
                                                    local)
+        per_config["base_fused"] = run_base_line(BASE_STEPS, args.warmup, args.soak_seconds, world, rank, local)
     if head == "backward":
         h = run_backward_line(args.steps, args.warmup, args.soak_seconds, world, rank, local)
+    elif head == "base_fused":
+        h = run_base_line(args.steps, args.warmup, args.soak_seconds, world, rank, local)
     else:
         h = config_line(head, args, world, rank, local, args.steps)
     out = {

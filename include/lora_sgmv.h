@@ -288,6 +288,31 @@ lora_status_t lora_sgmv_backward(const void* x, int64_t ldx, const void* dy, int
                                  int32_t* dev_err, lora_stream_t stream);
 
 /**
+ * The base projection with the adapter term added before y is written
+ * ("Multi-LoRA Serving: Many Adapters on One GPU", section "How batching
+ * across adapters works": one base product shared by the batch plus each
+ * token's own adapter term):
+ *     y[t, n] = bf16( sum_k x[t,k] W0[n,k] + s_i sum_j (x[t] . A_i[j]) B_i[j,n] )
+ * for every token t < T; tokens with id -1, or with an adapter that fails the
+ * checks (their error bits OR into *dev_err), get the base term alone.  y is
+ * written once and never read (it may hold anything before the call).
+ * x: device bf16 [T, ldx]; w0: device bf16 [d_out, ldw] (row n holds output
+ * n's weights over the d_in inputs, the layout of a linear layer's weight),
+ * ldw >= d_in, ldw % 8 == 0, 16-byte aligned; y: device bf16 [T, ldy];
+ * token_adapter: the device int32 [T] ids that seg was built from, with
+ * n_adapters = view->n_adapters.  The call runs the shrink stage into
+ * seg->h_scratch (by token) and keeps per-token scales in seg->scratch, so
+ * calls sharing a segment buffer must be ordered on one stream, and the
+ * buffer must be rebuilt before it serves lora_apply's staged paths again.
+ * y must not overlap x, w0 or the segment buffer.  The base product runs on
+ * the tensor cores through TMA tensor maps: LORA_ERR_UNSUPPORTED when the
+ * driver offers no tensor-map encoder.
+ */
+lora_status_t lora_base_apply(const void* x, int64_t ldx, const void* w0, int64_t ldw, void* y, int64_t ldy,
+                              const int32_t* token_adapter, const lora_segments_t* seg,
+                              const lora_pool_view_t* view, int32_t* dev_err, lora_stream_t stream);
+
+/**
  * Decode form without segments: each token t gathers its own adapter
  * token_adapter[t] (device int32 [T], -1 = no adapter), one token per request
  * (the batched gather path for size-1 segments of "Multi-LoRA serving: ...",

@@ -50,6 +50,7 @@ EXPORTED = (
     "lora_apply_fixed_scratch",
     "lora_bgmv",
     "lora_bgmv_ex",
+    "lora_base_apply",
     "lora_pool_pages_needed",
     "lora_status_string",
     "lora_abi_version",
@@ -147,6 +148,8 @@ def lib():
         L.lora_apply_fixed_scratch.argtypes = [vp, i64, vp, i64, seg_p, view_p, vp, vp]
         L.lora_bgmv.restype = i32
         L.lora_bgmv.argtypes = [vp, i64, vp, i64, vp, i32, view_p, vp, vp]
+        L.lora_base_apply.restype = i32
+        L.lora_base_apply.argtypes = [vp, i64, vp, i64, vp, i64, vp, seg_p, view_p, vp, vp]
         L.lora_bgmv_ex.restype = i32
         L.lora_bgmv_ex.argtypes = [vp, i64, vp, i64, vp, i32, view_p, ctypes.c_uint32, vp, vp]
         L.lora_pool_pages_needed.restype = i64
@@ -381,6 +384,14 @@ def debug_wait_probe(cycles: int) -> None:
 def launch_count() -> int:
     """Kernels the library has launched in this process (a recorded graph counts once)."""
     return int(lib().lora_launch_count())
+
+
+def lora_base_apply(x: torch.Tensor, w0: torch.Tensor, y: torch.Tensor, token_adapter: torch.Tensor, seg: Segments,
+                    view: PoolView, err: Optional[torch.Tensor] = None, stream=None):
+    """y = bf16(x W0^T + s_i (x A_i^T) B_i), y written only; w0 bf16 [d_out, ldw >= d_in]."""
+    _check(lib().lora_base_apply(_ptr(x), _ld(x), _ptr(w0), _ld(w0), _ptr(y), _ld(y), _ptr(token_adapter),
+                                 ctypes.byref(seg.c), ctypes.byref(view.c), _ptr(err), _stream(stream)),
+           "lora_base_apply")
 
 
 def lora_bgmv(x: torch.Tensor, y: torch.Tensor, token_adapter: torch.Tensor, view: PoolView,

@@ -453,6 +453,29 @@ lora_status_t lora_sgmv_backward(const void* x, int64_t ldx, const void* dy, int
   return run_segmented(kModeExpand, nullptr, 0, dx, lddx, u, ldh, seg, &vt, dev_err, s);
 }
 
+lora_status_t lora_base_apply(const void* x, int64_t ldx, const void* w0, int64_t ldw, void* y, int64_t ldy,
+                              const int32_t* token_adapter, const lora_segments_t* seg,
+                              const lora_pool_view_t* view, int32_t* dev_err, lora_stream_t stream) {
+  lora_status_t st = check_view(view);
+  if (st != LORA_OK) return st;
+  if ((st = check_seg(seg)) != LORA_OK) return st;
+  const int T = seg->T;
+  if ((st = check_act(x, ldx, view->d_in, T)) != LORA_OK) return st;
+  if ((st = check_act(y, ldy, view->d_out, T)) != LORA_OK) return st;
+  if (T > 0 && token_adapter == nullptr) return LORA_ERR_INVALID_ARG;
+  if (w0 == nullptr || !aligned16(w0) || ldw < view->d_in || ldw % 8 != 0) return LORA_ERR_INVALID_ARG;
+  if (T == 0) return LORA_OK;
+  if (overlap(x, (long long)T * ldx * 2, y, (long long)T * ldy * 2) ||
+      overlap(w0, (long long)view->d_out * ldw * 2, y, (long long)T * ldy * 2))
+    return LORA_ERR_INVALID_ARG;
+  if (!base_gemm_ok(view)) return LORA_ERR_UNSUPPORTED;
+  const cudaStream_t s = (cudaStream_t)stream;
+  st = run_segmented(kModeShrink, x, ldx, nullptr, 0, seg->h_scratch, LORA_MAX_RANK, seg, view, dev_err, s);
+  if (st != LORA_OK) return st;
+  return launch_base_gemm(x, ldx, w0, ldw, y, ldy, seg->h_scratch, LORA_MAX_RANK, reinterpret_cast<float*>(seg->scratch),
+                          token_adapter, T, seg, view, dev_err, s);
+}
+
 lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy, const int32_t* token_adapter,
                         int32_t T, const lora_pool_view_t* view, int32_t* dev_err, lora_stream_t stream) {
   return lora_bgmv_ex(x, ldx, y, ldy, token_adapter, T, view, 0u, dev_err, stream);
