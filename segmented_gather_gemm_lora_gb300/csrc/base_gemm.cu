@@ -18,8 +18,9 @@
 // 128-byte swizzle, into a 4-stage ring.  Warp 1 issues tcgen05.mma (M = 128,
 // N = 256, bf16, fp32 accumulator in tensor memory), alternating two
 // accumulators so that a tile's epilogue overlaps the next tile's MMAs.
-// Warps 2-5 run the epilogue, one tile row per thread (the tensor-memory lane
-// quarter of its warp): 32 columns at a time from tensor memory, plus the
+// Warps 2-17 run the epilogue, one tile row and a quarter of the tile's
+// columns per thread (the tensor-memory lane quarter of its warp): 32 columns
+// at a time from tensor memory, plus the
 // row's adapter term on the CUDA cores (fp32 FMA over the rank in order, from
 // B_i's rows for the tile staged once per adapter in shared memory), rounded
 // once to bf16 and stored.
@@ -36,9 +37,10 @@ namespace {
 
 constexpr int kBM = 128, kBN = 256, kBK = 64;
 constexpr int kBStages = 4;
-constexpr int kBEpiWarps = 4;   // one per tensor-memory lane quarter
+constexpr int kBEpiWarps = 16;  // four per tensor-memory lane quarter, one per quarter of the tile's columns
 constexpr int kBEpiThreads = 32 * kBEpiWarps;
-constexpr int kBThreads = 64 + kBEpiThreads;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kBThreads = 64 + kBEpiThreads;  // warp 0 TMA, warp 1 MMA, warps 2-17 epilogue
+constexpr int kBEpiChunks = kBN / 32 / (kBEpiWarps / 4);  // 32-column chunks per epilogue warp
 constexpr int kBABytes = kBM * kBK * 2;
 constexpr int kBBBytes = kBN * kBK * 2;
 constexpr int kBStageBytes = kBABytes + kBBBytes;  // 48 KB
@@ -66,16 +68,16 @@ struct BaseArgs {
   long long probe;
 };
 
-// The epilogue warps (128 threads) meet at named barrier 1; the other warps
+// The epilogue warps (512 threads) meet at named barrier 1; the other warps
 // never use it.
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 // true in every epilogue thread iff `p` holds in all of them (a barrier too)
 __device__ __forceinline__ bool epi_all(bool p) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred q, o;\n\t"
       "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.and.pred o, 1, 128, q;\n\t"
+      "bar.red.and.pred o, 1, 512, q;\n\t"
       "selp.u32 %0, 1, 0, o;\n\t}"
       : "=r"(r)
       : "r"((uint32_t)p)
@@ -90,7 +92,7 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
   uint64_t* full = bars;                    // [stages] TMA bytes
   uint64_t* empty = bars + kBStages;        // [stages] MMA commit
   uint64_t* acc_full = empty + kBStages;    // [2] MMA commit: a tile's accumulator is complete
-  uint64_t* acc_empty = acc_full + 2;       // [2] the 4 epilogue warps
+  uint64_t* acc_empty = acc_full + 2;       // [2] the 16 epilogue warps
   uint64_t* mma_done = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -194,7 +196,8 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
     // rounds; each round reads every column of the accumulator once per warp.
     const int quarter = warp & 3;  // the tensor-memory lanes this warp may read
     const int row = quarter * 32 + lane;
-    const int et = tid - 64;       // 0..127
+    const int part = (warp - 2) >> 2;  // the tile's columns [64 part, 64 part + 64)
+    const int et = tid - 64;           // 0..511
     const DevView& v = a.v;
     const int shift = v.page_shift;
     const long long pmask = (1LL << shift) - 1;
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
           epi_bar();
         }
         const bool mine = !done && (round == 0 ? ad < 0 : ad == cur);
-        for (int c = 0; c < kBN / 32; ++c) {
+        for (int c = kBEpiChunks * part; c < kBEpiChunks * (part + 1); ++c) {
           __syncwarp();  // the warp converged for the collective load
           uint32_t raw[32];
           tmem_ld32_nowait(tmem + ab * kBN + c * 32 + ((uint32_t)(quarter * 32) << 16), raw);
