@@ -38,6 +38,7 @@ namespace {
 constexpr int kBThreads = 256;
 constexpr int kBCols = 128;              // gradient columns per unit
 constexpr int kBTok = 16;                // tokens per step (the mma k dimension)
+constexpr int kBStages = 4;              // steps in flight
 constexpr int kBQStride = kBCols * 2 + 16;   // bytes per staged dy / x row (padded: conflict-free ldmatrix)
 constexpr int kBPStride = kBTok * 2 + 16;  // bytes per staged rank row of h / u (16 tokens, bf16, padded)
 
@@ -78,7 +79,11 @@ __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], uint32_t a0, uint32_
 }
 
 __global__ void __launch_bounds__(kBThreads) grad_kernel(const __grid_constant__ GradArgs a) {
-  __shared__ __align__(128) uint8_t qs[kBTok * kBQStride];      // dy or x rows of the block
+  // a ring of kBStages steps: each holds 16 token rows of dy (or x) for the block's
+  // columns and the same tokens' h (or u) rows as fp32; the step being computed
+  // has its h / u converted into bf16 hi + lo parts, transposed, in phi / plo
+  __shared__ __align__(128) uint8_t qs[kBStages][kBTok * kBQStride];
+  __shared__ __align__(16) float hraw[kBStages][kBTok][LORA_MAX_RANK];
   __shared__ __align__(128) uint8_t phi[LORA_MAX_RANK * kBPStride];  // h or u transposed [rank row][token], bf16 hi
   __shared__ __align__(128) uint8_t plo[LORA_MAX_RANK * kBPStride];  // lo part
   __shared__ int info[6];  // p0, count, rank, skip, a_page0 / b_page0 of the unit's matrix, scale bits
@@ -120,37 +125,45 @@ __global__ void __launch_bounds__(kBThreads) grad_kernel(const __grid_constant__
     const float* P = isB ? a.h : a.u;
     const uint16_t* Q = isB ? a.dy : a.x;
     const long long ldq = isB ? a.lddy : a.ldx;
-    float acc[8][4];
-#pragma unroll
-    for (int jt = 0; jt < 8; ++jt) acc[jt][0] = acc[jt][1] = acc[jt][2] = acc[jt][3] = 0.f;
-    for (int t0 = 0; t0 < count; t0 += kBTok) {
-      // stage: row tid / 16 of the 16 tokens, 16-byte piece tid % 16 of the block's columns
-      {
+    const int nsteps = (count + kBTok - 1) / kBTok;
+    // step i's copies: row tid / 16 of its 16 tokens, 16-byte piece tid % 16 of the
+    // block's columns and of the token's h / u row (zero past the rank or the tokens)
+    auto load_step = [&](int i) {
+      if (i < nsteps) {
+        const int st = i % kBStages;
         const int tr = tid >> 4, pc = tid & 15;
+        const int t0 = i * kBTok;
         const int tok = t0 + tr < count ? a.perm[p0 + t0 + tr] : -1;
         const int c = col0 + 8 * pc;
         const bool valid = tok >= 0 && c < d;  // d % 8 == 0: a piece is all in or all out
-        cp_async16(smem_u32(qs + tr * kBQStride + pc * 16), valid ? Q + (long long)tok * ldq + c : Q, valid);
-        // h / u row tr, columns 4 pc .. 4 pc + 3 as bf16 hi + lo (zero past the rank or the tokens)
-        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-        const int j = 4 * pc;
-        if (tok >= 0 && j < r) {
-          const float* prow = P + (long long)tok * a.ldh + j;
-          f.x = prow[0];
-          f.y = j + 1 < r ? prow[1] : 0.f;
-          f.z = j + 2 < r ? prow[2] : 0.f;
-          f.w = j + 3 < r ? prow[3] : 0.f;
-        }
+        cp_async16(smem_u32(&qs[st][tr * kBQStride + pc * 16]), valid ? Q + (long long)tok * ldq + c : Q, valid);
+        const bool hv = tok >= 0 && 4 * pc < r;
+        cp_async16(smem_u32(&hraw[st][tr][4 * pc]), hv ? P + (long long)tok * a.ldh + 4 * pc : P, hv);
+      }
+      cp_async_commit();  // one group per step, empty past the end, so the waits count evenly
+    };
+    float acc[8][4];
+#pragma unroll
+    for (int jt = 0; jt < 8; ++jt) acc[jt][0] = acc[jt][1] = acc[jt][2] = acc[jt][3] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kBStages - 1; ++i) load_step(i);
+    for (int i = 0; i < nsteps; ++i) {
+      cp_async_wait<kBStages - 2>();  // this thread's copies of step i have landed
+      __syncthreads();                // everyone's; the stage of step i - 1 and phi / plo are free
+      load_step(i + kBStages - 1);
+      const int st = i % kBStages;
+      {  // h / u of step i: rank row j + e, token tr, as bf16 hi + lo (columns past r are zero)
+        const int tr = tid >> 4, j = 4 * (tid & 15);
+        const float4 f = *reinterpret_cast<const float4*>(&hraw[st][tr][j]);
         const float fv[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {  // transposed: rank row j + e, token tr
-          const __nv_bfloat16 hi = __float2bfloat16_rn(fv[e]);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(fv[e] - __bfloat162float(hi));
+        for (int e = 0; e < 4; ++e) {
+          const float val = j + e < r ? fv[e] : 0.f;
+          const __nv_bfloat16 hi = __float2bfloat16_rn(val);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(val - __bfloat162float(hi));
           *reinterpret_cast<__nv_bfloat16*>(phi + (j + e) * kBPStride + tr * 2) = hi;
           *reinterpret_cast<__nv_bfloat16*>(plo + (j + e) * kBPStride + tr * 2) = lo;
         }
-        cp_async_commit();
-        cp_async_wait<0>();
       }
       __syncthreads();
       // warp w: columns 16 w .. 16 w + 15 of the block (A operand: the staged rows
@@ -158,7 +171,7 @@ __global__ void __launch_bounds__(kBThreads) grad_kernel(const __grid_constant__
       if (col0 + 16 * warp < d) {
         const int trow = (lane & 7) + 8 * (lane >> 4), tcol = 16 * warp + 8 * ((lane >> 3) & 1);
         uint32_t a0, a1, a2, a3;
-        ldsm_x4_trans(smem_u32(qs + trow * kBQStride + tcol * 2), a0, a1, a2, a3);
+        ldsm_x4_trans(smem_u32(&qs[st][trow * kBQStride + tcol * 2]), a0, a1, a2, a3);
         // B operand: rank rows 8 jt .. 8 jt + 7 of the transposed h / u, tokens 0-7
         // (lanes 0-7) and 8-15 (lanes 8-15)
         const int prow = lane & 7, pcol = 16 * ((lane >> 3) & 1);
@@ -172,8 +185,9 @@ __global__ void __launch_bounds__(kBThreads) grad_kernel(const __grid_constant__
           mma_m16n8k16(acc[jt], a0, a1, a2, a3, b0, b1);
         }
       }
-      __syncthreads();  // the stage is free for the next 16 tokens
     }
+    cp_async_wait<0>();
+    __syncthreads();  // every copy of this unit landed and every warp is done with the ring
     // acc[jt]: columns 16 w + lane / 4 (+ 8), rank rows 8 jt + 2 (lane % 4) (+ 1)
     const int g = lane >> 2, q = lane & 3;
 #pragma unroll
