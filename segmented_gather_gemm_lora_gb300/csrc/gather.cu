@@ -52,8 +52,9 @@ constexpr int kGCons = 8;            // consumer warps
 constexpr int kGProd = kGCons;       // the first producer warp
 constexpr int kGSched = kGCons + 1;  // the scheduler warp
 constexpr int kGProd2 = kGCons + 2;  // the second producer warp
-constexpr int kGProds = 2;           // producer warps: a stage's copies alternate between them
-constexpr int kGThreads = 32 * (kGCons + 3);
+constexpr int kGProd3 = kGCons + 3;  // the third producer warp
+constexpr int kGProds = 3;           // producer warps: a stage's copies go round them
+constexpr int kGThreads = 32 * (kGCons + 4);
 constexpr int kGConsThreads = 32 * kGCons;
 constexpr int kMaxCluster = 8;
 constexpr int kStages = 4;
@@ -456,14 +457,14 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       }
     }
     if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
-  } else if (warp == kGProd || warp == kGProd2) {
+  } else if (warp == kGProd || warp == kGProd2 || warp == kGProd3) {
     // ---------------- producers ----------------
-    // Both producer warps walk the same units and stages; a stage's copies
-    // (adapter rows, then token rows) alternate between them, copy i going to
-    // producer i % 2, since one warp alone issues bulk copies too slowly to keep
+    // The producer warps walk the same units and stages; a stage's copies
+    // (adapter rows, then token rows) go round them, copy i to producer
+    // i % kGProds, since one warp alone issues bulk copies too slowly to keep
     // the memory system busy.  Each arrives on the stage barrier with the bytes
     // of its own copies; producer 0 writes the stage's record.
-    const int pi = warp == kGProd ? 0 : 1;
+    const int pi = warp == kGProd ? 0 : warp == kGProd2 ? 1 : 2;
     uint32_t g = 0;  // stages posted
     auto take_stage = [&]() -> uint32_t {
       const uint32_t st = g % kStages;
@@ -537,10 +538,11 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
               r2.flags = flags;
               recs[st] = r2;
             }
-            mbar_arrive_expect_tx(bar, (uint32_t)((ncopy + 1 - pi) / 2) * rowb);  // copies pi, pi + 2, ...
+            // copies pi, pi + kGProds, ...
+            mbar_arrive_expect_tx(bar, (uint32_t)((ncopy + kGProds - 1 - pi) / kGProds) * rowb);
           }
           __syncwarp();
-          const int idx = 2 * lane + pi;  // this lane's copy of the stage
+          const int idx = kGProds * lane + pi;  // this lane's copy of the stage
           const int tk = __shfl_sync(0xffffffffu, mytok, (idx - nrows) & (kNT - 1));
           if (idx < nrows) {
             const long long rowlen = shrink ? v.d_in : v.d_out;
