@@ -22,11 +22,12 @@
 // CTA 0 of a cluster claiming and handing the claim to its peers, when the
 // segments give one; one-token units go round-robin), resolves each unit's
 // tokens and adapter, checks every page slot of the adapter and caches its
-// physical pages, one unit ahead of the producer.  Warp 8 produces: it stages
-// 16-row chunks of the adapter (1 KB row runs, translated through the page
-// table, "Multi-LoRA Serving in Production", section "Unified Paged Memory";
-// one bulk copy per row run and page) with the unit's token rows for the same
-// columns into a 4-stage ring; every stage carries a record of what it holds.
+// physical pages, one unit ahead of the producers.  Warps 8, 10 and 11
+// produce: they stage 16-row chunks of the adapter (1 KB row runs, translated
+// through the page table, "Multi-LoRA Serving in Production", section "Unified
+// Paged Memory"; one bulk copy per row run and page) with the unit's token rows
+// for the same columns into a 4-stage ring, a stage's copies going round the
+// three warps; every stage carries a record of what it holds.
 // Warps 0-7 consume the ring.  Between a group's shrink and expand each CTA
 // pushes its partial h into every peer's shared memory (asynchronous stores
 // whose bytes complete on the peer's own mbarrier) and sums what it received

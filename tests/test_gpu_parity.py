@@ -385,6 +385,41 @@ def test_bgmv_static_adapters_chain_in_graph():
     assert int(err.item()) == 0
 
 
+def test_bgmv_rows_independent_of_the_batch():
+    """A few adapters shared by many tokens (runs of one adapter included), -1 ids and a
+    bad id, at T = 256 and 257: against the oracle, with the oracle's error word; every
+    token's row is the same, bit for bit, when the batch is shuffled, and when the same
+    256 tokens come with 44 more -1 tokens after them."""
+    rng = np.random.default_rng(4242)
+    d = 2048
+    pool = W.build_pool(rng, d, d, [16, 4, 9, 16, 1, 12], max_rank=16)
+    for T in (256, 257):
+        ids = rng.integers(-1, pool.n_adapters, size=T).astype(np.int32)
+        ids[T - 9:] = 2
+        ids[17] = pool.n_adapters + 3
+        batch = W.make_batch(rng, ids, d, d, ldx=d + 8, ldy=d + 24)
+        y, err = run_bgmv(batch, pool)
+        ref, oerr = oracle_apply(batch.x, batch.y0, ids, pool)
+        assert err == oerr == B.LORA_DERR_BAD_ADAPTER
+        compare_bf16(y[:, :d], ref, "decode kernel T=%d" % T)
+        assert np.array_equal(y[ids < 0], batch.y0[ids < 0])
+        assert np.array_equal(y[:, d:], batch.y0[:, d:])
+        perm = rng.permutation(T)
+        shuf = W.Batch(x=batch.x[perm], y0=batch.y0[perm], ids=ids[perm], d_in=d, d_out=d)
+        ys, es = run_bgmv(shuf, pool)
+        assert es == err
+        assert np.array_equal(ys, y[perm]), "a token's row depends on its place in the batch (T=%d)" % T
+    ids = rng.integers(0, 3, size=256).astype(np.int32)
+    batch = W.make_batch(rng, ids, d, d)
+    yg, eg = run_bgmv(batch, pool)
+    pad = np.full(44, -1, dtype=np.int32)
+    big = W.Batch(x=np.concatenate([batch.x, batch.x[:44]]), y0=np.concatenate([batch.y0, batch.y0[:44]]),
+                  ids=np.concatenate([ids, pad]), d_in=d, d_out=d)
+    yu, eu = run_bgmv(big, pool)
+    assert eg == eu == 0
+    assert np.array_equal(yg, yu[:256]), "a token's row depends on the batch's size"
+
+
 def test_bgmv_decode_kernel_shapes_and_pages():
     """The decode kernel on the shapes it takes: one CTA (d = 256), slices narrower than
     a sub-slice, d_in != d_out, 1024-element pages, rows that cross pages (d = 1000),
