@@ -17,11 +17,12 @@
 //
 // Gradient kernel.  A unit is (segment, matrix, 128-column block): the block's
 // columns of dB_i (a slice of d_out) or of dA_i (a slice of d_in), for all the
-// adapter's r_i rows.  Its CTA walks the segment's tokens 16 at a time: the 16
-// token rows of dy (or x) for the block's columns and of h (or u) go to shared
-// memory (h and u as bf16 hi + lo parts), and each of the 8 warps accumulates
-// its 16 columns x r_i rows with mma.sync m16n8k16 (the contraction runs over
-// the tokens).  At the end each element of the block is added once into the
+// adapter's r_i rows.  Its CTA walks the segment's tokens 32 at a time, four
+// steps in flight: the token rows of dy (or x) for the block's columns and of h
+// (or u) arrive in shared memory by asynchronous copies, their token indices
+// four steps earlier, and each of the 8 warps accumulates its 16 columns x r_i
+// rows with mma.sync m16n8k16 (the contraction runs over the tokens, 16 per
+// MMA), taking h / u from the fp32 rows as bf16 hi + lo parts in registers.  At the end each element of the block is added once into the
 // gradient pool, at its pool position, by one atomic add: with GROUP segments
 // an adapter has one segment, so a call's sums are deterministic.
 #include <algorithm>
@@ -37,10 +38,17 @@ namespace {
 
 constexpr int kBThreads = 256;
 constexpr int kBCols = 128;              // gradient columns per unit
-constexpr int kBTok = 16;                // tokens per step (the mma k dimension)
+constexpr int kBTok = 16;                // tokens per MMA (its k dimension)
+constexpr int kBStepTok = 32;            // tokens per step
 constexpr int kBStages = 4;              // steps in flight
-constexpr int kBQStride = kBCols * 2 + 16;   // bytes per staged dy / x row (padded: conflict-free ldmatrix)
-constexpr int kBPStride = kBTok * 2 + 16;  // bytes per staged rank row of h / u (16 tokens, bf16, padded)
+constexpr int kBTokRing = 2 * kBStages;  // token-index slots: step m's indices arrive kBStages steps ahead
+constexpr int kBQStride = kBCols * 2 + 16;    // bytes per staged dy / x row (padded: conflict-free ldmatrix)
+constexpr int kBHStride = LORA_MAX_RANK + 4;  // floats per staged h / u row (padded: conflict-free fragments)
+constexpr size_t kBOffH = (size_t)kBStages * kBStepTok * kBQStride;
+constexpr size_t kBOffTok = kBOffH + (size_t)kBStages * kBStepTok * kBHStride * sizeof(float);
+constexpr size_t kBSmem = kBOffTok + (size_t)kBTokRing * kBStepTok * sizeof(int);
+static_assert(kBOffH % 16 == 0 && (kBHStride * 4) % 16 == 0, "16-byte copy destinations");
+static_assert(kBStepTok * 16 == 2 * kBThreads, "two 16-byte pieces of a row per thread and step");
 
 struct GradArgs {
   const uint16_t* x;
@@ -59,15 +67,17 @@ struct GradArgs {
   int32_t* err;
 };
 
+// 4-byte global -> shared copy (LSU async copy, through L1)
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                               uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr)
                : "memory");
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr) : "memory");
 }
 __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                              uint32_t b0, uint32_t b1) {
@@ -79,13 +89,12 @@ __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], uint32_t a0, uint32_
 }
 
 __global__ void __launch_bounds__(kBThreads) grad_kernel(const __grid_constant__ GradArgs a) {
-  // a ring of kBStages steps: each holds 16 token rows of dy (or x) for the block's
-  // columns and the same tokens' h (or u) rows as fp32; the step being computed
-  // has its h / u converted into bf16 hi + lo parts, transposed, in phi / plo
-  __shared__ __align__(128) uint8_t qs[kBStages][kBTok * kBQStride];
-  __shared__ __align__(16) float hraw[kBStages][kBTok][LORA_MAX_RANK];
-  __shared__ __align__(128) uint8_t phi[LORA_MAX_RANK * kBPStride];  // h or u transposed [rank row][token], bf16 hi
-  __shared__ __align__(128) uint8_t plo[LORA_MAX_RANK * kBPStride];  // lo part
+  // a ring of kBStages steps: each holds 32 token rows of dy (or x) for the block's
+  // columns and the same tokens' h (or u) rows as fp32; and the steps' token indices
+  extern __shared__ __align__(128) uint8_t sm[];
+  uint8_t* const qs = sm;                                        // [stage][token][kBQStride bytes]
+  float* const hraw = reinterpret_cast<float*>(sm + kBOffH);     // [stage][token][kBHStride]
+  int* const tokring = reinterpret_cast<int*>(sm + kBOffTok);    // [slot][token]
   __shared__ int info[6];  // p0, count, rank, skip, a_page0 / b_page0 of the unit's matrix, scale bits
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const DevView& v = a.v;
@@ -125,71 +134,85 @@ __global__ void __launch_bounds__(kBThreads) grad_kernel(const __grid_constant__
     const float* P = isB ? a.h : a.u;
     const uint16_t* Q = isB ? a.dy : a.x;
     const long long ldq = isB ? a.lddy : a.ldx;
-    const int nsteps = (count + kBTok - 1) / kBTok;
-    // step i's copies: row tid / 16 of its 16 tokens, 16-byte piece tid % 16 of the
-    // block's columns and of the token's h / u row (zero past the rank or the tokens)
+    const int nsteps = (count + kBStepTok - 1) / kBStepTok;
+    // Step m's token indices go to their ring slot by asynchronous copies, kBStages
+    // steps before the step's own copies need them, so no copy waits on an index load.
+    auto load_idx = [&](int m, int e) {
+      const int ti = m * kBStepTok + e;
+      if (ti < count) cp_async4(smem_u32(&tokring[(m % kBTokRing) * kBStepTok + e]), a.perm + p0 + ti);
+    };
+    // step i's copies: rows tr and tr + 16 of its 32 tokens, 16-byte piece pc of the
+    // block's columns and of the token's h / u row (zero past the rank or the
+    // tokens; pieces past the rank rounded up to 8 are not read); with them, in the
+    // same group, the indices of step i + kBStages
     auto load_step = [&](int i) {
       if (i < nsteps) {
         const int st = i % kBStages;
-        const int tr = tid >> 4, pc = tid & 15;
-        const int t0 = i * kBTok;
-        const int tok = t0 + tr < count ? a.perm[p0 + t0 + tr] : -1;
+        const int pc = tid & 15;
         const int c = col0 + 8 * pc;
-        const bool valid = tok >= 0 && c < d;  // d % 8 == 0: a piece is all in or all out
-        cp_async16(smem_u32(&qs[st][tr * kBQStride + pc * 16]), valid ? Q + (long long)tok * ldq + c : Q, valid);
-        const bool hv = tok >= 0 && 4 * pc < r;
-        cp_async16(smem_u32(&hraw[st][tr][4 * pc]), hv ? P + (long long)tok * a.ldh + 4 * pc : P, hv);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int tr = (tid >> 4) + 16 * h2;
+          const int t = i * kBStepTok + tr;
+          const int tok = t < count ? tokring[(i % kBTokRing) * kBStepTok + tr] : -1;
+          const bool valid = tok >= 0 && c < d;  // d % 8 == 0: a piece is all in or all out
+          cp_async16(smem_u32(qs + ((size_t)st * kBStepTok + tr) * kBQStride + pc * 16),
+                     valid ? Q + (long long)tok * ldq + c : Q, valid);
+          if (4 * pc < rpad) {
+            const bool hv = tok >= 0 && 4 * pc < r;
+            cp_async16(smem_u32(hraw + ((size_t)st * kBStepTok + tr) * kBHStride + 4 * pc),
+                       hv ? P + (long long)tok * a.ldh + 4 * pc : P, hv);
+          }
+        }
       }
+      if (tid < kBStepTok && i + kBStages < nsteps) load_idx(i + kBStages, tid);
       cp_async_commit();  // one group per step, empty past the end, so the waits count evenly
     };
+    if (tid < kBStages * kBStepTok && tid / kBStepTok < nsteps) load_idx(tid / kBStepTok, tid % kBStepTok);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();  // the first kBStages steps' indices
     float acc[8][4];
 #pragma unroll
     for (int jt = 0; jt < 8; ++jt) acc[jt][0] = acc[jt][1] = acc[jt][2] = acc[jt][3] = 0.f;
 #pragma unroll
     for (int i = 0; i < kBStages - 1; ++i) load_step(i);
+    const int g = lane >> 2, q = lane & 3;
     for (int i = 0; i < nsteps; ++i) {
-      cp_async_wait<kBStages - 2>();  // this thread's copies of step i have landed
-      __syncthreads();                // everyone's; the stage of step i - 1 and phi / plo are free
+      cp_async_wait<kBStages - 2>();  // this thread's copies of step i, and the indices up to step i + kBStages
+      __syncthreads();                // everyone's; the stage of step i - 1 is free
       load_step(i + kBStages - 1);
       const int st = i % kBStages;
-      {  // h / u of step i: rank row j + e, token tr, as bf16 hi + lo (columns past r are zero)
-        const int tr = tid >> 4, j = 4 * (tid & 15);
-        const float4 f = *reinterpret_cast<const float4*>(&hraw[st][tr][j]);
-        const float fv[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float val = j + e < r ? fv[e] : 0.f;
-          const __nv_bfloat16 hi = __float2bfloat16_rn(val);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(val - __bfloat162float(hi));
-          *reinterpret_cast<__nv_bfloat16*>(phi + (j + e) * kBPStride + tr * 2) = hi;
-          *reinterpret_cast<__nv_bfloat16*>(plo + (j + e) * kBPStride + tr * 2) = lo;
-        }
-      }
-      __syncthreads();
       // warp w: columns 16 w .. 16 w + 15 of the block (A operand: the staged rows
-      // transposed, k = token); the rank rows 8 at a time (B operand: h / u)
+      // transposed, k = token); the rank rows 8 at a time (B operand: h / u, as
+      // bf16 hi and lo parts, two MMAs each); 16 tokens per MMA, in token order
       if (col0 + 16 * warp < d) {
-        const int trow = (lane & 7) + 8 * (lane >> 4), tcol = 16 * warp + 8 * ((lane >> 3) & 1);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_trans(smem_u32(&qs[st][trow * kBQStride + tcol * 2]), a0, a1, a2, a3);
-        // B operand: rank rows 8 jt .. 8 jt + 7 of the transposed h / u, tokens 0-7
-        // (lanes 0-7) and 8-15 (lanes 8-15)
-        const int prow = lane & 7, pcol = 16 * ((lane >> 3) & 1);
 #pragma unroll
-        for (int jt = 0; jt < 8; ++jt) {
-          if (8 * jt >= rpad) break;
-          uint32_t b0, b1;
-          ldsm_x2(smem_u32(phi + (8 * jt + prow) * kBPStride + pcol), b0, b1);
-          mma_m16n8k16(acc[jt], a0, a1, a2, a3, b0, b1);
-          ldsm_x2(smem_u32(plo + (8 * jt + prow) * kBPStride + pcol), b0, b1);
-          mma_m16n8k16(acc[jt], a0, a1, a2, a3, b0, b1);
+        for (int ks = 0; ks < kBStepTok / kBTok; ++ks) {
+          if (i * kBStepTok + ks * kBTok >= count) break;  // nothing but zero rows left
+          const int trow = ks * kBTok + (lane & 7) + 8 * (lane >> 4), tcol = 16 * warp + 8 * ((lane >> 3) & 1);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(smem_u32(qs + ((size_t)st * kBStepTok + trow) * kBQStride + tcol * 2), a0, a1, a2, a3);
+          // the lane's B entries: tokens 2q, 2q + 1 (b0) and 2q + 8, 2q + 9 (b1) of the
+          // MMA's 16, rank row 8 jt + g
+          const float* hb = hraw + ((size_t)st * kBStepTok + ks * kBTok + 2 * q) * kBHStride + g;
+#pragma unroll
+          for (int jt = 0; jt < 8; ++jt) {
+            if (8 * jt >= rpad) break;
+            const float h0 = hb[8 * jt], h1 = hb[kBHStride + 8 * jt];
+            const float h2 = hb[8 * kBHStride + 8 * jt], h3 = hb[9 * kBHStride + 8 * jt];
+            const uint32_t bh0 = pack_bf16x2(h0, h1), bh1 = pack_bf16x2(h2, h3);
+            const uint32_t bl0 = pack_bf16x2(h0 - bf_lo(bh0), h1 - bf_hi(bh0));
+            const uint32_t bl1 = pack_bf16x2(h2 - bf_lo(bh1), h3 - bf_hi(bh1));
+            mma_m16n8k16(acc[jt], a0, a1, a2, a3, bh0, bh1);
+            mma_m16n8k16(acc[jt], a0, a1, a2, a3, bl0, bl1);
+          }
         }
       }
     }
     cp_async_wait<0>();
     __syncthreads();  // every copy of this unit landed and every warp is done with the ring
     // acc[jt]: columns 16 w + lane / 4 (+ 8), rank rows 8 jt + 2 (lane % 4) (+ 1)
-    const int g = lane >> 2, q = lane & 3;
 #pragma unroll
     for (int jt = 0; jt < 8; ++jt) {
       if (8 * jt >= rpad) break;
@@ -230,7 +253,9 @@ lora_status_t launch_grad(const void* x, long long ldx, const void* dy, long lon
   const long long per_seg = (view->d_out + kBCols - 1) / kBCols + (view->d_in + kBCols - 1) / kBCols;
   long long grid = (long long)sm_count() * 8;
   grid = std::min(grid, std::max(1LL, (long long)seg->T * per_seg));
-  return launch_pdl((const void*)grad_kernel, dim3((unsigned)grid), dim3(kBThreads), 0, stream, 0, &a) == cudaSuccess
+  if (ensure_smem_attr((const void*)grad_kernel, kBSmem) != cudaSuccess) return LORA_ERR_CUDA;
+  return launch_pdl((const void*)grad_kernel, dim3((unsigned)grid), dim3(kBThreads), kBSmem, stream, 0, &a) ==
+                 cudaSuccess
              ? LORA_OK
              : LORA_ERR_CUDA;
 }

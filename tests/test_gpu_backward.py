@@ -111,6 +111,25 @@ def test_backward_group_sums_are_repeatable_bitwise():
         assert np.array_equal(dx, outs[0][0]) and np.array_equal(grad, outs[0][1])
 
 
+@pytest.mark.parametrize("mode", [B.LORA_SEG_GROUP, B.LORA_SEG_CONTIGUOUS])
+def test_backward_long_segments(mode):
+    """Segments of 2 000, 1 100 and 900 tokens (many 32-token steps of the gradient
+    kernel, a partial last step) next to short ones: against the oracle, and, with GROUP
+    segments, bit for bit the same on a second call."""
+    pool, batch, g = case(78, 1024, 1024, [16, 64, 8, 32, 16, 8], [2000, 2, 1100, 1, 40, 900],
+                          shuffle=(mode == B.LORA_SEG_GROUP))
+    dx0 = W._normal_bf16(np.random.default_rng(79), (batch.T, 1024), 1.0)
+    dx, grad, err = run_backward(pool, batch, g, mode=mode, dx0=dx0)
+    assert err == 0
+    rdx, rgrad, oerr = oracle.lora_backward(batch.x, g, batch.ids, pool)
+    assert oerr == 0
+    compare_grad(grad, rgrad, owned_positions(pool), "long-segment gradients")
+    compare_bf16(dx, W.bf16_bits_to_f32(dx0).astype(np.float64) + rdx, "dx beside long segments")
+    if mode == B.LORA_SEG_GROUP:
+        dx2, grad2, err2 = run_backward(pool, batch, g, mode=mode, dx0=dx0)
+        assert err2 == 0 and np.array_equal(dx2, dx) and np.array_equal(grad2, grad)
+
+
 def test_backward_bad_adapters_add_nothing():
     pool, batch, g = case(76, 1024, 1024, [16, 16, 16], [140, 3, 150])
     pool.desc[1]["rank"] = 0  # not resident
