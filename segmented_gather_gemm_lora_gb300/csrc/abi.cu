@@ -292,9 +292,12 @@ static lora_status_t run_segmented(int mode, const void* x, long long ldx, void*
                                    float* yf = nullptr, long long ldyf = 0, bool staged = false) {
   // Long tiles go to the tensor-core kernels when the shapes allow it: the fused
   // kernel for lora_apply, the staged ones for the separate stages.
+  // A shrink alone goes to the fused kernel's shrink-only form when it can (its
+  // cluster sums the d_in slices on chip), else to the staged shrink.
   bool tc;
+  const bool fused_shrink = mode == kModeShrink && tc_fused_shrink_ok(view);
   if (mode == kModeApply) tc = staged ? tc_shrink_ok(view) && tc_expand_ok(view) : tc_fused_ok(view);
-  else if (mode == kModeShrink) tc = tc_shrink_ok(view);
+  else if (mode == kModeShrink) tc = fused_shrink || tc_shrink_ok(view);
   else tc = tc_expand_ok(view);
   lora_status_t st = launch_gather(mode, kSrcSegments, tc ? 1 : 0, x, ldx, y, ldy, h, ldh, seg, nullptr, 0, view,
                                    dev_err, s, yf, ldyf);
@@ -309,6 +312,12 @@ static lora_status_t run_segmented(int mode, const void* x, long long ldx, void*
     st = launch_shrink_tc(x, ldx, seg->h_scratch, LORA_MAX_RANK, 0, after_gather, seg, view, dev_err, s);
     if (st != LORA_OK) return st;
     return launch_expand_tc(seg->h_scratch, LORA_MAX_RANK, 0, 0, y, ldy, seg, view, dev_err, s, yf, ldyf);
+  }
+  if (fused_shrink) {
+    ProjCall p{x, ldx, nullptr, 0, nullptr, 0, view};
+    p.h = h;
+    p.ldh = ldh;
+    return launch_fused_tc(1, &p, seg, after_gather, dev_err, s, 1);
   }
   if (mode == kModeShrink) return launch_shrink_tc(x, ldx, h, ldh, 1, after_gather, seg, view, dev_err, s);
   return launch_expand_tc(h, ldh, 1, after_gather, y, ldy, seg, view, dev_err, s);

@@ -25,6 +25,11 @@
 //   expand   CTA c:  Y[128, slice c of d_out] = bf16(Y0 + H_hi . B_i + H_lo . B_i),
 //            64 output columns per stage (M = 128, N = 64, K = r padded to 16).
 // So h never leaves the chip, and x, y0 and y are each read or written once.
+// The shrink-only form (the shrink stage of "Multi-LoRA Serving in
+// Production", section "Punica and Segmented Gather Matrix-Vector
+// Multiplication (SGMV)", alone) runs the same shrink and exchange, and the
+// owner of each row also writes the row's unscaled h to global memory; no
+// expand stage runs.
 // Rows past a partial tile's end compute garbage that is never stored.
 //
 // Warp roles (10 warps).  Warp 0 resolves units (tile, adapter, page of each
@@ -91,7 +96,8 @@ struct FProj {
   const uint16_t* x;
   uint16_t* y;
   float* yf;  // non-null: fp32 output rows (y is then read only, for y0)
-  long long ldx, ldy, ldyf;
+  float* h;   // shrink-only form: h rows by token, unscaled, columns < r
+  long long ldx, ldy, ldyf, ldh;
   DevView v;
   int tma;  // every map valid
 };
@@ -108,6 +114,7 @@ struct FusedArgs {
   int n_proj;
   int klen;          // columns per d_in slice (a multiple of 64)
   int after_gather;  // launched right after this call's gather kernel (disjoint data): no wait at entry
+  int shrink_only;   // the shrink-only form: h out, no expand
   long long probe;   // > 0: the timeout probe's wait limit in cycles (lora_debug_wait_probe)
 };
 
@@ -278,7 +285,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
       const int k0 = (int)crank * a.klen;
       const int nk = (min(v.d_in, k0 + a.klen) - k0) / 64;
       const int n_nc = v.d_out / 64;
-      const int nc0 = (int)(((long long)n_nc * crank) / ncta), nc1 = (int)(((long long)n_nc * (crank + 1)) / ncta);
+      const int nc0 = (int)(((long long)n_nc * crank) / ncta);
+      const int nc1 = a.shrink_only ? nc0 : (int)(((long long)n_nc * (crank + 1)) / ncta);
       if (lane == 0) {
         fu->flags = tma ? kFRecTma : 0;
         fu->g = g;
@@ -361,7 +369,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
       const bool tma = U.flags & kFRecTma;
       if (lead && tma) {
         prefetch_tensormap(&P.xmap);
-        prefetch_tensormap(&P.ymap);
+        if (U.nn > 0) prefetch_tensormap(&P.ymap);
       }
       const int tok = reinterpret_cast<const int*>(slot + 128)[ltid];
       const int shift = v.page_shift;
@@ -441,7 +449,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
   } else if (warp == kFWarpMma) {
     // ---------------- MMA issue ----------------
     if (lane == 0) {
-      uint32_t gs = 0, ne = 0;
+      uint32_t gs = 0, ne = 0, nu = 0;
       bool issued = false;
       for (uint32_t np = 0; ok; ++np) {
         const uint32_t q = np % kFSlots;
@@ -451,6 +459,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
         }
         const FUnit U = *reinterpret_cast<const FUnit*>(slot_at(q));
         if (U.flags & kFRecEnd) break;
+        nu = np + 1;
         const uint32_t ub = np & 1;
         if (np >= 2 && !mbar_wait(smem_u32(&accs_empty[ub]), ((np >> 1) - 1) & 1)) {
           ok = false;
@@ -474,6 +483,18 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
           mma_commit(smem_u32(&empty[st]));
         }
         if (!ok) break;
+        if (a.shrink_only) {
+          // No expand: the previous unit's H only says that its owners are done
+          // with their receive buffers, which this unit's partial is about to
+          // refill; waited for after this unit's MMAs are issued.
+          if (np >= 1 && !mbar_wait(smem_u32(h_full), (np - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          mma_commit(smem_u32(&accs_full[ub]));
+          mbar_arrive(smem_u32(&slot_empty[q]));
+          continue;
+        }
         mma_commit(smem_u32(&accs_full[ub]));
         // the H operand of this unit, written by the owners of its rows
         if (!mbar_wait(smem_u32(h_full), np & 1)) {
@@ -509,6 +530,9 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
         if (!ok) break;
         mbar_arrive(smem_u32(&slot_empty[q]));
       }
+      // the last unit's H has landed here before the CTA can end (the peers' copies
+      // into this CTA are complete)
+      if (a.shrink_only && ok && nu > 0 && !mbar_wait(smem_u32(h_full), (nu - 1) & 1)) ok = false;
       if (issued) {  // every MMA of this CTA has completed before tensor memory is freed
         mma_commit(smem_u32(mma_done));
         mbar_wait(smem_u32(mma_done), 0);
@@ -606,6 +630,17 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
             hi4 = pc[1];
             sum[0] += lo4.x; sum[1] += lo4.y; sum[2] += lo4.z; sum[3] += lo4.w;
             sum[4] += hi4.x; sum[5] += hi4.y; sum[6] += hi4.z; sum[7] += hi4.w;
+          }
+          if (P.h != nullptr && mm < U.cnt) {  // the shrink-only form: row mm's h, unscaled, columns < r
+            float* hrow = P.h + (long long)reinterpret_cast<const int*>(slot + 128)[mm] * P.ldh + 8 * cg;
+            if (8 * cg + 8 <= U.r) {
+              reinterpret_cast<float4*>(hrow)[0] = make_float4(sum[0], sum[1], sum[2], sum[3]);
+              reinterpret_cast<float4*>(hrow)[1] = make_float4(sum[4], sum[5], sum[6], sum[7]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (8 * cg + e < U.r) hrow[e] = sum[e];
+            }
           }
           uint32_t hv[4], lv[4];
 #pragma unroll
@@ -733,6 +768,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_tc_kernel(const __grid_con
 
 // ---------------------------------------------------------------- launcher --
 
+bool tc_fused_shrink_ok(const lora_pool_view_t* v) { return v->d_in % 64 == 0 && v->page_elems >= 64; }
+
 bool tc_fused_ok(const lora_pool_view_t* v) {
   int ks, klen;
   shrink_split(v->d_in, &ks, &klen);
@@ -740,7 +777,7 @@ bool tc_fused_ok(const lora_pool_view_t* v) {
 }
 
 lora_status_t launch_fused_tc(int n_proj, const ProjCall* projs, const lora_segments_t* seg, int after_gather,
-                              int32_t* err, cudaStream_t stream) {
+                              int32_t* err, cudaStream_t stream, int shrink_only) {
   if (n_proj < 1 || n_proj > kMaxFusedProj) return LORA_ERR_INVALID_ARG;
   FusedArgs a;
   memset(&a, 0, sizeof(a));
@@ -753,12 +790,14 @@ lora_status_t launch_fused_tc(int n_proj, const ProjCall* projs, const lora_segm
     P.x = static_cast<const uint16_t*>(h.x);
     P.y = static_cast<uint16_t*>(h.y);
     P.yf = h.yf;
+    P.h = shrink_only ? h.h : nullptr;
     P.ldx = h.ldx;
     P.ldy = h.ldy;
     P.ldyf = h.ldyf;
+    P.ldh = h.ldh;
     P.tma = make_act_map(&P.xmap, h.x, seg->T, h.view->d_in, h.ldx, kTM) &&
-                    make_act_map(&P.ymap, h.y, seg->T, h.view->d_out, h.ldy, kTM) &&
-                    make_act_map(&P.ystore, h.y, seg->T, h.view->d_out, h.ldy, 32)
+                    (shrink_only || (make_act_map(&P.ymap, h.y, seg->T, h.view->d_out, h.ldy, kTM) &&
+                                     make_act_map(&P.ystore, h.y, seg->T, h.view->d_out, h.ldy, 32)))
                 ? 1
                 : 0;
   }
@@ -772,6 +811,7 @@ lora_status_t launch_fused_tc(int n_proj, const ProjCall* projs, const lora_segm
   a.n_proj = n_proj;
   a.klen = klen;
   a.after_gather = after_gather;
+  a.shrink_only = shrink_only;
   a.probe = wait_probe_cycles();
   const long long upper = (long long)seg->max_long_units * n_proj;
   if (upper <= 0) return LORA_OK;
