@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   // units of one projection (a segment's group of tokens, or a token), times the projections
   const int n_base = a.src == kSrcTokens ? a.T : a.meta[2] + (a.short_only ? 0 : a.meta[3]);
   const int n_units = n_base * G;
+  if (n_units == 0) return;  // every CTA of every cluster leaves: nothing has touched a peer or the counter
   // When the same call's fused tensor-core kernel follows with long tiles to do,
   // half of the clusters take part and the others leave at once: their SMs go to
   // the fused kernel, which then runs beside this one instead of after it (the
