@@ -305,7 +305,9 @@ static lora_status_t run_segmented(int mode, const void* x, long long ldx, void*
   // the gather kernel was launched iff the buffer has tokens (its short-only bound is T)
   const int after_gather = seg->T > 0 ? 1 : 0;
   if (mode == kModeApply && !staged) {
-    const ProjCall p{x, ldx, y, ldy, yf, ldyf, view};
+    ProjCall p{x, ldx, y, ldy, yf, ldyf, view};
+    p.h = h;  // with an h array, the apply writes its intermediate there too
+    p.ldh = ldh;
     return launch_fused_tc(1, &p, seg, after_gather, dev_err, s);
   }
   if (mode == kModeApply) {
@@ -453,13 +455,14 @@ lora_status_t lora_sgmv_backward(const void* x, int64_t ldx, const void* dy, int
   lora_pool_view_t vt = *view;  // the adapters transposed: B_i as the shrink's matrix, A_i as the expand's
   std::swap(vt.d_in, vt.d_out);
   {
-    TransposedViews transposed;  // u = dy B_i^T
-    if ((st = run_segmented(kModeShrink, dy, lddy, nullptr, 0, u, ldh, seg, &vt, dev_err, s)) != LORA_OK) return st;
+    TransposedViews transposed;
+    // u = dy B_i^T, and with dx, dx += s_i u A_i in the same pass: lora_apply over
+    // the transposed adapters (x = dy, y = dx), writing its intermediate u
+    st = dx == nullptr ? run_segmented(kModeShrink, dy, lddy, nullptr, 0, u, ldh, seg, &vt, dev_err, s)
+                       : run_segmented(kModeApply, dy, lddy, dx, lddx, u, ldh, seg, &vt, dev_err, s);
+    if (st != LORA_OK) return st;
   }
-  if ((st = launch_grad(x, ldx, dy, lddy, h, u, ldh, grad_pool, seg, view, dev_err, s)) != LORA_OK) return st;
-  if (dx == nullptr) return LORA_OK;
-  TransposedViews transposed;  // dx += s_i u A_i
-  return run_segmented(kModeExpand, nullptr, 0, dx, lddx, u, ldh, seg, &vt, dev_err, s);
+  return launch_grad(x, ldx, dy, lddy, h, u, ldh, grad_pool, seg, view, dev_err, s);
 }
 
 lora_status_t lora_base_apply(const void* x, int64_t ldx, const void* w0, int64_t ldw, void* y, int64_t ldy,

@@ -11,9 +11,10 @@
 //     dB_i     += s_i sum_{t in i} h[t]^T dy[t]
 //     dA_i     += s_i sum_{t in i} u[t]^T x[t]
 //     dx[t]    += s_i u[t] A_i                (expand of u over A_i)
-// The two shrinks and the expand are the forward kernels, the second shrink and
-// the expand on transposed views of the adapters; this file holds the
-// gradient kernel and the entry point.
+// The shrinks and the expand are the forward kernels: h by the shrink path; u
+// and dx in one pass of the apply path over transposed views of the adapters
+// (x = dy, y = dx, B_i as the shrink's matrix and A_i as the expand's), which
+// also writes its intermediate u; this file holds the gradient kernel.
 //
 // Gradient kernel.  A unit is (segment, matrix, 128-column block): the block's
 // columns of dB_i (a slice of d_out) or of dA_i (a slice of d_in), for all the

@@ -702,7 +702,9 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
           float sum = 0.f;  // in fixed CTA order
           for (uint32_t c = 0; c < ncta; ++c) sum += rb[(c * kNT + t) * kHMax + j];
           hs[t * kHMax + j] = mode == kModeApply ? rc.sc * sum : sum;
-          if (mode == kModeShrink && ok && (uint32_t)t % ncta == crank) hout[(long long)recs[st].tok[t] * ldh + j] = sum;
+          // the unscaled h: the shrink's output, or, with an h array, the apply's intermediate too
+          if ((mode == kModeShrink || (mode == kModeApply && hout != nullptr)) && ok && (uint32_t)t % ncta == crank)
+            hout[(long long)recs[st].tok[t] * ldh + j] = sum;
         }
         cons_sync();  // h complete here
         ++ngroup;

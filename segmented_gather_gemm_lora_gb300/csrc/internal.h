@@ -64,8 +64,8 @@ struct ProjCall {
   float* yf;  // optional fp32 output
   long long ldyf;
   const lora_pool_view_t* view;
-  float* h = nullptr;  // the fused kernel's shrink-only form: h rows by token, unscaled
-  long long ldh = 0;
+  float* h = nullptr;  // non-null: the fused kernel also writes h rows by token, unscaled
+  long long ldh = 0;   // (its only output in the shrink-only form)
 };
 
 enum GatherMode { kModeApply = 0, kModeShrink = 1, kModeExpand = 2 };
@@ -128,9 +128,9 @@ bool tc_expand_ok(const lora_pool_view_t* v);
 // Fused tensor-core path (tc_fused.cu): shrink, exchange of the intermediate
 // between the CTAs of a cluster and expand of each long tile in one kernel, for
 // up to kMaxFusedProj projections that share the segments and d_in.
-// Eligibility: d_in % 64 == 0, d_out % 64 == 0.  With shrink_only the kernel
-// writes each long tile's h rows (unscaled, by token, into projs[g].h) and runs
-// no expand; eligibility then: d_in % 64 == 0.
+// Eligibility: d_in % 64 == 0, d_out % 64 == 0.  With projs[g].h set the kernel
+// also writes each long tile's h rows (unscaled, by token); with shrink_only it
+// writes them and runs no expand (eligibility then: d_in % 64 == 0).
 bool tc_fused_ok(const lora_pool_view_t* v);
 bool tc_fused_shrink_ok(const lora_pool_view_t* v);
 lora_status_t launch_fused_tc(int n_proj, const ProjCall* projs, const lora_segments_t* seg, int after_gather,

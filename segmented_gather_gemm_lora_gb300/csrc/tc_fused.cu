@@ -96,7 +96,7 @@ struct FProj {
   const uint16_t* x;
   uint16_t* y;
   float* yf;  // non-null: fp32 output rows (y is then read only, for y0)
-  float* h;   // shrink-only form: h rows by token, unscaled, columns < r
+  float* h;   // non-null: h rows by token, unscaled, columns < r (the shrink-only form's output)
   long long ldx, ldy, ldyf, ldh;
   DevView v;
   int tma;  // every map valid
@@ -790,7 +790,7 @@ lora_status_t launch_fused_tc(int n_proj, const ProjCall* projs, const lora_segm
     P.x = static_cast<const uint16_t*>(h.x);
     P.y = static_cast<uint16_t*>(h.y);
     P.yf = h.yf;
-    P.h = shrink_only ? h.h : nullptr;
+    P.h = h.h;
     P.ldx = h.ldx;
     P.ldy = h.ldy;
     P.ldyf = h.ldyf;
