@@ -788,8 +788,9 @@ def run_backward_line(steps, warmup, soak_seconds, world, rank, local):
                    "step": "lora_segments_build + lora_sgmv_backward",
                    "l2": "inputs larger than L2: %d rotating input sets" % len(sets),
                    "timing": "CUDA graph of %d steps replayed; CUDA events on the launching stream" % g_steps},
-        "roofline": {"bound": "hbm", "kernel": "lora_sgmv_backward (gather, shrink_tc, reduce_partials, "
-                                               "grad_kernel, expand_tc)",
+        "roofline": {"bound": "hbm", "kernel": "lora_sgmv_backward (fused_tc shrink-only for h, fused_tc apply "
+                                               "over the transposed adapters for u and dx, grad_kernel; gather "
+                                               "for short segments)",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "peak_kind": peak_kind, "traffic": None,
                      "algorithmic_bytes_per_launch": bytes_avg, "avg_launch_us": step_s * 1e6,
