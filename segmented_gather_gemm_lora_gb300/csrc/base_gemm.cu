@@ -18,12 +18,20 @@
 // 128-byte swizzle, into a 4-stage ring.  Warp 1 issues tcgen05.mma (M = 128,
 // N = 256, bf16, fp32 accumulator in tensor memory), alternating two
 // accumulators so that a tile's epilogue overlaps the next tile's MMAs.
-// Warps 2-17 run the epilogue, one tile row and a quarter of the tile's
-// columns per thread (the tensor-memory lane quarter of its warp): 32 columns
-// at a time from tensor memory, plus the
-// row's adapter term on the CUDA cores (fp32 FMA over the rank in order, from
-// B_i's rows for the tile staged once per adapter in shared memory), rounded
-// once to bf16 and stored.
+//
+// Adapter term: on the tensor cores, into the same accumulator, after the tile's
+// K loop.  The tile's rows fall into runs of one adapter (rows without a usable
+// adapter in none); each run's adapter contributes ceil(r / 16) blocks of 16
+// rank rows, and a round takes two blocks:
+//     D += H . Bk,  H[m, k] = s_t h[t, j(k)] if row m is in block k's run, else 0,
+//                   Bk[k, n] = B_i(k)[j(k), n],  k < 32,
+// with H as bf16 hi and lo parts (one 128-byte row: hi in K 0..31, lo in K
+// 32..63, four K-16 MMAs per N-64 block) so that the intermediate keeps about
+// fp32 accuracy.  Warps 2-17 (the epilogue) build each round's H and B in
+// shared memory while the MMA warp runs the tile's K loop, then, once the
+// accumulator is complete, read it 32 columns at a time (each warp a quarter of
+// the tile's columns in its tensor-memory lane quarter), round once to bf16 and
+// store.
 #include <cudaTypedefs.h>
 
 #include <cstring>
@@ -44,12 +52,16 @@ constexpr int kBEpiChunks = kBN / 32 / (kBEpiWarps / 4);  // 32-column chunks pe
 constexpr int kBABytes = kBM * kBK * 2;
 constexpr int kBBBytes = kBN * kBK * 2;
 constexpr int kBStageBytes = kBABytes + kBBBytes;  // 48 KB
-constexpr size_t kBOffBars = (size_t)kBStages * kBStageBytes;
-constexpr int kBNBars = 2 * kBStages + 2 + 2 + 1;
-constexpr size_t kBOffB = (kBOffBars + kBNBars * 8 + 16 + 15) / 16 * 16;  // an adapter's B rows for the tile: [64][kBN] bf16
-constexpr size_t kBOffCtl = kBOffB + (size_t)LORA_MAX_RANK * kBN * 2;  // round control: 4 ints + [128] row adapters
-constexpr size_t kBSmem = kBOffCtl + (4 + kBM) * 4 + 1024;          // + 1024-byte alignment
-static_assert(kBOffB % 16 == 0, "16-byte staging stores");
+constexpr int kBRoundK = 32;  // rank rows of one adapter-term round (two 16-row blocks)
+constexpr size_t kBOffH = (size_t)kBStages * kBStageBytes;        // H: [128 rows][hi K 0..31 | lo K 0..31], 128-byte swizzle
+constexpr size_t kBOffD = kBOffH + (size_t)kBM * 128;             // B rows: [4 N-blocks][32 K rows][64 bf16], 128-byte swizzle
+constexpr size_t kBOffBars = kBOffD + (size_t)(kBN / 64) * kBRoundK * 128;
+constexpr int kBNBars = 2 * kBStages + 2 + 2 + 2 + 1;
+// control: row runs [128], run adapters [128], the round's blocks [2][4], the MMA's round words [2], runs
+// in the tile, tensor-memory slot
+constexpr size_t kBOffCtl = (kBOffBars + kBNBars * 8 + 15) / 16 * 16;
+constexpr size_t kBSmem = kBOffCtl + (2 * kBM + 8 + 2 + 1 + 1) * 4 + 1024;  // + 1024-byte alignment
+static_assert(kBOffH % 1024 == 0 && kBOffD % 1024 == 0, "swizzle atoms");
 static_assert(kBSmem <= 232448, "shared memory of one CTA");
 
 struct BaseArgs {
@@ -93,8 +105,15 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
   uint64_t* empty = bars + kBStages;        // [stages] MMA commit
   uint64_t* acc_full = empty + kBStages;    // [2] MMA commit: a tile's accumulator is complete
   uint64_t* acc_empty = acc_full + 2;       // [2] the 16 epilogue warps
-  uint64_t* mma_done = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* delta_full = acc_empty + 2;     // [1] the epilogue: a round's H and B are staged
+  uint64_t* delta_empty = delta_full + 1;   // [1] MMA commit: the round's MMAs have read them
+  uint64_t* mma_done = delta_empty + 1;
+  int* row_run = reinterpret_cast<int*>(sm + kBOffCtl);  // [128] the row's run in the tile (-1: none)
+  int* run_ad = row_run + kBM;                            // [128] each run's adapter
+  int* rblk = run_ad + kBM;                               // [2][4] the round's blocks: run, j0, rank, b_page0
+  int* rmma = rblk + 8;                                   // [2] blocks in the round, last round of the tile
+  int* nruns = rmma + 2;                                  // runs in the tile
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(nruns + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -106,6 +125,8 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
       mbar_init(smem_u32(&acc_full[b]), 1);
       mbar_init(smem_u32(&acc_empty[b]), kBEpiWarps);
     }
+    mbar_init(smem_u32(delta_full), 1);
+    mbar_init(smem_u32(delta_empty), 1);
     mbar_init(smem_u32(mma_done), 1);
     fence_mbar_init();
   }
@@ -124,6 +145,7 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
     ok = probe_ok != 0;
   }
   const int n_tiles = a.n_m * a.n_n;
+  const uint32_t hbuf = smem_u32(sm + kBOffH), dbuf = smem_u32(sm + kBOffD);
 
   if (warp == 0) {
     // ---------------- TMA loads ----------------
@@ -152,7 +174,8 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
     // ---------------- MMA issue ----------------
     if (lane == 0 && ok) {
       const uint32_t idesc = idesc_bf16(kBM, kBN, 0);
-      uint32_t g = 0, lt = 0;
+      const uint32_t idesc_d = idesc_bf16(kBM, 64, 1);  // the adapter term: N = 64 per block, B MN-major
+      uint32_t g = 0, lt = 0, rd = 0;
       bool issued = false;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++lt) {
         const uint32_t ab = lt & 1;
@@ -177,6 +200,28 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
           mma_commit(smem_u32(&empty[st]));
         }
         if (!ok) break;
+        // the adapter term, a round at a time (a tile without one has one empty round)
+        for (bool last = false; !last; ++rd) {
+          if (!mbar_wait(smem_u32(delta_full), rd & 1)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_smem();  // the epilogue's shared-memory writes, seen here, before the tensor cores read them
+          tc_fence_after();
+          const int nblk = rmma[0];
+          last = rmma[1] != 0;
+          // H's K slices: hi of blocks 0, 1, then lo of blocks 0, 1
+          for (int kk = 0; kk < 4; ++kk) {
+            const int bk = kk & 1;
+            if (bk >= nblk) continue;
+#pragma unroll
+            for (int nb = 0; nb < kBN / 64; ++nb)
+              mma_bf16(tmem + ab * kBN + nb * 64, sdesc_sw128(hbuf + 32 * kk, 16, 1024),
+                       sdesc_sw128(dbuf + nb * (kBRoundK * 128) + bk * 2048, 0, 1024), idesc_d, 1u);
+          }
+          mma_commit(smem_u32(delta_empty));
+        }
+        if (!ok) break;
         mma_commit(smem_u32(&acc_full[ab]));
       }
       if (issued) {  // every MMA has completed before tensor memory is freed
@@ -188,33 +233,21 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
     __syncwarp();
   } else {
     // ---------------- epilogue ----------------
-    // Per tile, in rounds: round 0 stores the rows without an adapter term; each
-    // later round takes the adapter of the lowest row not yet stored, stages its
-    // B_i[0 .. r)[n-tile] in shared memory (every epilogue thread copies 16-byte
-    // pieces through the page table), and the rows of that adapter add their
-    // term from it and store.  A tile of one request's tokens takes one or two
-    // rounds; each round reads every column of the accumulator once per warp.
+    // Per tile: its rows' runs of one adapter; the adapter term's rounds staged
+    // (H and B in shared memory), each once the MMA warp is done with the last;
+    // then the accumulator rounded to bf16 and stored.
     const int quarter = warp & 3;  // the tensor-memory lanes this warp may read
     const int row = quarter * 32 + lane;
-    const int part = (warp - 2) >> 2;  // the tile's columns [64 part, 64 part + 64)
+    const int part = (warp - 2) >> 2;  // the tile's columns [64 part, 64 part + 64); H chunks part, part + 4
     const int et = tid - 64;           // 0..511
     const DevView& v = a.v;
     const int shift = v.page_shift;
-    const long long pmask = (1LL << shift) - 1;
-    uint16_t* bs = reinterpret_cast<uint16_t*>(sm + kBOffB);
-    int* cand = reinterpret_cast<int*>(sm + kBOffCtl);  // [0] lowest row left; [1] its adapter, [2] rank, [3] b_page0
-    int* row_ad = cand + 4;                             // [128] each row's adapter (-1: none)
-    uint32_t lt = 0;
+    uint32_t lt = 0, rd = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++lt) {
       const int m = tile / a.n_n, n = tile - m * a.n_n;
       const uint32_t ab = lt & 1;
-      // the epilogue warps leave together when a wait ran out (they meet at named barriers)
-      if (!epi_all(mbar_wait(smem_u32(&acc_full[ab]), (lt >> 1) & 1))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
       const int t = m * kBM + row;
+      const int n_base = n * kBN;
       int ad = -1;
       float s = 0.f;
       if (t < a.T) {
@@ -224,94 +257,150 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
           if (s != 0.f) ad = id;
         }
       }
-      row_ad[row] = ad;
-      const float* hrow = a.h + (long long)(t < a.T ? t : 0) * a.ldh;
-      const int n_base = n * kBN;
-      const int wt = min(kBN, v.d_out - n_base);  // columns of this tile, a multiple of 8
-      bool done = t >= a.T;
-      for (int round = 0;; ++round) {
-        int cur = -1, r = 0;
-        if (round > 0) {
-          if (et == 0) cand[0] = 0x7fffffff;
-          epi_bar();
-          if (!done) atomicMin(&cand[0], row);
-          epi_bar();
-          const int first = cand[0];
-          if (first == 0x7fffffff) break;  // every row stored
-          cur = row_ad[first];
-          if (et == 0) {
-            const lora_adapter_desc_t d = adapter_desc(v, cur);
-            cand[2] = d.rank;
-            cand[3] = d.b_page0;
-          }
-          epi_bar();
-          r = cand[2];
-          const long long b0 = cand[3];
-          // stage B_cur[j][n_base .. n_base + wt) as [r][kBN] bf16
-          const int pieces = r * (kBN / 8);
-          for (int p0 = et; p0 < pieces; p0 += 4 * kBEpiThreads) {
-            long long pg[4];
-            long long el[4];
+      if (part == 0) row_run[row] = ad;
+      epi_bar();
+      if (warp == 2) {  // runs: a row starts one when its adapter differs from the row before
+        int a0[kBM / 32], ap[kBM / 32];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int p = p0 + kBEpiThreads * u;
-              const int j = p / (kBN / 8), q = p - j * (kBN / 8);
-              el[u] = (long long)j * v.d_out + n_base + 8 * q;
-              pg[u] = (p < pieces && 8 * q < wt) ? v.page_list[b0 + (el[u] >> shift)] : -1;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int p = p0 + kBEpiThreads * u;
-              if (pg[u] >= 0) {
-                const int j = p / (kBN / 8), q = p - j * (kBN / 8);
-                *reinterpret_cast<uint4*>(bs + j * kBN + 8 * q) =
-                    __ldg(reinterpret_cast<const uint4*>(v.pool + (pg[u] << shift) + (el[u] & pmask)));
-              }
-            }
-          }
-          epi_bar();
+        for (int i = 0; i < kBM / 32; ++i) {  // every row read before any is overwritten
+          const int rr = 32 * i + lane;
+          a0[i] = row_run[rr];
+          ap[i] = rr > 0 ? row_run[rr - 1] : -1;
         }
-        const bool mine = !done && (round == 0 ? ad < 0 : ad == cur);
-        for (int c = kBEpiChunks * part; c < kBEpiChunks * (part + 1); ++c) {
-          __syncwarp();  // the warp converged for the collective load
-          uint32_t raw[32];
-          tmem_ld32_nowait(tmem + ab * kBN + c * 32 + ((uint32_t)(quarter * 32) << 16), raw);
-          tmem_wait_ld();
-          const int n0 = n_base + c * 32;
-          if (mine && n0 < v.d_out) {
-            float o[32];
+        __syncwarp();
+        int base = 0;
 #pragma unroll
-            for (int q = 0; q < 32; ++q) o[q] = __uint_as_float(raw[q]);
-            const int w = min(32, v.d_out - n0);
-            for (int j = 0; j < r; ++j) {
-              const float hj = s * hrow[j];
-              const uint16_t* brow = bs + j * kBN + c * 32;
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                if (8 * q < w) {
-                  float bv[8];
-                  unpack8(*reinterpret_cast<const uint4*>(brow + 8 * q), bv);
-#pragma unroll
-                  for (int e8 = 0; e8 < 8; ++e8) o[8 * q + e8] = fmaf(hj, bv[e8], o[8 * q + e8]);
+        for (int i = 0; i < kBM / 32; ++i) {
+          const bool head = a0[i] >= 0 && a0[i] != ap[i];
+          const uint32_t hm = __ballot_sync(0xffffffffu, head);
+          const int k = base + __popc(hm & ((2u << lane) - 1u)) - 1;  // heads up to this row, less one
+          if (head) run_ad[k] = a0[i];
+          row_run[32 * i + lane] = a0[i] >= 0 ? k : -1;
+          base += __popc(hm);
+        }
+        if (lane == 0) *nruns = base;
+      }
+      epi_bar();
+      const int n_runs = *nruns;
+      const int my_run = row_run[row];
+      const float* hrow = a.h + (long long)(t < a.T ? t : 0) * a.ldh;
+      // rounds: two 16-row blocks each, walking the runs in order
+      int cur_run = 0, cur_j0 = 0, cur_r = 0, cur_bp = 0;  // thread 0's cursor
+      if (et == 0 && n_runs > 0) {
+        const lora_adapter_desc_t d0 = adapter_desc(v, run_ad[0]);
+        cur_r = d0.rank;
+        cur_bp = d0.b_page0;
+      }
+      for (bool last = false; !last; ++rd) {
+        // the MMA warp is done with the previous round's H and B
+        if (!epi_all(rd == 0 || mbar_wait(smem_u32(delta_empty), (rd - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        if (et == 0) {
+          int nb = 0;
+          for (int b = 0; b < 2; ++b) {
+            if (cur_run < n_runs) {
+              rblk[4 * b] = cur_run;
+              rblk[4 * b + 1] = cur_j0;
+              rblk[4 * b + 2] = cur_r;
+              rblk[4 * b + 3] = cur_bp;
+              ++nb;
+              cur_j0 += 16;
+              if (cur_j0 >= cur_r) {
+                cur_j0 = 0;
+                if (++cur_run < n_runs) {
+                  const lora_adapter_desc_t d1 = adapter_desc(v, run_ad[cur_run]);
+                  cur_r = d1.rank;
+                  cur_bp = d1.b_page0;
                 }
               }
+            } else {
+              rblk[4 * b] = -1;
             }
-            uint4* dst = reinterpret_cast<uint4*>(a.y + (long long)t * a.ldy + n0);
+          }
+          rmma[0] = nb;
+          rmma[1] = cur_run >= n_runs ? 1 : 0;
+        }
+        epi_bar();
+        last = rmma[1] != 0;
+        // H: this thread's row, chunk pair `part` (K 8 part .. 8 part + 7 of block part / 2)
+        if (rmma[0] > 0) {
+          const int bk = part >> 1;
+          const int brun = rblk[4 * bk], j = rblk[4 * bk + 1] + 8 * (part & 1), br = rblk[4 * bk + 2];
+          float hv[8];
+          if (brun >= 0 && my_run == brun && j < br) {
+            const float4 h0 = *reinterpret_cast<const float4*>(hrow + j);
+            const float4 h1 = *reinterpret_cast<const float4*>(hrow + j + 4);
+            hv[0] = h0.x; hv[1] = h0.y; hv[2] = h0.z; hv[3] = h0.w;
+            hv[4] = h1.x; hv[5] = h1.y; hv[6] = h1.z; hv[7] = h1.w;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (8 * q < w) {
-                uint4 pk;
-                pk.x = pack_bf16x2(o[8 * q + 0], o[8 * q + 1]);
-                pk.y = pack_bf16x2(o[8 * q + 2], o[8 * q + 3]);
-                pk.z = pack_bf16x2(o[8 * q + 4], o[8 * q + 5]);
-                pk.w = pack_bf16x2(o[8 * q + 6], o[8 * q + 7]);
-                dst[q] = pk;
-              }
+            for (int e = 0; e < 8; ++e) hv[e] = j + e < br ? s * hv[e] : 0.f;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) hv[e] = 0.f;
+          }
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hi[e] = pack_bf16x2(hv[2 * e], hv[2 * e + 1]);
+            lo[e] = pack_bf16x2(hv[2 * e] - bf_lo(hi[e]), hv[2 * e + 1] - bf_hi(hi[e]));
+          }
+          *reinterpret_cast<uint4*>(sm + kBOffH + sw128_offset(row, part)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(sm + kBOffH + sw128_offset(row, part + 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        // B: rows k of the round (block k / 16, rank row j0 + k % 16) for the tile's
+        // 256 columns, 16-byte pieces through the page table, zero past the rank,
+        // past d_out or without a block
+#pragma unroll
+        for (int u = 0; u < (kBRoundK * kBN / 8) / kBEpiThreads; ++u) {
+          const int pc = et + kBEpiThreads * u;
+          const int k = pc / (kBN / 8), q = pc - k * (kBN / 8);
+          const int bk = k >> 4;
+          const int brun = rblk[4 * bk], j = rblk[4 * bk + 1] + (k & 15), br = rblk[4 * bk + 2];
+          const int col = n_base + 8 * q;
+          const bool valid = brun >= 0 && j < br && col < v.d_out;
+          const uint16_t* src = v.pool;
+          if (valid) {
+            const long long el = (long long)j * v.d_out + col;
+            src = v.pool + ((long long)v.page_list[rblk[4 * bk + 3] + (el >> shift)] << shift) + (el & ((1LL << shift) - 1));
+          }
+          if (rmma[0] > 0) cp_async16(dbuf + (uint32_t)((q >> 3) * (kBRoundK * 128)) + sw128_offset(k, q & 7), src, valid);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_proxy_async_smem();  // this thread's writes, before the tensor cores read them
+        epi_bar();
+        if (et == 0) mbar_arrive(smem_u32(delta_full));
+      }
+      if (!ok) break;
+      // the accumulator: base product + adapter term
+      if (!epi_all(mbar_wait(smem_u32(&acc_full[ab]), (lt >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool store = t < a.T;
+      for (int c = kBEpiChunks * part; c < kBEpiChunks * (part + 1); ++c) {
+        uint32_t raw[32];
+        tmem_ld32_nowait(tmem + ab * kBN + c * 32 + ((uint32_t)(quarter * 32) << 16), raw);
+        tmem_wait_ld();
+        const int n0 = n_base + c * 32;
+        if (store && n0 < v.d_out) {
+          const int w = min(32, v.d_out - n0);
+          uint4* dst = reinterpret_cast<uint4*>(a.y + (long long)t * a.ldy + n0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (8 * q < w) {
+              uint4 pk;
+              pk.x = pack_bf16x2(__uint_as_float(raw[8 * q + 0]), __uint_as_float(raw[8 * q + 1]));
+              pk.y = pack_bf16x2(__uint_as_float(raw[8 * q + 2]), __uint_as_float(raw[8 * q + 3]));
+              pk.z = pack_bf16x2(__uint_as_float(raw[8 * q + 4]), __uint_as_float(raw[8 * q + 5]));
+              pk.w = pack_bf16x2(__uint_as_float(raw[8 * q + 6]), __uint_as_float(raw[8 * q + 7]));
+              dst[q] = pk;
             }
           }
         }
-        done = done || mine;
-        epi_bar();  // the staged rows are free for the next round
       }
       tc_fence_before();
       __syncwarp();
