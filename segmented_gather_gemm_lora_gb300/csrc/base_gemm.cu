@@ -11,12 +11,16 @@
 // token, fp32) and s_i the token's scale (0 when the token has no usable
 // adapter, which then gets the base product alone).
 //
-// Base product: a persistent tcgen05 GEMM over 128 x 256 output tiles, tiles
-// taken in order (m = tile / n_tiles_n, n = tile % n_tiles_n) so that a wave of
-// CTAs shares W0's tiles in L2 and x streams once.  Warp 0 loads: per 64-column
-// K step one TMA box of x (128 x 64) and one of W0 (256 x 64), both with the
-// 128-byte swizzle, into a 4-stage ring.  Warp 1 issues tcgen05.mma (M = 128,
-// N = 256, bf16, fp32 accumulator in tensor memory), alternating two
+// Base product: a persistent tcgen05 GEMM over 128 x 256 output tiles.  A
+// cluster of two CTAs takes the tiles (m, n) and (m + 1, n) together, pairs
+// taken in order (m / 2 major, n minor) so that a wave of clusters shares W0's
+// tiles in L2 and x streams once.  Warp 0 loads, per 64-column K step, its own
+// TMA box of x (128 x 64) and one half (128 x 64) of the W0 box the two tiles
+// share, multicast into both CTAs, all with the 128-byte swizzle, into a
+// 4-stage ring: each CTA then reads two thirds of the bytes a CTA loading its
+// own W0 box would.  A stage is free again once both CTAs' MMAs have read it
+// (each MMA warp's commit arrives in both CTAs).  Warp 1 issues tcgen05.mma
+// (M = 128, N = 256, bf16, fp32 accumulator in tensor memory), alternating two
 // accumulators so that a tile's epilogue overlaps the next tile's MMAs.
 //
 // Adapter term: on the tensor cores, into the same accumulator, after the tile's
@@ -66,7 +70,7 @@ static_assert(kBSmem <= 232448, "shared memory of one CTA");
 
 struct BaseArgs {
   CUtensorMap xmap;  // x [T, d_in], boxes of 128 rows x 64 columns
-  CUtensorMap wmap;  // W0 [d_out, d_in], boxes of 256 rows x 64 columns
+  CUtensorMap wmap;  // W0 [d_out, d_in], boxes of 128 rows x 64 columns (half a tile's W0 box)
   uint16_t* y;
   long long ldy;
   const float* h;  // [T, ldh]: h[t, j] = x[t] . A_i[j] for tokens with a usable adapter
@@ -76,6 +80,7 @@ struct BaseArgs {
   DevView v;
   int T;
   int n_m, n_n, nk;
+  int n_pairs;  // (m / 2, n) pairs of tiles
   int32_t* err;
   long long probe;
 };
@@ -116,10 +121,11 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(nruns + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  const uint32_t crank = cluster_ctarank(), cid = cluster_id_x(), ncl = ncluster_x();
   if (tid == 0) {
     for (int s = 0; s < kBStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 2);  // both CTAs' MMA commits
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&acc_full[b]), 1);
@@ -132,7 +138,8 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 2 * kBN);
   tc_fence_before();
-  __syncthreads();
+  // every barrier of both CTAs initialised before the peer's copies or commits reach it
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait_then_release();
@@ -144,7 +151,7 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
     __syncthreads();
     ok = probe_ok != 0;
   }
-  const int n_tiles = a.n_m * a.n_n;
+  // this CTA's tiles: (2 (p / n_n) + crank, p % n_n) for the cluster's pairs p
   const uint32_t hbuf = smem_u32(sm + kBOffH), dbuf = smem_u32(sm + kBOffD);
 
   if (warp == 0) {
@@ -153,8 +160,8 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
       prefetch_tensormap(&a.xmap);
       prefetch_tensormap(&a.wmap);
       uint32_t g = 0;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const int m = tile / a.n_n, n = tile - m * a.n_n;
+      for (int p = (int)cid; p < a.n_pairs && ok; p += (int)ncl) {
+        const int m = 2 * (p / a.n_n) + (int)crank, n = p % a.n_n;
         for (int kb = 0; kb < a.nk; ++kb, ++g) {
           const uint32_t st = g % kBStages;
           if (g >= kBStages && !mbar_wait(smem_u32(&empty[st]), ((g / kBStages) - 1) & 1)) {
@@ -162,9 +169,12 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
             break;
           }
           const uint32_t dst = smem_u32(sm + (size_t)st * kBStageBytes);
+          // this CTA's x box, then its half of the shared W0 box into both CTAs
+          // (the peer's half lands here too, on the same barrier)
           mbar_arrive_expect_tx(smem_u32(&full[st]), kBStageBytes);
           tma_load_2d(dst, &a.xmap, kb * kBK, m * kBM, smem_u32(&full[st]));
-          tma_load_2d(dst + kBABytes, &a.wmap, kb * kBK, n * kBN, smem_u32(&full[st]));
+          tma_load_2d_mc(dst + kBABytes + crank * (kBBBytes / 2), &a.wmap, kb * kBK, n * kBN + (int)crank * (kBN / 2),
+                         smem_u32(&full[st]), (uint16_t)3u);
         }
       }
       if (!ok) report(a.err, LORA_DERR_TIMEOUT);
@@ -177,7 +187,7 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
       const uint32_t idesc_d = idesc_bf16(kBM, 64, 1);  // the adapter term: N = 64 per block, B MN-major
       uint32_t g = 0, lt = 0, rd = 0;
       bool issued = false;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++lt) {
+      for (int p = (int)cid; p < a.n_pairs && ok; p += (int)ncl, ++lt) {
         const uint32_t ab = lt & 1;
         if (lt >= 2 && !mbar_wait(smem_u32(&acc_empty[ab]), ((lt >> 1) - 1) & 1)) {
           ok = false;
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
             mma_bf16(tmem + ab * kBN, sdesc_sw128(as + 32 * kk, 16, 1024), sdesc_sw128(bs + 32 * kk, 16, 1024), idesc,
                      (kb | kk) != 0);
           issued = true;
-          mma_commit(smem_u32(&empty[st]));
+          mma_commit_mc(smem_u32(&empty[st]), (uint16_t)3u);  // the stage is free in both CTAs once both read it
         }
         if (!ok) break;
         // the adapter term, a round at a time (a tile without one has one empty round)
@@ -243,8 +253,8 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
     const DevView& v = a.v;
     const int shift = v.page_shift;
     uint32_t lt = 0, rd = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++lt) {
-      const int m = tile / a.n_n, n = tile - m * a.n_n;
+    for (int p = (int)cid; p < a.n_pairs; p += (int)ncl, ++lt) {
+      const int m = 2 * (p / a.n_n) + (int)crank, n = p % a.n_n;
       const uint32_t ab = lt & 1;
       const int t = m * kBM + row;
       const int n_base = n * kBN;
@@ -409,7 +419,8 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
     if (!ok && lane == 0) report(a.err, LORA_DERR_TIMEOUT);
   }
   tc_fence_before();
-  __syncthreads();
+  // neither CTA leaves while the peer may still copy into it or arrive on its barriers
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 2 * kBN);
@@ -473,7 +484,7 @@ lora_status_t launch_base_gemm(const void* x, long long ldx, const void* w0, lon
   BaseArgs a;
   memset(&a, 0, sizeof(a));
   if (!make_act_map(&a.xmap, x, T, view->d_in, ldx, kBM)) return LORA_ERR_UNSUPPORTED;
-  if (!make_act_map(&a.wmap, w0, view->d_out, view->d_in, ldw, kBN)) return LORA_ERR_UNSUPPORTED;
+  if (!make_act_map(&a.wmap, w0, view->d_out, view->d_in, ldw, kBN / 2)) return LORA_ERR_UNSUPPORTED;
   a.y = static_cast<uint16_t*>(y);
   a.ldy = ldy;
   a.h = h;
@@ -485,12 +496,14 @@ lora_status_t launch_base_gemm(const void* x, long long ldx, const void* w0, lon
   a.n_m = (T + kBM - 1) / kBM;
   a.n_n = (view->d_out + kBN - 1) / kBN;
   a.nk = (view->d_in + kBK - 1) / kBK;
+  a.n_pairs = (a.n_m + 1) / 2 * a.n_n;
   a.err = err;
   a.probe = wait_probe_cycles();
   if (ensure_smem_attr((const void*)base_gemm_kernel, kBSmem) != cudaSuccess) return LORA_ERR_CUDA;
-  const long long tiles = (long long)a.n_m * a.n_n;
-  const int grid = (int)std::min<long long>(tiles, sm_count());
-  return launch_pdl((const void*)base_gemm_kernel, dim3((unsigned)grid), dim3(kBThreads), kBSmem, stream, 0, &a) ==
+  const int cap = max_active_clusters((const void*)base_gemm_kernel, kBThreads, kBSmem, 2);
+  const int clusters = (int)std::min<long long>(a.n_pairs, std::max(1, cap));
+  return launch_pdl((const void*)base_gemm_kernel, dim3((unsigned)(2 * clusters)), dim3(kBThreads), kBSmem, stream, 2,
+                    &a) ==
                  cudaSuccess
              ? LORA_OK
              : LORA_ERR_CUDA;
