@@ -319,7 +319,7 @@ lora_status_t lora_base_apply(const void* x, int64_t ldx, const void* w0, int64_
  * section "SGMV: the kernel that holds it all up"; MBGMV in "Multi-LoRA
  * Serving in Production", section "S-LoRA: MBGMV and MBGMM Kernels").
  * Same result as lora_apply up to rounding.  Views with max_rank <= 16,
- * d_in, d_out <= 4096 and at most 128 page-list slots per adapter run on a
+ * d_in, d_out <= 8192 and at most 128 page-list slots per adapter run on a
  * decode kernel of small CTAs with fp32 CUDA-core arithmetic, where a token's
  * output depends only on its own row, its adapter and the projection's shape
  * (not on the rest of the batch); other views run on lora_apply's gather

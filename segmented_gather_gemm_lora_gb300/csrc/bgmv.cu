@@ -11,7 +11,7 @@
 // adapter id, its descriptor, its page list, the rows, the shrink, the cluster
 // exchange, the expand.  This kernel shortens that chain and lets consecutive
 // calls overlap:
-//   - small CTAs (4 warps, about 21 KB of shared memory), so that the next
+//   - CTAs small enough (8 warps, about 38 KB of shared memory) that the next
 //     call's CTAs are resident, with their set-up done, while this call runs;
 //   - no record pipeline: a CTA holds its whole adapter slice, at most 16 rows,
 //     so every copy is issued as soon as the page list is read, and B's rows
@@ -24,9 +24,10 @@
 //     x, y0 and y wait for it.
 //
 // Work decomposition: the token's cluster has C CTAs, C = ceil(max(d_in,
-// d_out) / 512) (at most 8, the gather kernel's width for the projection); CTA
-// c owns slice c of d_in (shrink) and of d_out (expand), at most 512 columns
-// each.  Each CTA pushes its partial h to every CTA of the cluster through
+// d_out) / 1024) (at most 8); CTA c owns slice c of d_in (shrink) and of d_out
+// (expand), at most 1024 columns each (clusters of 8 CTAs of 512 columns
+// measured 1-7 % slower for calls of 64-256 tokens, of 2 CTAs of 2048 columns
+// slower still).  Each CTA pushes its partial h to every CTA of the cluster through
 // distributed shared memory, and each adds the C partials in CTA order, so the
 // result is deterministic and depends only on the token's row, its adapter and
 // the projection's shape.  The sums are the exact fp32 ones (h not split into
@@ -42,14 +43,15 @@ namespace lora {
 
 namespace {
 
-constexpr int kDThreads = 128;
+constexpr int kDHalves = 2;  // 512-column halves of a CTA's slice
+constexpr int kDThreads = 128 * kDHalves;
 constexpr int kDWarps = kDThreads / 32;
 constexpr int kDMaxRank = 16;    // the adapter's rows held at once
-constexpr int kDMaxCols = 512;   // columns of a CTA's slice of d_in or d_out
+constexpr int kDMaxCols = 512 * kDHalves;   // columns of a CTA's slice of d_in or d_out
 constexpr int kDRowStride = kDMaxCols * 2 + 16;  // bytes between staged rows
 constexpr int kDMaxCluster = 8;
 constexpr int kDMaxPg = 128;  // page-list slots of one adapter cached in shared memory (A's, then B's)
-static_assert(kDMaxCols == 4 * kDThreads && kDMaxCols == 16 * 32, "column ownership of the expand and the shrink");
+static_assert(kDMaxCols == 4 * kDThreads && kDMaxCols == 16 * 32 * kDHalves, "column ownership of the expand and the shrink");
 
 // shared memory: adapter rows (A, then B) and the token's y0 row after them;
 // the x row; page cache; this CTA's partial h; the cluster's partials; h; the
@@ -59,7 +61,7 @@ constexpr size_t kDOffY0 = kDOffBuf + (size_t)kDMaxRank * kDRowStride;
 constexpr size_t kDOffX = kDOffY0 + kDRowStride;
 constexpr size_t kDOffPg = kDOffX + kDRowStride;
 constexpr size_t kDOffPw = kDOffPg + kDMaxPg * sizeof(int);
-constexpr size_t kDOffRecv = kDOffPw + kDMaxRank * sizeof(float);
+constexpr size_t kDOffRecv = kDOffPw + kDHalves * kDMaxRank * sizeof(float);
 constexpr size_t kDOffHs = kDOffRecv + kDMaxCluster * kDMaxRank * sizeof(float);
 constexpr size_t kDOffInfo = kDOffHs + kDMaxRank * sizeof(float);
 constexpr size_t kDOffBars = kDOffInfo + 8 * sizeof(int);
@@ -224,13 +226,15 @@ __global__ void __launch_bounds__(kDThreads) bgmv_kernel(const __grid_constant__
     ok = __syncthreads_and(mbar_wait(bar_a, 0) && mbar_wait(bar_xy, 0)) != 0;
     if (ok) {
       // Shrink on the CUDA cores (one token: a matrix-vector product): warp w owns
-      // rows w, w + 4, w + 8, w + 12; lane l the 16-byte pieces at columns 8 l and
-      // 256 + 8 l of the slice.  Each lane sums its 16 products in column order,
-      // then a fixed butterfly of shuffles adds the lanes.
+      // rows w % 4 + 4 i of half w / 4 of the slice (512 columns); lane l the
+      // 16-byte pieces at columns 8 l and 256 + 8 l of the half.  Each lane sums
+      // its 16 products in column order, then a fixed butterfly of shuffles adds
+      // the lanes; the halves' partials are added in order before the exchange.
+      const int rw = warp & 3, hf = warp >> 2;
       float xv[2][8];
 #pragma unroll
       for (int p = 0; p < 2; ++p) {
-        const int c = 8 * lane + 256 * p;
+        const int c = 512 * hf + 8 * lane + 256 * p;
         if (c < kw) {
           unpack8(*reinterpret_cast<const uint4*>(sm + kDOffX + 2 * c), xv[p]);
         } else {
@@ -240,15 +244,15 @@ __global__ void __launch_bounds__(kDThreads) bgmv_kernel(const __grid_constant__
       }
       // the warp's four rows side by side, so that their loads, products and
       // shuffles overlap
-      constexpr int kRows = kDMaxRank / kDWarps;
+      constexpr int kRows = kDMaxRank / 4;
       float sr[kRows];
 #pragma unroll
       for (int i = 0; i < kRows; ++i) {
-        const int j = warp + kDWarps * i;
+        const int j = rw + 4 * i;
         sr[i] = 0.f;
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
-          const int c = 8 * lane + 256 * p;
+          const int c = 512 * hf + 8 * lane + 256 * p;
           if (j < r && c < kw) {
             float av[8];
             unpack8(*reinterpret_cast<const uint4*>(buf + j * kDRowStride + 2 * c), av);
@@ -264,7 +268,7 @@ __global__ void __launch_bounds__(kDThreads) bgmv_kernel(const __grid_constant__
       if (lane == 0) {
 #pragma unroll
         for (int i = 0; i < kRows; ++i)
-          if (warp + kDWarps * i < r) pw[warp + kDWarps * i] = sr[i];
+          if (rw + 4 * i < r) pw[hf * kDMaxRank + rw + 4 * i] = sr[i];
       }
     }
     __syncthreads();  // every block's partial is in; A's rows are free
@@ -280,7 +284,11 @@ __global__ void __launch_bounds__(kDThreads) bgmv_kernel(const __grid_constant__
     const int q4 = (r + 3) >> 2;
     if (ok && tid == 0) mbar_arrive_expect_tx(bar_recv, C * (uint32_t)q4 * 16u);
     if (ok && tid < q4) {
-      const float4 part = *reinterpret_cast<const float4*>(pw + 4 * tid);
+      float4 part = *reinterpret_cast<const float4*>(pw + 4 * tid);
+      for (int hh = 1; hh < kDHalves; ++hh) {  // the halves' partials in order
+        const float4 p2 = *reinterpret_cast<const float4*>(pw + hh * kDMaxRank + 4 * tid);
+        part.x += p2.x; part.y += p2.y; part.z += p2.z; part.w += p2.w;
+      }
       const uint32_t dst = smem_u32(recv + crank * kDMaxRank + 4 * tid);
       for (uint32_t c = 0; c < C; ++c) st_async_v4(mapa(dst, c), part, mapa(bar_recv, c));
     }
@@ -334,8 +342,8 @@ __global__ void __launch_bounds__(kDThreads) bgmv_kernel(const __grid_constant__
   cluster_wait();
 }
 
-// Cluster width of the gather kernel's slices for a view: one CTA per 512
-// columns of the wider side, at most eight.
+// Cluster width of the decode kernel for a view: one CTA per kDMaxCols columns
+// of the wider side, at most eight.
 int slice_width(const lora_pool_view_t* v) {
   const int d = std::max(v->d_in, v->d_out);
   return std::min(std::max((d + kDMaxCols - 1) / kDMaxCols, 1), kDMaxCluster);
@@ -368,6 +376,7 @@ lora_status_t launch_bgmv(const void* x, long long ldx, void* y, long long ldy, 
   a.early = early;
   a.probe = wait_probe_cycles();
   const int C = slice_width(view);
+  if (ensure_smem_attr((const void*)bgmv_kernel, kDSmem) != cudaSuccess) return LORA_ERR_CUDA;
   return launch_pdl((const void*)bgmv_kernel, dim3((unsigned)(T * C)), dim3(kDThreads), kDSmem, stream, C, &a) ==
                  cudaSuccess
              ? LORA_OK

@@ -423,11 +423,12 @@ def test_bgmv_rows_independent_of_the_batch():
 def test_bgmv_decode_kernel_shapes_and_pages():
     """The decode kernel on the shapes it takes: one CTA (d = 256), slices narrower than
     a sub-slice, d_in != d_out, 1024-element pages, rows that cross pages (d = 1000),
+    clusters of five and eight CTAs (5120 -> 8192),
     ranks 1..16 with max_rank 16, strides wider than the rows; and a view with more page
     slots than the kernel caches (256-element pages), which lora_bgmv runs on the gather
     kernel.  Against the oracle; -1 rows and the guard columns untouched."""
     for seed, (d_in, d_out, page) in enumerate([(256, 256, 4096), (1024, 2048, 4096), (4096, 1024, 1024),
-                                                (1000, 4096, 4096), (2048, 4096, 256)]):
+                                                (1000, 4096, 4096), (5120, 8192, 4096), (2048, 4096, 256)]):
         rng = np.random.default_rng(900 + seed)
         ranks = [1, 16, 3, 8, 16, 5, 12, 2]
         pool = W.build_pool(rng, d_in, d_out, ranks, max_rank=16, page_elems=page)
