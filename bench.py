@@ -904,8 +904,8 @@ def run_base_line(steps, warmup, soak_seconds, world, rank, local):
         "config": {"workload": "base projection with the adapter term in its epilogue on the prefill SGMV batch: "
                                "32 requests of U{64..512} tokens, y = x W0^T + s_i (x A_i^T) B_i with a random "
                                "4096 x 4096 bf16 W0, 200 rank-16 adapters, Zipf(1.1), contiguous segments",
-                   "step": "lora_segments_build + lora_base_apply (shrink, per-token scales, tcgen05 base GEMM "
-                           "with the adapter term in its epilogue; y written once)",
+                   "step": "lora_segments_build + lora_base_apply (shrink, then the tcgen05 base GEMM with the "
+                           "adapter term on the tensor cores into the same accumulator; y written once)",
                    "l2": "inputs larger than L2: 2 rotating input sets",
                    "timing": "CUDA graph of %d steps replayed; CUDA events on the launching stream" % n,
                    "unfused_ms_per_step": ms_u,

@@ -301,9 +301,8 @@ lora_status_t lora_sgmv_backward(const void* x, int64_t ldx, const void* dy, int
  * ldw >= d_in, ldw % 8 == 0, 16-byte aligned; y: device bf16 [T, ldy];
  * token_adapter: the device int32 [T] ids that seg was built from, with
  * n_adapters = view->n_adapters.  The call runs the shrink stage into
- * seg->h_scratch (by token) and keeps per-token scales in seg->scratch, so
- * calls sharing a segment buffer must be ordered on one stream, and the
- * buffer must be rebuilt before it serves lora_apply's staged paths again.
+ * seg->h_scratch (by token), so calls sharing a segment buffer must be
+ * ordered on one stream.
  * y must not overlap x, w0 or the segment buffer.  The base product runs on
  * the tensor cores through TMA tensor maps: LORA_ERR_UNSUPPORTED when the
  * driver offers no tensor-map encoder.

@@ -484,8 +484,7 @@ lora_status_t lora_base_apply(const void* x, int64_t ldx, const void* w0, int64_
   const cudaStream_t s = (cudaStream_t)stream;
   st = run_segmented(kModeShrink, x, ldx, nullptr, 0, seg->h_scratch, LORA_MAX_RANK, seg, view, dev_err, s);
   if (st != LORA_OK) return st;
-  return launch_base_gemm(x, ldx, w0, ldw, y, ldy, seg->h_scratch, LORA_MAX_RANK, reinterpret_cast<float*>(seg->scratch),
-                          token_adapter, T, seg, view, dev_err, s);
+  return launch_base_gemm(x, ldx, w0, ldw, y, ldy, seg->h_scratch, LORA_MAX_RANK, token_adapter, T, view, dev_err, s);
 }
 
 lora_status_t lora_bgmv(const void* x, int64_t ldx, void* y, int64_t ldy, const int32_t* token_adapter,

@@ -8,8 +8,9 @@
 // before y is written, so y is written once and never read:
 //     y[t, n] = bf16( sum_k x[t,k] W0[n,k]  +  s_i sum_j h[t,j] B_i[j,n] ),
 // with h[t, j] = x[t] . A_i[j] computed beforehand by the shrink stage (by
-// token, fp32) and s_i the token's scale (0 when the token has no usable
-// adapter, which then gets the base product alone).
+// token, fp32) and s_i the adapter's scale; a token without a usable adapter
+// (id -1, or an adapter that fails the shrink's checks of id, rank and every
+// page) gets the base product alone.
 //
 // Base product: a persistent tcgen05 GEMM over 128 x 256 output tiles.  A
 // cluster of two CTAs takes the tiles (m, n) and (m + 1, n) together, pairs
@@ -61,10 +62,10 @@ constexpr size_t kBOffH = (size_t)kBStages * kBStageBytes;        // H: [128 row
 constexpr size_t kBOffD = kBOffH + (size_t)kBM * 128;             // B rows: [4 N-blocks][32 K rows][64 bf16], 128-byte swizzle
 constexpr size_t kBOffBars = kBOffD + (size_t)(kBN / 64) * kBRoundK * 128;
 constexpr int kBNBars = 2 * kBStages + 2 + 2 + 2 + 1;
-// control: row runs [128], run adapters [128], the round's blocks [2][4], the MMA's round words [2], runs
-// in the tile, tensor-memory slot
+// control: row runs [128], run adapters [128], run scales [128], the round's blocks [2][4], the MMA's
+// round words [2], runs in the tile, tensor-memory slot
 constexpr size_t kBOffCtl = (kBOffBars + kBNBars * 8 + 15) / 16 * 16;
-constexpr size_t kBSmem = kBOffCtl + (2 * kBM + 8 + 2 + 1 + 1) * 4 + 1024;  // + 1024-byte alignment
+constexpr size_t kBSmem = kBOffCtl + (3 * kBM + 8 + 2 + 1 + 1) * 4 + 1024;  // + 1024-byte alignment
 static_assert(kBOffH % 1024 == 0 && kBOffD % 1024 == 0, "swizzle atoms");
 static_assert(kBSmem <= 232448, "shared memory of one CTA");
 
@@ -75,7 +76,6 @@ struct BaseArgs {
   long long ldy;
   const float* h;  // [T, ldh]: h[t, j] = x[t] . A_i[j] for tokens with a usable adapter
   long long ldh;
-  const float* tscale;  // [T]: s_i for tokens with a usable adapter, else 0 (only read for ids >= 0)
   const int32_t* ids;
   DevView v;
   int T;
@@ -114,8 +114,9 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
   uint64_t* delta_empty = delta_full + 1;   // [1] MMA commit: the round's MMAs have read them
   uint64_t* mma_done = delta_empty + 1;
   int* row_run = reinterpret_cast<int*>(sm + kBOffCtl);  // [128] the row's run in the tile (-1: none)
-  int* run_ad = row_run + kBM;                            // [128] each run's adapter
-  int* rblk = run_ad + kBM;                               // [2][4] the round's blocks: run, j0, rank, b_page0
+  int* run_ad = row_run + kBM;                            // [128] each run's adapter (-1: it failed the checks)
+  float* run_s = reinterpret_cast<float*>(run_ad + kBM);  // [128] each run's scale
+  int* rblk = reinterpret_cast<int*>(run_s + kBM);        // [2][4] the round's blocks: run, j0, rank, b_page0
   int* rmma = rblk + 8;                                   // [2] blocks in the round, last round of the tile
   int* nruns = rmma + 2;                                  // runs in the tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(nruns + 1);
@@ -259,13 +260,9 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
       const int t = m * kBM + row;
       const int n_base = n * kBN;
       int ad = -1;
-      float s = 0.f;
       if (t < a.T) {
         const int id = a.ids[t];
-        if (id >= 0 && id < v.n_adapters) {
-          s = a.tscale[t];
-          if (s != 0.f) ad = id;
-        }
+        if (id >= 0 && id < v.n_adapters) ad = id;
       }
       if (part == 0) row_run[row] = ad;
       epi_bar();
@@ -292,14 +289,32 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
       }
       epi_bar();
       const int n_runs = *nruns;
-      const int my_run = row_run[row];
+      // each run's adapter checked as the shrink checks it (id, rank, every page),
+      // the sixteen warps taking the runs in turn; a run that fails adds nothing
+      for (int k = warp - 2; k < n_runs; k += kBEpiWarps) {
+        const int rad = run_ad[k];
+        const lora_adapter_desc_t dk = adapter_desc(v, rad);
+        const int bad = check_adapter_warp(v, rad, dk, lane);
+        __syncwarp();
+        if (lane == 0) {
+          run_s[k] = dk.scale;
+          if (bad) run_ad[k] = -1;
+        }
+      }
+      epi_bar();
+      int my_run = row_run[row];
+      if (my_run >= 0 && run_ad[my_run] < 0) my_run = -1;
+      const float s = my_run >= 0 ? run_s[my_run] : 0.f;
       const float* hrow = a.h + (long long)(t < a.T ? t : 0) * a.ldh;
-      // rounds: two 16-row blocks each, walking the runs in order
+      // rounds: two 16-row blocks each, walking the runs that passed in order
       int cur_run = 0, cur_j0 = 0, cur_r = 0, cur_bp = 0;  // thread 0's cursor
-      if (et == 0 && n_runs > 0) {
-        const lora_adapter_desc_t d0 = adapter_desc(v, run_ad[0]);
-        cur_r = d0.rank;
-        cur_bp = d0.b_page0;
+      if (et == 0) {
+        while (cur_run < n_runs && run_ad[cur_run] < 0) ++cur_run;
+        if (cur_run < n_runs) {
+          const lora_adapter_desc_t d0 = adapter_desc(v, run_ad[cur_run]);
+          cur_r = d0.rank;
+          cur_bp = d0.b_page0;
+        }
       }
       for (bool last = false; !last; ++rd) {
         // the MMA warp is done with the previous round's H and B
@@ -319,7 +334,9 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
               cur_j0 += 16;
               if (cur_j0 >= cur_r) {
                 cur_j0 = 0;
-                if (++cur_run < n_runs) {
+                ++cur_run;
+                while (cur_run < n_runs && run_ad[cur_run] < 0) ++cur_run;
+                if (cur_run < n_runs) {
                   const lora_adapter_desc_t d1 = adapter_desc(v, run_ad[cur_run]);
                   cur_r = d1.rank;
                   cur_bp = d1.b_page0;
@@ -427,60 +444,13 @@ __global__ void __launch_bounds__(kBThreads, 1) base_gemm_kernel(const __grid_co
   }
 }
 
-// Per-token scale for the base kernel: s_i for every token of a segment whose
-// adapter passes the checks (id, rank, every page of A_i and B_i) -- the same
-// checks the shrink makes before it writes a token's h -- and 0 (set before
-// this kernel) for every other token.  One warp per segment.
-struct ScaleArgs {
-  const int32_t* perm;
-  const int32_t* indptr;
-  const int32_t* seg_adapter;
-  const int32_t* meta;
-  float* tscale;
-  DevView v;
-  int32_t* err;
-};
-
-__global__ void __launch_bounds__(256) token_scale_kernel(const __grid_constant__ ScaleArgs a) {
-  pdl_wait_then_release();
-  const int lane = threadIdx.x & 31;
-  const int w0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
-  const int n_segs = a.meta[0];
-  for (int sg = w0; sg < n_segs; sg += nw) {
-    const int ad = a.seg_adapter[sg];
-    const lora_adapter_desc_t d = adapter_desc(a.v, ad);
-    const int bad = check_adapter_warp(a.v, ad, d, lane);
-    if (bad && lane == 0) report(a.err, bad);
-    const float s = bad ? 0.f : d.scale;
-    for (int p = a.indptr[sg] + lane; p < a.indptr[sg + 1]; p += 32) a.tscale[a.perm[p]] = s;
-  }
-}
-
 }  // namespace
 
 bool base_gemm_ok(const lora_pool_view_t* v) { return v->page_elems >= 32 && v->max_rank <= LORA_MAX_RANK; }
 
 lora_status_t launch_base_gemm(const void* x, long long ldx, const void* w0, long long ldw, void* y, long long ldy,
-                               const float* h, long long ldh, float* tscale, const int32_t* ids, int T,
-                               const lora_segments_t* seg, const lora_pool_view_t* view, int32_t* err,
-                               cudaStream_t stream) {
-  // per-token scales from the segments
-  {
-    ScaleArgs s;
-    memset(&s, 0, sizeof(s));
-    s.perm = seg->token_perm;
-    s.indptr = seg->seg_indptr;
-    s.seg_adapter = seg->seg_adapter;
-    s.meta = seg->meta;
-    s.tscale = tscale;
-    make_dev_view(view, &s.v);
-    s.err = err;
-    if (cudaMemsetAsync(tscale, 0, (size_t)T * sizeof(float), stream) != cudaSuccess) return LORA_ERR_CUDA;
-    const int blocks = std::max(1, std::min(sm_count() * 4, (T + 7) / 8));
-    if (launch_pdl((const void*)token_scale_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, 0, &s) !=
-        cudaSuccess)
-      return LORA_ERR_CUDA;
-  }
+                               const float* h, long long ldh, const int32_t* ids, int T, const lora_pool_view_t* view,
+                               int32_t* err, cudaStream_t stream) {
   BaseArgs a;
   memset(&a, 0, sizeof(a));
   if (!make_act_map(&a.xmap, x, T, view->d_in, ldx, kBM)) return LORA_ERR_UNSUPPORTED;
@@ -489,7 +459,6 @@ lora_status_t launch_base_gemm(const void* x, long long ldx, const void* w0, lon
   a.ldy = ldy;
   a.h = h;
   a.ldh = ldh;
-  a.tscale = tscale;
   a.ids = ids;
   make_dev_view(view, &a.v);
   a.T = T;

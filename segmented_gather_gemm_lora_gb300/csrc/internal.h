@@ -96,15 +96,14 @@ bool bgmv_decode_ok(const lora_pool_view_t* v, int T);
 lora_status_t launch_bgmv(const void* x, long long ldx, void* y, long long ldy, const int32_t* ids, int T,
                           const lora_pool_view_t* view, int early, int32_t* err, cudaStream_t stream);
 
-// Base projection with the adapter term in its epilogue (base_gemm.cu): the
-// per-token scales from the segments into tscale [T] (zeroed first), then the
-// tcgen05 GEMM y = x W0^T + tscale[t] h[t] B_i.  h: [T, ldh] by token, as the
-// shrink writes it.
+// Base projection with the adapter term (base_gemm.cu): the tcgen05 GEMM
+// y = x W0^T + s_i h[t] B_i for tokens whose adapter passes the shrink's
+// checks.  h: [T, ldh] by token, as the shrink writes it; ids: the tokens'
+// adapters.
 bool base_gemm_ok(const lora_pool_view_t* v);
 lora_status_t launch_base_gemm(const void* x, long long ldx, const void* w0, long long ldw, void* y, long long ldy,
-                               const float* h, long long ldh, float* tscale, const int32_t* ids, int T,
-                               const lora_segments_t* seg, const lora_pool_view_t* view, int32_t* err,
-                               cudaStream_t stream);
+                               const float* h, long long ldh, const int32_t* ids, int T, const lora_pool_view_t* view,
+                               int32_t* err, cudaStream_t stream);
 
 // Slices of d_in the tensor-core shrink splits a tile into (ks, each of klen
 // columns, a multiple of 64; the last may be shorter): about 512 columns each,
