@@ -18,12 +18,13 @@
 //
 // Gradient kernel.  A unit is (segment, matrix, 128-column block): the block's
 // columns of dB_i (a slice of d_out) or of dA_i (a slice of d_in), for all the
-// adapter's r_i rows.  Its CTA walks the segment's tokens 32 at a time, four
-// steps in flight: the token rows of dy (or x) for the block's columns and of h
-// (or u) arrive in shared memory by asynchronous copies, their token indices
-// four steps earlier, and each of the 8 warps accumulates its 16 columns x r_i
-// rows with mma.sync m16n8k16 (the contraction runs over the tokens, 16 per
-// MMA), taking h / u from the fp32 rows as bf16 hi + lo parts in registers.  At the end each element of the block is added once into the
+// adapter's r_i rows.  Its CTA walks the segment's tokens 32 at a time through
+// a five-step ring: the token rows of dy (or x) for the block's columns and of
+// h (or u) arrive in shared memory by asynchronous copies, their token indices
+// five steps earlier; each step's h / u is converted once, a step ahead, into
+// bf16 hi + lo parts, transposed; and each of the 8 warps accumulates its 16
+// columns x r_i rows with mma.sync m16n8k16 (the contraction runs over the
+// tokens, 16 per MMA).  At the end each element of the block is added once into the
 // gradient pool, at its pool position, by one atomic add: with GROUP segments
 // an adapter has one segment, so a call's sums are deterministic.
 #include <algorithm>
@@ -41,13 +42,16 @@ constexpr int kBThreads = 256;
 constexpr int kBCols = 128;              // gradient columns per unit
 constexpr int kBTok = 16;                // tokens per MMA (its k dimension)
 constexpr int kBStepTok = 32;            // tokens per step
-constexpr int kBStages = 4;              // steps in flight
+constexpr int kBStages = 5;              // steps in the ring
 constexpr int kBTokRing = 2 * kBStages;  // token-index slots: step m's indices arrive kBStages steps ahead
 constexpr int kBQStride = kBCols * 2 + 16;    // bytes per staged dy / x row (padded: conflict-free ldmatrix)
 constexpr int kBHStride = LORA_MAX_RANK + 4;  // floats per staged h / u row (padded: conflict-free fragments)
 constexpr size_t kBOffH = (size_t)kBStages * kBStepTok * kBQStride;
 constexpr size_t kBOffTok = kBOffH + (size_t)kBStages * kBStepTok * kBHStride * sizeof(float);
-constexpr size_t kBSmem = kBOffTok + (size_t)kBTokRing * kBStepTok * sizeof(int);
+constexpr int kBPStride = kBStepTok * 2 + 16;   // bytes per row of the transposed h / u (padded: conflict-free ldmatrix)
+constexpr int kBPPart = LORA_MAX_RANK * kBPStride;  // the hi part, then the lo part
+constexpr size_t kBOffP = kBOffTok + (size_t)kBTokRing * kBStepTok * sizeof(int);
+constexpr size_t kBSmem = kBOffP + 2 * 2 * (size_t)kBPPart;  // two steps' transposed h / u
 static_assert(kBOffH % 16 == 0 && (kBHStride * 4) % 16 == 0, "16-byte copy destinations");
 static_assert(kBStepTok * 16 == 2 * kBThreads, "two 16-byte pieces of a row per thread and step");
 
@@ -80,6 +84,9 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
                : "r"(addr)
                : "memory");
 }
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr) : "memory");
+}
 __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                              uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -96,6 +103,7 @@ __global__ void __launch_bounds__(kBThreads) grad_kernel(const __grid_constant__
   uint8_t* const qs = sm;                                        // [stage][token][kBQStride bytes]
   float* const hraw = reinterpret_cast<float*>(sm + kBOffH);     // [stage][token][kBHStride]
   int* const tokring = reinterpret_cast<int*>(sm + kBOffTok);    // [slot][token]
+  uint8_t* const pbuf = sm + kBOffP;  // [step & 1][hi, lo][rank row][token] bf16
   __shared__ int info[6];  // p0, count, rank, skip, a_page0 / b_page0 of the unit's matrix, scale bits
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const DevView& v = a.v;
@@ -173,16 +181,40 @@ __global__ void __launch_bounds__(kBThreads) grad_kernel(const __grid_constant__
     cp_async_commit();
     cp_async_wait<0>();
     __syncthreads();  // the first kBStages steps' indices
+    // step m's h / u as bf16 hi + lo parts, transposed (rank row, token), into
+    // buffer m & 1: thread (token pair tid % 16, rank rows 4 (tid / 16) ..), once
+    // for all the warps
+    auto convert = [&](int m) {
+      const int cst = m % kBStages, tp = tid & 15, q4 = tid >> 4;
+      if (4 * q4 < rpad) {
+        const float* hp = hraw + ((size_t)cst * kBStepTok + 2 * tp) * kBHStride + 4 * q4;
+        const float4 f0 = *reinterpret_cast<const float4*>(hp);
+        const float4 f1 = *reinterpret_cast<const float4*>(hp + kBHStride);
+        const float v0[4] = {f0.x, f0.y, f0.z, f0.w}, v1[4] = {f1.x, f1.y, f1.z, f1.w};
+        uint8_t* ph = pbuf + (size_t)(m & 1) * 2 * kBPPart + (size_t)(4 * q4) * kBPStride + 4 * tp;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t hi = pack_bf16x2(v0[e], v1[e]);
+          const uint32_t lo = pack_bf16x2(v0[e] - bf_lo(hi), v1[e] - bf_hi(hi));
+          *reinterpret_cast<uint32_t*>(ph + e * kBPStride) = hi;
+          *reinterpret_cast<uint32_t*>(ph + kBPPart + e * kBPStride) = lo;
+        }
+      }
+    };
     float acc[8][4];
 #pragma unroll
     for (int jt = 0; jt < 8; ++jt) acc[jt][0] = acc[jt][1] = acc[jt][2] = acc[jt][3] = 0.f;
 #pragma unroll
     for (int i = 0; i < kBStages - 1; ++i) load_step(i);
+    cp_async_wait<kBStages - 2>();  // step 0's copies
+    __syncthreads();
+    convert(0);
     const int g = lane >> 2, q = lane & 3;
     for (int i = 0; i < nsteps; ++i) {
-      cp_async_wait<kBStages - 2>();  // this thread's copies of step i, and the indices up to step i + kBStages
-      __syncthreads();                // everyone's; the stage of step i - 1 is free
+      cp_async_wait<kBStages - 3>();  // this thread's copies of step i + 1, and the indices up to step i + kBStages + 1
+      __syncthreads();                // everyone's; step i's parts are converted; the stage of step i - 1 is free
       load_step(i + kBStages - 1);
+      if (i + 1 < nsteps) convert(i + 1);
       const int st = i % kBStages;
       // warp w: columns 16 w .. 16 w + 15 of the block (A operand: the staged rows
       // transposed, k = token); the rank rows 8 at a time (B operand: h / u, as
@@ -194,17 +226,16 @@ __global__ void __launch_bounds__(kBThreads) grad_kernel(const __grid_constant__
           const int trow = ks * kBTok + (lane & 7) + 8 * (lane >> 4), tcol = 16 * warp + 8 * ((lane >> 3) & 1);
           uint32_t a0, a1, a2, a3;
           ldsm_x4_trans(smem_u32(qs + ((size_t)st * kBStepTok + trow) * kBQStride + tcol * 2), a0, a1, a2, a3);
-          // the lane's B entries: tokens 2q, 2q + 1 (b0) and 2q + 8, 2q + 9 (b1) of the
-          // MMA's 16, rank row 8 jt + g
-          const float* hb = hraw + ((size_t)st * kBStepTok + ks * kBTok + 2 * q) * kBHStride + g;
+          // B operand: rank rows 8 jt .. 8 jt + 7 of the transposed h / u, the MMA's
+          // tokens 0-7 (lanes 0-7) and 8-15 (lanes 8-15)
+          const uint32_t pb = smem_u32(pbuf + (size_t)(i & 1) * 2 * kBPPart) + (uint32_t)((lane & 7) * kBPStride +
+                                                                                       32 * ks + 16 * ((lane >> 3) & 1));
 #pragma unroll
           for (int jt = 0; jt < 8; ++jt) {
             if (8 * jt >= rpad) break;
-            const float h0 = hb[8 * jt], h1 = hb[kBHStride + 8 * jt];
-            const float h2 = hb[8 * kBHStride + 8 * jt], h3 = hb[9 * kBHStride + 8 * jt];
-            const uint32_t bh0 = pack_bf16x2(h0, h1), bh1 = pack_bf16x2(h2, h3);
-            const uint32_t bl0 = pack_bf16x2(h0 - bf_lo(bh0), h1 - bf_hi(bh0));
-            const uint32_t bl1 = pack_bf16x2(h2 - bf_lo(bh1), h3 - bf_hi(bh1));
+            uint32_t bh0, bh1, bl0, bl1;
+            ldsm_x2(pb + 8 * jt * kBPStride, bh0, bh1);
+            ldsm_x2(pb + kBPPart + 8 * jt * kBPStride, bl0, bl1);
             mma_m16n8k16(acc[jt], a0, a1, a2, a3, bh0, bh1);
             mma_m16n8k16(acc[jt], a0, a1, a2, a3, bl0, bl1);
           }
