@@ -746,6 +746,62 @@ def backward_bytes(batch, pool) -> int:
     return n * pool.d_in * 2 + n * pool.d_out * 2 + n * pool.d_in * 4 + elems * 2 + elems * 8
 
 
+def pipelined_e2e(torch, dev, inputs, run, n_out, steps, world, tokens):
+    """End to end through the public calls for the lines of one call per step:
+    `inputs` (device tensors: the step's inputs, the ones it updates in place first)
+    are copied in every step from one pinned host buffer into one of two device staging
+    slots, `run(views)` enqueues the step on the current stream on that slot's copies,
+    and the first `n_out` of them (the step's result) are read back into pinned host
+    memory.  Step k + 1's copy in runs under step k's calls, on streams of their own; a
+    slot is refilled once the step that last used it has been read back.  Returns
+    (tokens/s, bytes in, bytes out per step)."""
+    offs, cur = [], 0
+    for t in inputs:
+        offs.append(cur)
+        cur += (t.numel() * t.element_size() + 255) // 256 * 256
+    hstage = torch.empty(cur, dtype=torch.uint8).pin_memory()
+    for t, o in zip(inputs, offs):
+        hstage[o:o + t.numel() * t.element_size()].copy_(t.reshape(-1).view(torch.uint8).cpu())
+    out_end = offs[n_out - 1] + inputs[n_out - 1].numel() * inputs[n_out - 1].element_size()
+    slots = []
+    for _ in range(2):
+        d = torch.empty(cur, dtype=torch.uint8, device=dev)
+        views = [d[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(inputs, offs)]
+        slots.append((d, views, torch.empty(out_end, dtype=torch.uint8).pin_memory()))
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def one(k):
+        d, views, hout = slots[k & 1]
+        with torch.cuda.stream(s_in):
+            if k >= 2:
+                s_in.wait_event(ev_out[k & 1])
+            d.copy_(hstage, non_blocking=True)
+            ev_in[k & 1].record(s_in)
+        comp.wait_event(ev_in[k & 1])
+        run(views)
+        ev_comp[k & 1].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[k & 1])
+            hout.copy_(d[:out_end], non_blocking=True)
+            ev_out[k & 1].record(s_out)
+
+    for k in range(3):
+        one(k)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for k in range(3, 3 + steps):
+        one(k)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    del slots, hstage
+    return sum_over_ranks(steps * tokens, world) / e2e_s, cur, out_end
+
+
 def run_backward_line(steps, warmup, soak_seconds, world, rank, local):
     """The backward pass (adapter training) on the prefill-shaped batch: a step is
     lora_segments_build + lora_sgmv_backward (dA, dB into an fp32 gradient pool, dx
@@ -818,6 +874,14 @@ def run_backward_line(steps, warmup, soak_seconds, world, rank, local):
     clocks = sampler.stop()
     ms = max_over_ranks(e0.elapsed_time(e1), world)
     assert int(err.item()) == 0, "device error word %d" % int(err.item())
+    S0 = sets[0]
+
+    def run_bw(vw):  # dx (updated in place, read back), x, dy, ids
+        B.lora_segments_build(vw[3], S0["n_ad"], S0["seg"], mode=B.LORA_SEG_GROUP, err=err)
+        B.lora_sgmv_backward(vw[1], vw[2], vw[0], S0["grad"], S0["hu"], S0["seg"], S0["view"], err=err)
+
+    e2e_value, e2e_in, e2e_out = pipelined_e2e(torch, dev, [S0["dx"], S0["x"], S0["dy"], S0["ids"]], run_bw, 1,
+                                               min(steps, 50), world, S0["T"])
     n_steps = reps * g_steps
     tokens = sum_over_ranks(reps * sum(sets[i % len(sets)]["T"] for i in range(g_steps)), world)
     bytes_avg = statistics.fmean(sets[i % len(sets)]["bytes"] for i in range(g_steps))
@@ -843,6 +907,10 @@ def run_backward_line(steps, warmup, soak_seconds, world, rank, local):
                      "peak_kind": peak_kind, "traffic": None,
                      "algorithmic_bytes_per_launch": bytes_avg, "avg_launch_us": step_s * 1e6,
                      "tflops": flops_avg / step_s / 1e12},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": e2e_in, "d2h_bytes_per_step": e2e_out,
+                "note": "lora_segments_build + lora_sgmv_backward, eager; x, dy, dx and the ids copied in from "
+                        "pinned host memory and dx read back every step (the gradient pool stays on the device "
+                        "for the optimizer), pipelined over two staging slots"},
         "gpu_launches": int(round(launches_per_step * n_steps)),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
@@ -933,6 +1001,14 @@ def run_base_line(steps, warmup, soak_seconds, world, rank, local):
     clocks = sampler.stop()
     ms_u = timed(g_u, reps, n)
     assert int(err.item()) == 0, "device error word %d" % int(err.item())
+    S0 = sets[0]
+
+    def run_base(vw):  # y (written, read back), x, ids
+        B.lora_segments_build(vw[2], S0["n_ad"], S0["seg"], mode=B.LORA_SEG_CONTIGUOUS, err=err)
+        B.lora_base_apply(vw[1], S0["w0"], vw[0], vw[2], S0["seg"], S0["view"], err=err)
+
+    e2e_value, e2e_in, e2e_out = pipelined_e2e(torch, dev, [S0["y"], S0["x"], S0["ids"]], run_base, 1,
+                                               min(steps, 50), world, S0["T"])
     tokens = sum_over_ranks(statistics.fmean(S["T"] for S in sets), world)
     flops = statistics.fmean(S["flops"] for S in sets)
     step_s = ms_f / 1e3
@@ -963,6 +1039,10 @@ def run_base_line(steps, warmup, soak_seconds, world, rank, local):
                      "frac": achieved / tc_sustained,
                      "peak_kind": "measured sustained bf16 (cuBLAS loop, MEASURED_PEAKS.json)", "traffic": None,
                      "flops_per_step": flops, "avg_launch_us": step_s * 1e6},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": e2e_in, "d2h_bytes_per_step": e2e_out,
+                "note": "lora_segments_build + lora_base_apply, eager; x and the ids copied in from pinned host "
+                        "memory and y read back every step (W0 and the adapters resident), pipelined over two "
+                        "staging slots"},
         "gpu_launches": int(round(launches_per_step * reps * n)),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
