@@ -1147,6 +1147,42 @@ def cpu_baseline(workload: str, seconds: float):
     return res, ys, [pool.d_out for pool, _ in calls]
 
 
+def cpu_baseline_line(kind: str, seconds: float):
+    """The fp64 oracle as it stands, single-threaded, for the backward ("backward":
+    oracle.lora_backward) or the fused base projection ("base_fused": oracle.base_apply)
+    on the first tokens of the same prefill batch, repeated for a bounded time; tokens/s.
+    The sample is sized so that one pass takes about a quarter of the time."""
+    import oracle
+    from segmented_gather_gemm_lora_gb300 import workloads as W
+
+    wl = W.prefill(0)
+    pool, b = wl.pools[0], wl.batch
+    rng = np.random.default_rng([0, 9])
+    if kind == "backward":
+        g = W._normal_bf16(rng, (b.T, pool.d_out), 1.0)
+        run = lambda n: oracle.lora_backward(b.x[:n], g[:n], b.ids[:n], pool)
+        what = "oracle.lora_backward (h, u, dA, dB, dx)"
+    else:
+        w0 = W.f32_to_bf16_bits((rng.standard_normal((pool.d_out, pool.d_in)) / 64.0).astype(np.float32))
+        run = lambda n: oracle.base_apply(b.x[:n], w0, b.ids[:n], pool)
+        what = "oracle.base_apply (x W0^T and the adapter term)"
+    t1 = time.perf_counter()
+    run(8)
+    per_tok = (time.perf_counter() - t1) / 8
+    n = int(min(b.T, max(8, seconds / 4 / max(per_tok, 1e-9))))
+    n_tok = int((b.ids[:n] >= 0).sum())
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        run(n)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": reps * n_tok / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%s on the batch's first %d tokens, %d times, %.1f s" % (what, n, reps, dt)}
+
+
 def run_reference(args, world, rank):
     """The reference arm: the CPU fp64 oracle, unchanged, over the step's calls on every
     host core (one spawned process per core, each on an interleaved share of the tokens),
@@ -1228,10 +1264,15 @@ def main(argv=None):
         per_config["backward"] = run_backward_line(BACKWARD_STEPS, args.warmup, args.soak_seconds, world, rank,
                                                    local)
         per_config["base_fused"] = run_base_line(BASE_STEPS, args.warmup, args.soak_seconds, world, rank, local)
+        if rank == 0 and world == 1 and args.cpu_seconds > 0:
+            for k in ("backward", "base_fused"):
+                per_config[k]["cpu_baseline"] = cpu_baseline_line(k, args.cpu_seconds)
     if head == "backward":
         h = run_backward_line(args.steps, args.warmup, args.soak_seconds, world, rank, local)
     elif head == "base_fused":
         h = run_base_line(args.steps, args.warmup, args.soak_seconds, world, rank, local)
+    if head in ("backward", "base_fused") and rank == 0 and world == 1 and args.cpu_seconds > 0:
+        h["cpu_baseline"] = cpu_baseline_line(head, args.cpu_seconds)
     else:
         h = config_line(head, args, world, rank, local, args.steps)
     out = {
