@@ -1190,6 +1190,19 @@ def run_reference(args, world, rank):
     import oracle
 
     name = HEADLINE if args.workload == "all" else args.workload
+    if name in ("backward", "base_fused"):  # the oracle's backward or base projection, on one core
+        from segmented_gather_gemm_lora_gb300 import workloads as W
+
+        step_tokens = W.prefill(0).batch.T
+        base = cpu_baseline_line(name, min(60.0, max(5.0, float(args.steps))))
+        return {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": step_tokens / base["value"] * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": name + " on the prefill SGMV batch",
+                           "step": "the CPU fp64 oracle (%s)" % base["sample"]},
+                "cpu_baseline": base,
+                "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     wl, calls, scale = oracle_sample(name)
     b = wl.batch
     n_tok = int((b.ids >= 0).sum())
