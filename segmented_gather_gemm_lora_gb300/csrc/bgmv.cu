@@ -45,7 +45,6 @@ namespace {
 
 constexpr int kDHalves = 2;  // 512-column halves of a CTA's slice
 constexpr int kDThreads = 128 * kDHalves;
-constexpr int kDWarps = kDThreads / 32;
 constexpr int kDMaxRank = 16;    // the adapter's rows held at once
 constexpr int kDMaxCols = 512 * kDHalves;   // columns of a CTA's slice of d_in or d_out
 constexpr int kDRowStride = kDMaxCols * 2 + 16;  // bytes between staged rows
