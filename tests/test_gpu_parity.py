@@ -739,6 +739,44 @@ def test_tc_device_errors_in_long_tiles():
         assert np.array_equal(y[~good], batch.y0[~good])
 
 
+def test_fused_shrink_only_bad_adapters_and_counters():
+    """lora_sgmv_shrink on long tiles (the fused kernel's shrink-only form): an adapter
+    whose rank is above the view's max_rank and one with a page slot outside the pool
+    write no h (their rows keep the caller's values) and set the oracle's error bits;
+    the good adapters' h match the oracle; two calls in a row on one segment buffer give
+    the same h, and a lora_apply on that buffer afterwards equals one on a fresh buffer
+    bit for bit (the work counter is back at zero after each call)."""
+    rng = np.random.default_rng(31)
+    pool = W.build_pool(rng, 4096, 1024, [16, 16, 16, 64], max_rank=64)
+    pool.desc[1]["rank"] = 80
+    pool.page_list[int(pool.desc[2]["a_page0"]) + 2] = pool.n_pages + 9
+    ids = np.repeat(np.array([0, 1, 2, 3, 0], dtype=np.int32), [300, 140, 130, 200, 40])
+    batch = W.make_batch(rng, ids, 4096, 1024)
+    view = B.PoolView.from_host(pool)
+    seg = B.Segments(batch.T)
+    err = new_err()
+    B.lora_segments_build(ids_dev(ids), 4, seg, mode=B.LORA_SEG_GROUP, err=err)
+    href, oerr = oracle.shrink(batch.x, ids, pool, h_init=np.full((batch.T, 64), -3.0), ldh=64)
+    assert oerr == B.LORA_DERR_BAD_RANK | B.LORA_DERR_BAD_PAGE
+    outs = []
+    for _ in range(2):
+        err.zero_()
+        h = torch.full((batch.T, 64), -3.0, dtype=torch.float32, device="cuda")
+        B.lora_sgmv_shrink(to_dev_bits(batch.x), h, seg, view, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == oerr
+        hh = h.cpu().numpy()
+        np.testing.assert_allclose(hh, href, rtol=1e-4, atol=1e-4)
+        outs.append(hh)
+    assert np.array_equal(outs[0], outs[1])
+    y = to_dev_bits(batch.y0)
+    B.lora_apply(to_dev_bits(batch.x), y, seg, view, err=err)
+    torch.cuda.synchronize()
+    fresh, e2, _ = run_apply(batch, pool, B.LORA_SEG_GROUP, 4, view=view)
+    assert e2 == oerr
+    assert np.array_equal(to_host_bits(y), fresh)
+
+
 def test_tc_segments_reused_across_calls_and_shapes():
     """One segment buffer serves several projections of different d_in in a row (the
     tensor-core kernels' work counters must be back at zero after each call);
