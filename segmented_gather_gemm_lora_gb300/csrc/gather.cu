@@ -22,7 +22,8 @@
 // CTA 0 of a cluster claiming and handing the claim to its peers, when the
 // segments give one; one-token units go round-robin), resolves each unit's
 // tokens and adapter, checks every page slot of the adapter and caches its
-// physical pages, one unit ahead of the producers.  Warps 8, 10 and 11
+// physical pages, up to three units ahead of the producers (one when the
+// same call's fused kernel runs beside it).  Warps 8, 10 and 11
 // produce: they stage 16-row chunks of the adapter (1 KB row runs, translated
 // through the page table, "Multi-LoRA Serving in Production", section "Unified
 // Paged Memory"; one bulk copy per row run and page) with the unit's token rows
@@ -60,7 +61,8 @@ constexpr int kGConsThreads = 32 * kGCons;
 constexpr int kMaxCluster = 8;
 constexpr int kStages = 4;
 constexpr int kStageBytes = (kChunkRows + kNT) * kRowStride;  // 20.3 KB
-constexpr int kMaxPgSlots = 512;  // page-list slots of one adapter cached in shared memory
+constexpr int kMaxPgSlots = 320;  // page-list slots of one adapter cached in shared memory
+constexpr int kUSlots = 4;        // unit slots: the scheduler resolves up to three units ahead
 
 enum GKind { kGShrink = 0, kGExpand = 1, kGReduce = 2, kGEnd = 3 };
 enum GFlag {
@@ -133,13 +135,13 @@ constexpr size_t kOffRec = (size_t)kStages * kStageBytes;
 constexpr size_t kOffPw = kOffRec + (size_t)kStages * 64;                     // fp32 [kGCons][kNT][kHMax]
 constexpr size_t kOffRecv = kOffPw + (size_t)kGCons * kNT * kHMax * sizeof(float);  // fp32 [2][kMaxCluster][kNT][kHMax]
 constexpr size_t kOffHs = kOffRecv + 2 * (size_t)kMaxCluster * kNT * kHMax * sizeof(float);  // fp32 [kNT][kHMax]
-constexpr size_t kOffPgt = kOffHs + kNT * kHMax * sizeof(float);          // int [2][kMaxPgSlots]
-constexpr size_t kOffUnit = kOffPgt + 2 * kMaxPgSlots * sizeof(int);      // GUnit [2], 64-byte slots
-constexpr size_t kOffClaim = kOffUnit + 2 * 64;                           // int [2]
+constexpr size_t kOffPgt = kOffHs + kNT * kHMax * sizeof(float);          // int [kUSlots][kMaxPgSlots]
+constexpr size_t kOffUnit = kOffPgt + kUSlots * kMaxPgSlots * sizeof(int);  // GUnit [kUSlots], 64-byte slots
+constexpr size_t kOffClaim = kOffUnit + kUSlots * 64;                     // int [2]
 constexpr size_t kOffCls = kOffClaim + 16;                                // uint32 [3][32] unit classes
 constexpr size_t kOffProj = kOffCls + 3 * 32 * sizeof(uint32_t);        // GProj [kMaxFusedProj], 16-byte slots
 constexpr size_t kOffBars = kOffProj + kMaxFusedProj * ((sizeof(GProj) + 15) / 16 * 16);
-constexpr int kNBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1 + 1;
+constexpr int kNBars = 2 * kStages + 2 + 2 + 2 + 2 * kUSlots + 1 + 1;
 constexpr size_t kGatherSmem = kOffBars + kNBars * 8;
 // two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
 static_assert(kGatherSmem <= 233472 / 2 - 1024, "two gather CTAs per SM");
@@ -200,9 +202,9 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   uint64_t* recv_full = bars + 2 * kStages;  // [2] this CTA's arrival + every CTA's partial bytes
   uint64_t* claim_full = recv_full + 2;     // [2] CTA 0's scheduler
   uint64_t* claim_empty = claim_full + 2;  // [2] (CTA 0 only) one arrival per CTA
-  uint64_t* unit_full = claim_empty + 2;   // [2] the scheduler
-  uint64_t* unit_empty = unit_full + 2;    // [2] the producer
-  uint64_t* cons = unit_empty + 2;         // 8 consumer warps, twice per group
+  uint64_t* unit_full = claim_empty + 2;   // [kUSlots] the scheduler
+  uint64_t* unit_empty = unit_full + kUSlots;  // [kUSlots] the producers
+  uint64_t* cons = unit_empty + kUSlots;   // 8 consumer warps, twice per group
   uint64_t* cls_ready = cons + 1;          // 8 consumer warps, once
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -221,6 +223,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       mbar_init(smem_u32(&recv_full[b]), 1);
       mbar_init(smem_u32(&claim_full[b]), 1);
       mbar_init(smem_u32(&claim_empty[b]), ncta);
+    }
+    for (int b = 0; b < kUSlots; ++b) {
       mbar_init(smem_u32(&unit_full[b]), 1);
       mbar_init(smem_u32(&unit_empty[b]), kGProds);
     }
@@ -268,13 +272,18 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   if (warp == kGSched) {
     // ---------------- scheduler ----------------
     // Claims a unit, resolves its segment, tokens and adapter, checks every
-    // page slot of the adapter and caches the physical pages, a unit ahead of
-    // the producer (two unit slots).
+    // page slot of the adapter and caches the physical pages, `depth` - 1
+    // units ahead of the producers.
     // Claims: unit cid first, then units ncl + counter, CTA 0 claiming for the
     // cluster.  Each cluster over-claims the counter exactly once; the last
     // claim of all puts it back to zero for the next call.  A unit is claimed
-    // only once the producer has started on the previous one, so that when
-    // the units run out no cluster holds more than one in reserve.
+    // only once the producers have started on the one `depth` - 1 before it,
+    // so that the resolution of small units (a chain of dependent loads) hides
+    // behind the copies of the units between, and when the units run out no
+    // cluster holds more than `depth` - 1 in reserve.  Measured on the hetero
+    // up + down pair (µs): depth 2 123.5, 3 119.6, 4 116.2; beside the fused
+    // kernel deeper reserves cost more at the tail than they hide (13B-shaped
+    // forward, ms: 17.33, 17.49, 17.64), so there the depth is 2.
     int u = (int)cid;
     int claim = 0;      // CTA 0, lane 0: the counter's last answer
     bool over = false;  // CTA 0, lane 0: this cluster's over-claim is made
@@ -347,11 +356,17 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       ++nclaim;
     };
     uint32_t nposted = 0;  // units handed to the producer
-    // the slot of the next unit, once the producer is done with its last use
-    // (it has then started on the previous unit)
+    const uint32_t depth = beside_fused ? 2u : (uint32_t)kUSlots;
+    // the slot of the next unit, once the producers are done with the unit
+    // `depth` before it (they have then started on the one after that).  Units
+    // are released in order, so that unit's slot barrier has completed every
+    // earlier phase, and a slot is free once the unit kUSlots before it is done.
     auto take_slot = [&]() -> uint32_t {
-      const uint32_t q = nposted & 1;
-      if (nposted >= 2 && !mbar_wait(smem_u32(&unit_empty[q]), ((nposted >> 1) - 1) & 1)) ok = false;
+      const uint32_t q = nposted % kUSlots;
+      if (nposted >= depth) {
+        const uint32_t pu = nposted - depth;
+        if (!mbar_wait(smem_u32(&unit_empty[pu % kUSlots]), (pu / kUSlots) & 1)) ok = false;
+      }
       return q;
     };
     for (uint32_t k = 0; ok; ++k) {
@@ -483,8 +498,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       ++g;
     };
     for (uint32_t nu = 0; ok; ++nu) {
-      const uint32_t q = nu & 1;
-      if (!mbar_wait(smem_u32(&unit_full[q]), (nu >> 1) & 1)) {
+      const uint32_t q = nu % kUSlots;
+      if (!mbar_wait(smem_u32(&unit_full[q]), (nu / kUSlots) & 1)) {
         ok = false;
         break;
       }
