@@ -745,13 +745,32 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   cluster_sync();
 }
 
+// Cluster width.  CTA c of a cluster of w owns the c-th of w equal runs of
+// d_in and of d_out, staged in kSub-column sub-slices, so a unit of one row
+// block costs w * (sub-slices of a d_in run + of a d_out run) stages, and a
+// stage costs the same hand-offs however few columns it carries.  The width is
+// the one with the fewest stages per unit among w in [w0 / 2, w0], w0 the width
+// whose runs are one sub-slice (at most kMaxCluster); ties go to the wider.
+// For d = 5120 that is 5 CTAs of 1024 columns (8 CTAs of 640 would stage every
+// row block as a 512- and a 128-column piece).
 static int cluster_size_for(const lora_pool_view_t* const* views, int n) {
   int d = 0;
   for (int g = 0; g < n; ++g) d = std::max(d, std::max(views[g]->d_in, views[g]->d_out));
-  int cl = (d + 511) / 512;
-  if (cl < 1) cl = 1;
-  if (cl > kMaxCluster) cl = kMaxCluster;
-  return cl;
+  const int w0 = std::min(std::max((d + kSub - 1) / kSub, 1), kMaxCluster);
+  int best = w0;
+  long long best_cost = -1;
+  for (int w = w0; w >= std::max(1, w0 / 2); --w) {
+    long long cost = 0;
+    for (int g = 0; g < n; ++g) {
+      const int kc = ((views[g]->d_in + w - 1) / w + 7) & ~7, nc = ((views[g]->d_out + w - 1) / w + 7) & ~7;
+      cost += (long long)w * ((kc + kSub - 1) / kSub + (nc + kSub - 1) / kSub);
+    }
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = w;
+    }
+  }
+  return best;
 }
 
 lora_status_t launch_gather_multi(int mode, int src, int short_only, int n_proj, const ProjCall* projs, float* h,
