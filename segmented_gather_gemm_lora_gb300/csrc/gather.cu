@@ -22,8 +22,7 @@
 // CTA 0 of a cluster claiming and handing the claim to its peers, when the
 // segments give one; one-token units go round-robin), resolves each unit's
 // tokens and adapter, checks every page slot of the adapter and caches its
-// physical pages, up to three units ahead of the producers (one when the
-// same call's fused kernel runs beside it).  Warps 8, 10 and 11
+// physical pages, up to three units ahead of the producers.  Warps 8, 10 and 11
 // produce: they stage 16-row chunks of the adapter (1 KB row runs, translated
 // through the page table, "Multi-LoRA Serving in Production", section "Unified
 // Paged Memory"; one bulk copy per row run and page) with the unit's token rows
@@ -272,18 +271,18 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
   if (warp == kGSched) {
     // ---------------- scheduler ----------------
     // Claims a unit, resolves its segment, tokens and adapter, checks every
-    // page slot of the adapter and caches the physical pages, `depth` - 1
+    // page slot of the adapter and caches the physical pages, up to three
     // units ahead of the producers.
     // Claims: unit cid first, then units ncl + counter, CTA 0 claiming for the
     // cluster.  Each cluster over-claims the counter exactly once; the last
     // claim of all puts it back to zero for the next call.  A unit is claimed
-    // only once the producers have started on the one `depth` - 1 before it,
-    // so that the resolution of small units (a chain of dependent loads) hides
-    // behind the copies of the units between, and when the units run out no
-    // cluster holds more than `depth` - 1 in reserve.  Measured on the hetero
-    // up + down pair (µs): depth 2 123.5, 3 119.6, 4 116.2; beside the fused
-    // kernel deeper reserves cost more at the tail than they hide (13B-shaped
-    // forward, ms: 17.33, 17.49, 17.64), so there the depth is 2.
+    // once the producers have started on the one three before it (kUSlots
+    // unit slots), so that the resolution of small units (a chain of dependent
+    // loads) hides behind the copies of the units between.  Measured on the
+    // hetero up + down pair (µs), units claimed once the producers started on
+    // the one 1 / 2 / 3 before: 123.5, 119.6, 116.2; a reserve cut back to one
+    // unit once fewer than two per cluster remain took it back to 123.1, and
+    // the 13B-shaped forward is fastest with three too.
     int u = (int)cid;
     int claim = 0;      // CTA 0, lane 0: the counter's last answer
     bool over = false;  // CTA 0, lane 0: this cluster's over-claim is made
@@ -356,17 +355,11 @@ __global__ void __launch_bounds__(kGThreads, 2) gather_kernel(const __grid_const
       ++nclaim;
     };
     uint32_t nposted = 0;  // units handed to the producer
-    const uint32_t depth = beside_fused ? 2u : (uint32_t)kUSlots;
-    // the slot of the next unit, once the producers are done with the unit
-    // `depth` before it (they have then started on the one after that).  Units
-    // are released in order, so that unit's slot barrier has completed every
-    // earlier phase, and a slot is free once the unit kUSlots before it is done.
+    // the slot of the next unit, once the producers are done with its last
+    // use (they have then started on the unit after that one)
     auto take_slot = [&]() -> uint32_t {
       const uint32_t q = nposted % kUSlots;
-      if (nposted >= depth) {
-        const uint32_t pu = nposted - depth;
-        if (!mbar_wait(smem_u32(&unit_empty[pu % kUSlots]), (pu / kUSlots) & 1)) ok = false;
-      }
+      if (nposted >= kUSlots && !mbar_wait(smem_u32(&unit_empty[q]), ((nposted / kUSlots) - 1) & 1)) ok = false;
       return q;
     };
     for (uint32_t k = 0; ok; ++k) {
