@@ -1255,6 +1255,21 @@ def config_line(name, args, world, rank, local, steps):
     return out
 
 
+def head_line(head, args, world, rank, local):
+    """The line of the workload the JSON line leads with: the backward and base-projection
+    lines have runners of their own (and their single-core oracle baseline, on rank 0 of a
+    one-process run when --cpu-seconds is above zero); every other workload is a config line."""
+    if head == "backward":
+        h = run_backward_line(args.steps, args.warmup, args.soak_seconds, world, rank, local)
+    elif head == "base_fused":
+        h = run_base_line(args.steps, args.warmup, args.soak_seconds, world, rank, local)
+    else:
+        return config_line(head, args, world, rank, local, args.steps)
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        h["cpu_baseline"] = cpu_baseline_line(head, args.cpu_seconds)
+    return h
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_info()
@@ -1280,14 +1295,7 @@ def main(argv=None):
         if rank == 0 and world == 1 and args.cpu_seconds > 0:
             for k in ("backward", "base_fused"):
                 per_config[k]["cpu_baseline"] = cpu_baseline_line(k, args.cpu_seconds)
-    if head == "backward":
-        h = run_backward_line(args.steps, args.warmup, args.soak_seconds, world, rank, local)
-    elif head == "base_fused":
-        h = run_base_line(args.steps, args.warmup, args.soak_seconds, world, rank, local)
-    if head in ("backward", "base_fused") and rank == 0 and world == 1 and args.cpu_seconds > 0:
-        h["cpu_baseline"] = cpu_baseline_line(head, args.cpu_seconds)
-    else:
-        h = config_line(head, args, world, rank, local, args.steps)
+    h = head_line(head, args, world, rank, local)
     out = {
         "metric": METRIC,
         "value": h["value"],

@@ -1,7 +1,7 @@
 """The bench's multi-process arithmetic, on CPU with two gloo ranks: the timed region
 is the slowest rank's (max over ranks), the throughput counts every rank's tokens
 (sum over ranks), and the shards are independent (weak scaling, no data-path
-collective)."""
+collective).  Also the choice of runner for the line the JSON leads with."""
 
 import os
 import socket
@@ -55,3 +55,33 @@ def test_single_process_helpers_are_identity():
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.sum_over_ranks(7.0, 1) == 7.0
     bench.barrier(1)
+
+
+@pytest.mark.parametrize("head", ["backward", "base_fused", "prefill"])
+@pytest.mark.parametrize("cpu_seconds", [0.0, 2.0])
+def test_head_line_runs_one_runner(monkeypatch, head, cpu_seconds):
+    """The leading line runs exactly one runner for its workload, whatever --cpu-seconds is,
+    and the backward and base-projection lines get their own oracle baseline only when asked."""
+    import argparse
+
+    import bench
+
+    calls = []
+
+    def runner(kind):
+        def run(*a, **k):
+            calls.append(kind)
+            return {"value": 1.0}
+        return run
+
+    monkeypatch.setattr(bench, "run_backward_line", runner("backward"))
+    monkeypatch.setattr(bench, "run_base_line", runner("base_fused"))
+    monkeypatch.setattr(bench, "config_line", runner("config"))
+    monkeypatch.setattr(bench, "cpu_baseline_line", lambda kind, s: {"kind": "oracle", "of": kind})
+    args = argparse.Namespace(steps=3, warmup=3, soak_seconds=0.0, cpu_seconds=cpu_seconds)
+    h = bench.head_line(head, args, 1, 0, 0)
+    assert calls == [head if head in ("backward", "base_fused") else "config"]
+    if head in ("backward", "base_fused") and cpu_seconds > 0:
+        assert h["cpu_baseline"] == {"kind": "oracle", "of": head}
+    else:
+        assert "cpu_baseline" not in h
