@@ -513,9 +513,12 @@ def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, loca
     # it through the public calls, and reads its y back into pinned host memory (one
     # copy).  The 13B forward stages layer 0's seven x / y0 in and reads layer 39's seven
     # y out.  When a step copies 8 MB or more in, the steps are pipelined as a serving
-    # loop would run them: two device staging slots alternate, the copies in and out run
-    # on streams of their own, and step k + 1's copy in overlaps step k's calls; a slot
-    # is refilled only after the read-back of the step that last used it.  Smaller steps
+    # loop would run them: device staging slots take turns, the copies in and out run
+    # on streams of their own, and step k + 1's copy in overlaps step k's calls and step
+    # k - 1's read-back (both directions of the host link at once); a slot
+    # is refilled once the step that last used it no longer needs what the copy
+    # overwrites (its calls are done, and its outputs read back when they sit in the
+    # staging buffer).  Smaller steps
     # (decode, tiny) are bound by the host's launches, where the extra streams and events
     # cost more than they hide: one slot, everything on the launching stream.  All of
     # every step's copies are inside the timed region.
@@ -540,8 +543,12 @@ def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, loca
     n_in = len(ins)
     y_lo, y_hi = offs[n_in], offs[-1] + pieces[-1].numel() * 2  # the staged y, contiguous
     pipelined = cur >= (8 << 20)
+    # staging slots: three where the outputs sit in the staging buffer (a slot's read-back
+    # then runs beside the next slot's copy in), two for the 13B forward (its outputs have
+    # buffers of their own), one when not pipelined
+    ns = (2 if name == "mixed13b" else 3) if pipelined else 1
     slots = []
-    for _ in range(2 if pipelined else 1):
+    for _ in range(ns):
         dstage = torch.empty(cur, dtype=torch.uint8, device=dev)
         views = [dstage[o:o + t.numel() * 2].view(torch.bfloat16).view(t.shape) for t, o in zip(pieces, offs)]
         e_calls, k = [], n_in
@@ -565,9 +572,9 @@ def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, loca
                           if not bgmv else None))
     comp = torch.cuda.current_stream(dev)
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_comp = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(ns)]
+    ev_comp = [torch.cuda.Event() for _ in range(ns)]
+    ev_out = [torch.cuda.Event() for _ in range(ns)]
     e2e_steps = max(1, min(e2e_steps, steps))
     n_e2e = [0]
 
@@ -584,23 +591,30 @@ def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, loca
             return
         k = n_e2e[0]
         n_e2e[0] += 1
-        sl = slots[k & 1]
+        q = k % ns
+        sl = slots[q]
         with torch.cuda.stream(s_in):
-            if k >= 2:
-                s_in.wait_event(ev_out[k & 1])  # the step that last used this slot has been read back
+            if k >= ns:
+                # The step that last used this slot: once its calls are done its inputs are free,
+                # unless its outputs sit in the staging buffer too, which must be read back first.
+                # The 13B forward's outputs (layer 39's) do not, so its copy in runs beside the
+                # read-back (the two directions of the host link at once).
+                s_in.wait_event(ev_comp[q] if name == "mixed13b" else ev_out[q])
             sl["dstage"].copy_(hstage, non_blocking=True)
-            ev_in[k & 1].record(s_in)
-        comp.wait_event(ev_in[k & 1])
+            ev_in[q].record(s_in)
+        comp.wait_event(ev_in[q])
+        if k >= ns and name == "mixed13b":
+            comp.wait_event(ev_out[q])  # its outputs are read back before this step rewrites them
         if not bgmv:
             B.lora_segments_build(sl["ids"], n_ad, sl["seg"], mode=mode, err=err)
         for c in sl["calls"]:
             run_call(c, sl["ids"], sl["seg"])
-        ev_comp[k & 1].record(comp)
+        ev_comp[q].record(comp)
         with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_comp[k & 1])
+            s_out.wait_event(ev_comp[q])
             for d, h in sl["outs"]:
                 h.copy_(d, non_blocking=True)
-            ev_out[k & 1].record(s_out)
+            ev_out[q].record(s_out)
 
     for _ in range(3):
         e2e_step()
@@ -658,8 +672,8 @@ def run_workload(name, steps, warmup, e2e_steps, soak_seconds, world, rank, loca
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "public calls, eager; every step's inputs copied in from pinned host memory and its y "
                         "read back inside the timed region; " +
-                        ("pipelined over two staging slots (step k + 1's copy in overlaps step k's calls)"
-                         if pipelined else "one slot, in order on the launching stream")},
+                        ("pipelined over %d staging slots (step k + 1's copy in overlaps step k's calls and "
+                         "step k - 1's read-back)" % ns if pipelined else "one slot, in order on the launching stream")},
         "call_timing": {"graph_us": calls_avg_s * 1e6, "single_launch_us": single_us, "hot_l2_us": hot_us,
                         "note": "the step's projection calls: graph-amortised over rotating sets (cold L2), "
                                 "one eager launch group on an idle GPU, and one set repeated (warm L2)"},
@@ -752,10 +766,11 @@ def backward_bytes(batch, pool) -> int:
 def pipelined_e2e(torch, dev, inputs, run, n_out, steps, world, tokens):
     """End to end through the public calls for the lines of one call per step:
     `inputs` (device tensors: the step's inputs, the ones it updates in place first)
-    are copied in every step from one pinned host buffer into one of two device staging
+    are copied in every step from one pinned host buffer into one of three device staging
     slots, `run(views)` enqueues the step on the current stream on that slot's copies,
     and the first `n_out` of them (the step's result) are read back into pinned host
-    memory.  Step k + 1's copy in runs under step k's calls, on streams of their own; a
+    memory.  Step k + 1's copy in runs under step k's calls and beside step k - 1's
+    read-back (the two directions of the host link at once), on streams of their own; a
     slot is refilled once the step that last used it has been read back.  Returns
     (tokens/s, bytes in, bytes out per step)."""
     offs, cur = [], 0
@@ -766,31 +781,33 @@ def pipelined_e2e(torch, dev, inputs, run, n_out, steps, world, tokens):
     for t, o in zip(inputs, offs):
         hstage[o:o + t.numel() * t.element_size()].copy_(t.reshape(-1).view(torch.uint8).cpu())
     out_end = offs[n_out - 1] + inputs[n_out - 1].numel() * inputs[n_out - 1].element_size()
+    ns = 3
     slots = []
-    for _ in range(2):
+    for _ in range(ns):
         d = torch.empty(cur, dtype=torch.uint8, device=dev)
         views = [d[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(inputs, offs)]
         slots.append((d, views, torch.empty(out_end, dtype=torch.uint8).pin_memory()))
     comp = torch.cuda.current_stream(dev)
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_comp = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(ns)]
+    ev_comp = [torch.cuda.Event() for _ in range(ns)]
+    ev_out = [torch.cuda.Event() for _ in range(ns)]
 
     def one(k):
-        d, views, hout = slots[k & 1]
+        q = k % ns
+        d, views, hout = slots[q]
         with torch.cuda.stream(s_in):
-            if k >= 2:
-                s_in.wait_event(ev_out[k & 1])
+            if k >= ns:
+                s_in.wait_event(ev_out[q])  # the step that last used this slot has been read back
             d.copy_(hstage, non_blocking=True)
-            ev_in[k & 1].record(s_in)
-        comp.wait_event(ev_in[k & 1])
+            ev_in[q].record(s_in)
+        comp.wait_event(ev_in[q])
         run(views)
-        ev_comp[k & 1].record(comp)
+        ev_comp[q].record(comp)
         with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_comp[k & 1])
+            s_out.wait_event(ev_comp[q])
             hout.copy_(d[:out_end], non_blocking=True)
-            ev_out[k & 1].record(s_out)
+            ev_out[q].record(s_out)
 
     for k in range(3):
         one(k)
@@ -913,7 +930,7 @@ def run_backward_line(steps, warmup, soak_seconds, world, rank, local):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": e2e_in, "d2h_bytes_per_step": e2e_out,
                 "note": "lora_segments_build + lora_sgmv_backward, eager; x, dy, dx and the ids copied in from "
                         "pinned host memory and dx read back every step (the gradient pool stays on the device "
-                        "for the optimizer), pipelined over two staging slots"},
+                        "for the optimizer), pipelined over three staging slots"},
         "gpu_launches": int(round(launches_per_step * n_steps)),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
@@ -1044,7 +1061,7 @@ def run_base_line(steps, warmup, soak_seconds, world, rank, local):
                      "flops_per_step": flops, "avg_launch_us": step_s * 1e6},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": e2e_in, "d2h_bytes_per_step": e2e_out,
                 "note": "lora_segments_build + lora_base_apply, eager; x and the ids copied in from pinned host "
-                        "memory and y read back every step (W0 and the adapters resident), pipelined over two "
+                        "memory and y read back every step (W0 and the adapters resident), pipelined over three "
                         "staging slots"},
         "gpu_launches": int(round(launches_per_step * reps * n)),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
