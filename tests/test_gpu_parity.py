@@ -191,6 +191,28 @@ def test_apply_small_pages():
     compare_bf16(y, ref, "64-element pages")
 
 
+def test_gather_page_cache_edges():
+    """Short segments and one-token calls on adapters whose page-list slots fill the gather
+    kernel's per-unit cache exactly, exceed it by a few, or by far (then the producers read
+    the page list from global memory): d_in 256, d_out 384 and 64-element pages, so an
+    adapter of rank r takes 10 r slots -- rank 32 takes 320, rank 33 330, rank 64 640."""
+    rng = np.random.default_rng(31)
+    ranks = [32, 33, 64, 8, 64, 33]
+    pool = W.build_pool(rng, 256, 384, ranks, page_elems=64, max_rank=64)
+    ids = np.repeat(np.arange(len(ranks), dtype=np.int32), [1, 3, 2, 1, 3, 2])  # at most 3 tokens an adapter
+    ids = np.concatenate([ids, np.array([-1, -1], dtype=np.int32)])
+    rng.shuffle(ids)
+    batch = W.make_batch(rng, ids, 256, 384)
+    ref, _ = oracle.lora_apply(batch.x, batch.y0, ids, pool)
+    for mode in (B.LORA_SEG_GROUP, B.LORA_SEG_CONTIGUOUS):
+        y, err, _ = run_apply(batch, pool, mode, len(ranks))
+        assert err == 0
+        compare_bf16(y[:, :384], ref, "page cache edges, segments mode %d" % mode)
+    y, err = run_bgmv(batch, pool)  # max_rank 64: the gather kernel's one-token form
+    assert err == 0
+    compare_bf16(y[:, :384], ref, "page cache edges, one-token form")
+
+
 MIXED13B_PROJ = [p[0] for p in W.PROJ_13B]
 
 
