@@ -46,9 +46,9 @@ if ROOT not in sys.path:
 METRIC = "SGMV/BGMV adapter-path tokens/s and achieved HBM GB/s (% of roofline), 1×GB300"
 UNIT = "tokens/s"
 HEADLINE = "mixed13b"
-# Decode first: a decode call is a chain of latencies (~5 us), and timed after any other timing
-# in the same process (another decode included) it reads ~0.45 us slower per call than timed
-# first, for a cause not established; the other lines move by under 0.5 %.
+# Decode first: a decode call is a chain of latencies (~5 us), and timed a few seconds into the
+# process (after any other timing, another decode included) it reads ~0.45 us slower per call
+# than timed first, with the memory and SM clocks unchanged; the other lines move by under 0.5 %.
 OTHERS = ("decode", "tiny", "prefill", "hetero")
 
 WORKLOAD_TEXT = {
