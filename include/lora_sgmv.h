@@ -404,6 +404,20 @@ uint64_t lora_launch_count(void);
 void lora_debug_wait_probe(int64_t cycles);
 
 /**
+ * Test-only, host only (no device work): the thread-block cluster width the
+ * gather kernel is given for a call over the n projections `views` (1 <= n <=
+ * LORA_MAX_PROJ; only d_in and d_out are read), before the launcher narrows it
+ * by halves to fit every unit of the call in the resident clusters at once.
+ * CTA c of a cluster of w owns the c-th of w equal column runs of d_in and of
+ * d_out, staged 512 columns at a time; the width is the one with the fewest
+ * stages per unit among w0 / 2 .. w0 (w0 = ceil(max(d_in, d_out) / 512), at
+ * most 8), ties to the wider.  Returns -1 for a null pointer, n out of range or
+ * a dimension below 8.  (No passage of the pages: a work decomposition of this
+ * library.)
+ */
+int32_t lora_debug_gather_width(const lora_pool_view_t* views, int32_t n);
+
+/**
  * Pages one adapter of rank r occupies in a pool of page_elems-element pages:
  * ceil(r * d_in / page_elems) + ceil(r * d_out / page_elems) (bytes per matrix
  * pair (d_in * r + r * d_out) * 2 before rounding to pages: "Multi-LoRA

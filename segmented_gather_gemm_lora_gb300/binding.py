@@ -56,6 +56,7 @@ EXPORTED = (
     "lora_abi_version",
     "lora_launch_count",
     "lora_debug_wait_probe",
+    "lora_debug_gather_width",
     "lora_pool_mgr_create",
     "lora_pool_mgr_destroy",
     "lora_pool_mgr_page_list_len",
@@ -124,6 +125,8 @@ def lib():
         L.lora_launch_count.argtypes = []
         L.lora_debug_wait_probe.restype = None
         L.lora_debug_wait_probe.argtypes = [ctypes.c_int64]
+        L.lora_debug_gather_width.restype = ctypes.c_int32
+        L.lora_debug_gather_width.argtypes = [ctypes.POINTER(lora_pool_view_t), ctypes.c_int32]
         L.lora_segments_buffer_bytes.restype = sz
         L.lora_segments_buffer_bytes.argtypes = [i32]
         L.lora_segments_carve.restype = i32
@@ -379,6 +382,15 @@ def lora_apply_fixed_scratch(x: torch.Tensor, y: torch.Tensor, seg: Segments, vi
 def debug_wait_probe(cycles: int) -> None:
     """Test-only: arm (cycles > 0) or disarm the kernels' timeout probe."""
     lib().lora_debug_wait_probe(int(cycles))
+
+
+def debug_gather_width(shapes) -> int:
+    """Test-only, host only: the gather kernel's cluster width for a call over projections
+    of the given (d_in, d_out) shapes, before the launcher's occupancy narrowing."""
+    arr = (lora_pool_view_t * max(1, len(shapes)))()
+    for i, (d_in, d_out) in enumerate(shapes):
+        arr[i].d_in, arr[i].d_out = int(d_in), int(d_out)
+    return int(lib().lora_debug_gather_width(arr, len(shapes)))
 
 
 def launch_count() -> int:

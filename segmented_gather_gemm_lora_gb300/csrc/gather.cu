@@ -831,3 +831,14 @@ lora_status_t launch_gather(int mode, int src, int short_only, const void* x, lo
 }
 
 }  // namespace lora
+
+extern "C" int32_t lora_debug_gather_width(const lora_pool_view_t* views, int32_t n) {
+  if (views == nullptr || n < 1 || n > lora::kMaxFusedProj) return -1;
+  const lora_pool_view_t* v[lora::kMaxFusedProj];
+  for (int g = 0; g < n; ++g) {
+    if (views[g].d_in < 8 || views[g].d_out < 8) return -1;
+    v[g] = &views[g];
+  }
+  return lora::cluster_size_for(v, n);
+}
+

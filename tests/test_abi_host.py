@@ -182,3 +182,40 @@ def test_apply_multi_rejects_bad_groups_on_the_host():
     projs[1].view.d_in = 4096
     projs[1].view.max_rank = 65
     assert L.lora_apply_multi(projs, 2, ctypes.byref(seg), None, None) == B.LORA_ERR_UNSUPPORTED
+
+
+def _width_rule(shapes):
+    """The gather kernel's width rule restated: fewest 512-column stages per unit among
+    w0 / 2 .. w0, ties to the wider."""
+    d = max(max(a, b) for a, b in shapes)
+    w0 = min(max(-(-d // 512), 1), 8)
+    best, best_cost = w0, None
+    for w in range(w0, max(1, w0 // 2) - 1, -1):
+        cost = 0
+        for a, b in shapes:
+            kc = (-(-a // w) + 7) // 8 * 8
+            nc = (-(-b // w) + 7) // 8 * 8
+            cost += w * (-(-kc // 512) + -(-nc // 512))
+        if best_cost is None or cost < best_cost:
+            best, best_cost = w, cost
+    return best
+
+
+def test_gather_cluster_width():
+    """The widths of the benchmark's projections (host only), a restatement of the rule on
+    random shapes, and the argument checks."""
+    assert B.debug_gather_width([(5120, 5120)] * 3) == 5  # 13B-shaped q, k, v: 1024 columns a CTA
+    assert B.debug_gather_width([(5120, 13824)] * 2) == 5
+    assert B.debug_gather_width([(13824, 5120)]) == 5
+    assert B.debug_gather_width([(4096, 11008)]) == 8
+    assert B.debug_gather_width([(11008, 4096)]) == 8
+    assert B.debug_gather_width([(4096, 4096)]) == 8
+    assert B.debug_gather_width([(256, 256)]) == 1
+    rng = np.random.default_rng(5)
+    for _ in range(300):
+        n = int(rng.integers(1, 4))
+        shapes = [(8 * int(rng.integers(1, 2200)), 8 * int(rng.integers(1, 2200))) for _ in range(n)]
+        assert B.debug_gather_width(shapes) == _width_rule(shapes), shapes
+    assert B.debug_gather_width([]) == -1
+    assert B.debug_gather_width([(4, 4096)]) == -1
+    assert B.debug_gather_width([(4096, 4096)] * (B.LORA_MAX_PROJ + 1)) == -1
